@@ -1,0 +1,295 @@
+"""CPU oracle for causal grouped-query attention with RoPE, split-KV decode and latent decode.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline leg may import this module.  The product path (the CUDA library and its Python binding)
+never calls it, and this module never calls the CUDA path: the two share no code.
+
+Everything here is plain NumPy in float64, written as the textbook definition: materialise the
+full score matrix, mask it, subtract the row maximum, exponentiate, normalise, multiply by V.  No
+blocking, no online softmax, no fusion.  The only library primitives used are ``@`` (matmul),
+``np.exp``/``np.log``/``np.cos``/``np.sin`` and reductions.
+
+Where the pages are silent, the readings used are (each is repeated in the design notes):
+
+* RoPE is the rotate-half pairing (i, i + D/2) with inverse frequency theta^(-2i/D).  The pages
+  only name "RoPE-attention fusion" (Lesson: shape adaptive attention negative 20260722, rows
+  "해본 것" / "당시 조건").
+* Query head hq reads KV head hq // G with G = Hq / Hkv (contiguous grouping).
+* Causal masking hides key j from query i when j > i + (Skv - Sq) (bottom-right alignment; the
+  workloads only use Sq == Skv, where this is the usual j > i).
+* Decode: the single query sits at position L = cache_len[b] and attends the L cached keys
+  0..L-1, which are stored already rotated; only the query is rotated.
+* Latent decode: the query and every cache row have 448 latent dims followed by 64 RoPE dims;
+  scores use all 512 dims, values are the first 448 dims of the cache row (Fixed-budget decode
+  audit — 2026-09-11, "Which implementation was tested": 448-dimensional latent + 64-dimensional
+  RoPE).  RoPE is applied to the last 64 query dims only.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+LATENT_DIM = 448
+LATENT_ROPE_DIM = 64
+
+
+def as_f64(x) -> np.ndarray:
+    """Exact float64 copy of a torch tensor (any storage dtype) or array-like."""
+    try:
+        import torch
+
+        if isinstance(x, torch.Tensor):
+            return x.detach().to("cpu").to(torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------------------------
+# RoPE
+# --------------------------------------------------------------------------------------------
+
+def rope_inv_freq(D: int, theta: float) -> np.ndarray:
+    """theta^(-2i/D) for i < D/2, in float64."""
+    i = np.arange(D // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / D)
+
+
+def rope_rotate_half(x: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
+    """Rotate each pair (x_i, x_{i+D/2}) of the last axis by angle pos * theta^(-2i/D).
+
+    ``x`` has shape [..., n, D]; ``positions`` has shape [n] (one position per row).
+    Returns x'_i = x_i cos a - x_{i+D/2} sin a and x'_{i+D/2} = x_{i+D/2} cos a + x_i sin a.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    assert D % 2 == 0
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * rope_inv_freq(D, theta)[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    x1 = x[..., : D // 2]
+    x2 = x[..., D // 2:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+# --------------------------------------------------------------------------------------------
+# Attention by its definition
+# --------------------------------------------------------------------------------------------
+
+def softmax_rows(s: np.ndarray) -> np.ndarray:
+    """Row softmax with max subtraction; rows that are entirely -inf are not allowed."""
+    m = np.max(s, axis=-1, keepdims=True)
+    assert np.all(np.isfinite(m)), "fully masked row"
+    p = np.exp(s - m)
+    return p / np.sum(p, axis=-1, keepdims=True)
+
+
+def scores(q: np.ndarray, k: np.ndarray, scale: float, causal: bool, q_pos=None) -> np.ndarray:
+    """Masked score matrix scale * q k^T for one head: q [Sq,D], k [Skv,D] -> [Sq,Skv].
+
+    ``q_pos`` gives each query row's position in key coordinates (default: bottom-right aligned
+    positions Skv - Sq + i).  Key j is hidden from a row at position p when j > p.
+    """
+    Sq, Skv = q.shape[0], k.shape[0]
+    s = scale * (q @ k.T)
+    if causal:
+        if q_pos is None:
+            q_pos = np.arange(Sq) + (Skv - Sq)
+        j = np.arange(Skv)[None, :]
+        s = np.where(j > np.asarray(q_pos)[:, None], -np.inf, s)
+    return s
+
+
+def attention(q, k, v, causal: bool, scale: float | None = None, q_pos=None):
+    """O = softmax(scale * Q K^T + mask) V and LSE = log sum_j exp(S_ij), per (b, hq).
+
+    q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv] (float64).  Query head hq uses KV head
+    hq // (Hq / Hkv).  Returns (O [B,Hq,Sq,Dv], LSE [B,Hq,Sq]) in float64.
+    """
+    q, k, v = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
+    B, Hq, Sq, D = q.shape
+    Hkv = k.shape[1]
+    assert Hq % Hkv == 0
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    O = np.empty((B, Hq, Sq, v.shape[-1]))
+    LSE = np.empty((B, Hq, Sq))
+    for b in range(B):
+        for hq in range(Hq):
+            h = hq // G
+            s = scores(q[b, hq], k[b, h], scale, causal, q_pos)
+            m = np.max(s, axis=-1, keepdims=True)
+            e = np.exp(s - m)
+            l = np.sum(e, axis=-1, keepdims=True)
+            O[b, hq] = (e / l) @ v[b, h]
+            LSE[b, hq] = (m + np.log(l))[:, 0]
+    return O, LSE
+
+
+def attention_probs(q, k, causal: bool, scale: float | None = None):
+    """The normalised probability matrices P [B,Hq,Sq,Skv] (for invariant checks)."""
+    q, k = np.asarray(q, np.float64), np.asarray(k, np.float64)
+    B, Hq, Sq, D = q.shape
+    G = Hq // k.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    P = np.empty((B, Hq, Sq, k.shape[2]))
+    for b in range(B):
+        for hq in range(Hq):
+            P[b, hq] = softmax_rows(scores(q[b, hq], k[b, hq // G], scale, causal))
+    return P
+
+
+def prefill(q, k, v, causal=True, scale=None, rope=False, theta=10000.0, pos0=0):
+    """Prefill: optionally rotate Q and K at positions pos0 .. pos0+S-1, then attention.
+
+    Positions follow the reading that prefill tokens sit at 0..S-1 (pos0 = 0) on a fresh
+    sequence.  Returns (O, LSE) in float64.
+    """
+    q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
+    if rope:
+        pos_q = pos0 + np.arange(q.shape[2])
+        pos_k = pos0 + np.arange(k.shape[2])
+        q = rope_rotate_half(q, pos_q, theta)
+        k = rope_rotate_half(k, pos_k, theta)
+    return attention(q, k, v, causal, scale)
+
+
+def prefill_rows(q, k, v, rows, causal=True, scale=None, rope=False, theta=10000.0, pos0=0):
+    """Selected output rows of ``prefill`` (for sizes where the full oracle is too slow).
+
+    ``rows`` is a list of (b, hq, i).  Each row is computed by the same definition: rotate the
+    query row at position pos0+i and all keys, form the row of scores, mask keys j > i (causal,
+    Sq == Skv), softmax, multiply by V.  Returns (O [n,Dv], LSE [n]).
+    """
+    q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
+    B, Hq, S, D = q.shape
+    G = Hq // k.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    cache = {}
+    out_o, out_l = [], []
+    for (b, hq, i) in rows:
+        h = hq // G
+        key = (b, h)
+        if key not in cache:
+            kk = k[b, h]
+            if rope:
+                kk = rope_rotate_half(kk, pos0 + np.arange(kk.shape[0]), theta)
+            cache[key] = kk
+        kk = cache[key]
+        qi = q[b, hq, i][None, :]
+        if rope:
+            qi = rope_rotate_half(qi, np.array([pos0 + i]), theta)
+        s = scores(qi, kk, scale, causal, q_pos=np.array([i + (kk.shape[0] - S)]))
+        m = np.max(s)
+        e = np.exp(s - m)
+        l = np.sum(e)
+        out_o.append(((e / l) @ v[b, h])[0])
+        out_l.append(m + np.log(l))
+    return np.array(out_o), np.array(out_l)
+
+
+def decode(q, k_cache, v_cache, cache_len, scale=None, rope=True, theta=10000.0):
+    """Single-token decode against a static cache.
+
+    q [B,Hq,D]; k_cache/v_cache [B,Hkv,Lmax,D] (keys stored already rotated); cache_len [B].
+    Sequence b's query sits at position L = cache_len[b]; it is rotated there when ``rope``;
+    it attends keys 0..L-1.  Returns (O [B,Hq,D], LSE [B,Hq]).
+    """
+    q, kc, vc = (np.asarray(t, np.float64) for t in (q, k_cache, v_cache))
+    lens = np.asarray(cache_len).astype(np.int64)
+    B, Hq, D = q.shape
+    Dv = vc.shape[-1]
+    O = np.empty((B, Hq, Dv))
+    LSE = np.empty((B, Hq))
+    for b in range(B):
+        L = int(lens[b])
+        assert 1 <= L <= kc.shape[2]
+        qb = q[b][:, None, :]  # [Hq, 1, D]
+        if rope:
+            qb = rope_rotate_half(qb, np.array([L]), theta)
+        o, lse = attention(qb[None], kc[b: b + 1, :, :L], vc[b: b + 1, :, :L], causal=False,
+                           scale=scale)
+        O[b] = o[0, :, 0]
+        LSE[b] = lse[0, :, 0]
+    return O, LSE
+
+
+def latent_decode(q, c_cache, cache_len, scale=None, rope=True, theta=10000.0,
+                  d_latent=LATENT_DIM, d_rope=LATENT_ROPE_DIM):
+    """Absorbed latent (MLA-style) decode.
+
+    q [B,H,d_latent+d_rope]; c_cache [B,Lmax,d_latent+d_rope] (rope part stored rotated);
+    every head attends the same latent rows: S = scale * q C^T over all dims, V = C[:, :d_latent].
+    The last ``d_rope`` query dims are rotated at position L = cache_len[b] when ``rope``.
+    Returns (O [B,H,d_latent], LSE [B,H]).
+    """
+    q, c = np.asarray(q, np.float64), np.asarray(c_cache, np.float64)
+    lens = np.asarray(cache_len).astype(np.int64)
+    B, H, dqk = q.shape
+    assert dqk == d_latent + d_rope == c.shape[-1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(dqk)
+    O = np.empty((B, H, d_latent))
+    LSE = np.empty((B, H))
+    for b in range(B):
+        L = int(lens[b])
+        assert 1 <= L <= c.shape[1]
+        qb = q[b].copy()
+        if rope:
+            qb[:, d_latent:] = rope_rotate_half(qb[:, None, d_latent:], np.array([L]), theta)[:, 0]
+        cb = c[b, :L]
+        o, lse = attention(qb[None, :, None, :], cb[None, None], cb[None, None, :, :d_latent],
+                           causal=False, scale=scale)
+        O[b] = o[0, :, 0]
+        LSE[b] = lse[0, :, 0]
+    return O, LSE
+
+
+# --------------------------------------------------------------------------------------------
+# Merging partial attention results
+# --------------------------------------------------------------------------------------------
+
+def merge_one_key(o_hist, lse_hist, s_cur, v_cur):
+    """Merge one extra key into an already normalised partial attention.
+
+    Fixed-budget decode audit — 2026-09-11, "A: group-entry queries and one joint history scan":
+    with alpha = sigmoid(s_cur - lse_hist), the merged output is (1-alpha) o_hist + alpha v_cur.
+    The merged log-sum-exp is log(exp(lse_hist) + exp(s_cur)).
+    """
+    o_hist, v_cur = np.asarray(o_hist, np.float64), np.asarray(v_cur, np.float64)
+    lse_hist, s_cur = np.asarray(lse_hist, np.float64), np.asarray(s_cur, np.float64)
+    alpha = 1.0 / (1.0 + np.exp(-(s_cur - lse_hist)))
+    out = (1.0 - alpha)[..., None] * o_hist + alpha[..., None] * v_cur
+    return out, np.logaddexp(lse_hist, s_cur)
+
+
+def combine_partials(o_parts, lse_parts):
+    """Combine split partials: LSE = log sum_s exp(lse_s), O = sum_s exp(lse_s - LSE) o_s.
+
+    o_parts [..., n, D], lse_parts [..., n]; a split with lse = -inf contributes nothing.
+    """
+    o_parts, lse_parts = np.asarray(o_parts, np.float64), np.asarray(lse_parts, np.float64)
+    m = np.max(lse_parts, axis=-1, keepdims=True)
+    w = np.exp(lse_parts - m)
+    tot = np.sum(w, axis=-1, keepdims=True)
+    lse = (m + np.log(tot))[..., 0]
+    o = np.sum((w / tot)[..., None] * o_parts, axis=-2)
+    return o, lse
+
+
+def split_decode_partials(q_row, k, v, split: int, scale: float):
+    """Attention of one query row over k/v [L,D] computed split by split (partials + LSE).
+
+    Each split of ``split`` keys is attention restricted to that split; returns
+    (o_parts [n, Dv], lse_parts [n]).  Used to check that combining splits equals the whole.
+    """
+    q_row, k, v = (np.asarray(t, np.float64) for t in (q_row, k, v))
+    L = k.shape[0]
+    o_parts, lse_parts = [], []
+    for s0 in range(0, L, split):
+        o, lse = attention(q_row[None, None, None, :], k[None, None, s0:s0 + split],
+                           v[None, None, s0:s0 + split], causal=False, scale=scale)
+        o_parts.append(o[0, 0, 0])
+        lse_parts.append(lse[0, 0, 0])
+    return np.array(o_parts), np.array(lse_parts)

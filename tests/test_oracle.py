@@ -1,0 +1,423 @@
+"""Pins for the float64 CPU oracle: checks against things other than the oracle itself.
+
+Each check uses a closed form, an invariant the mathematics fixes, an independent library
+routine (torch's scaled_dot_product_attention in float64), brute force over tiny enumerated
+inputs with a separately written scalar loop, or a number printed on the pages
+(tests/golden/page_facts.json).  The last tests plant typical mistakes in copies of the oracle
+and check that the pins catch every one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import attention_fp64 as O
+from attention_attn_prefill_02_gb300 import synthetic, workload
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+FACTS = json.load(open(os.path.join(GOLDEN, "page_facts.json")))
+RNG = np.random.default_rng(1234)
+
+
+def rnd(*shape):
+    return RNG.standard_normal(shape)
+
+
+# ---------------------------------------------------------------------------------------------
+# pin functions: each takes the functions under test, so planted mistakes can be fed in
+# ---------------------------------------------------------------------------------------------
+
+def pin_softmax_sums_to_one(probs=O.attention_probs):
+    q, k = rnd(1, 2, 7, 4), rnd(1, 2, 7, 4)
+    for causal in (False, True):
+        P = probs(q, k, causal)
+        np.testing.assert_allclose(P.sum(-1), 1.0, rtol=0, atol=1e-12)
+        assert np.all(P >= 0)
+
+
+def pin_zero_query_is_causal_mean(attn=O.attention):
+    """q = 0: all logits equal, so causal row i is the plain mean of v_0..v_i, LSE = ln(i+1)."""
+    S, D = 9, 5
+    q = np.zeros((1, 1, S, D))
+    k, v = rnd(1, 1, S, D), rnd(1, 1, S, 3)
+    o, lse = attn(q, k, v, True, 0.37)
+    for i in range(S):
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0, : i + 1].mean(0), rtol=0, atol=1e-13)
+        assert abs(lse[0, 0, i] - math.log(i + 1)) < 1e-13
+
+
+def pin_hand_two_key_case(attn=O.attention):
+    """logits (0, ln 3) give weights (1/4, 3/4): O = (1, 6) for v0 = (4, 0), v1 = (0, 8)."""
+    q = np.array([[[[math.log(3.0), 0.0]]]])
+    k = np.array([[[[0.0, 0.0], [1.0, 0.0]]]])
+    v = np.array([[[[4.0, 0.0], [0.0, 8.0]]]])
+    o, lse = attn(q, k, v, False, 1.0)
+    np.testing.assert_allclose(o[0, 0, 0], [1.0, 6.0], rtol=0, atol=1e-13)
+    assert abs(lse[0, 0, 0] - math.log(4.0)) < 1e-13
+
+
+def pin_one_hot_and_single_key(attn=O.attention):
+    S, D = 6, 4
+    k, v = rnd(1, 1, S, D), rnd(1, 1, S, D)
+    # one large logit on key 3 -> output is v_3 (other keys are orthogonal to q)
+    k[0, 0, :, 0] = 0.0
+    k[0, 0, 3] = [1.0, 0.0, 0.0, 0.0]
+    q = np.array([[[[60.0, 0.0, 0.0, 0.0]]]])
+    o, _ = attn(q, k, v, False, 1.0)
+    np.testing.assert_allclose(o[0, 0, 0], v[0, 0, 3], rtol=0, atol=1e-12)
+    # a single key -> output is v_0 whatever q is
+    o1, lse1 = attn(rnd(1, 1, 1, D), k[:, :, :1], v[:, :, :1], True, 0.5)
+    np.testing.assert_allclose(o1[0, 0, 0], v[0, 0, 0], rtol=0, atol=1e-15)
+
+
+def pin_causal_ignores_future(attn=O.attention):
+    S, D = 8, 4
+    q, k, v = rnd(1, 2, S, D), rnd(1, 2, S, D), rnd(1, 2, S, D)
+    o, lse = attn(q, k, v, True, 0.5)
+    for i in range(S - 1):
+        k2, v2 = k.copy(), v.copy()
+        k2[:, :, i + 1:] = rnd(1, 2, S - i - 1, D) * 10
+        v2[:, :, i + 1:] = rnd(1, 2, S - i - 1, D) * 10
+        o2, lse2 = attn(q, k2, v2, True, 0.5)
+        assert np.array_equal(o2[:, :, : i + 1], o[:, :, : i + 1])
+        assert np.array_equal(lse2[:, :, : i + 1], lse[:, :, : i + 1])
+
+
+def pin_matches_torch_sdpa(attn=O.attention):
+    """Independent library routine: torch SDPA in float64 on the CPU (KV heads repeated)."""
+    for causal, (B, Hq, Hkv, S, D) in itertools.product(
+            (False, True), [(2, 4, 1, 13, 8), (1, 6, 3, 20, 16), (1, 2, 2, 5, 64)]):
+        q, k, v = rnd(B, Hq, S, D), rnd(B, Hkv, S, D), rnd(B, Hkv, S, D)
+        scale = 1 / math.sqrt(D)
+        o, _ = attn(q, k, v, causal, scale)
+        G = Hq // Hkv
+        tq = torch.from_numpy(q)
+        tk = torch.from_numpy(k).repeat_interleave(G, dim=1)
+        tv = torch.from_numpy(v).repeat_interleave(G, dim=1)
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal,
+                                                               scale=scale)
+        np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def scalar_attention_row(qi, keys, vals, scale):
+    """Separately written scalar loop: softmax-weighted average with math.exp."""
+    logits = [scale * sum(a * b for a, b in zip(qi, kj)) for kj in keys]
+    z = sum(math.exp(t) for t in logits)
+    out = [0.0] * len(vals[0])
+    for t, vj in zip(logits, vals):
+        w = math.exp(t) / z
+        for d in range(len(out)):
+            out[d] += w * vj[d]
+    return out, math.log(z)
+
+
+def pin_bruteforce_enumeration(attn=O.attention):
+    """Every q, k in {-1,0,1}^2 for S = 2 plus random v; S = 3, 4 on a sample of grids."""
+    vals3 = (-1.0, 0.0, 1.0)
+    vecs = list(itertools.product(vals3, repeat=2))
+    for S in (1, 2, 3, 4):
+        combos = list(itertools.product(vecs, repeat=S))
+        if len(combos) > 200:
+            idx = np.random.default_rng(S).choice(len(combos), 200, replace=False)
+            combos = [combos[i] for i in idx]
+        for kq in combos:
+            k = np.array(kq, dtype=np.float64)[None, None]
+            q = k[:, :, ::-1].copy()  # queries: the keys with rows reversed
+            v = np.arange(S * 2, dtype=np.float64).reshape(1, 1, S, 2) - 2.5
+            for causal in (False, True):
+                o, lse = attn(q, k, v, causal, 0.75)
+                for i in range(S):
+                    n = i + 1 if causal else S
+                    ref_o, ref_l = scalar_attention_row(q[0, 0, i], k[0, 0, :n], v[0, 0, :n], 0.75)
+                    np.testing.assert_allclose(o[0, 0, i], ref_o, rtol=0, atol=1e-13)
+                    assert abs(lse[0, 0, i] - ref_l) < 1e-13
+
+
+def pin_gqa_equals_repeated_mha(attn=O.attention):
+    B, Hq, Hkv, S, D = 2, 8, 2, 6, 4
+    q, k, v = rnd(B, Hq, S, D), rnd(B, Hkv, S, D), rnd(B, Hkv, S, D)
+    o, lse = attn(q, k, v, True, 0.5)
+    o2, lse2 = attn(q, np.repeat(k, 4, axis=1), np.repeat(v, 4, axis=1), True, 0.5)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-14)
+    # and each query head really uses head hq // G (contiguous grouping)
+    o3, _ = attn(q[:, 5:6], k[:, 1:2], v[:, 1:2], True, 0.5)
+    np.testing.assert_allclose(o[:, 5:6], o3, rtol=0, atol=1e-14)
+
+
+def pin_rope(rope=O.rope_rotate_half):
+    D, n = 16, 11
+    x = rnd(3, n, D)
+    pos = np.arange(n) * 37 + 5
+    y = rope(x, pos, 10000.0)
+    # norm preserved
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), atol=1e-12)
+    # position 0 is the identity
+    np.testing.assert_allclose(rope(x, np.zeros(n), 10000.0), x, rtol=0, atol=0)
+    # <R(m) q, R(n) k> depends only on m - n
+    q, k = rnd(1, 1, D), rnd(1, 1, D)
+    for (m, nn, t) in [(3, 1, 100), (0, 7, 2048), (16000, 5, 123)]:
+        a = np.sum(rope(q, [m], 500.0) * rope(k, [nn], 500.0))
+        b = np.sum(rope(q, [m + t], 500.0) * rope(k, [nn + t], 500.0))
+        assert abs(a - b) < 1e-9
+    # D = 2: a plain 2x2 rotation by angle pos (inverse frequency theta^0 = 1)
+    for p in (0.0, 1.0, 2.0, 7.5, 2048.0):
+        out = rope(np.array([[[0.3, -1.2]]]), [p], 10000.0)[0, 0]
+        c, s = math.cos(p), math.sin(p)
+        np.testing.assert_allclose(out, [0.3 * c + 1.2 * s, -1.2 * c + 0.3 * s], atol=1e-12)
+    # D = 4, theta = 100: pairs (0,2) at angle p and (1,3) at angle p/10
+    p = 10.0
+    out = rope(np.array([[[1.0, 2.0, 3.0, 4.0]]]), [p], 100.0)[0, 0]
+    c0, s0, c1, s1 = math.cos(p), math.sin(p), math.cos(p / 10), math.sin(p / 10)
+    np.testing.assert_allclose(out, [c0 - 3 * s0, 2 * c1 - 4 * s1, 3 * c0 + s0, 4 * c1 + 2 * s1],
+                               atol=1e-12)
+
+
+def pin_latent_absorbed_equals_explicit(latent=O.latent_decode):
+    """Absorbed attention over the shared latent equals the explicit up-projected form.
+
+    Explicit: k_h = [W_UK,h c || k_rope], v_h = W_UV,h c, q_h = [q_nope,h || q_rope,h].
+    Absorbed: q_lat,h = [W_UK,h^T q_nope,h || q_rope,h] attends C directly, then W_UV,h is
+    applied to the latent output.  (Fixed-budget decode audit — 2026-09-11, "Which
+    implementation was tested": MLA with eager absorption, 448 latent + 64 RoPE dims.)
+    """
+    dl, dr = FACTS["mla_latent_dims"]["value"], FACTS["mla_rope_dims"]["value"]
+    B, H, L, d_nope, d_v = 2, 3, 17, 128, 128
+    c = rnd(B, L, dl + dr)
+    W_UK, W_UV = rnd(H, d_nope, dl) * 0.05, rnd(H, d_v, dl) * 0.05
+    q_nope, q_rope = rnd(B, H, d_nope), rnd(B, H, dr)
+    lens = np.array([L, 9])
+    scale = 1.0 / math.sqrt(d_nope + dr)
+    q_lat = np.concatenate([np.einsum("hnl,bhn->bhl", W_UK, q_nope), q_rope], axis=-1)
+    o_lat, _ = latent(q_lat, c, lens, scale=scale, rope=False)
+    o_abs = np.einsum("hvl,bhl->bhv", W_UV, o_lat)
+    for b in range(B):
+        Lb = lens[b]
+        cb = c[b, :Lb]
+        for h in range(H):
+            kh = np.concatenate([cb[:, :dl] @ W_UK[h].T, cb[:, dl:]], axis=-1)
+            vh = cb[:, :dl] @ W_UV[h].T
+            qh = np.concatenate([q_nope[b, h], q_rope[b, h]])
+            ref, _ = scalar_attention_row(qh, kh, vh, scale)
+            np.testing.assert_allclose(o_abs[b, h], ref, rtol=0, atol=1e-10)
+
+
+def pin_merge_identity(merge=O.merge_one_key, combine=O.combine_partials):
+    tol = FACTS["merge_identity_tolerance"]["value"]
+    L, D = 37, 8
+    q, k, v = rnd(D), rnd(L + 1, D), rnd(L + 1, D)
+    s = k @ q * 0.4
+    o_hist, lse_hist = O.attention(q[None, None, None], k[None, None, :L], v[None, None, :L],
+                                   False, 0.4)
+    o_m, lse_m = merge(o_hist[0, 0, 0], lse_hist[0, 0, 0], s[L], v[L])
+    ref_o, ref_l = scalar_attention_row(q, k, v, 0.4)
+    np.testing.assert_allclose(o_m, ref_o, rtol=0, atol=tol)
+    assert abs(lse_m - ref_l) < tol
+    # split into chunks of the audit's split size (and ragged ones), combine == whole
+    for split in (FACTS["decode_split_size"]["value"], 5, 1, 64):
+        kk, vv = rnd(300, D), rnd(300, D)
+        op, lp = O.split_decode_partials(q, kk, vv, split, 0.4)
+        o_c, l_c = combine(op, lp)
+        ref_o, ref_l = scalar_attention_row(q, kk, vv, 0.4)
+        np.testing.assert_allclose(o_c, ref_o, rtol=0, atol=1e-12)
+        assert abs(l_c - ref_l) < 1e-11
+    # an empty split (lse = -inf) contributes nothing
+    o_c, l_c = combine(np.stack([op[0], np.full(D, 7.0)]), np.array([lp[0], -np.inf]))
+    np.testing.assert_allclose(o_c, op[0], atol=0)
+
+
+ALL_PINS = [pin_softmax_sums_to_one, pin_zero_query_is_causal_mean, pin_hand_two_key_case,
+            pin_one_hot_and_single_key, pin_causal_ignores_future, pin_matches_torch_sdpa,
+            pin_bruteforce_enumeration, pin_gqa_equals_repeated_mha, pin_rope,
+            pin_latent_absorbed_equals_explicit, pin_merge_identity]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+# ---------------------------------------------------------------------------------------------
+# entry-point level checks of the oracle (decode / latent / prefill wrappers)
+# ---------------------------------------------------------------------------------------------
+
+def test_decode_matches_sdpa_and_rotation():
+    """Decode = one query row at position L attending the L cached (pre-rotated) keys."""
+    B, Hq, Hkv, Lmax, D = 3, 8, 2, 40, 16
+    q, kc, vc = rnd(B, Hq, D), rnd(B, Hkv, Lmax, D), rnd(B, Hkv, Lmax, D)
+    lens = np.array([40, 1, 23])
+    o, lse = O.decode(q, kc, vc, lens, rope=True, theta=10000.0)
+    for b in range(B):
+        L = lens[b]
+        # rotate q by hand per pair at angle L * theta^(-2i/D)
+        qr = q[b].copy()
+        for i in range(D // 2):
+            a = L * 10000.0 ** (-2 * i / D)
+            x1, x2 = q[b, :, i].copy(), q[b, :, i + D // 2].copy()
+            qr[:, i] = x1 * math.cos(a) - x2 * math.sin(a)
+            qr[:, i + D // 2] = x2 * math.cos(a) + x1 * math.sin(a)
+        tk = torch.from_numpy(kc[b, :, :L]).repeat_interleave(4, 0)
+        tv = torch.from_numpy(vc[b, :, :L]).repeat_interleave(4, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(qr)[:, None], tk, tv, scale=1 / math.sqrt(D))
+        np.testing.assert_allclose(o[b], ref[:, 0].numpy(), atol=1e-12)
+
+
+def test_prefill_rows_equals_full_prefill():
+    q, k, v = rnd(2, 4, 33, 8), rnd(2, 2, 33, 8), rnd(2, 2, 33, 8)
+    full_o, full_l = O.prefill(q, k, v, causal=True, rope=True, theta=50.0)
+    rows = [(0, 0, 0), (1, 3, 32), (0, 2, 17), (1, 1, 5)]
+    ro, rl = O.prefill_rows(q, k, v, rows, causal=True, rope=True, theta=50.0)
+    for n, (b, h, i) in enumerate(rows):
+        np.testing.assert_allclose(ro[n], full_o[b, h, i], atol=1e-13)
+        assert abs(rl[n] - full_l[b, h, i]) < 1e-13
+
+
+def test_prefill_rope_equals_rotated_sdpa():
+    """Prefill with RoPE = SDPA on Q, K rotated at 0..S-1 (rotation written out here)."""
+    B, H, S, D, theta = 1, 2, 12, 8, 10000.0
+    q, k, v = rnd(B, H, S, D), rnd(B, H, S, D), rnd(B, H, S, D)
+
+    def rot(x):
+        y = x.copy()
+        for s in range(S):
+            for i in range(D // 2):
+                a = s * theta ** (-2 * i / D)
+                x1, x2 = x[..., s, i], x[..., s, i + D // 2]
+                y[..., s, i] = x1 * math.cos(a) - x2 * math.sin(a)
+                y[..., s, i + D // 2] = x2 * math.cos(a) + x1 * math.sin(a)
+        return y
+
+    o, _ = O.prefill(q, k, v, causal=True, rope=True, theta=theta)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(rot(q)), torch.from_numpy(rot(k)), torch.from_numpy(v), is_causal=True)
+    np.testing.assert_allclose(o, ref.numpy(), atol=1e-12)
+
+
+def test_fp8_inputs_dequantise_exactly():
+    """The oracle sees the stored e5m2 values exactly (per-tensor scale 1)."""
+    x = synthetic.normal((4, 64), 3, "fp8")
+    f = oracle.as_f64(x)
+    # e5m2 has 2 mantissa bits: every finite value is m * 2^e with |m| < 8 an integer
+    nz = f[f != 0]
+    e = np.floor(np.log2(np.abs(nz)))
+    mant = np.abs(nz) / 2.0 ** (e - 2)
+    assert np.allclose(mant, np.round(mant))
+    assert np.array_equal(f, x.float().double().numpy())
+
+
+# ---------------------------------------------------------------------------------------------
+# the pages' printed numbers pin the workload counts the bench divides by
+# ---------------------------------------------------------------------------------------------
+
+def test_golden_page_volumes():
+    f = FACTS
+    assert 4 * 2 * 4 * 64 == f["gqa_history_elements_per_token_per_group"]["value"]
+    # decode config: Hkv = 8, D = 128 -> 2 * 8 * 128 = 2048 elements/token, the audit's figure
+    assert 2 * 8 * 128 == f["gqa_history_elements_per_token_per_group"]["value"]
+    hist = workload.decode_bytes(128, 32, 8, 2048, 128) - 128 * 32 * 128 * 4
+    assert hist == f["gqa_history_bytes_batch128_ctx2048"]["value"]
+    assert workload.latent_bytes(128, 16, 2048) - 128 * 16 * (512 + 448) * 2 == 128 * 2048 * 512 * 2
+    assert f["mla_latent_dims"]["value"] + f["mla_rope_dims"]["value"] == 512
+    assert (oracle.LATENT_DIM, oracle.LATENT_ROPE_DIM) == (448, 64)
+
+
+def test_flop_counts_match_enumeration():
+    """Causal FLOPs count exactly the scored pairs: enumerate them for a small S."""
+    S, D = 37, 8
+    pairs = sum(1 for i in range(S) for j in range(S) if j <= i)
+    assert workload.prefill_flops(1, 1, S, D, True) == 2 * pairs * 2 * D
+    assert workload.prefill_flops(2, 3, S, D, False) == 2 * 3 * 4 * S * S * D
+    assert workload.decode_flops(2, 4, 10, 8) == 2 * 4 * 10 * 8 * 4
+
+
+# ---------------------------------------------------------------------------------------------
+# planted mistakes: each mutant of the oracle must fail at least one pin
+# ---------------------------------------------------------------------------------------------
+
+def _mutant_attention(kind):
+    def attn(q, k, v, causal, scale=None, q_pos=None):
+        q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
+        B, Hq, Sq, D = q.shape
+        G = Hq // k.shape[1]
+        scale = 1 / np.sqrt(D) if scale is None else scale
+        Ov = np.empty((B, Hq, Sq, v.shape[-1]))
+        L = np.empty((B, Hq, Sq))
+        for b in range(B):
+            for hq in range(Hq):
+                h = hq % k.shape[1] if kind == "gqa_modulo" else hq // G
+                kk = k[b, h]
+                s = (1.0 if kind == "no_scale" else scale) * (q[b, hq] @ kk.T)
+                if causal:
+                    j = np.arange(kk.shape[0])[None, :]
+                    i = np.arange(Sq)[:, None] + (kk.shape[0] - Sq)
+                    s = np.where((j >= i) if kind == "mask_diag" else (j > i), -np.inf, s)
+                m = s.max(-1, keepdims=True)
+                e = np.exp(s - m)
+                l = e.sum(-1, keepdims=True)
+                if kind == "no_norm":
+                    l = np.ones_like(l)
+                vv = v[b, h]
+                Ov[b, hq] = (e / l) @ (vv[::-1] if kind == "v_reversed" else vv)
+                L[b, hq] = (m + (0 if kind == "lse_no_log" else np.log(l)))[:, 0]
+        return Ov, L
+    return attn
+
+
+def _mutant_rope(kind):
+    def rope(x, positions, theta):
+        x = np.asarray(x, np.float64)
+        D = x.shape[-1]
+        i = np.arange(D // 2)
+        inv = theta ** (-(2.0 if kind != "freq_no2" else 1.0) * i / D)
+        a = np.asarray(positions, np.float64)[:, None] * inv[None]
+        c, s = np.cos(a), np.sin(a)
+        x1, x2 = x[..., : D // 2], x[..., D // 2:]
+        if kind == "sign":
+            return np.concatenate([x1 * c + x2 * s, x2 * c - x1 * s], -1)
+        if kind == "interleaved_swap":
+            return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], -1)[..., ::-1]
+        return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], -1)
+    return rope
+
+
+def _fails_some(pins, **kw):
+    for p in pins:
+        try:
+            p(**kw)
+        except AssertionError:
+            return True
+    return False
+
+
+ATTN_PINS = [pin_zero_query_is_causal_mean, pin_hand_two_key_case, pin_one_hot_and_single_key,
+             pin_causal_ignores_future, pin_matches_torch_sdpa, pin_bruteforce_enumeration,
+             pin_gqa_equals_repeated_mha]
+
+
+@pytest.mark.parametrize("kind", ["gqa_modulo", "no_scale", "mask_diag", "no_norm", "v_reversed",
+                                  "lse_no_log"])
+def test_planted_attention_mistake_is_caught(kind):
+    assert _fails_some(ATTN_PINS, attn=_mutant_attention(kind))
+
+
+@pytest.mark.parametrize("kind", ["sign", "freq_no2", "interleaved_swap"])
+def test_planted_rope_mistake_is_caught(kind):
+    assert _fails_some([pin_rope], rope=_mutant_rope(kind))
+
+
+def test_planted_merge_mistake_is_caught():
+    def bad_merge(o_hist, lse_hist, s_cur, v_cur):
+        alpha = 1.0 / (1.0 + np.exp(s_cur - lse_hist))  # sign flipped
+        return (1 - alpha) * o_hist + alpha * v_cur, np.logaddexp(lse_hist, s_cur)
+
+    def bad_combine(o_parts, lse_parts):
+        w = np.exp(lse_parts - lse_parts.max())
+        return (w[:, None] * o_parts).sum(0), np.log(w.sum())  # not normalised
+
+    assert _fails_some([pin_merge_identity], merge=bad_merge)
+    assert _fails_some([pin_merge_identity], combine=bad_combine)
