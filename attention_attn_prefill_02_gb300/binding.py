@@ -1,0 +1,186 @@
+"""Thin ctypes binding over the C ABI in ``include/attn.h``.
+
+Every function here only marshals arguments (tensor -> device pointer, sizes, the current CUDA
+stream) and turns a non-OK status into ``AttnError``.  All arithmetic runs in the library's CUDA
+kernels; there is no CPU fallback.  The names match the C entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+ATTN_OK = 0
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA",
+                5: "TIMEOUT", 6: "NO_DEVICE", 7: "DEVICE_ARG"}
+DTYPE_CODES = {torch.bfloat16: 0, torch.float8_e5m2: 1}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
+                         f"({lib().attn_status_string(status).decode()})")
+
+
+def lib(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first when needed) the in-tree shared library."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing:
+        path = _build.build_library()
+    if not os.path.exists(path):
+        raise RuntimeError(f"attention library not built: {path} is missing")
+    L = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_status_string.argtypes = [i]
+    L.attn_version.restype = i
+    L.attn_version.argtypes = []
+    L.rope_apply.restype = i
+    L.rope_apply.argtypes = [vp, vp, i, i, i, i, i, i, f, vp]
+    L.attn_prefill.restype = i
+    L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i, f, f, f, i, i, i, i, i, i, f, i, f, i, vp]
+    L.attn_decode_workspace_size.restype = sz
+    L.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
+    L.attn_decode.restype = i
+    L.attn_decode.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp, sz, vp]
+    L.attn_decode_latent_workspace_size.restype = sz
+    L.attn_decode_latent_workspace_size.argtypes = [i, i, i]
+    L.attn_decode_latent.restype = i
+    L.attn_decode_latent.argtypes = [vp, vp, vp, i, vp, vp, i, i, f, i, f, vp, sz, vp]
+    L.attn_rope_table_reserve.restype = i
+    L.attn_rope_table_reserve.argtypes = [i, f, i]
+    L.attn_get_device_status.restype = i
+    L.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def _require_cuda(*tensors):
+    for t in tensors:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def rope_apply(x, y=None, pos0=0, theta=10000.0, stream=None):
+    """Rotate x [B,H,S,D] at positions pos0 + s into y (new tensor when None; may be x)."""
+    _require_cuda(x)
+    if y is None:
+        y = torch.empty_like(x)
+    B, H, S, D = x.shape
+    _check(lib().rope_apply(_ptr(x), _ptr(y), DTYPE_CODES[x.dtype], B, H, S, D, int(pos0),
+                            float(theta), _stream(stream)), "rope_apply")
+    return y
+
+
+def attn_prefill(q, k, v, causal=True, softmax_scale=0.0, rope=False, rope_theta=10000.0,
+                 pos0=0, o=None, lse=None, want_lse=False, q_scale=1.0, k_scale=1.0,
+                 v_scale=1.0, stream=None):
+    """O [B,Hq,S,D] bf16 (and LSE [B,Hq,S] fp32 when requested) for q [B,Hq,S,D], k/v [B,Hkv,S,D]."""
+    _require_cuda(q, k, v, o, lse)
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    if o is None:
+        o = torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _check(lib().attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                              DTYPE_CODES[q.dtype], float(q_scale), float(k_scale),
+                              float(v_scale), B, Hq, Hkv, S, D, int(bool(causal)),
+                              float(softmax_scale), int(bool(rope)), float(rope_theta), int(pos0),
+                              _stream(stream)), "attn_prefill")
+    return (o, lse) if (want_lse or lse is not None) else o
+
+
+def attn_decode_workspace_size(B, Hq, Hkv, D, Lmax):
+    return int(lib().attn_decode_workspace_size(B, Hq, Hkv, D, Lmax))
+
+
+def attn_decode(q, k_cache, v_cache, cache_len, o=None, lse=None, want_lse=False,
+                softmax_scale=0.0, rope=True, rope_theta=10000.0, workspace=None, stream=None):
+    """O [B,Hq,D] for q [B,Hq,D] against caches [B,Hkv,Lmax,D] with device cache_len [B]."""
+    _require_cuda(q, k_cache, v_cache, cache_len, o, lse, workspace)
+    B, Hq, D = q.shape
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    if o is None:
+        o = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = attn_decode_workspace_size(B, Hq, Hkv, D, Lmax)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len), Lmax,
+                             _ptr(o), _ptr(lse), DTYPE_CODES[q.dtype], B, Hq, Hkv, D,
+                             float(softmax_scale), int(bool(rope)), float(rope_theta),
+                             _ptr(workspace), wbytes, _stream(stream)), "attn_decode")
+    return (o, lse) if (want_lse or lse is not None) else o
+
+
+def attn_decode_latent_workspace_size(B, H, Lmax):
+    return int(lib().attn_decode_latent_workspace_size(B, H, Lmax))
+
+
+def attn_decode_latent(q, c_cache, cache_len, o=None, lse=None, want_lse=False,
+                       softmax_scale=0.0, rope=True, rope_theta=10000.0, workspace=None,
+                       stream=None):
+    """O [B,H,448] for q [B,H,512] against the latent cache [B,Lmax,512]."""
+    _require_cuda(q, c_cache, cache_len, o, lse, workspace)
+    B, H, _ = q.shape
+    Lmax = c_cache.shape[1]
+    if o is None:
+        o = torch.empty((B, H, 448), dtype=torch.bfloat16, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    need = attn_decode_latent_workspace_size(B, H, Lmax)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().attn_decode_latent(_ptr(q), _ptr(c_cache), _ptr(cache_len), Lmax, _ptr(o),
+                                    _ptr(lse), B, H, float(softmax_scale), int(bool(rope)),
+                                    float(rope_theta), _ptr(workspace), wbytes,
+                                    _stream(stream)), "attn_decode_latent")
+    return (o, lse) if (want_lse or lse is not None) else o
+
+
+def attn_rope_table_reserve(D, theta, max_pos):
+    _check(lib().attn_rope_table_reserve(int(D), float(theta), int(max_pos)),
+           "attn_rope_table_reserve")
+
+
+def attn_get_device_status(stream=None) -> int:
+    out = ctypes.c_int(-1)
+    _check(lib().attn_get_device_status(_stream(stream), ctypes.byref(out)),
+           "attn_get_device_status")
+    return out.value
+
+
+def attn_status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def attn_version() -> int:
+    return int(lib().attn_version())

@@ -1,0 +1,195 @@
+// api.cpp — the C ABI: argument validation, workspace planning and dispatch to the kernels.
+// Validation happens entirely on the host before anything is enqueued, so an invalid call
+// returns its status without touching the GPU (this is what the CPU-only tests exercise).
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+
+using namespace attn;
+
+namespace {
+
+cudaStream_t as_stream(attn_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool finite_pos(float x) { return std::isfinite(x) && x > 0.f; }
+
+bool overlap_partial(const void* a, const void* b, size_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  if (x == y) return false;
+  return x < y + bytes && y < x + bytes;
+}
+
+size_t dtype_bytes(attn_dtype_t dt) { return dt == ATTN_BF16 ? 2 : 1; }
+
+bool valid_dtype(int dt) { return dt == ATTN_BF16 || dt == ATTN_FP8_E5M2; }
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA runtime or launch error";
+    case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    case ATTN_ERR_NO_DEVICE: return "no usable sm_100-family CUDA device";
+    case ATTN_ERR_DEVICE_ARG: return "device-resident argument out of range";
+  }
+  return "unknown status";
+}
+
+int attn_version(void) { return 100; }
+
+attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, int B, int H, int S, int D,
+                         int pos0, float theta, attn_stream_t stream) {
+  if (!x || !y || !aligned16(x) || !aligned16(y)) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1 || D < 2 || D > 256 || (D & 1) || pos0 < 0) return ATTN_ERR_INVALID_ARG;
+  if (!finite_pos(theta)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(pos0) + S > (1LL << 30)) return ATTN_ERR_INVALID_ARG;
+  const size_t bytes = static_cast<size_t>(B) * H * S * D * dtype_bytes(dtype);
+  if (overlap_partial(x, y, bytes)) return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  const float2* tab = rope_table(D, theta, pos0 + S, &st);
+  if (!tab) return st;
+  return launch_rope(x, y, dtype, B, H, S, D, pos0, tab, as_stream(stream));
+}
+
+attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                           attn_dtype_t dtype, float q_scale, float k_scale, float v_scale,
+                           int B, int Hq, int Hkv, int S, int D, int causal, float softmax_scale,
+                           int rope, float rope_theta, int pos0, attn_stream_t stream) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  if (rope && (!finite_pos(rope_theta) || pos0 < 0)) return ATTN_ERR_INVALID_ARG;
+  if (!finite_pos(q_scale) || !finite_pos(k_scale) || !finite_pos(v_scale))
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(S) > (1LL << 30) || static_cast<long long>(B) * Hq > (1LL << 24))
+    return ATTN_ERR_UNSUPPORTED;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  const float2* tab = nullptr;
+  if (rope) {
+    tab = rope_table(D, rope_theta, pos0 + S, &st);
+    if (!tab) return st;
+  }
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return launch_prefill(q, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, S, D,
+                        causal, scale, tab, pos0, as_stream(stream));
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int Lmax) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || (D != 64 && D != 128) || Hq % Hkv) return 0;
+  return plan_decode(B, Hq, Hkv, D, Lmax).ws_bytes;
+}
+
+attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* cache_len, int Lmax, void* o, float* lse,
+                          attn_dtype_t dtype, int B, int Hq, int Hkv, int D, float softmax_scale,
+                          int rope, float rope_theta, void* workspace, size_t workspace_bytes,
+                          attn_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !cache_len || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+    return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cache_len) & 3u) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16 || dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(Lmax) > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  const DecodePlan plan = plan_decode(B, Hq, Hkv, D, Lmax);
+  if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes ||
+                            !aligned16(workspace)))
+    return ATTN_ERR_WORKSPACE;
+  const float2* tab = nullptr;
+  if (rope) {
+    tab = rope_table(D, rope_theta, Lmax + 1, &st);
+    if (!tab) return st;
+  }
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return launch_decode(q, k_cache, v_cache, cache_len, Lmax, o, lse, B, Hq, Hkv, D, scale, tab,
+                       workspace, plan, as_stream(stream));
+}
+
+size_t attn_decode_latent_workspace_size(int B, int H, int Lmax) {
+  if (B < 1 || H < 1 || H > 16 || Lmax < 1) return 0;
+  return plan_latent(B, H, Lmax).ws_bytes;
+}
+
+attn_status_t attn_decode_latent(const void* q, const void* c_cache, const int32_t* cache_len,
+                                 int Lmax, void* o, float* lse, int B, int H,
+                                 float softmax_scale, int rope, float rope_theta,
+                                 void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if (!q || !c_cache || !cache_len || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(c_cache) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cache_len) & 3u) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Lmax < 1) return ATTN_ERR_INVALID_ARG;
+  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
+  if (H > 16) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(Lmax) > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  const DecodePlan plan = plan_latent(B, H, Lmax);
+  if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes ||
+                            !aligned16(workspace)))
+    return ATTN_ERR_WORKSPACE;
+  const float2* tab = nullptr;
+  if (rope) {
+    tab = rope_table(64, rope_theta, Lmax + 1, &st);
+    if (!tab) return st;
+  }
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(512.0f);
+  return launch_latent(q, c_cache, cache_len, Lmax, o, lse, B, H, scale, tab, workspace, plan,
+                       as_stream(stream));
+}
+
+attn_status_t attn_rope_table_reserve(int D, float theta, int max_pos) {
+  if (D < 2 || D > 512 || (D & 1) || !finite_pos(theta) || max_pos < 0 || max_pos >= (1 << 30))
+    return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  return rope_table(D, theta, max_pos + 1, &st) ? ATTN_OK : st;
+}
+
+attn_status_t attn_get_device_status(attn_stream_t stream, int* status_out) {
+  if (!status_out) return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned int* p = device_status_ptr();
+  if (!p) return ATTN_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (cudaMemset(p, 0, sizeof(word)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  *status_out = (word & (1u << ATTN_ERR_TIMEOUT))      ? ATTN_ERR_TIMEOUT
+                : (word & (1u << ATTN_ERR_DEVICE_ARG)) ? ATTN_ERR_DEVICE_ARG
+                                                       : ATTN_OK;
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,764 @@
+// decode.cu — single-token decode against a static cache: grouped-query split-KV decode, the
+// absorbed-latent (MLA-style) decode, and the log-sum-exp combine of split partials.
+//
+// Both decode kernels are HBM-bound (4 and 30 useful flop per cache byte), so the design goal is
+// to keep enough cache bytes in flight: a persistent grid, one TMA producer warp per CTA
+// streaming 64-key tiles of the cache through a multi-stage mbarrier ring (128-byte swizzled, so
+// ldmatrix reads are bank-conflict free), and four compute warps that consume each tile with
+// warp-level bf16 MMAs.  The GQA group's query heads (G = Hq/Hkv <= 16) share one 16-row MMA
+// tile, so every K/V byte is read from HBM once for the whole group (Fixed-budget decode audit —
+// 2026-09-11, "What theory can and cannot establish": once-per-KV-head reuse; the padded row
+// tile is the same observation).  Work items are (sequence, KV head, split of the key range);
+// splits are merged by their log-sum-exp ("A: group-entry queries and one joint history scan").
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kTileKeys = 64;
+constexpr int kComputeWarps = 4;
+constexpr int kThreads = (kComputeWarps + 1) * 32;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+__device__ __forceinline__ void compute_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kComputeWarps * 32) : "memory");
+}
+
+struct GqaParams {
+  const __nv_bfloat16* q;
+  const int32_t* lens;
+  __nv_bfloat16* o;
+  float* lse;
+  float* ws_o;    // [B*Hq, nsplit, D] fp32 partial outputs (normalised)
+  float* ws_lse;  // [B*Hq, nsplit] fp32 partial log2-sum-exp (scaled-log2 domain)
+  const float2* table;
+  unsigned int* status;
+  int B, Hq, Hkv, G, Lmax, nsplit, chunk;
+  float scale_log2;  // softmax_scale * log2(e)
+};
+
+template <int D, int NST>
+struct GqaSmem {
+  static constexpr int kTileBytes = kTileKeys * D * 2;  // one K (or V) tile
+  static constexpr int kQPitch = D * 2 + 16;            // padded row pitch of the query tile
+  static constexpr int kStageOff = 0;
+  static constexpr int kQOff = NST * 2 * kTileBytes;
+  static constexpr int kRedOff = kQOff + 16 * kQPitch;      // m, l per warp per row
+  static constexpr int kOOff = kRedOff + 2 * kComputeWarps * 16 * 4;
+  static int bytes(int G) { return kOOff + kComputeWarps * G * D * 4 + 2 * NST * 8 + 1024; }
+};
+
+// Grouped-query split-KV decode.  Grid: persistent; items (b, kv head, split) in row-major
+// order, CTA c takes items c, c + grid, ...
+template <int D, int NST>
+__global__ void __launch_bounds__(kThreads, 2)
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
+  using L = GqaSmem<D, NST>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int G = p.G;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOOff + kComputeWarps * G * D * 4);
+  uint64_t* empty = full + NST;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_items = p.B * p.Hkv * p.nsplit;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kComputeWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kComputeWarps) {
+    // ---------------- producer warp: stream K/V tiles of every item of this CTA ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int sp = it % p.nsplit;
+        const int bh = it / p.nsplit;  // b * Hkv + kv head
+        const int b = bh / p.Hkv;
+        int len = p.lens[b];
+        if (len < 1 || len > p.Lmax) len = 0;
+        const int k0 = sp * p.chunk;
+        const int k1 = min(k0 + p.chunk, len);
+        for (int t0 = k0; t0 < k1; t0 += kTileKeys) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) return;
+          mbar_arrive_expect_tx(&full[stage], 2 * L::kTileBytes);
+          uint8_t* kt = smem + L::kStageOff + stage * 2 * L::kTileBytes;
+          uint8_t* vt = kt + L::kTileBytes;
+#pragma unroll
+          for (int bx = 0; bx < D / 64; ++bx) {
+            tma_load_3d(kt + bx * kTileKeys * 128, &tmK, &full[stage], bx * 64, t0, bh);
+            tma_load_3d(vt + bx * kTileKeys * 128, &tmV, &full[stage], bx * 64, t0, bh);
+          }
+          if (++stage == NST) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- compute warps ----------------
+  const int tid = threadIdx.x;  // 0..127
+  const int g = lane >> 2, tq = lane & 3;
+  uint8_t* qs = smem + L::kQOff;
+  float* red_m = reinterpret_cast<float*>(smem + L::kRedOff);
+  float* red_l = red_m + kComputeWarps * 16;
+  float* red_o = reinterpret_cast<float*>(smem + L::kOOff);
+  const uint32_t qs_addr = smem_u32(qs);
+  int stage = 0;
+  uint32_t phase = 0;
+  bool alive = true;
+
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const int sp = it % p.nsplit;
+    const int bh = it / p.nsplit;
+    const int b = bh / p.Hkv, kvh = bh % p.Hkv;
+    int len = p.lens[b];
+    const bool valid = len >= 1 && len <= p.Lmax;
+    if (!valid) {
+      if (tid == 0 && sp == 0) report_status(p.status, ATTN_ERR_DEVICE_ARG);
+      len = 0;
+    }
+    const int k0 = sp * p.chunk;
+    const int k1 = min(k0 + p.chunk, len);
+
+    // query tile: G rows (rotated at position len), zero-padded to 16 rows
+    compute_bar_sync();
+    for (int idx = tid; idx < 16 * (D / 2); idx += kComputeWarps * 32) {
+      const int r = idx / (D / 2), i = idx % (D / 2);
+      float x1 = 0.f, x2 = 0.f;
+      if (r < G && valid) {
+        const __nv_bfloat16* qr = p.q + (static_cast<size_t>(b) * p.Hq + kvh * G + r) * D;
+        x1 = __bfloat162float(qr[i]);
+        x2 = __bfloat162float(qr[i + D / 2]);
+        if (p.table) {
+          const float2 cs = p.table[static_cast<size_t>(len) * (D / 2) + i];
+          const float y1 = x1 * cs.x - x2 * cs.y;
+          const float y2 = x2 * cs.x + x1 * cs.y;
+          x1 = y1;
+          x2 = y2;
+        }
+      }
+      __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(qs + r * L::kQPitch);
+      row[i] = __float2bfloat16_rn(x1);
+      row[i + D / 2] = __float2bfloat16_rn(x2);
+    }
+    compute_bar_sync();
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+      ldsm_x4(qs_addr + (lane & 15) * L::kQPitch + (kk * 16 + (lane >> 4) * 8) * 2, qa[kk][0],
+              qa[kk][1], qa[kk][2], qa[kk][3]);
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float acc[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+    for (int t0 = k0; t0 < k1 && alive; t0 += kTileKeys) {
+      if (!mbar_wait(&full[stage], phase, p.status)) {
+        alive = false;
+        break;
+      }
+      const uint8_t* kt = smem + L::kStageOff + stage * 2 * L::kTileBytes;
+      const uint32_t kt_addr = smem_u32(kt);
+      const uint32_t vt_addr = kt_addr + L::kTileBytes;
+      // S (16 query rows x this warp's 16 keys)
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int m = lane >> 3;
+        const int key = warp * 16 + (m >> 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int c = kk * 2 + (m & 1);  // 16-byte chunk index along d
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kt_addr + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2,
+                  b3);
+          mma_bf16_16816(s[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+          mma_bf16_16816(s[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+        }
+      }
+      // scale, mask keys >= k1, online softmax (rows g and g + 8)
+      float rm0 = -INFINITY, rm1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int key = t0 + warp * 16 + nt * 8 + tq * 2 + (j & 1);
+          const float v = key < k1 ? s[nt][j] * p.scale_log2 : -INFINITY;
+          s[nt][j] = v;
+          if (j < 2)
+            rm0 = fmaxf(rm0, v);
+          else
+            rm1 = fmaxf(rm1, v);
+        }
+      rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 1));
+      rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 2));
+      rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 1));
+      rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 2));
+      const float mn0 = fmaxf(m0, rm0), mn1 = fmaxf(m1, rm1);
+      const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float c0 = fast_exp2(m0 - base0), c1 = fast_exp2(m1 - base1);
+      m0 = mn0;
+      m1 = mn1;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        s[nt][0] = fast_exp2(s[nt][0] - base0);
+        s[nt][1] = fast_exp2(s[nt][1] - base0);
+        s[nt][2] = fast_exp2(s[nt][2] - base1);
+        s[nt][3] = fast_exp2(s[nt][3] - base1);
+        ps0 += s[nt][0] + s[nt][1];
+        ps1 += s[nt][2] + s[nt][3];
+      }
+      l0 = l0 * c0 + ps0;
+      l1 = l1 * c1 + ps1;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        acc[n][0] *= c0;
+        acc[n][1] *= c0;
+        acc[n][2] *= c1;
+        acc[n][3] *= c1;
+      }
+      const uint32_t pa0 = pack_bf16(s[0][0], s[0][1]);
+      const uint32_t pa1 = pack_bf16(s[0][2], s[0][3]);
+      const uint32_t pa2 = pack_bf16(s[1][0], s[1][1]);
+      const uint32_t pa3 = pack_bf16(s[1][2], s[1][3]);
+      // O += P V over this warp's 16 keys
+      {
+        const int m = lane >> 3;
+        const int key = warp * 16 + (m & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int n2 = 0; n2 < D / 16; ++n2) {
+          const int c = n2 * 2 + (m >> 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vt_addr + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2,
+                    b3);
+          mma_bf16_16816(acc[2 * n2], pa0, pa1, pa2, pa3, b0, b1);
+          mma_bf16_16816(acc[2 * n2 + 1], pa0, pa1, pa2, pa3, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (++stage == NST) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    if (!alive) return;
+
+    // merge the four warps' partial states (each covered a quarter of every tile's keys)
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if (tq == 0) {
+      red_m[warp * 16 + g] = m0;
+      red_m[warp * 16 + g + 8] = m1;
+      red_l[warp * 16 + g] = l0;
+      red_l[warp * 16 + g + 8] = l1;
+    }
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      const int d = n * 8 + tq * 2;
+      if (g < G) {
+        red_o[(warp * G + g) * D + d] = acc[n][0];
+        red_o[(warp * G + g) * D + d + 1] = acc[n][1];
+      }
+      if (g + 8 < G) {
+        red_o[(warp * G + g + 8) * D + d] = acc[n][2];
+        red_o[(warp * G + g + 8) * D + d + 1] = acc[n][3];
+      }
+    }
+    compute_bar_sync();
+    for (int idx = tid; idx < G * D; idx += kComputeWarps * 32) {
+      const int r = idx / D, d = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, red_m[w * 16 + r]);
+      float lsum = 0.f, osum = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kComputeWarps; ++w) {
+          const float mw = red_m[w * 16 + r];
+          const float wgt = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+          lsum += wgt * red_l[w * 16 + r];
+          osum += wgt * red_o[(w * G + r) * D + d];
+        }
+      }
+      const float o = lsum > 0.f ? osum / lsum : 0.f;
+      const float lse2 = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
+      const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + r;
+      if (p.nsplit == 1) {
+        p.o[row * D + d] = __float2bfloat16_rn(o);
+        if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
+      } else {
+        p.ws_o[(row * p.nsplit + sp) * D + d] = o;
+        if (d == 0) p.ws_lse[row * p.nsplit + sp] = lse2;
+      }
+    }
+  }
+}
+
+// Merge the split partials of one (sequence, query head) row per block.
+__global__ void __launch_bounds__(128)
+    combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse, int nsplit,
+                   int D, __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  const size_t row = blockIdx.x;
+  const float* lp = ws_lse + row * nsplit;
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, lp[s]);
+  float wsum = 0.f;
+  for (int s = 0; s < nsplit; ++s) wsum += lp[s] == -INFINITY ? 0.f : exp2f(lp[s] - M);
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float acc = 0.f;
+    if (wsum > 0.f)
+      for (int s = 0; s < nsplit; ++s)
+        if (lp[s] != -INFINITY) acc += exp2f(lp[s] - M) * ws_o[(row * nsplit + s) * D + d];
+    o[row * D + d] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+  }
+  if (lse && threadIdx.x == 0) lse[row] = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Absorbed latent decode: all H (<= 16) heads of a sequence share each 512-dim cache row.
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kLatQK = 512;
+constexpr int kLatV = 448;
+constexpr int kLatRope = 64;
+constexpr int kLatStages = 3;
+constexpr int kLatTileBytes = kTileKeys * kLatQK * 2;  // 64 KB
+constexpr int kLatQPitch = kLatQK * 2 + 16;
+constexpr int kLatPPitch = kTileKeys * 2 + 16;
+constexpr int kLatColsPerWarp = kLatV / kComputeWarps;  // 112 = 14 n-tiles
+
+struct LatSmem {
+  static constexpr int kQOff = kLatStages * kLatTileBytes;
+  static constexpr int kPOff = kQOff + 16 * kLatQPitch;
+  static constexpr int kRedOff = kPOff + 2 * 16 * kLatPPitch;       // [2][warps][16] row max
+  static constexpr int kLOff = kRedOff + 2 * kComputeWarps * 16 * 4;  // [warps][16] row sums
+  static constexpr int kBarOff = kLOff + kComputeWarps * 16 * 4;
+  static constexpr int kBytes = kBarOff + 2 * kLatStages * 8 + 1024;
+};
+
+struct LatParams {
+  const __nv_bfloat16* q;
+  const int32_t* lens;
+  __nv_bfloat16* o;
+  float* lse;
+  float* ws_o;
+  float* ws_lse;
+  const float2* table;  // D = 64 table for the RoPE dims
+  unsigned int* status;
+  int B, H, Lmax, nsplit, chunk;
+  float scale_log2;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    latent_decode_kernel(const __grid_constant__ CUtensorMap tmC, const LatParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + LatSmem::kBarOff);
+  uint64_t* empty = full + kLatStages;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_items = p.B * p.nsplit;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLatStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kComputeWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kComputeWarps) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmC);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int sp = it % p.nsplit, b = it / p.nsplit;
+        int len = p.lens[b];
+        if (len < 1 || len > p.Lmax) len = 0;
+        const int k0 = sp * p.chunk, k1 = min(k0 + p.chunk, len);
+        for (int t0 = k0; t0 < k1; t0 += kTileKeys) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) return;
+          mbar_arrive_expect_tx(&full[stage], kLatTileBytes);
+          uint8_t* ct = smem + stage * kLatTileBytes;
+#pragma unroll
+          for (int bx = 0; bx < kLatQK / 64; ++bx)
+            tma_load_3d(ct + bx * kTileKeys * 128, &tmC, &full[stage], bx * 64, t0, b);
+          if (++stage == kLatStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  const int tid = threadIdx.x;
+  const int g = lane >> 2, tq = lane & 3;
+  uint8_t* qs = smem + LatSmem::kQOff;
+  const uint32_t qs_addr = smem_u32(qs);
+  const uint32_t ps_addr0 = smem_u32(smem + LatSmem::kPOff);
+  float* red = reinterpret_cast<float*>(smem + LatSmem::kRedOff);
+  float* lred = reinterpret_cast<float*>(smem + LatSmem::kLOff);
+  int stage = 0;
+  uint32_t phase = 0;
+  int tcount = 0;
+  const int H = p.H;
+
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const int sp = it % p.nsplit, b = it / p.nsplit;
+    int len = p.lens[b];
+    const bool valid = len >= 1 && len <= p.Lmax;
+    if (!valid) {
+      if (tid == 0 && sp == 0) report_status(p.status, ATTN_ERR_DEVICE_ARG);
+      len = 0;
+    }
+    const int k0 = sp * p.chunk, k1 = min(k0 + p.chunk, len);
+
+    compute_bar_sync();
+    // query rows: 448 latent dims as given, the 64 RoPE dims rotated at position len
+    for (int idx = tid; idx < 16 * (kLatQK / 2); idx += kComputeWarps * 32) {
+      const int r = idx / (kLatQK / 2), j = idx % (kLatQK / 2);
+      __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(qs + r * kLatQPitch);
+      const __nv_bfloat16* qr = p.q + (static_cast<size_t>(b) * H + r) * kLatQK;
+      if (j < kLatV / 2) {
+        row[2 * j] = (r < H && valid) ? qr[2 * j] : __float2bfloat16_rn(0.f);
+        row[2 * j + 1] = (r < H && valid) ? qr[2 * j + 1] : __float2bfloat16_rn(0.f);
+      } else if (j < kLatV / 2 + kLatRope / 2) {
+        const int i = j - kLatV / 2;  // pair (i, i + 32) of the RoPE part
+        float x1 = 0.f, x2 = 0.f;
+        if (r < H && valid) {
+          x1 = __bfloat162float(qr[kLatV + i]);
+          x2 = __bfloat162float(qr[kLatV + i + kLatRope / 2]);
+          if (p.table) {
+            const float2 cs = p.table[static_cast<size_t>(len) * (kLatRope / 2) + i];
+            const float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
+            x1 = y1;
+            x2 = y2;
+          }
+        }
+        row[kLatV + i] = __float2bfloat16_rn(x1);
+        row[kLatV + i + kLatRope / 2] = __float2bfloat16_rn(x2);
+      }
+    }
+    compute_bar_sync();
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float acc[kLatColsPerWarp / 8][4];
+#pragma unroll
+    for (int n = 0; n < kLatColsPerWarp / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+    for (int t0 = k0; t0 < k1; t0 += kTileKeys, ++tcount) {
+      if (!mbar_wait(&full[stage], phase, p.status)) return;
+      const uint32_t ct = smem_u32(smem + stage * kLatTileBytes);
+      const int par = tcount & 1;
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int m = lane >> 3;
+        const int key = warp * 16 + (m >> 1) * 8 + (lane & 7);
+#pragma unroll 8
+        for (int kk = 0; kk < kLatQK / 16; ++kk) {
+          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+          ldsm_x4(qs_addr + (lane & 15) * kLatQPitch + (kk * 16 + (lane >> 4) * 8) * 2, a0, a1,
+                  a2, a3);
+          const int c = kk * 2 + (m & 1);
+          ldsm_x4(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
+          mma_bf16_16816(s[0], a0, a1, a2, a3, b0, b1);
+          mma_bf16_16816(s[1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+      float rm0 = -INFINITY, rm1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int key = t0 + warp * 16 + nt * 8 + tq * 2 + (j & 1);
+          const float v = key < k1 ? s[nt][j] * p.scale_log2 : -INFINITY;
+          s[nt][j] = v;
+          if (j < 2)
+            rm0 = fmaxf(rm0, v);
+          else
+            rm1 = fmaxf(rm1, v);
+        }
+      rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 1));
+      rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 2));
+      rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 1));
+      rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 2));
+      if (tq == 0) {
+        red[(par * kComputeWarps + warp) * 16 + g] = rm0;
+        red[(par * kComputeWarps + warp) * 16 + g + 8] = rm1;
+      }
+      compute_bar_sync();
+      float tm0 = -INFINITY, tm1 = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kComputeWarps; ++w) {
+        tm0 = fmaxf(tm0, red[(par * kComputeWarps + w) * 16 + g]);
+        tm1 = fmaxf(tm1, red[(par * kComputeWarps + w) * 16 + g + 8]);
+      }
+      const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+      const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float c0 = fast_exp2(m0 - base0), c1 = fast_exp2(m1 - base1);
+      m0 = mn0;
+      m1 = mn1;
+      float ps0 = 0.f, ps1 = 0.f;
+      uint8_t* pw = smem + LatSmem::kPOff + par * 16 * kLatPPitch;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const float e0 = fast_exp2(s[nt][0] - base0), e1 = fast_exp2(s[nt][1] - base0);
+        const float e2 = fast_exp2(s[nt][2] - base1), e3 = fast_exp2(s[nt][3] - base1);
+        ps0 += e0 + e1;
+        ps1 += e2 + e3;
+        const int col = warp * 16 + nt * 8 + tq * 2;
+        *reinterpret_cast<uint32_t*>(pw + g * kLatPPitch + col * 2) = pack_bf16(e0, e1);
+        *reinterpret_cast<uint32_t*>(pw + (g + 8) * kLatPPitch + col * 2) = pack_bf16(e2, e3);
+      }
+      l0 = l0 * c0 + ps0;
+      l1 = l1 * c1 + ps1;
+#pragma unroll
+      for (int n = 0; n < kLatColsPerWarp / 8; ++n) {
+        acc[n][0] *= c0;
+        acc[n][1] *= c0;
+        acc[n][2] *= c1;
+        acc[n][3] *= c1;
+      }
+      compute_bar_sync();
+      // O[:, this warp's 112 columns] += P (16 x 64) * C[:, cols]
+      const uint32_t ps_addr = ps_addr0 + par * 16 * kLatPPitch;
+#pragma unroll
+      for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(ps_addr + (lane & 15) * kLatPPitch + (kk * 16 + (lane >> 4) * 8) * 2, a0, a1, a2,
+                a3);
+        const int m = lane >> 3;
+        const int key = kk * 16 + (m & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int n2 = 0; n2 < kLatColsPerWarp / 16; ++n2) {
+          const int c = (warp * kLatColsPerWarp) / 8 + n2 * 2 + (m >> 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
+          mma_bf16_16816(acc[2 * n2], a0, a1, a2, a3, b0, b1);
+          mma_bf16_16816(acc[2 * n2 + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (++stage == kLatStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+
+    // every warp used the same running max; row sums are split by key quarter
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if (tq == 0) {
+      lred[warp * 16 + g] = l0;
+      lred[warp * 16 + g + 8] = l1;
+    }
+    compute_bar_sync();
+    float lt0 = 0.f, lt1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kComputeWarps; ++w) {
+      lt0 += lred[w * 16 + g];
+      lt1 += lred[w * 16 + g + 8];
+    }
+    const float inv0 = lt0 > 0.f ? 1.f / lt0 : 0.f, inv1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
+    const float lse0 = lt0 > 0.f ? m0 + log2f(lt0) : -INFINITY;
+    const float lse1 = lt1 > 0.f ? m1 + log2f(lt1) : -INFINITY;
+#pragma unroll
+    for (int n = 0; n < kLatColsPerWarp / 8; ++n) {
+      const int d = warp * kLatColsPerWarp + n * 8 + tq * 2;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = g + hh * 8;
+        if (r >= H) continue;
+        const float inv = hh ? inv1 : inv0;
+        const size_t row = static_cast<size_t>(b) * H + r;
+        const float o0 = acc[n][hh * 2] * inv, o1 = acc[n][hh * 2 + 1] * inv;
+        if (p.nsplit == 1) {
+          *reinterpret_cast<uint32_t*>(p.o + row * kLatV + d) = pack_bf16(o0, o1);
+        } else {
+          float* wo = p.ws_o + (row * p.nsplit + sp) * kLatV + d;
+          wo[0] = o0;
+          wo[1] = o1;
+        }
+      }
+    }
+    if (tq == 0 && warp == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = g + hh * 8;
+        if (r >= H) continue;
+        const size_t row = static_cast<size_t>(b) * H + r;
+        const float l2 = hh ? lse1 : lse0;
+        if (p.nsplit == 1) {
+          if (p.lse) p.lse[row] = l2 * kLn2;
+        } else {
+          p.ws_lse[row * p.nsplit + sp] = l2;
+        }
+      }
+    }
+  }
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Pick the number of key-range splits.  Cost model in bytes of HBM traffic (the kernels are
+// bandwidth bound): a CTA streams at most twice its fair share of the bandwidth, so the time is
+// max(busiest CTA's bytes * ctas / 2, all cache bytes) plus the split partials written and read
+// back by the combine.
+DecodePlan plan_common(int units, int Lmax, int ctas, double key_bytes, int rows_per_unit,
+                       int out_dim) {
+  const int max_split = std::max(1, (Lmax + kTileKeys - 1) / kTileKeys);
+  int best = 1;
+  double best_cost = 1e300;
+  for (int ns = 1; ns <= max_split; ns *= 2) {
+    const int chunk = round_up((Lmax + ns - 1) / ns, kTileKeys);
+    const int nsp = (Lmax + chunk - 1) / chunk;
+    const double items = static_cast<double>(units) * nsp;
+    const double waves = std::ceil(items / ctas);
+    const double part = nsp > 1 ? static_cast<double>(rows_per_unit) * (out_dim + 1) * 4 : 0.0;
+    const double busiest = waves * (chunk * key_bytes + part);
+    const double total = static_cast<double>(units) * Lmax * key_bytes;
+    const double cost = std::max(busiest * ctas / 2.0, total) + 2.0 * items * part;
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = nsp;
+    }
+  }
+  DecodePlan pl;
+  pl.chunk = round_up((Lmax + best - 1) / best, kTileKeys);
+  pl.nsplit = (Lmax + pl.chunk - 1) / pl.chunk;
+  pl.grid = ctas;
+  pl.ws_bytes = pl.nsplit > 1
+                    ? static_cast<size_t>(units) * rows_per_unit * pl.nsplit * (out_dim + 1) * 4
+                    : 0;
+  return pl;
+}
+
+template <int D>
+attn_status_t launch_gqa_typed(const void* q, const void* k, const void* v, const int32_t* lens,
+                               int Lmax, void* o, float* lse, int B, int Hq, int Hkv, float scale,
+                               const float2* table, void* ws, const DecodePlan& plan,
+                               cudaStream_t st) {
+  constexpr int NST = 3;
+  using L = GqaSmem<D, NST>;
+  CUtensorMap tk, tv;
+  if (!make_tmap_3d(&tk, k, 2, D, Lmax, static_cast<uint64_t>(B) * Hkv, 64, kTileKeys, 128) ||
+      !make_tmap_3d(&tv, v, 2, D, Lmax, static_cast<uint64_t>(B) * Hkv, 64, kTileKeys, 128))
+    return ATTN_ERR_CUDA;
+  GqaParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.lens = lens;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  const size_t rows = static_cast<size_t>(B) * Hq;
+  p.ws_o = plan.nsplit > 1 ? static_cast<float*>(ws) : nullptr;
+  p.ws_lse = plan.nsplit > 1 ? static_cast<float*>(ws) + rows * plan.nsplit * D : nullptr;
+  p.table = table;
+  p.status = device_status_ptr();
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.Lmax = Lmax;
+  p.nsplit = plan.nsplit;
+  p.chunk = plan.chunk;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int smem = L::bytes(p.G);
+  auto kern = gqa_decode_kernel<D, NST>;
+  if (!set_smem_attr(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
+  const int items = B * Hkv * plan.nsplit;
+  const int grid = std::min(items, plan.grid);
+  kern<<<grid, kThreads, smem, st>>>(tk, tv, p);
+  if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
+  if (plan.nsplit > 1) {
+    combine_kernel<<<static_cast<unsigned>(rows), 128, 0, st>>>(p.ws_o, p.ws_lse, plan.nsplit, D,
+                                                              p.o, lse);
+    return launch_status();
+  }
+  return ATTN_OK;
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int Lmax) {
+  return plan_common(B * Hkv, Lmax, 2 * sm_count(), 2.0 * D * 2, Hq / Hkv, D);
+}
+
+DecodePlan plan_latent(int B, int H, int Lmax) {
+  return plan_common(B, Lmax, sm_count(), kLatQK * 2, H, kLatV);
+}
+
+attn_status_t launch_decode(const void* q, const void* k, const void* v, const int32_t* lens,
+                            int Lmax, void* o, float* lse, int B, int Hq, int Hkv, int D,
+                            float scale, const float2* table, void* ws, const DecodePlan& plan,
+                            cudaStream_t st) {
+  if (D == 128)
+    return launch_gqa_typed<128>(q, k, v, lens, Lmax, o, lse, B, Hq, Hkv, scale, table, ws, plan,
+                                 st);
+  return launch_gqa_typed<64>(q, k, v, lens, Lmax, o, lse, B, Hq, Hkv, scale, table, ws, plan,
+                              st);
+}
+
+attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, int Lmax, void* o,
+                            float* lse, int B, int H, float scale, const float2* table, void* ws,
+                            const DecodePlan& plan, cudaStream_t st) {
+  CUtensorMap tc;
+  if (!make_tmap_3d(&tc, c, 2, kLatQK, Lmax, B, 64, kTileKeys, 128)) return ATTN_ERR_CUDA;
+  LatParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.lens = lens;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  const size_t rows = static_cast<size_t>(B) * H;
+  p.ws_o = plan.nsplit > 1 ? static_cast<float*>(ws) : nullptr;
+  p.ws_lse = plan.nsplit > 1 ? static_cast<float*>(ws) + rows * plan.nsplit * kLatV : nullptr;
+  p.table = table;
+  p.status = device_status_ptr();
+  p.B = B;
+  p.H = H;
+  p.Lmax = Lmax;
+  p.nsplit = plan.nsplit;
+  p.chunk = plan.chunk;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  if (!set_smem_attr(reinterpret_cast<const void*>(latent_decode_kernel), LatSmem::kBytes))
+    return ATTN_ERR_CUDA;
+  const int items = B * plan.nsplit;
+  const int grid = std::min(items, plan.grid);
+  latent_decode_kernel<<<grid, kThreads, LatSmem::kBytes, st>>>(tc, p);
+  if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
+  if (plan.nsplit > 1) {
+    combine_kernel<<<static_cast<unsigned>(rows), 128, 0, st>>>(p.ws_o, p.ws_lse, plan.nsplit,
+                                                              kLatV, p.o, lse);
+    return launch_status();
+  }
+  return ATTN_OK;
+}
+
+}  // namespace attn

@@ -1,0 +1,75 @@
+// internal.h — declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+// Device status word (an unsigned int in device global memory, one per device).  Kernels OR
+// in (1 << attn_status_t).  Returns nullptr if it could not be resolved.
+unsigned int* device_status_ptr();
+
+// Number of SMs of the current device (152 if no device is visible).
+int sm_count();
+
+// True when the current device is an sm_100-family part this library was built for.
+attn_status_t check_device();
+
+// Cos/sin table for (D, theta) covering positions [0, npos): float2 {cos, sin} laid out
+// [pos][D/2].  Builds or grows it on the current device on first use (synchronous cudaMalloc +
+// copy).  Returns nullptr on failure and sets *err.
+const float2* rope_table(int D, float theta, int npos, attn_status_t* err);
+
+// Encode a 3-D tiled TMA descriptor for a dense row-major tensor of `elem_bytes`-byte elements
+// with logical sizes {inner, mid, outer} (innermost first), box {box_inner, box_mid, 1} and
+// 128-byte swizzling.  Returns false on failure.
+bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
+                  uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid,
+                  int swizzle_bytes);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize), done once per (kernel, device, size).
+bool set_smem_attr(const void* kernel, int bytes);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch-status helper: map the last launch error to a status.
+inline attn_status_t launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------------
+// entry points implemented per translation unit (called from api.cpp after validation)
+// ------------------------------------------------------------------------------------------
+attn_status_t launch_rope(const void* x, void* y, attn_dtype_t dt, int B, int H, int S, int D,
+                          int pos0, const float2* table, cudaStream_t st);
+
+struct DecodePlan {
+  int nsplit;      // splits of the key range per (b, kv head)
+  int chunk;       // keys per split (multiple of the key tile)
+  int grid;        // persistent CTAs
+  size_t ws_bytes; // partial O (fp32) + partial LSE (fp32)
+};
+DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int Lmax);
+DecodePlan plan_latent(int B, int H, int Lmax);
+
+attn_status_t launch_decode(const void* q, const void* k, const void* v, const int32_t* lens,
+                            int Lmax, void* o, float* lse, int B, int Hq, int Hkv, int D,
+                            float scale, const float2* table, void* ws, const DecodePlan& plan,
+                            cudaStream_t st);
+
+attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, int Lmax, void* o,
+                            float* lse, int B, int H, float scale, const float2* table, void* ws,
+                            const DecodePlan& plan, cudaStream_t st);
+
+attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                             attn_dtype_t dt, float q_scale, float k_scale, float v_scale, int B,
+                             int Hq, int Hkv, int S, int D, int causal, float scale,
+                             const float2* table, int pos0, cudaStream_t st);
+
+}  // namespace attn

@@ -1,0 +1,444 @@
+// prefill.cu — grouped-query attention prefill on the 5th-generation tensor cores (tcgen05).
+//
+// One persistent CTA per SM.  A work item is 256 query rows (two 128-row Q tiles) of one
+// (batch, query head); items are ordered heaviest-first for causal attention and dealt to CTAs
+// in a serpentine order (the persistent, causal-aware scheduling of the persistent-attention
+// refactor page, "概要").  Inside a CTA the roles are warp-specialised:
+//
+//   warp 8      TMA producer: Q tiles, then K_j / V_j tiles through a shared-memory ring
+//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, O_t += P_t V_j from TMEM
+//   warps 0-7   two softmax warpgroups, one per Q tile; each thread owns one query row (one
+//               TMEM lane): masks, online softmax in the exp2 domain, writes P (bf16) over its
+//               S columns in TMEM, rescales O lazily, and runs the epilogue.
+//
+// The two Q tiles ping-pong: while the softmax of tile 0 runs, the tensor core works on tile 1
+// (and the reverse), so the exponentials (the "softmax partition" the refactor page singles out
+// as the slow part, "性能ベンチマーク") overlap the matrix products.  TMEM holds S0, S1 (128
+// columns each) and O0, O1 (D columns each); P_t is written as packed bf16 into the first 64
+// columns of S_t and consumed by the next MMA as its A operand straight from TMEM.
+//
+// Lazy rescaling: the running row maximum used for the exponentials is only raised when a tile's
+// maximum exceeds it by more than 8 (log2 units); O and the row sum share that stale maximum, so
+// the final O / l is exact.
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;  // query rows per Q tile (TMEM lanes)
+constexpr int BN = 128;  // keys per KV tile
+constexpr int kRowsPerItem = 2 * BM;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kBoxes = D / 64;                 // 128-byte swizzle boxes per row
+  static constexpr int kQTileBytes = BM * D * 2;
+  static constexpr int kKVTileBytes = BN * D * 2;
+  static constexpr int kStages = D == 128 ? 4 : 6;      // K/V ring depth
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = 2 * kQTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kKVTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+};
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  unsigned int* status;
+  int B, Hq, Hkv, G, S, causal;
+  int n_items, nM, nKV;
+  float c_log2;   // softmax_scale * q_scale * k_scale * log2(e)
+  float v_scale;
+};
+
+struct Bars {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t kv_full[8], kv_empty[8];
+  uint32_t tmem_slot;
+};
+
+// Item -> (query block m, batch b, query head hq).  Causal items go heaviest (largest m) first.
+__device__ __forceinline__ void item_coords(const Params& p, int it, int& m, int& b, int& hq) {
+  const int per_m = p.B * p.Hq;
+  const int mi = it / per_m;
+  const int rest = it - mi * per_m;
+  m = p.causal ? (p.nM - 1 - mi) : mi;
+  b = rest / p.Hq;
+  hq = rest - b * p.Hq;
+}
+
+// KV tiles Q tile starting at row r0 must visit (0 when the tile is past the sequence).
+__device__ __forceinline__ int kv_tiles_for(const Params& p, int r0) {
+  if (r0 >= p.S) return 0;
+  if (!p.causal) return p.nKV;
+  return min(r0 / BN + 1, p.nKV);
+}
+
+// Serpentine assignment of items to persistent CTAs: round k visits CTAs forwards when k is even
+// and backwards when odd, so heavy and light items pair up.
+__device__ __forceinline__ int item_for(int round, int cta, int ncta) {
+  return round * ncta + ((round & 1) ? (ncta - 1 - cta) : cta);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->q_full[t], 1);
+      mbar_init(&bars->q_empty[t], 1);
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->o_full[t], 1);
+      mbar_init(&bars->o_empty[t], 128);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&bars->tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  const int rounds = (p.n_items + gridDim.x - 1) / gridDim.x;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t ph_qe[2] = {0, 0};
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int r = 0; r < rounds && ok; ++r) {
+        const int it = item_for(r, blockIdx.x, gridDim.x);
+        if (it >= p.n_items) continue;
+        int m, b, hq;
+        item_coords(p, it, m, b, hq);
+        const int hkv = hq / p.G;
+        int n[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) n[t] = kv_tiles_for(p, m * kRowsPerItem + t * BM);
+        const int nkv = max(n[0], n[1]);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (n[t] == 0 || !ok) continue;
+          ok = mbar_wait(&bars->q_empty[t], ph_qe[t] ^ 1, p.status);
+          ph_qe[t] ^= 1;
+          if (!ok) continue;
+          mbar_arrive_expect_tx(&bars->q_full[t], C::kQTileBytes);
+          uint8_t* dst = smem + C::kQOff + t * C::kQTileBytes;
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_3d(dst + bx * BM * 128, &tmQ, &bars->q_full[t], bx * 64,
+                        m * kRowsPerItem + t * BM, b * p.Hq + hq);
+        }
+        for (int j = 0; j < nkv && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
+            if (!(ok = mbar_wait(&bars->kv_empty[stage], ph ^ 1, p.status))) break;
+            mbar_arrive_expect_tx(&bars->kv_full[stage], C::kKVTileBytes);
+            uint8_t* dst = smem + C::kKVOff + stage * C::kKVTileBytes;
+            const CUtensorMap* tm = kv ? &tmV : &tmK;
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_3d(dst + bx * BN * 128, tm, &bars->kv_full[stage], bx * 64, j * BN,
+                          b * p.Hkv + hkv);
+            if (++stage == C::kStages) {
+              stage = 0;
+              ph ^= 1;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = make_idesc(1, 1, false, false, BN, BM);  // bf16 x bf16 -> f32
+      const uint32_t idesc_pv = make_idesc(1, 1, false, true, D, BM);   // V is MN-major
+      const uint32_t q_base = smem_u32(smem + C::kQOff);
+      const uint32_t kv_base = smem_u32(smem + C::kKVOff);
+      uint32_t ph_qf[2] = {0, 0}, ph_pf[2] = {0, 0}, ph_oe[2] = {0, 0};
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      auto issue_s = [&](int t, int slot) {
+        const uint32_t qa = q_base + t * C::kQTileBytes;
+        const uint32_t ka = kv_base + slot * C::kKVTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          const uint64_t ad = smem_desc(qa + off, 16, 1024, 2);
+          const uint64_t bd = smem_desc(ka + off, 16, 1024, 2);
+          umma_ss(tmem + (t ? C::kColS1 : C::kColS0), ad, bd, idesc_s, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const uint32_t va = kv_base + slot * C::kKVTileBytes;
+        const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = smem_desc(va + kk * 16 * 128, BN * 128, 1024, 2);
+          umma_ts(tmem + (t ? C::kColO1 : C::kColO0), pcol + kk * 8, bd, idesc_pv,
+                  (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      for (int r = 0; r < rounds && ok; ++r) {
+        const int it = item_for(r, blockIdx.x, gridDim.x);
+        if (it >= p.n_items) continue;
+        int m, b, hq;
+        item_coords(p, it, m, b, hq);
+        int n[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) n[t] = kv_tiles_for(p, m * kRowsPerItem + t * BM);
+        const int nkv = max(n[0], n[1]);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (n[t] == 0 || !ok) continue;
+          ok = mbar_wait(&bars->q_full[t], ph_qf[t], p.status);
+          ph_qf[t] ^= 1;
+        }
+        if (!ok) break;
+        // j = 0: S_t = Q_t K_0^T for both tiles
+        const int kslot = stage;
+        if (!(ok = mbar_wait(&bars->kv_full[kslot], ph, p.status))) break;
+        if (++stage == C::kStages) { stage = 0; ph ^= 1; }
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (n[t] == 0) continue;
+          issue_s(t, kslot);
+          umma_commit(&bars->s_full[t]);
+          if (n[t] == 1) umma_commit(&bars->q_empty[t]);
+        }
+        umma_commit(&bars->kv_empty[kslot]);
+        for (int j = 1; j <= nkv && ok; ++j) {
+          const int vslot = stage;
+          if (!(ok = mbar_wait(&bars->kv_full[vslot], ph, p.status))) break;
+          if (++stage == C::kStages) { stage = 0; ph ^= 1; }
+          int kslot2 = -1;
+          if (j < nkv) {
+            kslot2 = stage;
+            if (!(ok = mbar_wait(&bars->kv_full[kslot2], ph, p.status))) break;
+            if (++stage == C::kStages) { stage = 0; ph ^= 1; }
+          }
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok) continue;
+            if (j - 1 < n[t]) {
+              ok = mbar_wait(&bars->p_full[t], ph_pf[t], p.status);
+              ph_pf[t] ^= 1;
+              if (ok && j == 1) {
+                ok = mbar_wait(&bars->o_empty[t], ph_oe[t] ^ 1, p.status);
+                ph_oe[t] ^= 1;
+              }
+              if (!ok) continue;
+              tc_fence_after();
+              issue_pv(t, vslot, j > 1);
+              if (j - 1 == n[t] - 1) umma_commit(&bars->o_full[t]);
+            }
+            if (j < n[t]) {
+              issue_s(t, kslot2);
+              umma_commit(&bars->s_full[t]);
+              if (j == n[t] - 1) umma_commit(&bars->q_empty[t]);
+            }
+          }
+          umma_commit(&bars->kv_empty[vslot]);
+          if (kslot2 >= 0) umma_commit(&bars->kv_empty[kslot2]);
+        }
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;          // Q tile of this warpgroup
+    const int quarter = warp & 3;     // TMEM lane quarter of this warp
+    const int lrow = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (t ? C::kColS1 : C::kColS0);
+    const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
+    uint32_t ph_s = 0, ph_o = 0;
+    bool ok = true;
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int it = item_for(r, blockIdx.x, gridDim.x);
+      if (it >= p.n_items) continue;
+      int m, b, hq;
+      item_coords(p, it, m, b, hq);
+      const int r0 = m * kRowsPerItem + t * BM;
+      const int n = kv_tiles_for(p, r0);
+      if (n == 0) continue;
+      const int row = r0 + lrow;
+      float m_run = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        if (!(ok = mbar_wait(&bars->s_full[t], ph_s, p.status))) break;
+        ph_s ^= 1;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+        const bool need_mask = (p.causal && j == n - 1) || (j * BN + BN > p.S);
+        if (need_mask) {
+          const int lim = p.causal ? min(row + 1, p.S) : p.S;  // keys >= lim are hidden
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (j * BN + c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+        const float m_tile = mx * p.c_log2;
+        float f = 1.f;  // factor for O and l when the running maximum is raised
+        if (j == 0) {
+          m_run = m_tile;
+        } else if (m_tile > m_run + kRescaleThreshold) {
+          f = fast_exp2(m_run - m_tile);
+          l *= f;
+          m_run = m_tile;
+        }
+        const float neg_m = -m_run;
+        float sum = 0.f;
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][e]), p.c_log2, neg_m));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][e + 1]), p.c_log2, neg_m));
+            __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+            const float2 back = __bfloat1622float2(h);
+            sum += back.x + back.y;
+            pk[c >> 1][(c & 1) * 16 + e / 2] = *reinterpret_cast<uint32_t*>(&h);
+          }
+        l += sum;
+        tmem_st32(tS, pk[0]);
+        tmem_st32(tS + 32, pk[1]);
+        if (f != 1.f) {
+          // O_t holds the tiles before j (their PV completed before S_t(j) was signalled)
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+            tmem_st32(tO + c * 32, ov);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[t]);
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16, LSE
+      if (!(ok = mbar_wait(&bars->o_full[t], ph_o, p.status))) break;
+      ph_o ^= 1;
+      tc_fence_after();
+      const float inv = p.v_scale / l;
+      __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.S + row) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tO + c * 32, ov);
+        if (row < p.S) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(ov[q4 * 8 + 0]) * inv, __uint_as_float(ov[q4 * 8 + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(ov[q4 * 8 + 2]) * inv, __uint_as_float(ov[q4 * 8 + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(ov[q4 * 8 + 4]) * inv, __uint_as_float(ov[q4 * 8 + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(ov[q4 * 8 + 6]) * inv, __uint_as_float(ov[q4 * 8 + 7]) * inv);
+            dst[q4] = w;
+          }
+        }
+      }
+      if (p.lse && row < p.S)
+        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + row] = (m_run + log2f(l)) * kLn2;
+      tc_fence_before();
+      mbar_arrive(&bars->o_empty[t]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o, float* lse,
+                           float q_scale, float k_scale, float v_scale, int B, int Hq, int Hkv,
+                           int S, int causal, float scale, cudaStream_t st) {
+  using C = Cfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_3d(&tq, q, 2, D, S, static_cast<uint64_t>(B) * Hq, 64, BM, 128) ||
+      !make_tmap_3d(&tk, k, 2, D, S, static_cast<uint64_t>(B) * Hkv, 64, BN, 128) ||
+      !make_tmap_3d(&tv, v, 2, D, S, static_cast<uint64_t>(B) * Hkv, 64, BN, 128))
+    return ATTN_ERR_CUDA;
+  Params p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.status = device_status_ptr();
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.S = S;
+  p.causal = causal;
+  p.nM = (S + kRowsPerItem - 1) / kRowsPerItem;
+  p.nKV = (S + BN - 1) / BN;
+  p.n_items = p.nM * B * Hq;
+  p.c_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
+  p.v_scale = v_scale;
+  auto kern = prefill_kernel<D>;
+  if (!set_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes)) return ATTN_ERR_CUDA;
+  const int grid = std::min(p.n_items, sm_count());
+  kern<<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, p);
+  return launch_status();
+}
+
+}  // namespace
+
+attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                             attn_dtype_t dt, float q_scale, float k_scale, float v_scale, int B,
+                             int Hq, int Hkv, int S, int D, int causal, float scale,
+                             const float2* table, int pos0, cudaStream_t st) {
+  (void)pos0;
+  if (table != nullptr || dt != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (D == 128)
+    return launch_typed<128>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S, causal,
+                             scale, st);
+  return launch_typed<64>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S, causal,
+                          scale, st);
+}
+
+}  // namespace attn

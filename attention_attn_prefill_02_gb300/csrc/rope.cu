@@ -1,0 +1,156 @@
+// rope.cu — rope_apply: the unfused rotary position embedding pass over a [B,H,S,D] tensor.
+//
+// Row r = ((b*H + h)*S + s) is rotated at position pos0 + s: each pair (x_i, x_{i+D/2}) becomes
+// (x_i c - x_{i+D/2} s, x_{i+D/2} c + x_i s) with (c, s) = table[pos][i].  The pass is HBM
+// bound (every element read and written once); each thread moves one 16-byte chunk of the
+// first half of a row and the matching chunk of the second half, fully coalesced.
+#include "common.cuh"
+
+namespace attn {
+namespace {
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;  // elements per 16-byte chunk
+  __device__ static void load(const void* p, float* f) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 t = __bfloat1622float2(h[j]);
+      f[2 * j] = t.x;
+      f[2 * j + 1] = t.y;
+    }
+  }
+  __device__ static void store(void* p, const float* f) {
+    uint4 u;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = pack_bf16(f[2 * j], f[2 * j + 1]);
+    *reinterpret_cast<uint4*>(p) = u;
+  }
+  __device__ static float load1(const void* p, int i) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+  }
+  __device__ static void store1(void* p, int i, float f) {
+    reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(f);
+  }
+};
+template <>
+struct Vec<__nv_fp8_e5m2> {
+  static constexpr int N = 16;
+  __device__ static void load(const void* p, float* f) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const __nv_fp8x2_e5m2* h = reinterpret_cast<const __nv_fp8x2_e5m2*>(&u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float2 t = static_cast<float2>(h[j]);
+      f[2 * j] = t.x;
+      f[2 * j + 1] = t.y;
+    }
+  }
+  __device__ static void store(void* p, const float* f) {
+    uint4 u;
+    __nv_fp8x2_storage_t* w = reinterpret_cast<__nv_fp8x2_storage_t*>(&u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      w[j] = __nv_cvt_float2_to_fp8x2(make_float2(f[2 * j], f[2 * j + 1]), __NV_SATFINITE,
+                                      __NV_E5M2);
+    *reinterpret_cast<uint4*>(p) = u;
+  }
+  __device__ static float load1(const void* p, int i) {
+    return static_cast<float>(reinterpret_cast<const __nv_fp8_e5m2*>(p)[i]);
+  }
+  __device__ static void store1(void* p, int i, float f) {
+    reinterpret_cast<__nv_fp8_e5m2*>(p)[i] = __nv_fp8_e5m2(f);
+  }
+};
+
+// One thread per (row, 16-byte chunk of the first half).
+template <typename T>
+__global__ void __launch_bounds__(256) rope_vec_kernel(const T* __restrict__ x, T* y,
+                                                       long long rows, int S, int D, int pos0,
+                                                       const float2* __restrict__ table) {
+  constexpr int N = Vec<T>::N;
+  const int half = D / 2;
+  const int chunks = half / N;
+  const long long total = rows * chunks;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+       t += (long long)gridDim.x * blockDim.x) {
+    const long long row = t / chunks;
+    const int i0 = static_cast<int>(t - row * chunks) * N;
+    const int pos = pos0 + static_cast<int>(row % S);
+    const T* xr = x + row * D;
+    T* yr = y + row * D;
+    float a[N], b[N];
+    Vec<T>::load(xr + i0, a);
+    Vec<T>::load(xr + half + i0, b);
+    const float2* cs = table + static_cast<long long>(pos) * half + i0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      const float2 r = __ldg(cs + j);
+      const float a1 = a[j] * r.x - b[j] * r.y;
+      const float b1 = b[j] * r.x + a[j] * r.y;
+      a[j] = a1;
+      b[j] = b1;
+    }
+    Vec<T>::store(yr + i0, a);
+    Vec<T>::store(yr + half + i0, b);
+  }
+}
+
+// Any even D: one thread per pair.
+template <typename T>
+__global__ void __launch_bounds__(256) rope_pair_kernel(const T* __restrict__ x, T* y,
+                                                        long long rows, int S, int D, int pos0,
+                                                        const float2* __restrict__ table) {
+  const int half = D / 2;
+  const long long total = rows * half;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+       t += (long long)gridDim.x * blockDim.x) {
+    const long long row = t / half;
+    const int i = static_cast<int>(t - row * half);
+    const int pos = pos0 + static_cast<int>(row % S);
+    const float2 r = table[static_cast<long long>(pos) * half + i];
+    const float a = Vec<T>::load1(x + row * D, i);
+    const float b = Vec<T>::load1(x + row * D, i + half);
+    Vec<T>::store1(y + row * D, i, a * r.x - b * r.y);
+    Vec<T>::store1(y + row * D, i + half, b * r.x + a * r.y);
+  }
+}
+
+template <typename T>
+attn_status_t launch_typed(const void* x, void* y, int B, int H, int S, int D, int pos0,
+                           const float2* table, cudaStream_t st) {
+  const long long rows = static_cast<long long>(B) * H * S;
+  const int sms = sm_count();
+  const int threads = 256;
+  if ((D / 2) % Vec<T>::N == 0) {
+    const long long work = rows * ((D / 2) / Vec<T>::N);
+    long long blocks = (work + threads - 1) / threads;
+    const long long cap = static_cast<long long>(sms) * 16;
+    if (blocks > cap) blocks = cap;
+    rope_vec_kernel<T><<<static_cast<int>(blocks), threads, 0, st>>>(
+        static_cast<const T*>(x), static_cast<T*>(y), rows, S, D, pos0, table);
+  } else {
+    const long long work = rows * (D / 2);
+    long long blocks = (work + threads - 1) / threads;
+    const long long cap = static_cast<long long>(sms) * 16;
+    if (blocks > cap) blocks = cap;
+    rope_pair_kernel<T><<<static_cast<int>(blocks), threads, 0, st>>>(
+        static_cast<const T*>(x), static_cast<T*>(y), rows, S, D, pos0, table);
+  }
+  return launch_status();
+}
+
+}  // namespace
+
+attn_status_t launch_rope(const void* x, void* y, attn_dtype_t dt, int B, int H, int S, int D,
+                          int pos0, const float2* table, cudaStream_t st) {
+  if (dt == ATTN_BF16) return launch_typed<__nv_bfloat16>(x, y, B, H, S, D, pos0, table, st);
+  return launch_typed<__nv_fp8_e5m2>(x, y, B, H, S, D, pos0, table, st);
+}
+
+}  // namespace attn

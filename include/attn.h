@@ -1,0 +1,178 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) attention library.
+ *
+ * Four operations, all from the pages' problem statement of LLM-serving attention:
+ *   rope_apply          rotary position embedding on a [B,H,S,D] tensor
+ *   attn_prefill        causal / non-causal grouped-query attention, RoPE optionally fused
+ *   attn_decode         one query token per sequence against a static KV cache (split-KV)
+ *   attn_decode_latent  absorbed latent (MLA-style) decode: 448 latent + 64 RoPE dims
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise.  The caller owns every
+ *     buffer; the library never frees caller memory.
+ *   - Tensors are dense, row-major, innermost dimension last, base addresses 16-byte aligned.
+ *   - Storage types: ATTN_BF16 = bfloat16, ATTN_FP8_E5M2 = OCP float8 e5m2.  Outputs O are
+ *     always bfloat16; optional LSE outputs are float32 natural-log log-sum-exp of the scaled
+ *     scores.
+ *   - Grouped-query mapping: query head hq reads KV head hq / (Hq / Hkv).
+ *   - RoPE is the rotate-half pairing (x_i, x_{i+D/2}) rotated by pos * theta^(-2i/D).
+ *   - softmax_scale <= 0 selects 1/sqrt(head dim used for scores).
+ *   - Calls are asynchronous on `stream` and return after enqueueing.  Host-side validation
+ *     happens before anything is enqueued; on any error nothing is launched and outputs are
+ *     untouched.  Kernels never trap: a device-side problem (a cache_len out of range, a wait
+ *     that timed out) sets a device status word read by attn_get_device_status().
+ *   - The cos/sin table used by RoPE is built on the host in float64, stored as float32 and
+ *     cached per device and (D, theta).  The first call that needs a table (or more positions
+ *     than the cached one holds) allocates it with cudaMalloc and copies it synchronously; call
+ *     attn_rope_table_reserve() first to keep that out of timed regions and graph captures.
+ *     Every other path allocates nothing.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* A cudaStream_t.  NULL selects the legacy default stream. */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, Hq % Hkv != 0 ... */
+  ATTN_ERR_UNSUPPORTED = 2,   /* valid but not built: head dim, dtype or group size not covered */
+  ATTN_ERR_WORKSPACE = 3,     /* workspace pointer null or smaller than the *_workspace_size() */
+  ATTN_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  ATTN_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up (from attn_get_device_status) */
+  ATTN_ERR_NO_DEVICE = 6,     /* no CUDA device, or not an sm_100-family device */
+  ATTN_ERR_DEVICE_ARG = 7     /* a device-resident argument (cache_len) was out of range */
+} attn_status_t;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP8_E5M2 = 1 } attn_dtype_t;
+
+/* Static English description of a status code.  Never NULL. */
+ATTN_API const char* attn_status_string(attn_status_t status);
+
+/* Library ABI version (major * 100 + minor). */
+ATTN_API int attn_version(void);
+
+/*
+ * rope_apply — rotary position embedding, the unfused form.
+ * Defines: the RoPE the pages fuse into attention or run as a separate pass (Lesson: shape
+ * adaptive attention negative 20260722, rows "해본 것" and "실제 결과": fused versus unfused
+ * RoPE + attention).
+ *   x      [B,H,S,D] input, dtype `dtype`.
+ *   y      [B,H,S,D] output, same dtype; y == x (in place) is allowed, partial overlap is not.
+ *   pos0   position of row s = 0; row s is rotated at position pos0 + s (pos0 >= 0).
+ *   theta  RoPE base (> 0), e.g. 10000.
+ *   D      even, 2 <= D <= 256; B, H, S >= 1.  fp8 values are rotated in float32 and rounded
+ *          back to e5m2.
+ * Errors: INVALID_ARG for null/misaligned pointers or bad sizes; CUDA on launch failure.
+ */
+ATTN_API attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, int B, int H, int S, int D,
+                         int pos0, float theta, attn_stream_t stream);
+
+/*
+ * attn_prefill — grouped-query attention over a whole prompt, one GPU.
+ * Defines: softmax(scale * Q K^T + causal mask) V for Hq query heads sharing Hkv KV heads,
+ * the causal GQA prefill of Lesson: shape adaptive attention negative 20260722 ("당시 조건")
+ * and the Z/H/D attention workloads of the persistent-attention refactor page
+ * ("性能ベンチマーク").
+ *   q        [B,Hq,S,D]   k, v  [B,Hkv,S,D]   (dtype `dtype`)
+ *   o        [B,Hq,S,D] bfloat16 output.
+ *   lse      NULL or [B,Hq,S] float32: natural-log log-sum-exp of each row of scaled scores.
+ *   q_scale, k_scale, v_scale: dequantisation factors (stored value * scale = real value);
+ *            pass 1 for bf16 and for the per-tensor-scale-1 fp8 workloads.
+ *   causal   0 or 1; causal hides key j from query i when j > i (S_q == S_kv).
+ *   rope     0 = Q and K used as given; 1 = Q and K rotated inside the kernel at positions
+ *            pos0 + s as they are loaded (fused RoPE).
+ *   D in {64, 128}; Hq % Hkv == 0; S >= 1.  fp8 e5m2 is supported for rope = 0.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+ATTN_API attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                           attn_dtype_t dtype, float q_scale, float k_scale, float v_scale,
+                           int B, int Hq, int Hkv, int S, int D, int causal, float softmax_scale,
+                           int rope, float rope_theta, int pos0, attn_stream_t stream);
+
+/*
+ * attn_decode_workspace_size — bytes of device workspace attn_decode needs for these sizes
+ * (split-KV partial outputs and their log-sum-exp).  May be 0.  Needs no device memory; uses
+ * the current device's SM count (152 when no device is visible).
+ */
+ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int Lmax);
+
+/*
+ * attn_decode — single-token grouped-query decode against a static KV cache.
+ * Defines: the grouped split-score decode of Fixed-budget decode audit — 2026-09-11 ("Which
+ * implementation was tested": static append cache; "Optimized full-model results": split
+ * size 128), with split partials merged by log-sum-exp weights ("A: group-entry queries ...").
+ *   q          [B,Hq,D]      the new token's query (un-rotated; rotated here when rope = 1)
+ *   k_cache    [B,Hkv,Lmax,D], v_cache [B,Hkv,Lmax,D]  keys stored ALREADY rotated.
+ *   cache_len  DEVICE int32 [B]; sequence b attends keys 0 .. cache_len[b]-1 and its query
+ *              sits at position cache_len[b].  Needs 1 <= cache_len[b] <= Lmax; a row with an
+ *              out-of-range length gets O = 0, LSE = -inf and the device status DEVICE_ARG.
+ *   o          [B,Hq,D] bfloat16.  lse: NULL or [B,Hq] float32.
+ *   workspace  device buffer of at least attn_decode_workspace_size(B,Hq,Hkv,D,Lmax) bytes
+ *              (may be NULL when that size is 0).  Contents need no initialisation.
+ *   D in {64, 128}; Hq % Hkv == 0; Hq / Hkv <= 16; dtype ATTN_BF16.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ */
+ATTN_API attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* cache_len, int Lmax, void* o, float* lse,
+                          attn_dtype_t dtype, int B, int Hq, int Hkv, int D, float softmax_scale,
+                          int rope, float rope_theta, void* workspace, size_t workspace_bytes,
+                          attn_stream_t stream);
+
+/*
+ * attn_decode_latent_workspace_size — bytes of workspace attn_decode_latent needs.
+ */
+ATTN_API size_t attn_decode_latent_workspace_size(int B, int H, int Lmax);
+
+/*
+ * attn_decode_latent — absorbed latent (MLA-style) single-token decode.
+ * Defines: the MLA decode of Fixed-budget decode audit — 2026-09-11 ("Which implementation was
+ * tested": 448-dimensional latent + 64-dimensional RoPE), with W_UK already absorbed into q and
+ * W_UV applied by the caller to the latent output.
+ *   q          [B,H,512] bfloat16: 448 absorbed-latent dims then 64 RoPE dims (the RoPE dims
+ *              are rotated at position cache_len[b] when rope = 1).
+ *   c_cache    [B,Lmax,512] bfloat16: per token the 448-dim latent then the 64-dim rotated key.
+ *              Scores use all 512 dims; values are the first 448 dims.
+ *   cache_len  DEVICE int32 [B], as in attn_decode.
+ *   o          [B,H,448] bfloat16.  lse: NULL or [B,H] float32.
+ *   H <= 16 (all heads of a sequence share one MMA tile).  softmax_scale <= 0 means 1/sqrt(512).
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ */
+ATTN_API attn_status_t attn_decode_latent(const void* q, const void* c_cache, const int32_t* cache_len,
+                                 int Lmax, void* o, float* lse, int B, int H,
+                                 float softmax_scale, int rope, float rope_theta,
+                                 void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * attn_rope_table_reserve — build (if needed) the cos/sin table for head dim D and base theta
+ * covering positions 0 .. max_pos on the current device.  Allocates and copies synchronously.
+ * Call before timing or stream capture.  Errors: INVALID_ARG, CUDA, NO_DEVICE.
+ */
+ATTN_API attn_status_t attn_rope_table_reserve(int D, float theta, int max_pos);
+
+/*
+ * attn_get_device_status — synchronise `stream`, then return (in *status_out) the device status
+ * word the kernels set since the last call (ATTN_OK, ATTN_ERR_TIMEOUT or ATTN_ERR_DEVICE_ARG)
+ * and clear it.  The return value reports failures of this call itself.
+ */
+ATTN_API attn_status_t attn_get_device_status(attn_stream_t stream, int* status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,161 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads, exports every
+entry point include/attn.h declares, and rejects invalid arguments before touching a device.
+
+Only invalid calls are made here (or valid ones when no device is visible), so nothing is ever
+launched with the fake pointers these tests pass.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from attention_attn_prefill_02_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA, TIMEOUT, NO_DEVICE, DEVICE_ARG = range(8)
+FAKE = ctypes.c_void_p(0x7F0000000000)  # 16-byte aligned, never dereferenced
+FAKE2 = ctypes.c_void_p(0x7F0000100000)
+MIS = ctypes.c_void_p(0x7F0000000008)   # misaligned
+
+
+@pytest.fixture(scope="module")
+def L():
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_four_operations():
+    names = declared_functions()
+    for fn in ("rope_apply", "attn_prefill", "attn_decode", "attn_decode_latent"):
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    # and nothing of the internal namespace leaks as a dynamic symbol
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", binding._build.LIB], capture_output=True,
+                         text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert set(names) <= exported
+    assert not any("attn4" in e or "_ZN4attn" in e for e in exported)
+
+
+def test_status_strings(L):
+    for s in range(8):
+        assert len(binding.attn_status_string(s)) > 0
+    assert binding.attn_status_string(99) == "unknown status"
+    assert binding.attn_version() >= 100
+
+
+def _stream():
+    return ctypes.c_void_p(0)
+
+
+def test_rope_apply_rejects_bad_arguments(L):
+    bad = [
+        (None, FAKE, 0, 1, 1, 1, 8, 0, 1e4),     # null input
+        (FAKE, MIS, 0, 1, 1, 1, 8, 0, 1e4),      # misaligned output
+        (FAKE, FAKE2, 5, 1, 1, 1, 8, 0, 1e4),    # bad dtype
+        (FAKE, FAKE2, 0, 0, 1, 1, 8, 0, 1e4),    # B = 0
+        (FAKE, FAKE2, 0, 1, 1, 1, 7, 0, 1e4),    # odd D
+        (FAKE, FAKE2, 0, 1, 1, 1, 8, -1, 1e4),   # negative pos0
+        (FAKE, FAKE2, 0, 1, 1, 1, 8, 0, 0.0),    # theta 0
+        (FAKE, FAKE2, 0, 1, 1, 1, 8, 0, float("nan")),
+        (FAKE, ctypes.c_void_p(0x7F0000000010), 0, 1, 1, 4, 8, 0, 1e4),  # partial overlap
+    ]
+    for a in bad:
+        assert L.rope_apply(*a, _stream()) == INVALID, a
+
+
+def _prefill(L, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE2, lse=None, dt=0, qs=1.0, ks=1.0, vs=1.0, B=1,
+                Hq=4, Hkv=1, S=128, D=64, causal=1, scale=0.0, rope=1, theta=1e4, pos0=0)
+    args.update(kw)
+    return L.attn_prefill(*args.values(), _stream())
+
+
+def test_prefill_validation(L):
+    assert _prefill(L, q=None) == INVALID
+    assert _prefill(L, o=MIS) == INVALID
+    assert _prefill(L, Hq=6, Hkv=4) == INVALID          # Hq % Hkv
+    assert _prefill(L, S=0) == INVALID
+    assert _prefill(L, causal=2) == INVALID
+    assert _prefill(L, rope=1, theta=-1.0) == INVALID
+    assert _prefill(L, qs=0.0) == INVALID
+    assert _prefill(L, lse=ctypes.c_void_p(0x7F0000000002)) == INVALID
+    assert _prefill(L, D=96) == UNSUPPORTED
+    assert _prefill(L, D=256) == UNSUPPORTED
+
+
+def _decode(L, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, lens=FAKE2, Lmax=2048, o=FAKE2, lse=None, dt=0, B=1,
+                Hq=32, Hkv=8, D=128, scale=0.0, rope=1, theta=1e4, ws=FAKE2, wsb=1 << 30)
+    args.update(kw)
+    return L.attn_decode(*args.values(), _stream())
+
+
+def test_decode_validation(L):
+    assert _decode(L, lens=None) == INVALID
+    assert _decode(L, Lmax=0) == INVALID
+    assert _decode(L, Hq=30) == INVALID
+    assert _decode(L, D=80) == UNSUPPORTED
+    assert _decode(L, Hq=64, Hkv=2) == UNSUPPORTED      # group of 32 > 16
+    assert _decode(L, dt=1) == UNSUPPORTED              # fp8 decode not built
+    assert _decode(L, rope=3) == INVALID
+
+
+def _latent(L, **kw):
+    args = dict(q=FAKE, c=FAKE, lens=FAKE2, Lmax=2048, o=FAKE2, lse=None, B=128, H=16,
+                scale=0.0, rope=1, theta=1e4, ws=FAKE2, wsb=1 << 30)
+    args.update(kw)
+    return L.attn_decode_latent(*args.values(), _stream())
+
+
+def test_latent_validation(L):
+    assert _latent(L, c=None) == INVALID
+    assert _latent(L, H=0) == INVALID
+    assert _latent(L, H=17) == UNSUPPORTED
+    assert _latent(L, q=MIS) == INVALID
+
+
+def test_workspace_sizes_are_consistent(L):
+    # sizes that split the key range need workspace; the batch-128 decode config needs none
+    assert binding.attn_decode_workspace_size(1, 32, 8, 128, 2048) > 0
+    assert binding.attn_decode_workspace_size(128, 32, 8, 128, 2048) == 0
+    assert binding.attn_decode_workspace_size(1, 30, 8, 128, 2048) == 0  # invalid -> 0
+    assert binding.attn_decode_latent_workspace_size(128, 16, 2048) == 0
+    assert binding.attn_decode_latent_workspace_size(1, 16, 2048) > 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_calls_report_no_device_without_gpu(L):
+    assert _prefill(L) == NO_DEVICE
+    assert _decode(L) == NO_DEVICE
+    assert _decode(L, ws=None, wsb=0) in (NO_DEVICE, WORKSPACE)
+    assert _latent(L) == NO_DEVICE
+    assert L.rope_apply(FAKE, FAKE, 0, 1, 1, 4, 8, 0, 1e4, _stream()) == NO_DEVICE
+    st = ctypes.c_int(-1)
+    assert L.attn_get_device_status(_stream(), ctypes.byref(st)) == NO_DEVICE
+    assert L.attn_rope_table_reserve(64, 1e4, 100) == NO_DEVICE
+
+
+def test_product_path_does_not_import_the_oracle():
+    """The CUDA path's Python package never refers to the oracle package."""
+    pkg = os.path.join(ROOT, "attention_attn_prefill_02_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cpp", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f

@@ -1,0 +1,168 @@
+"""GPU parity: every entry point, called through the C ABI, against the float64 oracle on the
+same seeded inputs.
+
+Tolerances (north-star): bf16 outputs max-abs <= 2e-2 and mean-abs <= 2e-3; fp8 e5m2 max-abs
+<= 8e-2 (oracle on the dequantised inputs).  LSE is compared to 5e-3 absolute (its error is the
+relative error of the row sum, which bf16 rounding of P keeps near 1e-3).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_attn_prefill_02_gb300 import binding, synthetic
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX, BF16_MEAN, FP8_MAX, LSE_TOL = 2e-2, 2e-3, 8e-2, 5e-3
+
+
+def f64(t):
+    return oracle.as_f64(t)
+
+
+def check(gpu, ref, max_abs=BF16_MAX, mean_abs=BF16_MEAN, what=""):
+    g = f64(gpu)
+    d = np.abs(g - ref)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    assert d.max() <= max_abs, f"{what}: max-abs {d.max():.3e} > {max_abs}"
+    if mean_abs is not None:
+        assert d.mean() <= mean_abs, f"{what}: mean-abs {d.mean():.3e} > {mean_abs}"
+
+
+def status_ok():
+    assert binding.attn_get_device_status() == 0
+
+
+# --------------------------------------------------------------------------------------------
+# rope_apply
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape,pos0", [((2, 3, 37, 64), 5), ((1, 2, 130, 128), 0),
+                                        ((1, 1, 3, 6), 11), ((2, 4, 256, 128), 16000)])
+def test_rope_apply_bf16(shape, pos0):
+    x = synthetic.rope_input(*shape, dtype="bf16", seed=1)
+    y = binding.rope_apply(x.cuda(), pos0=pos0, theta=10000.0)
+    torch.cuda.synchronize()
+    ref = oracle.rope_rotate_half(f64(x), pos0 + np.arange(shape[2]), 10000.0)
+    check(y.cpu(), ref, what="rope bf16")
+    # the kernel rounds once to bf16: it must agree with the rounded oracle almost everywhere
+    rounded = torch.from_numpy(ref).to(torch.bfloat16)
+    assert (y.cpu() == rounded).float().mean() > 0.99
+
+
+def test_rope_apply_in_place_and_fp8():
+    x = synthetic.rope_input(2, 2, 50, 64, dtype="fp8", seed=2)
+    xd = x.cuda()
+    binding.rope_apply(xd, xd, pos0=3, theta=500.0)
+    torch.cuda.synchronize()
+    ref = oracle.rope_rotate_half(f64(x), 3 + np.arange(50), 500.0)
+    rounded = torch.from_numpy(ref).to(torch.float8_e5m2)
+    agree = (xd.cpu().float() == rounded.float()).float().mean().item()
+    assert agree > 0.99, agree
+    # disagreements are at most one e5m2 step (rounding of a float32 vs float64 value)
+    g, r = f64(xd.cpu()), f64(rounded)
+    step = np.maximum(np.abs(r), 2.0 ** -14) * 0.25
+    assert np.all(np.abs(g - r) <= step * 1.0001)
+
+
+# --------------------------------------------------------------------------------------------
+# prefill
+# --------------------------------------------------------------------------------------------
+
+PREFILL_CASES = [
+    # B, Hq, Hkv, S, D, causal
+    (1, 4, 1, 128, 64, True),      # the tiny config's shape
+    (1, 4, 1, 128, 64, False),
+    (2, 4, 2, 640, 128, True),     # several tiles, two items per head, GQA
+    (1, 2, 2, 300, 128, True),     # ragged tail
+    (1, 2, 1, 77, 64, False),      # shorter than one tile
+    (1, 1, 1, 1, 128, True),       # S = 1
+    (1, 8, 8, 513, 64, True),      # ragged, MHA
+    (1, 2, 1, 1000, 128, False),   # ragged non-causal, many KV tiles
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", PREFILL_CASES)
+def test_prefill_bf16(B, Hq, Hkv, S, D, causal):
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=S)
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, want_lse=True)
+    status_ok()
+    ro, rl = oracle.prefill(f64(q), f64(k), f64(v), causal=causal)
+    check(o.cpu(), ro, what="O")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE")
+
+
+def test_prefill_unfused_rope_tiny_config():
+    """Tiny config: B=1, Hq=4, Hkv=1, S=128, D=64, RoPE 1e4 via rope_apply then attention."""
+    q, k, v = synthetic.prefill_inputs(1, 4, 1, 128, 64, "bf16", seed=0)
+    qd, kd = binding.rope_apply(q.cuda()), binding.rope_apply(k.cuda())
+    o = binding.attn_prefill(qd, kd, v.cuda(), causal=True)
+    status_ok()
+    ro, _ = oracle.prefill(f64(q), f64(k), f64(v), causal=True, rope=True, theta=10000.0)
+    check(o.cpu(), ro, what="O")
+
+
+def test_prefill_large_logits_rescale_path():
+    """Rows whose maximum grows late force the lazy O rescale; scale 1 makes logits large."""
+    B, Hq, Hkv, S, D = 1, 2, 1, 700, 64
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=9)
+    k = (f64(k) * np.linspace(0.2, 3.0, S)[None, None, :, None])
+    k = torch.from_numpy(k).to(torch.bfloat16)
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, softmax_scale=1.0,
+                                  want_lse=True)
+    status_ok()
+    ro, rl = oracle.prefill(f64(q), f64(k), f64(v), causal=True, scale=1.0)
+    check(o.cpu(), ro, 3e-2, BF16_MEAN, what="O")
+    np.testing.assert_allclose(f64(lse.cpu()), rl, rtol=2e-3, atol=2e-2)
+
+
+# --------------------------------------------------------------------------------------------
+# decode
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,Lmax,lens", [
+    (1, 32, 8, 128, 2048, [2048]),            # the decode config at batch 1 (split KV)
+    (3, 32, 8, 128, 2048, [2048, 1, 777]),    # ragged lengths, one single-key sequence
+    (8, 32, 8, 128, 2048, 2048),              # batch 8 (split KV)
+    (2, 8, 1, 64, 300, [300, 129]),           # D = 64, group 8, Lmax not a tile multiple
+    (2, 16, 1, 128, 100, [64, 100]),          # group of 16 fills the MMA tile
+])
+def test_decode_bf16(B, Hq, Hkv, D, Lmax, lens):
+    q, kc, vc, cl = synthetic.decode_inputs(B, Hq, Hkv, Lmax, D, lens, seed=B)
+    o, lse = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda(), want_lse=True)
+    status_ok()
+    ro, rl = oracle.decode(f64(q), f64(kc), f64(vc), cl.numpy(), rope=True, theta=10000.0)
+    check(o.cpu(), ro, what="O")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE")
+
+
+def test_decode_bad_cache_len_sets_status():
+    q, kc, vc, cl = synthetic.decode_inputs(2, 8, 2, 64, 64, [64, 64], seed=1)
+    cl[1] = 65  # > Lmax
+    o = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda())
+    assert binding.attn_get_device_status() == 7  # ATTN_ERR_DEVICE_ARG
+    assert binding.attn_get_device_status() == 0  # cleared
+    ro, _ = oracle.decode(f64(q[:1]), f64(kc[:1]), f64(vc[:1]), cl[:1].numpy())
+    check(o[:1].cpu(), ro, what="valid row")
+    assert torch.all(o[1].cpu() == 0)
+
+
+# --------------------------------------------------------------------------------------------
+# latent decode
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,H,Lmax,lens", [
+    (4, 16, 2048, [2048, 1, 1000, 64]),
+    (1, 16, 2048, [2048]),
+    (2, 5, 200, [200, 37]),
+])
+def test_latent_decode(B, H, Lmax, lens):
+    q, c, cl = synthetic.latent_inputs(B, H, Lmax, lens, seed=B)
+    o, lse = binding.attn_decode_latent(q.cuda(), c.cuda(), cl.cuda(), want_lse=True)
+    status_ok()
+    ro, rl = oracle.latent_decode(f64(q), f64(c), cl.numpy(), rope=True, theta=10000.0)
+    check(o.cpu(), ro, what="O")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE")
