@@ -33,7 +33,9 @@ constexpr int BN = 128;  // keys per KV tile
 constexpr int kRowsPerItem = 2 * BM;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kRopeWarp0 = 10;  // fused RoPE: warps 10-11 rotate each K tile in shared memory
+constexpr int kRopeThreads = 64;
+__host__ __device__ constexpr int threads_for(bool rope) { return rope ? 384 : 320; }
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -42,7 +44,8 @@ struct Cfg {
   static constexpr int kBoxes = D / 64;                 // 128-byte swizzle boxes per row
   static constexpr int kQTileBytes = BM * D * 2;
   static constexpr int kKVTileBytes = BN * D * 2;
-  static constexpr int kStages = D == 128 ? 4 : 6;      // K/V ring depth
+  static constexpr int kStages = D == 128 ? 4 : 6;      // K/V ring depth (even: K in even slots)
+  static_assert(kStages % 2 == 0, "K tiles must always land in even ring slots");
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kQTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kKVTileBytes;
@@ -59,12 +62,15 @@ struct Params {
   int n_items, nM, nKV;
   float c_log2;   // softmax_scale * q_scale * k_scale * log2(e)
   float v_scale;
+  const float2* table;  // RoPE cos/sin [position][D/2] (fused RoPE only)
+  int pos0;
 };
 
 struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t kv_full[8], kv_empty[8];
+  uint64_t q_ready[2], k_ready[8];  // fused RoPE: tile rotated in shared memory
   uint32_t tmem_slot;
 };
 
@@ -91,8 +97,36 @@ __device__ __forceinline__ int item_for(int round, int cta, int ncta) {
   return round * ncta + ((round & 1) ? (ncta - 1 - cta) : cta);
 }
 
+// Rotate one row of a 128-row tile held in shared memory as D/64 boxes of 128-byte swizzled
+// rows: pairs (i, i + D/2) by the float32 cos/sin of this row's position (8 pairs per step).
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void rope_rotate_row(uint8_t* tile, int row,
+                                                const float2* __restrict__ cs_row) {
+#pragma unroll
+  for (int c = 0; c < D / 16; ++c) {
+    const int c2 = c + D / 16;
+    uint4* p1 = reinterpret_cast<uint4*>(tile + (c >> 3) * (128 * 128) + sw128_offset(row, c & 7));
+    uint4* p2 =
+        reinterpret_cast<uint4*>(tile + (c2 >> 3) * (128 * 128) + sw128_offset(row, c2 & 7));
+    uint4 a = *p1, b = *p2;
+    const float4* t4 = reinterpret_cast<const float4*>(cs_row + c * 8);
+    uint32_t* aw = reinterpret_cast<uint32_t*>(&a);
+    uint32_t* bw = reinterpret_cast<uint32_t*>(&b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 t = __ldg(t4 + q);  // (cos, sin) of pairs 8c + 2q and 8c + 2q + 1
+      const float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&aw[q]));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&bw[q]));
+      aw[q] = pack_bf16(x.x * t.x - y.x * t.y, x.y * t.z - y.y * t.w);
+      bw[q] = pack_bf16(y.x * t.x + x.x * t.y, y.y * t.z + x.y * t.w);
+    }
+    *p1 = a;
+    *p2 = b;
+  }
+}
+
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(threads_for(ROPE), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
   using C = Cfg<D>;
@@ -114,7 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_ready[s], kRopeThreads);
     }
+    mbar_init(&bars->q_ready[0], 128);
+    mbar_init(&bars->q_ready[1], 128);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&bars->tmem_slot, C::kTmemCols);
@@ -219,13 +256,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (n[t] == 0 || !ok) continue;
-          ok = mbar_wait(&bars->q_full[t], ph_qf[t], p.status);
+          ok = mbar_wait(ROPE ? &bars->q_ready[t] : &bars->q_full[t], ph_qf[t], p.status);
           ph_qf[t] ^= 1;
         }
         if (!ok) break;
         // j = 0: S_t = Q_t K_0^T for both tiles
         const int kslot = stage;
-        if (!(ok = mbar_wait(&bars->kv_full[kslot], ph, p.status))) break;
+        if (!(ok = mbar_wait(ROPE ? &bars->k_ready[kslot] : &bars->kv_full[kslot], ph, p.status)))
+          break;
         if (++stage == C::kStages) { stage = 0; ph ^= 1; }
         tc_fence_after();
 #pragma unroll
@@ -243,7 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           int kslot2 = -1;
           if (j < nkv) {
             kslot2 = stage;
-            if (!(ok = mbar_wait(&bars->kv_full[kslot2], ph, p.status))) break;
+            if (!(ok = mbar_wait(ROPE ? &bars->k_ready[kslot2] : &bars->kv_full[kslot2], ph,
+                                 p.status)))
+              break;
             if (++stage == C::kStages) { stage = 0; ph ^= 1; }
           }
 #pragma unroll
@@ -272,6 +312,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  } else if (ROPE && warp >= kRopeWarp0) {
+    // ------------------------------------------------------------------ K-tile RoPE warps
+    const int rt = threadIdx.x - kRopeWarp0 * 32;  // 0..63: rows rt and rt + 64 of each tile
+    int stage = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int it = item_for(r, blockIdx.x, gridDim.x);
+      if (it >= p.n_items) continue;
+      int m, b, hq;
+      item_coords(p, it, m, b, hq);
+      const int nkv = max(kv_tiles_for(p, m * kRowsPerItem), kv_tiles_for(p, m * kRowsPerItem + BM));
+      for (int j = 0; j < nkv && ok; ++j) {
+        if (!(ok = mbar_wait(&bars->kv_full[stage], ph, p.status))) break;
+        uint8_t* tile = smem + C::kKVOff + stage * C::kKVTileBytes;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int key = j * BN + rt + h * 64;
+          if (key < p.S)
+            rope_rotate_row<D>(tile, rt + h * 64,
+                               p.table + static_cast<size_t>(p.pos0 + key) * (D / 2));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->k_ready[stage]);
+        stage += 2;  // skip the V tile that follows in the ring
+        if (stage >= C::kStages) {
+          stage -= C::kStages;
+          ph ^= 1;
+        }
+      }
+    }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;          // Q tile of this warpgroup
@@ -280,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + (t ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
-    uint32_t ph_s = 0, ph_o = 0;
+    uint32_t ph_s = 0, ph_o = 0, ph_q = 0;
     bool ok = true;
     for (int r = 0; r < rounds && ok; ++r) {
       const int it = item_for(r, blockIdx.x, gridDim.x);
@@ -291,6 +362,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = kv_tiles_for(p, r0);
       if (n == 0) continue;
       const int row = r0 + lrow;
+      if constexpr (ROPE) {
+        if (!(ok = mbar_wait(&bars->q_full[t], ph_q, p.status))) break;
+        ph_q ^= 1;
+        if (row < p.S)
+          rope_rotate_row<D>(smem + C::kQOff + t * C::kQTileBytes, lrow,
+                             p.table + static_cast<size_t>(p.pos0 + row) * (D / 2));
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->q_ready[t]);
+      }
       float m_run = -INFINITY, l = 0.f;
       for (int j = 0; j < n; ++j) {
         if (!(ok = mbar_wait(&bars->s_full[t], ph_s, p.status))) break;
@@ -339,7 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         l += sum;
         tmem_st32(tS, pk[0]);
         tmem_st32(tS + 32, pk[1]);
-        if (f != 1.f) {
+        // tcgen05.ld / st are warp-collective: rescale when any lane of the warp needs it
+        // (lanes that do not have f == 1).
+        if (__any_sync(0xffffffffu, f != 1.f)) {
           // O_t holds the tiles before j (their PV completed before S_t(j) was signalled)
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -394,10 +476,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool ROPE>
 attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o, float* lse,
                            float q_scale, float k_scale, float v_scale, int B, int Hq, int Hkv,
-                           int S, int causal, float scale, cudaStream_t st) {
+                           int S, int causal, float scale, const float2* table, int pos0,
+                           cudaStream_t st) {
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_3d(&tq, q, 2, D, S, static_cast<uint64_t>(B) * Hq, 64, BM, 128) ||
@@ -419,10 +502,12 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   p.n_items = p.nM * B * Hq;
   p.c_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
   p.v_scale = v_scale;
-  auto kern = prefill_kernel<D>;
+  p.table = table;
+  p.pos0 = pos0;
+  auto kern = prefill_kernel<D, ROPE>;
   if (!set_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes)) return ATTN_ERR_CUDA;
   const int grid = std::min(p.n_items, sm_count());
-  kern<<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, p);
+  kern<<<grid, threads_for(ROPE), C::kSmemBytes, st>>>(tq, tk, tv, p);
   return launch_status();
 }
 
@@ -432,13 +517,17 @@ attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* 
                              attn_dtype_t dt, float q_scale, float k_scale, float v_scale, int B,
                              int Hq, int Hkv, int S, int D, int causal, float scale,
                              const float2* table, int pos0, cudaStream_t st) {
-  (void)pos0;
-  if (table != nullptr || dt != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (D == 128)
-    return launch_typed<128>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S, causal,
-                             scale, st);
-  return launch_typed<64>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S, causal,
-                          scale, st);
+  if (dt != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+#define ATTN_PREFILL_CASE(DD, RR)                                                             \
+  if (D == DD && (table != nullptr) == RR)                                                    \
+    return launch_typed<DD, RR>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S,   \
+                                causal, scale, table, pos0, st);
+  ATTN_PREFILL_CASE(128, false)
+  ATTN_PREFILL_CASE(128, true)
+  ATTN_PREFILL_CASE(64, false)
+  ATTN_PREFILL_CASE(64, true)
+#undef ATTN_PREFILL_CASE
+  return ATTN_ERR_UNSUPPORTED;
 }
 
 }  // namespace attn

@@ -1,0 +1,535 @@
+"""Benchmark: prefill TFLOPS and decode HBM GB/s on one GB300, against the roofline.
+
+One step = one pass of the whole hot path over one batch of synthetic inputs (all resident in
+HBM, each larger than the 129 MB L2, so no flush is needed between steps):
+
+  1. causal GQA prefill, Z=4, Hq=32, Hkv=8, D=128, S=16384, bf16, RoPE (theta 1e4) fused
+  2. GQA decode, B=128, Hq=32, Hkv=8, D=128, static cache of 2048 tokens, q at position 2048
+  3. absorbed latent decode, B=128, 16 heads, 448 latent + 64 RoPE dims, cache 2048 tokens
+
+`value` is the prefill throughput in useful TFLOPS (the step's dominant kernel); the decode
+bandwidths ride along in the same line.  Under torchrun every rank runs the same per-GPU step on
+its own seeded batch (weak scaling, no data-path collective); `value` = all ranks' FLOPs over the
+slowest rank's time.
+
+`--impl reference` times the float64 CPU oracle instead (bounded per-step sample, rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill TFLOPS & decode HBM GB/s (ms/step) at 1 GB300; % of roofline"
+PREFILL = dict(B=4, Hq=32, Hkv=8, S=16384, D=128)
+DECODE = dict(B=128, Hq=32, Hkv=8, D=128, L=2048)
+LATENT = dict(B=128, H=16, L=2048)
+THETA = 10000.0
+
+
+# ----------------------------------------------------------------------------------------------
+# distributed helpers (weak scaling; also exercised by the gloo tests)
+# ----------------------------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(work_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: every rank did `work_per_rank`; the job took the slowest rank's time."""
+    return work_per_rank * world / max_seconds
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own independent batch."""
+    return 17 + rank
+
+
+# ----------------------------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------------
+# our CUDA path
+# ----------------------------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Timer:
+    """Accumulates CUDA-event durations of one kind of launch on the current stream."""
+
+    def __init__(self):
+        import torch
+        self.torch = torch
+        self.pairs = []
+
+    def __enter__(self):
+        s = self.torch.cuda.Event(enable_timing=True)
+        s.record()
+        self._s = s
+        return self
+
+    def __exit__(self, *exc):
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.pairs.append((self._s, e))
+
+    def ms(self):
+        return [s.elapsed_time(e) for s, e in self.pairs]
+
+
+def make_inputs(seed: int):
+    import torch
+    from attention_attn_prefill_02_gb300 import synthetic
+
+    dev = "cuda"
+    P, Dd, Lt = PREFILL, DECODE, LATENT
+    q, k, v = synthetic.prefill_inputs(P["B"], P["Hq"], P["Hkv"], P["S"], P["D"], "bf16", seed)
+    dq, dk, dv, dl = synthetic.decode_inputs(Dd["B"], Dd["Hq"], Dd["Hkv"], Dd["L"], Dd["D"],
+                                             Dd["L"], seed=seed)
+    lq, lc, ll = synthetic.latent_inputs(Lt["B"], Lt["H"], Lt["L"], Lt["L"], seed=seed)
+    host = dict(q=q, k=k, v=v)
+    d = {n: t.to(dev) for n, t in dict(q=q, k=k, v=v, dq=dq, dk=dk, dv=dv, dl=dl, lq=lq, lc=lc,
+                                      ll=ll).items()}
+    d["o"] = torch.empty((P["B"], P["Hq"], P["S"], P["D"]), dtype=torch.bfloat16, device=dev)
+    d["do"] = torch.empty((Dd["B"], Dd["Hq"], Dd["D"]), dtype=torch.bfloat16, device=dev)
+    d["lo"] = torch.empty((Lt["B"], Lt["H"], 448), dtype=torch.bfloat16, device=dev)
+    return d, host
+
+
+def run_step(b, d, timers=None):
+    """One pass of the hot path.  `timers` (dict of Timer) brackets each call with events."""
+    import contextlib
+
+    t = timers or {}
+    with t.get("prefill", contextlib.nullcontext()):
+        b.attn_prefill(d["q"], d["k"], d["v"], causal=True, rope=True, rope_theta=THETA,
+                       o=d["o"])
+    with t.get("decode", contextlib.nullcontext()):
+        b.attn_decode(d["dq"], d["dk"], d["dv"], d["dl"], o=d["do"], rope=True, rope_theta=THETA,
+                      workspace=d.get("dws"))
+    with t.get("latent", contextlib.nullcontext()):
+        b.attn_decode_latent(d["lq"], d["lc"], d["ll"], o=d["lo"], rope=True, rope_theta=THETA,
+                             workspace=d.get("lws"))
+
+
+def time_call(fn, iters=20, warmup=3):
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(iters):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def time_graph(fn, iters=20):
+    import torch
+
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        fn()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=st):
+            fn()
+    torch.cuda.current_stream().wait_stream(st)
+    torch.cuda.synchronize()
+    return time_call(g.replay, iters=iters, warmup=2)
+
+
+def variants(b, d):
+    """Pages' lessons: eager vs graph, fused vs unfused RoPE, decode batch sweep, L2 residency."""
+    import torch
+    from attention_attn_prefill_02_gb300 import synthetic, workload
+
+    out = {}
+    P = PREFILL
+    fl = workload.prefill_flops(P["B"], P["Hq"], P["S"], P["D"], True)
+    # fused vs unfused RoPE (unfused = rope_apply on Q and K, then attention without RoPE)
+    qr, kr = torch.empty_like(d["q"]), torch.empty_like(d["k"])
+
+    def unfused():
+        b.rope_apply(d["q"], qr, theta=THETA)
+        b.rope_apply(d["k"], kr, theta=THETA)
+        b.attn_prefill(qr, kr, d["v"], causal=True, rope=False, o=d["o"])
+
+    def fused():
+        b.attn_prefill(d["q"], d["k"], d["v"], causal=True, rope=True, rope_theta=THETA, o=d["o"])
+
+    def attn_only():
+        b.attn_prefill(qr, kr, d["v"], causal=True, rope=False, o=d["o"])
+
+    def rope_only():
+        b.rope_apply(d["q"], qr, theta=THETA)
+        b.rope_apply(d["k"], kr, theta=THETA)
+
+    tf, tu = time_call(fused, 5, 1), time_call(unfused, 5, 1)
+    ta, tr = time_call(attn_only, 5, 1), time_call(rope_only, 5, 1)
+    rope_bytes = workload.rope_bytes(P["B"] * (P["Hq"] + P["Hkv"]) * P["S"], P["D"])
+    out["prefill_rope"] = {
+        "fused_ms": round(tf, 4), "unfused_ms": round(tu, 4), "attention_only_ms": round(ta, 4),
+        "rope_apply_ms": round(tr, 4), "rope_apply_gbs": round(rope_bytes / tr / 1e6, 1),
+        "fused_tflops": round(fl / tf / 1e9, 1), "unfused_tflops": round(fl / tu / 1e9, 1),
+        "fused_speedup": round(tu / tf, 3)}
+    # prefill shapes of the pages' configs (eager), one global tile configuration
+    shapes = {}
+    for name, (B, Hq, Hkv, S, D, causal) in {
+            "noncausal_d64_s4096": (4, 32, 32, 4096, 64, False),
+            "noncausal_d64_s16384": (4, 32, 32, 16384, 64, False),
+            "causal_d128_s1024": (4, 32, 8, 1024, 128, True),
+            "causal_d128_s4096": (4, 32, 8, 4096, 128, True)}.items():
+        q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=3)
+        q, k, v = q.cuda(), k.cuda(), v.cuda()
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+
+        def f(q=q, k=k, v=v, o=o, causal=causal):
+            b.attn_prefill(q, k, v, causal=causal, o=o)
+
+        t = time_call(f, 5, 1)
+        shapes[name] = {"ms": round(t, 4),
+                        "tflops": round(workload.prefill_flops(B, Hq, S, D, causal) / t / 1e9, 1)}
+        del q, k, v, o
+    out["prefill_shapes"] = shapes
+    # decode batch sweep: eager vs CUDA-graph replay, L2-resident vs streaming
+    sweep = {}
+    Dd = DECODE
+    for B in (1, 8, 32, 64, 128):
+        q, kc, vc, cl = synthetic.decode_inputs(B, Dd["Hq"], Dd["Hkv"], Dd["L"], Dd["D"], Dd["L"],
+                                                seed=5)
+        q, kc, vc, cl = q.cuda(), kc.cuda(), vc.cuda(), cl.cuda()
+        o = torch.empty((B, Dd["Hq"], Dd["D"]), dtype=torch.bfloat16, device="cuda")
+        ws_n = b.attn_decode_workspace_size(B, Dd["Hq"], Dd["Hkv"], Dd["D"], Dd["L"])
+        ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+
+        def f(q=q, kc=kc, vc=vc, cl=cl, o=o, ws=ws):
+            b.attn_decode(q, kc, vc, cl, o=o, rope=True, rope_theta=THETA, workspace=ws)
+
+        nbytes = workload.decode_bytes(B, Dd["Hq"], Dd["Hkv"], Dd["L"], Dd["D"])
+        te, tg = time_call(f, 50, 5), time_graph(f, 50)
+        sweep[str(B)] = {"eager_ms": round(te, 5), "graph_ms": round(tg, 5),
+                         "graph_gbs": round(nbytes / tg / 1e6, 1),
+                         "l2_resident": nbytes < 100e6}
+        del q, kc, vc, cl, o, ws
+    out["decode_sweep"] = sweep
+    return out
+
+
+def ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from attention_attn_prefill_02_gb300 import binding as b
+    from attention_attn_prefill_02_gb300 import workload
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    b.lib()
+    b.attn_rope_table_reserve(128, THETA, PREFILL["S"] + 1)
+    b.attn_rope_table_reserve(64, THETA, LATENT["L"] + 1)
+    d, host = make_inputs(rank_seed(rank))
+    dws = b.attn_decode_workspace_size(DECODE["B"], DECODE["Hq"], DECODE["Hkv"], DECODE["D"],
+                                       DECODE["L"])
+    lws = b.attn_decode_latent_workspace_size(LATENT["B"], LATENT["H"], LATENT["L"])
+    d["dws"] = torch.empty(max(dws, 16), dtype=torch.uint8, device=dev)
+    d["lws"] = torch.empty(max(lws, 16), dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        run_step(b, d)
+    torch.cuda.synchronize()
+    timers = {k: Timer() for k in ("prefill", "decode", "latent")}
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            run_step(b, d, timers)
+        t1.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = reduce_max(t0.elapsed_time(t1) / args.steps, dev if world > 1 else None)
+    status = b.attn_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed steps")
+    per = {k: statistics.mean(v.ms()) for k, v in timers.items()}
+    per_max = {k: reduce_max(v, dev if world > 1 else None) for k, v in per.items()}
+
+    P, Dd, Lt = PREFILL, DECODE, LATENT
+    pf_flops = workload.prefill_flops(P["B"], P["Hq"], P["S"], P["D"], True)
+    dec_bytes = workload.decode_bytes(Dd["B"], Dd["Hq"], Dd["Hkv"], Dd["L"], Dd["D"])
+    lat_bytes = workload.latent_bytes(Lt["B"], Lt["H"], Lt["L"])
+    value = aggregate_rate(pf_flops, world, per_max["prefill"] / 1e3) / 1e12
+    hbm, tf_burst, tf_sust, peak_kind = measured_peaks()
+    achieved = pf_flops / (per["prefill"] / 1e3) / 1e12
+
+    # end to end through the public API with host buffers: H2D q/k/v, prefill, D2H o
+    e2e = None
+    if not args.no_e2e:
+        qh = host["q"].pin_memory()
+        kh = host["k"].pin_memory()
+        vh = host["v"].pin_memory()
+        oh = torch.empty(d["o"].shape, dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step():
+            d["q"].copy_(qh, non_blocking=True)
+            d["k"].copy_(kh, non_blocking=True)
+            d["v"].copy_(vh, non_blocking=True)
+            b.attn_prefill(d["q"], d["k"], d["v"], causal=True, rope=True, rope_theta=THETA,
+                           o=d["o"])
+            oh.copy_(d["o"], non_blocking=True)
+
+        te = time_call(e2e_step, iters=max(2, args.steps // 2), warmup=1)
+        te = reduce_max(te, dev if world > 1 else None)
+        e2e = {"value": round(aggregate_rate(pf_flops, world, te / 1e3) / 1e12, 2),
+               "unit": "TFLOPS",
+               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (qh, kh, vh))),
+               "d2h_bytes_per_step": int(oh.numel() * oh.element_size()),
+               "ms_per_step": round(te, 4)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, random caches)",
+        "config": {"workload": "causal GQA prefill Z=4 Hq=32 Hkv=8 D=128 S=16384 bf16 fused "
+                               "RoPE 1e4 + GQA decode B=128 Hq=32 Hkv=8 D=128 L=2048 + latent "
+                               "decode B=128 H=16 448+64 L=2048",
+                   "l2": "every input > 129 MB L2 (no flush needed)",
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "decode": {"ms": round(per["decode"], 5),
+                   "gbs": round(dec_bytes / (per_max["decode"] / 1e3) / 1e9 * world, 1),
+                   "frac_of_hbm": round(dec_bytes / (per["decode"] / 1e3) / 1e9 / hbm, 4)},
+        "latent_decode": {"ms": round(per["latent"], 5),
+                          "gbs": round(lat_bytes / (per_max["latent"] / 1e3) / 1e9 * world, 1),
+                          "frac_of_hbm": round(lat_bytes / (per["latent"] / 1e3) / 1e9 / hbm, 4)},
+        "prefill": {"ms": round(per["prefill"], 4), "tflops": round(achieved, 2)},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": tf_sust,
+                     "unit": "TFLOP/s", "frac": round(achieved / tf_sust, 4),
+                     "traffic": None,
+                     "peak_kind": f"bf16 sustained ({peak_kind}); kernel timed inside the step"},
+        "gpu_launches": args.steps * (1 + 1 + 1),
+        "clocks": clocks.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_variants:
+        line["variants"] = variants(b, d)
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(seconds_budget=20.0)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------------------------
+# the CPU oracle as the reference arm / CPU baseline
+# ----------------------------------------------------------------------------------------------
+
+def oracle_prefill_sample(S: int, seed: int = 0):
+    """One (batch, query head) of the causal RoPE prefill, computed by the float64 oracle."""
+    import oracle
+    from attention_attn_prefill_02_gb300 import synthetic, workload
+
+    D = PREFILL["D"]
+    q = synthetic.normal((1, 1, S, D), seed, "bf16")
+    k = synthetic.normal((1, 1, S, D), seed + 1, "bf16")
+    v = synthetic.normal((1, 1, S, D), seed + 2, "bf16")
+    args = [oracle.as_f64(x) for x in (q, k, v)]
+    t = time.perf_counter()
+    oracle.prefill(*args, causal=True, rope=True, theta=THETA)
+    dt = time.perf_counter() - t
+    return workload.prefill_flops(1, 1, S, D, True), dt
+
+
+def cpu_baseline(seconds_budget=20.0):
+    S = 8192
+    flops, dt = oracle_prefill_sample(S)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOPS", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"one (batch, head) of the causal RoPE prefill at S={S}, D=128, float64 "
+                      f"NumPy ({dt:.1f} s)"}
+
+
+def reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    S = 2048
+    for _ in range(args.warmup):
+        oracle_prefill_sample(S)
+    tot_f, tot_t = 0.0, 0.0
+    for i in range(args.steps):
+        f, t = oracle_prefill_sample(S, seed=i)
+        tot_f += f
+        tot_t += t
+    value = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16 dequantised to float64)",
+            "config": {"workload": "causal GQA prefill D=128 fused RoPE 1e4: per step one "
+                                   f"(batch, head) at S={S} on the host CPU"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"one (batch, head) at S={S} per step"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def single_case(args):
+    """Run one kernel alone `steps` times (the small cases the ncu captures use)."""
+    import torch
+
+    from attention_attn_prefill_02_gb300 import binding as b
+    from attention_attn_prefill_02_gb300 import synthetic
+
+    torch.cuda.set_device(0)
+    b.lib()
+    if args.case in ("prefill", "prefill-unfused", "prefill-d64"):
+        D = 64 if args.case == "prefill-d64" else 128
+        Hkv = 32 if D == 64 else 8
+        causal = D == 128
+        q, k, v = synthetic.prefill_inputs(4, 32, Hkv, args.S, D, "bf16", seed=1)
+        q, k, v = q.cuda(), k.cuda(), v.cuda()
+        b.attn_rope_table_reserve(D, THETA, args.S + 1)
+        rope = args.case == "prefill"
+        fn = lambda: b.attn_prefill(q, k, v, causal=causal, rope=rope, rope_theta=THETA)
+    elif args.case == "decode":
+        q, kc, vc, cl = synthetic.decode_inputs(args.B, 32, 8, 2048, 128, 2048, seed=1)
+        q, kc, vc, cl = q.cuda(), kc.cuda(), vc.cuda(), cl.cuda()
+        b.attn_rope_table_reserve(128, THETA, 2049)
+        fn = lambda: b.attn_decode(q, kc, vc, cl, rope=True, rope_theta=THETA)
+    elif args.case == "latent":
+        q, c, cl = synthetic.latent_inputs(args.B, 16, 2048, 2048, seed=1)
+        q, c, cl = q.cuda(), c.cuda(), cl.cuda()
+        b.attn_rope_table_reserve(64, THETA, 2049)
+        fn = lambda: b.attn_decode_latent(q, c, cl, rope=True, rope_theta=THETA)
+    else:
+        q = synthetic.rope_input(4, 40, args.S, 128, "bf16", seed=1).cuda()
+        b.attn_rope_table_reserve(128, THETA, args.S + 1)
+        fn = lambda: b.rope_apply(q, theta=THETA)
+    ms = time_call(fn, iters=args.steps, warmup=args.warmup)
+    assert b.attn_get_device_status() == 0
+    print(json.dumps({"case": args.case, "S": args.S, "B": args.B, "ms": round(ms, 5)}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--case", default=None,
+                    choices=["prefill", "prefill-unfused", "prefill-d64", "decode", "latent",
+                             "rope"], help="time one kernel alone (for profiler captures)")
+    ap.add_argument("--S", type=int, default=4096)
+    ap.add_argument("--B", type=int, default=128)
+    args = ap.parse_args()
+    if args.case:
+        return single_case(args)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

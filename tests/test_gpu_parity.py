@@ -105,6 +105,33 @@ def test_prefill_unfused_rope_tiny_config():
     check(o.cpu(), ro, what="O")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,pos0", [
+    (1, 4, 1, 128, 64, True, 0),       # the tiny config: RoPE fused into the Q/K loads
+    (2, 8, 2, 700, 128, True, 0),      # GQA, ragged tail, several items per head
+    (1, 2, 2, 300, 64, False, 5000),   # non-causal, positions offset
+    (1, 4, 1, 257, 128, True, 3),      # one row past a whole item
+])
+def test_prefill_fused_rope(B, Hq, Hkv, S, D, causal, pos0):
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=S + 1)
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, rope=True,
+                                  rope_theta=10000.0, pos0=pos0, want_lse=True)
+    status_ok()
+    ro, rl = oracle.prefill(f64(q), f64(k), f64(v), causal=causal, rope=True, theta=10000.0,
+                            pos0=pos0)
+    check(o.cpu(), ro, what="O")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE")
+
+
+def test_prefill_fused_equals_unfused_closely():
+    """Fused RoPE and rope_apply + attention round the rotated Q/K identically (both bf16)."""
+    q, k, v = synthetic.prefill_inputs(1, 8, 2, 512, 128, "bf16", seed=4)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    of = binding.attn_prefill(qd, kd, vd, causal=True, rope=True)
+    ou = binding.attn_prefill(binding.rope_apply(qd), binding.rope_apply(kd), vd, causal=True)
+    status_ok()
+    assert (of.float() - ou.float()).abs().max().item() <= 1e-2
+
+
 def test_prefill_large_logits_rescale_path():
     """Rows whose maximum grows late force the lazy O rescale; scale 1 makes logits large."""
     B, Hq, Hkv, S, D = 1, 2, 1, 700, 64
