@@ -52,6 +52,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
     L.attn_decode.restype = i
     L.attn_decode.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp, sz, vp]
+    L.attn_decode_noalloc.restype = i
+    L.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp]
     L.attn_decode_latent_workspace_size.restype = sz
     L.attn_decode_latent_workspace_size.argtypes = [i, i, i]
     L.attn_decode_latent.restype = i
@@ -137,6 +139,24 @@ def attn_decode(q, k_cache, v_cache, cache_len, o=None, lse=None, want_lse=False
                              _ptr(o), _ptr(lse), DTYPE_CODES[q.dtype], B, Hq, Hkv, D,
                              float(softmax_scale), int(bool(rope)), float(rope_theta),
                              _ptr(workspace), wbytes, _stream(stream)), "attn_decode")
+    return (o, lse) if (want_lse or lse is not None) else o
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, cache_len, o=None, lse=None, want_lse=False,
+                        softmax_scale=0.0, rope=True, rope_theta=10000.0, stream=None):
+    """attn_decode without a workspace: its split partials use the library's fixed 2 MiB
+    device array (for callers that cannot allocate at call time)."""
+    _require_cuda(q, k_cache, v_cache, cache_len, o, lse)
+    B, Hq, D = q.shape
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    if o is None:
+        o = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len),
+                                     Lmax, _ptr(o), _ptr(lse), DTYPE_CODES[q.dtype], B, Hq, Hkv,
+                                     D, float(softmax_scale), int(bool(rope)), float(rope_theta),
+                                     _stream(stream)), "attn_decode_noalloc")
     return (o, lse) if (want_lse or lse is not None) else o
 
 

@@ -25,6 +25,10 @@ attn_status_t check_device();
 // copy).  Returns nullptr on failure and sets *err.
 const float2* rope_table(int D, float theta, int npos, attn_status_t* err);
 
+// The cached table for (D, theta) if it already covers [0, npos) on the current device, else
+// nullptr.  Never allocates.
+const float2* rope_table_find(int D, float theta, int npos);
+
 // Encode a 3-D tiled TMA descriptor for a dense row-major tensor of `elem_bytes`-byte elements
 // with logical sizes {inner, mid, outer} (innermost first), box {box_inner, box_mid, 1} and
 // 128-byte swizzling.  Returns false on failure.

@@ -82,6 +82,20 @@ std::map<std::tuple<int, int, uint32_t>, RopeEntry> g_rope;
 std::vector<float2*> g_rope_retired;  // grown-out tables stay alive: kernels may still read them
 }  // namespace
 
+const float2* rope_table_find(int D, float theta, int npos) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  uint32_t tbits;
+  memcpy(&tbits, &theta, 4);
+  std::lock_guard<std::mutex> lk(g_rope_mu);
+  auto it = g_rope.find(std::make_tuple(dev, D, tbits));
+  if (it == g_rope.end() || !it->second.ptr || it->second.npos < npos) return nullptr;
+  return it->second.ptr;
+}
+
 const float2* rope_table(int D, float theta, int npos, attn_status_t* err) {
   *err = ATTN_OK;
   int dev = 0;

@@ -134,6 +134,34 @@ ATTN_API attn_status_t attn_decode(const void* q, const void* k_cache, const voi
                           attn_stream_t stream);
 
 /*
+ * attn_decode_noalloc — attn_decode for callers that cannot allocate device memory at call
+ * time: a host that forbids allocation in its enqueue path (inference-engine plugins), a
+ * process whose device memory is entirely owned by another allocator, or a latency-bound
+ * serving loop that cannot afford an allocation's cost or implicit synchronisation.  It takes
+ * the same arguments as attn_decode minus the workspace, computes the same result, and calls
+ * no cudaMalloc, cudaFree or other allocating routine.  The pages have no counterpart; this is
+ * an interface convenience around the same kernels.
+ *   Scratch: the split partials live in one file-scope device array of 2 MiB (2097152 bytes)
+ *   that every GPU loading this library holds until the process exits.  A call whose
+ *   attn_decode_workspace_size(B,Hq,Hkv,D,Lmax) exceeds 2 MiB returns ATTN_ERR_WORKSPACE
+ *   without launching.  All calls share the array and it keeps the last call's contents; every
+ *   slot a call reads is written earlier in the same call, so nothing needs clearing.  Calls
+ *   whose execution overlaps on the GPU (e.g. on two streams) race on the array: serialise them.
+ *   Set-up: the first call on each device resolves the array's device address with
+ *   cudaGetSymbolAddress (which may load the library's device code on that device); make that
+ *   first call before any stream capture.
+ *   RoPE: rope = 1 needs the cos/sin table for (D, rope_theta) covering position Lmax to exist
+ *   already (attn_rope_table_reserve(D, rope_theta, Lmax) or an earlier attn_decode call);
+ *   otherwise ATTN_ERR_WORKSPACE, because building it would allocate.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA, NO_DEVICE (as attn_decode otherwise).
+ */
+ATTN_API attn_status_t attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* cache_len, int Lmax, void* o, float* lse,
+                                  attn_dtype_t dtype, int B, int Hq, int Hkv, int D,
+                                  float softmax_scale, int rope, float rope_theta,
+                                  attn_stream_t stream);
+
+/*
  * attn_decode_latent_workspace_size — bytes of workspace attn_decode_latent needs.
  */
 ATTN_API size_t attn_decode_latent_workspace_size(int B, int H, int Lmax);
