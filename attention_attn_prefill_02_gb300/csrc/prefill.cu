@@ -314,7 +314,28 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
     }
   } else if (ROPE && warp >= kRopeWarp0) {
     // ------------------------------------------------------------------ K-tile RoPE warps
-    const int rt = threadIdx.x - kRopeWarp0 * 32;  // 0..63: rows rt and rt + 64 of each tile
+    // Thread rt owns 8 frequency pairs (chunk c) and the rows g, g + kGroups, ... of every K
+    // tile.  The cos/sin of those rows come from a rotation recurrence in float32 instead of
+    // table loads: one step advances the position by kGroups, one tile step by 128, and every
+    // item restarts from the table value at position pos0 + g.
+    constexpr int kChunks = D / 16;                 // 8-pair chunks in the first half of a row
+    constexpr int kGroups = kRopeThreads / kChunks;  // row stride between a thread's rows
+    constexpr int kRowsPer = BN / kGroups;
+    const int rt = threadIdx.x - kRopeWarp0 * 32;
+    const int c = rt % kChunks, g = rt / kChunks;
+    float anc[16], stp[16], til[16];  // (cos, sin) x 8 pairs: anchor, row step, tile step
+    {
+      const float* t0 = reinterpret_cast<const float*>(p.table + static_cast<size_t>(p.pos0 + g) * (D / 2) + c * 8);
+      const float* t1 = reinterpret_cast<const float*>(p.table + static_cast<size_t>(kGroups) * (D / 2) + c * 8);
+      const float* t2 = reinterpret_cast<const float*>(p.table + static_cast<size_t>(BN) * (D / 2) + c * 8);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        anc[e] = __ldg(t0 + e);
+        stp[e] = __ldg(t1 + e);
+        til[e] = __ldg(t2 + e);
+      }
+    }
+    const int c2 = c + kChunks;
     int stage = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -324,15 +345,49 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
       int m, b, hq;
       item_coords(p, it, m, b, hq);
       const int nkv = max(kv_tiles_for(p, m * kRowsPerItem), kv_tiles_for(p, m * kRowsPerItem + BM));
+      float cs[16];  // (cos, sin) of this thread's first row in tile j
+#pragma unroll
+      for (int e = 0; e < 16; ++e) cs[e] = anc[e];
       for (int j = 0; j < nkv && ok; ++j) {
         if (!(ok = mbar_wait(&bars->kv_full[stage], ph, p.status))) break;
         uint8_t* tile = smem + C::kKVOff + stage * C::kKVTileBytes;
+        float w[16];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int key = j * BN + rt + h * 64;
-          if (key < p.S)
-            rope_rotate_row<D>(tile, rt + h * 64,
-                               p.table + static_cast<size_t>(p.pos0 + key) * (D / 2));
+        for (int e = 0; e < 16; ++e) w[e] = cs[e];
+#pragma unroll 4
+        for (int k = 0; k < kRowsPer; ++k) {
+          const int row = g + k * kGroups;
+          if (j * BN + row < p.S) {
+            uint4* p1 = reinterpret_cast<uint4*>(tile + (c >> 3) * (128 * 128) + sw128_offset(row, c & 7));
+            uint4* p2 = reinterpret_cast<uint4*>(tile + (c2 >> 3) * (128 * 128) + sw128_offset(row, c2 & 7));
+            uint4 a = *p1, bq = *p2;
+            uint32_t* aw = reinterpret_cast<uint32_t*>(&a);
+            uint32_t* bw = reinterpret_cast<uint32_t*>(&bq);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&aw[q]));
+              const float2 y = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&bw[q]));
+              const float c0 = w[4 * q], s0 = w[4 * q + 1], c1 = w[4 * q + 2], s1 = w[4 * q + 3];
+              aw[q] = pack_bf16(x.x * c0 - y.x * s0, x.y * c1 - y.y * s1);
+              bw[q] = pack_bf16(y.x * c0 + x.x * s0, y.y * c1 + x.y * s1);
+            }
+            *p1 = a;
+            *p2 = bq;
+          }
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {  // advance kGroups positions
+            const float cc = w[e] * stp[e] - w[e + 1] * stp[e + 1];
+            const float ss = w[e + 1] * stp[e] + w[e] * stp[e + 1];
+            w[e] = cc;
+            w[e + 1] = ss;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {  // advance one tile (128 positions)
+          const float cc = cs[e] * til[e] - cs[e + 1] * til[e + 1];
+          const float ss = cs[e + 1] * til[e] + cs[e] * til[e + 1];
+          cs[e] = cc;
+          cs[e + 1] = ss;
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars->k_ready[stage]);
