@@ -6,7 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/attn.h"
+#include "attn.h"
 
 namespace attn {
 

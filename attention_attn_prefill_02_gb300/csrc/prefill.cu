@@ -44,11 +44,14 @@ struct Cfg {
   static constexpr int kBoxes = D / 64;                 // 128-byte swizzle boxes per row
   static constexpr int kQTileBytes = BM * D * 2;
   static constexpr int kKVTileBytes = BN * D * 2;
-  static constexpr int kStages = D == 128 ? 4 : 6;      // K/V ring depth (even: K in even slots)
-  static_assert(kStages % 2 == 0, "K tiles must always land in even ring slots");
+  // Separate K and V rings; K is fetched one KV step ahead of V, so a K tile has about two KV
+  // steps between landing and its first MMA (room for the TMA latency plus the fused RoPE).
+  static constexpr int kKStages = D == 128 ? 3 : 4;
+  static constexpr int kVStages = D == 128 ? 2 : 3;
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kQTileBytes;
-  static constexpr int kBarOff = kKVOff + kStages * kKVTileBytes;
+  static constexpr int kVOff = kKVOff + kKStages * kKVTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kKVTileBytes;
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
@@ -69,8 +72,8 @@ struct Params {
 struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
-  uint64_t kv_full[8], kv_empty[8];
-  uint64_t q_ready[2], k_ready[8];  // fused RoPE: tile rotated in shared memory
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t q_ready[2], k_ready[4];  // fused RoPE: tile rotated in shared memory
   uint32_t tmem_slot;
 };
 
@@ -145,10 +148,14 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
       mbar_init(&bars->o_full[t], 1);
       mbar_init(&bars->o_empty[t], 128);
     }
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->k_ready[s], kRopeThreads);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     mbar_init(&bars->q_ready[0], 128);
     mbar_init(&bars->q_ready[1], 128);
@@ -168,8 +175,8 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       uint32_t ph_qe[2] = {0, 0};
-      int stage = 0;
-      uint32_t ph = 0;
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;
       bool ok = true;
       for (int r = 0; r < rounds && ok; ++r) {
         const int it = item_for(r, blockIdx.x, gridDim.x);
@@ -194,21 +201,33 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
             tma_load_3d(dst + bx * BM * 128, &tmQ, &bars->q_full[t], bx * 64,
                         m * kRowsPerItem + t * BM, b * p.Hq + hq);
         }
-        for (int j = 0; j < nkv && ok; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
-            if (!(ok = mbar_wait(&bars->kv_empty[stage], ph ^ 1, p.status))) break;
-            mbar_arrive_expect_tx(&bars->kv_full[stage], C::kKVTileBytes);
-            uint8_t* dst = smem + C::kKVOff + stage * C::kKVTileBytes;
-            const CUtensorMap* tm = kv ? &tmV : &tmK;
+        // issue order K_0, K_1, V_0, K_2, V_1, ...: K runs one tile ahead of V
+        auto load_k = [&](int j) {
+          ok = mbar_wait(&bars->k_empty[ks], kph ^ 1, p.status);
+          if (!ok) return;
+          mbar_arrive_expect_tx(&bars->k_full[ks], C::kKVTileBytes);
+          uint8_t* dst = smem + C::kKVOff + ks * C::kKVTileBytes;
 #pragma unroll
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-              tma_load_3d(dst + bx * BN * 128, tm, &bars->kv_full[stage], bx * 64, j * BN,
-                          b * p.Hkv + hkv);
-            if (++stage == C::kStages) {
-              stage = 0;
-              ph ^= 1;
-            }
-          }
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_3d(dst + bx * BN * 128, &tmK, &bars->k_full[ks], bx * 64, j * BN,
+                        b * p.Hkv + hkv);
+          if (++ks == C::kKStages) { ks = 0; kph ^= 1; }
+        };
+        auto load_v = [&](int j) {
+          ok = mbar_wait(&bars->v_empty[vs], vph ^ 1, p.status);
+          if (!ok) return;
+          mbar_arrive_expect_tx(&bars->v_full[vs], C::kKVTileBytes);
+          uint8_t* dst = smem + C::kVOff + vs * C::kKVTileBytes;
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_3d(dst + bx * BN * 128, &tmV, &bars->v_full[vs], bx * 64, j * BN,
+                        b * p.Hkv + hkv);
+          if (++vs == C::kVStages) { vs = 0; vph ^= 1; }
+        };
+        if (ok) load_k(0);
+        for (int j = 0; j < nkv && ok; ++j) {
+          if (j + 1 < nkv) load_k(j + 1);
+          if (ok) load_v(j);
         }
       }
     }
@@ -218,14 +237,15 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
       const uint32_t idesc_s = make_idesc(1, 1, false, false, BN, BM);  // bf16 x bf16 -> f32
       const uint32_t idesc_pv = make_idesc(1, 1, false, true, D, BM);   // V is MN-major
       const uint32_t q_base = smem_u32(smem + C::kQOff);
-      const uint32_t kv_base = smem_u32(smem + C::kKVOff);
+      const uint32_t k_base = smem_u32(smem + C::kKVOff);
+      const uint32_t v_base = smem_u32(smem + C::kVOff);
       uint32_t ph_qf[2] = {0, 0}, ph_pf[2] = {0, 0}, ph_oe[2] = {0, 0};
-      int stage = 0;
-      uint32_t ph = 0;
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;
       bool ok = true;
       auto issue_s = [&](int t, int slot) {
         const uint32_t qa = q_base + t * C::kQTileBytes;
-        const uint32_t ka = kv_base + slot * C::kKVTileBytes;
+        const uint32_t ka = k_base + slot * C::kKVTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
@@ -235,7 +255,7 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         }
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t va = kv_base + slot * C::kKVTileBytes;
+        const uint32_t va = v_base + slot * C::kKVTileBytes;
         const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
@@ -261,10 +281,10 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         }
         if (!ok) break;
         // j = 0: S_t = Q_t K_0^T for both tiles
-        const int kslot = stage;
-        if (!(ok = mbar_wait(ROPE ? &bars->k_ready[kslot] : &bars->kv_full[kslot], ph, p.status)))
+        const int kslot = ks;
+        if (!(ok = mbar_wait(ROPE ? &bars->k_ready[kslot] : &bars->k_full[kslot], kph, p.status)))
           break;
-        if (++stage == C::kStages) { stage = 0; ph ^= 1; }
+        if (++ks == C::kKStages) { ks = 0; kph ^= 1; }
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -273,18 +293,18 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           umma_commit(&bars->s_full[t]);
           if (n[t] == 1) umma_commit(&bars->q_empty[t]);
         }
-        umma_commit(&bars->kv_empty[kslot]);
+        umma_commit(&bars->k_empty[kslot]);
         for (int j = 1; j <= nkv && ok; ++j) {
-          const int vslot = stage;
-          if (!(ok = mbar_wait(&bars->kv_full[vslot], ph, p.status))) break;
-          if (++stage == C::kStages) { stage = 0; ph ^= 1; }
+          const int vslot = vs;
+          if (!(ok = mbar_wait(&bars->v_full[vslot], vph, p.status))) break;
+          if (++vs == C::kVStages) { vs = 0; vph ^= 1; }
           int kslot2 = -1;
           if (j < nkv) {
-            kslot2 = stage;
-            if (!(ok = mbar_wait(ROPE ? &bars->k_ready[kslot2] : &bars->kv_full[kslot2], ph,
+            kslot2 = ks;
+            if (!(ok = mbar_wait(ROPE ? &bars->k_ready[kslot2] : &bars->k_full[kslot2], kph,
                                  p.status)))
               break;
-            if (++stage == C::kStages) { stage = 0; ph ^= 1; }
+            if (++ks == C::kKStages) { ks = 0; kph ^= 1; }
           }
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
@@ -307,8 +327,8 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
               if (j == n[t] - 1) umma_commit(&bars->q_empty[t]);
             }
           }
-          umma_commit(&bars->kv_empty[vslot]);
-          if (kslot2 >= 0) umma_commit(&bars->kv_empty[kslot2]);
+          umma_commit(&bars->v_empty[vslot]);
+          if (kslot2 >= 0) umma_commit(&bars->k_empty[kslot2]);
         }
       }
     }
@@ -323,19 +343,26 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
     constexpr int kRowsPer = BN / kGroups;
     const int rt = threadIdx.x - kRopeWarp0 * 32;
     const int c = rt % kChunks, g = rt / kChunks;
-    float anc[16], stp[16], til[16];  // (cos, sin) x 8 pairs: anchor, row step, tile step
+    // cos / sin of the 8 pairs as float2 over pairs (2q, 2q+1): anchor (position pos0 + g) and
+    // row step (kGroups positions).  After a tile's kRowsPer steps the recurrence stands on row
+    // g of the next tile, so it simply continues; each item restarts from the anchor.
+    float2 anc_c[4], anc_s[4], stp_c[4], stp_s[4];
     {
-      const float* t0 = reinterpret_cast<const float*>(p.table + static_cast<size_t>(p.pos0 + g) * (D / 2) + c * 8);
-      const float* t1 = reinterpret_cast<const float*>(p.table + static_cast<size_t>(kGroups) * (D / 2) + c * 8);
-      const float* t2 = reinterpret_cast<const float*>(p.table + static_cast<size_t>(BN) * (D / 2) + c * 8);
+      const float2* t0 = p.table + static_cast<size_t>(p.pos0 + g) * (D / 2) + c * 8;
+      const float2* t1 = p.table + static_cast<size_t>(kGroups) * (D / 2) + c * 8;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        anc[e] = __ldg(t0 + e);
-        stp[e] = __ldg(t1 + e);
-        til[e] = __ldg(t2 + e);
+      for (int q = 0; q < 4; ++q) {
+        const float2 a = __ldg(t0 + 2 * q), a1 = __ldg(t0 + 2 * q + 1);
+        const float2 b = __ldg(t1 + 2 * q), b1 = __ldg(t1 + 2 * q + 1);
+        anc_c[q] = make_float2(a.x, a1.x);
+        anc_s[q] = make_float2(a.y, a1.y);
+        stp_c[q] = make_float2(b.x, b1.x);
+        stp_s[q] = make_float2(-b.y, -b1.y);  // negated: see advance()
       }
     }
     const int c2 = c + kChunks;
+    const uint32_t off1 = (c >> 3) * (128 * 128) + ((c & 7) << 4);
+    const uint32_t off2 = (c2 >> 3) * (128 * 128) + ((c2 & 7) << 4);
     int stage = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -345,21 +372,23 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
       int m, b, hq;
       item_coords(p, it, m, b, hq);
       const int nkv = max(kv_tiles_for(p, m * kRowsPerItem), kv_tiles_for(p, m * kRowsPerItem + BM));
-      float cs[16];  // (cos, sin) of this thread's first row in tile j
+      float2 wc[4], ws[4];  // (cos, sin) at this thread's current row
 #pragma unroll
-      for (int e = 0; e < 16; ++e) cs[e] = anc[e];
+      for (int q = 0; q < 4; ++q) {
+        wc[q] = anc_c[q];
+        ws[q] = anc_s[q];
+      }
       for (int j = 0; j < nkv && ok; ++j) {
-        if (!(ok = mbar_wait(&bars->kv_full[stage], ph, p.status))) break;
+        if (!(ok = mbar_wait(&bars->k_full[stage], ph, p.status))) break;
         uint8_t* tile = smem + C::kKVOff + stage * C::kKVTileBytes;
-        float w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = cs[e];
-#pragma unroll 4
+        const int rows_valid = p.S - j * BN;  // rows >= this are past the sequence (zeros)
+#pragma unroll 2
         for (int k = 0; k < kRowsPer; ++k) {
           const int row = g + k * kGroups;
-          if (j * BN + row < p.S) {
-            uint4* p1 = reinterpret_cast<uint4*>(tile + (c >> 3) * (128 * 128) + sw128_offset(row, c & 7));
-            uint4* p2 = reinterpret_cast<uint4*>(tile + (c2 >> 3) * (128 * 128) + sw128_offset(row, c2 & 7));
+          const uint32_t rsw = static_cast<uint32_t>((row & 7) << 4);
+          uint4* p1 = reinterpret_cast<uint4*>(tile + row * 128 + (off1 ^ rsw));
+          uint4* p2 = reinterpret_cast<uint4*>(tile + row * 128 + (off2 ^ rsw));
+          if (row < rows_valid) {
             uint4 a = *p1, bq = *p2;
             uint32_t* aw = reinterpret_cast<uint32_t*>(&a);
             uint32_t* bw = reinterpret_cast<uint32_t*>(&bq);
@@ -367,33 +396,27 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
             for (int q = 0; q < 4; ++q) {
               const float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&aw[q]));
               const float2 y = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&bw[q]));
-              const float c0 = w[4 * q], s0 = w[4 * q + 1], c1 = w[4 * q + 2], s1 = w[4 * q + 3];
-              aw[q] = pack_bf16(x.x * c0 - y.x * s0, x.y * c1 - y.y * s1);
-              bw[q] = pack_bf16(y.x * c0 + x.x * s0, y.y * c1 + x.y * s1);
+              const float2 xn = __ffma2_rn(x, wc[q], __fmul2_rn(y, make_float2(-ws[q].x, -ws[q].y)));
+              const float2 yn = __ffma2_rn(y, wc[q], __fmul2_rn(x, ws[q]));
+              aw[q] = pack_bf16(xn.x, xn.y);
+              bw[q] = pack_bf16(yn.x, yn.y);
             }
             *p1 = a;
             *p2 = bq;
           }
+          // advance kGroups positions: c' = c dc - s ds, s' = s dc + c ds (stp_s holds -ds)
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {  // advance kGroups positions
-            const float cc = w[e] * stp[e] - w[e + 1] * stp[e + 1];
-            const float ss = w[e + 1] * stp[e] + w[e] * stp[e + 1];
-            w[e] = cc;
-            w[e + 1] = ss;
+          for (int q = 0; q < 4; ++q) {
+            const float2 c1 = __ffma2_rn(wc[q], stp_c[q], __fmul2_rn(ws[q], stp_s[q]));
+            const float2 s1 = __ffma2_rn(ws[q], stp_c[q], __fmul2_rn(wc[q], make_float2(-stp_s[q].x, -stp_s[q].y)));
+            wc[q] = c1;
+            ws[q] = s1;
           }
-        }
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {  // advance one tile (128 positions)
-          const float cc = cs[e] * til[e] - cs[e + 1] * til[e + 1];
-          const float ss = cs[e + 1] * til[e] + cs[e] * til[e + 1];
-          cs[e] = cc;
-          cs[e + 1] = ss;
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars->k_ready[stage]);
-        stage += 2;  // skip the V tile that follows in the ring
-        if (stage >= C::kStages) {
-          stage -= C::kStages;
+        if (++stage == C::kKStages) {
+          stage = 0;
           ph ^= 1;
         }
       }
@@ -431,23 +454,25 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         if (!(ok = mbar_wait(&bars->s_full[t], ph_s, p.status))) break;
         ph_s ^= 1;
         tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+        uint32_t sr[128];
+        tmem_ld128(tS, sr);
         const bool need_mask = (p.causal && j == n - 1) || (j * BN + BN > p.S);
         if (need_mask) {
-          const int lim = p.causal ? min(row + 1, p.S) : p.S;  // keys >= lim are hidden
+          const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BN;  // keys >= lim hidden
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (j * BN + c * 32 + e >= lim) sr[c][e] = __float_as_uint(-INFINITY);
+          for (int e = 0; e < 128; ++e)
+            if (e >= lim) sr[e] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // row maximum: four independent 3-input max chains
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+        for (int e = 0; e < 128; e += 8) {
+          a0 = fmax3(a0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+          a1 = fmax3(a1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+          a2 = fmax3(a2, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+          a3 = fmax3(a3, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
+        }
+        const float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
         const float m_tile = mx * p.c_log2;
         float f = 1.f;  // factor for O and l when the running maximum is raised
         if (j == 0) {
@@ -457,23 +482,33 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           l *= f;
           m_run = m_tile;
         }
-        const float neg_m = -m_run;
-        float sum = 0.f;
-        uint32_t pk[2][32];
+        // p = 2^(s * c - m): packed f32x2 FMA, one ex2 per element, four partial row sums
+        const float2 c2 = make_float2(p.c_log2, p.c_log2);
+        const float2 nm2 = make_float2(-m_run, -m_run);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
+        uint32_t pk[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][e]), p.c_log2, neg_m));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][e + 1]), p.c_log2, neg_m));
-            __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-            const float2 back = __bfloat1622float2(h);
-            sum += back.x + back.y;
-            pk[c >> 1][(c & 1) * 16 + e / 2] = *reinterpret_cast<uint32_t*>(&h);
-          }
-        l += sum;
-        tmem_st32(tS, pk[0]);
-        tmem_st32(tS + 32, pk[1]);
+        for (int e = 0; e < 128; e += 8) {
+          float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
+          float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
+          float2 x2 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5])), c2, nm2);
+          float2 x3 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7])), c2, nm2);
+          x0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+          x1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+          x2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
+          x3 = make_float2(fast_exp2(x3.x), fast_exp2(x3.y));
+          acc0 = __fadd2_rn(acc0, x0);
+          acc1 = __fadd2_rn(acc1, x1);
+          acc2 = __fadd2_rn(acc2, x2);
+          acc3 = __fadd2_rn(acc3, x3);
+          pk[e / 2] = pack_bf16(x0.x, x0.y);
+          pk[e / 2 + 1] = pack_bf16(x1.x, x1.y);
+          pk[e / 2 + 2] = pack_bf16(x2.x, x2.y);
+          pk[e / 2 + 3] = pack_bf16(x3.x, x3.y);
+        }
+        const float2 accs = __fadd2_rn(__fadd2_rn(acc0, acc1), __fadd2_rn(acc2, acc3));
+        l += accs.x + accs.y;
+        tmem_st64(tS, pk);
         // tcgen05.ld / st are warp-collective: rescale when any lane of the warp needs it
         // (lanes that do not have f == 1).
         if (__any_sync(0xffffffffu, f != 1.f)) {
