@@ -465,6 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     compute_bar_sync();
 
+    // the 16 x 512 query tile stays in registers for the whole item (A fragments)
+    uint32_t qa[kLatQK / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < kLatQK / 16; ++kk)
+      ldsm_x4(qs_addr + (lane & 15) * kLatQPitch + (kk * 16 + (lane >> 4) * 8) * 2, qa[kk][0],
+              qa[kk][1], qa[kk][2], qa[kk][3]);
+
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float acc[kLatColsPerWarp / 8][4];
 #pragma unroll
@@ -474,20 +481,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&full[stage], phase, p.status)) return;
       const uint32_t ct = smem_u32(smem + stage * kLatTileBytes);
       const int par = tcount & 1;
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float s[2][4];
       {
+        // two independent accumulator chains over the 32 k-steps (even / odd), summed at the end
+        float se[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float so[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int m = lane >> 3;
         const int key = warp * 16 + (m >> 1) * 8 + (lane & 7);
-#pragma unroll 8
-        for (int kk = 0; kk < kLatQK / 16; ++kk) {
-          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-          ldsm_x4(qs_addr + (lane & 15) * kLatQPitch + (kk * 16 + (lane >> 4) * 8) * 2, a0, a1,
-                  a2, a3);
+#pragma unroll
+        for (int kk = 0; kk < kLatQK / 16; kk += 2) {
+          uint32_t b0, b1, b2, b3, b4, b5, b6, b7;
           const int c = kk * 2 + (m & 1);
+          const int cn = c + 2;
           ldsm_x4(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
-          mma_bf16_16816(s[0], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(s[1], a0, a1, a2, a3, b2, b3);
+          ldsm_x4(ct + (cn >> 3) * kTileKeys * 128 + sw128_offset(key, cn & 7), b4, b5, b6, b7);
+          mma_bf16_16816(se[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+          mma_bf16_16816(se[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+          mma_bf16_16816(so[0], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2], qa[kk + 1][3], b4, b5);
+          mma_bf16_16816(so[1], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2], qa[kk + 1][3], b6, b7);
         }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[nt][e] = se[nt][e] + so[nt][e];
       }
       float rm0 = -INFINITY, rm1 = -INFINITY;
 #pragma unroll

@@ -39,15 +39,27 @@ __host__ __device__ constexpr int threads_for(bool rope) { return rope ? 384 : 3
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D>
+// Tile geometry for head dim D and element size ESZ (2 = bf16, 1 = fp8 e5m2).  Rows of 128 (or,
+// for 64-byte rows, 64) bytes are TMA-swizzled; the MMA advances 32 bytes per K step (16 bf16
+// or 32 fp8 elements) and 16 / 32 keys per PV step.
+template <int D, int ESZ>
 struct Cfg {
-  static constexpr int kBoxes = D / 64;                 // 128-byte swizzle boxes per row
-  static constexpr int kQTileBytes = BM * D * 2;
-  static constexpr int kKVTileBytes = BN * D * 2;
+  static constexpr int kRowBytes = D * ESZ;
+  static constexpr int kSwz = kRowBytes >= 128 ? 128 : kRowBytes;  // swizzle span (128 or 64 B)
+  static constexpr int kBoxElems = kSwz / ESZ;                    // elements per box row
+  static constexpr int kBoxes = kRowBytes / kSwz;                 // boxes per 128-row tile
+  static constexpr int kBoxBytes = 128 * kSwz;
+  static constexpr uint32_t kSwzCode = kSwz == 128 ? 2u : 4u;     // descriptor swizzle mode
+  static constexpr int kSBO = 8 * kSwz;                           // bytes per 8-row group
+  static constexpr int kKSteps = kRowBytes / 32;                  // QK^T steps over D
+  static constexpr int kPVKeys = 32 / ESZ;                        // keys per PV step
+  static constexpr int kPVSteps = BN / kPVKeys;
+  static constexpr int kQTileBytes = BM * kRowBytes;
+  static constexpr int kKVTileBytes = BN * kRowBytes;
   // Separate K and V rings; K is fetched one KV step ahead of V, so a K tile has about two KV
   // steps between landing and its first MMA (room for the TMA latency plus the fused RoPE).
-  static constexpr int kKStages = D == 128 ? 3 : 4;
-  static constexpr int kVStages = D == 128 ? 2 : 3;
+  static constexpr int kKStages = ESZ == 2 ? (D == 128 ? 3 : 4) : (D == 128 ? 4 : 6);
+  static constexpr int kVStages = ESZ == 2 ? (D == 128 ? 2 : 3) : (D == 128 ? 4 : 6);
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kQTileBytes;
   static constexpr int kVOff = kKVOff + kKStages * kKVTileBytes;
@@ -55,6 +67,7 @@ struct Cfg {
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  static_assert(kKStages <= 8 && kVStages <= 8, "barrier arrays hold 8 stages");
 };
 
 struct Params {
@@ -72,8 +85,8 @@ struct Params {
 struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t q_ready[2], k_ready[4];  // fused RoPE: tile rotated in shared memory
+  uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
+  uint64_t q_ready[2], k_ready[8];  // fused RoPE: tile rotated in shared memory
   uint32_t tmem_slot;
 };
 
@@ -128,11 +141,13 @@ __device__ __forceinline__ void rope_rotate_row(uint8_t* tile, int row,
   }
 }
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, int ESZ>
 __global__ void __launch_bounds__(threads_for(ROPE), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, ESZ>;
+  constexpr bool FP8 = ESZ == 1;
+  static_assert(!(FP8 && ROPE), "fp8 inputs take RoPE through a bf16 staging path (not fused here)");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -198,7 +213,7 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           uint8_t* dst = smem + C::kQOff + t * C::kQTileBytes;
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_3d(dst + bx * BM * 128, &tmQ, &bars->q_full[t], bx * 64,
+            tma_load_3d(dst + bx * C::kBoxBytes, &tmQ, &bars->q_full[t], bx * C::kBoxElems,
                         m * kRowsPerItem + t * BM, b * p.Hq + hq);
         }
         // issue order K_0, K_1, V_0, K_2, V_1, ...: K runs one tile ahead of V
@@ -209,8 +224,8 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           uint8_t* dst = smem + C::kKVOff + ks * C::kKVTileBytes;
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_3d(dst + bx * BN * 128, &tmK, &bars->k_full[ks], bx * 64, j * BN,
-                        b * p.Hkv + hkv);
+            tma_load_3d(dst + bx * C::kBoxBytes, &tmK, &bars->k_full[ks], bx * C::kBoxElems,
+                        j * BN, b * p.Hkv + hkv);
           if (++ks == C::kKStages) { ks = 0; kph ^= 1; }
         };
         auto load_v = [&](int j) {
@@ -220,8 +235,8 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           uint8_t* dst = smem + C::kVOff + vs * C::kKVTileBytes;
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_3d(dst + bx * BN * 128, &tmV, &bars->v_full[vs], bx * 64, j * BN,
-                        b * p.Hkv + hkv);
+            tma_load_3d(dst + bx * C::kBoxBytes, &tmV, &bars->v_full[vs], bx * C::kBoxElems,
+                        j * BN, b * p.Hkv + hkv);
           if (++vs == C::kVStages) { vs = 0; vph ^= 1; }
         };
         if (ok) load_k(0);
@@ -234,8 +249,9 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_s = make_idesc(1, 1, false, false, BN, BM);  // bf16 x bf16 -> f32
-      const uint32_t idesc_pv = make_idesc(1, 1, false, true, D, BM);   // V is MN-major
+      // bf16 (format 1) x bf16, or e5m2 (1) x e5m2 for S and e4m3 (0) P x e5m2 V for PV
+      const uint32_t idesc_s = make_idesc(1, 1, false, false, BN, BM);
+      const uint32_t idesc_pv = make_idesc(FP8 ? 0u : 1u, 1, false, true, D, BM);  // V MN-major
       const uint32_t q_base = smem_u32(smem + C::kQOff);
       const uint32_t k_base = smem_u32(smem + C::kKVOff);
       const uint32_t v_base = smem_u32(smem + C::kVOff);
@@ -247,21 +263,31 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         const uint32_t qa = q_base + t * C::kQTileBytes;
         const uint32_t ka = k_base + slot * C::kKVTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          const uint64_t ad = smem_desc(qa + off, 16, 1024, 2);
-          const uint64_t bd = smem_desc(ka + off, 16, 1024, 2);
-          umma_ss(tmem + (t ? C::kColS1 : C::kColS0), ad, bd, idesc_s, kk > 0);
+        for (int kk = 0; kk < C::kKSteps; ++kk) {
+          constexpr int kPerBox = C::kSwz / 32;
+          const uint32_t off = (kk / kPerBox) * C::kBoxBytes + (kk % kPerBox) * 32;
+          const uint64_t ad = smem_desc(qa + off, 16, C::kSBO, C::kSwzCode);
+          const uint64_t bd = smem_desc(ka + off, 16, C::kSBO, C::kSwzCode);
+          if constexpr (FP8)
+            umma_ss_f8(tmem + (t ? C::kColS1 : C::kColS0), ad, bd, idesc_s, kk > 0);
+          else
+            umma_ss(tmem + (t ? C::kColS1 : C::kColS0), ad, bd, idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
         const uint32_t va = v_base + slot * C::kKVTileBytes;
         const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = smem_desc(va + kk * 16 * 128, BN * 128, 1024, 2);
-          umma_ts(tmem + (t ? C::kColO1 : C::kColO0), pcol + kk * 8, bd, idesc_pv,
-                  (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < C::kPVSteps; ++kk) {
+          // P: 8 TMEM columns per step (16 bf16 or 32 fp8 keys); V rows of kSwz bytes per key
+          const uint64_t bd =
+              smem_desc(va + kk * C::kPVKeys * C::kSwz, C::kBoxBytes, C::kSBO, C::kSwzCode);
+          if constexpr (FP8)
+            umma_ts_f8(tmem + (t ? C::kColO1 : C::kColO0), pcol + kk * 8, bd, idesc_pv,
+                       (acc || kk > 0) ? 1u : 0u);
+          else
+            umma_ts(tmem + (t ? C::kColO1 : C::kColO0), pcol + kk * 8, bd, idesc_pv,
+                    (acc || kk > 0) ? 1u : 0u);
         }
       };
       for (int r = 0; r < rounds && ok; ++r) {
@@ -332,7 +358,8 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         }
       }
     }
-  } else if (ROPE && warp >= kRopeWarp0) {
+  } else if constexpr (ROPE) {
+   if (warp >= kRopeWarp0) {
     // ------------------------------------------------------------------ K-tile RoPE warps
     // Thread rt owns 8 frequency pairs (chunk c) and the rows g, g + kGroups, ... of every K
     // tile.  The cos/sin of those rows come from a rotation recurrence in float32 instead of
@@ -421,7 +448,9 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         }
       }
     }
-  } else if (warp < 8) {
+   }
+  }
+  if (warp < 8) {
     // ------------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;          // Q tile of this warpgroup
     const int quarter = warp & 3;     // TMEM lane quarter of this warp
@@ -440,7 +469,7 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
       const int n = kv_tiles_for(p, r0);
       if (n == 0) continue;
       const int row = r0 + lrow;
-      if constexpr (ROPE) {
+      if constexpr (ROPE && !FP8) {
         if (!(ok = mbar_wait(&bars->q_full[t], ph_q, p.status))) break;
         ph_q ^= 1;
         if (row < p.S)
@@ -486,7 +515,7 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         const float2 c2 = make_float2(p.c_log2, p.c_log2);
         const float2 nm2 = make_float2(-m_run, -m_run);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
-        uint32_t pk[64];
+        uint32_t pk[FP8 ? 32 : 64];
 #pragma unroll
         for (int e = 0; e < 128; e += 8) {
           float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
@@ -501,14 +530,25 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           acc1 = __fadd2_rn(acc1, x1);
           acc2 = __fadd2_rn(acc2, x2);
           acc3 = __fadd2_rn(acc3, x3);
-          pk[e / 2] = pack_bf16(x0.x, x0.y);
-          pk[e / 2 + 1] = pack_bf16(x1.x, x1.y);
-          pk[e / 2 + 2] = pack_bf16(x2.x, x2.y);
-          pk[e / 2 + 3] = pack_bf16(x3.x, x3.y);
+          if constexpr (FP8) {
+            // e4m3, four keys per TMEM column, lowest key in the lowest byte
+            pk[e / 4] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x0, __NV_SATFINITE, __NV_E4M3)) |
+                        (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x1, __NV_SATFINITE, __NV_E4M3)) << 16);
+            pk[e / 4 + 1] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x2, __NV_SATFINITE, __NV_E4M3)) |
+                            (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x3, __NV_SATFINITE, __NV_E4M3)) << 16);
+          } else {
+            pk[e / 2] = pack_bf16(x0.x, x0.y);
+            pk[e / 2 + 1] = pack_bf16(x1.x, x1.y);
+            pk[e / 2 + 2] = pack_bf16(x2.x, x2.y);
+            pk[e / 2 + 3] = pack_bf16(x3.x, x3.y);
+          }
         }
         const float2 accs = __fadd2_rn(__fadd2_rn(acc0, acc1), __fadd2_rn(acc2, acc3));
         l += accs.x + accs.y;
-        tmem_st64(tS, pk);
+        if constexpr (FP8)
+          tmem_st32(tS, pk);
+        else
+          tmem_st64(tS, pk);
         // tcgen05.ld / st are warp-collective: rescale when any lane of the warp needs it
         // (lanes that do not have f == 1).
         if (__any_sync(0xffffffffu, f != 1.f)) {
@@ -566,16 +606,16 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
   }
 }
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, int ESZ>
 attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o, float* lse,
                            float q_scale, float k_scale, float v_scale, int B, int Hq, int Hkv,
                            int S, int causal, float scale, const float2* table, int pos0,
                            cudaStream_t st) {
-  using C = Cfg<D>;
+  using C = Cfg<D, ESZ>;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_3d(&tq, q, 2, D, S, static_cast<uint64_t>(B) * Hq, 64, BM, 128) ||
-      !make_tmap_3d(&tk, k, 2, D, S, static_cast<uint64_t>(B) * Hkv, 64, BN, 128) ||
-      !make_tmap_3d(&tv, v, 2, D, S, static_cast<uint64_t>(B) * Hkv, 64, BN, 128))
+  if (!make_tmap_3d(&tq, q, ESZ, D, S, static_cast<uint64_t>(B) * Hq, C::kBoxElems, BM, C::kSwz) ||
+      !make_tmap_3d(&tk, k, ESZ, D, S, static_cast<uint64_t>(B) * Hkv, C::kBoxElems, BN, C::kSwz) ||
+      !make_tmap_3d(&tv, v, ESZ, D, S, static_cast<uint64_t>(B) * Hkv, C::kBoxElems, BN, C::kSwz))
     return ATTN_ERR_CUDA;
   Params p;
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -594,7 +634,7 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   p.v_scale = v_scale;
   p.table = table;
   p.pos0 = pos0;
-  auto kern = prefill_kernel<D, ROPE>;
+  auto kern = prefill_kernel<D, ROPE, ESZ>;
   if (!set_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes)) return ATTN_ERR_CUDA;
   const int grid = std::min(p.n_items, sm_count());
   kern<<<grid, threads_for(ROPE), C::kSmemBytes, st>>>(tq, tk, tv, p);
@@ -607,15 +647,17 @@ attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* 
                              attn_dtype_t dt, float q_scale, float k_scale, float v_scale, int B,
                              int Hq, int Hkv, int S, int D, int causal, float scale,
                              const float2* table, int pos0, cudaStream_t st) {
-  if (dt != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
-#define ATTN_PREFILL_CASE(DD, RR)                                                             \
-  if (D == DD && (table != nullptr) == RR)                                                    \
-    return launch_typed<DD, RR>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S,   \
-                                causal, scale, table, pos0, st);
-  ATTN_PREFILL_CASE(128, false)
-  ATTN_PREFILL_CASE(128, true)
-  ATTN_PREFILL_CASE(64, false)
-  ATTN_PREFILL_CASE(64, true)
+  const int esz = dt == ATTN_BF16 ? 2 : 1;
+#define ATTN_PREFILL_CASE(DD, RR, EE)                                                          \
+  if (D == DD && (table != nullptr) == RR && esz == EE)                                        \
+    return launch_typed<DD, RR, EE>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S, \
+                                    causal, scale, table, pos0, st);
+  ATTN_PREFILL_CASE(128, false, 2)
+  ATTN_PREFILL_CASE(128, true, 2)
+  ATTN_PREFILL_CASE(64, false, 2)
+  ATTN_PREFILL_CASE(64, true, 2)
+  ATTN_PREFILL_CASE(128, false, 1)
+  ATTN_PREFILL_CASE(64, false, 1)
 #undef ATTN_PREFILL_CASE
   return ATTN_ERR_UNSUPPORTED;
 }

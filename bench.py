@@ -272,6 +272,22 @@ def variants(b, d):
         shapes[name] = {"ms": round(t, 4),
                         "tflops": round(workload.prefill_flops(B, Hq, S, D, causal) / t / 1e9, 1)}
         del q, k, v, o
+    for name, (B, Hq, Hkv, S, D, causal) in {
+            "fp8_noncausal_d64_s4096": (4, 32, 32, 4096, 64, False),
+            "fp8_noncausal_d64_s16384": (4, 32, 32, 16384, 64, False),
+            "fp8_causal_d128_s4096": (4, 32, 8, 4096, 128, True),
+            "fp8_causal_d128_s16384": (4, 32, 8, 16384, 128, True)}.items():
+        q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "fp8", seed=3)
+        q, k, v = q.cuda(), k.cuda(), v.cuda()
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+
+        def f(q=q, k=k, v=v, o=o, causal=causal):
+            b.attn_prefill(q, k, v, causal=causal, o=o)
+
+        t = time_call(f, 5, 1)
+        shapes[name] = {"ms": round(t, 4),
+                        "tflops": round(workload.prefill_flops(B, Hq, S, D, causal) / t / 1e9, 1)}
+        del q, k, v, o
     out["prefill_shapes"] = shapes
     # decode batch sweep: eager vs CUDA-graph replay, L2-resident vs streaming
     sweep = {}

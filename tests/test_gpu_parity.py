@@ -132,6 +132,37 @@ def test_prefill_fused_equals_unfused_closely():
     assert (of.float() - ou.float()).abs().max().item() <= 1e-2
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", [
+    (1, 4, 4, 256, 64, False),     # non-causal D=64 (the persistent-kernel shape, fp8)
+    (1, 4, 1, 640, 128, True),     # causal GQA D=128, several items
+    (2, 2, 2, 333, 64, True),      # ragged, causal
+    (1, 2, 1, 1000, 128, False),   # ragged non-causal
+])
+def test_prefill_fp8_e5m2(B, Hq, Hkv, S, D, causal):
+    """fp8 e5m2 Q/K/V (per-tensor scale 1); the oracle runs on the dequantised values."""
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "fp8", seed=S + 3)
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, want_lse=True)
+    status_ok()
+    ro, rl = oracle.prefill(f64(q), f64(k), f64(v), causal=causal)
+    check(o.cpu(), ro, FP8_MAX, 1e-2, what="O fp8")
+    check(lse.cpu(), rl, 2e-2, None, what="LSE fp8")
+
+
+def test_prefill_fp8_scales():
+    """Dequantisation scales: q,k,v stored as x/scale give the same attention as x itself."""
+    B, H, S, D = 1, 2, 200, 128
+    q, k, v = synthetic.prefill_inputs(B, H, H, S, D, "fp8", seed=5)
+    o1 = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    # halve the stored q (exact in e5m2 for normal values) and pass q_scale = 2
+    qh = (q.float() / 2).to(torch.float8_e5m2)
+    o2 = binding.attn_prefill(qh.cuda(), k.cuda(), v.cuda(), causal=True, q_scale=2.0)
+    vh = (v.float() / 4).to(torch.float8_e5m2)
+    o3 = binding.attn_prefill(q.cuda(), k.cuda(), vh.cuda(), causal=True, v_scale=4.0)
+    status_ok()
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (o1.float() - o3.float()).abs().max().item() <= 1e-2
+
+
 def test_prefill_large_logits_rescale_path():
     """Rows whose maximum grows late force the lazy O rescale; scale 1 makes logits large."""
     B, Hq, Hkv, S, D = 1, 2, 1, 700, 64
