@@ -343,17 +343,34 @@ constexpr int kLatQK = 512;
 constexpr int kLatV = 448;
 constexpr int kLatRope = 64;
 constexpr int kLatStages = 3;
-constexpr int kLatTileBytes = kTileKeys * kLatQK * 2;  // 64 KB
+constexpr int kLatWarps = 8;                              // compute warps (no separate producer:
+constexpr int kLatThreads = kLatWarps * 32;               // warp 0, lane 0 issues the TMA loads)
+constexpr int kLatTileBytes = kTileKeys * kLatQK * 2;     // 64 KB: 64 keys x 512 dims
 constexpr int kLatQPitch = kLatQK * 2 + 16;
 constexpr int kLatPPitch = kTileKeys * 2 + 16;
-constexpr int kLatColsPerWarp = kLatV / kComputeWarps;  // 112 = 14 n-tiles
+constexpr int kLatColsPerWarp = kLatV / kLatWarps;        // 56 = 7 n-tiles of the 448 outputs
+constexpr int kLatKeysPerWarp = kTileKeys / kLatWarps;    // 8 keys scored per warp per tile
+
+__device__ __forceinline__ void lat_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kLatWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
+constexpr int kLatMaxB = 2048;  // sequences per call (the tile prefix sums live in smem)
 
 struct LatSmem {
   static constexpr int kQOff = kLatStages * kLatTileBytes;
   static constexpr int kPOff = kQOff + 16 * kLatQPitch;
-  static constexpr int kRedOff = kPOff + 2 * 16 * kLatPPitch;       // [2][warps][16] row max
-  static constexpr int kLOff = kRedOff + 2 * kComputeWarps * 16 * 4;  // [warps][16] row sums
-  static constexpr int kBarOff = kLOff + kComputeWarps * 16 * 4;
+  static constexpr int kRedOff = kPOff + 2 * 16 * kLatPPitch;        // [2][warps][16] row max
+  static constexpr int kLOff = kRedOff + 2 * kLatWarps * 16 * 4;      // [warps][16] row sums
+  static constexpr int kScanOff = kLOff + kLatWarps * 16 * 4;         // [warps] scan scratch
+  static constexpr int kPrefOff = kScanOff + 64;                      // [B + 1] tile prefix
+  static constexpr int kBarOff = kPrefOff + (kLatMaxB + 1) * 4 + 60;
   static constexpr int kBytes = kBarOff + 2 * kLatStages * 8 + 1024;
 };
 
@@ -362,60 +379,186 @@ struct LatParams {
   const int32_t* lens;
   __nv_bfloat16* o;
   float* lse;
-  float* ws_o;
-  float* ws_lse;
+  float* ws_o;    // [B + grid - 1][H][448] partial outputs of sequences split between CTAs
+  float* ws_lse;  // [B + grid - 1][H]
   const float2* table;  // D = 64 table for the RoPE dims
   unsigned int* status;
-  int B, H, Lmax, nsplit, chunk;
+  int B, H, Lmax;
+  int streamk;  // 1: split all key tiles evenly over the CTAs; 0: whole sequences c, c+grid, ...
   float scale_log2;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Key tiles (64 keys) of sequence b; 0 for an out-of-range length.
+__device__ __forceinline__ int lat_tiles(const int32_t* lens, int b, int Lmax) {
+  const int len = lens[b];
+  return (len >= 1 && len <= Lmax) ? (len + kTileKeys - 1) / kTileKeys : 0;
+}
+
+// Stream-K split: the T key tiles of all sequences, in order, are cut into gridDim.x equal
+// contiguous ranges, one per CTA; tile range of CTA c is [T c / G, T (c+1) / G).
+__device__ __forceinline__ long long lat_range_lo(long long T, int c, int G) {
+  return T * c / G;
+}
+
+// One contiguous run of a sequence's keys inside a CTA's share of the work.
+struct LatSeg {
+  int b, k0, k1;
+  bool whole;    // the CTA covers every key of sequence b: it writes the final output
+  bool invalid;  // sequence b has an out-of-range length (whole-sequence mode only)
+};
+
+struct LatSegIter {
+  long long lo, hi;
+  int b, stride;
+  bool streamk;
+  // whole-sequence mode: sequences first, first + stride, ...
+  __device__ void init_whole(int first, int stride_) {
+    streamk = false;
+    b = first;
+    stride = stride_;
+  }
+  __device__ void init(const int* pref, int B, long long lo_, long long hi_) {
+    streamk = true;
+    lo = lo_;
+    hi = hi_;
+    int a = 0, z = B - 1;  // largest b with pref[b] <= lo
+    while (a < z) {
+      const int mid = (a + z + 1) >> 1;
+      if (pref[mid] <= lo) a = mid; else z = mid - 1;
+    }
+    b = a;
+  }
+  __device__ bool next(const int* pref, int B, const int32_t* lens, LatSeg& sg) {
+    if (!streamk) {
+      if (b >= B) return false;
+      const int len = lens[b];
+      sg.b = b;
+      sg.k0 = 0;
+      sg.invalid = !(len >= 1 && len <= 0x40000000);
+      sg.k1 = sg.invalid ? 0 : len;
+      sg.whole = true;
+      b += stride;
+      return true;
+    }
+    while (b < B && pref[b] < hi) {
+      const long long tb = pref[b], te = pref[b + 1];
+      const int cur = b++;
+      const long long s0 = lo > tb ? lo : tb, s1 = hi < te ? hi : te;
+      if (s0 >= s1) continue;
+      sg.b = cur;
+      sg.k0 = static_cast<int>(s0 - tb) * kTileKeys;
+      sg.k1 = min(static_cast<int>(s1 - tb) * kTileKeys, static_cast<int>(lens[cur]));
+      sg.whole = (s0 == tb && s1 == te);
+      sg.invalid = false;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Issues this CTA's tiles, in order, into the stage ring.  Run by one thread.
+struct LatLoader {
+  LatSegIter seg;
+  LatSeg cur;
+  int t0, stage;
+  uint32_t phase;
+  bool done;
+  __device__ void advance(const int* pref, int B, const int32_t* lens, int Lmax) {
+    while (true) {
+      done = !seg.next(pref, B, lens, cur);
+      if (done) return;
+      if (cur.k1 > Lmax) cur.k1 = 0;  // out-of-range length: nothing to load
+      if (cur.k0 < cur.k1) break;
+    }
+    t0 = cur.k0;
+  }
+  __device__ bool next(const LatParams& p, const int* pref, uint8_t* smem, uint64_t* full,
+                       uint64_t* empty, const CUtensorMap* tm) {
+    if (done) return true;
+    if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) return false;
+    mbar_arrive_expect_tx(&full[stage], kLatTileBytes);
+    uint8_t* ct = smem + stage * kLatTileBytes;
+#pragma unroll
+    for (int bx = 0; bx < kLatQK / 64; ++bx)
+      tma_load_3d(ct + bx * kTileKeys * 128, tm, &full[stage], bx * 64, t0, cur.b);
+    if (++stage == kLatStages) {
+      stage = 0;
+      phase ^= 1;
+    }
+    t0 += kTileKeys;
+    if (t0 >= cur.k1) advance(pref, p.B, p.lens, p.Lmax);
+    return true;
+  }
+};
+
+// Absorbed latent decode, stream-K over all sequences' key tiles.  Per 64-key tile: warp w
+// scores keys 8w..8w+7 against the 16 query rows over all 512 dims (query fragments held in
+// registers, four independent MMA chains), the tile's row maximum and P go through shared
+// memory, then warp w accumulates output columns 56w..56w+55 over all 64 keys.  Thread 0
+// refills each stage as soon as all warps released it.
+__global__ void __launch_bounds__(kLatThreads, 1)
     latent_decode_kernel(const __grid_constant__ CUtensorMap tmC, const LatParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + LatSmem::kBarOff);
   uint64_t* empty = full + kLatStages;
+  int* pref = reinterpret_cast<int*>(smem + LatSmem::kPrefOff);
+  int* scan = reinterpret_cast<int*>(smem + LatSmem::kScanOff);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_items = p.B * p.nsplit;
-  if (threadIdx.x == 0) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
     for (int s = 0; s < kLatStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kComputeWarps);
+      mbar_init(&empty[s], kLatWarps);
     }
     fence_barrier_init();
   }
-  __syncthreads();
-
-  if (warp == kComputeWarps) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tmC);
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const int sp = it % p.nsplit, b = it / p.nsplit;
-        int len = p.lens[b];
-        if (len < 1 || len > p.Lmax) len = 0;
-        const int k0 = sp * p.chunk, k1 = min(k0 + p.chunk, len);
-        for (int t0 = k0; t0 < k1; t0 += kTileKeys) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) return;
-          mbar_arrive_expect_tx(&full[stage], kLatTileBytes);
-          uint8_t* ct = smem + stage * kLatTileBytes;
+  // stream-K mode: prefix sums of the tiles per sequence (each thread owns a contiguous chunk)
+  if (p.streamk) {
+    const int per = (p.B + kLatThreads - 1) / kLatThreads;
+    const int b0 = tid * per, b1 = min(b0 + per, p.B);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) sum += lat_tiles(p.lens, b, p.Lmax);
+    int x = sum;  // inclusive scan over the warp
 #pragma unroll
-          for (int bx = 0; bx < kLatQK / 64; ++bx)
-            tma_load_3d(ct + bx * kTileKeys * 128, &tmC, &full[stage], bx * 64, t0, b);
-          if (++stage == kLatStages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
     }
-    return;
+    if (lane == 31) scan[warp] = x;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += scan[w];
+    int run = base + x - sum;  // exclusive prefix of this thread's chunk
+    for (int b = b0; b < b1; ++b) {
+      pref[b] = run;
+      run += lat_tiles(p.lens, b, p.Lmax);
+    }
+    if (tid == kLatThreads - 1) pref[p.B] = base + x;
+  }
+  __syncthreads();
+  long long lo = 0, hi = 0;
+  if (p.streamk) {
+    const long long T = pref[p.B];
+    lo = lat_range_lo(T, blockIdx.x, gridDim.x);
+    hi = lat_range_lo(T, blockIdx.x + 1, gridDim.x);
   }
 
-  const int tid = threadIdx.x;
+  LatLoader loader;
+  if (tid == 0) {
+    tma_prefetch_desc(&tmC);
+    if (p.streamk)
+      loader.seg.init(pref, p.B, lo, hi);
+    else
+      loader.seg.init_whole(blockIdx.x, gridDim.x);
+    loader.stage = 0;
+    loader.phase = 0;
+    loader.advance(pref, p.B, p.lens, p.Lmax);
+    for (int s = 0; s < kLatStages; ++s) loader.next(p, pref, smem, full, empty, &tmC);
+  }
+  bool alive = true;
+
   const int g = lane >> 2, tq = lane & 3;
   uint8_t* qs = smem + LatSmem::kQOff;
   const uint32_t qs_addr = smem_u32(qs);
@@ -427,29 +570,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   int tcount = 0;
   const int H = p.H;
 
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const int sp = it % p.nsplit, b = it / p.nsplit;
-    int len = p.lens[b];
-    const bool valid = len >= 1 && len <= p.Lmax;
-    if (!valid) {
-      if (tid == 0 && sp == 0) report_status(p.status, ATTN_ERR_DEVICE_ARG);
-      len = 0;
+  LatSegIter segs;
+  if (p.streamk)
+    segs.init(pref, p.B, lo, hi);
+  else
+    segs.init_whole(blockIdx.x, gridDim.x);
+  LatSeg sg;
+  while (segs.next(pref, p.B, p.lens, sg)) {
+    const int b = sg.b, k0 = sg.k0;
+    const int len = p.lens[b];
+    if (sg.invalid || len > p.Lmax) {  // whole-sequence mode: out-of-range length
+      if (tid == 0) report_status(p.status, ATTN_ERR_DEVICE_ARG);
+      for (int i = tid; i < H * kLatV; i += kLatThreads)
+        p.o[static_cast<size_t>(b) * H * kLatV + i] = __float2bfloat16_rn(0.f);
+      if (p.lse && tid < H) p.lse[static_cast<size_t>(b) * H + tid] = -INFINITY;
+      continue;
     }
-    const int k0 = sp * p.chunk, k1 = min(k0 + p.chunk, len);
+    const int k1 = sg.k1;
 
-    compute_bar_sync();
+    lat_bar_sync();
     // query rows: 448 latent dims as given, the 64 RoPE dims rotated at position len
-    for (int idx = tid; idx < 16 * (kLatQK / 2); idx += kComputeWarps * 32) {
+    for (int idx = tid; idx < 16 * (kLatQK / 2); idx += kLatWarps * 32) {
       const int r = idx / (kLatQK / 2), j = idx % (kLatQK / 2);
       __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(qs + r * kLatQPitch);
       const __nv_bfloat16* qr = p.q + (static_cast<size_t>(b) * H + r) * kLatQK;
       if (j < kLatV / 2) {
-        row[2 * j] = (r < H && valid) ? qr[2 * j] : __float2bfloat16_rn(0.f);
-        row[2 * j + 1] = (r < H && valid) ? qr[2 * j + 1] : __float2bfloat16_rn(0.f);
-      } else if (j < kLatV / 2 + kLatRope / 2) {
+        row[2 * j] = r < H ? qr[2 * j] : __float2bfloat16_rn(0.f);
+        row[2 * j + 1] = r < H ? qr[2 * j + 1] : __float2bfloat16_rn(0.f);
+      } else {
         const int i = j - kLatV / 2;  // pair (i, i + 32) of the RoPE part
         float x1 = 0.f, x2 = 0.f;
-        if (r < H && valid) {
+        if (r < H) {
           x1 = __bfloat162float(qr[kLatV + i]);
           x2 = __bfloat162float(qr[kLatV + i + kLatRope / 2]);
           if (p.table) {
@@ -463,10 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         row[kLatV + i + kLatRope / 2] = __float2bfloat16_rn(x2);
       }
     }
-    compute_bar_sync();
-
-    // the 16 x 512 query tile stays in registers for the whole item (A fragments)
-    uint32_t qa[kLatQK / 16][4];
+    lat_bar_sync();
+    uint32_t qa[kLatQK / 16][4];  // the 16 x 512 query tile as A fragments, for the segment
 #pragma unroll
     for (int kk = 0; kk < kLatQK / 16; ++kk)
       ldsm_x4(qs_addr + (lane & 15) * kLatQPitch + (kk * 16 + (lane >> 4) * 8) * 2, qa[kk][0],
@@ -478,60 +627,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 0; n < kLatColsPerWarp / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
     for (int t0 = k0; t0 < k1; t0 += kTileKeys, ++tcount) {
-      if (!mbar_wait(&full[stage], phase, p.status)) return;
+      if (!mbar_wait(&full[stage], phase, p.status)) {
+        alive = false;
+        break;
+      }
       const uint32_t ct = smem_u32(smem + stage * kLatTileBytes);
       const int par = tcount & 1;
-      float s[2][4];
+      float s[4];  // rows g / g+8 x keys 8w + 2tq + {0,1}
       {
-        // two independent accumulator chains over the 32 k-steps (even / odd), summed at the end
-        float se[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        float so[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const int m = lane >> 3;
-        const int key = warp * 16 + (m >> 1) * 8 + (lane & 7);
+        float ch[4][4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ch[c][0] = ch[c][1] = ch[c][2] = ch[c][3] = 0.f;
+        const int key = warp * kLatKeysPerWarp + (lane & 7);
+        const int mi = lane >> 3;  // matrix index: 16-byte dim chunk within a pair of k-steps
 #pragma unroll
         for (int kk = 0; kk < kLatQK / 16; kk += 2) {
-          uint32_t b0, b1, b2, b3, b4, b5, b6, b7;
-          const int c = kk * 2 + (m & 1);
-          const int cn = c + 2;
+          const int c = kk * 2 + mi;  // dims 8c .. 8c+7
+          uint32_t b0, b1, b2, b3;
           ldsm_x4(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
-          ldsm_x4(ct + (cn >> 3) * kTileKeys * 128 + sw128_offset(key, cn & 7), b4, b5, b6, b7);
-          mma_bf16_16816(se[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-          mma_bf16_16816(se[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
-          mma_bf16_16816(so[0], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2], qa[kk + 1][3], b4, b5);
-          mma_bf16_16816(so[1], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2], qa[kk + 1][3], b6, b7);
+          mma_bf16_16816(ch[kk & 3], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+          mma_bf16_16816(ch[(kk + 1) & 3], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2],
+                         qa[kk + 1][3], b2, b3);
         }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) s[nt][e] = se[nt][e] + so[nt][e];
+        for (int e = 0; e < 4; ++e) s[e] = (ch[0][e] + ch[1][e]) + (ch[2][e] + ch[3][e]);
       }
       float rm0 = -INFINITY, rm1 = -INFINITY;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int key = t0 + warp * 16 + nt * 8 + tq * 2 + (j & 1);
-          const float v = key < k1 ? s[nt][j] * p.scale_log2 : -INFINITY;
-          s[nt][j] = v;
-          if (j < 2)
-            rm0 = fmaxf(rm0, v);
-          else
-            rm1 = fmaxf(rm1, v);
-        }
+      for (int e = 0; e < 4; ++e) {
+        const int key = t0 + warp * kLatKeysPerWarp + tq * 2 + (e & 1);
+        const float v = key < k1 ? s[e] * p.scale_log2 : -INFINITY;
+        s[e] = v;
+        if (e < 2)
+          rm0 = fmaxf(rm0, v);
+        else
+          rm1 = fmaxf(rm1, v);
+      }
       rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 1));
       rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 2));
       rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 1));
       rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 2));
       if (tq == 0) {
-        red[(par * kComputeWarps + warp) * 16 + g] = rm0;
-        red[(par * kComputeWarps + warp) * 16 + g + 8] = rm1;
+        red[(par * kLatWarps + warp) * 16 + g] = rm0;
+        red[(par * kLatWarps + warp) * 16 + g + 8] = rm1;
       }
-      compute_bar_sync();
+      lat_bar_sync();
       float tm0 = -INFINITY, tm1 = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kComputeWarps; ++w) {
-        tm0 = fmaxf(tm0, red[(par * kComputeWarps + w) * 16 + g]);
-        tm1 = fmaxf(tm1, red[(par * kComputeWarps + w) * 16 + g + 8]);
+      for (int w = 0; w < kLatWarps; ++w) {
+        tm0 = fmaxf(tm0, red[(par * kLatWarps + w) * 16 + g]);
+        tm1 = fmaxf(tm1, red[(par * kLatWarps + w) * 16 + g + 8]);
       }
       const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
       const float base0 = mn0 == -INFINITY ? 0.f : mn0;
@@ -539,20 +684,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float c0 = fast_exp2(m0 - base0), c1 = fast_exp2(m1 - base1);
       m0 = mn0;
       m1 = mn1;
-      float ps0 = 0.f, ps1 = 0.f;
       uint8_t* pw = smem + LatSmem::kPOff + par * 16 * kLatPPitch;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const float e0 = fast_exp2(s[nt][0] - base0), e1 = fast_exp2(s[nt][1] - base0);
-        const float e2 = fast_exp2(s[nt][2] - base1), e3 = fast_exp2(s[nt][3] - base1);
-        ps0 += e0 + e1;
-        ps1 += e2 + e3;
-        const int col = warp * 16 + nt * 8 + tq * 2;
-        *reinterpret_cast<uint32_t*>(pw + g * kLatPPitch + col * 2) = pack_bf16(e0, e1);
-        *reinterpret_cast<uint32_t*>(pw + (g + 8) * kLatPPitch + col * 2) = pack_bf16(e2, e3);
-      }
-      l0 = l0 * c0 + ps0;
-      l1 = l1 * c1 + ps1;
+      const float e0 = fast_exp2(s[0] - base0), e1 = fast_exp2(s[1] - base0);
+      const float e2 = fast_exp2(s[2] - base1), e3 = fast_exp2(s[3] - base1);
+      const int col = warp * kLatKeysPerWarp + tq * 2;
+      *reinterpret_cast<uint32_t*>(pw + g * kLatPPitch + col * 2) = pack_bf16(e0, e1);
+      *reinterpret_cast<uint32_t*>(pw + (g + 8) * kLatPPitch + col * 2) = pack_bf16(e2, e3);
+      l0 = l0 * c0 + (e0 + e1);
+      l1 = l1 * c1 + (e2 + e3);
 #pragma unroll
       for (int n = 0; n < kLatColsPerWarp / 8; ++n) {
         acc[n][0] *= c0;
@@ -560,34 +699,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[n][2] *= c1;
         acc[n][3] *= c1;
       }
-      compute_bar_sync();
-      // O[:, this warp's 112 columns] += P (16 x 64) * C[:, cols]
+      lat_bar_sync();
+      // O[:, this warp's 56 columns] += P (16 x 64) * C[:, cols]
       const uint32_t ps_addr = ps_addr0 + par * 16 * kLatPPitch;
+      const int cbase = (warp * kLatColsPerWarp) / 8;  // first 8-column chunk of this warp
 #pragma unroll
       for (int kk = 0; kk < kTileKeys / 16; ++kk) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(ps_addr + (lane & 15) * kLatPPitch + (kk * 16 + (lane >> 4) * 8) * 2, a0, a1, a2,
                 a3);
-        const int m = lane >> 3;
-        const int key = kk * 16 + (m & 1) * 8 + (lane & 7);
+        const int mi = lane >> 3;
+        const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
-        for (int n2 = 0; n2 < kLatColsPerWarp / 16; ++n2) {
-          const int c = (warp * kLatColsPerWarp) / 8 + n2 * 2 + (m >> 1);
+        for (int n2 = 0; n2 < 3; ++n2) {  // n-tiles 2*n2, 2*n2+1
+          const int c = cbase + n2 * 2 + (mi >> 1);
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
           mma_bf16_16816(acc[2 * n2], a0, a1, a2, a3, b0, b1);
           mma_bf16_16816(acc[2 * n2 + 1], a0, a1, a2, a3, b2, b3);
         }
+        {  // n-tile 6 (two 8x8 matrices: keys 0-7 and 8-15 of this step)
+          const int c = cbase + 6;
+          uint32_t b0, b1;
+          ldsm_x2_t(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1);
+          mma_bf16_16816(acc[6], a0, a1, a2, a3, b0, b1);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
+      if (tid == 0) alive = loader.next(p, pref, smem, full, empty, &tmC);
+      __syncwarp();
       if (++stage == kLatStages) {
         stage = 0;
         phase ^= 1;
       }
     }
+    if (!__all_sync(0xffffffffu, alive)) return;
 
-    // every warp used the same running max; row sums are split by key quarter
+    // every warp used the same running max; row sums are split by key slice
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -596,16 +745,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       lred[warp * 16 + g] = l0;
       lred[warp * 16 + g + 8] = l1;
     }
-    compute_bar_sync();
+    lat_bar_sync();
     float lt0 = 0.f, lt1 = 0.f;
 #pragma unroll
-    for (int w = 0; w < kComputeWarps; ++w) {
+    for (int w = 0; w < kLatWarps; ++w) {
       lt0 += lred[w * 16 + g];
       lt1 += lred[w * 16 + g + 8];
     }
     const float inv0 = lt0 > 0.f ? 1.f / lt0 : 0.f, inv1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
     const float lse0 = lt0 > 0.f ? m0 + log2f(lt0) : -INFINITY;
     const float lse1 = lt1 > 0.f ? m1 + log2f(lt1) : -INFINITY;
+    const size_t slot = static_cast<size_t>(blockIdx.x) + b;  // unique per (CTA, sequence)
 #pragma unroll
     for (int n = 0; n < kLatColsPerWarp / 8; ++n) {
       const int d = warp * kLatColsPerWarp + n * 8 + tq * 2;
@@ -614,12 +764,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = g + hh * 8;
         if (r >= H) continue;
         const float inv = hh ? inv1 : inv0;
-        const size_t row = static_cast<size_t>(b) * H + r;
         const float o0 = acc[n][hh * 2] * inv, o1 = acc[n][hh * 2 + 1] * inv;
-        if (p.nsplit == 1) {
+        if (sg.whole) {
+          const size_t row = static_cast<size_t>(b) * H + r;
           *reinterpret_cast<uint32_t*>(p.o + row * kLatV + d) = pack_bf16(o0, o1);
         } else {
-          float* wo = p.ws_o + (row * p.nsplit + sp) * kLatV + d;
+          float* wo = p.ws_o + (slot * H + r) * kLatV + d;
           wo[0] = o0;
           wo[1] = o1;
         }
@@ -630,16 +780,123 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hh = 0; hh < 2; ++hh) {
         const int r = g + hh * 8;
         if (r >= H) continue;
-        const size_t row = static_cast<size_t>(b) * H + r;
         const float l2 = hh ? lse1 : lse0;
-        if (p.nsplit == 1) {
-          if (p.lse) p.lse[row] = l2 * kLn2;
+        if (sg.whole) {
+          if (p.lse) p.lse[static_cast<size_t>(b) * H + r] = l2 * kLn2;
         } else {
-          p.ws_lse[row * p.nsplit + sp] = l2;
+          p.ws_lse[slot * H + r] = l2;
         }
       }
     }
   }
+}
+
+// Finish the sequences that were split between CTAs (merge their partials by log-sum-exp) and
+// the sequences with an out-of-range length (O = 0, LSE = -inf, status DEVICE_ARG).  One block
+// per (sequence, head); sequences a single CTA covered were written directly and are skipped.
+constexpr int kFinishThreads = 128;
+constexpr int kMaxParts = 256;  // CTAs one sequence may be spread over (>= the SM count)
+
+__global__ void __launch_bounds__(kFinishThreads)
+    latent_finish_kernel(const int32_t* __restrict__ lens, int B, int H, int Lmax, int G,
+                         const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                         __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                         unsigned int* status) {
+  const int b = blockIdx.x, h = blockIdx.y;
+  __shared__ long long red_t[kFinishThreads / 32], red_b[kFinishThreads / 32];
+  __shared__ int parts[kMaxParts];
+  __shared__ float wgt[kMaxParts];
+  __shared__ int nparts;
+  __shared__ float inv_s, lse_s;
+  long long T = 0, tb = 0;  // all tiles, and tiles of the sequences before b
+  for (int i = threadIdx.x; i < B; i += blockDim.x) {
+    const int t = lat_tiles(lens, i, Lmax);
+    T += t;
+    if (i < b) tb += t;
+  }
+#pragma unroll
+  for (int o2 = 16; o2 > 0; o2 >>= 1) {
+    T += __shfl_xor_sync(0xffffffffu, T, o2);
+    tb += __shfl_xor_sync(0xffffffffu, tb, o2);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red_t[threadIdx.x >> 5] = T;
+    red_b[threadIdx.x >> 5] = tb;
+  }
+  __syncthreads();
+  T = 0;
+  tb = 0;
+#pragma unroll
+  for (int w = 0; w < kFinishThreads / 32; ++w) {
+    T += red_t[w];
+    tb += red_b[w];
+  }
+  const int tiles = lat_tiles(lens, b, Lmax);
+  const size_t orow = static_cast<size_t>(b) * H + h;
+  if (tiles == 0) {
+    if (threadIdx.x == 0 && h == 0) report_status(status, ATTN_ERR_DEVICE_ARG);
+    for (int d = threadIdx.x; d < kLatV; d += blockDim.x) o[orow * kLatV + d] = __float2bfloat16_rn(0.f);
+    if (lse && threadIdx.x == 0) lse[orow] = -INFINITY;
+    return;
+  }
+  // CTAs whose non-empty tile range overlaps this sequence's tiles [tb, tb + tiles)
+  auto cta_of = [&](long long t) {  // the CTA whose (non-empty) range holds tile t
+    long long c = t * G / T;
+    while (c > 0 && lat_range_lo(T, static_cast<int>(c), G) > t) --c;
+    while (c + 1 < G && lat_range_lo(T, static_cast<int>(c) + 1, G) <= t) ++c;
+    return c;
+  };
+  if (cta_of(tb) == cta_of(tb + tiles - 1)) return;  // one CTA covered it: already final
+  if (threadIdx.x == 0) {
+    long long c = cta_of(tb);
+    int n = 0;
+    bool whole = false;
+    for (; c < G && lat_range_lo(T, static_cast<int>(c), G) < tb + tiles; ++c) {
+      const long long a = lat_range_lo(T, static_cast<int>(c), G);
+      const long long z = lat_range_lo(T, static_cast<int>(c) + 1, G);
+      if (a >= z) continue;  // empty range: this CTA wrote nothing
+      if (a <= tb && z >= tb + tiles) whole = true;
+      if (n < kMaxParts) parts[n] = static_cast<int>(c);
+      ++n;
+    }
+    if (n > kMaxParts) report_status(status, ATTN_ERR_UNSUPPORTED);
+    nparts = whole ? 0 : min(n, kMaxParts);
+  }
+  __syncthreads();
+  const int np = nparts;
+  if (np == 0) return;  // written directly by the one CTA that covered it
+  if (threadIdx.x < 32) {  // one warp: partial log-sum-exps -> weights, in parallel
+    const int lane = threadIdx.x;
+    float M = -INFINITY;
+    for (int i = lane; i < np; i += 32) {
+      const float l = ws_lse[(static_cast<size_t>(parts[i]) + b) * H + h];
+      wgt[i] = l;
+      M = fmaxf(M, l);
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    float wsum = 0.f;
+    for (int i = lane; i < np; i += 32) {
+      const float l = wgt[i];
+      const float w = l == -INFINITY ? 0.f : exp2f(l - M);
+      wgt[i] = w;
+      wsum += w;
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o2);
+    if (lane == 0) {
+      inv_s = wsum > 0.f ? 1.f / wsum : 0.f;
+      lse_s = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
+    }
+  }
+  __syncthreads();
+  for (int d = threadIdx.x; d < kLatV; d += blockDim.x) {
+    float acc = 0.f;
+    for (int i = 0; i < np; ++i)
+      acc += wgt[i] * ws_o[((static_cast<size_t>(parts[i]) + b) * H + h) * kLatV + d];
+    o[orow * kLatV + d] = __float2bfloat16_rn(acc * inv_s);
+  }
+  if (lse && threadIdx.x == 0) lse[orow] = lse_s;
 }
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
@@ -728,7 +985,18 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int Lmax) {
 }
 
 DecodePlan plan_latent(int B, int H, int Lmax) {
-  return plan_common(B, Lmax, sm_count(), kLatQK * 2, H, kLatV);
+  (void)Lmax;
+  DecodePlan pl;
+  // Few sequences: spread their key tiles over every SM (partials merged afterwards).  Many
+  // sequences: one CTA per sequence (equal lengths then need no merge); measured faster there.
+  const int sms = sm_count();
+  const bool streamk = 2 * B < sms;
+  pl.grid = streamk ? sms : std::min(B, sms);
+  pl.nsplit = streamk ? 1 : 0;  // 1 = stream-K mode (nsplit doubles as the mode flag here)
+  pl.chunk = 0;
+  // stream-K: partial outputs of sequences split between CTAs, slot (CTA + sequence)
+  pl.ws_bytes = streamk ? static_cast<size_t>(B + pl.grid - 1) * H * (kLatV + 1) * 4 : 0;
+  return pl;
 }
 
 attn_status_t launch_decode(const void* q, const void* k, const void* v, const int32_t* lens,
@@ -745,6 +1013,7 @@ attn_status_t launch_decode(const void* q, const void* k, const void* v, const i
 attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, int Lmax, void* o,
                             float* lse, int B, int H, float scale, const float2* table, void* ws,
                             const DecodePlan& plan, cudaStream_t st) {
+  if (B > kLatMaxB) return ATTN_ERR_UNSUPPORTED;
   CUtensorMap tc;
   if (!make_tmap_3d(&tc, c, 2, kLatQK, Lmax, B, 64, kTileKeys, 128)) return ATTN_ERR_CUDA;
   LatParams p;
@@ -752,29 +1021,24 @@ attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, i
   p.lens = lens;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
-  const size_t rows = static_cast<size_t>(B) * H;
-  p.ws_o = plan.nsplit > 1 ? static_cast<float*>(ws) : nullptr;
-  p.ws_lse = plan.nsplit > 1 ? static_cast<float*>(ws) + rows * plan.nsplit * kLatV : nullptr;
+  p.ws_o = ws ? static_cast<float*>(ws) : nullptr;
+  p.ws_lse = ws ? static_cast<float*>(ws) + static_cast<size_t>(B + plan.grid - 1) * H * kLatV
+                : nullptr;
   p.table = table;
   p.status = device_status_ptr();
   p.B = B;
   p.H = H;
   p.Lmax = Lmax;
-  p.nsplit = plan.nsplit;
-  p.chunk = plan.chunk;
+  p.streamk = plan.nsplit;  // the plan marks stream-K mode with nsplit = 1
   p.scale_log2 = scale * 1.4426950408889634f;
   if (!set_smem_attr(reinterpret_cast<const void*>(latent_decode_kernel), LatSmem::kBytes))
     return ATTN_ERR_CUDA;
-  const int items = B * plan.nsplit;
-  const int grid = std::min(items, plan.grid);
-  latent_decode_kernel<<<grid, kThreads, LatSmem::kBytes, st>>>(tc, p);
+  latent_decode_kernel<<<plan.grid, kLatThreads, LatSmem::kBytes, st>>>(tc, p);
   if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
-  if (plan.nsplit > 1) {
-    combine_kernel<<<static_cast<unsigned>(rows), 128, 0, st>>>(p.ws_o, p.ws_lse, plan.nsplit,
-                                                              kLatV, p.o, lse);
-    return launch_status();
-  }
-  return ATTN_OK;
+  if (!p.streamk) return ATTN_OK;
+  latent_finish_kernel<<<dim3(B, H), kFinishThreads, 0, st>>>(lens, B, H, Lmax, plan.grid, p.ws_o,
+                                                              p.ws_lse, p.o, lse, p.status);
+  return launch_status();
 }
 
 }  // namespace attn

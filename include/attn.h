@@ -177,7 +177,9 @@ ATTN_API size_t attn_decode_latent_workspace_size(int B, int H, int Lmax);
  *              Scores use all 512 dims; values are the first 448 dims.
  *   cache_len  DEVICE int32 [B], as in attn_decode.
  *   o          [B,H,448] bfloat16.  lse: NULL or [B,H] float32.
- *   H <= 16 (all heads of a sequence share one MMA tile).  softmax_scale <= 0 means 1/sqrt(512).
+ *   H <= 16 (all heads of a sequence share one MMA tile); B <= 2048.  softmax_scale <= 0 means
+ *   1/sqrt(512).  The key tiles of all sequences are split evenly over the SMs, so a sequence
+ *   may be computed in pieces that a second kernel merges; the workspace holds those pieces.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */
 ATTN_API attn_status_t attn_decode_latent(const void* q, const void* c_cache, const int32_t* cache_len,

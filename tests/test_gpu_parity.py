@@ -214,8 +214,9 @@ def test_decode_bad_cache_len_sets_status():
 
 @pytest.mark.parametrize("B,H,Lmax,lens", [
     (4, 16, 2048, [2048, 1, 1000, 64]),
-    (1, 16, 2048, [2048]),
+    (1, 16, 2048, [2048]),                 # one sequence spread over many SMs
     (2, 5, 200, [200, 37]),
+    (160, 16, 256, [256 - (i % 7) * 33 for i in range(160)]),  # more sequences than SMs
 ])
 def test_latent_decode(B, H, Lmax, lens):
     q, c, cl = synthetic.latent_inputs(B, H, Lmax, lens, seed=B)
@@ -224,3 +225,15 @@ def test_latent_decode(B, H, Lmax, lens):
     ro, rl = oracle.latent_decode(f64(q), f64(c), cl.numpy(), rope=True, theta=10000.0)
     check(o.cpu(), ro, what="O")
     check(lse.cpu(), rl, LSE_TOL, None, what="LSE")
+
+
+def test_latent_bad_cache_len_sets_status():
+    q, c, cl = synthetic.latent_inputs(3, 16, 128, [128, 128, 50], seed=6)
+    cl[1] = 0  # out of range
+    o = binding.attn_decode_latent(q.cuda(), c.cuda(), cl.cuda())
+    assert binding.attn_get_device_status() == 7
+    assert binding.attn_get_device_status() == 0
+    keep = [0, 2]
+    ro, _ = oracle.latent_decode(f64(q[keep]), f64(c[keep]), cl[keep].numpy())
+    check(o[keep].cpu(), ro, what="valid rows")
+    assert torch.all(o[1].cpu() == 0)
