@@ -121,6 +121,26 @@ class ClockSampler:
 # our CUDA path
 # ----------------------------------------------------------------------------------------------
 
+def prefill_traffic():
+    """DRAM bytes per launch of the bench's prefill, from the committed ncu summary, or None
+    when the kernel source changed since those counters were taken."""
+    import hashlib
+    import re
+
+    prof = os.path.join(ROOT, "profiles", "prefill_fused_rope_s16384_dram.md")
+    src = os.path.join(ROOT, "attention_attn_prefill_02_gb300", "csrc", "prefill.cu")
+    try:
+        text = open(prof).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m = re.search(r"prefill.cu sha256 ([0-9a-f]{16})", text)
+    n = re.search(r"dram_bytes_per_launch_s16384=(\d+)", text)
+    if not m or not n or m.group(1) != sha or PREFILL["S"] != 16384:
+        return None
+    return int(n.group(1))
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -410,7 +430,7 @@ def ours(args):
         "prefill": {"ms": round(per["prefill"], 4), "tflops": round(achieved, 2)},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": tf_sust,
                      "unit": "TFLOP/s", "frac": round(achieved / tf_sust, 4),
-                     "traffic": None,
+                     "traffic": prefill_traffic(),
                      "peak_kind": f"bf16 sustained ({peak_kind}); kernel timed inside the step"},
         "gpu_launches": args.steps * (1 + 1 + 1),
         "clocks": clocks.summary(),
