@@ -41,33 +41,58 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 // Tile geometry for head dim D and element size ESZ (2 = bf16, 1 = fp8 e5m2).  Rows of 128 (or,
 // for 64-byte rows, 64) bytes are TMA-swizzled; the MMA advances 32 bytes per K step (16 bf16
-// or 32 fp8 elements) and 16 / 32 keys per PV step.
-template <int D, int ESZ>
+// or 32 fp8 elements) and 16 / 32 keys per PV step.  STAGED (fp8 with fused RoPE): Q and K land
+// as fp8 in staging tiles and are rotated into bf16 tiles, so QK^T runs in bf16 while V stays fp8.
+template <int SWZ_BYTES_ROW>
+struct Swz {
+  static constexpr int kSwz = SWZ_BYTES_ROW >= 128 ? 128 : SWZ_BYTES_ROW;  // 128 or 64 bytes
+  static constexpr uint32_t kCode = kSwz == 128 ? 2u : 4u;                  // descriptor mode
+  static constexpr int kBoxBytes = 128 * kSwz;                               // one 128-row box
+  static constexpr int kSBO = 8 * kSwz;                                      // 8-row group
+};
+
+template <int D, int ESZ, bool STAGED>
 struct Cfg {
-  static constexpr int kRowBytes = D * ESZ;
-  static constexpr int kSwz = kRowBytes >= 128 ? 128 : kRowBytes;  // swizzle span (128 or 64 B)
-  static constexpr int kBoxElems = kSwz / ESZ;                    // elements per box row
-  static constexpr int kBoxes = kRowBytes / kSwz;                 // boxes per 128-row tile
-  static constexpr int kBoxBytes = 128 * kSwz;
-  static constexpr uint32_t kSwzCode = kSwz == 128 ? 2u : 4u;     // descriptor swizzle mode
-  static constexpr int kSBO = 8 * kSwz;                           // bytes per 8-row group
-  static constexpr int kKSteps = kRowBytes / 32;                  // QK^T steps over D
-  static constexpr int kPVKeys = 32 / ESZ;                        // keys per PV step
-  static constexpr int kPVSteps = BN / kPVKeys;
+  // Q / K tiles read by the QK^T MMA
+  static constexpr int kQKE = STAGED ? 2 : ESZ;
+  static constexpr int kRowBytes = D * kQKE;
+  static constexpr int kSwz = Swz<kRowBytes>::kSwz;
+  static constexpr int kBoxElems = kSwz / kQKE;
+  static constexpr int kBoxes = kRowBytes / kSwz;
+  static constexpr int kBoxBytes = Swz<kRowBytes>::kBoxBytes;
+  static constexpr uint32_t kSwzCode = Swz<kRowBytes>::kCode;
+  static constexpr int kSBO = Swz<kRowBytes>::kSBO;
+  static constexpr int kKSteps = kRowBytes / 32;
   static constexpr int kQTileBytes = BM * kRowBytes;
-  static constexpr int kKVTileBytes = BN * kRowBytes;
+  static constexpr int kKVTileBytes = BN * kRowBytes;  // K tile as the MMA reads it
+  // V tiles (storage type)
+  static constexpr int kVRowBytes = D * ESZ;
+  static constexpr int kVSwz = Swz<kVRowBytes>::kSwz;
+  static constexpr int kVBoxElems = kVSwz / ESZ;
+  static constexpr int kVBoxes = kVRowBytes / kVSwz;
+  static constexpr int kVBoxBytes = Swz<kVRowBytes>::kBoxBytes;
+  static constexpr uint32_t kVSwzCode = Swz<kVRowBytes>::kCode;
+  static constexpr int kVSBO = Swz<kVRowBytes>::kSBO;
+  static constexpr int kVTileBytes = BN * kVRowBytes;
+  static constexpr int kPVKeys = 32 / ESZ;  // keys per PV step
+  static constexpr int kPVSteps = BN / kPVKeys;
+  // staging tiles (STAGED only): fp8 Q / K as loaded, one 128-byte box per row for D = 128
+  static constexpr int kStTileBytes = STAGED ? BM * D : 0;
   // Separate K and V rings; K is fetched one KV step ahead of V, so a K tile has about two KV
   // steps between landing and its first MMA (room for the TMA latency plus the fused RoPE).
-  static constexpr int kKStages = ESZ == 2 ? (D == 128 ? 3 : 4) : (D == 128 ? 4 : 6);
-  static constexpr int kVStages = ESZ == 2 ? (D == 128 ? 2 : 3) : (D == 128 ? 4 : 6);
+  static constexpr int kKStages = STAGED ? 2 : ESZ == 2 ? (D == 128 ? 3 : 4) : (D == 128 ? 4 : 6);
+  static constexpr int kVStages = STAGED ? 2 : ESZ == 2 ? (D == 128 ? 2 : 3) : (D == 128 ? 4 : 6);
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = 2 * kQTileBytes;
-  static constexpr int kVOff = kKVOff + kKStages * kKVTileBytes;
-  static constexpr int kBarOff = kVOff + kVStages * kKVTileBytes;
+  static constexpr int kQStOff = kQOff + 2 * kQTileBytes;
+  static constexpr int kKVOff = kQStOff + 2 * kStTileBytes;
+  static constexpr int kKStOff = kKVOff + kKStages * kKVTileBytes;
+  static constexpr int kVOff = kKStOff + kKStages * kStTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kVTileBytes;
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static_assert(kKStages <= 8 && kVStages <= 8, "barrier arrays hold 8 stages");
+  static_assert(!STAGED || D == 128, "fp8 with fused RoPE is built for D = 128");
 };
 
 struct Params {
@@ -87,6 +112,7 @@ struct Bars {
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
   uint64_t q_ready[2], k_ready[8];  // fused RoPE: tile rotated in shared memory
+  uint64_t k_st_full[8], k_st_free[8];  // fp8 + RoPE: K staging tiles (loaded / consumed)
   uint32_t tmem_slot;
 };
 
@@ -141,13 +167,42 @@ __device__ __forceinline__ void rope_rotate_row(uint8_t* tile, int row,
   }
 }
 
+// fp8 (e5m2) Q row from a 128-byte-swizzled staging tile (D = 128: one box) -> rotated bf16 row
+// in a two-box bf16 tile.  Pairs (i, i + 64) rotate by the row position's cos / sin.
+__device__ __forceinline__ void rope_rotate_row_fp8_to_bf16(const uint8_t* st, uint8_t* bf, int row,
+                                                           const float2* __restrict__ cs_row) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // 8 pairs per step: fp8 elements 8c..8c+7 and 64+8c..64+8c+7
+    const uint2 a8 =
+        *reinterpret_cast<const uint2*>(st + sw128_offset(row, c >> 1) + (c & 1) * 8);
+    const uint2 b8 =
+        *reinterpret_cast<const uint2*>(st + sw128_offset(row, 4 + (c >> 1)) + (c & 1) * 8);
+    const __nv_fp8x2_storage_t* a2 = reinterpret_cast<const __nv_fp8x2_storage_t*>(&a8);
+    const __nv_fp8x2_storage_t* b2 = reinterpret_cast<const __nv_fp8x2_storage_t*>(&b8);
+    const float4* t4 = reinterpret_cast<const float4*>(cs_row + c * 8);
+    uint4 oa, ob;
+    uint32_t* aw = reinterpret_cast<uint32_t*>(&oa);
+    uint32_t* bw = reinterpret_cast<uint32_t*>(&ob);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 t = __ldg(t4 + q);
+      const float2 x = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(a2[q], __NV_E5M2)));
+      const float2 y = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(b2[q], __NV_E5M2)));
+      aw[q] = pack_bf16(x.x * t.x - y.x * t.y, x.y * t.z - y.y * t.w);
+      bw[q] = pack_bf16(y.x * t.x + x.x * t.y, y.y * t.z + x.y * t.w);
+    }
+    *reinterpret_cast<uint4*>(bf + sw128_offset(row, c)) = oa;
+    *reinterpret_cast<uint4*>(bf + 128 * 128 + sw128_offset(row, c)) = ob;
+  }
+}
+
 template <int D, bool ROPE, int ESZ>
 __global__ void __launch_bounds__(threads_for(ROPE), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using C = Cfg<D, ESZ>;
   constexpr bool FP8 = ESZ == 1;
-  static_assert(!(FP8 && ROPE), "fp8 inputs take RoPE through a bf16 staging path (not fused here)");
+  constexpr bool STAGED = FP8 && ROPE;  // fp8 inputs, RoPE fused: rotate into bf16 Q/K tiles
+  using C = Cfg<D, ESZ, STAGED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -167,6 +222,8 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->k_ready[s], kRopeThreads);
+      mbar_init(&bars->k_st_full[s], 1);
+      mbar_init(&bars->k_st_free[s], kRopeThreads);
     }
     for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(&bars->v_full[s], 1);
@@ -209,15 +266,30 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           ok = mbar_wait(&bars->q_empty[t], ph_qe[t] ^ 1, p.status);
           ph_qe[t] ^= 1;
           if (!ok) continue;
-          mbar_arrive_expect_tx(&bars->q_full[t], C::kQTileBytes);
-          uint8_t* dst = smem + C::kQOff + t * C::kQTileBytes;
-#pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_3d(dst + bx * C::kBoxBytes, &tmQ, &bars->q_full[t], bx * C::kBoxElems,
+          if constexpr (STAGED) {  // fp8 Q into its staging tile (one 128-byte box per row)
+            mbar_arrive_expect_tx(&bars->q_full[t], C::kStTileBytes);
+            tma_load_3d(smem + C::kQStOff + t * C::kStTileBytes, &tmQ, &bars->q_full[t], 0,
                         m * kRowsPerItem + t * BM, b * p.Hq + hq);
+          } else {
+            mbar_arrive_expect_tx(&bars->q_full[t], C::kQTileBytes);
+            uint8_t* dst = smem + C::kQOff + t * C::kQTileBytes;
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_3d(dst + bx * C::kBoxBytes, &tmQ, &bars->q_full[t], bx * C::kBoxElems,
+                          m * kRowsPerItem + t * BM, b * p.Hq + hq);
+          }
         }
         // issue order K_0, K_1, V_0, K_2, V_1, ...: K runs one tile ahead of V
         auto load_k = [&](int j) {
+          if constexpr (STAGED) {  // fp8 K into a staging tile; the RoPE warps convert it
+            ok = mbar_wait(&bars->k_st_free[ks], kph ^ 1, p.status);
+            if (!ok) return;
+            mbar_arrive_expect_tx(&bars->k_st_full[ks], C::kStTileBytes);
+            tma_load_3d(smem + C::kKStOff + ks * C::kStTileBytes, &tmK, &bars->k_st_full[ks], 0,
+                        j * BN, b * p.Hkv + hkv);
+            if (++ks == C::kKStages) { ks = 0; kph ^= 1; }
+            return;
+          }
           ok = mbar_wait(&bars->k_empty[ks], kph ^ 1, p.status);
           if (!ok) return;
           mbar_arrive_expect_tx(&bars->k_full[ks], C::kKVTileBytes);
@@ -231,11 +303,11 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         auto load_v = [&](int j) {
           ok = mbar_wait(&bars->v_empty[vs], vph ^ 1, p.status);
           if (!ok) return;
-          mbar_arrive_expect_tx(&bars->v_full[vs], C::kKVTileBytes);
-          uint8_t* dst = smem + C::kVOff + vs * C::kKVTileBytes;
+          mbar_arrive_expect_tx(&bars->v_full[vs], C::kVTileBytes);
+          uint8_t* dst = smem + C::kVOff + vs * C::kVTileBytes;
 #pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_3d(dst + bx * C::kBoxBytes, &tmV, &bars->v_full[vs], bx * C::kBoxElems,
+          for (int bx = 0; bx < C::kVBoxes; ++bx)
+            tma_load_3d(dst + bx * C::kVBoxBytes, &tmV, &bars->v_full[vs], bx * C::kVBoxElems,
                         j * BN, b * p.Hkv + hkv);
           if (++vs == C::kVStages) { vs = 0; vph ^= 1; }
         };
@@ -268,20 +340,20 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           const uint32_t off = (kk / kPerBox) * C::kBoxBytes + (kk % kPerBox) * 32;
           const uint64_t ad = smem_desc(qa + off, 16, C::kSBO, C::kSwzCode);
           const uint64_t bd = smem_desc(ka + off, 16, C::kSBO, C::kSwzCode);
-          if constexpr (FP8)
+          if constexpr (C::kQKE == 1)
             umma_ss_f8(tmem + (t ? C::kColS1 : C::kColS0), ad, bd, idesc_s, kk > 0);
           else
             umma_ss(tmem + (t ? C::kColS1 : C::kColS0), ad, bd, idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t va = v_base + slot * C::kKVTileBytes;
+        const uint32_t va = v_base + slot * C::kVTileBytes;
         const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0);
 #pragma unroll
         for (int kk = 0; kk < C::kPVSteps; ++kk) {
           // P: 8 TMEM columns per step (16 bf16 or 32 fp8 keys); V rows of kSwz bytes per key
           const uint64_t bd =
-              smem_desc(va + kk * C::kPVKeys * C::kSwz, C::kBoxBytes, C::kSBO, C::kSwzCode);
+              smem_desc(va + kk * C::kPVKeys * C::kVSwz, C::kVBoxBytes, C::kVSBO, C::kVSwzCode);
           if constexpr (FP8)
             umma_ts_f8(tmem + (t ? C::kColO1 : C::kColO0), pcol + kk * 8, bd, idesc_pv,
                        (acc || kk > 0) ? 1u : 0u);
@@ -406,8 +478,14 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         ws[q] = anc_s[q];
       }
       for (int j = 0; j < nkv && ok; ++j) {
-        if (!(ok = mbar_wait(&bars->k_full[stage], ph, p.status))) break;
+        if constexpr (STAGED) {
+          if (!(ok = mbar_wait(&bars->k_st_full[stage], ph, p.status))) break;
+          if (!(ok = mbar_wait(&bars->k_empty[stage], ph ^ 1, p.status))) break;
+        } else {
+          if (!(ok = mbar_wait(&bars->k_full[stage], ph, p.status))) break;
+        }
         uint8_t* tile = smem + C::kKVOff + stage * C::kKVTileBytes;
+        const uint8_t* st = smem + C::kKStOff + stage * C::kStTileBytes;  // fp8 staging (STAGED)
         const int rows_valid = p.S - j * BN;  // rows >= this are past the sequence (zeros)
 #pragma unroll 2
         for (int k = 0; k < kRowsPer; ++k) {
@@ -415,8 +493,28 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           const uint32_t rsw = static_cast<uint32_t>((row & 7) << 4);
           uint4* p1 = reinterpret_cast<uint4*>(tile + row * 128 + (off1 ^ rsw));
           uint4* p2 = reinterpret_cast<uint4*>(tile + row * 128 + (off2 ^ rsw));
-          if (row < rows_valid) {
-            uint4 a = *p1, bq = *p2;
+          if (STAGED || row < rows_valid) {  // staged tiles are always written (zeros past S)
+            uint4 a, bq;
+            if constexpr (STAGED) {  // fp8 elements 8c..8c+7 and 64+8c.. -> 4 + 4 packed pairs
+              const uint2 a8 =
+                  *reinterpret_cast<const uint2*>(st + sw128_offset(row, c >> 1) + (c & 1) * 8);
+              const uint2 b8 = *reinterpret_cast<const uint2*>(
+                  st + sw128_offset(row, 4 + (c >> 1)) + (c & 1) * 8);
+              const __nv_fp8x2_storage_t* a2 = reinterpret_cast<const __nv_fp8x2_storage_t*>(&a8);
+              const __nv_fp8x2_storage_t* b2 = reinterpret_cast<const __nv_fp8x2_storage_t*>(&b8);
+              uint32_t* aw0 = reinterpret_cast<uint32_t*>(&a);
+              uint32_t* bw0 = reinterpret_cast<uint32_t*>(&bq);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {  // widen to bf16 pairs (exact: e5m2 fits in bf16)
+                const float2 xa = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(a2[q], __NV_E5M2)));
+                const float2 xb = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(b2[q], __NV_E5M2)));
+                aw0[q] = pack_bf16(xa.x, xa.y);
+                bw0[q] = pack_bf16(xb.x, xb.y);
+              }
+            } else {
+              a = *p1;
+              bq = *p2;
+            }
             uint32_t* aw = reinterpret_cast<uint32_t*>(&a);
             uint32_t* bw = reinterpret_cast<uint32_t*>(&bq);
 #pragma unroll
@@ -442,6 +540,7 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars->k_ready[stage]);
+        if constexpr (STAGED) mbar_arrive(&bars->k_st_free[stage]);
         if (++stage == C::kKStages) {
           stage = 0;
           ph ^= 1;
@@ -469,12 +568,19 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
       const int n = kv_tiles_for(p, r0);
       if (n == 0) continue;
       const int row = r0 + lrow;
-      if constexpr (ROPE && !FP8) {
+      if constexpr (ROPE) {
         if (!(ok = mbar_wait(&bars->q_full[t], ph_q, p.status))) break;
         ph_q ^= 1;
-        if (row < p.S)
-          rope_rotate_row<D>(smem + C::kQOff + t * C::kQTileBytes, lrow,
-                             p.table + static_cast<size_t>(p.pos0 + row) * (D / 2));
+        if constexpr (STAGED) {
+          // rows past S are zero in the staging tile; their table row may not exist: use row 0
+          rope_rotate_row_fp8_to_bf16(smem + C::kQStOff + t * C::kStTileBytes,
+                                      smem + C::kQOff + t * C::kQTileBytes, lrow,
+                                      p.table + static_cast<size_t>(row < p.S ? p.pos0 + row : 0) * (D / 2));
+        } else {
+          if (row < p.S)
+            rope_rotate_row<D>(smem + C::kQOff + t * C::kQTileBytes, lrow,
+                               p.table + static_cast<size_t>(p.pos0 + row) * (D / 2));
+        }
         fence_proxy_async_smem();
         mbar_arrive(&bars->q_ready[t]);
       }
@@ -611,11 +717,16 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
                            float q_scale, float k_scale, float v_scale, int B, int Hq, int Hkv,
                            int S, int causal, float scale, const float2* table, int pos0,
                            cudaStream_t st) {
-  using C = Cfg<D, ESZ>;
+  constexpr bool STAGED = ESZ == 1 && ROPE;
+  using C = Cfg<D, ESZ, STAGED>;
+  // Q / K boxes: as the MMA reads them, or (STAGED) the fp8 staging tiles; V in its own geometry
+  constexpr int kQKBoxElems = STAGED ? D : C::kBoxElems;
+  constexpr int kQKSwz = STAGED ? 128 : C::kSwz;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_3d(&tq, q, ESZ, D, S, static_cast<uint64_t>(B) * Hq, C::kBoxElems, BM, C::kSwz) ||
-      !make_tmap_3d(&tk, k, ESZ, D, S, static_cast<uint64_t>(B) * Hkv, C::kBoxElems, BN, C::kSwz) ||
-      !make_tmap_3d(&tv, v, ESZ, D, S, static_cast<uint64_t>(B) * Hkv, C::kBoxElems, BN, C::kSwz))
+  if (!make_tmap_3d(&tq, q, ESZ, D, S, static_cast<uint64_t>(B) * Hq, kQKBoxElems, BM, kQKSwz) ||
+      !make_tmap_3d(&tk, k, ESZ, D, S, static_cast<uint64_t>(B) * Hkv, kQKBoxElems, BN, kQKSwz) ||
+      !make_tmap_3d(&tv, v, ESZ, D, S, static_cast<uint64_t>(B) * Hkv, C::kVBoxElems, BN,
+                    C::kVSwz))
     return ATTN_ERR_CUDA;
   Params p;
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -658,6 +769,7 @@ attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* 
   ATTN_PREFILL_CASE(64, true, 2)
   ATTN_PREFILL_CASE(128, false, 1)
   ATTN_PREFILL_CASE(64, false, 1)
+  ATTN_PREFILL_CASE(128, true, 1)
 #undef ATTN_PREFILL_CASE
   return ATTN_ERR_UNSUPPORTED;
 }

@@ -296,13 +296,15 @@ def variants(b, d):
             "fp8_noncausal_d64_s4096": (4, 32, 32, 4096, 64, False),
             "fp8_noncausal_d64_s16384": (4, 32, 32, 16384, 64, False),
             "fp8_causal_d128_s4096": (4, 32, 8, 4096, 128, True),
-            "fp8_causal_d128_s16384": (4, 32, 8, 16384, 128, True)}.items():
+            "fp8_causal_d128_s16384": (4, 32, 8, 16384, 128, True),
+            "fp8_causal_d128_s16384_fused_rope": (4, 32, 8, 16384, 128, True)}.items():
         q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "fp8", seed=3)
         q, k, v = q.cuda(), k.cuda(), v.cuda()
         o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+        rope = name.endswith("fused_rope")
 
-        def f(q=q, k=k, v=v, o=o, causal=causal):
-            b.attn_prefill(q, k, v, causal=causal, o=o)
+        def f(q=q, k=k, v=v, o=o, causal=causal, rope=rope):
+            b.attn_prefill(q, k, v, causal=causal, o=o, rope=rope, rope_theta=THETA)
 
         t = time_call(f, 5, 1)
         shapes[name] = {"ms": round(t, 4),

@@ -96,7 +96,10 @@ ATTN_API attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, in
  *   causal   0 or 1; causal hides key j from query i when j > i (S_q == S_kv).
  *   rope     0 = Q and K used as given; 1 = Q and K rotated inside the kernel at positions
  *            pos0 + s as they are loaded (fused RoPE).
- *   D in {64, 128}; Hq % Hkv == 0; S >= 1.  fp8 e5m2 is supported for rope = 0.
+ *   D in {64, 128}; Hq % Hkv == 0; S >= 1.  fp8 e5m2 inputs: P is rounded to e4m3 for the PV
+ *   product; with rope = 1 (D = 128 only) Q and K are rotated into bf16 tiles inside the
+ *   kernel (QK^T then runs in bf16, PV stays fp8), because rotated values re-rounded to fp8
+ *   would exceed the fp8 error budget.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
  */
 ATTN_API attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -148,6 +148,23 @@ def test_prefill_fp8_e5m2(B, Hq, Hkv, S, D, causal):
     check(lse.cpu(), rl, 2e-2, None, what="LSE fp8")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,pos0", [
+    (1, 4, 1, 640, 128, True, 0),      # causal GQA fp8, RoPE fused (config shape, small S)
+    (2, 2, 2, 300, 128, True, 7),      # ragged, offset positions
+    (1, 2, 1, 520, 128, False, 0),     # non-causal
+])
+def test_prefill_fp8_fused_rope(B, Hq, Hkv, S, D, causal, pos0):
+    """fp8 e5m2 Q/K/V with RoPE fused: rotated Q/K are kept in bf16 inside the kernel."""
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "fp8", seed=S + 11)
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, rope=True,
+                                  rope_theta=10000.0, pos0=pos0, want_lse=True)
+    status_ok()
+    ro, rl = oracle.prefill(f64(q), f64(k), f64(v), causal=causal, rope=True, theta=10000.0,
+                            pos0=pos0)
+    check(o.cpu(), ro, FP8_MAX, 1e-2, what="O fp8 rope")
+    check(lse.cpu(), rl, 2e-2, None, what="LSE fp8 rope")
+
+
 def test_prefill_fp8_scales():
     """Dequantisation scales: q,k,v stored as x/scale give the same attention as x itself."""
     B, H, S, D = 1, 2, 200, 128
