@@ -33,9 +33,9 @@ constexpr int BN = 128;  // keys per KV tile
 constexpr int kRowsPerItem = 2 * BM;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kRopeWarp0 = 10;  // fused RoPE: warps 10-11 rotate each K tile in shared memory
-constexpr int kRopeThreads = 64;
-__host__ __device__ constexpr int threads_for(bool rope) { return rope ? 384 : 320; }
+constexpr int kRopeWarp0 = 10;  // fused RoPE: warps 10-13 rotate each K tile in shared memory
+constexpr int kRopeThreads = 128;
+__host__ __device__ constexpr int threads_for(bool rope) { return rope ? 448 : 320; }
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -203,6 +203,10 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
   constexpr bool FP8 = ESZ == 1;
   constexpr bool STAGED = FP8 && ROPE;  // fp8 inputs, RoPE fused: rotate into bf16 Q/K tiles
   using C = Cfg<D, ESZ, STAGED>;
+  // First TMEM column of P inside S_t.  The RoPE variants (four more warps, so fewer registers
+  // per thread) run the softmax in two passes and write P over the upper half of S; the others
+  // hold the whole S row in registers and write P over its first columns.
+  constexpr uint32_t kPCol = ROPE ? (FP8 ? 96u : 64u) : 0u;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -348,7 +352,7 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
         const uint32_t va = v_base + slot * C::kVTileBytes;
-        const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0);
+        const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0) + kPCol;
 #pragma unroll
         for (int kk = 0; kk < C::kPVSteps; ++kk) {
           // P: 8 TMEM columns per step (16 bf16 or 32 fp8 keys); V rows of kSwz bytes per key
@@ -589,11 +593,97 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         if (!(ok = mbar_wait(&bars->s_full[t], ph_s, p.status))) break;
         ph_s ^= 1;
         tc_fence_after();
+        const bool need_mask = (p.causal && j == n - 1) || (j * BN + BN > p.S);
+        const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BN;  // keys >= lim hidden
+        float f = 1.f;  // factor for O and l when the running maximum is raised
+        if constexpr (ROPE) {
+          // two passes over 64-column halves: max of both, then P of the upper half (kept in
+          // registers) and of the lower half (loaded again); P goes to columns kPCol.. which
+          // only hold scores already read
+          float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+          uint32_t hb[64];
+          {
+            uint32_t ha[64];
+            tmem_ld64(tS, ha);
+            if (need_mask) {
+#pragma unroll
+              for (int e = 0; e < 64; ++e)
+                if (e >= lim) ha[e] = __float_as_uint(-INFINITY);
+            }
+#pragma unroll
+            for (int e = 0; e < 64; e += 8) {
+              a0 = fmax3(a0, __uint_as_float(ha[e]), __uint_as_float(ha[e + 1]));
+              a1 = fmax3(a1, __uint_as_float(ha[e + 2]), __uint_as_float(ha[e + 3]));
+              a2 = fmax3(a2, __uint_as_float(ha[e + 4]), __uint_as_float(ha[e + 5]));
+              a3 = fmax3(a3, __uint_as_float(ha[e + 6]), __uint_as_float(ha[e + 7]));
+            }
+          }
+          tmem_ld64(tS + 64, hb);
+          if (need_mask) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (e + 64 >= lim) hb[e] = __float_as_uint(-INFINITY);
+          }
+#pragma unroll
+          for (int e = 0; e < 64; e += 8) {
+            a0 = fmax3(a0, __uint_as_float(hb[e]), __uint_as_float(hb[e + 1]));
+            a1 = fmax3(a1, __uint_as_float(hb[e + 2]), __uint_as_float(hb[e + 3]));
+            a2 = fmax3(a2, __uint_as_float(hb[e + 4]), __uint_as_float(hb[e + 5]));
+            a3 = fmax3(a3, __uint_as_float(hb[e + 6]), __uint_as_float(hb[e + 7]));
+          }
+          const float m_tile = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * p.c_log2;
+          if (j == 0) {
+            m_run = m_tile;
+          } else if (m_tile > m_run + kRescaleThreshold) {
+            f = fast_exp2(m_run - m_tile);
+            l *= f;
+            m_run = m_tile;
+          }
+          const float2 c2 = make_float2(p.c_log2, p.c_log2);
+          const float2 nm2 = make_float2(-m_run, -m_run);
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
+          // 64 scores -> 32 packed bf16 pairs or 16 packed e4m3 quads, stored at column `col`
+          auto emit = [&](const uint32_t (&h)[64], uint32_t col) {
+            constexpr int kW = FP8 ? 16 : 32;
+            uint32_t pk[kW];
+#pragma unroll
+            for (int e = 0; e < 64; e += 4) {
+              float2 x0 = __ffma2_rn(make_float2(__uint_as_float(h[e]), __uint_as_float(h[e + 1])), c2, nm2);
+              float2 x1 = __ffma2_rn(make_float2(__uint_as_float(h[e + 2]), __uint_as_float(h[e + 3])), c2, nm2);
+              x0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+              x1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+              acc0 = __fadd2_rn(acc0, x0);
+              acc1 = __fadd2_rn(acc1, x1);
+              if constexpr (FP8) {
+                pk[e / 4] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x0, __NV_SATFINITE, __NV_E4M3)) |
+                            (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x1, __NV_SATFINITE, __NV_E4M3)) << 16);
+              } else {
+                pk[e / 2] = pack_bf16(x0.x, x0.y);
+                pk[e / 2 + 1] = pack_bf16(x1.x, x1.y);
+              }
+            }
+            if constexpr (FP8)
+              tmem_st16(col, pk);
+            else
+              tmem_st32(col, pk);
+          };
+          emit(hb, tS + kPCol + (FP8 ? 16 : 32));  // keys 64..127
+          {
+            uint32_t ha[64];
+            tmem_ld64(tS, ha);
+            if (need_mask) {
+#pragma unroll
+              for (int e = 0; e < 64; ++e)
+                if (e >= lim) ha[e] = __float_as_uint(-INFINITY);
+            }
+            emit(ha, tS + kPCol);  // keys 0..63
+          }
+          const float2 accs = __fadd2_rn(acc0, acc1);
+          l += accs.x + accs.y;
+        } else {
         uint32_t sr[128];
         tmem_ld128(tS, sr);
-        const bool need_mask = (p.causal && j == n - 1) || (j * BN + BN > p.S);
         if (need_mask) {
-          const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BN;  // keys >= lim hidden
 #pragma unroll
           for (int e = 0; e < 128; ++e)
             if (e >= lim) sr[e] = __float_as_uint(-INFINITY);
@@ -609,7 +699,6 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         }
         const float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
         const float m_tile = mx * p.c_log2;
-        float f = 1.f;  // factor for O and l when the running maximum is raised
         if (j == 0) {
           m_run = m_tile;
         } else if (m_tile > m_run + kRescaleThreshold) {
@@ -655,6 +744,7 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           tmem_st32(tS, pk);
         else
           tmem_st64(tS, pk);
+        }
         // tcgen05.ld / st are warp-collective: rescale when any lane of the warp needs it
         // (lanes that do not have f == 1).
         if (__any_sync(0xffffffffu, f != 1.f)) {
