@@ -315,24 +315,57 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-// Merge the split partials of one (sequence, query head) row per block.
+// Merge the split partials of one (sequence, query head) row per block: weights first (one
+// warp), then every output column reads its partials eight at a time.
+constexpr int kMaxSplits = 1024;
+
 __global__ void __launch_bounds__(128)
     combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse, int nsplit,
                    int D, __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  __shared__ float wgt[kMaxSplits];
+  __shared__ float inv_s, lse_s;
   const size_t row = blockIdx.x;
   const float* lp = ws_lse + row * nsplit;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, lp[s]);
-  float wsum = 0.f;
-  for (int s = 0; s < nsplit; ++s) wsum += lp[s] == -INFINITY ? 0.f : exp2f(lp[s] - M);
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.f;
-    if (wsum > 0.f)
-      for (int s = 0; s < nsplit; ++s)
-        if (lp[s] != -INFINITY) acc += exp2f(lp[s] - M) * ws_o[(row * nsplit + s) * D + d];
-    o[row * D + d] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float M = -INFINITY;
+    for (int s2 = lane; s2 < nsplit; s2 += 32) {
+      const float l = lp[s2];
+      wgt[s2] = l;
+      M = fmaxf(M, l);
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    float wsum = 0.f;
+    for (int s2 = lane; s2 < nsplit; s2 += 32) {
+      const float l = wgt[s2];
+      const float w = l == -INFINITY ? 0.f : exp2f(l - M);
+      wgt[s2] = w;
+      wsum += w;
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o2);
+    if (lane == 0) {
+      inv_s = wsum > 0.f ? 1.f / wsum : 0.f;
+      lse_s = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
+    }
   }
-  if (lse && threadIdx.x == 0) lse[row] = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int i = 0;
+    for (; i + 8 <= nsplit; i += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = ws_o[(row * nsplit + i + u) * D + d];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] += wgt[i + u] * v[u];
+    }
+    for (; i < nsplit; ++i) acc[0] += wgt[i] * ws_o[(row * nsplit + i) * D + d];
+    const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    o[row * D + d] = __float2bfloat16_rn(sum * inv_s);
+  }
+  if (lse && threadIdx.x == 0) lse[row] = lse_s;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -362,6 +395,7 @@ __device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t&
 }
 
 constexpr int kLatMaxB = 2048;  // sequences per call (the tile prefix sums live in smem)
+constexpr int kLatMaxCtas = 128;
 
 struct LatSmem {
   static constexpr int kQOff = kLatStages * kLatTileBytes;
@@ -794,7 +828,7 @@ __global__ void __launch_bounds__(kLatThreads, 1)
 // Finish the sequences that were split between CTAs (merge their partials by log-sum-exp) and
 // the sequences with an out-of-range length (O = 0, LSE = -inf, status DEVICE_ARG).  One block
 // per (sequence, head); sequences a single CTA covered were written directly and are skipped.
-constexpr int kFinishThreads = 128;
+constexpr int kFinishThreads = 448;  // one thread per output column
 constexpr int kMaxParts = 256;  // CTAs one sequence may be spread over (>= the SM count)
 
 __global__ void __launch_bounds__(kFinishThreads)
@@ -803,10 +837,9 @@ __global__ void __launch_bounds__(kFinishThreads)
                          __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                          unsigned int* status) {
   const int b = blockIdx.x, h = blockIdx.y;
-  __shared__ long long red_t[kFinishThreads / 32], red_b[kFinishThreads / 32];
+  __shared__ long long red_t[(kFinishThreads + 31) / 32], red_b[(kFinishThreads + 31) / 32];
   __shared__ int parts[kMaxParts];
   __shared__ float wgt[kMaxParts];
-  __shared__ int nparts;
   __shared__ float inv_s, lse_s;
   long long T = 0, tb = 0;  // all tiles, and tiles of the sequences before b
   for (int i = threadIdx.x; i < B; i += blockDim.x) {
@@ -827,7 +860,7 @@ __global__ void __launch_bounds__(kFinishThreads)
   T = 0;
   tb = 0;
 #pragma unroll
-  for (int w = 0; w < kFinishThreads / 32; ++w) {
+  for (int w = 0; w < (kFinishThreads + 31) / 32; ++w) {
     T += red_t[w];
     tb += red_b[w];
   }
@@ -839,32 +872,22 @@ __global__ void __launch_bounds__(kFinishThreads)
     if (lse && threadIdx.x == 0) lse[orow] = -INFINITY;
     return;
   }
-  // CTAs whose non-empty tile range overlaps this sequence's tiles [tb, tb + tiles)
-  auto cta_of = [&](long long t) {  // the CTA whose (non-empty) range holds tile t
-    long long c = t * G / T;
-    while (c > 0 && lat_range_lo(T, static_cast<int>(c), G) > t) --c;
-    while (c + 1 < G && lat_range_lo(T, static_cast<int>(c) + 1, G) <= t) ++c;
-    return c;
-  };
-  if (cta_of(tb) == cta_of(tb + tiles - 1)) return;  // one CTA covered it: already final
-  if (threadIdx.x == 0) {
-    long long c = cta_of(tb);
-    int n = 0;
-    bool whole = false;
-    for (; c < G && lat_range_lo(T, static_cast<int>(c), G) < tb + tiles; ++c) {
-      const long long a = lat_range_lo(T, static_cast<int>(c), G);
-      const long long z = lat_range_lo(T, static_cast<int>(c) + 1, G);
-      if (a >= z) continue;  // empty range: this CTA wrote nothing
-      if (a <= tb && z >= tb + tiles) whole = true;
-      if (n < kMaxParts) parts[n] = static_cast<int>(c);
-      ++n;
-    }
-    if (n > kMaxParts) report_status(status, ATTN_ERR_UNSUPPORTED);
-    nparts = whole ? 0 : min(n, kMaxParts);
+  // The CTA whose range [T c / G, T (c+1) / G) holds tile t is the largest c with
+  // T c < (t + 1) G, i.e. ((t + 1) G - 1) / T.
+  auto cta_of = [&](long long t) { return ((t + 1) * G - 1) / T; };
+  const long long c_first = cta_of(tb), c_last = cta_of(tb + tiles - 1);
+  if (c_first == c_last) return;  // one CTA covered the whole sequence: already final
+  // With T >= G every CTA owns at least one tile, so the pieces come from c_first..c_last; with
+  // T < G every CTA owns at most one tile, so piece i is the CTA of tile tb + i.
+  const bool dense = T >= G;
+  const int np = static_cast<int>(dense ? c_last - c_first + 1 : tiles);
+  if (np > kMaxParts) {
+    if (threadIdx.x == 0) report_status(status, ATTN_ERR_UNSUPPORTED);
+    return;
   }
+  for (int i = threadIdx.x; i < np; i += blockDim.x)
+    parts[i] = static_cast<int>(dense ? c_first + i : cta_of(tb + i));
   __syncthreads();
-  const int np = nparts;
-  if (np == 0) return;  // written directly by the one CTA that covered it
   if (threadIdx.x < 32) {  // one warp: partial log-sum-exps -> weights, in parallel
     const int lane = threadIdx.x;
     float M = -INFINITY;
@@ -891,10 +914,21 @@ __global__ void __launch_bounds__(kFinishThreads)
   }
   __syncthreads();
   for (int d = threadIdx.x; d < kLatV; d += blockDim.x) {
-    float acc = 0.f;
-    for (int i = 0; i < np; ++i)
-      acc += wgt[i] * ws_o[((static_cast<size_t>(parts[i]) + b) * H + h) * kLatV + d];
-    o[orow * kLatV + d] = __float2bfloat16_rn(acc * inv_s);
+    // sixteen pieces per step, loads issued before any use (in-order issue would otherwise
+    // wait for each load in turn)
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int i = 0;
+    for (; i + 16 <= np; i += 16) {
+      float v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        v[u] = ws_o[((static_cast<size_t>(parts[i + u]) + b) * H + h) * kLatV + d];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) acc[u & 7] += wgt[i + u] * v[u];
+    }
+    for (; i < np; ++i) acc[0] += wgt[i] * ws_o[((static_cast<size_t>(parts[i]) + b) * H + h) * kLatV + d];
+    const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    o[orow * kLatV + d] = __float2bfloat16_rn(sum * inv_s);
   }
   if (lse && threadIdx.x == 0) lse[orow] = lse_s;
 }
@@ -907,7 +941,7 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 // back by the combine.
 DecodePlan plan_common(int units, int Lmax, int ctas, double key_bytes, int rows_per_unit,
                        int out_dim) {
-  const int max_split = std::max(1, (Lmax + kTileKeys - 1) / kTileKeys);
+  const int max_split = std::min(kMaxSplits, std::max(1, (Lmax + kTileKeys - 1) / kTileKeys));
   int best = 1;
   double best_cost = 1e300;
   for (int ns = 1; ns <= max_split; ns *= 2) {
@@ -987,11 +1021,13 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int Lmax) {
 DecodePlan plan_latent(int B, int H, int Lmax) {
   (void)Lmax;
   DecodePlan pl;
-  // Few sequences: spread their key tiles over every SM (partials merged afterwards).  Many
-  // sequences: one CTA per sequence (equal lengths then need no merge); measured faster there.
-  const int sms = sm_count();
-  const bool streamk = 2 * B < sms;
-  pl.grid = streamk ? sms : std::min(B, sms);
+  // At most 128 CTAs: on GB300 the latent stream reached 5.2 TB/s with 128 streaming CTAs and
+  // only 4.6 TB/s with 140 or 152 (measured with the compute removed).  B equal to the CTA
+  // count: one CTA per sequence, no merge.  Otherwise the key tiles of all sequences are spread
+  // evenly over the CTAs and the pieces of split sequences merged afterwards.
+  const int ctas = std::min(sm_count(), kLatMaxCtas);
+  const bool streamk = B != ctas;
+  pl.grid = ctas;
   pl.nsplit = streamk ? 1 : 0;  // 1 = stream-K mode (nsplit doubles as the mode flag here)
   pl.chunk = 0;
   // stream-K: partial outputs of sequences split between CTAs, slot (CTA + sequence)
