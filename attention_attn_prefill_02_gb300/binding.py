@@ -123,7 +123,8 @@ def attn_decode_workspace_size(B, Hq, Hkv, D, Lmax):
 
 def attn_decode(q, k_cache, v_cache, cache_len, o=None, lse=None, want_lse=False,
                 softmax_scale=0.0, rope=True, rope_theta=10000.0, workspace=None, stream=None):
-    """O [B,Hq,D] for q [B,Hq,D] against caches [B,Hkv,Lmax,D] with device cache_len [B]."""
+    """O [B,Hq,D] for q [B,Hq,D] (bf16) against caches [B,Hkv,Lmax,D] (bf16 or fp8 e5m2) with
+    device cache_len [B]."""
     _require_cuda(q, k_cache, v_cache, cache_len, o, lse, workspace)
     B, Hq, D = q.shape
     Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
@@ -136,7 +137,7 @@ def attn_decode(q, k_cache, v_cache, cache_len, o=None, lse=None, want_lse=False
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len), Lmax,
-                             _ptr(o), _ptr(lse), DTYPE_CODES[q.dtype], B, Hq, Hkv, D,
+                             _ptr(o), _ptr(lse), DTYPE_CODES[k_cache.dtype], B, Hq, Hkv, D,
                              float(softmax_scale), int(bool(rope)), float(rope_theta),
                              _ptr(workspace), wbytes, _stream(stream)), "attn_decode")
     return (o, lse) if (want_lse or lse is not None) else o
@@ -154,7 +155,7 @@ def attn_decode_noalloc(q, k_cache, v_cache, cache_len, o=None, lse=None, want_l
     if want_lse and lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     _check(lib().attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len),
-                                     Lmax, _ptr(o), _ptr(lse), DTYPE_CODES[q.dtype], B, Hq, Hkv,
+                                     Lmax, _ptr(o), _ptr(lse), DTYPE_CODES[k_cache.dtype], B, Hq, Hkv,
                                      D, float(softmax_scale), int(bool(rope)), float(rope_theta),
                                      _stream(stream)), "attn_decode_noalloc")
     return (o, lse) if (want_lse or lse is not None) else o

@@ -112,7 +112,8 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
   if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (Hq / Hkv > 16 || dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (dtype == ATTN_FP8_E5M2 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(Lmax) > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
@@ -126,6 +127,9 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
     if (!tab) return st;
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  if (dtype == ATTN_FP8_E5M2)
+    return launch_decode_fp8(q, k_cache, v_cache, cache_len, Lmax, o, lse, B, Hq, Hkv, scale,
+                             tab, workspace, plan, as_stream(stream));
   return launch_decode(q, k_cache, v_cache, cache_len, Lmax, o, lse, B, Hq, Hkv, D, scale, tab,
                        workspace, plan, as_stream(stream));
 }

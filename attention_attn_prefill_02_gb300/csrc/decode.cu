@@ -315,6 +315,320 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// ------------------------------------------------------------------------------------------------
+// GQA decode with an fp8 (e5m2) cache: the same streaming structure at half the bytes.  Every
+// e5m2 value is exactly an f16 value (its bits are the top byte of the f16), so the MMAs run in
+// f16 on widened values: K fragments are read straight from the swizzled fp8 tile (4 bytes =
+// 4 consecutive dims; the query fragments use the same dimension order, which leaves every dot
+// product unchanged), V rows are widened into a small per-warp f16 tile that ldmatrix.trans
+// reads.  The query stays bf16 in memory and is converted to f16 (values beyond f16 range are
+// not supported).
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kF8Stages = 5;  // 2 CTAs per SM: 2 x 111 KB of shared memory
+constexpr int kF8D = 128;
+constexpr int kF8TileBytes = kTileKeys * kF8D;       // 8 KB: 64 keys x 128 fp8
+constexpr int kF8VPitch = kF8D * 2 + 16;            // per-warp f16 V tile row pitch (272 B)
+
+struct GqaF8Smem {
+  static constexpr int kQOff = kF8Stages * 2 * kF8TileBytes;           // 96 KB of stages
+  static constexpr int kQPitch = kF8D * 2 + 16;
+  static constexpr int kVOff = kQOff + 16 * kQPitch;                   // [warps][16][pitch]
+  static constexpr int kRedOff = kVOff + kComputeWarps * 16 * kF8VPitch;
+  static constexpr int kOOff = kRedOff + 2 * kComputeWarps * 16 * 4;
+  static int bytes(int G) { return kOOff + kComputeWarps * G * kF8D * 4 + 2 * kF8Stages * 8 + 1024; }
+};
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+      " {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Bytes 0,1 (or 2,3) of four e5m2 values -> an f16x2 holding them exactly.
+__device__ __forceinline__ uint32_t e5m2x2_lo(uint32_t w) { return __byte_perm(w, 0u, 0x1404); }
+__device__ __forceinline__ uint32_t e5m2x2_hi(uint32_t w) { return __byte_perm(w, 0u, 0x3424); }
+
+template <int NST>
+__global__ void __launch_bounds__(kThreads, 2)
+    gqa_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
+  constexpr int D = kF8D;
+  using L = GqaF8Smem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int G = p.G;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOOff + kComputeWarps * G * D * 4);
+  uint64_t* empty = full + NST;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_items = p.B * p.Hkv * p.nsplit;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kComputeWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kComputeWarps) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int sp = it % p.nsplit;
+        const int bh = it / p.nsplit;
+        const int b = bh / p.Hkv;
+        int len = p.lens[b];
+        if (len < 1 || len > p.Lmax) len = 0;
+        const int k0 = sp * p.chunk;
+        const int k1 = min(k0 + p.chunk, len);
+        for (int t0 = k0; t0 < k1; t0 += kTileKeys) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) return;
+          mbar_arrive_expect_tx(&full[stage], 2 * kF8TileBytes);
+          uint8_t* kt = smem + stage * 2 * kF8TileBytes;
+          tma_load_3d(kt, &tmK, &full[stage], 0, t0, bh);
+          tma_load_3d(kt + kF8TileBytes, &tmV, &full[stage], 0, t0, bh);
+          if (++stage == NST) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  const int tid = threadIdx.x;
+  const int g = lane >> 2, tq = lane & 3;
+  uint8_t* qs = smem + L::kQOff;
+  uint8_t* vw = smem + L::kVOff + warp * 16 * kF8VPitch;  // this warp's f16 V rows
+  const uint32_t vw_addr = smem_u32(vw);
+  float* red_m = reinterpret_cast<float*>(smem + L::kRedOff);
+  float* red_l = red_m + kComputeWarps * 16;
+  float* red_o = reinterpret_cast<float*>(smem + L::kOOff);
+  int stage = 0;
+  uint32_t phase = 0;
+  bool alive = true;
+
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const int sp = it % p.nsplit;
+    const int bh = it / p.nsplit;
+    const int b = bh / p.Hkv, kvh = bh % p.Hkv;
+    int len = p.lens[b];
+    const bool valid = len >= 1 && len <= p.Lmax;
+    if (!valid) {
+      if (tid == 0 && sp == 0) report_status(p.status, ATTN_ERR_DEVICE_ARG);
+      len = 0;
+    }
+    const int k0 = sp * p.chunk;
+    const int k1 = min(k0 + p.chunk, len);
+
+    // query rows as f16 (rotated at position len), zero-padded to 16 rows
+    compute_bar_sync();
+    for (int idx = tid; idx < 16 * (D / 2); idx += kComputeWarps * 32) {
+      const int r = idx / (D / 2), i = idx % (D / 2);
+      float x1 = 0.f, x2 = 0.f;
+      if (r < G && valid) {
+        const __nv_bfloat16* qr = p.q + (static_cast<size_t>(b) * p.Hq + kvh * G + r) * D;
+        x1 = __bfloat162float(qr[i]);
+        x2 = __bfloat162float(qr[i + D / 2]);
+        if (p.table) {
+          const float2 cs = p.table[static_cast<size_t>(len) * (D / 2) + i];
+          const float y1 = x1 * cs.x - x2 * cs.y;
+          const float y2 = x2 * cs.x + x1 * cs.y;
+          x1 = y1;
+          x2 = y2;
+        }
+      }
+      __half* row = reinterpret_cast<__half*>(qs + r * L::kQPitch);
+      row[i] = __float2half_rn(x1);
+      row[i + D / 2] = __float2half_rn(x2);
+    }
+    compute_bar_sync();
+    // A fragments with the dimension order the K loads use: logical k = 2t+e -> dim 16kk+4t+e,
+    // k = 8+2t+e -> dim 16kk+4t+2+e
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int d0 = 16 * kk + 4 * tq;
+      qa[kk][0] = *reinterpret_cast<const uint32_t*>(qs + g * L::kQPitch + d0 * 2);
+      qa[kk][1] = *reinterpret_cast<const uint32_t*>(qs + (g + 8) * L::kQPitch + d0 * 2);
+      qa[kk][2] = *reinterpret_cast<const uint32_t*>(qs + g * L::kQPitch + (d0 + 2) * 2);
+      qa[kk][3] = *reinterpret_cast<const uint32_t*>(qs + (g + 8) * L::kQPitch + (d0 + 2) * 2);
+    }
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float acc[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+    for (int t0 = k0; t0 < k1 && alive; t0 += kTileKeys) {
+      if (!mbar_wait(&full[stage], phase, p.status)) {
+        alive = false;
+        break;
+      }
+      const uint8_t* kt = smem + stage * 2 * kF8TileBytes;
+      const uint8_t* vt = kt + kF8TileBytes;
+      // S (16 query rows x this warp's 16 keys) from 4-byte K reads
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int key = warp * 16 + nt * 8 + g;
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + sw128_offset(key, kk) + 4 * tq);
+          mma_f16_16816(s[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], e5m2x2_lo(w),
+                        e5m2x2_hi(w));
+        }
+      }
+      // widen this warp's 16 V rows to f16 (lane: row lane / 2, dims 64 (lane & 1) .. +63)
+      {
+        const int key = warp * 16 + (lane >> 1);
+        const int half = lane & 1;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(vt + sw128_offset(key, half * 4 + c));
+          uint4 o0, o1;
+          o0.x = e5m2x2_lo(w.x); o0.y = e5m2x2_hi(w.x); o0.z = e5m2x2_lo(w.y); o0.w = e5m2x2_hi(w.y);
+          o1.x = e5m2x2_lo(w.z); o1.y = e5m2x2_hi(w.z); o1.z = e5m2x2_lo(w.w); o1.w = e5m2x2_hi(w.w);
+          uint8_t* dst = vw + (lane >> 1) * kF8VPitch + (half * 64 + c * 16) * 2;
+          *reinterpret_cast<uint4*>(dst) = o0;
+          *reinterpret_cast<uint4*>(dst + 16) = o1;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);  // the stage is no longer read
+      if (++stage == NST) {
+        stage = 0;
+        phase ^= 1;
+      }
+      float rm0 = -INFINITY, rm1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int key = t0 + warp * 16 + nt * 8 + tq * 2 + (j & 1);
+          const float v = key < k1 ? s[nt][j] * p.scale_log2 : -INFINITY;
+          s[nt][j] = v;
+          if (j < 2)
+            rm0 = fmaxf(rm0, v);
+          else
+            rm1 = fmaxf(rm1, v);
+        }
+      rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 1));
+      rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 2));
+      rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 1));
+      rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 2));
+      const float mn0 = fmaxf(m0, rm0), mn1 = fmaxf(m1, rm1);
+      const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float c0 = fast_exp2(m0 - base0), c1 = fast_exp2(m1 - base1);
+      m0 = mn0;
+      m1 = mn1;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        s[nt][0] = fast_exp2(s[nt][0] - base0);
+        s[nt][1] = fast_exp2(s[nt][1] - base0);
+        s[nt][2] = fast_exp2(s[nt][2] - base1);
+        s[nt][3] = fast_exp2(s[nt][3] - base1);
+        ps0 += s[nt][0] + s[nt][1];
+        ps1 += s[nt][2] + s[nt][3];
+      }
+      l0 = l0 * c0 + ps0;
+      l1 = l1 * c1 + ps1;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        acc[n][0] *= c0;
+        acc[n][1] *= c0;
+        acc[n][2] *= c1;
+        acc[n][3] *= c1;
+      }
+      const uint32_t pa0 = pack_f16(s[0][0], s[0][1]);
+      const uint32_t pa1 = pack_f16(s[0][2], s[0][3]);
+      const uint32_t pa2 = pack_f16(s[1][0], s[1][1]);
+      const uint32_t pa3 = pack_f16(s[1][2], s[1][3]);
+      {
+        const int m = lane >> 3;
+        const int r = (m & 1) * 8 + (lane & 7);  // key row within the warp's 16
+#pragma unroll
+        for (int n2 = 0; n2 < D / 16; ++n2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vw_addr + r * kF8VPitch + (n2 * 16 + (m >> 1) * 8) * 2, b0, b1, b2, b3);
+          mma_f16_16816(acc[2 * n2], pa0, pa1, pa2, pa3, b0, b1);
+          mma_f16_16816(acc[2 * n2 + 1], pa0, pa1, pa2, pa3, b2, b3);
+        }
+      }
+      __syncwarp();  // the f16 V rows are rewritten for the next tile
+    }
+    if (!alive) return;
+
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if (tq == 0) {
+      red_m[warp * 16 + g] = m0;
+      red_m[warp * 16 + g + 8] = m1;
+      red_l[warp * 16 + g] = l0;
+      red_l[warp * 16 + g + 8] = l1;
+    }
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      const int d = n * 8 + tq * 2;
+      if (g < G) {
+        red_o[(warp * G + g) * D + d] = acc[n][0];
+        red_o[(warp * G + g) * D + d + 1] = acc[n][1];
+      }
+      if (g + 8 < G) {
+        red_o[(warp * G + g + 8) * D + d] = acc[n][2];
+        red_o[(warp * G + g + 8) * D + d + 1] = acc[n][3];
+      }
+    }
+    compute_bar_sync();
+    for (int idx = tid; idx < G * D; idx += kComputeWarps * 32) {
+      const int r = idx / D, d = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, red_m[w * 16 + r]);
+      float lsum = 0.f, osum = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kComputeWarps; ++w) {
+          const float mw = red_m[w * 16 + r];
+          const float wgt = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+          lsum += wgt * red_l[w * 16 + r];
+          osum += wgt * red_o[(w * G + r) * D + d];
+        }
+      }
+      const float o = lsum > 0.f ? osum / lsum : 0.f;
+      const float lse2 = lsum > 0.f ? M + log2f(lsum) : -INFINITY;
+      const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + r;
+      if (p.nsplit == 1) {
+        p.o[row * D + d] = __float2bfloat16_rn(o);
+        if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
+      } else {
+        p.ws_o[(row * p.nsplit + sp) * D + d] = o;
+        if (d == 0) p.ws_lse[row * p.nsplit + sp] = lse2;
+      }
+    }
+  }
+}
+
 // Merge the split partials of one (sequence, query head) row per block: weights first (one
 // warp), then every output column reads its partials eight at a time.
 constexpr int kMaxSplits = 1024;
@@ -1033,6 +1347,47 @@ DecodePlan plan_latent(int B, int H, int Lmax) {
   // stream-K: partial outputs of sequences split between CTAs, slot (CTA + sequence)
   pl.ws_bytes = streamk ? static_cast<size_t>(B + pl.grid - 1) * H * (kLatV + 1) * 4 : 0;
   return pl;
+}
+
+attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
+                                const int32_t* lens, int Lmax, void* o, float* lse, int B, int Hq,
+                                int Hkv, float scale, const float2* table, void* ws,
+                                const DecodePlan& plan, cudaStream_t st) {
+  constexpr int D = kF8D;
+  CUtensorMap tk, tv;
+  if (!make_tmap_3d(&tk, k, 1, D, Lmax, static_cast<uint64_t>(B) * Hkv, D, kTileKeys, 128) ||
+      !make_tmap_3d(&tv, v, 1, D, Lmax, static_cast<uint64_t>(B) * Hkv, D, kTileKeys, 128))
+    return ATTN_ERR_CUDA;
+  GqaParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.lens = lens;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  const size_t rows = static_cast<size_t>(B) * Hq;
+  p.ws_o = plan.nsplit > 1 ? static_cast<float*>(ws) : nullptr;
+  p.ws_lse = plan.nsplit > 1 ? static_cast<float*>(ws) + rows * plan.nsplit * D : nullptr;
+  p.table = table;
+  p.status = device_status_ptr();
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.Lmax = Lmax;
+  p.nsplit = plan.nsplit;
+  p.chunk = plan.chunk;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int smem = GqaF8Smem::bytes(p.G);
+  auto kern = gqa_decode_fp8_kernel<kF8Stages>;
+  if (!set_smem_attr(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
+  const int items = B * Hkv * plan.nsplit;
+  kern<<<std::min(items, plan.grid), kThreads, smem, st>>>(tk, tv, p);
+  if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
+  if (plan.nsplit > 1) {
+    combine_kernel<<<static_cast<unsigned>(rows), 128, 0, st>>>(p.ws_o, p.ws_lse, plan.nsplit, D,
+                                                              p.o, lse);
+    return launch_status();
+  }
+  return ATTN_OK;
 }
 
 attn_status_t launch_decode(const void* q, const void* k, const void* v, const int32_t* lens,

@@ -67,6 +67,11 @@ attn_status_t launch_decode(const void* q, const void* k, const void* v, const i
                             float scale, const float2* table, void* ws, const DecodePlan& plan,
                             cudaStream_t st);
 
+attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
+                                const int32_t* lens, int Lmax, void* o, float* lse, int B, int Hq,
+                                int Hkv, float scale, const float2* table, void* ws,
+                                const DecodePlan& plan, cudaStream_t st);
+
 attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, int Lmax, void* o,
                             float* lse, int B, int H, float scale, const float2* table, void* ws,
                             const DecodePlan& plan, cudaStream_t st);

@@ -39,14 +39,16 @@ def prefill_inputs(B, Hq, Hkv, S, D, dtype="bf16", seed=0):
     return q, k, v
 
 
-def decode_inputs(B, Hq, Hkv, Lmax, D, cache_len, seed=0, dtype="bf16"):
+def decode_inputs(B, Hq, Hkv, Lmax, D, cache_len, seed=0, dtype="bf16", cache_dtype=None):
     """q [B,Hq,D], k/v caches [B,Hkv,Lmax,D], cache_len int32 [B].
 
-    ``cache_len`` may be an int (same for every sequence) or a sequence of B ints.
+    ``cache_len`` may be an int (same for every sequence) or a sequence of B ints.  The caches
+    use ``cache_dtype`` (default: ``dtype``).
     """
+    cd = dtype if cache_dtype is None else cache_dtype
     q = normal((B, Hq, D), 1000 * seed + SEED_Q, dtype)
-    k = normal((B, Hkv, Lmax, D), 1000 * seed + SEED_CACHE, dtype)
-    v = normal((B, Hkv, Lmax, D), 1000 * seed + SEED_CACHE + 10, dtype)
+    k = normal((B, Hkv, Lmax, D), 1000 * seed + SEED_CACHE, cd)
+    v = normal((B, Hkv, Lmax, D), 1000 * seed + SEED_CACHE + 10, cd)
     if isinstance(cache_len, int):
         lens = torch.full((B,), cache_len, dtype=torch.int32)
     else:

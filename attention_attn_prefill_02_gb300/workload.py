@@ -32,8 +32,8 @@ def decode_bytes(B, Hq, Hkv, L, D, dtype="bf16"):
     The history part is 2 * Hkv * D elements per token per sequence — for Hkv=8, D=128 that is
     the audit's 2048 BF16 elements per token per group, 1 GiB at batch 128 / context 2048.
     """
-    e = DTYPE_BYTES[dtype]
-    return 2 * B * Hkv * L * D * e + B * Hq * D * e + B * Hq * D * 2
+    e = DTYPE_BYTES[dtype]  # cache storage type; q and o are bf16
+    return 2 * B * Hkv * L * D * e + B * Hq * D * 2 + B * Hq * D * 2
 
 
 def decode_flops(B, Hq, L, D):

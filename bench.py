@@ -332,6 +332,20 @@ def variants(b, d):
                          "l2_resident": nbytes < 100e6}
         del q, kc, vc, cl, o, ws
     out["decode_sweep"] = sweep
+    # fp8 e5m2 cache (half the bytes), batch 128
+    q, kc, vc, cl = synthetic.decode_inputs(128, Dd["Hq"], Dd["Hkv"], Dd["L"], Dd["D"], Dd["L"],
+                                            seed=6, cache_dtype="fp8")
+    q, kc, vc, cl = q.cuda(), kc.cuda(), vc.cuda(), cl.cuda()
+    o = torch.empty((128, Dd["Hq"], Dd["D"]), dtype=torch.bfloat16, device="cuda")
+
+    def f8():
+        b.attn_decode(q, kc, vc, cl, o=o, rope=True, rope_theta=THETA)
+
+    nbytes = workload.decode_bytes(128, Dd["Hq"], Dd["Hkv"], Dd["L"], Dd["D"], dtype="fp8")
+    tg = time_graph(f8, 50)
+    out["decode_fp8_cache_b128"] = {"graph_ms": round(tg, 5), "gbs": round(nbytes / tg / 1e6, 1),
+                                    "frac_of_hbm": round(nbytes / tg / 1e6 / measured_peaks()[0], 4)}
+    del q, kc, vc, cl, o
     return out
 
 

@@ -127,7 +127,9 @@ ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int Lm
  *   o          [B,Hq,D] bfloat16.  lse: NULL or [B,Hq] float32.
  *   workspace  device buffer of at least attn_decode_workspace_size(B,Hq,Hkv,D,Lmax) bytes
  *              (may be NULL when that size is 0).  Contents need no initialisation.
- *   D in {64, 128}; Hq % Hkv == 0; Hq / Hkv <= 16; dtype ATTN_BF16.
+ *   dtype      storage type of the caches: ATTN_BF16, or ATTN_FP8_E5M2 (D = 128 only; values
+ *              are widened exactly to f16 for the products).  q is always bfloat16.
+ *   D in {64, 128}; Hq % Hkv == 0; Hq / Hkv <= 16.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */
 ATTN_API attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,

@@ -112,7 +112,7 @@ def test_decode_validation(L):
     assert _decode(L, Hq=30) == INVALID
     assert _decode(L, D=80) == UNSUPPORTED
     assert _decode(L, Hq=64, Hkv=2) == UNSUPPORTED      # group of 32 > 16
-    assert _decode(L, dt=1) == UNSUPPORTED              # fp8 decode not built
+    assert _decode(L, dt=1, D=64) == UNSUPPORTED        # fp8 cache only for D = 128
     assert _decode(L, rope=3) == INVALID
 
 

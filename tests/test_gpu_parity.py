@@ -214,6 +214,18 @@ def test_decode_bf16(B, Hq, Hkv, D, Lmax, lens):
     check(lse.cpu(), rl, LSE_TOL, None, what="LSE")
 
 
+@pytest.mark.parametrize("B,lens", [(1, [2048]), (3, [2048, 1, 777]), (8, 2048), (40, 1500)])
+def test_decode_fp8_cache(B, lens):
+    """fp8 e5m2 K/V cache (q bf16): the kernel widens the cache exactly, so bf16 bounds hold."""
+    q, kc, vc, cl = synthetic.decode_inputs(B, 32, 8, 2048, 128, lens, seed=B + 50,
+                                            cache_dtype="fp8")
+    o, lse = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda(), want_lse=True)
+    status_ok()
+    ro, rl = oracle.decode(f64(q), f64(kc), f64(vc), cl.numpy(), rope=True, theta=10000.0)
+    check(o.cpu(), ro, what="O fp8 cache")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE fp8 cache")
+
+
 def test_decode_bad_cache_len_sets_status():
     q, kc, vc, cl = synthetic.decode_inputs(2, 8, 2, 64, 64, [64, 64], seed=1)
     cl[1] = 65  # > Lmax
