@@ -318,25 +318,32 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ------------------------------------------------------------------------------------------------
 // GQA decode with an fp8 (e5m2) cache: the same streaming structure at half the bytes.  Every
 // e5m2 value is exactly an f16 value (its bits are the top byte of the f16), so the MMAs run in
-// f16 on widened values: K fragments are read straight from the swizzled fp8 tile (4 bytes =
-// 4 consecutive dims; the query fragments use the same dimension order, which leaves every dot
-// product unchanged), V rows are widened into a small per-warp f16 tile that ldmatrix.trans
-// reads.  The query stays bf16 in memory and is converted to f16 (values beyond f16 range are
-// not supported).
+// f16 on values widened in registers by byte permutes.
+//
+// The MMAs are transposed with respect to the bf16 kernel: S^T = K Q^T and O^T = V^T P^T.  Keys
+// (and, for PV, head dimensions) take the 16-row side of m16n8k16 and the group's query heads the
+// 8-column side, so a group of up to 8 heads wastes no MMA rows on padding (NT = 2 column tiles
+// for groups of 9..16).  K fragments are 4-byte reads of the swizzled tile (4 consecutive dims;
+// the query fragments use the same dimension order, which leaves every dot product unchanged).
+// V^T fragments come from ldmatrix.trans on the fp8 tile read as 16-bit pairs: one register holds
+// dims (2c, 2c+1) of keys (2t, 2t+1), and the two byte permutes split it into the rows of dims 2c
+// and 2c+1, so MMA row r of a 16-dim chunk is dim 2r (r < 8) or dim 2(r-8)+1.  The probabilities
+// go from the S^T accumulator layout to the P^T operand layout with movmatrix.trans.  The query
+// stays bf16 in memory and is converted to f16 (values beyond f16 range are not supported).
 // ------------------------------------------------------------------------------------------------
 
-constexpr int kF8Stages = 5;  // 2 CTAs per SM: 2 x 111 KB of shared memory
 constexpr int kF8D = 128;
-constexpr int kF8TileBytes = kTileKeys * kF8D;       // 8 KB: 64 keys x 128 fp8
-constexpr int kF8VPitch = kF8D * 2 + 16;            // per-warp f16 V tile row pitch (272 B)
+constexpr int kF8TileBytes = kTileKeys * kF8D;  // 8 KB: 64 keys x 128 fp8
+// 5 stages for groups of up to 8 heads, 4 for larger groups (two CTAs per SM either way)
+constexpr int f8_stages(int nt) { return nt == 1 ? 5 : 4; }
 
+template <int NST>
 struct GqaF8Smem {
-  static constexpr int kQOff = kF8Stages * 2 * kF8TileBytes;           // 96 KB of stages
+  static constexpr int kQOff = NST * 2 * kF8TileBytes;
   static constexpr int kQPitch = kF8D * 2 + 16;
-  static constexpr int kVOff = kQOff + 16 * kQPitch;                   // [warps][16][pitch]
-  static constexpr int kRedOff = kVOff + kComputeWarps * 16 * kF8VPitch;
+  static constexpr int kRedOff = kQOff + 16 * kQPitch;
   static constexpr int kOOff = kRedOff + 2 * kComputeWarps * 16 * 4;
-  static int bytes(int G) { return kOOff + kComputeWarps * G * kF8D * 4 + 2 * kF8Stages * 8 + 1024; }
+  static int bytes(int G) { return kOOff + kComputeWarps * G * kF8D * 4 + 2 * NST * 8 + 1024; }
 };
 
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -354,16 +361,27 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Bytes 0,1 (or 2,3) of four e5m2 values -> an f16x2 holding them exactly.
+// 8x8 16-bit matrix held one row pair per lane -> its transpose in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// e5m2 bytes -> f16x2 holding them exactly: bytes 0,1 / 2,3 (consecutive dims of one key), or
+// bytes 0,2 / 1,3 (one dim of two keys, as ldmatrix.trans delivers V).
 __device__ __forceinline__ uint32_t e5m2x2_lo(uint32_t w) { return __byte_perm(w, 0u, 0x1404); }
 __device__ __forceinline__ uint32_t e5m2x2_hi(uint32_t w) { return __byte_perm(w, 0u, 0x3424); }
+__device__ __forceinline__ uint32_t e5m2x2_even(uint32_t w) { return __byte_perm(w, 0u, 0x2404); }
+__device__ __forceinline__ uint32_t e5m2x2_odd(uint32_t w) { return __byte_perm(w, 0u, 0x3414); }
 
-template <int NST>
+template <int NST, int NT>
 __global__ void __launch_bounds__(kThreads, 2)
     gqa_decode_fp8_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
   constexpr int D = kF8D;
-  using L = GqaF8Smem;
+  constexpr int NC = D / 16;  // 16-dim chunks
+  using L = GqaF8Smem<NST>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -415,11 +433,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tid = threadIdx.x;
   const int g = lane >> 2, tq = lane & 3;
   uint8_t* qs = smem + L::kQOff;
-  uint8_t* vw = smem + L::kVOff + warp * 16 * kF8VPitch;  // this warp's f16 V rows
-  const uint32_t vw_addr = smem_u32(vw);
   float* red_m = reinterpret_cast<float*>(smem + L::kRedOff);
   float* red_l = red_m + kComputeWarps * 16;
   float* red_o = reinterpret_cast<float*>(smem + L::kOOff);
+  // this warp's 16 keys: S^T rows g and g + 8
+  const int key_a = warp * 16 + g;
+  // ldmatrix.trans row of this lane: matrices (keys 0-7 | 8-15) x (chunk 2c | 2c + 1)
+  const int v_key = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int v_chunk = lane >> 4;
   int stage = 0;
   uint32_t phase = 0;
   bool alive = true;
@@ -437,9 +458,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int k0 = sp * p.chunk;
     const int k1 = min(k0 + p.chunk, len);
 
-    // query rows as f16 (rotated at position len), zero-padded to 16 rows
+    // query rows as f16 (rotated at position len), zero-padded to 8 NT rows
     compute_bar_sync();
-    for (int idx = tid; idx < 16 * (D / 2); idx += kComputeWarps * 32) {
+    for (int idx = tid; idx < 8 * NT * (D / 2); idx += kComputeWarps * 32) {
       const int r = idx / (D / 2), i = idx % (D / 2);
       float x1 = 0.f, x2 = 0.f;
       if (r < G && valid) {
@@ -459,22 +480,28 @@ __global__ void __launch_bounds__(kThreads, 2)
       row[i + D / 2] = __float2half_rn(x2);
     }
     compute_bar_sync();
-    // A fragments with the dimension order the K loads use: logical k = 2t+e -> dim 16kk+4t+e,
-    // k = 8+2t+e -> dim 16kk+4t+2+e
-    uint32_t qa[D / 16][4];
+    // Q^T operand: column g is query 8 nt + g; logical k = 2t+e -> dim 16kk+4t+e and
+    // k = 8+2t+e -> dim 16kk+4t+2+e, the order the K reads deliver
+    uint32_t qb[NT][NC][2];
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const int d0 = 16 * kk + 4 * tq;
-      qa[kk][0] = *reinterpret_cast<const uint32_t*>(qs + g * L::kQPitch + d0 * 2);
-      qa[kk][1] = *reinterpret_cast<const uint32_t*>(qs + (g + 8) * L::kQPitch + d0 * 2);
-      qa[kk][2] = *reinterpret_cast<const uint32_t*>(qs + g * L::kQPitch + (d0 + 2) * 2);
-      qa[kk][3] = *reinterpret_cast<const uint32_t*>(qs + (g + 8) * L::kQPitch + (d0 + 2) * 2);
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int kk = 0; kk < NC; ++kk) {
+        const uint8_t* src = qs + (nt * 8 + g) * L::kQPitch + (16 * kk + 4 * tq) * 2;
+        qb[nt][kk][0] = *reinterpret_cast<const uint32_t*>(src);
+        qb[nt][kk][1] = *reinterpret_cast<const uint32_t*>(src + 4);
+      }
 
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float acc[D / 8][4];
+    // softmax state of queries 8 nt + 2 tq + e; l is this lane's partial sum over its keys
+    float m[NT][2], l[NT][2];
+    float acc[NT][NC][4];
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) acc[nt][c][0] = acc[nt][c][1] = acc[nt][c][2] = acc[nt][c][3] = 0.f;
+    }
 
     for (int t0 = k0; t0 < k1 && alive; t0 += kTileKeys) {
       if (!mbar_wait(&full[stage], phase, p.status)) {
@@ -482,122 +509,117 @@ __global__ void __launch_bounds__(kThreads, 2)
         break;
       }
       const uint8_t* kt = smem + stage * 2 * kF8TileBytes;
-      const uint8_t* vt = kt + kF8TileBytes;
-      // S (16 query rows x this warp's 16 keys) from 4-byte K reads
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const uint32_t vt_addr = smem_u32(kt + kF8TileBytes);
+      uint32_t kw[NC][2];
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int key = warp * 16 + nt * 8 + g;
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + sw128_offset(key, kk) + 4 * tq);
-          mma_f16_16816(s[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], e5m2x2_lo(w),
-                        e5m2x2_hi(w));
-        }
+      for (int kk = 0; kk < NC; ++kk) {
+        kw[kk][0] = *reinterpret_cast<const uint32_t*>(kt + sw128_offset(key_a, kk) + 4 * tq);
+        kw[kk][1] = *reinterpret_cast<const uint32_t*>(kt + sw128_offset(key_a + 8, kk) + 4 * tq);
       }
-      // widen this warp's 16 V rows to f16 (lane: row lane / 2, dims 64 (lane & 1) .. +63)
-      {
-        const int key = warp * 16 + (lane >> 1);
-        const int half = lane & 1;
+      uint32_t vw[NC / 2][4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(vt + sw128_offset(key, half * 4 + c));
-          uint4 o0, o1;
-          o0.x = e5m2x2_lo(w.x); o0.y = e5m2x2_hi(w.x); o0.z = e5m2x2_lo(w.y); o0.w = e5m2x2_hi(w.y);
-          o1.x = e5m2x2_lo(w.z); o1.y = e5m2x2_hi(w.z); o1.z = e5m2x2_lo(w.w); o1.w = e5m2x2_hi(w.w);
-          uint8_t* dst = vw + (lane >> 1) * kF8VPitch + (half * 64 + c * 16) * 2;
-          *reinterpret_cast<uint4*>(dst) = o0;
-          *reinterpret_cast<uint4*>(dst + 16) = o1;
-        }
-      }
+      for (int c2 = 0; c2 < NC / 2; ++c2)
+        ldsm_x4_t(vt_addr + sw128_offset(v_key, 2 * c2 + v_chunk), vw[c2][0], vw[c2][1],
+                  vw[c2][2], vw[c2][3]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);  // the stage is no longer read
       if (++stage == NST) {
         stage = 0;
         phase ^= 1;
       }
-      float rm0 = -INFINITY, rm1 = -INFINITY;
+
+      // S^T: two accumulation chains (even / odd dim chunks) per column tile
+      float s[NT][2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) s[nt][h][0] = s[nt][h][1] = s[nt][h][2] = s[nt][h][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < NC; ++kk) {
+        const uint32_t a0 = e5m2x2_lo(kw[kk][0]), a1 = e5m2x2_lo(kw[kk][1]);
+        const uint32_t a2 = e5m2x2_hi(kw[kk][0]), a3 = e5m2x2_hi(kw[kk][1]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_f16_16816(s[nt][kk & 1], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+      }
+
+      const bool in0 = t0 + key_a < k1, in1 = t0 + key_a + 8 < k1;
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        // rows: key_a (j = 0, 1) and key_a + 8 (j = 2, 3); columns: queries 2 tq + (j & 1)
+        float v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int key = t0 + warp * 16 + nt * 8 + tq * 2 + (j & 1);
-          const float v = key < k1 ? s[nt][j] * p.scale_log2 : -INFINITY;
-          s[nt][j] = v;
-          if (j < 2)
-            rm0 = fmaxf(rm0, v);
-          else
-            rm1 = fmaxf(rm1, v);
+          const bool in = j < 2 ? in0 : in1;
+          v[j] = in ? (s[nt][0][j] + s[nt][1][j]) * p.scale_log2 : -INFINITY;
         }
-      rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 1));
-      rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 2));
-      rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 1));
-      rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 2));
-      const float mn0 = fmaxf(m0, rm0), mn1 = fmaxf(m1, rm1);
-      const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-      const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float c0 = fast_exp2(m0 - base0), c1 = fast_exp2(m1 - base1);
-      m0 = mn0;
-      m1 = mn1;
-      float ps0 = 0.f, ps1 = 0.f;
+        float rm0 = fmaxf(v[0], v[2]), rm1 = fmaxf(v[1], v[3]);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        s[nt][0] = fast_exp2(s[nt][0] - base0);
-        s[nt][1] = fast_exp2(s[nt][1] - base0);
-        s[nt][2] = fast_exp2(s[nt][2] - base1);
-        s[nt][3] = fast_exp2(s[nt][3] - base1);
-        ps0 += s[nt][0] + s[nt][1];
-        ps1 += s[nt][2] + s[nt][3];
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+          rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, o2));
+          rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, o2));
+        }
+        const float mn0 = fmaxf(m[nt][0], rm0), mn1 = fmaxf(m[nt][1], rm1);
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float c0 = fast_exp2(m[nt][0] - base0), c1 = fast_exp2(m[nt][1] - base1);
+        m[nt][0] = mn0;
+        m[nt][1] = mn1;
+        v[0] = fast_exp2(v[0] - base0);
+        v[2] = fast_exp2(v[2] - base0);
+        v[1] = fast_exp2(v[1] - base1);
+        v[3] = fast_exp2(v[3] - base1);
+        l[nt][0] = l[nt][0] * c0 + v[0] + v[2];
+        l[nt][1] = l[nt][1] * c1 + v[1] + v[3];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          acc[nt][c][0] *= c0;
+          acc[nt][c][2] *= c0;
+          acc[nt][c][1] *= c1;
+          acc[nt][c][3] *= c1;
+        }
+        pb[nt][0] = movmatrix_t(pack_f16(v[0], v[1]));  // keys 2 tq, 2 tq + 1 of query g
+        pb[nt][1] = movmatrix_t(pack_f16(v[2], v[3]));  // keys 8 + 2 tq, 9 + 2 tq
       }
-      l0 = l0 * c0 + ps0;
-      l1 = l1 * c1 + ps1;
+
+      // O^T += V^T P^T
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        acc[n][0] *= c0;
-        acc[n][1] *= c0;
-        acc[n][2] *= c1;
-        acc[n][3] *= c1;
-      }
-      const uint32_t pa0 = pack_f16(s[0][0], s[0][1]);
-      const uint32_t pa1 = pack_f16(s[0][2], s[0][3]);
-      const uint32_t pa2 = pack_f16(s[1][0], s[1][1]);
-      const uint32_t pa3 = pack_f16(s[1][2], s[1][3]);
-      {
-        const int m = lane >> 3;
-        const int r = (m & 1) * 8 + (lane & 7);  // key row within the warp's 16
+      for (int c2 = 0; c2 < NC / 2; ++c2) {
 #pragma unroll
-        for (int n2 = 0; n2 < D / 16; ++n2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vw_addr + r * kF8VPitch + (n2 * 16 + (m >> 1) * 8) * 2, b0, b1, b2, b3);
-          mma_f16_16816(acc[2 * n2], pa0, pa1, pa2, pa3, b0, b1);
-          mma_f16_16816(acc[2 * n2 + 1], pa0, pa1, pa2, pa3, b2, b3);
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t lo = vw[c2][2 * h], hi = vw[c2][2 * h + 1];  // keys 0-7, 8-15
+          const uint32_t a0 = e5m2x2_even(lo), a1 = e5m2x2_odd(lo);
+          const uint32_t a2 = e5m2x2_even(hi), a3 = e5m2x2_odd(hi);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_f16_16816(acc[nt][2 * c2 + h], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
         }
       }
-      __syncwarp();  // the f16 V rows are rewritten for the next tile
     }
     if (!alive) return;
 
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    if (tq == 0) {
-      red_m[warp * 16 + g] = m0;
-      red_m[warp * 16 + g + 8] = m1;
-      red_l[warp * 16 + g] = l0;
-      red_l[warp * 16 + g + 8] = l1;
-    }
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      const int d = n * 8 + tq * 2;
-      if (g < G) {
-        red_o[(warp * G + g) * D + d] = acc[n][0];
-        red_o[(warp * G + g) * D + d + 1] = acc[n][1];
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) l[nt][e] += __shfl_xor_sync(0xffffffffu, l[nt][e], o2);
+      if (g == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          red_m[warp * 16 + nt * 8 + 2 * tq + e] = m[nt][e];
+          red_l[warp * 16 + nt * 8 + 2 * tq + e] = l[nt][e];
+        }
       }
-      if (g + 8 < G) {
-        red_o[(warp * G + g + 8) * D + d] = acc[n][2];
-        red_o[(warp * G + g + 8) * D + d + 1] = acc[n][3];
-      }
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int qr = nt * 8 + 2 * tq + (j & 1);
+          const int d = 16 * c + 2 * g + (j >> 1);
+          if (qr < G) red_o[(warp * G + qr) * D + d] = acc[nt][c][j];
+        }
     }
     compute_bar_sync();
     for (int idx = tid; idx < G * D; idx += kComputeWarps * 32) {
@@ -1349,6 +1371,25 @@ DecodePlan plan_latent(int B, int H, int Lmax) {
   return pl;
 }
 
+template <int NT>
+attn_status_t launch_decode_fp8_nt(const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const GqaParams& p, size_t rows, const DecodePlan& plan,
+                                   float* lse, cudaStream_t st) {
+  constexpr int NST = f8_stages(NT);
+  const int smem = GqaF8Smem<NST>::bytes(p.G);
+  auto kern = gqa_decode_fp8_kernel<NST, NT>;
+  if (!set_smem_attr(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
+  const int items = p.B * p.Hkv * plan.nsplit;
+  kern<<<std::min(items, plan.grid), kThreads, smem, st>>>(tk, tv, p);
+  if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
+  if (plan.nsplit > 1) {
+    combine_kernel<<<static_cast<unsigned>(rows), 128, 0, st>>>(p.ws_o, p.ws_lse, plan.nsplit,
+                                                              kF8D, p.o, lse);
+    return launch_status();
+  }
+  return ATTN_OK;
+}
+
 attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
                                 const int32_t* lens, int Lmax, void* o, float* lse, int B, int Hq,
                                 int Hkv, float scale, const float2* table, void* ws,
@@ -1376,18 +1417,8 @@ attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
   p.nsplit = plan.nsplit;
   p.chunk = plan.chunk;
   p.scale_log2 = scale * 1.4426950408889634f;
-  const int smem = GqaF8Smem::bytes(p.G);
-  auto kern = gqa_decode_fp8_kernel<kF8Stages>;
-  if (!set_smem_attr(reinterpret_cast<const void*>(kern), smem)) return ATTN_ERR_CUDA;
-  const int items = B * Hkv * plan.nsplit;
-  kern<<<std::min(items, plan.grid), kThreads, smem, st>>>(tk, tv, p);
-  if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
-  if (plan.nsplit > 1) {
-    combine_kernel<<<static_cast<unsigned>(rows), 128, 0, st>>>(p.ws_o, p.ws_lse, plan.nsplit, D,
-                                                              p.o, lse);
-    return launch_status();
-  }
-  return ATTN_OK;
+  if (p.G <= 8) return launch_decode_fp8_nt<1>(tk, tv, p, rows, plan, lse, st);
+  return launch_decode_fp8_nt<2>(tk, tv, p, rows, plan, lse, st);
 }
 
 attn_status_t launch_decode(const void* q, const void* k, const void* v, const int32_t* lens,

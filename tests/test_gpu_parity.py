@@ -214,10 +214,16 @@ def test_decode_bf16(B, Hq, Hkv, D, Lmax, lens):
     check(lse.cpu(), rl, LSE_TOL, None, what="LSE")
 
 
-@pytest.mark.parametrize("B,lens", [(1, [2048]), (3, [2048, 1, 777]), (8, 2048), (40, 1500)])
-def test_decode_fp8_cache(B, lens):
+@pytest.mark.parametrize("B,Hq,Hkv,lens", [
+    (1, 32, 8, [2048]), (3, 32, 8, [2048, 1, 777]), (8, 32, 8, 2048), (40, 32, 8, 1500),
+    (2, 8, 8, [5, 2048]),            # group of 1
+    (3, 64, 8, [300, 2048, 64]),     # group of 8: one full column tile
+    (3, 24, 2, [1999, 65, 2048]),    # group of 12: two column tiles, the second ragged
+    (2, 32, 2, [2048, 129]),         # group of 16
+])
+def test_decode_fp8_cache(B, Hq, Hkv, lens):
     """fp8 e5m2 K/V cache (q bf16): the kernel widens the cache exactly, so bf16 bounds hold."""
-    q, kc, vc, cl = synthetic.decode_inputs(B, 32, 8, 2048, 128, lens, seed=B + 50,
+    q, kc, vc, cl = synthetic.decode_inputs(B, Hq, Hkv, 2048, 128, lens, seed=B + Hq + 50,
                                             cache_dtype="fp8")
     o, lse = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda(), want_lse=True)
     status_ok()
