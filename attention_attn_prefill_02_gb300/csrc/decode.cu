@@ -731,7 +731,10 @@ __device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t&
 }
 
 constexpr int kLatMaxB = 2048;  // sequences per call (the tile prefix sums live in smem)
-constexpr int kLatMaxCtas = 128;
+#ifndef ATTN_LAT_MAX_CTAS
+#define ATTN_LAT_MAX_CTAS 128
+#endif
+constexpr int kLatMaxCtas = ATTN_LAT_MAX_CTAS;
 
 struct LatSmem {
   static constexpr int kQOff = kLatStages * kLatTileBytes;
