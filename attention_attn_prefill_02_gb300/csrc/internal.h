@@ -32,9 +32,10 @@ const float2* rope_table_find(int D, float theta, int npos);
 // Encode a 3-D tiled TMA descriptor for a dense row-major tensor of `elem_bytes`-byte elements
 // with logical sizes {inner, mid, outer} (innermost first), box {box_inner, box_mid, 1} and
 // 128-byte swizzling.  Returns false on failure.
+// mid_pitch: rows between consecutive outer indices (0: mid, a dense tensor).
 bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
                   uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid,
-                  int swizzle_bytes);
+                  int swizzle_bytes, uint64_t mid_pitch = 0);
 
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize), done once per (kernel, device, size).
 bool set_smem_attr(const void* kernel, int bytes);
@@ -76,9 +77,12 @@ attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, i
                             float* lse, int B, int H, float scale, const float2* table, void* ws,
                             const DecodePlan& plan, cudaStream_t st);
 
+// S query rows at positions Skv - S .. Skv - 1 against Skv keys (rows kv_pitch apart per head);
+// rope_k: the fused RoPE rotates the keys too (else only the queries).
 attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                              attn_dtype_t dt, float q_scale, float k_scale, float v_scale, int B,
-                             int Hq, int Hkv, int S, int D, int causal, float scale,
-                             const float2* table, int pos0, cudaStream_t st);
+                             int Hq, int Hkv, int S, int Skv, int kv_pitch, int D, int causal,
+                             float scale, const float2* table, int rope_k, int pos0,
+                             cudaStream_t st);
 
 }  // namespace attn

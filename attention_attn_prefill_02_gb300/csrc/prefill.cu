@@ -100,6 +100,9 @@ struct Params {
   float* lse;
   unsigned int* status;
   int B, Hq, Hkv, G, S, causal;
+  int Skv;    // keys (S for self-attention; a chunk's queries see Skv >= S keys)
+  int off;    // absolute position of query row i is i + off (off = Skv - S: bottom-right causal)
+  int rope_k;  // fused RoPE: rotate the K tiles too (0: keys arrive rotated, only q is rotated)
   int n_items, nM, nKV;
   float c_log2;   // softmax_scale * q_scale * k_scale * log2(e)
   float v_scale;
@@ -126,11 +129,12 @@ __device__ __forceinline__ void item_coords(const Params& p, int it, int& m, int
   hq = rest - b * p.Hq;
 }
 
-// KV tiles Q tile starting at row r0 must visit (0 when the tile is past the sequence).
+// KV tiles Q tile starting at row r0 must visit (0 when the tile is past the queries): causal
+// tiles stop at the one holding the key at the tile's last row's position.
 __device__ __forceinline__ int kv_tiles_for(const Params& p, int r0) {
   if (r0 >= p.S) return 0;
   if (!p.causal) return p.nKV;
-  return min(r0 / BN + 1, p.nKV);
+  return min((min(r0 + BM - 1, p.S - 1) + p.off) / BN + 1, p.nKV);
 }
 
 // Serpentine assignment of items to persistent CTAs: round k visits CTAs forwards when k is even
@@ -461,6 +465,10 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         anc_s[q] = make_float2(a.y, a1.y);
         stp_c[q] = make_float2(b.x, b1.x);
         stp_s[q] = make_float2(-b.y, -b1.y);  // negated: see advance()
+        if (!p.rope_k) {  // keys already rotated: the identity (the fp8 tiles still widen)
+          anc_c[q] = stp_c[q] = make_float2(1.f, 1.f);
+          anc_s[q] = stp_s[q] = make_float2(0.f, 0.f);
+        }
       }
     }
     const int c2 = c + kChunks;
@@ -490,9 +498,9 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         }
         uint8_t* tile = smem + C::kKVOff + stage * C::kKVTileBytes;
         const uint8_t* st = smem + C::kKStOff + stage * C::kStTileBytes;  // fp8 staging (STAGED)
-        const int rows_valid = p.S - j * BN;  // rows >= this are past the sequence (zeros)
+        const int rows_valid = p.Skv - j * BN;  // rows >= this are past the keys (zeros)
 #pragma unroll 2
-        for (int k = 0; k < kRowsPer; ++k) {
+        for (int k = 0; k < ((STAGED || p.rope_k) ? kRowsPer : 0); ++k) {
           const int row = g + k * kGroups;
           const uint32_t rsw = static_cast<uint32_t>((row & 7) << 4);
           uint4* p1 = reinterpret_cast<uint4*>(tile + row * 128 + (off1 ^ rsw));
@@ -579,11 +587,11 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
           // rows past S are zero in the staging tile; their table row may not exist: use row 0
           rope_rotate_row_fp8_to_bf16(smem + C::kQStOff + t * C::kStTileBytes,
                                       smem + C::kQOff + t * C::kQTileBytes, lrow,
-                                      p.table + static_cast<size_t>(row < p.S ? p.pos0 + row : 0) * (D / 2));
+                                      p.table + static_cast<size_t>(row < p.S ? p.pos0 + p.off + row : 0) * (D / 2));
         } else {
           if (row < p.S)
             rope_rotate_row<D>(smem + C::kQOff + t * C::kQTileBytes, lrow,
-                               p.table + static_cast<size_t>(p.pos0 + row) * (D / 2));
+                               p.table + static_cast<size_t>(p.pos0 + p.off + row) * (D / 2));
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars->q_ready[t]);
@@ -593,8 +601,9 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
         if (!(ok = mbar_wait(&bars->s_full[t], ph_s, p.status))) break;
         ph_s ^= 1;
         tc_fence_after();
-        const bool need_mask = (p.causal && j == n - 1) || (j * BN + BN > p.S);
-        const int lim = (p.causal ? min(row + 1, p.S) : p.S) - j * BN;  // keys >= lim hidden
+        // a tile is masked where it holds keys past the tile's first row's position, or past Skv
+        const bool need_mask = (p.causal && j * BN + BN - 1 > r0 + p.off) || (j * BN + BN > p.Skv);
+        const int lim = (p.causal ? min(row + p.off + 1, p.Skv) : p.Skv) - j * BN;  // keys >= lim hidden
         float f = 1.f;  // factor for O and l when the running maximum is raised
         if constexpr (ROPE) {
           // two passes over 64-column halves: max of both, then P of the upper half (kept in
@@ -805,8 +814,8 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
 template <int D, bool ROPE, int ESZ>
 attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o, float* lse,
                            float q_scale, float k_scale, float v_scale, int B, int Hq, int Hkv,
-                           int S, int causal, float scale, const float2* table, int pos0,
-                           cudaStream_t st) {
+                           int S, int Skv, int kv_pitch, int causal, float scale,
+                           const float2* table, int rope_k, int pos0, cudaStream_t st) {
   constexpr bool STAGED = ESZ == 1 && ROPE;
   using C = Cfg<D, ESZ, STAGED>;
   // Q / K boxes: as the MMA reads them, or (STAGED) the fp8 staging tiles; V in its own geometry
@@ -814,9 +823,10 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   constexpr int kQKSwz = STAGED ? 128 : C::kSwz;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_3d(&tq, q, ESZ, D, S, static_cast<uint64_t>(B) * Hq, kQKBoxElems, BM, kQKSwz) ||
-      !make_tmap_3d(&tk, k, ESZ, D, S, static_cast<uint64_t>(B) * Hkv, kQKBoxElems, BN, kQKSwz) ||
-      !make_tmap_3d(&tv, v, ESZ, D, S, static_cast<uint64_t>(B) * Hkv, C::kVBoxElems, BN,
-                    C::kVSwz))
+      !make_tmap_3d(&tk, k, ESZ, D, Skv, static_cast<uint64_t>(B) * Hkv, kQKBoxElems, BN, kQKSwz,
+                    kv_pitch) ||
+      !make_tmap_3d(&tv, v, ESZ, D, Skv, static_cast<uint64_t>(B) * Hkv, C::kVBoxElems, BN,
+                    C::kVSwz, kv_pitch))
     return ATTN_ERR_CUDA;
   Params p;
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -827,9 +837,12 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
   p.S = S;
+  p.Skv = Skv;
+  p.off = Skv - S;
+  p.rope_k = rope_k;
   p.causal = causal;
   p.nM = (S + kRowsPerItem - 1) / kRowsPerItem;
-  p.nKV = (S + BN - 1) / BN;
+  p.nKV = (Skv + BN - 1) / BN;
   p.n_items = p.nM * B * Hq;
   p.c_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
   p.v_scale = v_scale;
@@ -846,13 +859,14 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
 
 attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                              attn_dtype_t dt, float q_scale, float k_scale, float v_scale, int B,
-                             int Hq, int Hkv, int S, int D, int causal, float scale,
-                             const float2* table, int pos0, cudaStream_t st) {
+                             int Hq, int Hkv, int S, int Skv, int kv_pitch, int D, int causal,
+                             float scale, const float2* table, int rope_k, int pos0,
+                             cudaStream_t st) {
   const int esz = dt == ATTN_BF16 ? 2 : 1;
 #define ATTN_PREFILL_CASE(DD, RR, EE)                                                          \
   if (D == DD && (table != nullptr) == RR && esz == EE)                                        \
     return launch_typed<DD, RR, EE>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S, \
-                                    causal, scale, table, pos0, st);
+                                    Skv, kv_pitch, causal, scale, table, rope_k, pos0, st);
   ATTN_PREFILL_CASE(128, false, 2)
   ATTN_PREFILL_CASE(128, true, 2)
   ATTN_PREFILL_CASE(64, false, 2)

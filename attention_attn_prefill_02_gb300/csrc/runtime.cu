@@ -163,11 +163,12 @@ EncodeFn encode_fn() {
 
 bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
                   uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid,
-                  int swizzle_bytes) {
+                  int swizzle_bytes, uint64_t mid_pitch) {
   EncodeFn fn = encode_fn();
   if (!fn) return false;
+  if (mid_pitch == 0) mid_pitch = mid;
   cuuint64_t dims[3] = {inner, mid, outer};
-  cuuint64_t strides[2] = {inner * elem_bytes, inner * mid * elem_bytes};
+  cuuint64_t strides[2] = {inner * elem_bytes, inner * mid_pitch * elem_bytes};
   cuuint32_t box[3] = {box_inner, box_mid, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B

@@ -215,6 +215,56 @@ def decode(q, k_cache, v_cache, cache_len, scale=None, rope=True, theta=10000.0)
     return O, LSE
 
 
+def prefill_chunk(q, k, v, skv, scale=None, rope=False, theta=10000.0, pos0=0):
+    """One chunk of a prompt against the keys before it and its own (chunked prefill).
+
+    The prompt is prefilled a chunk at a time into a static cache before decoding (Fixed-budget
+    decode audit — 2026-09-11, "Setup and interpretation").  q [B,Hq,Sq,D]; k, v
+    [B,Hkv,>=skv,D] whose first ``skv`` rows are the keys before the chunk followed by the
+    chunk's own, stored already rotated.  Query row i sits at position skv - Sq + i (rotated at
+    pos0 plus that when ``rope``) and attends keys 0..skv - Sq + i.  Returns (O, LSE).
+    """
+    q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
+    Sq = q.shape[2]
+    assert 1 <= Sq <= skv <= k.shape[2]
+    if rope:
+        q = rope_rotate_half(q, pos0 + skv - Sq + np.arange(Sq), theta)
+    return attention(q, k[:, :, :skv], v[:, :, :skv], causal=True, scale=scale)
+
+
+def decode_append(q, k_cache, v_cache, cache_len, k_new, v_new, scale=None, rope=True,
+                  theta=10000.0):
+    """Decode step that also attends the current token, whose key/value join the cache.
+
+    Sequence b's query and new key sit at position L = cache_len[b]; both are rotated there when
+    ``rope``.  The query attends the L cached keys plus the new one: the plain definition over
+    L + 1 keys (the kernel reaches it by merging the new key into the cached-history result, the
+    merge of ``merge_one_key``).  k_new, v_new [B,Hkv,D].  Returns (O [B,Hq,D], LSE [B,Hq],
+    K_ROW [B,Hkv,D]: the new key as the cache stores it, i.e. rotated).
+    """
+    q, kc, vc, kn, vn = (np.asarray(t, np.float64) for t in (q, k_cache, v_cache, k_new, v_new))
+    lens = np.asarray(cache_len).astype(np.int64)
+    B, Hq, D = q.shape
+    O = np.empty((B, Hq, vc.shape[-1]))
+    LSE = np.empty((B, Hq))
+    K_ROW = np.empty(kn.shape)
+    for b in range(B):
+        L = int(lens[b])
+        assert 0 <= L < kc.shape[2]
+        kr = kn[b][:, None, :]  # [Hkv, 1, D]
+        qb = q[b][:, None, :]
+        if rope:
+            kr = rope_rotate_half(kr, np.array([L]), theta)
+            qb = rope_rotate_half(qb, np.array([L]), theta)
+        K_ROW[b] = kr[:, 0]
+        keys = np.concatenate([kc[b, :, :L], kr], axis=1)
+        vals = np.concatenate([vc[b, :, :L], vn[b][:, None, :]], axis=1)
+        o, lse = attention(qb[None], keys[None], vals[None], causal=False, scale=scale)
+        O[b] = o[0, :, 0]
+        LSE[b] = lse[0, :, 0]
+    return O, LSE, K_ROW
+
+
 def latent_decode(q, c_cache, cache_len, scale=None, rope=True, theta=10000.0,
                   d_latent=LATENT_DIM, d_rope=LATENT_ROPE_DIM):
     """Absorbed latent (MLA-style) decode.

@@ -230,10 +230,61 @@ def pin_merge_identity(merge=O.merge_one_key, combine=O.combine_partials):
     np.testing.assert_allclose(o_c, op[0], atol=0)
 
 
+def pin_chunk_equals_prompt_rows(chunk=O.prefill_chunk):
+    """A chunk of queries against a cache equals the same rows of the whole-prompt prefill.
+
+    The cache holds the keys rotated at their positions, as a decode cache stores them; rows
+    past ``skv`` hold huge values that no chunk may touch.  Chunks of 1 and 32 rows (the audit's
+    chunk size), ragged ones, and the whole prompt as one chunk.
+    """
+    B, Hq, Hkv, S, D, theta = 2, 4, 2, 45, 8, 500.0
+    q, k, v = rnd(B, Hq, S, D), rnd(B, Hkv, S, D), rnd(B, Hkv, S, D)
+    full_o, full_l = O.prefill(q, k, v, causal=True, rope=True, theta=theta)
+    kc = np.full((B, Hkv, S + 7, D), 1e6)
+    vc = np.full((B, Hkv, S + 7, D), -1e6)
+    kc[:, :, :S] = O.rope_rotate_half(k, np.arange(S), theta)
+    vc[:, :, :S] = v
+    for sq, skv in [(32, 32), (32, 45), (1, 45), (13, 20), (45, 45), (1, 1)]:
+        o, l = chunk(q[:, :, skv - sq: skv], kc, vc, skv, rope=True, theta=theta)
+        np.testing.assert_allclose(o, full_o[:, :, skv - sq: skv], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l, full_l[:, :, skv - sq: skv], rtol=0, atol=1e-12)
+
+
+def pin_append_equals_longer_prompt(append=O.decode_append, merge=O.merge_one_key):
+    """A decode step that appends its token equals the last row of a prefill over the L + 1
+    tokens, and equals the cached-history decode with the new key merged in by the sigmoid
+    identity (Fixed-budget decode audit — 2026-09-11, "A: group-entry queries and one joint
+    history scan")."""
+    B, Hq, Hkv, Lmax, D, theta = 3, 4, 2, 30, 8, 10000.0
+    G = Hq // Hkv
+    lens = np.array([29, 1, 12])
+    q, k_raw, v = rnd(B, Hq, D), rnd(B, Hkv, Lmax, D), rnd(B, Hkv, Lmax, D)
+    k_new, v_new = rnd(B, Hkv, D), rnd(B, Hkv, D)
+    kc = O.rope_rotate_half(k_raw, np.arange(Lmax), theta)
+    o, lse, krow = append(q, kc, v, lens, k_new, v_new, rope=True, theta=theta)
+    o_h, lse_h = O.decode(q, kc, v, lens, rope=True, theta=theta)
+    for b in range(B):
+        L = int(lens[b])
+        qp = np.zeros((1, Hq, L + 1, D))
+        qp[0, :, L] = q[b]
+        kp = np.concatenate([k_raw[b, :, :L], k_new[b][:, None]], axis=1)[None]
+        vp = np.concatenate([v[b, :, :L], v_new[b][:, None]], axis=1)[None]
+        ref_o, ref_l = O.prefill(qp, kp, vp, causal=True, rope=True, theta=theta)
+        np.testing.assert_allclose(o[b], ref_o[0, :, L], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[b], ref_l[0, :, L], rtol=0, atol=1e-12)
+        for hq in range(Hq):
+            qr = O.rope_rotate_half(q[b, hq][None], np.array([L]), theta)[0]
+            s_cur = float(qr @ krow[b, hq // G]) / math.sqrt(D)
+            mo, ml = merge(o_h[b, hq], lse_h[b, hq], s_cur, v_new[b, hq // G])
+            np.testing.assert_allclose(o[b, hq], mo, rtol=0, atol=1e-12)
+            assert abs(lse[b, hq] - ml) < 1e-12
+
+
 ALL_PINS = [pin_softmax_sums_to_one, pin_zero_query_is_causal_mean, pin_hand_two_key_case,
             pin_one_hot_and_single_key, pin_causal_ignores_future, pin_matches_torch_sdpa,
             pin_bruteforce_enumeration, pin_gqa_equals_repeated_mha, pin_rope,
-            pin_latent_absorbed_equals_explicit, pin_merge_identity]
+            pin_latent_absorbed_equals_explicit, pin_merge_identity,
+            pin_chunk_equals_prompt_rows, pin_append_equals_longer_prompt]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -421,3 +472,35 @@ def test_planted_merge_mistake_is_caught():
 
     assert _fails_some([pin_merge_identity], merge=bad_merge)
     assert _fails_some([pin_merge_identity], combine=bad_combine)
+
+
+def test_planted_chunk_and_append_mistakes_are_caught():
+    """Queries rotated from position 0 instead of their place after the cache, a mask aligned
+    top-left, and an appended key left unrotated all fail the pins."""
+    def chunk_pos0(q, k, v, skv, scale=None, rope=False, theta=10000.0, pos0=0):
+        qq = O.rope_rotate_half(np.asarray(q, np.float64), pos0 + np.arange(q.shape[2]), theta)
+        return O.attention(qq, k[:, :, :skv], v[:, :, :skv], causal=True, scale=scale)
+
+    def chunk_topleft(q, k, v, skv, scale=None, rope=False, theta=10000.0, pos0=0):
+        sq = q.shape[2]
+        qq = O.rope_rotate_half(np.asarray(q, np.float64), pos0 + skv - sq + np.arange(sq), theta)
+        return O.attention(qq, k[:, :, :skv], v[:, :, :skv], causal=True, scale=scale,
+                           q_pos=np.arange(sq))
+
+    def append_unrotated(q, k_cache, v_cache, cache_len, k_new, v_new, scale=None, rope=True,
+                         theta=10000.0):
+        # the new key joins the cache as given instead of rotated at position L
+        B, Hq, D = q.shape
+        o_all, l_all = np.empty((B, Hq, D)), np.empty((B, Hq))
+        for b in range(B):
+            L = int(cache_len[b])
+            qb = O.rope_rotate_half(np.asarray(q[b])[:, None], np.array([L]), theta)
+            keys = np.concatenate([k_cache[b, :, :L], np.asarray(k_new[b])[:, None]], 1)
+            vals = np.concatenate([v_cache[b, :, :L], np.asarray(v_new[b])[:, None]], 1)
+            o, l = O.attention(qb[None], keys[None], vals[None], causal=False, scale=scale)
+            o_all[b], l_all[b] = o[0, :, 0], l[0, :, 0]
+        return o_all, l_all, np.asarray(k_new)
+
+    assert _fails_some([pin_chunk_equals_prompt_rows], chunk=chunk_pos0)
+    assert _fails_some([pin_chunk_equals_prompt_rows], chunk=chunk_topleft)
+    assert _fails_some([pin_append_equals_longer_prompt], append=append_unrotated)
