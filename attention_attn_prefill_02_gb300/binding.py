@@ -48,6 +48,9 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.rope_apply.argtypes = [vp, vp, i, i, i, i, i, i, f, vp]
     L.attn_prefill.restype = i
     L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i, f, f, f, i, i, i, i, i, i, f, i, f, i, vp]
+    L.attn_prefill_chunk.restype = i
+    L.attn_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, i, f, f, f, i, i, i, i, i, i, i, f, i, f,
+                                     i, vp]
     L.attn_decode_workspace_size.restype = sz
     L.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
     L.attn_decode.restype = i
@@ -114,6 +117,26 @@ def attn_prefill(q, k, v, causal=True, softmax_scale=0.0, rope=False, rope_theta
                               float(v_scale), B, Hq, Hkv, S, D, int(bool(causal)),
                               float(softmax_scale), int(bool(rope)), float(rope_theta), int(pos0),
                               _stream(stream)), "attn_prefill")
+    return (o, lse) if (want_lse or lse is not None) else o
+
+
+def attn_prefill_chunk(q, k_cache, v_cache, skv, softmax_scale=0.0, rope=True,
+                       rope_theta=10000.0, pos0=0, o=None, lse=None, want_lse=False, q_scale=1.0,
+                       k_scale=1.0, v_scale=1.0, stream=None):
+    """O [B,Hq,Sq,D] bf16 for a chunk q [B,Hq,Sq,D] whose rows are the last Sq of `skv` tokens,
+    against the first `skv` rows of the caches [B,Hkv,Lmax,D] (keys stored rotated)."""
+    _require_cuda(q, k_cache, v_cache, o, lse)
+    B, Hq, Sq, D = q.shape
+    Hkv, pitch = k_cache.shape[1], k_cache.shape[2]
+    if o is None:
+        o = torch.empty((B, Hq, Sq, D), dtype=torch.bfloat16, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check(lib().attn_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
+                                    DTYPE_CODES[q.dtype], float(q_scale), float(k_scale),
+                                    float(v_scale), B, Hq, Hkv, Sq, int(skv), pitch, D,
+                                    float(softmax_scale), int(bool(rope)), float(rope_theta),
+                                    int(pos0), _stream(stream)), "attn_prefill_chunk")
     return (o, lse) if (want_lse or lse is not None) else o
 
 

@@ -1,6 +1,7 @@
 // api.cpp — the C ABI: argument validation, workspace planning and dispatch to the kernels.
 // Validation happens entirely on the host before anything is enqueued, so an invalid call
 // returns its status without touching the GPU (this is what the CPU-only tests exercise).
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -82,12 +83,45 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   if (st != ATTN_OK) return st;
   const float2* tab = nullptr;
   if (rope) {
-    tab = rope_table(D, rope_theta, pos0 + S, &st);
+    // the fused K rotation starts every thread's recurrence from rows pos0 .. pos0 + 31
+    tab = rope_table(D, rope_theta, pos0 + std::max(S, 128), &st);
     if (!tab) return st;
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  return launch_prefill(q, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, S, D,
-                        causal, scale, tab, pos0, as_stream(stream));
+  return launch_prefill(q, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, S, S, S,
+                        D, causal, scale, tab, 1, pos0, as_stream(stream));
+}
+
+attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 attn_dtype_t dtype, float q_scale, float k_scale, float v_scale,
+                                 int B, int Hq, int Hkv, int Sq, int Skv, int kv_pitch, int D,
+                                 float softmax_scale, int rope, float rope_theta, int pos0,
+                                 attn_stream_t stream) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (Sq < 1 || Skv < Sq || kv_pitch < Skv) return ATTN_ERR_INVALID_ARG;
+  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  if (rope && (!finite_pos(rope_theta) || pos0 < 0)) return ATTN_ERR_INVALID_ARG;
+  if (!finite_pos(q_scale) || !finite_pos(k_scale) || !finite_pos(v_scale))
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(kv_pitch) > (1LL << 30) || static_cast<long long>(B) * Hq > (1LL << 24))
+    return ATTN_ERR_UNSUPPORTED;
+  if (rope && dtype == ATTN_FP8_E5M2 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  const float2* tab = nullptr;
+  if (rope) {
+    tab = rope_table(D, rope_theta, pos0 + std::max(Skv, 128), &st);
+    if (!tab) return st;
+  }
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return launch_prefill(q, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, Sq, Skv,
+                        kv_pitch, D, 1, scale, tab, 0, pos0, as_stream(stream));
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int Lmax) {

@@ -4,6 +4,7 @@
  * Four operations, all from the pages' problem statement of LLM-serving attention:
  *   rope_apply          rotary position embedding on a [B,H,S,D] tensor
  *   attn_prefill        causal / non-causal grouped-query attention, RoPE optionally fused
+ *   attn_prefill_chunk  a prompt chunk against a static cache (bottom-right causal)
  *   attn_decode         one query token per sequence against a static KV cache (split-KV)
  *   attn_decode_latent  absorbed latent (MLA-style) decode: 448 latent + 64 RoPE dims
  *
@@ -106,6 +107,30 @@ ATTN_API attn_status_t attn_prefill(const void* q, const void* k, const void* v,
                            attn_dtype_t dtype, float q_scale, float k_scale, float v_scale,
                            int B, int Hq, int Hkv, int S, int D, int causal, float softmax_scale,
                            int rope, float rope_theta, int pos0, attn_stream_t stream);
+
+/*
+ * attn_prefill_chunk — one chunk of a prompt against a static cache (chunked prefill).
+ * Defines: filling a static cache a chunk at a time before the decode steps (Fixed-budget
+ * decode audit — 2026-09-11, "Setup and interpretation": chunked prefill with chunks of 32).
+ * The chunk's Sq queries are the last Sq of Skv tokens: query row i sits at position
+ * Skv - Sq + i and attends keys 0 .. Skv - Sq + i (causal, aligned at the bottom-right corner
+ * of the Sq x Skv score matrix; Sq == Skv is the ordinary causal prefill).
+ *   q        [B,Hq,Sq,D] (dtype `dtype`).
+ *   k, v     the first Skv rows of [B,Hkv,kv_pitch,D]: a cache of kv_pitch >= Skv rows per
+ *            head holding the keys before the chunk followed by the chunk's own.  Keys are used
+ *            as stored (a cache holds them already rotated); rows >= Skv are never read.
+ *   o        [B,Hq,Sq,D] bfloat16.   lse  NULL or [B,Hq,Sq] float32 (natural log).
+ *   rope     1: q rotated inside the kernel at positions pos0 + Skv - Sq + i; 0: q as given.
+ *   1 <= Sq <= Skv <= kv_pitch; D in {64, 128} (fp8 with rope = 1: D = 128); the other
+ *   arguments as attn_prefill.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+ATTN_API attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, void* o,
+                                          float* lse, attn_dtype_t dtype, float q_scale,
+                                          float k_scale, float v_scale, int B, int Hq, int Hkv,
+                                          int Sq, int Skv, int kv_pitch, int D,
+                                          float softmax_scale, int rope, float rope_theta,
+                                          int pos0, attn_stream_t stream);
 
 /*
  * attn_decode_workspace_size — bytes of device workspace attn_decode needs for these sizes

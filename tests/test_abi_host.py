@@ -99,6 +99,24 @@ def test_prefill_validation(L):
     assert _prefill(L, D=256) == UNSUPPORTED
 
 
+def _chunk(L, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE2, lse=None, dt=0, qs=1.0, ks=1.0, vs=1.0, B=1,
+                Hq=4, Hkv=1, Sq=32, Skv=300, pitch=320, D=128, scale=0.0, rope=1, theta=1e4,
+                pos0=0)
+    args.update(kw)
+    return L.attn_prefill_chunk(*args.values(), _stream())
+
+
+def test_prefill_chunk_validation(L):
+    assert _chunk(L, Sq=0) == INVALID
+    assert _chunk(L, Sq=301) == INVALID               # more queries than keys
+    assert _chunk(L, pitch=299) == INVALID            # keys past the cache rows
+    assert _chunk(L, Hq=6, Hkv=4) == INVALID
+    assert _chunk(L, v=MIS) == INVALID
+    assert _chunk(L, D=96) == UNSUPPORTED
+    assert _chunk(L, dt=1, D=64) == UNSUPPORTED       # fp8 with q RoPE: D = 128 only
+
+
 def _decode(L, **kw):
     args = dict(q=FAKE, k=FAKE, v=FAKE, lens=FAKE2, Lmax=2048, o=FAKE2, lse=None, dt=0, B=1,
                 Hq=32, Hkv=8, D=128, scale=0.0, rope=1, theta=1e4, ws=FAKE2, wsb=1 << 30)
@@ -146,6 +164,7 @@ def test_workspace_sizes_are_consistent(L):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_valid_calls_report_no_device_without_gpu(L):
     assert _prefill(L) == NO_DEVICE
+    assert _chunk(L) == NO_DEVICE
     assert _decode(L) == NO_DEVICE
     assert _decode(L, ws=None, wsb=0) in (NO_DEVICE, WORKSPACE)
     assert _latent(L) == NO_DEVICE

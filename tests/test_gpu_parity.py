@@ -244,6 +244,45 @@ def test_decode_bad_cache_len_sets_status():
 
 
 # --------------------------------------------------------------------------------------------
+# chunked prefill against a static cache
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,D,Hq,Hkv,Sq,Skv,pitch,rope", [
+    ("bf16", 128, 8, 2, 32, 300, 320, True),     # a 32-row chunk, offset not a tile multiple
+    ("bf16", 128, 8, 2, 1, 257, 257, True),      # one row after a ragged cache
+    ("bf16", 128, 4, 1, 200, 700, 704, True),    # two query tiles, a partial item
+    ("bf16", 128, 8, 2, 384, 384, 512, True),    # the whole prompt as one chunk
+    ("bf16", 128, 8, 2, 96, 1000, 1000, False),
+    ("bf16", 64, 8, 8, 64, 1000, 1024, True),
+    ("fp8", 128, 8, 2, 128, 513, 640, True),     # fp8: rotated q in bf16, keys widened as stored
+    ("fp8", 64, 4, 4, 50, 333, 333, False),
+])
+def test_prefill_chunk(dtype, D, Hq, Hkv, Sq, Skv, pitch, rope):
+    B = 2
+    q = synthetic.normal((B, Hq, Sq, D), 900 + Sq, dtype)
+    kc = synthetic.normal((B, Hkv, pitch, D), 901 + Skv, dtype)
+    vc = synthetic.normal((B, Hkv, pitch, D), 902 + Skv, dtype)
+    o, lse = binding.attn_prefill_chunk(q.cuda(), kc.cuda(), vc.cuda(), Skv, rope=rope,
+                                        rope_theta=10000.0, want_lse=True)
+    status_ok()
+    ro, rl = oracle.prefill_chunk(f64(q), f64(kc), f64(vc), Skv, rope=rope, theta=10000.0)
+    if dtype == "fp8":
+        check(o.cpu(), ro, FP8_MAX, 1e-2, what="O chunk fp8")
+    else:
+        check(o.cpu(), ro, what="O chunk")
+    check(lse.cpu(), rl, 2e-2 if dtype == "fp8" else LSE_TOL, None, what="LSE chunk")
+
+
+def test_prefill_chunk_rejects_bad_lengths():
+    q = torch.zeros((1, 4, 8, 64), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((1, 4, 16, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.AttnError):
+        binding.attn_prefill_chunk(q, kc, kc, 7)      # Sq > Skv
+    with pytest.raises(binding.AttnError):
+        binding.attn_prefill_chunk(q, kc, kc, 17)     # Skv > cache rows
+
+
+# --------------------------------------------------------------------------------------------
 # latent decode
 # --------------------------------------------------------------------------------------------
 
