@@ -57,6 +57,11 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_decode.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp, sz, vp]
     L.attn_decode_noalloc.restype = i
     L.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp]
+    L.attn_decode_append_workspace_size.restype = sz
+    L.attn_decode_append_workspace_size.argtypes = [i, i, i, i, i]
+    L.attn_decode_append.restype = i
+    L.attn_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f,
+                                     vp, sz, vp]
     L.attn_decode_latent_workspace_size.restype = sz
     L.attn_decode_latent_workspace_size.argtypes = [i, i, i]
     L.attn_decode_latent.restype = i
@@ -181,6 +186,35 @@ def attn_decode_noalloc(q, k_cache, v_cache, cache_len, o=None, lse=None, want_l
                                      Lmax, _ptr(o), _ptr(lse), DTYPE_CODES[k_cache.dtype], B, Hq, Hkv,
                                      D, float(softmax_scale), int(bool(rope)), float(rope_theta),
                                      _stream(stream)), "attn_decode_noalloc")
+    return (o, lse) if (want_lse or lse is not None) else o
+
+
+def attn_decode_append_workspace_size(B, Hq, Hkv, D, Lmax):
+    return int(lib().attn_decode_append_workspace_size(B, Hq, Hkv, D, Lmax))
+
+
+def attn_decode_append(q, k_new, v_new, k_cache, v_cache, cache_len, o=None, lse=None,
+                       want_lse=False, softmax_scale=0.0, rope=True, rope_theta=10000.0,
+                       workspace=None, stream=None):
+    """One growing-decode step: O [B,Hq,D] over the cache rows 0..L-1 plus the current token,
+    whose key/value are written to row L = cache_len[b]; cache_len is incremented on device."""
+    _require_cuda(q, k_new, v_new, k_cache, v_cache, cache_len, o, lse, workspace)
+    B, Hq, D = q.shape
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    if o is None:
+        o = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(attn_decode_append_workspace_size(B, Hq, Hkv, D, Lmax),
+                                dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    _check(lib().attn_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                    _ptr(v_cache), _ptr(cache_len), Lmax, _ptr(o), _ptr(lse),
+                                    DTYPE_CODES[k_cache.dtype], B, Hq, Hkv, D,
+                                    float(softmax_scale), int(bool(rope)), float(rope_theta),
+                                    _ptr(workspace), wbytes, _stream(stream)),
+           "attn_decode_append")
     return (o, lse) if (want_lse or lse is not None) else o
 
 

@@ -168,6 +168,47 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
                        workspace, plan, as_stream(stream));
 }
 
+size_t attn_decode_append_workspace_size(int B, int Hq, int Hkv, int D, int Lmax) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 2 || (D != 64 && D != 128) || Hq % Hkv) return 0;
+  return append_ws_bytes(plan_decode(B, Hq, Hkv, D, Lmax), B, Hq);
+}
+
+attn_status_t attn_decode_append(const void* q, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, int32_t* cache_len, int Lmax,
+                                 void* o, float* lse, attn_dtype_t dtype, int B, int Hq, int Hkv,
+                                 int D, float softmax_scale, int rope, float rope_theta,
+                                 void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !cache_len || !o || !workspace)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace))
+    return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cache_len) & 3u) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 2 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(Lmax) > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  const DecodePlan plan = plan_decode(B, Hq, Hkv, D, Lmax);
+  if (workspace_bytes < append_ws_bytes(plan, B, Hq)) return ATTN_ERR_WORKSPACE;
+  const float2* tab = nullptr;
+  if (rope) {
+    tab = rope_table(D, rope_theta, Lmax + 1, &st);
+    if (!tab) return st;
+  }
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return launch_decode_append(q, k_new, v_new, k_cache, v_cache, cache_len, Lmax, o, lse, B, Hq,
+                              Hkv, D, scale, tab, workspace, plan, as_stream(stream));
+}
+
 size_t attn_decode_latent_workspace_size(int B, int H, int Lmax) {
   if (B < 1 || H < 1 || H > 16 || Lmax < 1) return 0;
   return plan_latent(B, H, Lmax).ws_bytes;

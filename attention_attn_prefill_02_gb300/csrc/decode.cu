@@ -1424,6 +1424,128 @@ attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
   return launch_decode_fp8_nt<2>(tk, tv, p, rows, plan, lse, st);
 }
 
+// ------------------------------------------------------------------------------------------------
+// Decode with the current token appended: after the history decode (keys 0..L-1), the current
+// token's key (rotated at position L) and value are written to cache row L, and every query row
+// of the group merges that one key into its history result (Fixed-budget decode audit —
+// 2026-09-11, "A: group-entry queries and one joint history scan": the weight of the current
+// token is the logistic function of its score minus the history's log-sum-exp, the history
+// output takes the rest).  The query and the new key are rounded to bf16 after rotation, as the
+// history decode and the cache hold them.  One block per (sequence, KV head).
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kAppendThreads = 128;
+
+template <int D>
+__global__ void __launch_bounds__(kAppendThreads)
+    append_merge_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
+                        const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* k_cache,
+                        __nv_bfloat16* v_cache, const int32_t* __restrict__ lens, int Lmax,
+                        __nv_bfloat16* o, const float* __restrict__ lse_hist, float* lse_out,
+                        int Hq, int Hkv, float scale, const float2* __restrict__ table,
+                        unsigned int* status) {
+  __shared__ float kr[D];
+  __shared__ float red[kAppendThreads / 32];
+  const int b = blockIdx.x, kvh = blockIdx.y, tid = threadIdx.x;
+  const int G = Hq / Hkv;
+  const int L = lens[b];
+  if (L < 1 || L >= Lmax) {  // no history, or no row left for the new token
+    if (tid == 0 && kvh == 0) report_status(status, ATTN_ERR_DEVICE_ARG);
+    return;
+  }
+  const size_t kv = static_cast<size_t>(b) * Hkv + kvh;
+  const size_t crow = (kv * Lmax + L) * D;
+  for (int i = tid; i < D / 2; i += kAppendThreads) {
+    float x1 = __bfloat162float(k_new[kv * D + i]);
+    float x2 = __bfloat162float(k_new[kv * D + i + D / 2]);
+    if (table) {
+      const float2 cs = table[static_cast<size_t>(L) * (D / 2) + i];
+      const float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
+      x1 = y1;
+      x2 = y2;
+    }
+    const __nv_bfloat16 r1 = __float2bfloat16_rn(x1), r2 = __float2bfloat16_rn(x2);
+    k_cache[crow + i] = r1;
+    k_cache[crow + i + D / 2] = r2;
+    kr[i] = __bfloat162float(r1);
+    kr[i + D / 2] = __bfloat162float(r2);
+  }
+  for (int d = tid; d < D; d += kAppendThreads) v_cache[crow + d] = v_new[kv * D + d];
+  __syncthreads();
+  for (int g = 0; g < G; ++g) {
+    const size_t row = static_cast<size_t>(b) * Hq + kvh * G + g;
+    float part = 0.f;
+    for (int i = tid; i < D / 2; i += kAppendThreads) {
+      float x1 = __bfloat162float(q[row * D + i]);
+      float x2 = __bfloat162float(q[row * D + i + D / 2]);
+      if (table) {
+        const float2 cs = table[static_cast<size_t>(L) * (D / 2) + i];
+        const float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
+        x1 = y1;
+        x2 = y2;
+      }
+      x1 = __bfloat162float(__float2bfloat16_rn(x1));
+      x2 = __bfloat162float(__float2bfloat16_rn(x2));
+      part = fmaf(x1, kr[i], fmaf(x2, kr[i + D / 2], part));
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+    if ((tid & 31) == 0) red[tid >> 5] = part;
+    __syncthreads();
+    float sc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAppendThreads / 32; ++w) sc += red[w];
+    sc *= scale;
+    const float lh = lse_hist[row];
+    const float a = 1.f / (1.f + expf(lh - sc));  // weight of the current token
+    for (int d = tid; d < D; d += kAppendThreads) {
+      const float oh = __bfloat162float(o[row * D + d]);
+      o[row * D + d] = __float2bfloat16_rn(fmaf(a, __bfloat162float(v_new[kv * D + d]) - oh, oh));
+    }
+    if (lse_out && tid == 0) lse_out[row] = fmaxf(lh, sc) + log1pf(expf(-fabsf(sc - lh)));
+    __syncthreads();  // red is rewritten for the next query head
+  }
+}
+
+// cache_len[b] += 1 where the append wrote a row (after every block of the merge has read it).
+__global__ void append_len_kernel(int32_t* lens, int B, int Lmax) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) {
+    const int L = lens[b];
+    if (L >= 1 && L < Lmax) lens[b] = L + 1;
+  }
+}
+
+attn_status_t launch_decode_append(const void* q, const void* k_new, const void* v_new,
+                                   void* k_cache, void* v_cache, int32_t* lens, int Lmax,
+                                   void* o, float* lse, int B, int Hq, int Hkv, int D,
+                                   float scale, const float2* table, void* ws,
+                                   const DecodePlan& plan, cudaStream_t st) {
+  // workspace: the history decode's own part, then the history LSE [B*Hq] (natural log)
+  float* lse_hist = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + append_ws_offset(plan));
+  attn_status_t r = launch_decode(q, k_cache, v_cache, lens, Lmax, o, lse_hist, B, Hq, Hkv, D,
+                                  scale, table, plan.ws_bytes ? ws : nullptr, plan, st);
+  if (r != ATTN_OK) return r;
+  const dim3 grid(B, Hkv);
+  const auto* qq = static_cast<const __nv_bfloat16*>(q);
+  const auto* kn = static_cast<const __nv_bfloat16*>(k_new);
+  const auto* vn = static_cast<const __nv_bfloat16*>(v_new);
+  auto* kc = static_cast<__nv_bfloat16*>(k_cache);
+  auto* vc = static_cast<__nv_bfloat16*>(v_cache);
+  auto* oo = static_cast<__nv_bfloat16*>(o);
+  if (D == 128)
+    append_merge_kernel<128><<<grid, kAppendThreads, 0, st>>>(qq, kn, vn, kc, vc, lens, Lmax, oo,
+                                                              lse_hist, lse, Hq, Hkv, scale,
+                                                              table, device_status_ptr());
+  else
+    append_merge_kernel<64><<<grid, kAppendThreads, 0, st>>>(qq, kn, vn, kc, vc, lens, Lmax, oo,
+                                                             lse_hist, lse, Hq, Hkv, scale,
+                                                             table, device_status_ptr());
+  if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
+  append_len_kernel<<<(B + 255) / 256, 256, 0, st>>>(lens, B, Lmax);
+  return launch_status();
+}
+
 attn_status_t launch_decode(const void* q, const void* k, const void* v, const int32_t* lens,
                             int Lmax, void* o, float* lse, int B, int Hq, int Hkv, int D,
                             float scale, const float2* table, void* ws, const DecodePlan& plan,

@@ -61,6 +61,17 @@ struct DecodePlan {
   size_t ws_bytes; // partial O (fp32) + partial LSE (fp32)
 };
 DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int Lmax);
+
+// Append decode workspace: the decode's own (rounded up to 256 bytes), then B*Hq floats.
+inline size_t append_ws_offset(const DecodePlan& pl) { return (pl.ws_bytes + 255) & ~size_t(255); }
+inline size_t append_ws_bytes(const DecodePlan& pl, int B, int Hq) {
+  return append_ws_offset(pl) + static_cast<size_t>(B) * Hq * sizeof(float);
+}
+attn_status_t launch_decode_append(const void* q, const void* k_new, const void* v_new,
+                                   void* k_cache, void* v_cache, int32_t* lens, int Lmax,
+                                   void* o, float* lse, int B, int Hq, int Hkv, int D,
+                                   float scale, const float2* table, void* ws,
+                                   const DecodePlan& plan, cudaStream_t st);
 DecodePlan plan_latent(int B, int H, int Lmax);
 
 attn_status_t launch_decode(const void* q, const void* k, const void* v, const int32_t* lens,

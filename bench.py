@@ -346,6 +346,53 @@ def variants(b, d):
     out["decode_fp8_cache_b128"] = {"graph_ms": round(tg, 5), "gbs": round(nbytes / tg / 1e6, 1),
                                     "frac_of_hbm": round(nbytes / tg / 1e6 / measured_peaks()[0], 4)}
     del q, kc, vc, cl, o
+    # growing decode: one CUDA graph of an append step (history decode + current-token merge +
+    # cache write + length increment) replayed while the cache grows; lengths live on the
+    # device, so the same graph serves every step
+    B, L0, steps = 128, Dd["L"], 64
+    Lmax = L0 + steps
+    q, kc, vc, cl = synthetic.decode_inputs(B, Dd["Hq"], Dd["Hkv"], Lmax, Dd["D"], L0, seed=7)
+    kn = synthetic.normal((B, Dd["Hkv"], Dd["D"]), 7077)
+    vn = synthetic.normal((B, Dd["Hkv"], Dd["D"]), 7078)
+    q, kc, vc, cl0, kn, vn = q.cuda(), kc.cuda(), vc.cuda(), cl.cuda(), kn.cuda(), vn.cuda()
+    cl = cl0.clone()
+    o = torch.empty((B, Dd["Hq"], Dd["D"]), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(b.attn_decode_append_workspace_size(B, Dd["Hq"], Dd["Hkv"], Dd["D"], Lmax),
+                     dtype=torch.uint8, device="cuda")
+    b.attn_rope_table_reserve(Dd["D"], THETA, Lmax + 1)
+
+    def step():
+        b.attn_decode_append(q, kn, vn, kc, vc, cl, o=o, rope=True, rope_theta=THETA, workspace=ws)
+
+    def run(fn):
+        cl.copy_(cl0)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(steps):
+            fn()
+        s1.record()
+        torch.cuda.synchronize()
+        assert int(cl.min()) == Lmax and int(cl.max()) == Lmax  # every step appended one row
+        return s0.elapsed_time(s1) / steps
+
+    step()  # warm-up (then the lengths are reset by run)
+    te = run(step)
+    gs = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
+        with torch.cuda.graph(g, stream=gs):
+            b.attn_decode_append(q, kn, vn, kc, vc, cl, o=o, rope=True, rope_theta=THETA,
+                                 workspace=ws, stream=gs)
+    torch.cuda.current_stream().wait_stream(gs)
+    tg = run(g.replay)
+    nbytes = workload.decode_bytes(B, Dd["Hq"], Dd["Hkv"], L0 + steps // 2, Dd["D"])
+    out["decode_growing_b128"] = {
+        "steps": steps, "L": f"{L0}..{Lmax - 1}", "eager_ms_per_step": round(te, 5),
+        "graph_ms_per_step": round(tg, 5), "graph_gbs": round(nbytes / tg / 1e6, 1),
+        "launches_per_step": 3}
+    del q, kc, vc, cl, cl0, kn, vn, o, ws
     return out
 
 

@@ -6,6 +6,7 @@
  *   attn_prefill        causal / non-causal grouped-query attention, RoPE optionally fused
  *   attn_prefill_chunk  a prompt chunk against a static cache (bottom-right causal)
  *   attn_decode         one query token per sequence against a static KV cache (split-KV)
+ *   attn_decode_append  a decode step whose token joins the cache (growing decode)
  *   attn_decode_latent  absorbed latent (MLA-style) decode: 448 latent + 64 RoPE dims
  *
  * Conventions shared by every call
@@ -190,6 +191,39 @@ ATTN_API attn_status_t attn_decode_noalloc(const void* q, const void* k_cache, c
                                   attn_dtype_t dtype, int B, int Hq, int Hkv, int D,
                                   float softmax_scale, int rope, float rope_theta,
                                   attn_stream_t stream);
+
+/*
+ * attn_decode_append — one decode step whose token joins the cache (growing decode).
+ * Defines: the decode steps of a static append cache that grows by one row per step, run as
+ * growing CUDA graphs (Fixed-budget decode audit — 2026-09-11, "Which implementation was
+ * tested" and "Setup and interpretation"), with the current token merged into the
+ * cached-history result ("A: group-entry queries and one joint history scan": the current
+ * token's weight is the logistic function of its score minus the history log-sum-exp).
+ * Sequence b's query and new key sit at position L = cache_len[b] (read on the device):
+ *   1. the history: attn_decode of q over cache rows 0 .. L-1;
+ *   2. k_new rotated at L (when rope = 1) and v_new are written to cache row L (bf16), and each
+ *      query row merges that key into its history output;
+ *   3. cache_len[b] becomes L + 1.
+ * The result is attention over the L + 1 keys.  Because positions and lengths live on the
+ * device, one captured CUDA graph of this call serves every later step.
+ *   q        [B,Hq,D] bf16 (rotated at L inside when rope = 1).
+ *   k_new, v_new [B,Hkv,D] bf16, the current token's key (unrotated) and value.
+ *   k_cache, v_cache [B,Hkv,Lmax,D] bf16, written at row L.
+ *   cache_len device int32 [B], 1 <= cache_len[b] <= Lmax - 1, incremented.
+ *   o        [B,Hq,D] bf16.   lse  NULL or [B,Hq] float32 (natural log, over the L + 1 keys).
+ *   workspace  device buffer of attn_decode_append_workspace_size() bytes (never zero).
+ *   dtype    ATTN_BF16 only; D in {64, 128}; Hq / Hkv <= 16.
+ * Device errors: a cache_len outside [1, Lmax - 1] sets DEVICE_ARG; that sequence's row is not
+ * written, its length not changed, and its output is the history result (zero when L < 1).
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ */
+ATTN_API size_t attn_decode_append_workspace_size(int B, int Hq, int Hkv, int D, int Lmax);
+ATTN_API attn_status_t attn_decode_append(const void* q, const void* k_new, const void* v_new,
+                                          void* k_cache, void* v_cache, int32_t* cache_len,
+                                          int Lmax, void* o, float* lse, attn_dtype_t dtype,
+                                          int B, int Hq, int Hkv, int D, float softmax_scale,
+                                          int rope, float rope_theta, void* workspace,
+                                          size_t workspace_bytes, attn_stream_t stream);
 
 /*
  * attn_decode_latent_workspace_size — bytes of workspace attn_decode_latent needs.

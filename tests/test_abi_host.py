@@ -134,6 +134,31 @@ def test_decode_validation(L):
     assert _decode(L, rope=3) == INVALID
 
 
+def _append(L, **kw):
+    args = dict(q=FAKE, kn=FAKE, vn=FAKE, kc=FAKE, vc=FAKE, lens=FAKE2, Lmax=2048, o=FAKE2,
+                lse=None, dt=0, B=2, Hq=32, Hkv=8, D=128, scale=0.0, rope=1, theta=1e4, ws=FAKE2,
+                wsb=1 << 20)
+    args.update(kw)
+    return L.attn_decode_append(*args.values(), _stream())
+
+
+def test_decode_append_validation(L):
+    assert _append(L, ws=None) == INVALID                # the history LSE always needs room
+    assert _append(L, kn=None) == INVALID
+    assert _append(L, vc=MIS) == INVALID
+    assert _append(L, Lmax=1) == INVALID                 # no row for the new token
+    assert _append(L, Hq=30) == INVALID
+    assert _append(L, D=80) == UNSUPPORTED
+    assert _append(L, dt=1) == UNSUPPORTED               # bf16 caches only
+    assert _append(L, Hq=64, Hkv=2) == UNSUPPORTED
+    # history workspace (rounded to 256 bytes) plus one float per query row
+    assert binding.attn_decode_append_workspace_size(128, 32, 8, 128, 2048) == 128 * 32 * 4
+    w1 = binding.attn_decode_append_workspace_size(1, 32, 8, 128, 2048)
+    d1 = binding.attn_decode_workspace_size(1, 32, 8, 128, 2048)
+    assert w1 == ((d1 + 255) // 256) * 256 + 32 * 4
+    assert binding.attn_decode_append_workspace_size(1, 30, 8, 128, 2048) == 0
+
+
 def _latent(L, **kw):
     args = dict(q=FAKE, c=FAKE, lens=FAKE2, Lmax=2048, o=FAKE2, lse=None, B=128, H=16,
                 scale=0.0, rope=1, theta=1e4, ws=FAKE2, wsb=1 << 30)
@@ -166,6 +191,7 @@ def test_valid_calls_report_no_device_without_gpu(L):
     assert _prefill(L) == NO_DEVICE
     assert _chunk(L) == NO_DEVICE
     assert _decode(L) == NO_DEVICE
+    assert _append(L) == NO_DEVICE
     assert _decode(L, ws=None, wsb=0) in (NO_DEVICE, WORKSPACE)
     assert _latent(L) == NO_DEVICE
     assert L.rope_apply(FAKE, FAKE, 0, 1, 1, 4, 8, 0, 1e4, _stream()) == NO_DEVICE

@@ -283,6 +283,92 @@ def test_prefill_chunk_rejects_bad_lengths():
 
 
 # --------------------------------------------------------------------------------------------
+# growing decode: the current token joins the cache
+# --------------------------------------------------------------------------------------------
+
+def _append_inputs(B, Hq, Hkv, Lmax, D, lens, seed):
+    q, kc, vc, cl = synthetic.decode_inputs(B, Hq, Hkv, Lmax, D, lens, seed=seed)
+    kn = synthetic.normal((B, Hkv, D), 1000 * seed + 77)
+    vn = synthetic.normal((B, Hkv, D), 1000 * seed + 78)
+    return q, kc, vc, cl, kn, vn
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,D,lens", [
+    (3, 32, 8, 2048, 128, [2047, 1, 700]),   # last free row, a one-key history, a middle one
+    (2, 8, 2, 300, 64, [5, 256]),
+    (5, 16, 1, 600, 128, [599, 129, 128, 1, 300]),   # group of 16
+    (40, 32, 8, 520, 128, 400),
+])
+def test_decode_append(B, Hq, Hkv, Lmax, D, lens):
+    q, kc, vc, cl, kn, vn = _append_inputs(B, Hq, Hkv, Lmax, D, lens, seed=B + D)
+    gk, gv, gl = kc.cuda(), vc.cuda(), cl.cuda()
+    o, lse = binding.attn_decode_append(q.cuda(), kn.cuda(), vn.cuda(), gk, gv, gl,
+                                        want_lse=True, rope=True, rope_theta=10000.0)
+    status_ok()
+    ro, rl, krow = oracle.decode_append(f64(q), f64(kc), f64(vc), cl.numpy(), f64(kn), f64(vn),
+                                        rope=True, theta=10000.0)
+    check(o.cpu(), ro, what="O append")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE append")
+    assert torch.equal(gl.cpu(), cl + 1)
+    gk, gv = gk.cpu(), gv.cpu()
+    for b in range(B):
+        L = int(cl[b])
+        # the new row: the rotated key rounded to bf16, the value as given
+        np.testing.assert_allclose(f64(gk[b, :, L]), krow[b], rtol=0, atol=1.6e-2)
+        assert torch.equal(gv[b, :, L], vn[b])
+        # every other row is untouched
+        assert torch.equal(gk[b, :, :L], kc[b, :, :L])
+        assert torch.equal(gk[b, :, L + 1:], kc[b, :, L + 1:])
+
+
+def test_decode_append_graph_replays_grow_the_cache():
+    """One captured step replayed three times: each replay reads the length it left behind."""
+    B, Hq, Hkv, Lmax, D, steps = 4, 32, 8, 1100, 128, 3
+    q, kc, vc, cl, kn, vn = _append_inputs(B, Hq, Hkv, Lmax, D, [1000, 7, 511, 1024], seed=5)
+    dq, dkn, dvn = q.cuda(), kn.cuda(), vn.cuda()
+    gk, gv, gl = kc.cuda(), vc.cuda(), cl.cuda()
+    o = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(binding.attn_decode_append_workspace_size(B, Hq, Hkv, D, Lmax),
+                     dtype=torch.uint8, device="cuda")
+    binding.attn_rope_table_reserve(D, 10000.0, Lmax + 1)
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            binding.attn_decode_append(dq, dkn, dvn, gk, gv, gl, o=o, workspace=ws, stream=st)
+    torch.cuda.synchronize()
+    assert torch.equal(gl.cpu(), cl)  # capturing ran nothing
+    for _ in range(steps):
+        g.replay()
+    torch.cuda.synchronize()
+    status_ok()
+    k_ref, v_ref, lens = f64(kc), f64(vc), cl.numpy().copy()
+    for _ in range(steps):
+        ro, _, krow = oracle.decode_append(f64(q), k_ref, v_ref, lens, f64(kn), f64(vn),
+                                           rope=True, theta=10000.0)
+        for b in range(B):
+            k_ref[b, :, lens[b]] = f64(torch.from_numpy(krow[b]).to(torch.bfloat16))
+            v_ref[b, :, lens[b]] = f64(vn[b])
+        lens = lens + 1
+    assert np.array_equal(gl.cpu().numpy(), lens)
+    check(o.cpu(), ro, what="O after replays")
+
+
+def test_decode_append_full_cache_sets_status():
+    B, Hq, Hkv, Lmax, D = 2, 8, 2, 64, 128
+    q, kc, vc, cl, kn, vn = _append_inputs(B, Hq, Hkv, Lmax, D, [64, 10], seed=9)
+    gk, gl = kc.cuda(), cl.cuda()
+    o = binding.attn_decode_append(q.cuda(), kn.cuda(), vn.cuda(), gk, vc.cuda(), gl)
+    assert binding.attn_get_device_status() == 7  # no row left for sequence 0
+    assert binding.attn_get_device_status() == 0
+    assert gl.cpu().tolist() == [64, 11]
+    ro, _, _ = oracle.decode_append(f64(q[1:]), f64(kc[1:]), f64(vc[1:]), cl[1:].numpy(),
+                                    f64(kn[1:]), f64(vn[1:]), rope=True, theta=10000.0)
+    check(o[1:].cpu(), ro, what="valid row")
+    assert torch.equal(gk[0].cpu(), kc[0])
+
+
+# --------------------------------------------------------------------------------------------
 # latent decode
 # --------------------------------------------------------------------------------------------
 
