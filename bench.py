@@ -81,7 +81,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -393,6 +393,15 @@ def variants(b, d):
         "graph_ms_per_step": round(tg, 5), "graph_gbs": round(nbytes / tg / 1e6, 1),
         "launches_per_step": 3}
     del q, kc, vc, cl, cl0, kn, vn, o, ws
+    # a streaming reference at the latent cache's size: one library reduction (read-only) over
+    # 256 MiB of bf16, timed the same way (graph replay); at this size a fixed ramp and tail
+    # weigh on any single pass
+    x = torch.empty(128 * 2048 * 512, dtype=torch.bfloat16, device="cuda").normal_()
+    ts = time_graph(lambda: x.sum(dtype=torch.float32), 30)
+    out["stream_reference_256mib"] = {
+        "what": "torch sum over 256 MiB bf16 (read-only library kernel), graph replay",
+        "graph_ms": round(ts, 5), "gbs": round(x.numel() * 2 / ts / 1e6, 1)}
+    del x
     return out
 
 
@@ -531,13 +540,20 @@ def oracle_prefill_sample(S: int, seed: int = 0):
     return workload.prefill_flops(1, 1, S, D, True), dt
 
 
-def cpu_baseline(seconds_budget=20.0):
+def cpu_baseline(seconds_budget=15.0):
+    """The oracle as it stands on the host cores: (batch, head) samples of the bench's causal RoPE
+    prefill at S=8192, one after another until about `seconds_budget` seconds of CPU work."""
     S = 8192
-    flops, dt = oracle_prefill_sample(S)
-    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOPS", "cores": os.cpu_count(),
+    tot_f, tot_t, n = 0.0, 0.0, 0
+    while tot_t < seconds_budget:
+        f, t = oracle_prefill_sample(S, seed=100 + n)
+        tot_f += f
+        tot_t += t
+        n += 1
+    return {"value": round(tot_f / tot_t / 1e12, 6), "unit": "TFLOPS", "cores": os.cpu_count(),
             "kind": "oracle",
-            "sample": f"one (batch, head) of the causal RoPE prefill at S={S}, D=128, float64 "
-                      f"NumPy ({dt:.1f} s)"}
+            "sample": f"{n} (batch, head) samples of the causal RoPE prefill at S={S}, D=128, "
+                      f"float64 NumPy, {tot_t:.1f} s in total (NumPy's default BLAS threads)"}
 
 
 def reference(args):
@@ -591,6 +607,12 @@ def single_case(args):
         q, kc, vc, cl = q.cuda(), kc.cuda(), vc.cuda(), cl.cuda()
         b.attn_rope_table_reserve(128, THETA, 2049)
         fn = lambda: b.attn_decode(q, kc, vc, cl, rope=True, rope_theta=THETA)
+    elif args.case == "decode-fp8":
+        q, kc, vc, cl = synthetic.decode_inputs(args.B, 32, 8, 2048, 128, 2048, seed=1,
+                                                cache_dtype="fp8")
+        q, kc, vc, cl = q.cuda(), kc.cuda(), vc.cuda(), cl.cuda()
+        b.attn_rope_table_reserve(128, THETA, 2049)
+        fn = lambda: b.attn_decode(q, kc, vc, cl, rope=True, rope_theta=THETA)
     elif args.case == "latent":
         q, c, cl = synthetic.latent_inputs(args.B, 16, 2048, 2048, seed=1)
         q, c, cl = q.cuda(), c.cuda(), cl.cuda()
@@ -608,14 +630,15 @@ def single_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--case", default=None,
-                    choices=["prefill", "prefill-unfused", "prefill-d64", "decode", "latent",
+                    choices=["prefill", "prefill-unfused", "prefill-d64", "decode", "decode-fp8",
+                             "latent",
                              "rope"], help="time one kernel alone (for profiler captures)")
     ap.add_argument("--S", type=int, default=4096)
     ap.add_argument("--B", type=int, default=128)
