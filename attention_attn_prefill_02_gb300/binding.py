@@ -48,6 +48,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.rope_apply.argtypes = [vp, vp, i, i, i, i, i, i, f, vp]
     L.attn_prefill.restype = i
     L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i, f, f, f, i, i, i, i, i, i, f, i, f, i, vp]
+    L.attn_prefill_reserve.restype = i
+    L.attn_prefill_reserve.argtypes = [i, i, i, i, i]
     L.attn_prefill_chunk.restype = i
     L.attn_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, i, f, f, f, i, i, i, i, i, i, i, f, i, f,
                                      i, vp]
@@ -106,6 +108,16 @@ def rope_apply(x, y=None, pos0=0, theta=10000.0, stream=None):
     return y
 
 
+def _rope_mode(rope):
+    """False/0: none; True/1: the library's choice; 2: Q and K both rotated inside the kernel."""
+    return 2 if (not isinstance(rope, bool) and rope == 2) else int(bool(rope))
+
+
+def attn_prefill_reserve(B, Hq, Hkv, S, D):
+    """Allocate ahead (e.g. before a graph capture) what a RoPE prefill of this size needs."""
+    _check(lib().attn_prefill_reserve(B, Hq, Hkv, S, D), "attn_prefill_reserve")
+
+
 def attn_prefill(q, k, v, causal=True, softmax_scale=0.0, rope=False, rope_theta=10000.0,
                  pos0=0, o=None, lse=None, want_lse=False, q_scale=1.0, k_scale=1.0,
                  v_scale=1.0, stream=None):
@@ -120,7 +132,7 @@ def attn_prefill(q, k, v, causal=True, softmax_scale=0.0, rope=False, rope_theta
     _check(lib().attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                               DTYPE_CODES[q.dtype], float(q_scale), float(k_scale),
                               float(v_scale), B, Hq, Hkv, S, D, int(bool(causal)),
-                              float(softmax_scale), int(bool(rope)), float(rope_theta), int(pos0),
+                              float(softmax_scale), _rope_mode(rope), float(rope_theta), int(pos0),
                               _stream(stream)), "attn_prefill")
     return (o, lse) if (want_lse or lse is not None) else o
 

@@ -71,7 +71,7 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
-  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  if (rope < 0 || rope > 2) return ATTN_ERR_INVALID_ARG;
   if (rope && (!finite_pos(rope_theta) || pos0 < 0)) return ATTN_ERR_INVALID_ARG;
   if (!finite_pos(q_scale) || !finite_pos(k_scale) || !finite_pos(v_scale))
     return ATTN_ERR_INVALID_ARG;
@@ -88,9 +88,32 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
     if (!tab) return st;
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  if (rope == 1 && dtype == ATTN_BF16 && S >= kRopePassMinS) {
+    // Q and K rotated once each into the library's scratch, then attention without RoPE
+    const size_t qb = rope_scratch_q_bytes(B, Hq, S, D);
+    uint8_t* sc = static_cast<uint8_t*>(
+        rope_scratch(qb + static_cast<size_t>(B) * Hkv * S * D * 2, &st));
+    if (!sc) return st;
+    st = launch_rope(q, sc, dtype, B, Hq, S, D, pos0, tab, as_stream(stream));
+    if (st != ATTN_OK) return st;
+    st = launch_rope(k, sc + qb, dtype, B, Hkv, S, D, pos0, tab, as_stream(stream));
+    if (st != ATTN_OK) return st;
+    return launch_prefill(sc, sc + qb, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv,
+                          S, S, S, D, causal, scale, nullptr, 0, pos0, as_stream(stream));
+  }
   return launch_prefill(q, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, S, S, S,
-                        D, causal, scale, tab, 1, pos0, as_stream(stream));
+                        D, causal, scale, tab, rope ? 1 : 0, pos0, as_stream(stream));
 }
+
+attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || (D != 64 && D != 128)) return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  const size_t qb = rope_scratch_q_bytes(B, Hq, S, D);
+  const size_t bytes = S >= kRopePassMinS ? qb + static_cast<size_t>(B) * Hkv * S * D * 2 : qb;
+  return rope_scratch(bytes, &st) ? ATTN_OK : st;
+}
+
 
 attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, void* o, float* lse,
                                  attn_dtype_t dtype, float q_scale, float k_scale, float v_scale,
@@ -120,6 +143,16 @@ attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, vo
     if (!tab) return st;
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  if (rope && dtype == ATTN_BF16) {
+    // the chunk's queries rotated once at their absolute positions, then attention without RoPE
+    void* sq = rope_scratch(rope_scratch_q_bytes(B, Hq, Sq, D), &st);
+    if (!sq) return st;
+    st = launch_rope(q, sq, dtype, B, Hq, Sq, D, pos0 + Skv - Sq, tab, as_stream(stream));
+    if (st != ATTN_OK) return st;
+    return launch_prefill(sq, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, Sq,
+                          Skv, kv_pitch, D, 1, scale, nullptr, 0, pos0, as_stream(stream));
+  }
+  // fp8: q rotated into bf16 inside the kernel; the staged keys are widened as stored
   return launch_prefill(q, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, Sq, Skv,
                         kv_pitch, D, 1, scale, tab, 0, pos0, as_stream(stream));
 }

@@ -35,7 +35,8 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kRopeWarp0 = 10;  // fused RoPE: warps 10-13 rotate each K tile in shared memory
 constexpr int kRopeThreads = 128;
-__host__ __device__ constexpr int threads_for(bool rope) { return rope ? 448 : 320; }
+// RoPE mode 1 adds the four K-rotation warps.
+__host__ __device__ constexpr int threads_for(int rm) { return rm == 1 ? 448 : 320; }
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -200,11 +201,14 @@ __device__ __forceinline__ void rope_rotate_row_fp8_to_bf16(const uint8_t* st, u
   }
 }
 
-template <int D, bool ROPE, int ESZ>
-__global__ void __launch_bounds__(threads_for(ROPE), 1)
+// RM, the RoPE mode: 0 none; 1 Q and K rotated inside (the softmax warps rotate each Q tile as
+// it lands, the RoPE warps every K tile).
+template <int D, int RM, int ESZ>
+__global__ void __launch_bounds__(threads_for(RM), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
   constexpr bool FP8 = ESZ == 1;
+  constexpr bool ROPE = RM == 1;  // Q and K rotated in shared memory
   constexpr bool STAGED = FP8 && ROPE;  // fp8 inputs, RoPE fused: rotate into bf16 Q/K tiles
   using C = Cfg<D, ESZ, STAGED>;
   // First TMEM column of P inside S_t.  The RoPE variants (four more warps, so fewer registers
@@ -811,12 +815,12 @@ __global__ void __launch_bounds__(threads_for(ROPE), 1)
   }
 }
 
-template <int D, bool ROPE, int ESZ>
+template <int D, int RM, int ESZ>
 attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o, float* lse,
                            float q_scale, float k_scale, float v_scale, int B, int Hq, int Hkv,
                            int S, int Skv, int kv_pitch, int causal, float scale,
                            const float2* table, int rope_k, int pos0, cudaStream_t st) {
-  constexpr bool STAGED = ESZ == 1 && ROPE;
+  constexpr bool STAGED = ESZ == 1 && RM == 1;
   using C = Cfg<D, ESZ, STAGED>;
   // Q / K boxes: as the MMA reads them, or (STAGED) the fp8 staging tiles; V in its own geometry
   constexpr int kQKBoxElems = STAGED ? D : C::kBoxElems;
@@ -848,10 +852,10 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   p.v_scale = v_scale;
   p.table = table;
   p.pos0 = pos0;
-  auto kern = prefill_kernel<D, ROPE, ESZ>;
+  auto kern = prefill_kernel<D, RM, ESZ>;
   if (!set_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes)) return ATTN_ERR_CUDA;
   const int grid = std::min(p.n_items, sm_count());
-  kern<<<grid, threads_for(ROPE), C::kSmemBytes, st>>>(tq, tk, tv, p);
+  kern<<<grid, threads_for(RM), C::kSmemBytes, st>>>(tq, tk, tv, p);
   return launch_status();
 }
 
@@ -863,17 +867,18 @@ attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* 
                              float scale, const float2* table, int rope_k, int pos0,
                              cudaStream_t st) {
   const int esz = dt == ATTN_BF16 ? 2 : 1;
+  const int rm = table == nullptr ? 0 : 1;
 #define ATTN_PREFILL_CASE(DD, RR, EE)                                                          \
-  if (D == DD && (table != nullptr) == RR && esz == EE)                                        \
+  if (D == DD && rm == RR && esz == EE)                                                        \
     return launch_typed<DD, RR, EE>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S, \
                                     Skv, kv_pitch, causal, scale, table, rope_k, pos0, st);
-  ATTN_PREFILL_CASE(128, false, 2)
-  ATTN_PREFILL_CASE(128, true, 2)
-  ATTN_PREFILL_CASE(64, false, 2)
-  ATTN_PREFILL_CASE(64, true, 2)
-  ATTN_PREFILL_CASE(128, false, 1)
-  ATTN_PREFILL_CASE(64, false, 1)
-  ATTN_PREFILL_CASE(128, true, 1)
+  ATTN_PREFILL_CASE(128, 0, 2)
+  ATTN_PREFILL_CASE(128, 1, 2)
+  ATTN_PREFILL_CASE(64, 0, 2)
+  ATTN_PREFILL_CASE(64, 1, 2)
+  ATTN_PREFILL_CASE(128, 0, 1)
+  ATTN_PREFILL_CASE(64, 0, 1)
+  ATTN_PREFILL_CASE(128, 1, 1)
 #undef ATTN_PREFILL_CASE
   return ATTN_ERR_UNSUPPORTED;
 }

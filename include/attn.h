@@ -96,18 +96,35 @@ ATTN_API attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, in
  *   q_scale, k_scale, v_scale: dequantisation factors (stored value * scale = real value);
  *            pass 1 for bf16 and for the per-tensor-scale-1 fp8 workloads.
  *   causal   0 or 1; causal hides key j from query i when j > i (S_q == S_kv).
- *   rope     0 = Q and K used as given; 1 = Q and K rotated inside the kernel at positions
- *            pos0 + s as they are loaded (fused RoPE).
+ *   rope     0 = Q and K used as given.  1 and 2 rotate Q and K at positions pos0 + s:
+ *            1 = the library's choice: bf16 prompts of S >= 1024 rotate Q and K once per call
+ *                (rope_apply passes into library-owned scratch, see attn_prefill_reserve), then
+ *                run attention without RoPE; shorter prompts and fp8 rotate both inside the
+ *                kernel;
+ *            2 = both inside the kernel as they are loaded (K once per query block that reads
+ *                it; the fully fused form, measured beside the other).
  *   D in {64, 128}; Hq % Hkv == 0; S >= 1.  fp8 e5m2 inputs: P is rounded to e4m3 for the PV
  *   product; with rope = 1 (D = 128 only) Q and K are rotated into bf16 tiles inside the
  *   kernel (QK^T then runs in bf16, PV stays fp8), because rotated values re-rounded to fp8
  *   would exceed the fp8 error budget.
+ *   With rope = 1 the scratch ((Hq + Hkv)*B*S*D bf16, per device, grown on demand, never
+ *   shrunk) is allocated on first use; overlapping calls on different streams share it and
+ *   must be serialised.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
  */
 ATTN_API attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                            attn_dtype_t dtype, float q_scale, float k_scale, float v_scale,
                            int B, int Hq, int Hkv, int S, int D, int causal, float softmax_scale,
                            int rope, float rope_theta, int pos0, attn_stream_t stream);
+
+/*
+ * attn_prefill_reserve — allocate ahead the per-device rotation scratch that attn_prefill
+ * (rope = 1) and attn_prefill_chunk (rope = 1, bf16) use at this size (S = the query rows), e.g.
+ * before a CUDA-graph capture, which cannot allocate.  Together with attn_rope_table_reserve it
+ * leaves nothing to allocate in later calls up to that size.
+ * Errors: INVALID_ARG (sizes, D not in {64, 128}), CUDA, NO_DEVICE.
+ */
+ATTN_API attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D);
 
 /*
  * attn_prefill_chunk — one chunk of a prompt against a static cache (chunked prefill).
@@ -121,7 +138,9 @@ ATTN_API attn_status_t attn_prefill(const void* q, const void* k, const void* v,
  *            head holding the keys before the chunk followed by the chunk's own.  Keys are used
  *            as stored (a cache holds them already rotated); rows >= Skv are never read.
  *   o        [B,Hq,Sq,D] bfloat16.   lse  NULL or [B,Hq,Sq] float32 (natural log).
- *   rope     1: q rotated inside the kernel at positions pos0 + Skv - Sq + i; 0: q as given.
+ *   rope     1: q rotated at positions pos0 + Skv - Sq + i (bf16: a rope_apply pass into the
+ *            library's scratch, see attn_prefill_reserve; fp8: inside the kernel, into bf16
+ *            tiles); 0: q as given.
  *   1 <= Sq <= Skv <= kv_pitch; D in {64, 128} (fp8 with rope = 1: D = 128); the other
  *   arguments as attn_prefill.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA.

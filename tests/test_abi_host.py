@@ -93,6 +93,9 @@ def test_prefill_validation(L):
     assert _prefill(L, S=0) == INVALID
     assert _prefill(L, causal=2) == INVALID
     assert _prefill(L, rope=1, theta=-1.0) == INVALID
+    assert _prefill(L, rope=3) == INVALID
+    assert L.attn_prefill_reserve(1, 1, 1, 0, 128) == INVALID
+    assert L.attn_prefill_reserve(1, 1, 1, 4096, 96) == INVALID
     assert _prefill(L, qs=0.0) == INVALID
     assert _prefill(L, lse=ctypes.c_void_p(0x7F0000000002)) == INVALID
     assert _prefill(L, D=96) == UNSUPPORTED
@@ -189,6 +192,8 @@ def test_workspace_sizes_are_consistent(L):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_valid_calls_report_no_device_without_gpu(L):
     assert _prefill(L) == NO_DEVICE
+    assert _prefill(L, rope=2) == NO_DEVICE
+    assert L.attn_prefill_reserve(4, 32, 8, 16384, 128) == NO_DEVICE
     assert _chunk(L) == NO_DEVICE
     assert _decode(L) == NO_DEVICE
     assert _append(L) == NO_DEVICE

@@ -59,12 +59,14 @@ def check_rows(o, lse, rows, ro, rl, max_abs, mean_abs):
     assert np.abs(gl - rl).max() <= 2e-2
 
 
-def test_causal_prefill_s16384_fused_rope_bf16():
-    """Causal GQA prefill, Z=4 Hq=32 Hkv=8 D=128 S=16384, bf16, RoPE 1e4 fused (the bench step)."""
+@pytest.mark.parametrize("rope", [1, 2])
+def test_causal_prefill_s16384_rope_bf16(rope):
+    """Causal GQA prefill, Z=4 Hq=32 Hkv=8 D=128 S=16384, bf16, RoPE 1e4 (the bench step):
+    rope=1 rotates K once per call and Q in the kernel, rope=2 both in the kernel."""
     B, Hq, Hkv, S, D = 4, 32, 8, 16384, 128
     q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=17)
     binding.attn_rope_table_reserve(D, 10000.0, S)
-    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, rope=True,
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, rope=rope,
                                   rope_theta=10000.0, want_lse=True)
     assert binding.attn_get_device_status() == 0
     rows = sample_rows(B, Hq, S)

@@ -105,15 +105,19 @@ def test_prefill_unfused_rope_tiny_config():
     check(o.cpu(), ro, what="O")
 
 
-@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,pos0", [
-    (1, 4, 1, 128, 64, True, 0),       # the tiny config: RoPE fused into the Q/K loads
-    (2, 8, 2, 700, 128, True, 0),      # GQA, ragged tail, several items per head
-    (1, 2, 2, 300, 64, False, 5000),   # non-causal, positions offset
-    (1, 4, 1, 257, 128, True, 3),      # one row past a whole item
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,pos0,rope", [
+    (1, 4, 1, 128, 64, True, 0, 1),       # the tiny config: RoPE fused into the Q/K loads
+    (2, 8, 2, 700, 128, True, 0, 1),      # GQA, ragged tail, several items per head
+    (1, 2, 2, 300, 64, False, 5000, 1),   # non-causal, positions offset
+    (1, 4, 1, 257, 128, True, 3, 1),      # one row past a whole item
+    (1, 4, 1, 1100, 128, True, 0, 1),     # long enough that K is rotated once per call
+    (1, 4, 4, 1500, 64, False, 77, 1),    # the same path at D = 64, non-causal, offset
+    (1, 4, 1, 1100, 128, True, 0, 2),     # forced: K rotated in every query block
+    (1, 2, 2, 1030, 64, True, 9, 2),
 ])
-def test_prefill_fused_rope(B, Hq, Hkv, S, D, causal, pos0):
+def test_prefill_fused_rope(B, Hq, Hkv, S, D, causal, pos0, rope):
     q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=S + 1)
-    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, rope=True,
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, rope=rope,
                                   rope_theta=10000.0, pos0=pos0, want_lse=True)
     status_ok()
     ro, rl = oracle.prefill(f64(q), f64(k), f64(v), causal=causal, rope=True, theta=10000.0,
