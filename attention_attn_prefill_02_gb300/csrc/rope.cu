@@ -2,8 +2,8 @@
 //
 // Row r = ((b*H + h)*S + s) is rotated at position pos0 + s: each pair (x_i, x_{i+D/2}) becomes
 // (x_i c - x_{i+D/2} s, x_{i+D/2} c + x_i s) with (c, s) = table[pos][i].  The pass is HBM
-// bound (every element read and written once); each thread moves one 16-byte chunk of the
-// first half of a row and the matching chunk of the second half, fully coalesced.
+// bound (every element read and written once); each thread moves 16-byte chunks of the first
+// half of a row and the matching chunks of the second half, fully coalesced.
 #include "common.cuh"
 
 namespace attn {
@@ -15,7 +15,9 @@ template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int N = 8;  // elements per 16-byte chunk
   __device__ static void load(const void* p, float* f) {
-    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    unpack(__ldg(reinterpret_cast<const uint4*>(p)), f);
+  }
+  __device__ static void unpack(const uint4& u, float* f) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -42,7 +44,9 @@ template <>
 struct Vec<__nv_fp8_e5m2> {
   static constexpr int N = 16;
   __device__ static void load(const void* p, float* f) {
-    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    unpack(__ldg(reinterpret_cast<const uint4*>(p)), f);
+  }
+  __device__ static void unpack(const uint4& u, float* f) {
     const __nv_fp8x2_e5m2* h = reinterpret_cast<const __nv_fp8x2_e5m2*>(&u);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -101,6 +105,60 @@ __global__ void __launch_bounds__(256) rope_vec_kernel(const T* __restrict__ x, 
   }
 }
 
+// One thread per (sequence b, position s, 16-byte chunk pair): its cos/sin are read once and
+// applied to that chunk pair in all H heads, HU heads at a time so several loads are in flight.
+// Consecutive threads take consecutive chunks of a row, then the next position, so every warp
+// access covers whole rows of one head.
+template <typename T, int HU>
+__global__ void __launch_bounds__(256, 2) rope_pos_kernel(const T* __restrict__ x, T* y, int B,
+                                                       int H, int S, int D, int pos0,
+                                                       const float2* __restrict__ table) {
+  constexpr int N = Vec<T>::N;
+  const int half = D / 2;
+  const int chunks = half / N;
+  const long long total = static_cast<long long>(B) * S * chunks;
+  const size_t head_stride = static_cast<size_t>(S) * D;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+       t += (long long)gridDim.x * blockDim.x) {
+    const long long bs = t / chunks;
+    const int i0 = static_cast<int>(t - bs * chunks) * N;
+    const int s = static_cast<int>(bs % S);
+    const long long b = bs / S;
+    float2 r[N];
+    const float2* cs = table + static_cast<long long>(pos0 + s) * half + i0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) r[j] = __ldg(cs + j);
+    const size_t row0 = (static_cast<size_t>(b) * H * S + s) * D + i0;
+    for (int h = 0; h < H; h += HU) {
+      uint4 ra[HU], rc[HU];  // raw chunks: all loads of the batch go out before any use
+#pragma unroll
+      for (int u = 0; u < HU; ++u)
+        if (h + u < H) {
+          const T* xr = x + row0 + static_cast<size_t>(h + u) * head_stride;
+          ra[u] = __ldg(reinterpret_cast<const uint4*>(xr));
+          rc[u] = __ldg(reinterpret_cast<const uint4*>(xr + half));
+        }
+#pragma unroll
+      for (int u = 0; u < HU; ++u)
+        if (h + u < H) {
+          float a[N], c[N];
+          Vec<T>::unpack(ra[u], a);
+          Vec<T>::unpack(rc[u], c);
+#pragma unroll
+          for (int j = 0; j < N; ++j) {
+            const float a1 = a[j] * r[j].x - c[j] * r[j].y;
+            const float c1 = c[j] * r[j].x + a[j] * r[j].y;
+            a[j] = a1;
+            c[j] = c1;
+          }
+          T* yr = y + row0 + static_cast<size_t>(h + u) * head_stride;
+          Vec<T>::store(yr, a);
+          Vec<T>::store(yr + half, c);
+        }
+    }
+  }
+}
+
 // Any even D: one thread per pair.
 template <typename T>
 __global__ void __launch_bounds__(256) rope_pair_kernel(const T* __restrict__ x, T* y,
@@ -127,7 +185,15 @@ attn_status_t launch_typed(const void* x, void* y, int B, int H, int S, int D, i
   const long long rows = static_cast<long long>(B) * H * S;
   const int sms = sm_count();
   const int threads = 256;
-  if ((D / 2) % Vec<T>::N == 0) {
+  if ((D / 2) % Vec<T>::N == 0 && H >= 4) {
+    const long long work = static_cast<long long>(B) * S * ((D / 2) / Vec<T>::N);
+    long long blocks = (work + threads - 1) / threads;
+    const long long cap = static_cast<long long>(sms) * 16;
+    if (blocks > cap) blocks = cap;
+    constexpr int HU = Vec<T>::N == 8 ? 4 : 2;
+    rope_pos_kernel<T, HU><<<static_cast<int>(blocks), threads, 0, st>>>(
+        static_cast<const T*>(x), static_cast<T*>(y), B, H, S, D, pos0, table);
+  } else if ((D / 2) % Vec<T>::N == 0) {
     const long long work = rows * ((D / 2) / Vec<T>::N);
     long long blocks = (work + threads - 1) / threads;
     const long long cap = static_cast<long long>(sms) * 16;

@@ -41,7 +41,9 @@ def status_ok():
 # --------------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("shape,pos0", [((2, 3, 37, 64), 5), ((1, 2, 130, 128), 0),
-                                        ((1, 1, 3, 6), 11), ((2, 4, 256, 128), 16000)])
+                                        ((1, 1, 3, 6), 11), ((2, 4, 256, 128), 16000),
+                                        ((3, 9, 41, 128), 7),      # heads not a multiple of 4
+                                        ((1, 32, 300, 64), 0)])
 def test_rope_apply_bf16(shape, pos0):
     x = synthetic.rope_input(*shape, dtype="bf16", seed=1)
     y = binding.rope_apply(x.cuda(), pos0=pos0, theta=10000.0)
@@ -51,6 +53,20 @@ def test_rope_apply_bf16(shape, pos0):
     # the kernel rounds once to bf16: it must agree with the rounded oracle almost everywhere
     rounded = torch.from_numpy(ref).to(torch.bfloat16)
     assert (y.cpu() == rounded).float().mean() > 0.99
+
+
+@pytest.mark.parametrize("H", [2, 7])
+def test_rope_apply_fp8_heads(H):
+    """fp8 e5m2 out of place, few heads and several (the per-position kernel walks the heads)."""
+    x = synthetic.rope_input(2, H, 70, 128, dtype="fp8", seed=H)
+    y = binding.rope_apply(x.cuda(), pos0=9, theta=10000.0)
+    torch.cuda.synchronize()
+    ref = oracle.rope_rotate_half(f64(x), 9 + np.arange(70), 10000.0)
+    rounded = torch.from_numpy(ref).to(torch.float8_e5m2)
+    g, r = f64(y.cpu()), f64(rounded)
+    step = np.maximum(np.abs(r), 2.0 ** -14) * 0.25
+    assert np.all(np.abs(g - r) <= step * 1.0001)
+    assert (g == r).mean() > 0.99
 
 
 def test_rope_apply_in_place_and_fp8():
