@@ -12,6 +12,7 @@
 // splits are merged by their log-sum-exp ("A: group-entry queries and one joint history scan").
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -39,6 +40,51 @@ struct GqaParams {
   int B, Hq, Hkv, G, Lmax, nsplit, chunk;
   float scale_log2;  // softmax_scale * log2(e)
 };
+
+// The query tile of one (sequence, KV head) item: rows r < G of `q_rows` (the group's first
+// query row; bf16, D dims each) into `qs` (row pitch `pitch` bytes) as T_OUT, rows G .. rows-1
+// zero; then, with a table, each pair (i, i + D/2) rotated at position len in float32 and
+// rounded once.  The 16-byte loads all go out before any store.  Ends before the final barrier:
+// the caller synchronises before reading the tile.
+template <int D, typename T_OUT>
+__device__ __forceinline__ void fill_query_tile(uint8_t* qs, int pitch, int rows,
+                                                const __nv_bfloat16* __restrict__ q_rows, int G,
+                                                bool valid, const float2* __restrict__ table,
+                                                int len, int tid) {
+  constexpr int kChunks = D / 8;  // 8-dim chunks per row
+  constexpr int kMaxPer = 16 * kChunks / (kComputeWarps * 32);
+  uint4 v[kMaxPer];
+#pragma unroll
+  for (int k = 0; k < kMaxPer; ++k) {
+    const int idx = tid + k * kComputeWarps * 32, r = idx / kChunks, c = idx % kChunks;
+    v[k] = (r < G && valid)
+               ? __ldg(reinterpret_cast<const uint4*>(q_rows + static_cast<size_t>(r) * D + c * 8))
+               : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < kMaxPer; ++k) {
+    const int idx = tid + k * kComputeWarps * 32, r = idx / kChunks, c = idx % kChunks;
+    if (r >= rows) continue;
+    uint4 w = v[k];
+    if constexpr (sizeof(T_OUT) == 2 && !std::is_same<T_OUT, __nv_bfloat16>::value) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[k]);
+      __half2* o = reinterpret_cast<__half2*>(&w);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = __float22half2_rn(__bfloat1622float2(h[j]));
+    }
+    *reinterpret_cast<uint4*>(qs + r * pitch + c * 16) = w;
+  }
+  if (!table || !valid) return;
+  compute_bar_sync();
+  for (int idx = tid; idx < G * (D / 2); idx += kComputeWarps * 32) {
+    const int r = idx / (D / 2), i = idx % (D / 2);
+    T_OUT* row = reinterpret_cast<T_OUT*>(qs + r * pitch);
+    const float x1 = static_cast<float>(row[i]), x2 = static_cast<float>(row[i + D / 2]);
+    const float2 cs = table[static_cast<size_t>(len) * (D / 2) + i];
+    row[i] = static_cast<T_OUT>(x1 * cs.x - x2 * cs.y);
+    row[i + D / 2] = static_cast<T_OUT>(x2 * cs.x + x1 * cs.y);
+  }
+}
 
 template <int D, int NST>
 struct GqaSmem {
@@ -138,25 +184,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // query tile: G rows (rotated at position len), zero-padded to 16 rows
     compute_bar_sync();
-    for (int idx = tid; idx < 16 * (D / 2); idx += kComputeWarps * 32) {
-      const int r = idx / (D / 2), i = idx % (D / 2);
-      float x1 = 0.f, x2 = 0.f;
-      if (r < G && valid) {
-        const __nv_bfloat16* qr = p.q + (static_cast<size_t>(b) * p.Hq + kvh * G + r) * D;
-        x1 = __bfloat162float(qr[i]);
-        x2 = __bfloat162float(qr[i + D / 2]);
-        if (p.table) {
-          const float2 cs = p.table[static_cast<size_t>(len) * (D / 2) + i];
-          const float y1 = x1 * cs.x - x2 * cs.y;
-          const float y2 = x2 * cs.x + x1 * cs.y;
-          x1 = y1;
-          x2 = y2;
-        }
-      }
-      __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(qs + r * L::kQPitch);
-      row[i] = __float2bfloat16_rn(x1);
-      row[i + D / 2] = __float2bfloat16_rn(x2);
-    }
+    fill_query_tile<D, __nv_bfloat16>(qs, L::kQPitch, 16,
+                                      p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * D, G,
+                                      valid, p.table, len, tid);
     compute_bar_sync();
     uint32_t qa[D / 16][4];
 #pragma unroll
@@ -460,25 +490,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // query rows as f16 (rotated at position len), zero-padded to 8 NT rows
     compute_bar_sync();
-    for (int idx = tid; idx < 8 * NT * (D / 2); idx += kComputeWarps * 32) {
-      const int r = idx / (D / 2), i = idx % (D / 2);
-      float x1 = 0.f, x2 = 0.f;
-      if (r < G && valid) {
-        const __nv_bfloat16* qr = p.q + (static_cast<size_t>(b) * p.Hq + kvh * G + r) * D;
-        x1 = __bfloat162float(qr[i]);
-        x2 = __bfloat162float(qr[i + D / 2]);
-        if (p.table) {
-          const float2 cs = p.table[static_cast<size_t>(len) * (D / 2) + i];
-          const float y1 = x1 * cs.x - x2 * cs.y;
-          const float y2 = x2 * cs.x + x1 * cs.y;
-          x1 = y1;
-          x2 = y2;
-        }
-      }
-      __half* row = reinterpret_cast<__half*>(qs + r * L::kQPitch);
-      row[i] = __float2half_rn(x1);
-      row[i + D / 2] = __float2half_rn(x2);
-    }
+    fill_query_tile<D, __half>(qs, L::kQPitch, 8 * NT,
+                               p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * D, G, valid,
+                               p.table, len, tid);
     compute_bar_sync();
     // Q^T operand: column g is query 8 nt + g; logical k = 2t+e -> dim 16kk+4t+e and
     // k = 8+2t+e -> dim 16kk+4t+2+e, the order the K reads deliver
@@ -754,6 +768,7 @@ struct LatParams {
   float* lse;
   float* ws_o;    // [B + grid - 1][H][448] partial outputs of sequences split between CTAs
   float* ws_lse;  // [B + grid - 1][H]
+  int* ws_pref;   // [B + 1] tile prefix sums (stream-K; written by CTA 0 for the merge)
   const float2* table;  // D = 64 table for the RoPE dims
   unsigned int* status;
   int B, H, Lmax;
@@ -911,6 +926,8 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     if (tid == kLatThreads - 1) pref[p.B] = base + x;
   }
   __syncthreads();
+  if (p.streamk && blockIdx.x == 0)  // the merge reads the same prefix sums
+    for (int b = tid; b <= p.B; b += kLatThreads) p.ws_pref[b] = pref[b];
   long long lo = 0, hi = 0;
   if (p.streamk) {
     const long long T = pref[p.B];
@@ -962,29 +979,35 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     const int k1 = sg.k1;
 
     lat_bar_sync();
-    // query rows: 448 latent dims as given, the 64 RoPE dims rotated at position len
-    for (int idx = tid; idx < 16 * (kLatQK / 2); idx += kLatWarps * 32) {
-      const int r = idx / (kLatQK / 2), j = idx % (kLatQK / 2);
-      __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(qs + r * kLatQPitch);
-      const __nv_bfloat16* qr = p.q + (static_cast<size_t>(b) * H + r) * kLatQK;
-      if (j < kLatV / 2) {
-        row[2 * j] = r < H ? qr[2 * j] : __float2bfloat16_rn(0.f);
-        row[2 * j + 1] = r < H ? qr[2 * j + 1] : __float2bfloat16_rn(0.f);
-      } else {
-        const int i = j - kLatV / 2;  // pair (i, i + 32) of the RoPE part
-        float x1 = 0.f, x2 = 0.f;
-        if (r < H) {
-          x1 = __bfloat162float(qr[kLatV + i]);
-          x2 = __bfloat162float(qr[kLatV + i + kLatRope / 2]);
-          if (p.table) {
-            const float2 cs = p.table[static_cast<size_t>(len) * (kLatRope / 2) + i];
-            const float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
-            x1 = y1;
-            x2 = y2;
-          }
-        }
-        row[kLatV + i] = __float2bfloat16_rn(x1);
-        row[kLatV + i + kLatRope / 2] = __float2bfloat16_rn(x2);
+    // query rows: 16-byte loads, all in flight before any store (rows >= H are zero) ...
+    {
+      constexpr int kChunks = kLatQK / 8;  // 8-dim chunks per row
+      constexpr int kPer = 16 * kChunks / kLatThreads;
+      uint4 v[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = tid + k * kLatThreads, r = idx / kChunks, c = idx % kChunks;
+        v[k] = r < H ? __ldg(reinterpret_cast<const uint4*>(
+                           p.q + (static_cast<size_t>(b) * H + r) * kLatQK + c * 8))
+                     : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = tid + k * kLatThreads, r = idx / kChunks, c = idx % kChunks;
+        *reinterpret_cast<uint4*>(qs + r * kLatQPitch + c * 16) = v[k];
+      }
+    }
+    lat_bar_sync();
+    // ... then the 64 RoPE dims rotated at position len, pairs (i, i + 32)
+    if (p.table) {
+      for (int idx = tid; idx < 16 * (kLatRope / 2); idx += kLatThreads) {
+        const int r = idx / (kLatRope / 2), i = idx % (kLatRope / 2);
+        __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(qs + r * kLatQPitch);
+        const float x1 = __bfloat162float(row[kLatV + i]);
+        const float x2 = __bfloat162float(row[kLatV + i + kLatRope / 2]);
+        const float2 cs = p.table[static_cast<size_t>(len) * (kLatRope / 2) + i];
+        row[kLatV + i] = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
+        row[kLatV + i + kLatRope / 2] = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
       }
     }
     lat_bar_sync();
@@ -1171,39 +1194,16 @@ constexpr int kFinishThreads = 448;  // one thread per output column
 constexpr int kMaxParts = 256;  // CTAs one sequence may be spread over (>= the SM count)
 
 __global__ void __launch_bounds__(kFinishThreads)
-    latent_finish_kernel(const int32_t* __restrict__ lens, int B, int H, int Lmax, int G,
+    latent_finish_kernel(const int* __restrict__ pref, int B, int H, int G,
                          const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                          __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                          unsigned int* status) {
   const int b = blockIdx.x, h = blockIdx.y;
-  __shared__ long long red_t[(kFinishThreads + 31) / 32], red_b[(kFinishThreads + 31) / 32];
   __shared__ int parts[kMaxParts];
   __shared__ float wgt[kMaxParts];
   __shared__ float inv_s, lse_s;
-  long long T = 0, tb = 0;  // all tiles, and tiles of the sequences before b
-  for (int i = threadIdx.x; i < B; i += blockDim.x) {
-    const int t = lat_tiles(lens, i, Lmax);
-    T += t;
-    if (i < b) tb += t;
-  }
-#pragma unroll
-  for (int o2 = 16; o2 > 0; o2 >>= 1) {
-    T += __shfl_xor_sync(0xffffffffu, T, o2);
-    tb += __shfl_xor_sync(0xffffffffu, tb, o2);
-  }
-  if ((threadIdx.x & 31) == 0) {
-    red_t[threadIdx.x >> 5] = T;
-    red_b[threadIdx.x >> 5] = tb;
-  }
-  __syncthreads();
-  T = 0;
-  tb = 0;
-#pragma unroll
-  for (int w = 0; w < (kFinishThreads + 31) / 32; ++w) {
-    T += red_t[w];
-    tb += red_b[w];
-  }
-  const int tiles = lat_tiles(lens, b, Lmax);
+  const long long T = pref[B], tb = pref[b];  // all tiles, and tiles of the sequences before b
+  const int tiles = pref[b + 1] - pref[b];
   const size_t orow = static_cast<size_t>(b) * H + h;
   if (tiles == 0) {
     if (threadIdx.x == 0 && h == 0) report_status(status, ATTN_ERR_DEVICE_ARG);
@@ -1370,7 +1370,10 @@ DecodePlan plan_latent(int B, int H, int Lmax) {
   pl.nsplit = streamk ? 1 : 0;  // 1 = stream-K mode (nsplit doubles as the mode flag here)
   pl.chunk = 0;
   // stream-K: partial outputs of sequences split between CTAs, slot (CTA + sequence)
-  pl.ws_bytes = streamk ? static_cast<size_t>(B + pl.grid - 1) * H * (kLatV + 1) * 4 : 0;
+  // and the tile prefix sums [B + 1] for the merge
+  pl.ws_bytes = streamk ? static_cast<size_t>(B + pl.grid - 1) * H * (kLatV + 1) * 4 +
+                              static_cast<size_t>(B + 1) * 4
+                        : 0;
   return pl;
 }
 
@@ -1571,6 +1574,8 @@ attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, i
   p.ws_o = ws ? static_cast<float*>(ws) : nullptr;
   p.ws_lse = ws ? static_cast<float*>(ws) + static_cast<size_t>(B + plan.grid - 1) * H * kLatV
                 : nullptr;
+  p.ws_pref = ws ? reinterpret_cast<int*>(p.ws_lse + static_cast<size_t>(B + plan.grid - 1) * H)
+                 : nullptr;
   p.table = table;
   p.status = device_status_ptr();
   p.B = B;
@@ -1583,7 +1588,7 @@ attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, i
   latent_decode_kernel<<<plan.grid, kLatThreads, LatSmem::kBytes, st>>>(tc, p);
   if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
   if (!p.streamk) return ATTN_OK;
-  latent_finish_kernel<<<dim3(B, H), kFinishThreads, 0, st>>>(lens, B, H, Lmax, plan.grid, p.ws_o,
+  latent_finish_kernel<<<dim3(B, H), kFinishThreads, 0, st>>>(p.ws_pref, B, H, plan.grid, p.ws_o,
                                                               p.ws_lse, p.o, lse, p.status);
   return launch_status();
 }

@@ -183,9 +183,10 @@ def test_workspace_sizes_are_consistent(L):
     assert binding.attn_decode_workspace_size(1, 30, 8, 128, 2048) == 0  # invalid -> 0
     # latent decode: 128 CTAs; with B = 128 each takes one whole sequence (no workspace),
     # otherwise the key tiles are split evenly over the CTAs and the pieces (B + 127 slots,
-    # 449 floats per head) are merged afterwards
+    # 449 floats per head) are merged afterwards, with the tile prefix sums (B + 1 ints)
     assert binding.attn_decode_latent_workspace_size(128, 16, 2048) == 0
-    assert binding.attn_decode_latent_workspace_size(8, 16, 2048) == (8 + 128 - 1) * 16 * 449 * 4
+    assert binding.attn_decode_latent_workspace_size(8, 16, 2048) == \
+        (8 + 128 - 1) * 16 * 449 * 4 + (8 + 1) * 4
     assert binding.attn_decode_latent_workspace_size(1, 16, 2048) > 0
 
 
