@@ -127,7 +127,7 @@ def prefill_traffic():
     import hashlib
     import re
 
-    prof = os.path.join(ROOT, "profiles", "prefill_fused_rope_s16384_dram.md")
+    prof = os.path.join(ROOT, "profiles", "prefill_attention_s16384_dram.md")
     src = os.path.join(ROOT, "attention_attn_prefill_02_gb300", "csrc", "prefill.cu")
     try:
         text = open(prof).read()
@@ -614,14 +614,16 @@ def single_case(args):
 
     torch.cuda.set_device(0)
     b.lib()
-    if args.case in ("prefill", "prefill-unfused", "prefill-d64"):
+    if args.case in ("prefill", "prefill-fused", "prefill-unfused", "prefill-d64"):
         D = 64 if args.case == "prefill-d64" else 128
         Hkv = 32 if D == 64 else 8
         causal = D == 128
         q, k, v = synthetic.prefill_inputs(4, 32, Hkv, args.S, D, "bf16", seed=1)
         q, k, v = q.cuda(), k.cuda(), v.cuda()
         b.attn_rope_table_reserve(D, THETA, args.S + 1)
-        rope = args.case == "prefill"
+        b.attn_prefill_reserve(4, 32, Hkv, args.S, D)
+        # prefill: RoPE as the library chooses; prefill-fused: Q and K rotated in the kernel
+        rope = {"prefill": 1, "prefill-fused": 2}.get(args.case, 0)
         fn = lambda: b.attn_prefill(q, k, v, causal=causal, rope=rope, rope_theta=THETA)
     elif args.case == "decode":
         q, kc, vc, cl = synthetic.decode_inputs(args.B, 32, 8, 2048, 128, 2048, seed=1)
@@ -658,7 +660,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--case", default=None,
-                    choices=["prefill", "prefill-unfused", "prefill-d64", "decode", "decode-fp8",
+                    choices=["prefill", "prefill-fused", "prefill-unfused", "prefill-d64",
+                             "decode", "decode-fp8",
                              "latent",
                              "rope"], help="time one kernel alone (for profiler captures)")
     ap.add_argument("--S", type=int, default=4096)
