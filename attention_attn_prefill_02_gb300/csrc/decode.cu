@@ -1437,77 +1437,75 @@ attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
 // history decode and the cache hold them.  One block per (sequence, KV head).
 // ------------------------------------------------------------------------------------------------
 
-constexpr int kAppendThreads = 128;
-
+// One block per (sequence, KV head), one warp per query head of the group.  Lane l owns the
+// rotation pairs i = 2l, 2l+1 (D = 128; i = l for D = 64), i.e. dims i and i + D/2, for the key,
+// the query and the merge.  The group's first warp writes the cache row.
 template <int D>
-__global__ void __launch_bounds__(kAppendThreads)
+__global__ void __launch_bounds__(16 * 32)
     append_merge_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
                         const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* k_cache,
                         __nv_bfloat16* v_cache, const int32_t* __restrict__ lens, int Lmax,
                         __nv_bfloat16* o, const float* __restrict__ lse_hist, float* lse_out,
                         int Hq, int Hkv, float scale, const float2* __restrict__ table,
                         unsigned int* status) {
-  __shared__ float kr[D];
-  __shared__ float red[kAppendThreads / 32];
-  const int b = blockIdx.x, kvh = blockIdx.y, tid = threadIdx.x;
+  constexpr int P = D / 64;  // pairs per lane
+  const int b = blockIdx.x, kvh = blockIdx.y;
+  const int g = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = Hq / Hkv;
   const int L = lens[b];
   if (L < 1 || L >= Lmax) {  // no history, or no row left for the new token
-    if (tid == 0 && kvh == 0) report_status(status, ATTN_ERR_DEVICE_ARG);
+    if (threadIdx.x == 0 && kvh == 0) report_status(status, ATTN_ERR_DEVICE_ARG);
     return;
   }
   const size_t kv = static_cast<size_t>(b) * Hkv + kvh;
   const size_t crow = (kv * Lmax + L) * D;
-  for (int i = tid; i < D / 2; i += kAppendThreads) {
-    float x1 = __bfloat162float(k_new[kv * D + i]);
-    float x2 = __bfloat162float(k_new[kv * D + i + D / 2]);
+  const size_t row = static_cast<size_t>(b) * Hq + kvh * G + g;
+  const int i0 = lane * P;
+  float k1[P], k2[P], q1[P], q2[P], v1[P], v2[P];
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    k1[j] = __bfloat162float(k_new[kv * D + i0 + j]);
+    k2[j] = __bfloat162float(k_new[kv * D + i0 + j + D / 2]);
+    q1[j] = __bfloat162float(q[row * D + i0 + j]);
+    q2[j] = __bfloat162float(q[row * D + i0 + j + D / 2]);
+    v1[j] = __bfloat162float(v_new[kv * D + i0 + j]);
+    v2[j] = __bfloat162float(v_new[kv * D + i0 + j + D / 2]);
+  }
+  float part = 0.f;
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    float c = 1.f, sn = 0.f;
     if (table) {
-      const float2 cs = table[static_cast<size_t>(L) * (D / 2) + i];
-      const float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
-      x1 = y1;
-      x2 = y2;
+      const float2 cs = table[static_cast<size_t>(L) * (D / 2) + i0 + j];
+      c = cs.x;
+      sn = cs.y;
     }
-    const __nv_bfloat16 r1 = __float2bfloat16_rn(x1), r2 = __float2bfloat16_rn(x2);
-    k_cache[crow + i] = r1;
-    k_cache[crow + i + D / 2] = r2;
-    kr[i] = __bfloat162float(r1);
-    kr[i + D / 2] = __bfloat162float(r2);
+    // key and query rotated at L and rounded to bf16, as the cache and the history hold them
+    const float kr1 = __bfloat162float(__float2bfloat16_rn(k1[j] * c - k2[j] * sn));
+    const float kr2 = __bfloat162float(__float2bfloat16_rn(k2[j] * c + k1[j] * sn));
+    const float qr1 = __bfloat162float(__float2bfloat16_rn(q1[j] * c - q2[j] * sn));
+    const float qr2 = __bfloat162float(__float2bfloat16_rn(q2[j] * c + q1[j] * sn));
+    part = fmaf(qr1, kr1, fmaf(qr2, kr2, part));
+    if (g == 0) {
+      k_cache[crow + i0 + j] = __float2bfloat16_rn(kr1);
+      k_cache[crow + i0 + j + D / 2] = __float2bfloat16_rn(kr2);
+      v_cache[crow + i0 + j] = v_new[kv * D + i0 + j];
+      v_cache[crow + i0 + j + D / 2] = v_new[kv * D + i0 + j + D / 2];
+    }
   }
-  for (int d = tid; d < D; d += kAppendThreads) v_cache[crow + d] = v_new[kv * D + d];
-  __syncthreads();
-  for (int g = 0; g < G; ++g) {
-    const size_t row = static_cast<size_t>(b) * Hq + kvh * G + g;
-    float part = 0.f;
-    for (int i = tid; i < D / 2; i += kAppendThreads) {
-      float x1 = __bfloat162float(q[row * D + i]);
-      float x2 = __bfloat162float(q[row * D + i + D / 2]);
-      if (table) {
-        const float2 cs = table[static_cast<size_t>(L) * (D / 2) + i];
-        const float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
-        x1 = y1;
-        x2 = y2;
-      }
-      x1 = __bfloat162float(__float2bfloat16_rn(x1));
-      x2 = __bfloat162float(__float2bfloat16_rn(x2));
-      part = fmaf(x1, kr[i], fmaf(x2, kr[i + D / 2], part));
-    }
 #pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
-    if ((tid & 31) == 0) red[tid >> 5] = part;
-    __syncthreads();
-    float sc = 0.f;
+  for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+  const float sc = part * scale;
+  const float lh = lse_hist[row];
+  const float a = 1.f / (1.f + expf(lh - sc));  // weight of the current token
 #pragma unroll
-    for (int w = 0; w < kAppendThreads / 32; ++w) sc += red[w];
-    sc *= scale;
-    const float lh = lse_hist[row];
-    const float a = 1.f / (1.f + expf(lh - sc));  // weight of the current token
-    for (int d = tid; d < D; d += kAppendThreads) {
-      const float oh = __bfloat162float(o[row * D + d]);
-      o[row * D + d] = __float2bfloat16_rn(fmaf(a, __bfloat162float(v_new[kv * D + d]) - oh, oh));
-    }
-    if (lse_out && tid == 0) lse_out[row] = fmaxf(lh, sc) + log1pf(expf(-fabsf(sc - lh)));
-    __syncthreads();  // red is rewritten for the next query head
+  for (int j = 0; j < P; ++j) {
+    __nv_bfloat16* orow = o + row * D;
+    const float oh1 = __bfloat162float(orow[i0 + j]), oh2 = __bfloat162float(orow[i0 + j + D / 2]);
+    orow[i0 + j] = __float2bfloat16_rn(fmaf(a, v1[j] - oh1, oh1));
+    orow[i0 + j + D / 2] = __float2bfloat16_rn(fmaf(a, v2[j] - oh2, oh2));
   }
+  if (lse_out && lane == 0) lse_out[row] = fmaxf(lh, sc) + log1pf(expf(-fabsf(sc - lh)));
 }
 
 // cache_len[b] += 1 where the append wrote a row (after every block of the merge has read it).
@@ -1530,6 +1528,7 @@ attn_status_t launch_decode_append(const void* q, const void* k_new, const void*
                                   scale, table, plan.ws_bytes ? ws : nullptr, plan, st);
   if (r != ATTN_OK) return r;
   const dim3 grid(B, Hkv);
+  const int threads = 32 * (Hq / Hkv);  // one warp per query head of the group (<= 16)
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
   const auto* kn = static_cast<const __nv_bfloat16*>(k_new);
   const auto* vn = static_cast<const __nv_bfloat16*>(v_new);
@@ -1537,11 +1536,11 @@ attn_status_t launch_decode_append(const void* q, const void* k_new, const void*
   auto* vc = static_cast<__nv_bfloat16*>(v_cache);
   auto* oo = static_cast<__nv_bfloat16*>(o);
   if (D == 128)
-    append_merge_kernel<128><<<grid, kAppendThreads, 0, st>>>(qq, kn, vn, kc, vc, lens, Lmax, oo,
+    append_merge_kernel<128><<<grid, threads, 0, st>>>(qq, kn, vn, kc, vc, lens, Lmax, oo,
                                                               lse_hist, lse, Hq, Hkv, scale,
                                                               table, device_status_ptr());
   else
-    append_merge_kernel<64><<<grid, kAppendThreads, 0, st>>>(qq, kn, vn, kc, vc, lens, Lmax, oo,
+    append_merge_kernel<64><<<grid, threads, 0, st>>>(qq, kn, vn, kc, vc, lens, Lmax, oo,
                                                              lse_hist, lse, Hq, Hkv, scale,
                                                              table, device_status_ptr());
   if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
