@@ -59,6 +59,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_decode.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp, sz, vp]
     L.attn_decode_noalloc.restype = i
     L.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp]
+    L.attn_set_decode_splits.restype = i
+    L.attn_set_decode_splits.argtypes = [i]
     L.attn_decode_append_workspace_size.restype = sz
     L.attn_decode_append_workspace_size.argtypes = [i, i, i, i, i]
     L.attn_decode_append.restype = i
@@ -199,6 +201,11 @@ def attn_decode_noalloc(q, k_cache, v_cache, cache_len, o=None, lse=None, want_l
                                      D, float(softmax_scale), int(bool(rope)), float(rope_theta),
                                      _stream(stream)), "attn_decode_noalloc")
     return (o, lse) if (want_lse or lse is not None) else o
+
+
+def attn_set_decode_splits(nsplit):
+    """nsplit > 0: force that split count for later decode calls; 0: the per-shape planner."""
+    _check(lib().attn_set_decode_splits(int(nsplit)), "attn_set_decode_splits")
 
 
 def attn_decode_append_workspace_size(B, Hq, Hkv, D, Lmax):

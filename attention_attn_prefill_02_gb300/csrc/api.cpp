@@ -201,6 +201,12 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
                        workspace, plan, as_stream(stream));
 }
 
+attn_status_t attn_set_decode_splits(int nsplit) {
+  if (nsplit < 0 || nsplit > 1024) return ATTN_ERR_INVALID_ARG;
+  force_decode_splits(nsplit);
+  return ATTN_OK;
+}
+
 size_t attn_decode_append_workspace_size(int B, int Hq, int Hkv, int D, int Lmax) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 2 || (D != 64 && D != 128) || Hq % Hkv) return 0;
   return append_ws_bytes(plan_decode(B, Hq, Hkv, D, Lmax), B, Hq);

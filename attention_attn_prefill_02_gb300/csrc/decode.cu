@@ -11,6 +11,7 @@
 // tile is the same observation).  Work items are (sequence, KV head, split of the key range);
 // splits are merged by their log-sum-exp ("A: group-entry queries and one joint history scan").
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <type_traits>
 
@@ -1279,11 +1280,11 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 // max(busiest CTA's bytes * ctas / 2, all cache bytes) plus the split partials written and read
 // back by the combine.
 DecodePlan plan_common(int units, int Lmax, int ctas, double key_bytes, int rows_per_unit,
-                       int out_dim) {
+                       int out_dim, int forced_split) {
   const int max_split = std::min(kMaxSplits, std::max(1, (Lmax + kTileKeys - 1) / kTileKeys));
   int best = 1;
   double best_cost = 1e300;
-  for (int ns = 1; ns <= max_split; ns *= 2) {
+  for (int ns = 1; ns <= max_split && forced_split <= 0; ns *= 2) {
     const int chunk = round_up((Lmax + ns - 1) / ns, kTileKeys);
     const int nsp = (Lmax + chunk - 1) / chunk;
     const double items = static_cast<double>(units) * nsp;
@@ -1297,6 +1298,7 @@ DecodePlan plan_common(int units, int Lmax, int ctas, double key_bytes, int rows
       best = nsp;
     }
   }
+  if (forced_split > 0) best = std::min(forced_split, max_split);
   DecodePlan pl;
   pl.chunk = round_up((Lmax + best - 1) / best, kTileKeys);
   pl.nsplit = (Lmax + pl.chunk - 1) / pl.chunk;
@@ -1353,9 +1355,14 @@ attn_status_t launch_gqa_typed(const void* q, const void* k, const void* v, cons
 
 }  // namespace
 
+std::atomic<int> g_forced_decode_splits{0};
+
 DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int Lmax) {
-  return plan_common(B * Hkv, Lmax, 2 * sm_count(), 2.0 * D * 2, Hq / Hkv, D);
+  return plan_common(B * Hkv, Lmax, 2 * sm_count(), 2.0 * D * 2, Hq / Hkv, D,
+                     g_forced_decode_splits.load());
 }
+
+void force_decode_splits(int nsplit) { g_forced_decode_splits.store(nsplit); }
 
 DecodePlan plan_latent(int B, int H, int Lmax) {
   (void)Lmax;

@@ -73,6 +73,8 @@ struct DecodePlan {
   size_t ws_bytes; // partial O (fp32) + partial LSE (fp32)
 };
 DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int Lmax);
+// nsplit > 0: every later GQA decode plan uses that split count; 0: the per-shape planner.
+void force_decode_splits(int nsplit);
 
 // Append decode workspace: the decode's own (rounded up to 256 bytes), then B*Hq floats.
 inline size_t append_ws_offset(const DecodePlan& pl) { return (pl.ws_bytes + 255) & ~size_t(255); }

@@ -240,6 +240,114 @@ def time_graph(fn, iters=20):
     return time_call(g.replay, iters=iters, warmup=2)
 
 
+def interleaved(fns, rounds=9, warmup=8, seed=0):
+    """The pages' timing protocol: `warmup` calls of every variant, then `rounds` rounds in which
+    the variants run once each in a seeded shuffled order.  CUDA events around each call.
+    Returns {name: {"median", "p10", "p90"}} in ms."""
+    import random
+
+    import torch
+
+    for _ in range(warmup):
+        for f in fns.values():
+            f()
+    torch.cuda.synchronize()
+    rng = random.Random(seed)
+    names = list(fns)
+    times = {n: [] for n in names}
+    for _ in range(rounds):
+        rng.shuffle(names)
+        for n in names:
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            fns[n]()
+            s1.record()
+            s1.synchronize()
+            times[n].append(s0.elapsed_time(s1))
+    out = {}
+    for n, ts in times.items():
+        ts = sorted(ts)
+        q = lambda f: ts[min(len(ts) - 1, int(round(f * (len(ts) - 1))))]
+        out[n] = {"median": round(statistics.median(ts), 5), "p10": round(q(0.1), 5),
+                  "p90": round(q(0.9), 5)}
+    return out
+
+
+def graph_of(fn):
+    """fn captured once in a CUDA graph (on a side stream); returns the replay callable."""
+    import torch
+
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            fn()
+    torch.cuda.current_stream().wait_stream(st)
+    torch.cuda.synchronize()
+    return g.replay
+
+
+def protocol(b, d):
+    """Every path eager vs graph, fused vs unfused RoPE, and global vs per-shape configuration,
+    in interleaved seeded-shuffled rounds (median, p10, p90)."""
+    import torch
+    from attention_attn_prefill_02_gb300 import synthetic
+
+    out = {}
+    qr, kr = torch.empty_like(d["q"]), torch.empty_like(d["k"])
+
+    def pf(rope):
+        return lambda: b.attn_prefill(d["q"], d["k"], d["v"], causal=True, rope=rope,
+                                      rope_theta=THETA, o=d["o"])
+
+    def unfused():
+        b.rope_apply(d["q"], qr, theta=THETA)
+        b.rope_apply(d["k"], kr, theta=THETA)
+        b.attn_prefill(qr, kr, d["v"], causal=True, rope=False, o=d["o"])
+
+    rope_pass = lambda: (b.rope_apply(d["q"], qr, theta=THETA), b.rope_apply(d["k"], kr, theta=THETA))
+    out["prefill_s16384"] = interleaved({
+        "rope1_eager": pf(1), "rope1_graph": graph_of(pf(1)), "fused_in_kernel_eager": pf(2),
+        "unfused_eager": unfused, "no_rope_eager": pf(False),
+        "rope_apply_qk_eager": rope_pass, "rope_apply_qk_graph": graph_of(rope_pass)})
+    dec = lambda: b.attn_decode(d["dq"], d["dk"], d["dv"], d["dl"], o=d["do"], rope=True,
+                                rope_theta=THETA, workspace=d.get("dws"))
+    lat = lambda: b.attn_decode_latent(d["lq"], d["lc"], d["ll"], o=d["lo"], rope=True,
+                                       rope_theta=THETA, workspace=d.get("lws"))
+    out["decode_b128"] = interleaved({"eager": dec, "graph": graph_of(dec)}, rounds=15)
+    out["latent_b128"] = interleaved({"eager": lat, "graph": graph_of(lat)}, rounds=15)
+    # global vs per-shape split-KV configuration: the per-shape planner against one split count
+    # for every batch (the planner's choice at batch 32), graph replay
+    Dd = DECODE
+    ws32 = b.attn_decode_workspace_size(32, Dd["Hq"], Dd["Hkv"], Dd["D"], Dd["L"])
+    g_split = max(1, ws32 // (32 * Dd["Hq"] * (Dd["D"] + 1) * 4))
+    cfg = {"global_split": g_split}
+    for B in (1, 8, 32, 128):
+        q, kc, vc, cl = synthetic.decode_inputs(B, Dd["Hq"], Dd["Hkv"], Dd["L"], Dd["D"], Dd["L"],
+                                                seed=8)
+        q, kc, vc, cl = q.cuda(), kc.cuda(), vc.cuda(), cl.cuda()
+        o = torch.empty((B, Dd["Hq"], Dd["D"]), dtype=torch.bfloat16, device="cuda")
+        fns, splits = {}, {}
+        for name, ns in (("per_shape", 0), ("global", g_split)):
+            b.attn_set_decode_splits(ns)
+            wsb = b.attn_decode_workspace_size(B, Dd["Hq"], Dd["Hkv"], Dd["D"], Dd["L"])
+            ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+            f = (lambda q=q, kc=kc, vc=vc, cl=cl, o=o, ws=ws:
+                 b.attn_decode(q, kc, vc, cl, o=o, rope=True, rope_theta=THETA, workspace=ws))
+            fns[name] = graph_of(f)  # the split is fixed into the captured launches
+            splits[name + "_splits"] = max(1, wsb // (B * Dd["Hq"] * (Dd["D"] + 1) * 4))
+        b.attn_set_decode_splits(0)
+        r = interleaved(fns, rounds=9, warmup=3)
+        cfg[str(B)] = {k: v["median"] for k, v in r.items()}
+        cfg[str(B)].update(splits)
+        del q, kc, vc, cl, o
+    out["decode_global_vs_per_shape_graph_ms"] = cfg
+    return out
+
+
 def variants(b, d):
     """Pages' lessons: eager vs graph, fused vs unfused RoPE, decode batch sweep, L2 residency."""
     import torch
@@ -532,6 +640,7 @@ def ours(args):
         line["e2e"] = e2e
     if rank == 0 and not args.no_variants:
         line["variants"] = variants(b, d)
+        line["protocol"] = protocol(b, d)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(seconds_budget=20.0)
     if rank == 0:
@@ -561,6 +670,43 @@ def oracle_prefill_sample(S: int, seed: int = 0):
     return workload.prefill_flops(1, 1, S, D, True), dt
 
 
+def oracle_decode_sample(B=1):
+    """The float64 oracle's GQA decode of the bench's decode shape for B sequences (seconds)."""
+    import oracle
+    from attention_attn_prefill_02_gb300 import synthetic
+
+    Dd = DECODE
+    q, kc, vc, cl = synthetic.decode_inputs(B, Dd["Hq"], Dd["Hkv"], Dd["L"], Dd["D"], Dd["L"])
+    args = [oracle.as_f64(x) for x in (q, kc, vc)]
+    t = time.perf_counter()
+    oracle.decode(*args, cl.numpy(), rope=True, theta=THETA)
+    return time.perf_counter() - t
+
+
+def oracle_tiny_sample():
+    """The float64 oracle on the tiny causal GQA config B=1 Hq=4 Hkv=1 S=128 D=64 with RoPE."""
+    import oracle
+    from attention_attn_prefill_02_gb300 import synthetic
+
+    q, k, v = synthetic.prefill_inputs(1, 4, 1, 128, 64, "bf16", seed=0)
+    args = [oracle.as_f64(x) for x in (q, k, v)]
+    t = time.perf_counter()
+    oracle.prefill(*args, causal=True, rope=True, theta=THETA)
+    return time.perf_counter() - t
+
+
+def oracle_one_core():
+    """One (batch, head) of the causal RoPE prefill at S=4096 with one BLAS / OpenMP thread (run
+    in a child process whose thread variables are set before NumPy loads)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-core"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    try:
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (ValueError, IndexError):
+        return None
+
+
 def cpu_baseline(seconds_budget=15.0):
     """The oracle as it stands on the host cores: (batch, head) samples of the bench's causal RoPE
     prefill at S=8192, one after another until about `seconds_budget` seconds of CPU work."""
@@ -574,7 +720,10 @@ def cpu_baseline(seconds_budget=15.0):
     return {"value": round(tot_f / tot_t / 1e12, 6), "unit": "TFLOPS", "cores": os.cpu_count(),
             "kind": "oracle",
             "sample": f"{n} (batch, head) samples of the causal RoPE prefill at S={S}, D=128, "
-                      f"float64 NumPy, {tot_t:.1f} s in total (NumPy's default BLAS threads)"}
+                      f"float64 NumPy, {tot_t:.1f} s in total (NumPy's default BLAS threads)",
+            "also": {"tiny_config_s": round(oracle_tiny_sample(), 4),
+                     "decode_b1_s": round(oracle_decode_sample(1), 4),
+                     "one_core_prefill_head_s4096": oracle_one_core()}}
 
 
 def reference(args):
@@ -659,6 +808,7 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--oracle-one-core", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--case", default=None,
                     choices=["prefill", "prefill-fused", "prefill-unfused", "prefill-d64",
                              "decode", "decode-fp8",
@@ -667,6 +817,10 @@ def main():
     ap.add_argument("--S", type=int, default=4096)
     ap.add_argument("--B", type=int, default=128)
     args = ap.parse_args()
+    if args.oracle_one_core:  # child of oracle_one_core(): thread variables already set
+        f, t = oracle_prefill_sample(4096)
+        print(json.dumps({"tflops": round(f / t / 1e12, 6), "seconds": round(t, 3), "threads": 1}))
+        return
     if args.case:
         return single_case(args)
     if args.warmup < 3 and args.impl == "ours":

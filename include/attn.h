@@ -212,6 +212,18 @@ ATTN_API attn_status_t attn_decode_noalloc(const void* q, const void* k_cache, c
                                   attn_stream_t stream);
 
 /*
+ * attn_set_decode_splits — the "one global configuration versus per-shape choice" comparison
+ * the Lesson page (shape adaptive attention negative 20260722, 다음에 기억할 것) asks every
+ * path to report, for the split-KV decode.  nsplit > 0: every later attn_decode,
+ * attn_decode_append and attn_decode_noalloc call (and their workspace sizes) splits each
+ * sequence's keys into nsplit chunks (at most one per 64-key tile) instead of the per-shape
+ * planner's choice; 0 restores the planner (the default).  Process-wide; set it only while no
+ * other thread plans a decode.
+ * Errors: INVALID_ARG (nsplit < 0 or > 1024).
+ */
+ATTN_API attn_status_t attn_set_decode_splits(int nsplit);
+
+/*
  * attn_decode_append — one decode step whose token joins the cache (growing decode).
  * Defines: the decode steps of a static append cache that grows by one row per step, run as
  * growing CUDA graphs (Fixed-budget decode audit — 2026-09-11, "Which implementation was

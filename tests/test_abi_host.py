@@ -127,6 +127,23 @@ def _decode(L, **kw):
     return L.attn_decode(*args.values(), _stream())
 
 
+def test_forced_decode_splits_change_the_plan(L):
+    """The global-split hook: the workspace follows the forced split, 0 restores the planner."""
+    planned = binding.attn_decode_workspace_size(1, 32, 8, 128, 2048)
+    assert L.attn_set_decode_splits(-1) == INVALID
+    assert L.attn_set_decode_splits(1025) == INVALID
+    try:
+        binding.attn_set_decode_splits(1)
+        assert binding.attn_decode_workspace_size(1, 32, 8, 128, 2048) == 0
+        binding.attn_set_decode_splits(4)
+        assert binding.attn_decode_workspace_size(1, 32, 8, 128, 2048) == 1 * 32 * 4 * 129 * 4
+        binding.attn_set_decode_splits(5000 // 64)  # more than one split per tile is capped
+        assert binding.attn_decode_workspace_size(1, 32, 8, 128, 640) == 1 * 32 * 10 * 129 * 4
+    finally:
+        binding.attn_set_decode_splits(0)
+    assert binding.attn_decode_workspace_size(1, 32, 8, 128, 2048) == planned
+
+
 def test_decode_validation(L):
     assert _decode(L, lens=None) == INVALID
     assert _decode(L, Lmax=0) == INVALID

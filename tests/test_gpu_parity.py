@@ -252,6 +252,21 @@ def test_decode_fp8_cache(B, Hq, Hkv, lens):
     check(lse.cpu(), rl, LSE_TOL, None, what="LSE fp8 cache")
 
 
+@pytest.mark.parametrize("nsplit", [1, 3, 32])
+def test_decode_forced_splits(nsplit):
+    """The global-split hook gives the same attention whatever the split count."""
+    q, kc, vc, cl = synthetic.decode_inputs(3, 32, 8, 2048, 128, [2048, 77, 1500], seed=60 + nsplit)
+    try:
+        binding.attn_set_decode_splits(nsplit)
+        o, lse = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda(), want_lse=True)
+        status_ok()
+    finally:
+        binding.attn_set_decode_splits(0)
+    ro, rl = oracle.decode(f64(q), f64(kc), f64(vc), cl.numpy(), rope=True, theta=10000.0)
+    check(o.cpu(), ro, what=f"O split {nsplit}")
+    check(lse.cpu(), rl, LSE_TOL, None, what=f"LSE split {nsplit}")
+
+
 def test_decode_bad_cache_len_sets_status():
     q, kc, vc, cl = synthetic.decode_inputs(2, 8, 2, 64, 64, [64, 64], seed=1)
     cl[1] = 65  # > Lmax
