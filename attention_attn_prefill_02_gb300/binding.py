@@ -69,7 +69,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_decode_latent_workspace_size.restype = sz
     L.attn_decode_latent_workspace_size.argtypes = [i, i, i]
     L.attn_decode_latent.restype = i
-    L.attn_decode_latent.argtypes = [vp, vp, vp, i, vp, vp, i, i, f, i, f, vp, sz, vp]
+    L.attn_decode_latent.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, f, i, f, vp, sz, vp]
     L.attn_rope_table_reserve.restype = i
     L.attn_rope_table_reserve.argtypes = [i, f, i]
     L.attn_get_device_status.restype = i
@@ -257,7 +257,8 @@ def attn_decode_latent(q, c_cache, cache_len, o=None, lse=None, want_lse=False,
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().attn_decode_latent(_ptr(q), _ptr(c_cache), _ptr(cache_len), Lmax, _ptr(o),
-                                    _ptr(lse), B, H, float(softmax_scale), int(bool(rope)),
+                                    _ptr(lse), DTYPE_CODES[c_cache.dtype], B, H,
+                                    float(softmax_scale), int(bool(rope)),
                                     float(rope_theta), _ptr(workspace), wbytes,
                                     _stream(stream)), "attn_decode_latent")
     return (o, lse) if (want_lse or lse is not None) else o

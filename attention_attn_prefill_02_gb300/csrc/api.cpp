@@ -254,7 +254,7 @@ size_t attn_decode_latent_workspace_size(int B, int H, int Lmax) {
 }
 
 attn_status_t attn_decode_latent(const void* q, const void* c_cache, const int32_t* cache_len,
-                                 int Lmax, void* o, float* lse, int B, int H,
+                                 int Lmax, void* o, float* lse, attn_dtype_t dtype, int B, int H,
                                  float softmax_scale, int rope, float rope_theta,
                                  void* workspace, size_t workspace_bytes, attn_stream_t stream) {
   if (!q || !c_cache || !cache_len || !o) return ATTN_ERR_INVALID_ARG;
@@ -262,6 +262,7 @@ attn_status_t attn_decode_latent(const void* q, const void* c_cache, const int32
   if ((reinterpret_cast<uintptr_t>(cache_len) & 3u) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Lmax < 1) return ATTN_ERR_INVALID_ARG;
   if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
   if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
@@ -280,8 +281,8 @@ attn_status_t attn_decode_latent(const void* q, const void* c_cache, const int32
     if (!tab) return st;
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(512.0f);
-  return launch_latent(q, c_cache, cache_len, Lmax, o, lse, B, H, scale, tab, workspace, plan,
-                       as_stream(stream));
+  return launch_latent(q, c_cache, cache_len, Lmax, o, lse, dtype, B, H, scale, tab, workspace,
+                       plan, as_stream(stream));
 }
 
 attn_status_t attn_rope_table_reserve(int D, float theta, int max_pos) {

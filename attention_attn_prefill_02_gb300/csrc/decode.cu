@@ -751,16 +751,29 @@ constexpr int kLatMaxB = 2048;  // sequences per call (the tile prefix sums live
 #endif
 constexpr int kLatMaxCtas = ATTN_LAT_MAX_CTAS;
 
+// Cache tile geometry: bf16 tiles of 64 keys x 512 dims (64 KB, three stages) or e5m2 tiles of
+// 64 keys x 512 bytes (32 KB, six stages); both rings hold 192 KB and arrive as TMA boxes of
+// 64 rows x 128 bytes with the 128-byte swizzle.
+template <bool F8>
+struct LatGeo {
+  static constexpr int kTileBytes = F8 ? kTileKeys * kLatQK : kLatTileBytes;
+  static constexpr int kStages = F8 ? 6 : kLatStages;
+  static constexpr int kBoxElems = F8 ? 128 : 64;
+  static constexpr int kBoxes = kLatQK / kBoxElems;
+};
+constexpr int kLatMaxStages = 6;
+
 struct LatSmem {
-  static constexpr int kQOff = kLatStages * kLatTileBytes;
+  static constexpr int kQOff = kLatStages * kLatTileBytes;  // 192 KB of stages for both dtypes
   static constexpr int kPOff = kQOff + 16 * kLatQPitch;
   static constexpr int kRedOff = kPOff + 2 * 16 * kLatPPitch;        // [2][warps][16] row max
   static constexpr int kLOff = kRedOff + 2 * kLatWarps * 16 * 4;      // [warps][16] row sums
   static constexpr int kScanOff = kLOff + kLatWarps * 16 * 4;         // [warps] scan scratch
   static constexpr int kPrefOff = kScanOff + 64;                      // [B + 1] tile prefix
   static constexpr int kBarOff = kPrefOff + (kLatMaxB + 1) * 4 + 60;
-  static constexpr int kBytes = kBarOff + 2 * kLatStages * 8 + 1024;
+  static constexpr int kBytes = kBarOff + 2 * kLatMaxStages * 8 + 1024;
 };
+static_assert(LatGeo<true>::kStages * LatGeo<true>::kTileBytes == LatSmem::kQOff, "ring size");
 
 struct LatParams {
   const __nv_bfloat16* q;
@@ -846,7 +859,9 @@ struct LatSegIter {
 };
 
 // Issues this CTA's tiles, in order, into the stage ring.  Run by one thread.
+template <bool F8>
 struct LatLoader {
+  using G = LatGeo<F8>;
   LatSegIter seg;
   LatSeg cur;
   int t0, stage;
@@ -865,12 +880,12 @@ struct LatLoader {
                        uint64_t* empty, const CUtensorMap* tm) {
     if (done) return true;
     if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) return false;
-    mbar_arrive_expect_tx(&full[stage], kLatTileBytes);
-    uint8_t* ct = smem + stage * kLatTileBytes;
+    mbar_arrive_expect_tx(&full[stage], G::kTileBytes);
+    uint8_t* ct = smem + stage * G::kTileBytes;
 #pragma unroll
-    for (int bx = 0; bx < kLatQK / 64; ++bx)
-      tma_load_3d(ct + bx * kTileKeys * 128, tm, &full[stage], bx * 64, t0, cur.b);
-    if (++stage == kLatStages) {
+    for (int bx = 0; bx < G::kBoxes; ++bx)
+      tma_load_3d(ct + bx * kTileKeys * 128, tm, &full[stage], bx * G::kBoxElems, t0, cur.b);
+    if (++stage == G::kStages) {
       stage = 0;
       phase ^= 1;
     }
@@ -883,21 +898,30 @@ struct LatLoader {
 // Absorbed latent decode, stream-K over all sequences' key tiles.  Per 64-key tile: warp w
 // scores keys 8w..8w+7 against the 16 query rows over all 512 dims (query fragments held in
 // registers, four independent MMA chains), the tile's row maximum and P go through shared
-// memory, then warp w accumulates output columns 56w..56w+55 over all 64 keys.  Thread 0
-// refills each stage as soon as all warps released it.
+// memory, then warp w accumulates its output columns over all 64 keys.  Thread 0 refills each
+// stage as soon as all warps released it.
+//
+// F8: an e5m2 cache.  Every e5m2 value is exactly an f16 value, so the MMAs run in f16 on values
+// widened in registers: key fragments are 4-byte reads of the swizzled tile (4 consecutive
+// dims, with the query fragments in the same dimension order), value fragments come from
+// ldmatrix.trans on the fp8 tile read as 16-bit pairs, split by byte permutes into an even-dim
+// and an odd-dim column tile of each 16-dim chunk; warp w owns chunks w, w + 8, w + 16, w + 24.
+template <bool F8>
 __global__ void __launch_bounds__(kLatThreads, 1)
     latent_decode_kernel(const __grid_constant__ CUtensorMap tmC, const LatParams p) {
+  using G = LatGeo<F8>;
+  constexpr int kNT = F8 ? 8 : kLatColsPerWarp / 8;  // output column tiles per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + LatSmem::kBarOff);
-  uint64_t* empty = full + kLatStages;
+  uint64_t* empty = full + kLatMaxStages;
   int* pref = reinterpret_cast<int*>(smem + LatSmem::kPrefOff);
   int* scan = reinterpret_cast<int*>(smem + LatSmem::kScanOff);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int tid = threadIdx.x;
   if (tid == 0) {
-    for (int s = 0; s < kLatStages; ++s) {
+    for (int s = 0; s < G::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kLatWarps);
     }
@@ -936,7 +960,7 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     hi = lat_range_lo(T, blockIdx.x + 1, gridDim.x);
   }
 
-  LatLoader loader;
+  LatLoader<F8> loader;
   if (tid == 0) {
     tma_prefetch_desc(&tmC);
     if (p.streamk)
@@ -946,7 +970,7 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     loader.stage = 0;
     loader.phase = 0;
     loader.advance(pref, p.B, p.lens, p.Lmax);
-    for (int s = 0; s < kLatStages; ++s) loader.next(p, pref, smem, full, empty, &tmC);
+    for (int s = 0; s < G::kStages; ++s) loader.next(p, pref, smem, full, empty, &tmC);
   }
   bool alive = true;
 
@@ -995,56 +1019,88 @@ __global__ void __launch_bounds__(kLatThreads, 1)
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
         const int idx = tid + k * kLatThreads, r = idx / kChunks, c = idx % kChunks;
-        *reinterpret_cast<uint4*>(qs + r * kLatQPitch + c * 16) = v[k];
+        uint4 w = v[k];
+        if constexpr (F8) {  // the query in f16 (values beyond f16 range are not supported)
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[k]);
+          __half2* o = reinterpret_cast<__half2*>(&w);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o[j] = __float22half2_rn(__bfloat1622float2(h[j]));
+        }
+        *reinterpret_cast<uint4*>(qs + r * kLatQPitch + c * 16) = w;
       }
     }
     lat_bar_sync();
     // ... then the 64 RoPE dims rotated at position len, pairs (i, i + 32)
     if (p.table) {
+      using QT = typename std::conditional<F8, __half, __nv_bfloat16>::type;
       for (int idx = tid; idx < 16 * (kLatRope / 2); idx += kLatThreads) {
         const int r = idx / (kLatRope / 2), i = idx % (kLatRope / 2);
-        __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(qs + r * kLatQPitch);
-        const float x1 = __bfloat162float(row[kLatV + i]);
-        const float x2 = __bfloat162float(row[kLatV + i + kLatRope / 2]);
+        QT* row = reinterpret_cast<QT*>(qs + r * kLatQPitch);
+        const float x1 = static_cast<float>(row[kLatV + i]);
+        const float x2 = static_cast<float>(row[kLatV + i + kLatRope / 2]);
         const float2 cs = p.table[static_cast<size_t>(len) * (kLatRope / 2) + i];
-        row[kLatV + i] = __float2bfloat16_rn(x1 * cs.x - x2 * cs.y);
-        row[kLatV + i + kLatRope / 2] = __float2bfloat16_rn(x2 * cs.x + x1 * cs.y);
+        row[kLatV + i] = static_cast<QT>(x1 * cs.x - x2 * cs.y);
+        row[kLatV + i + kLatRope / 2] = static_cast<QT>(x2 * cs.x + x1 * cs.y);
       }
     }
     lat_bar_sync();
     uint32_t qa[kLatQK / 16][4];  // the 16 x 512 query tile as A fragments, for the segment
+    if constexpr (F8) {
+      // logical k = 2t+e -> dim 16kk+4t+e, k = 8+2t+e -> dim 16kk+4t+2+e (the key reads' order)
 #pragma unroll
-    for (int kk = 0; kk < kLatQK / 16; ++kk)
-      ldsm_x4(qs_addr + (lane & 15) * kLatQPitch + (kk * 16 + (lane >> 4) * 8) * 2, qa[kk][0],
-              qa[kk][1], qa[kk][2], qa[kk][3]);
+      for (int kk = 0; kk < kLatQK / 16; ++kk) {
+        const uint8_t* r0 = qs + (lane >> 2) * kLatQPitch + (16 * kk + 4 * (lane & 3)) * 2;
+        qa[kk][0] = *reinterpret_cast<const uint32_t*>(r0);
+        qa[kk][1] = *reinterpret_cast<const uint32_t*>(r0 + 8 * kLatQPitch);
+        qa[kk][2] = *reinterpret_cast<const uint32_t*>(r0 + 4);
+        qa[kk][3] = *reinterpret_cast<const uint32_t*>(r0 + 8 * kLatQPitch + 4);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < kLatQK / 16; ++kk)
+        ldsm_x4(qs_addr + (lane & 15) * kLatQPitch + (kk * 16 + (lane >> 4) * 8) * 2, qa[kk][0],
+                qa[kk][1], qa[kk][2], qa[kk][3]);
+    }
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float acc[kLatColsPerWarp / 8][4];
+    float acc[kNT][4];
 #pragma unroll
-    for (int n = 0; n < kLatColsPerWarp / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int n = 0; n < kNT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
     for (int t0 = k0; t0 < k1; t0 += kTileKeys, ++tcount) {
       if (!mbar_wait(&full[stage], phase, p.status)) {
         alive = false;
         break;
       }
-      const uint32_t ct = smem_u32(smem + stage * kLatTileBytes);
+      const uint32_t ct = smem_u32(smem + stage * G::kTileBytes);
       const int par = tcount & 1;
       float s[4];  // rows g / g+8 x keys 8w + 2tq + {0,1}
       {
         float ch[4][4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) ch[c][0] = ch[c][1] = ch[c][2] = ch[c][3] = 0.f;
-        const int key = warp * kLatKeysPerWarp + (lane & 7);
-        const int mi = lane >> 3;  // matrix index: 16-byte dim chunk within a pair of k-steps
+        if constexpr (F8) {
+          const uint8_t* kt = smem + stage * G::kTileBytes;
+          const int key = warp * kLatKeysPerWarp + g;
 #pragma unroll
-        for (int kk = 0; kk < kLatQK / 16; kk += 2) {
-          const int c = kk * 2 + mi;  // dims 8c .. 8c+7
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
-          mma_bf16_16816(ch[kk & 3], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-          mma_bf16_16816(ch[(kk + 1) & 3], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2],
-                         qa[kk + 1][3], b2, b3);
+          for (int kk = 0; kk < kLatQK / 16; ++kk) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(
+                kt + (kk >> 3) * kTileKeys * 128 + sw128_offset(key, kk & 7) + 4 * tq);
+            mma_f16_16816(ch[kk & 3], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], e5m2x2_lo(w),
+                          e5m2x2_hi(w));
+          }
+        } else {
+          const int key = warp * kLatKeysPerWarp + (lane & 7);
+          const int mi = lane >> 3;  // matrix index: 16-byte dim chunk within a pair of k-steps
+#pragma unroll
+          for (int kk = 0; kk < kLatQK / 16; kk += 2) {
+            const int c = kk * 2 + mi;  // dims 8c .. 8c+7
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
+            mma_bf16_16816(ch[kk & 3], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+            mma_bf16_16816(ch[(kk + 1) & 3], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2],
+                           qa[kk + 1][3], b2, b3);
+          }
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) s[e] = (ch[0][e] + ch[1][e]) + (ch[2][e] + ch[3][e]);
@@ -1085,19 +1141,21 @@ __global__ void __launch_bounds__(kLatThreads, 1)
       const float e0 = fast_exp2(s[0] - base0), e1 = fast_exp2(s[1] - base0);
       const float e2 = fast_exp2(s[2] - base1), e3 = fast_exp2(s[3] - base1);
       const int col = warp * kLatKeysPerWarp + tq * 2;
-      *reinterpret_cast<uint32_t*>(pw + g * kLatPPitch + col * 2) = pack_bf16(e0, e1);
-      *reinterpret_cast<uint32_t*>(pw + (g + 8) * kLatPPitch + col * 2) = pack_bf16(e2, e3);
+      *reinterpret_cast<uint32_t*>(pw + g * kLatPPitch + col * 2) =
+          F8 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+      *reinterpret_cast<uint32_t*>(pw + (g + 8) * kLatPPitch + col * 2) =
+          F8 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
       l0 = l0 * c0 + (e0 + e1);
       l1 = l1 * c1 + (e2 + e3);
 #pragma unroll
-      for (int n = 0; n < kLatColsPerWarp / 8; ++n) {
+      for (int n = 0; n < kNT; ++n) {
         acc[n][0] *= c0;
         acc[n][1] *= c0;
         acc[n][2] *= c1;
         acc[n][3] *= c1;
       }
       lat_bar_sync();
-      // O[:, this warp's 56 columns] += P (16 x 64) * C[:, cols]
+      // O[:, this warp's columns] += P (16 x 64) * C[:, cols]
       const uint32_t ps_addr = ps_addr0 + par * 16 * kLatPPitch;
       const int cbase = (warp * kLatColsPerWarp) / 8;  // first 8-column chunk of this warp
 #pragma unroll
@@ -1105,6 +1163,20 @@ __global__ void __launch_bounds__(kLatThreads, 1)
         uint32_t a0, a1, a2, a3;
         ldsm_x4(ps_addr + (lane & 15) * kLatPPitch + (kk * 16 + (lane >> 4) * 8) * 2, a0, a1, a2,
                 a3);
+        if constexpr (F8) {
+          // chunk c = warp + 8 ci; matrices keys 0-7 / 8-15 of this step (lanes 0-15 address)
+          const int keyr = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+          for (int ci = 0; ci < 4; ++ci) {
+            const int c = warp + 8 * ci;
+            if (c >= kLatV / 16) continue;  // warp-uniform: warps 4-7 own three chunks
+            uint32_t r0, r1;
+            ldsm_x2_t(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(keyr, c & 7), r0, r1);
+            mma_f16_16816(acc[2 * ci], a0, a1, a2, a3, e5m2x2_even(r0), e5m2x2_even(r1));
+            mma_f16_16816(acc[2 * ci + 1], a0, a1, a2, a3, e5m2x2_odd(r0), e5m2x2_odd(r1));
+          }
+          continue;
+        }
         const int mi = lane >> 3;
         const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
@@ -1126,7 +1198,7 @@ __global__ void __launch_bounds__(kLatThreads, 1)
       if (lane == 0) mbar_arrive(&empty[stage]);
       if (tid == 0) alive = loader.next(p, pref, smem, full, empty, &tmC);
       __syncwarp();
-      if (++stage == kLatStages) {
+      if (++stage == G::kStages) {
         stage = 0;
         phase ^= 1;
       }
@@ -1153,8 +1225,33 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     const float lse0 = lt0 > 0.f ? m0 + log2f(lt0) : -INFINITY;
     const float lse1 = lt1 > 0.f ? m1 + log2f(lt1) : -INFINITY;
     const size_t slot = static_cast<size_t>(blockIdx.x) + b;  // unique per (CTA, sequence)
+    if constexpr (F8) {
+      // slot (ci, e) holds dims 16c + 4tq + e and 16c + 4tq + 2 + e: four consecutive dims per row
 #pragma unroll
-    for (int n = 0; n < kLatColsPerWarp / 8; ++n) {
+      for (int ci = 0; ci < 4; ++ci) {
+        const int c = warp + 8 * ci;
+        if (c >= kLatV / 16) continue;
+        const int d = 16 * c + 4 * tq;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = g + hh * 8;
+          if (r >= H) continue;
+          const float inv = hh ? inv1 : inv0;
+          const float o0 = acc[2 * ci][hh * 2] * inv, o1 = acc[2 * ci + 1][hh * 2] * inv;
+          const float o2 = acc[2 * ci][hh * 2 + 1] * inv, o3 = acc[2 * ci + 1][hh * 2 + 1] * inv;
+          if (sg.whole) {
+            const size_t row = static_cast<size_t>(b) * H + r;
+            *reinterpret_cast<uint2*>(p.o + row * kLatV + d) =
+                make_uint2(pack_bf16(o0, o1), pack_bf16(o2, o3));
+          } else {
+            *reinterpret_cast<float4*>(p.ws_o + (slot * H + r) * kLatV + d) =
+                make_float4(o0, o1, o2, o3);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < (F8 ? 0 : kLatColsPerWarp / 8); ++n) {
       const int d = warp * kLatColsPerWarp + n * 8 + tq * 2;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -1567,11 +1664,14 @@ attn_status_t launch_decode(const void* q, const void* k, const void* v, const i
 }
 
 attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, int Lmax, void* o,
-                            float* lse, int B, int H, float scale, const float2* table, void* ws,
-                            const DecodePlan& plan, cudaStream_t st) {
+                            float* lse, attn_dtype_t dt, int B, int H, float scale,
+                            const float2* table, void* ws, const DecodePlan& plan,
+                            cudaStream_t st) {
   if (B > kLatMaxB) return ATTN_ERR_UNSUPPORTED;
+  const bool f8 = dt == ATTN_FP8_E5M2;
   CUtensorMap tc;
-  if (!make_tmap_3d(&tc, c, 2, kLatQK, Lmax, B, 64, kTileKeys, 128)) return ATTN_ERR_CUDA;
+  if (!make_tmap_3d(&tc, c, f8 ? 1 : 2, kLatQK, Lmax, B, f8 ? 128 : 64, kTileKeys, 128))
+    return ATTN_ERR_CUDA;
   LatParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.lens = lens;
@@ -1589,9 +1689,9 @@ attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, i
   p.Lmax = Lmax;
   p.streamk = plan.nsplit;  // the plan marks stream-K mode with nsplit = 1
   p.scale_log2 = scale * 1.4426950408889634f;
-  if (!set_smem_attr(reinterpret_cast<const void*>(latent_decode_kernel), LatSmem::kBytes))
-    return ATTN_ERR_CUDA;
-  latent_decode_kernel<<<plan.grid, kLatThreads, LatSmem::kBytes, st>>>(tc, p);
+  auto kern = f8 ? latent_decode_kernel<true> : latent_decode_kernel<false>;
+  if (!set_smem_attr(reinterpret_cast<const void*>(kern), LatSmem::kBytes)) return ATTN_ERR_CUDA;
+  kern<<<plan.grid, kLatThreads, LatSmem::kBytes, st>>>(tc, p);
   if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
   if (!p.streamk) return ATTN_OK;
   latent_finish_kernel<<<dim3(B, H), kFinishThreads, 0, st>>>(p.ws_pref, B, H, plan.grid, p.ws_o,

@@ -99,8 +99,9 @@ attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
                                 const DecodePlan& plan, cudaStream_t st);
 
 attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, int Lmax, void* o,
-                            float* lse, int B, int H, float scale, const float2* table, void* ws,
-                            const DecodePlan& plan, cudaStream_t st);
+                            float* lse, attn_dtype_t dt, int B, int H, float scale,
+                            const float2* table, void* ws, const DecodePlan& plan,
+                            cudaStream_t st);
 
 // S query rows at positions Skv - S .. Skv - 1 against Skv keys (rows kv_pitch apart per head);
 // rope_k: the fused RoPE rotates the keys too (else only the queries).

@@ -56,10 +56,11 @@ def decode_inputs(B, Hq, Hkv, Lmax, D, cache_len, seed=0, dtype="bf16", cache_dt
     return q, k, v, lens
 
 
-def latent_inputs(B, H, Lmax, cache_len, d_qk=512, seed=0, dtype="bf16"):
-    """q [B,H,d_qk], latent cache [B,Lmax,d_qk], cache_len int32 [B]."""
+def latent_inputs(B, H, Lmax, cache_len, d_qk=512, seed=0, dtype="bf16", cache_dtype=None):
+    """q [B,H,d_qk], latent cache [B,Lmax,d_qk] (``cache_dtype``, default ``dtype``),
+    cache_len int32 [B]."""
     q = normal((B, H, d_qk), 1000 * seed + SEED_Q, dtype)
-    c = normal((B, Lmax, d_qk), 1000 * seed + SEED_LATENT, dtype)
+    c = normal((B, Lmax, d_qk), 1000 * seed + SEED_LATENT, dtype if cache_dtype is None else cache_dtype)
     if isinstance(cache_len, int):
         lens = torch.full((B,), cache_len, dtype=torch.int32)
     else:

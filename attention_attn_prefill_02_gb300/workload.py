@@ -42,9 +42,10 @@ def decode_flops(B, Hq, L, D):
 
 
 def latent_bytes(B, H, L, d_qk=512, d_v=448, dtype="bf16"):
-    """Compulsory HBM bytes: the latent cache rows once, q in, o out."""
+    """Compulsory HBM bytes: the latent cache rows once (cache storage type), q in and o out
+    (bf16)."""
     e = DTYPE_BYTES[dtype]
-    return B * L * d_qk * e + B * H * d_qk * e + B * H * d_v * 2
+    return B * L * d_qk * e + B * H * d_qk * 2 + B * H * d_v * 2
 
 
 def latent_flops(B, H, L, d_qk=512, d_v=448):

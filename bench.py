@@ -473,6 +473,17 @@ def variants(b, d):
     out["decode_fp8_cache_b128"] = {"graph_ms": round(tg, 5), "gbs": round(nbytes / tg / 1e6, 1),
                                     "frac_of_hbm": round(nbytes / tg / 1e6 / measured_peaks()[0], 4)}
     del q, kc, vc, cl, o
+    # fp8 e5m2 latent cache (half the bytes), batch 128
+    Lt = LATENT
+    lq, lc, ll = synthetic.latent_inputs(Lt["B"], Lt["H"], Lt["L"], Lt["L"], seed=6,
+                                         cache_dtype="fp8")
+    lq, lc, ll = lq.cuda(), lc.cuda(), ll.cuda()
+    lo = torch.empty((Lt["B"], Lt["H"], 448), dtype=torch.bfloat16, device="cuda")
+    tl = time_graph(lambda: b.attn_decode_latent(lq, lc, ll, o=lo, rope=True, rope_theta=THETA), 50)
+    nb = workload.latent_bytes(Lt["B"], Lt["H"], Lt["L"], dtype="fp8")
+    out["latent_fp8_cache_b128"] = {"graph_ms": round(tl, 5), "gbs": round(nb / tl / 1e6, 1),
+                                    "frac_of_hbm": round(nb / tl / 1e6 / measured_peaks()[0], 4)}
+    del lq, lc, ll, lo
     # growing decode: one CUDA graph of an append step (history decode + current-token merge +
     # cache write + length increment) replayed while the cache grows; lengths live on the
     # device, so the same graph serves every step

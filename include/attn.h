@@ -268,7 +268,9 @@ ATTN_API size_t attn_decode_latent_workspace_size(int B, int H, int Lmax);
  * W_UV applied by the caller to the latent output.
  *   q          [B,H,512] bfloat16: 448 absorbed-latent dims then 64 RoPE dims (the RoPE dims
  *              are rotated at position cache_len[b] when rope = 1).
- *   c_cache    [B,Lmax,512] bfloat16: per token the 448-dim latent then the 64-dim rotated key.
+ *   c_cache    [B,Lmax,512] of `dtype` (ATTN_BF16, or ATTN_FP8_E5M2 at half the bytes; every
+ *              e5m2 value is an exact f16, so the kernel runs f16 MMAs on the widened cache and
+ *              the query in f16): per token the 448-dim latent then the 64-dim rotated key.
  *              Scores use all 512 dims; values are the first 448 dims.
  *   cache_len  DEVICE int32 [B], as in attn_decode.
  *   o          [B,H,448] bfloat16.  lse: NULL or [B,H] float32.
@@ -277,10 +279,11 @@ ATTN_API size_t attn_decode_latent_workspace_size(int B, int H, int Lmax);
  *   may be computed in pieces that a second kernel merges; the workspace holds those pieces.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */
-ATTN_API attn_status_t attn_decode_latent(const void* q, const void* c_cache, const int32_t* cache_len,
-                                 int Lmax, void* o, float* lse, int B, int H,
-                                 float softmax_scale, int rope, float rope_theta,
-                                 void* workspace, size_t workspace_bytes, attn_stream_t stream);
+ATTN_API attn_status_t attn_decode_latent(const void* q, const void* c_cache,
+                                          const int32_t* cache_len, int Lmax, void* o, float* lse,
+                                          attn_dtype_t dtype, int B, int H, float softmax_scale,
+                                          int rope, float rope_theta, void* workspace,
+                                          size_t workspace_bytes, attn_stream_t stream);
 
 /*
  * attn_rope_table_reserve — build (if needed) the cos/sin table for head dim D and base theta

@@ -180,7 +180,7 @@ def test_decode_append_validation(L):
 
 
 def _latent(L, **kw):
-    args = dict(q=FAKE, c=FAKE, lens=FAKE2, Lmax=2048, o=FAKE2, lse=None, B=128, H=16,
+    args = dict(q=FAKE, c=FAKE, lens=FAKE2, Lmax=2048, o=FAKE2, lse=None, dt=0, B=128, H=16,
                 scale=0.0, rope=1, theta=1e4, ws=FAKE2, wsb=1 << 30)
     args.update(kw)
     return L.attn_decode_latent(*args.values(), _stream())
@@ -191,6 +191,7 @@ def test_latent_validation(L):
     assert _latent(L, H=0) == INVALID
     assert _latent(L, H=17) == UNSUPPORTED
     assert _latent(L, q=MIS) == INVALID
+    assert _latent(L, dt=7) == INVALID
 
 
 def test_workspace_sizes_are_consistent(L):

@@ -422,6 +422,22 @@ def test_latent_decode(B, H, Lmax, lens):
     check(lse.cpu(), rl, LSE_TOL, None, what="LSE")
 
 
+@pytest.mark.parametrize("B,H,Lmax,lens", [
+    (4, 16, 2048, [2048, 1, 1000, 64]),
+    (128, 16, 2048, 2048),                 # one whole sequence per CTA
+    (2, 5, 200, [200, 37]),
+    (160, 16, 256, [256 - (i % 7) * 33 for i in range(160)]),
+])
+def test_latent_decode_fp8_cache(B, H, Lmax, lens):
+    """e5m2 latent cache (q bf16): widened exactly to f16 in the MMAs, so the bf16 bounds apply."""
+    q, c, cl = synthetic.latent_inputs(B, H, Lmax, lens, seed=B + 7, cache_dtype="fp8")
+    o, lse = binding.attn_decode_latent(q.cuda(), c.cuda(), cl.cuda(), want_lse=True)
+    status_ok()
+    ro, rl = oracle.latent_decode(f64(q), f64(c), cl.numpy(), rope=True, theta=10000.0)
+    check(o.cpu(), ro, what="O fp8 latent")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE fp8 latent")
+
+
 def test_latent_bad_cache_len_sets_status():
     q, c, cl = synthetic.latent_inputs(3, 16, 128, [128, 128, 50], seed=6)
     cl[1] = 0  # out of range
