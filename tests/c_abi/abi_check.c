@@ -1,0 +1,65 @@
+/* Plain C99 use of the library's C ABI: the header compiles as C, every call links, and
+ * argument validation answers without a device (nothing here is ever launched). */
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "attn.h"
+
+static int failures = 0;
+
+static void expect(const char* what, attn_status_t got, attn_status_t want) {
+  if (got != want) {
+    printf("FAIL %s: got %d (%s), want %d\n", what, (int)got, attn_status_string(got), (int)want);
+    ++failures;
+  }
+}
+
+int main(void) {
+  /* 16-byte aligned fake device addresses: never dereferenced, validation fails first */
+  void* a = (void*)(uintptr_t)0x7F0000000000ull;
+  void* o = (void*)(uintptr_t)0x7F0000100000ull;
+  void* mis = (void*)(uintptr_t)0x7F0000000008ull;
+  if (attn_version() < 100) {
+    printf("FAIL attn_version\n");
+    ++failures;
+  }
+  if (strcmp(attn_status_string(ATTN_OK), attn_status_string(ATTN_ERR_INVALID_ARG)) == 0) {
+    printf("FAIL status strings\n");
+    ++failures;
+  }
+  expect("rope_apply null", rope_apply(NULL, o, ATTN_BF16, 1, 1, 1, 64, 0, 1e4f, NULL),
+         ATTN_ERR_INVALID_ARG);
+  expect("prefill misaligned",
+         attn_prefill(a, a, a, mis, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 1, 4, 1, 128, 64, 1, 0.f, 1,
+                      1e4f, 0, NULL),
+         ATTN_ERR_INVALID_ARG);
+  expect("prefill head dim",
+         attn_prefill(a, a, a, o, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 1, 4, 1, 128, 96, 1, 0.f, 1,
+                      1e4f, 0, NULL),
+         ATTN_ERR_UNSUPPORTED);
+  expect("chunk lengths",
+         attn_prefill_chunk(a, a, a, o, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 1, 4, 1, 64, 32, 64, 64,
+                            0.f, 1, 1e4f, 0, NULL),
+         ATTN_ERR_INVALID_ARG);
+  expect("decode groups",
+         attn_decode(a, a, a, (const int32_t*)o, 2048, o, NULL, ATTN_BF16, 1, 30, 8, 128, 0.f, 1,
+                     1e4f, o, 1u << 20, NULL),
+         ATTN_ERR_INVALID_ARG);
+  expect("append no workspace",
+         attn_decode_append(a, a, a, a, a, (int32_t*)o, 2048, o, NULL, ATTN_BF16, 1, 32, 8, 128,
+                            0.f, 1, 1e4f, NULL, 0, NULL),
+         ATTN_ERR_INVALID_ARG);
+  expect("latent heads",
+         attn_decode_latent(a, a, (const int32_t*)o, 2048, o, NULL, ATTN_BF16, 1, 17, 0.f, 1,
+                            1e4f, o, 1u << 20, NULL),
+         ATTN_ERR_UNSUPPORTED);
+  expect("split hook range", attn_set_decode_splits(-1), ATTN_ERR_INVALID_ARG);
+  expect("reserve sizes", attn_prefill_reserve(0, 1, 1, 128, 128), ATTN_ERR_INVALID_ARG);
+  if (attn_decode_workspace_size(1, 30, 8, 128, 2048) != 0) {
+    printf("FAIL workspace size of an invalid shape\n");
+    ++failures;
+  }
+  printf(failures ? "abi_check: %d failures\n" : "abi_check: ok\n", failures);
+  return failures ? 1 : 0;
+}
