@@ -105,6 +105,7 @@ struct Params {
   int off;    // absolute position of query row i is i + off (off = Skv - S: bottom-right causal)
   int rope_k;  // fused RoPE: rotate the K tiles too (0: keys arrive rotated, only q is rotated)
   int n_items, nM, nKV;
+  int mblk;   // query-block levels per scheduling block (see item_coords)
   float c_log2;   // softmax_scale * q_scale * k_scale * log2(e)
   float v_scale;
   const float2* table;  // RoPE cos/sin [position][D/2] (fused RoPE only)
@@ -120,14 +121,22 @@ struct Bars {
   uint32_t tmem_slot;
 };
 
-// Item -> (query block m, batch b, query head hq).  Causal items go heaviest (largest m) first.
+// Item -> (query block m, batch b, query head hq).  Items are grouped so that the CTAs running
+// at the same time read few K/V streams (one stream = the keys and values of one (batch, KV
+// head)), which keeps the streams they share resident in L2: query blocks are taken in blocks of
+// `mblk` levels (heaviest levels first when causal); inside a block, stream by stream, and for
+// each stream level by level over the G query heads that read it.
 __device__ __forceinline__ void item_coords(const Params& p, int it, int& m, int& b, int& hq) {
-  const int per_m = p.B * p.Hq;
-  const int mi = it / per_m;
-  const int rest = it - mi * per_m;
-  m = p.causal ? (p.nM - 1 - mi) : mi;
-  b = rest / p.Hq;
-  hq = rest - b * p.Hq;
+  const int per_blk = p.mblk * p.B * p.Hq;
+  const int k = it / per_blk;
+  const int nb = min(p.mblk, p.nM - k * p.mblk);  // levels in block k (the last may be short)
+  const int idx = it - k * per_blk;
+  const int s = idx / (nb * p.G);
+  const int rem = idx - s * nb * p.G;
+  const int li = k * p.mblk + rem / p.G;
+  b = s / p.Hkv;
+  hq = (s - b * p.Hkv) * p.G + rem % p.G;
+  m = p.causal ? (p.nM - 1 - li) : li;
 }
 
 // KV tiles Q tile starting at row r0 must visit (0 when the tile is past the queries): causal
@@ -848,6 +857,9 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   p.nM = (S + kRowsPerItem - 1) / kRowsPerItem;
   p.nKV = (Skv + BN - 1) / BN;
   p.n_items = p.nM * B * Hq;
+  // causal: blocks of levels give each stream at least 16 items per block while keeping the
+  // heaviest levels first; otherwise all levels of a stream run together
+  p.mblk = causal ? std::max(1, 16 / p.G) : p.nM;
   p.c_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
   p.v_scale = v_scale;
   p.table = table;
