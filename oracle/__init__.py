@@ -7,5 +7,6 @@ them.  See ``oracle/attention_fp64.py`` for the definitions and the readings of 
 from .attention_fp64 import (  # noqa: F401
     LATENT_DIM, LATENT_ROPE_DIM, as_f64, attention, attention_probs, combine_partials, decode,
     decode_append, latent_decode, prefill_chunk, merge_one_key, prefill, prefill_rows, rope_inv_freq, rope_rotate_half,
+    ROPE_STYLES, rope_rotate, rope_rotate_interleaved,
     scores, softmax_rows, split_decode_partials,
 )

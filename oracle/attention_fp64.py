@@ -13,7 +13,9 @@ Where the pages are silent, the readings used are (each is repeated in the desig
 
 * RoPE is the rotate-half pairing (i, i + D/2) with inverse frequency theta^(-2i/D).  The pages
   only name "RoPE-attention fusion" (Lesson: shape adaptive attention negative 20260722, rows
-  "해본 것" / "당시 조건").
+  "해본 것" / "당시 조건").  The other common convention, adjacent pairs (2i, 2i + 1) rotated by
+  the same angles ("interleaved"), is available as ``rope_style="interleaved"``; the pages do not
+  name a convention, so both are offered and the half-split one is the default.
 * Query head hq reads KV head hq // G with G = Hq / Hkv (contiguous grouping).
 * Causal masking hides key j from query i when j > i + (Skv - Sq) (bottom-right alignment; the
   workloads only use Sq == Skv, where this is the usual j > i).
@@ -68,6 +70,37 @@ def rope_rotate_half(x: np.ndarray, positions: np.ndarray, theta: float) -> np.n
     x1 = x[..., : D // 2]
     x2 = x[..., D // 2:]
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def rope_rotate_interleaved(x: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
+    """Rotate each adjacent pair (x_{2i}, x_{2i+1}) of the last axis by pos * theta^(-2i/D).
+
+    The interleaved convention: x'_{2i} = x_{2i} cos a - x_{2i+1} sin a and
+    x'_{2i+1} = x_{2i+1} cos a + x_{2i} sin a, with the same angle a for pair i as the
+    rotate-half form uses for its pair (i, i + D/2).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    assert D % 2 == 0
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * rope_inv_freq(D, theta)[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    out = np.empty_like(x)
+    even, odd = x[..., 0::2], x[..., 1::2]
+    out[..., 0::2] = even * c - odd * s
+    out[..., 1::2] = odd * c + even * s
+    return out
+
+
+ROPE_STYLES = ("half", "interleaved")
+
+
+def rope_rotate(x: np.ndarray, positions: np.ndarray, theta: float, style: str = "half"):
+    """RoPE in the given pairing convention ("half": (i, i + D/2); "interleaved": (2i, 2i+1))."""
+    if style == "half":
+        return rope_rotate_half(x, positions, theta)
+    if style == "interleaved":
+        return rope_rotate_interleaved(x, positions, theta)
+    raise ValueError(f"unknown RoPE style {style!r}")
 
 
 # --------------------------------------------------------------------------------------------
@@ -139,7 +172,8 @@ def attention_probs(q, k, causal: bool, scale: float | None = None):
     return P
 
 
-def prefill(q, k, v, causal=True, scale=None, rope=False, theta=10000.0, pos0=0):
+def prefill(q, k, v, causal=True, scale=None, rope=False, theta=10000.0, pos0=0,
+            rope_style="half"):
     """Prefill: optionally rotate Q and K at positions pos0 .. pos0+S-1, then attention.
 
     Positions follow the reading that prefill tokens sit at 0..S-1 (pos0 = 0) on a fresh
@@ -149,12 +183,13 @@ def prefill(q, k, v, causal=True, scale=None, rope=False, theta=10000.0, pos0=0)
     if rope:
         pos_q = pos0 + np.arange(q.shape[2])
         pos_k = pos0 + np.arange(k.shape[2])
-        q = rope_rotate_half(q, pos_q, theta)
-        k = rope_rotate_half(k, pos_k, theta)
+        q = rope_rotate(q, pos_q, theta, rope_style)
+        k = rope_rotate(k, pos_k, theta, rope_style)
     return attention(q, k, v, causal, scale)
 
 
-def prefill_rows(q, k, v, rows, causal=True, scale=None, rope=False, theta=10000.0, pos0=0):
+def prefill_rows(q, k, v, rows, causal=True, scale=None, rope=False, theta=10000.0, pos0=0,
+                 rope_style="half"):
     """Selected output rows of ``prefill`` (for sizes where the full oracle is too slow).
 
     ``rows`` is a list of (b, hq, i).  Each row is computed by the same definition: rotate the
@@ -174,12 +209,12 @@ def prefill_rows(q, k, v, rows, causal=True, scale=None, rope=False, theta=10000
         if key not in cache:
             kk = k[b, h]
             if rope:
-                kk = rope_rotate_half(kk, pos0 + np.arange(kk.shape[0]), theta)
+                kk = rope_rotate(kk, pos0 + np.arange(kk.shape[0]), theta, rope_style)
             cache[key] = kk
         kk = cache[key]
         qi = q[b, hq, i][None, :]
         if rope:
-            qi = rope_rotate_half(qi, np.array([pos0 + i]), theta)
+            qi = rope_rotate(qi, np.array([pos0 + i]), theta, rope_style)
         s = scores(qi, kk, scale, causal, q_pos=np.array([i + (kk.shape[0] - S)]))
         m = np.max(s)
         e = np.exp(s - m)
@@ -189,7 +224,8 @@ def prefill_rows(q, k, v, rows, causal=True, scale=None, rope=False, theta=10000
     return np.array(out_o), np.array(out_l)
 
 
-def decode(q, k_cache, v_cache, cache_len, scale=None, rope=True, theta=10000.0):
+def decode(q, k_cache, v_cache, cache_len, scale=None, rope=True, theta=10000.0,
+           rope_style="half"):
     """Single-token decode against a static cache.
 
     q [B,Hq,D]; k_cache/v_cache [B,Hkv,Lmax,D] (keys stored already rotated); cache_len [B].
@@ -207,7 +243,7 @@ def decode(q, k_cache, v_cache, cache_len, scale=None, rope=True, theta=10000.0)
         assert 1 <= L <= kc.shape[2]
         qb = q[b][:, None, :]  # [Hq, 1, D]
         if rope:
-            qb = rope_rotate_half(qb, np.array([L]), theta)
+            qb = rope_rotate(qb, np.array([L]), theta, rope_style)
         o, lse = attention(qb[None], kc[b: b + 1, :, :L], vc[b: b + 1, :, :L], causal=False,
                            scale=scale)
         O[b] = o[0, :, 0]
@@ -215,7 +251,8 @@ def decode(q, k_cache, v_cache, cache_len, scale=None, rope=True, theta=10000.0)
     return O, LSE
 
 
-def prefill_chunk(q, k, v, skv, scale=None, rope=False, theta=10000.0, pos0=0):
+def prefill_chunk(q, k, v, skv, scale=None, rope=False, theta=10000.0, pos0=0,
+                  rope_style="half"):
     """One chunk of a prompt against the keys before it and its own (chunked prefill).
 
     The prompt is prefilled a chunk at a time into a static cache before decoding (Fixed-budget
@@ -228,12 +265,12 @@ def prefill_chunk(q, k, v, skv, scale=None, rope=False, theta=10000.0, pos0=0):
     Sq = q.shape[2]
     assert 1 <= Sq <= skv <= k.shape[2]
     if rope:
-        q = rope_rotate_half(q, pos0 + skv - Sq + np.arange(Sq), theta)
+        q = rope_rotate(q, pos0 + skv - Sq + np.arange(Sq), theta, rope_style)
     return attention(q, k[:, :, :skv], v[:, :, :skv], causal=True, scale=scale)
 
 
 def decode_append(q, k_cache, v_cache, cache_len, k_new, v_new, scale=None, rope=True,
-                  theta=10000.0):
+                  theta=10000.0, rope_style="half"):
     """Decode step that also attends the current token, whose key/value join the cache.
 
     Sequence b's query and new key sit at position L = cache_len[b]; both are rotated there when
@@ -254,8 +291,8 @@ def decode_append(q, k_cache, v_cache, cache_len, k_new, v_new, scale=None, rope
         kr = kn[b][:, None, :]  # [Hkv, 1, D]
         qb = q[b][:, None, :]
         if rope:
-            kr = rope_rotate_half(kr, np.array([L]), theta)
-            qb = rope_rotate_half(qb, np.array([L]), theta)
+            kr = rope_rotate(kr, np.array([L]), theta, rope_style)
+            qb = rope_rotate(qb, np.array([L]), theta, rope_style)
         K_ROW[b] = kr[:, 0]
         keys = np.concatenate([kc[b, :, :L], kr], axis=1)
         vals = np.concatenate([vc[b, :, :L], vn[b][:, None, :]], axis=1)
@@ -266,7 +303,7 @@ def decode_append(q, k_cache, v_cache, cache_len, k_new, v_new, scale=None, rope
 
 
 def latent_decode(q, c_cache, cache_len, scale=None, rope=True, theta=10000.0,
-                  d_latent=LATENT_DIM, d_rope=LATENT_ROPE_DIM):
+                  d_latent=LATENT_DIM, d_rope=LATENT_ROPE_DIM, rope_style="half"):
     """Absorbed latent (MLA-style) decode.
 
     q [B,H,d_latent+d_rope]; c_cache [B,Lmax,d_latent+d_rope] (rope part stored rotated);
@@ -287,7 +324,8 @@ def latent_decode(q, c_cache, cache_len, scale=None, rope=True, theta=10000.0,
         assert 1 <= L <= c.shape[1]
         qb = q[b].copy()
         if rope:
-            qb[:, d_latent:] = rope_rotate_half(qb[:, None, d_latent:], np.array([L]), theta)[:, 0]
+            qb[:, d_latent:] = rope_rotate(qb[:, None, d_latent:], np.array([L]), theta,
+                                           rope_style)[:, 0]
         cb = c[b, :L]
         o, lse = attention(qb[None, :, None, :], cb[None, None], cb[None, None, :, :d_latent],
                            causal=False, scale=scale)

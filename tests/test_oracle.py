@@ -177,6 +177,74 @@ def pin_rope(rope=O.rope_rotate_half):
                                atol=1e-12)
 
 
+def _il_to_half(D):
+    """Index map taking the interleaved layout to the rotate-half one: dims 0, 2, 4, .. then
+    1, 3, 5, ..  (pair (2i, 2i+1) lands on (i, i + D/2))."""
+    return np.concatenate([np.arange(0, D, 2), np.arange(1, D, 2)])
+
+
+def pin_rope_interleaved(rope=O.rope_rotate_interleaved, rope_half=O.rope_rotate_half):
+    D, n = 16, 11
+    x = rnd(3, n, D)
+    pos = np.arange(n) * 37 + 5
+    y = rope(x, pos, 10000.0)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), atol=1e-12)
+    np.testing.assert_allclose(rope(x, np.zeros(n), 10000.0), x, rtol=0, atol=0)
+    q, k = rnd(1, 1, D), rnd(1, 1, D)
+    for (m, nn, t) in [(3, 1, 100), (0, 7, 2048), (16000, 5, 123)]:
+        a = np.sum(rope(q, [m], 500.0) * rope(k, [nn], 500.0))
+        b = np.sum(rope(q, [m + t], 500.0) * rope(k, [nn + t], 500.0))
+        assert abs(a - b) < 1e-9
+    # D = 4, theta = 100: adjacent pairs (0,1) at angle p and (2,3) at angle p/10
+    p = 10.0
+    out = rope(np.array([[[1.0, 2.0, 3.0, 4.0]]]), [p], 100.0)[0, 0]
+    c0, s0, c1, s1 = math.cos(p), math.sin(p), math.cos(p / 10), math.sin(p / 10)
+    np.testing.assert_allclose(out, [c0 - 2 * s0, 2 * c0 + s0, 3 * c1 - 4 * s1, 4 * c1 + 3 * s1],
+                               atol=1e-12)
+    # the same rotation as the (separately pinned) rotate-half form on re-ordered dims
+    perm = _il_to_half(D)
+    np.testing.assert_allclose(rope(x, pos, 10000.0)[..., perm], rope_half(x[..., perm], pos, 10000.0),
+                               atol=1e-12)
+
+
+def pin_rope_style_through_entry_points(prefill=O.prefill, decode=O.decode,
+                                        latent=O.latent_decode, append=O.decode_append,
+                                        chunk=O.prefill_chunk):
+    """With interleaved RoPE every entry point equals the half-split one on inputs whose q/k
+    dims are re-ordered the same way (scores are invariant under a common permutation)."""
+    D = 8
+    perm = _il_to_half(D)
+    q, k, v = rnd(1, 4, 6, D), rnd(1, 2, 6, D), rnd(1, 2, 6, D)
+    a = prefill(q, k, v, causal=True, rope=True, theta=50.0, pos0=3, rope_style="interleaved")
+    b = prefill(q[..., perm], k[..., perm], v, causal=True, rope=True, theta=50.0, pos0=3)
+    for x, y in zip(a, b):
+        np.testing.assert_allclose(x, y, atol=1e-12)
+    a = chunk(q[:, :, :2], k, v, 5, rope=True, theta=50.0, pos0=1, rope_style="interleaved")
+    b = chunk(q[:, :, :2][..., perm], k[..., perm], v, 5, rope=True, theta=50.0, pos0=1)
+    for x, y in zip(a, b):
+        np.testing.assert_allclose(x, y, atol=1e-12)
+    qd, lens = rnd(2, 4, D), np.array([3, 6])
+    kc, vc = rnd(2, 2, 7, D), rnd(2, 2, 7, D)
+    a = decode(qd, kc, vc, lens, theta=50.0, rope_style="interleaved")
+    b = decode(qd[..., perm], kc[..., perm], vc, lens, theta=50.0)
+    for x, y in zip(a, b):
+        np.testing.assert_allclose(x, y, atol=1e-12)
+    kn, vn = rnd(2, 2, D), rnd(2, 2, D)
+    a = append(qd, kc, vc, lens, kn, vn, theta=50.0, rope_style="interleaved")
+    b = append(qd[..., perm], kc[..., perm], vc, lens, kn[..., perm], vn, theta=50.0)
+    np.testing.assert_allclose(a[0], b[0], atol=1e-12)
+    np.testing.assert_allclose(a[1], b[1], atol=1e-12)
+    np.testing.assert_allclose(a[2][..., perm], b[2], atol=1e-12)  # the stored key, re-ordered
+    dl, dr = 6, 8  # latent: only the last dr dims rotate; re-order those
+    pl = np.concatenate([np.arange(dl), dl + _il_to_half(dr)])
+    ql, cl = rnd(2, 3, dl + dr), rnd(2, 5, dl + dr)
+    a = latent(ql, cl, np.array([2, 5]), theta=50.0, d_latent=dl, d_rope=dr,
+               rope_style="interleaved")
+    b = latent(ql[..., pl], cl[..., pl], np.array([2, 5]), theta=50.0, d_latent=dl, d_rope=dr)
+    for x, y in zip(a, b):
+        np.testing.assert_allclose(x, y, atol=1e-12)
+
+
 def pin_latent_absorbed_equals_explicit(latent=O.latent_decode):
     """Absorbed attention over the shared latent equals the explicit up-projected form.
 
@@ -284,7 +352,8 @@ ALL_PINS = [pin_softmax_sums_to_one, pin_zero_query_is_causal_mean, pin_hand_two
             pin_one_hot_and_single_key, pin_causal_ignores_future, pin_matches_torch_sdpa,
             pin_bruteforce_enumeration, pin_gqa_equals_repeated_mha, pin_rope,
             pin_latent_absorbed_equals_explicit, pin_merge_identity,
-            pin_chunk_equals_prompt_rows, pin_append_equals_longer_prompt]
+            pin_chunk_equals_prompt_rows, pin_append_equals_longer_prompt, pin_rope_interleaved,
+            pin_rope_style_through_entry_points]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -434,6 +503,42 @@ def _mutant_rope(kind):
             return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], -1)[..., ::-1]
         return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], -1)
     return rope
+
+
+def _mutant_rope_interleaved(kind):
+    def rope(x, positions, theta):
+        x = np.asarray(x, np.float64)
+        D = x.shape[-1]
+        i = np.arange(D // 2)
+        if kind == "pair_freq_index":  # pair i at the frequency of dim 2i's own index
+            inv = theta ** (-2.0 * (2 * i) / D)
+        else:
+            inv = theta ** (-2.0 * i / D)
+        a = np.asarray(positions, np.float64)[:, None] * inv[None]
+        c, s = np.cos(a), np.sin(a)
+        out = np.empty_like(x)
+        e, o = x[..., 0::2], x[..., 1::2]
+        if kind == "half_pairs":  # the rotate-half pairing under the interleaved name
+            return O.rope_rotate_half(x, positions, theta)
+        if kind == "sign":
+            out[..., 0::2], out[..., 1::2] = e * c + o * s, o * c - e * s
+        else:
+            out[..., 0::2], out[..., 1::2] = e * c - o * s, o * c + e * s
+        return out
+    return rope
+
+
+@pytest.mark.parametrize("kind", ["pair_freq_index", "half_pairs", "sign"])
+def test_planted_interleaved_rope_mistake_is_caught(kind):
+    assert _fails_some([pin_rope_interleaved], rope=_mutant_rope_interleaved(kind))
+
+
+def test_planted_style_plumbing_mistake_is_caught():
+    """A decode that ignores the requested style fails the entry-point pin."""
+    def decode_ignoring_style(q, k_cache, v_cache, cache_len, scale=None, rope=True,
+                              theta=10000.0, rope_style="half"):
+        return O.decode(q, k_cache, v_cache, cache_len, scale, rope, theta)
+    assert _fails_some([pin_rope_style_through_entry_points], decode=decode_ignoring_style)
 
 
 def _fails_some(pins, **kw):
