@@ -46,6 +46,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_version.argtypes = []
     L.rope_apply.restype = i
     L.rope_apply.argtypes = [vp, vp, i, i, i, i, i, i, f, vp]
+    L.rope_apply_style.restype = i
+    L.rope_apply_style.argtypes = [vp, vp, i, i, i, i, i, i, f, i, vp]
     L.attn_prefill.restype = i
     L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i, f, f, f, i, i, i, i, i, i, f, i, f, i, vp]
     L.attn_prefill_reserve.restype = i
@@ -99,20 +101,28 @@ def _require_cuda(*tensors):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
-def rope_apply(x, y=None, pos0=0, theta=10000.0, stream=None):
+# RoPE pairing: "half" pairs dims (i, i + D/2), "interleaved" pairs (2i, 2i+1); same angles.
+ROPE_STYLES = {"half": 0, "interleaved": 1}
+ROPE_FLAG_INTERLEAVED = 16  # ATTN_ROPE_FLAG_INTERLEAVED, OR'd into the attention calls' rope
+
+
+def rope_apply(x, y=None, pos0=0, theta=10000.0, stream=None, rope_style="half"):
     """Rotate x [B,H,S,D] at positions pos0 + s into y (new tensor when None; may be x)."""
     _require_cuda(x)
     if y is None:
         y = torch.empty_like(x)
     B, H, S, D = x.shape
-    _check(lib().rope_apply(_ptr(x), _ptr(y), DTYPE_CODES[x.dtype], B, H, S, D, int(pos0),
-                            float(theta), _stream(stream)), "rope_apply")
+    _check(lib().rope_apply_style(_ptr(x), _ptr(y), DTYPE_CODES[x.dtype], B, H, S, D, int(pos0),
+                                  float(theta), ROPE_STYLES[rope_style], _stream(stream)),
+           "rope_apply")
     return y
 
 
-def _rope_mode(rope):
-    """False/0: none; True/1: the library's choice; 2: Q and K both rotated inside the kernel."""
-    return 2 if (not isinstance(rope, bool) and rope == 2) else int(bool(rope))
+def _rope_mode(rope, rope_style="half"):
+    """False/0: none; True/1: the library's choice; 2: Q and K both rotated inside the kernel;
+    with the interleaved pairing the flag is OR'd in."""
+    mode = 2 if (not isinstance(rope, bool) and rope == 2) else int(bool(rope))
+    return mode | (ROPE_FLAG_INTERLEAVED if (mode and ROPE_STYLES[rope_style]) else 0)
 
 
 def attn_prefill_reserve(B, Hq, Hkv, S, D):
@@ -122,7 +132,7 @@ def attn_prefill_reserve(B, Hq, Hkv, S, D):
 
 def attn_prefill(q, k, v, causal=True, softmax_scale=0.0, rope=False, rope_theta=10000.0,
                  pos0=0, o=None, lse=None, want_lse=False, q_scale=1.0, k_scale=1.0,
-                 v_scale=1.0, stream=None):
+                 v_scale=1.0, stream=None, rope_style="half"):
     """O [B,Hq,S,D] bf16 (and LSE [B,Hq,S] fp32 when requested) for q [B,Hq,S,D], k/v [B,Hkv,S,D]."""
     _require_cuda(q, k, v, o, lse)
     B, Hq, S, D = q.shape
@@ -134,14 +144,15 @@ def attn_prefill(q, k, v, causal=True, softmax_scale=0.0, rope=False, rope_theta
     _check(lib().attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                               DTYPE_CODES[q.dtype], float(q_scale), float(k_scale),
                               float(v_scale), B, Hq, Hkv, S, D, int(bool(causal)),
-                              float(softmax_scale), _rope_mode(rope), float(rope_theta), int(pos0),
+                              float(softmax_scale), _rope_mode(rope, rope_style),
+                              float(rope_theta), int(pos0),
                               _stream(stream)), "attn_prefill")
     return (o, lse) if (want_lse or lse is not None) else o
 
 
 def attn_prefill_chunk(q, k_cache, v_cache, skv, softmax_scale=0.0, rope=True,
                        rope_theta=10000.0, pos0=0, o=None, lse=None, want_lse=False, q_scale=1.0,
-                       k_scale=1.0, v_scale=1.0, stream=None):
+                       k_scale=1.0, v_scale=1.0, stream=None, rope_style="half"):
     """O [B,Hq,Sq,D] bf16 for a chunk q [B,Hq,Sq,D] whose rows are the last Sq of `skv` tokens,
     against the first `skv` rows of the caches [B,Hkv,Lmax,D] (keys stored rotated)."""
     _require_cuda(q, k_cache, v_cache, o, lse)
@@ -154,8 +165,9 @@ def attn_prefill_chunk(q, k_cache, v_cache, skv, softmax_scale=0.0, rope=True,
     _check(lib().attn_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
                                     DTYPE_CODES[q.dtype], float(q_scale), float(k_scale),
                                     float(v_scale), B, Hq, Hkv, Sq, int(skv), pitch, D,
-                                    float(softmax_scale), int(bool(rope)), float(rope_theta),
-                                    int(pos0), _stream(stream)), "attn_prefill_chunk")
+                                    float(softmax_scale), _rope_mode(bool(rope), rope_style),
+                                    float(rope_theta), int(pos0), _stream(stream)),
+           "attn_prefill_chunk")
     return (o, lse) if (want_lse or lse is not None) else o
 
 
@@ -164,7 +176,8 @@ def attn_decode_workspace_size(B, Hq, Hkv, D, Lmax):
 
 
 def attn_decode(q, k_cache, v_cache, cache_len, o=None, lse=None, want_lse=False,
-                softmax_scale=0.0, rope=True, rope_theta=10000.0, workspace=None, stream=None):
+                softmax_scale=0.0, rope=True, rope_theta=10000.0, workspace=None, stream=None,
+                rope_style="half"):
     """O [B,Hq,D] for q [B,Hq,D] (bf16) against caches [B,Hkv,Lmax,D] (bf16 or fp8 e5m2) with
     device cache_len [B]."""
     _require_cuda(q, k_cache, v_cache, cache_len, o, lse, workspace)
@@ -180,13 +193,15 @@ def attn_decode(q, k_cache, v_cache, cache_len, o=None, lse=None, want_lse=False
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len), Lmax,
                              _ptr(o), _ptr(lse), DTYPE_CODES[k_cache.dtype], B, Hq, Hkv, D,
-                             float(softmax_scale), int(bool(rope)), float(rope_theta),
-                             _ptr(workspace), wbytes, _stream(stream)), "attn_decode")
+                             float(softmax_scale), _rope_mode(bool(rope), rope_style),
+                             float(rope_theta), _ptr(workspace), wbytes, _stream(stream)),
+           "attn_decode")
     return (o, lse) if (want_lse or lse is not None) else o
 
 
 def attn_decode_noalloc(q, k_cache, v_cache, cache_len, o=None, lse=None, want_lse=False,
-                        softmax_scale=0.0, rope=True, rope_theta=10000.0, stream=None):
+                        softmax_scale=0.0, rope=True, rope_theta=10000.0, stream=None,
+                        rope_style="half"):
     """attn_decode without a workspace: its split partials use the library's fixed 2 MiB
     device array (for callers that cannot allocate at call time)."""
     _require_cuda(q, k_cache, v_cache, cache_len, o, lse)
@@ -198,8 +213,8 @@ def attn_decode_noalloc(q, k_cache, v_cache, cache_len, o=None, lse=None, want_l
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     _check(lib().attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len),
                                      Lmax, _ptr(o), _ptr(lse), DTYPE_CODES[k_cache.dtype], B, Hq, Hkv,
-                                     D, float(softmax_scale), int(bool(rope)), float(rope_theta),
-                                     _stream(stream)), "attn_decode_noalloc")
+                                     D, float(softmax_scale), _rope_mode(bool(rope), rope_style),
+                                     float(rope_theta), _stream(stream)), "attn_decode_noalloc")
     return (o, lse) if (want_lse or lse is not None) else o
 
 
@@ -214,7 +229,7 @@ def attn_decode_append_workspace_size(B, Hq, Hkv, D, Lmax):
 
 def attn_decode_append(q, k_new, v_new, k_cache, v_cache, cache_len, o=None, lse=None,
                        want_lse=False, softmax_scale=0.0, rope=True, rope_theta=10000.0,
-                       workspace=None, stream=None):
+                       workspace=None, stream=None, rope_style="half"):
     """One growing-decode step: O [B,Hq,D] over the cache rows 0..L-1 plus the current token,
     whose key/value are written to row L = cache_len[b]; cache_len is incremented on device."""
     _require_cuda(q, k_new, v_new, k_cache, v_cache, cache_len, o, lse, workspace)
@@ -231,8 +246,8 @@ def attn_decode_append(q, k_new, v_new, k_cache, v_cache, cache_len, o=None, lse
     _check(lib().attn_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                     _ptr(v_cache), _ptr(cache_len), Lmax, _ptr(o), _ptr(lse),
                                     DTYPE_CODES[k_cache.dtype], B, Hq, Hkv, D,
-                                    float(softmax_scale), int(bool(rope)), float(rope_theta),
-                                    _ptr(workspace), wbytes, _stream(stream)),
+                                    float(softmax_scale), _rope_mode(bool(rope), rope_style),
+                                    float(rope_theta), _ptr(workspace), wbytes, _stream(stream)),
            "attn_decode_append")
     return (o, lse) if (want_lse or lse is not None) else o
 
@@ -243,7 +258,7 @@ def attn_decode_latent_workspace_size(B, H, Lmax):
 
 def attn_decode_latent(q, c_cache, cache_len, o=None, lse=None, want_lse=False,
                        softmax_scale=0.0, rope=True, rope_theta=10000.0, workspace=None,
-                       stream=None):
+                       stream=None, rope_style="half"):
     """O [B,H,448] for q [B,H,512] against the latent cache [B,Lmax,512]."""
     _require_cuda(q, c_cache, cache_len, o, lse, workspace)
     B, H, _ = q.shape
@@ -258,7 +273,7 @@ def attn_decode_latent(q, c_cache, cache_len, o=None, lse=None, want_lse=False,
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().attn_decode_latent(_ptr(q), _ptr(c_cache), _ptr(cache_len), Lmax, _ptr(o),
                                     _ptr(lse), DTYPE_CODES[c_cache.dtype], B, H,
-                                    float(softmax_scale), int(bool(rope)),
+                                    float(softmax_scale), _rope_mode(bool(rope), rope_style),
                                     float(rope_theta), _ptr(workspace), wbytes,
                                     _stream(stream)), "attn_decode_latent")
     return (o, lse) if (want_lse or lse is not None) else o

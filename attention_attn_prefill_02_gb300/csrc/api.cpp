@@ -47,6 +47,13 @@ int attn_version(void) { return 100; }
 
 attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, int B, int H, int S, int D,
                          int pos0, float theta, attn_stream_t stream) {
+  return rope_apply_style(x, y, dtype, B, H, S, D, pos0, theta, ATTN_ROPE_HALF_SPLIT, stream);
+}
+
+attn_status_t rope_apply_style(const void* x, void* y, attn_dtype_t dtype, int B, int H, int S,
+                               int D, int pos0, float theta, attn_rope_style_t style,
+                               attn_stream_t stream) {
+  if (style != ATTN_ROPE_HALF_SPLIT && style != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID_ARG;
   if (!x || !y || !aligned16(x) || !aligned16(y)) return ATTN_ERR_INVALID_ARG;
   if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || S < 1 || D < 2 || D > 256 || (D & 1) || pos0 < 0) return ATTN_ERR_INVALID_ARG;
@@ -58,7 +65,8 @@ attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, int B, int 
   if (st != ATTN_OK) return st;
   const float2* tab = rope_table(D, theta, pos0 + S, &st);
   if (!tab) return st;
-  return launch_rope(x, y, dtype, B, H, S, D, pos0, tab, as_stream(stream));
+  return launch_rope(x, y, dtype, B, H, S, D, pos0, tab, style == ATTN_ROPE_INTERLEAVED ? 1 : 0,
+                     as_stream(stream));
 }
 
 attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -71,7 +79,8 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
-  if (rope < 0 || rope > 2) return ATTN_ERR_INVALID_ARG;
+  int il = 0;
+  if (!split_rope_arg(rope, 2, &rope, &il)) return ATTN_ERR_INVALID_ARG;
   if (rope && (!finite_pos(rope_theta) || pos0 < 0)) return ATTN_ERR_INVALID_ARG;
   if (!finite_pos(q_scale) || !finite_pos(k_scale) || !finite_pos(v_scale))
     return ATTN_ERR_INVALID_ARG;
@@ -79,6 +88,9 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(S) > (1LL << 30) || static_cast<long long>(B) * Hq > (1LL << 24))
     return ATTN_ERR_UNSUPPORTED;
+  // the interleaved pairing runs only as rope_apply passes (bf16; the kernel's in-tile rotation
+  // is the half-split form)
+  if (il && (rope == 2 || dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
   const float2* tab = nullptr;
@@ -88,15 +100,15 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
     if (!tab) return st;
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  if (rope == 1 && dtype == ATTN_BF16 && S >= kRopePassMinS) {
+  if (rope == 1 && dtype == ATTN_BF16 && (S >= kRopePassMinS || il)) {
     // Q and K rotated once each into the library's scratch, then attention without RoPE
     const size_t qb = rope_scratch_q_bytes(B, Hq, S, D);
     uint8_t* sc = static_cast<uint8_t*>(
         rope_scratch(qb + static_cast<size_t>(B) * Hkv * S * D * 2, &st));
     if (!sc) return st;
-    st = launch_rope(q, sc, dtype, B, Hq, S, D, pos0, tab, as_stream(stream));
+    st = launch_rope(q, sc, dtype, B, Hq, S, D, pos0, tab, il, as_stream(stream));
     if (st != ATTN_OK) return st;
-    st = launch_rope(k, sc + qb, dtype, B, Hkv, S, D, pos0, tab, as_stream(stream));
+    st = launch_rope(k, sc + qb, dtype, B, Hkv, S, D, pos0, tab, il, as_stream(stream));
     if (st != ATTN_OK) return st;
     return launch_prefill(sc, sc + qb, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv,
                           S, S, S, D, causal, scale, nullptr, 0, pos0, as_stream(stream));
@@ -109,8 +121,8 @@ attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D) {
   if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || (D != 64 && D != 128)) return ATTN_ERR_INVALID_ARG;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
-  const size_t qb = rope_scratch_q_bytes(B, Hq, S, D);
-  const size_t bytes = S >= kRopePassMinS ? qb + static_cast<size_t>(B) * Hkv * S * D * 2 : qb;
+  // Q and K space at every size (the interleaved pairing uses the passes below 1024 rows too)
+  const size_t bytes = rope_scratch_q_bytes(B, Hq, S, D) + static_cast<size_t>(B) * Hkv * S * D * 2;
   return rope_scratch(bytes, &st) ? ATTN_OK : st;
 }
 
@@ -126,7 +138,8 @@ attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, vo
   if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (Sq < 1 || Skv < Sq || kv_pitch < Skv) return ATTN_ERR_INVALID_ARG;
-  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  int il = 0;
+  if (!split_rope_arg(rope, 1, &rope, &il)) return ATTN_ERR_INVALID_ARG;
   if (rope && (!finite_pos(rope_theta) || pos0 < 0)) return ATTN_ERR_INVALID_ARG;
   if (!finite_pos(q_scale) || !finite_pos(k_scale) || !finite_pos(v_scale))
     return ATTN_ERR_INVALID_ARG;
@@ -135,6 +148,7 @@ attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, vo
   if (static_cast<long long>(kv_pitch) > (1LL << 30) || static_cast<long long>(B) * Hq > (1LL << 24))
     return ATTN_ERR_UNSUPPORTED;
   if (rope && dtype == ATTN_FP8_E5M2 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (il && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
   const float2* tab = nullptr;
@@ -147,7 +161,7 @@ attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, vo
     // the chunk's queries rotated once at their absolute positions, then attention without RoPE
     void* sq = rope_scratch(rope_scratch_q_bytes(B, Hq, Sq, D), &st);
     if (!sq) return st;
-    st = launch_rope(q, sq, dtype, B, Hq, Sq, D, pos0 + Skv - Sq, tab, as_stream(stream));
+    st = launch_rope(q, sq, dtype, B, Hq, Sq, D, pos0 + Skv - Sq, tab, il, as_stream(stream));
     if (st != ATTN_OK) return st;
     return launch_prefill(sq, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, Sq,
                           Skv, kv_pitch, D, 1, scale, nullptr, 0, pos0, as_stream(stream));
@@ -175,7 +189,8 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
     return ATTN_ERR_INVALID_ARG;
   if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  int il = 0;
+  if (!split_rope_arg(rope, 1, &rope, &il)) return ATTN_ERR_INVALID_ARG;
   if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
@@ -196,9 +211,9 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   if (dtype == ATTN_FP8_E5M2)
     return launch_decode_fp8(q, k_cache, v_cache, cache_len, Lmax, o, lse, B, Hq, Hkv, scale,
-                             tab, workspace, plan, as_stream(stream));
+                             tab, il, workspace, plan, as_stream(stream));
   return launch_decode(q, k_cache, v_cache, cache_len, Lmax, o, lse, B, Hq, Hkv, D, scale, tab,
-                       workspace, plan, as_stream(stream));
+                       il, workspace, plan, as_stream(stream));
 }
 
 attn_status_t attn_set_decode_splits(int nsplit) {
@@ -227,7 +242,8 @@ attn_status_t attn_decode_append(const void* q, const void* k_new, const void* v
     return ATTN_ERR_INVALID_ARG;
   if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 2 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  int il = 0;
+  if (!split_rope_arg(rope, 1, &rope, &il)) return ATTN_ERR_INVALID_ARG;
   if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
@@ -245,7 +261,7 @@ attn_status_t attn_decode_append(const void* q, const void* k_new, const void* v
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   return launch_decode_append(q, k_new, v_new, k_cache, v_cache, cache_len, Lmax, o, lse, B, Hq,
-                              Hkv, D, scale, tab, workspace, plan, as_stream(stream));
+                              Hkv, D, scale, tab, il, workspace, plan, as_stream(stream));
 }
 
 size_t attn_decode_latent_workspace_size(int B, int H, int Lmax) {
@@ -264,7 +280,8 @@ attn_status_t attn_decode_latent(const void* q, const void* c_cache, const int32
     return ATTN_ERR_INVALID_ARG;
   if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Lmax < 1) return ATTN_ERR_INVALID_ARG;
-  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  int il = 0;
+  if (!split_rope_arg(rope, 1, &rope, &il)) return ATTN_ERR_INVALID_ARG;
   if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
   if (H > 16) return ATTN_ERR_UNSUPPORTED;
@@ -281,8 +298,8 @@ attn_status_t attn_decode_latent(const void* q, const void* c_cache, const int32
     if (!tab) return st;
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(512.0f);
-  return launch_latent(q, c_cache, cache_len, Lmax, o, lse, dtype, B, H, scale, tab, workspace,
-                       plan, as_stream(stream));
+  return launch_latent(q, c_cache, cache_len, Lmax, o, lse, dtype, B, H, scale, tab, il,
+                       workspace, plan, as_stream(stream));
 }
 
 attn_status_t attn_rope_table_reserve(int D, float theta, int max_pos) {

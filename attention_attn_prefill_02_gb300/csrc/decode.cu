@@ -37,6 +37,7 @@ struct GqaParams {
   float* ws_o;    // [B*Hq, nsplit, D] fp32 partial outputs (normalised)
   float* ws_lse;  // [B*Hq, nsplit] fp32 partial log2-sum-exp (scaled-log2 domain)
   const float2* table;
+  int rope_il;    // RoPE pairs (2i, 2i+1) instead of (i, i + D/2)
   unsigned int* status;
   int B, Hq, Hkv, G, Lmax, nsplit, chunk;
   float scale_log2;  // softmax_scale * log2(e)
@@ -44,14 +45,14 @@ struct GqaParams {
 
 // The query tile of one (sequence, KV head) item: rows r < G of `q_rows` (the group's first
 // query row; bf16, D dims each) into `qs` (row pitch `pitch` bytes) as T_OUT, rows G .. rows-1
-// zero; then, with a table, each pair (i, i + D/2) rotated at position len in float32 and
-// rounded once.  The 16-byte loads all go out before any store.  Ends before the final barrier:
+// zero; then, with a table, each pair (i, i + D/2) (or (2i, 2i+1) when `il`) rotated at
+// position len in float32 and rounded once.  The 16-byte loads all go out before any store.  Ends before the final barrier:
 // the caller synchronises before reading the tile.
 template <int D, typename T_OUT>
 __device__ __forceinline__ void fill_query_tile(uint8_t* qs, int pitch, int rows,
                                                 const __nv_bfloat16* __restrict__ q_rows, int G,
                                                 bool valid, const float2* __restrict__ table,
-                                                int len, int tid) {
+                                                int len, int tid, bool il) {
   constexpr int kChunks = D / 8;  // 8-dim chunks per row
   constexpr int kMaxPer = 16 * kChunks / (kComputeWarps * 32);
   uint4 v[kMaxPer];
@@ -79,11 +80,12 @@ __device__ __forceinline__ void fill_query_tile(uint8_t* qs, int pitch, int rows
   compute_bar_sync();
   for (int idx = tid; idx < G * (D / 2); idx += kComputeWarps * 32) {
     const int r = idx / (D / 2), i = idx % (D / 2);
+    const int ia = il ? 2 * i : i, ib = il ? 2 * i + 1 : i + D / 2;
     T_OUT* row = reinterpret_cast<T_OUT*>(qs + r * pitch);
-    const float x1 = static_cast<float>(row[i]), x2 = static_cast<float>(row[i + D / 2]);
+    const float x1 = static_cast<float>(row[ia]), x2 = static_cast<float>(row[ib]);
     const float2 cs = table[static_cast<size_t>(len) * (D / 2) + i];
-    row[i] = static_cast<T_OUT>(x1 * cs.x - x2 * cs.y);
-    row[i + D / 2] = static_cast<T_OUT>(x2 * cs.x + x1 * cs.y);
+    row[ia] = static_cast<T_OUT>(x1 * cs.x - x2 * cs.y);
+    row[ib] = static_cast<T_OUT>(x2 * cs.x + x1 * cs.y);
   }
 }
 
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     compute_bar_sync();
     fill_query_tile<D, __nv_bfloat16>(qs, L::kQPitch, 16,
                                       p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * D, G,
-                                      valid, p.table, len, tid);
+                                      valid, p.table, len, tid, p.rope_il != 0);
     compute_bar_sync();
     uint32_t qa[D / 16][4];
 #pragma unroll
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     compute_bar_sync();
     fill_query_tile<D, __half>(qs, L::kQPitch, 8 * NT,
                                p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * D, G, valid,
-                               p.table, len, tid);
+                               p.table, len, tid, p.rope_il != 0);
     compute_bar_sync();
     // Q^T operand: column g is query 8 nt + g; logical k = 2t+e -> dim 16kk+4t+e and
     // k = 8+2t+e -> dim 16kk+4t+2+e, the order the K reads deliver
@@ -784,6 +786,7 @@ struct LatParams {
   float* ws_lse;  // [B + grid - 1][H]
   int* ws_pref;   // [B + 1] tile prefix sums (stream-K; written by CTA 0 for the merge)
   const float2* table;  // D = 64 table for the RoPE dims
+  int rope_il;          // RoPE pairs (2i, 2i+1) of the RoPE dims instead of (i, i + 32)
   unsigned int* status;
   int B, H, Lmax;
   int streamk;  // 1: split all key tiles evenly over the CTAs; 0: whole sequences c, c+grid, ...
@@ -1030,17 +1033,19 @@ __global__ void __launch_bounds__(kLatThreads, 1)
       }
     }
     lat_bar_sync();
-    // ... then the 64 RoPE dims rotated at position len, pairs (i, i + 32)
+    // ... then the 64 RoPE dims rotated at position len, pairs (i, i + 32) or (2i, 2i+1)
     if (p.table) {
       using QT = typename std::conditional<F8, __half, __nv_bfloat16>::type;
       for (int idx = tid; idx < 16 * (kLatRope / 2); idx += kLatThreads) {
         const int r = idx / (kLatRope / 2), i = idx % (kLatRope / 2);
+        const int ia = kLatV + (p.rope_il ? 2 * i : i);
+        const int ib = kLatV + (p.rope_il ? 2 * i + 1 : i + kLatRope / 2);
         QT* row = reinterpret_cast<QT*>(qs + r * kLatQPitch);
-        const float x1 = static_cast<float>(row[kLatV + i]);
-        const float x2 = static_cast<float>(row[kLatV + i + kLatRope / 2]);
+        const float x1 = static_cast<float>(row[ia]);
+        const float x2 = static_cast<float>(row[ib]);
         const float2 cs = p.table[static_cast<size_t>(len) * (kLatRope / 2) + i];
-        row[kLatV + i] = static_cast<QT>(x1 * cs.x - x2 * cs.y);
-        row[kLatV + i + kLatRope / 2] = static_cast<QT>(x2 * cs.x + x1 * cs.y);
+        row[ia] = static_cast<QT>(x1 * cs.x - x2 * cs.y);
+        row[ib] = static_cast<QT>(x2 * cs.x + x1 * cs.y);
       }
     }
     lat_bar_sync();
@@ -1409,7 +1414,7 @@ DecodePlan plan_common(int units, int Lmax, int ctas, double key_bytes, int rows
 template <int D>
 attn_status_t launch_gqa_typed(const void* q, const void* k, const void* v, const int32_t* lens,
                                int Lmax, void* o, float* lse, int B, int Hq, int Hkv, float scale,
-                               const float2* table, void* ws, const DecodePlan& plan,
+                               const float2* table, int rope_il, void* ws, const DecodePlan& plan,
                                cudaStream_t st) {
   constexpr int NST = 3;
   using L = GqaSmem<D, NST>;
@@ -1426,6 +1431,7 @@ attn_status_t launch_gqa_typed(const void* q, const void* k, const void* v, cons
   p.ws_o = plan.nsplit > 1 ? static_cast<float*>(ws) : nullptr;
   p.ws_lse = plan.nsplit > 1 ? static_cast<float*>(ws) + rows * plan.nsplit * D : nullptr;
   p.table = table;
+  p.rope_il = rope_il;
   p.status = device_status_ptr();
   p.B = B;
   p.Hq = Hq;
@@ -1502,7 +1508,7 @@ attn_status_t launch_decode_fp8_nt(const CUtensorMap& tk, const CUtensorMap& tv,
 
 attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
                                 const int32_t* lens, int Lmax, void* o, float* lse, int B, int Hq,
-                                int Hkv, float scale, const float2* table, void* ws,
+                                int Hkv, float scale, const float2* table, int rope_il, void* ws,
                                 const DecodePlan& plan, cudaStream_t st) {
   constexpr int D = kF8D;
   CUtensorMap tk, tv;
@@ -1518,6 +1524,7 @@ attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
   p.ws_o = plan.nsplit > 1 ? static_cast<float*>(ws) : nullptr;
   p.ws_lse = plan.nsplit > 1 ? static_cast<float*>(ws) + rows * plan.nsplit * D : nullptr;
   p.table = table;
+  p.rope_il = rope_il;
   p.status = device_status_ptr();
   p.B = B;
   p.Hq = Hq;
@@ -1542,8 +1549,9 @@ attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
 // ------------------------------------------------------------------------------------------------
 
 // One block per (sequence, KV head), one warp per query head of the group.  Lane l owns the
-// rotation pairs i = 2l, 2l+1 (D = 128; i = l for D = 64), i.e. dims i and i + D/2, for the key,
-// the query and the merge.  The group's first warp writes the cache row.
+// rotation pairs i = 2l, 2l+1 (D = 128; i = l for D = 64), i.e. dims i and i + D/2 (dims 2i
+// and 2i+1 when `il`), for the key, the query and the merge.  The group's first warp writes the
+// cache row.
 template <int D>
 __global__ void __launch_bounds__(16 * 32)
     append_merge_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
@@ -1551,7 +1559,7 @@ __global__ void __launch_bounds__(16 * 32)
                         __nv_bfloat16* v_cache, const int32_t* __restrict__ lens, int Lmax,
                         __nv_bfloat16* o, const float* __restrict__ lse_hist, float* lse_out,
                         int Hq, int Hkv, float scale, const float2* __restrict__ table,
-                        unsigned int* status) {
+                        int il, unsigned int* status) {
   constexpr int P = D / 64;  // pairs per lane
   const int b = blockIdx.x, kvh = blockIdx.y;
   const int g = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -1565,15 +1573,21 @@ __global__ void __launch_bounds__(16 * 32)
   const size_t crow = (kv * Lmax + L) * D;
   const size_t row = static_cast<size_t>(b) * Hq + kvh * G + g;
   const int i0 = lane * P;
+  int da[P], db[P];  // the two dims of pair i0 + j
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    da[j] = il ? 2 * (i0 + j) : i0 + j;
+    db[j] = il ? 2 * (i0 + j) + 1 : i0 + j + D / 2;
+  }
   float k1[P], k2[P], q1[P], q2[P], v1[P], v2[P];
 #pragma unroll
   for (int j = 0; j < P; ++j) {
-    k1[j] = __bfloat162float(k_new[kv * D + i0 + j]);
-    k2[j] = __bfloat162float(k_new[kv * D + i0 + j + D / 2]);
-    q1[j] = __bfloat162float(q[row * D + i0 + j]);
-    q2[j] = __bfloat162float(q[row * D + i0 + j + D / 2]);
-    v1[j] = __bfloat162float(v_new[kv * D + i0 + j]);
-    v2[j] = __bfloat162float(v_new[kv * D + i0 + j + D / 2]);
+    k1[j] = __bfloat162float(k_new[kv * D + da[j]]);
+    k2[j] = __bfloat162float(k_new[kv * D + db[j]]);
+    q1[j] = __bfloat162float(q[row * D + da[j]]);
+    q2[j] = __bfloat162float(q[row * D + db[j]]);
+    v1[j] = __bfloat162float(v_new[kv * D + da[j]]);
+    v2[j] = __bfloat162float(v_new[kv * D + db[j]]);
   }
   float part = 0.f;
 #pragma unroll
@@ -1591,10 +1605,10 @@ __global__ void __launch_bounds__(16 * 32)
     const float qr2 = __bfloat162float(__float2bfloat16_rn(q2[j] * c + q1[j] * sn));
     part = fmaf(qr1, kr1, fmaf(qr2, kr2, part));
     if (g == 0) {
-      k_cache[crow + i0 + j] = __float2bfloat16_rn(kr1);
-      k_cache[crow + i0 + j + D / 2] = __float2bfloat16_rn(kr2);
-      v_cache[crow + i0 + j] = v_new[kv * D + i0 + j];
-      v_cache[crow + i0 + j + D / 2] = v_new[kv * D + i0 + j + D / 2];
+      k_cache[crow + da[j]] = __float2bfloat16_rn(kr1);
+      k_cache[crow + db[j]] = __float2bfloat16_rn(kr2);
+      v_cache[crow + da[j]] = v_new[kv * D + da[j]];
+      v_cache[crow + db[j]] = v_new[kv * D + db[j]];
     }
   }
 #pragma unroll
@@ -1605,9 +1619,9 @@ __global__ void __launch_bounds__(16 * 32)
 #pragma unroll
   for (int j = 0; j < P; ++j) {
     __nv_bfloat16* orow = o + row * D;
-    const float oh1 = __bfloat162float(orow[i0 + j]), oh2 = __bfloat162float(orow[i0 + j + D / 2]);
-    orow[i0 + j] = __float2bfloat16_rn(fmaf(a, v1[j] - oh1, oh1));
-    orow[i0 + j + D / 2] = __float2bfloat16_rn(fmaf(a, v2[j] - oh2, oh2));
+    const float oh1 = __bfloat162float(orow[da[j]]), oh2 = __bfloat162float(orow[db[j]]);
+    orow[da[j]] = __float2bfloat16_rn(fmaf(a, v1[j] - oh1, oh1));
+    orow[db[j]] = __float2bfloat16_rn(fmaf(a, v2[j] - oh2, oh2));
   }
   if (lse_out && lane == 0) lse_out[row] = fmaxf(lh, sc) + log1pf(expf(-fabsf(sc - lh)));
 }
@@ -1624,12 +1638,12 @@ __global__ void append_len_kernel(int32_t* lens, int B, int Lmax) {
 attn_status_t launch_decode_append(const void* q, const void* k_new, const void* v_new,
                                    void* k_cache, void* v_cache, int32_t* lens, int Lmax,
                                    void* o, float* lse, int B, int Hq, int Hkv, int D,
-                                   float scale, const float2* table, void* ws,
+                                   float scale, const float2* table, int rope_il, void* ws,
                                    const DecodePlan& plan, cudaStream_t st) {
   // workspace: the history decode's own part, then the history LSE [B*Hq] (natural log)
   float* lse_hist = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + append_ws_offset(plan));
   attn_status_t r = launch_decode(q, k_cache, v_cache, lens, Lmax, o, lse_hist, B, Hq, Hkv, D,
-                                  scale, table, plan.ws_bytes ? ws : nullptr, plan, st);
+                                  scale, table, rope_il, plan.ws_bytes ? ws : nullptr, plan, st);
   if (r != ATTN_OK) return r;
   const dim3 grid(B, Hkv);
   const int threads = 32 * (Hq / Hkv);  // one warp per query head of the group (<= 16)
@@ -1642,11 +1656,11 @@ attn_status_t launch_decode_append(const void* q, const void* k_new, const void*
   if (D == 128)
     append_merge_kernel<128><<<grid, threads, 0, st>>>(qq, kn, vn, kc, vc, lens, Lmax, oo,
                                                               lse_hist, lse, Hq, Hkv, scale,
-                                                              table, device_status_ptr());
+                                                              table, rope_il, device_status_ptr());
   else
     append_merge_kernel<64><<<grid, threads, 0, st>>>(qq, kn, vn, kc, vc, lens, Lmax, oo,
                                                              lse_hist, lse, Hq, Hkv, scale,
-                                                             table, device_status_ptr());
+                                                             table, rope_il, device_status_ptr());
   if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
   append_len_kernel<<<(B + 255) / 256, 256, 0, st>>>(lens, B, Lmax);
   return launch_status();
@@ -1654,18 +1668,18 @@ attn_status_t launch_decode_append(const void* q, const void* k_new, const void*
 
 attn_status_t launch_decode(const void* q, const void* k, const void* v, const int32_t* lens,
                             int Lmax, void* o, float* lse, int B, int Hq, int Hkv, int D,
-                            float scale, const float2* table, void* ws, const DecodePlan& plan,
-                            cudaStream_t st) {
+                            float scale, const float2* table, int rope_il, void* ws,
+                            const DecodePlan& plan, cudaStream_t st) {
   if (D == 128)
-    return launch_gqa_typed<128>(q, k, v, lens, Lmax, o, lse, B, Hq, Hkv, scale, table, ws, plan,
-                                 st);
-  return launch_gqa_typed<64>(q, k, v, lens, Lmax, o, lse, B, Hq, Hkv, scale, table, ws, plan,
-                              st);
+    return launch_gqa_typed<128>(q, k, v, lens, Lmax, o, lse, B, Hq, Hkv, scale, table, rope_il,
+                                 ws, plan, st);
+  return launch_gqa_typed<64>(q, k, v, lens, Lmax, o, lse, B, Hq, Hkv, scale, table, rope_il, ws,
+                              plan, st);
 }
 
 attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, int Lmax, void* o,
                             float* lse, attn_dtype_t dt, int B, int H, float scale,
-                            const float2* table, void* ws, const DecodePlan& plan,
+                            const float2* table, int rope_il, void* ws, const DecodePlan& plan,
                             cudaStream_t st) {
   if (B > kLatMaxB) return ATTN_ERR_UNSUPPORTED;
   const bool f8 = dt == ATTN_FP8_E5M2;
@@ -1683,6 +1697,7 @@ attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, i
   p.ws_pref = ws ? reinterpret_cast<int*>(p.ws_lse + static_cast<size_t>(B + plan.grid - 1) * H)
                  : nullptr;
   p.table = table;
+  p.rope_il = rope_il;
   p.status = device_status_ptr();
   p.B = B;
   p.H = H;

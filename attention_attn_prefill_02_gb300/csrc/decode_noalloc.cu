@@ -61,7 +61,8 @@ extern "C" ATTN_API attn_status_t attn_decode_noalloc(
     return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP8_E5M2) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (rope != 0 && rope != 1) return ATTN_ERR_INVALID_ARG;
+  int il = 0;
+  if (!split_rope_arg(rope, 1, &rope, &il)) return ATTN_ERR_INVALID_ARG;
   if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
@@ -83,5 +84,5 @@ extern "C" ATTN_API attn_status_t attn_decode_noalloc(
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   return launch_decode(q, k_cache, v_cache, cache_len, Lmax, o, lse, B, Hq, Hkv, D, scale, tab,
-                       scratch, plan, reinterpret_cast<cudaStream_t>(stream));
+                       il, scratch, plan, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -55,6 +55,17 @@ bool set_smem_attr(const void* kernel, int bytes);
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launch-status helper: map the last launch error to a status.
+// The `rope` argument of the attention calls: the mode (0 .. max_mode) in the low bits, optionally
+// OR'd with ATTN_ROPE_FLAG_INTERLEAVED.  False for anything else (and for the flag without a mode).
+inline bool split_rope_arg(int rope, int max_mode, int* mode, int* interleaved) {
+  const int m = rope & ~ATTN_ROPE_FLAG_INTERLEAVED;
+  const int il = (rope & ATTN_ROPE_FLAG_INTERLEAVED) ? 1 : 0;
+  if (m < 0 || m > max_mode || (il && m == 0)) return false;
+  *mode = m;
+  *interleaved = il;
+  return true;
+}
+
 inline attn_status_t launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -63,8 +74,9 @@ inline attn_status_t launch_status() {
 // ------------------------------------------------------------------------------------------
 // entry points implemented per translation unit (called from api.cpp after validation)
 // ------------------------------------------------------------------------------------------
+// interleaved: pairs (2i, 2i+1) instead of (i, i + D/2), same table.
 attn_status_t launch_rope(const void* x, void* y, attn_dtype_t dt, int B, int H, int S, int D,
-                          int pos0, const float2* table, cudaStream_t st);
+                          int pos0, const float2* table, int interleaved, cudaStream_t st);
 
 struct DecodePlan {
   int nsplit;      // splits of the key range per (b, kv head)
@@ -84,23 +96,23 @@ inline size_t append_ws_bytes(const DecodePlan& pl, int B, int Hq) {
 attn_status_t launch_decode_append(const void* q, const void* k_new, const void* v_new,
                                    void* k_cache, void* v_cache, int32_t* lens, int Lmax,
                                    void* o, float* lse, int B, int Hq, int Hkv, int D,
-                                   float scale, const float2* table, void* ws,
+                                   float scale, const float2* table, int rope_il, void* ws,
                                    const DecodePlan& plan, cudaStream_t st);
 DecodePlan plan_latent(int B, int H, int Lmax);
 
 attn_status_t launch_decode(const void* q, const void* k, const void* v, const int32_t* lens,
                             int Lmax, void* o, float* lse, int B, int Hq, int Hkv, int D,
-                            float scale, const float2* table, void* ws, const DecodePlan& plan,
-                            cudaStream_t st);
+                            float scale, const float2* table, int rope_il, void* ws,
+                            const DecodePlan& plan, cudaStream_t st);
 
 attn_status_t launch_decode_fp8(const void* q, const void* k, const void* v,
                                 const int32_t* lens, int Lmax, void* o, float* lse, int B, int Hq,
-                                int Hkv, float scale, const float2* table, void* ws,
+                                int Hkv, float scale, const float2* table, int rope_il, void* ws,
                                 const DecodePlan& plan, cudaStream_t st);
 
 attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, int Lmax, void* o,
                             float* lse, attn_dtype_t dt, int B, int H, float scale,
-                            const float2* table, void* ws, const DecodePlan& plan,
+                            const float2* table, int rope_il, void* ws, const DecodePlan& plan,
                             cudaStream_t st);
 
 // S query rows at positions Skv - S .. Skv - 1 against Skv keys (rows kv_pitch apart per head);

@@ -3,7 +3,9 @@
 // Row r = ((b*H + h)*S + s) is rotated at position pos0 + s: each pair (x_i, x_{i+D/2}) becomes
 // (x_i c - x_{i+D/2} s, x_{i+D/2} c + x_i s) with (c, s) = table[pos][i].  The pass is HBM
 // bound (every element read and written once); each thread moves 16-byte chunks of the first
-// half of a row and the matching chunks of the second half, fully coalesced.
+// half of a row and the matching chunks of the second half, fully coalesced.  The interleaved
+// convention pairs (x_{2i}, x_{2i+1}) with the same (c, s) = table[pos][i]; a 16-byte chunk then
+// holds whole pairs.
 #include "common.cuh"
 
 namespace attn {
@@ -179,6 +181,93 @@ __global__ void __launch_bounds__(256) rope_pair_kernel(const T* __restrict__ x,
   }
 }
 
+// Interleaved pairs, one thread per (sequence b, position s, 16-byte chunk): the chunk's N/2
+// pairs take table[pos][c*N/2 ..]; heads HU at a time as in rope_pos_kernel.
+template <typename T, int HU>
+__global__ void __launch_bounds__(256, 2) rope_il_pos_kernel(const T* __restrict__ x, T* y, int B,
+                                                          int H, int S, int D, int pos0,
+                                                          const float2* __restrict__ table) {
+  constexpr int N = Vec<T>::N;
+  const int chunks = D / N;
+  const long long total = static_cast<long long>(B) * S * chunks;
+  const size_t head_stride = static_cast<size_t>(S) * D;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+       t += (long long)gridDim.x * blockDim.x) {
+    const long long bs = t / chunks;
+    const int c = static_cast<int>(t - bs * chunks);
+    const int s = static_cast<int>(bs % S);
+    const long long b = bs / S;
+    float2 r[N / 2];
+    const float2* cs = table + static_cast<long long>(pos0 + s) * (D / 2) + c * (N / 2);
+#pragma unroll
+    for (int j = 0; j < N / 2; ++j) r[j] = __ldg(cs + j);
+    const size_t row0 = (static_cast<size_t>(b) * H * S + s) * D + c * N;
+    for (int h = 0; h < H; h += HU) {
+      uint4 ra[HU];
+#pragma unroll
+      for (int u = 0; u < HU; ++u)
+        if (h + u < H)
+          ra[u] = __ldg(reinterpret_cast<const uint4*>(x + row0 + static_cast<size_t>(h + u) * head_stride));
+#pragma unroll
+      for (int u = 0; u < HU; ++u)
+        if (h + u < H) {
+          float a[N];
+          Vec<T>::unpack(ra[u], a);
+#pragma unroll
+          for (int j = 0; j < N / 2; ++j) {
+            const float e = a[2 * j], o = a[2 * j + 1];
+            a[2 * j] = e * r[j].x - o * r[j].y;
+            a[2 * j + 1] = o * r[j].x + e * r[j].y;
+          }
+          Vec<T>::store(y + row0 + static_cast<size_t>(h + u) * head_stride, a);
+        }
+    }
+  }
+}
+
+// Interleaved pairs, any even D: one thread per pair.
+template <typename T>
+__global__ void __launch_bounds__(256) rope_il_pair_kernel(const T* __restrict__ x, T* y,
+                                                           long long rows, int S, int D, int pos0,
+                                                           const float2* __restrict__ table) {
+  const int half = D / 2;
+  const long long total = rows * half;
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+       t += (long long)gridDim.x * blockDim.x) {
+    const long long row = t / half;
+    const int i = static_cast<int>(t - row * half);
+    const int pos = pos0 + static_cast<int>(row % S);
+    const float2 r = table[static_cast<long long>(pos) * half + i];
+    const float e = Vec<T>::load1(x + row * D, 2 * i);
+    const float o = Vec<T>::load1(x + row * D, 2 * i + 1);
+    Vec<T>::store1(y + row * D, 2 * i, e * r.x - o * r.y);
+    Vec<T>::store1(y + row * D, 2 * i + 1, o * r.x + e * r.y);
+  }
+}
+
+template <typename T>
+attn_status_t launch_typed_il(const void* x, void* y, int B, int H, int S, int D, int pos0,
+                              const float2* table, cudaStream_t st) {
+  const int sms = sm_count();
+  const int threads = 256;
+  const long long cap = static_cast<long long>(sms) * 16;
+  if (D % Vec<T>::N == 0) {
+    const long long work = static_cast<long long>(B) * S * (D / Vec<T>::N);
+    long long blocks = (work + threads - 1) / threads;
+    if (blocks > cap) blocks = cap;
+    constexpr int HU = Vec<T>::N == 8 ? 4 : 2;
+    rope_il_pos_kernel<T, HU><<<static_cast<int>(blocks), threads, 0, st>>>(
+        static_cast<const T*>(x), static_cast<T*>(y), B, H, S, D, pos0, table);
+  } else {
+    const long long rows = static_cast<long long>(B) * H * S;
+    long long blocks = (rows * (D / 2) + threads - 1) / threads;
+    if (blocks > cap) blocks = cap;
+    rope_il_pair_kernel<T><<<static_cast<int>(blocks), threads, 0, st>>>(
+        static_cast<const T*>(x), static_cast<T*>(y), rows, S, D, pos0, table);
+  }
+  return launch_status();
+}
+
 template <typename T>
 attn_status_t launch_typed(const void* x, void* y, int B, int H, int S, int D, int pos0,
                            const float2* table, cudaStream_t st) {
@@ -214,7 +303,11 @@ attn_status_t launch_typed(const void* x, void* y, int B, int H, int S, int D, i
 }  // namespace
 
 attn_status_t launch_rope(const void* x, void* y, attn_dtype_t dt, int B, int H, int S, int D,
-                          int pos0, const float2* table, cudaStream_t st) {
+                          int pos0, const float2* table, int interleaved, cudaStream_t st) {
+  if (interleaved) {
+    if (dt == ATTN_BF16) return launch_typed_il<__nv_bfloat16>(x, y, B, H, S, D, pos0, table, st);
+    return launch_typed_il<__nv_fp8_e5m2>(x, y, B, H, S, D, pos0, table, st);
+  }
   if (dt == ATTN_BF16) return launch_typed<__nv_bfloat16>(x, y, B, H, S, D, pos0, table, st);
   return launch_typed<__nv_fp8_e5m2>(x, y, B, H, S, D, pos0, table, st);
 }

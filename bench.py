@@ -377,9 +377,18 @@ def variants(b, d):
         b.rope_apply(d["q"], qr, theta=THETA)
         b.rope_apply(d["k"], kr, theta=THETA)
 
+    def rope_once_il():  # the interleaved pairing (2i, 2i+1): always the passes
+        b.attn_prefill(d["q"], d["k"], d["v"], causal=True, rope=1, rope_theta=THETA, o=d["o"],
+                       rope_style="interleaved")
+
+    def rope_only_il():
+        b.rope_apply(d["q"], qr, theta=THETA, rope_style="interleaved")
+        b.rope_apply(d["k"], kr, theta=THETA, rope_style="interleaved")
+
     tf, tu = time_call(fused, 5, 1), time_call(unfused, 5, 1)
     tk = time_call(rope_once, 5, 1)
     ta, tr = time_call(attn_only, 5, 1), time_call(rope_only, 5, 1)
+    tki, tri = time_call(rope_once_il, 5, 1), time_call(rope_only_il, 5, 1)
     rope_bytes = workload.rope_bytes(P["B"] * (P["Hq"] + P["Hkv"]) * P["S"], P["D"])
     out["prefill_rope"] = {
         "fused_in_kernel_ms": round(tf, 4), "rope_once_ms": round(tk, 4),
@@ -388,7 +397,11 @@ def variants(b, d):
         "fused_in_kernel_tflops": round(fl / tf / 1e9, 1),
         "rope_once_tflops": round(fl / tk / 1e9, 1), "unfused_tflops": round(fl / tu / 1e9, 1),
         "fused_in_kernel_speedup_vs_unfused": round(tu / tf, 3),
-        "rope_once_speedup_vs_unfused": round(tu / tk, 3)}
+        "rope_once_speedup_vs_unfused": round(tu / tk, 3),
+        "interleaved_rope_once_ms": round(tki, 4),
+        "interleaved_rope_once_tflops": round(fl / tki / 1e9, 1),
+        "interleaved_rope_apply_ms": round(tri, 4),
+        "interleaved_rope_apply_gbs": round(rope_bytes / tri / 1e6, 1)}
     # where rotating K once per call starts to pay: both RoPE forms by prompt length
     by_s = {}
     for S in (512, 1024, 2048, 4096):

@@ -62,6 +62,19 @@ typedef enum {
 
 typedef enum { ATTN_BF16 = 0, ATTN_FP8_E5M2 = 1 } attn_dtype_t;
 
+/*
+ * RoPE pairing convention.  Both rotate pair i by the angle pos * theta^(-2i/D) (the same
+ * cos/sin table); they differ in which two dims form pair i:
+ *   ATTN_ROPE_HALF_SPLIT   dims (i, i + D/2)  (the default everywhere)
+ *   ATTN_ROPE_INTERLEAVED  dims (2i, 2i + 1)
+ * The pages do not fix a convention; the interleaved one is the other common form.
+ */
+typedef enum { ATTN_ROPE_HALF_SPLIT = 0, ATTN_ROPE_INTERLEAVED = 1 } attn_rope_style_t;
+
+/* OR'd into the `rope` argument of the attention calls (with a nonzero mode) to select the
+ * interleaved pairing; for the latent decode it applies to the 64 RoPE dims. */
+#define ATTN_ROPE_FLAG_INTERLEAVED 16
+
 /* Static English description of a status code.  Never NULL. */
 ATTN_API const char* attn_status_string(attn_status_t status);
 
@@ -85,6 +98,15 @@ ATTN_API attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, in
                          int pos0, float theta, attn_stream_t stream);
 
 /*
+ * rope_apply_style — rope_apply with the pairing convention given (rope_apply is this call with
+ * ATTN_ROPE_HALF_SPLIT).  Arguments and errors as rope_apply; `style` outside the enum is
+ * INVALID_ARG.
+ */
+ATTN_API attn_status_t rope_apply_style(const void* x, void* y, attn_dtype_t dtype, int B, int H,
+                               int S, int D, int pos0, float theta, attn_rope_style_t style,
+                               attn_stream_t stream);
+
+/*
  * attn_prefill — grouped-query attention over a whole prompt, one GPU.
  * Defines: softmax(scale * Q K^T + causal mask) V for Hq query heads sharing Hkv KV heads,
  * the causal GQA prefill of Lesson: shape adaptive attention negative 20260722 ("당시 조건")
@@ -103,6 +125,8 @@ ATTN_API attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, in
  *                kernel;
  *            2 = both inside the kernel as they are loaded (K once per query block that reads
  *                it; the fully fused form, measured beside the other).
+ *            | ATTN_ROPE_FLAG_INTERLEAVED: pairs (2i, 2i+1); bf16 with rope = 1 only (always
+ *                the rope_apply passes); fp8 or rope = 2 with the flag is UNSUPPORTED.
  *   D in {64, 128}; Hq % Hkv == 0; S >= 1.  fp8 e5m2 inputs: P is rounded to e4m3 for the PV
  *   product; with rope = 1 (D = 128 only) Q and K are rotated into bf16 tiles inside the
  *   kernel (QK^T then runs in bf16, PV stays fp8), because rotated values re-rounded to fp8
@@ -119,7 +143,8 @@ ATTN_API attn_status_t attn_prefill(const void* q, const void* k, const void* v,
 
 /*
  * attn_prefill_reserve — allocate ahead the per-device rotation scratch that attn_prefill
- * (rope = 1) and attn_prefill_chunk (rope = 1, bf16) use at this size (S = the query rows), e.g.
+ * (rope = 1, either pairing) and attn_prefill_chunk (rope = 1, bf16) use at this size (S = the
+ * query rows), e.g.
  * before a CUDA-graph capture, which cannot allocate.  Together with attn_rope_table_reserve it
  * leaves nothing to allocate in later calls up to that size.
  * Errors: INVALID_ARG (sizes, D not in {64, 128}), CUDA, NO_DEVICE.
@@ -140,7 +165,8 @@ ATTN_API attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D
  *   o        [B,Hq,Sq,D] bfloat16.   lse  NULL or [B,Hq,Sq] float32 (natural log).
  *   rope     1: q rotated at positions pos0 + Skv - Sq + i (bf16: a rope_apply pass into the
  *            library's scratch, see attn_prefill_reserve; fp8: inside the kernel, into bf16
- *            tiles); 0: q as given.
+ *            tiles); 0: q as given.  1 | ATTN_ROPE_FLAG_INTERLEAVED: pairs (2i, 2i+1), bf16
+ *            only (fp8: UNSUPPORTED).
  *   1 <= Sq <= Skv <= kv_pitch; D in {64, 128} (fp8 with rope = 1: D = 128); the other
  *   arguments as attn_prefill.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
@@ -164,7 +190,8 @@ ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int Lm
  * Defines: the grouped split-score decode of Fixed-budget decode audit — 2026-09-11 ("Which
  * implementation was tested": static append cache; "Optimized full-model results": split
  * size 128), with split partials merged by log-sum-exp weights ("A: group-entry queries ...").
- *   q          [B,Hq,D]      the new token's query (un-rotated; rotated here when rope = 1)
+ *   q          [B,Hq,D]      the new token's query (un-rotated; rotated here when rope = 1, or
+ *                            1 | ATTN_ROPE_FLAG_INTERLEAVED for the pairs (2i, 2i+1))
  *   k_cache    [B,Hkv,Lmax,D], v_cache [B,Hkv,Lmax,D]  keys stored ALREADY rotated.
  *   cache_len  DEVICE int32 [B]; sequence b attends keys 0 .. cache_len[b]-1 and its query
  *              sits at position cache_len[b].  Needs 1 <= cache_len[b] <= Lmax; a row with an
@@ -232,7 +259,8 @@ ATTN_API attn_status_t attn_set_decode_splits(int nsplit);
  * token's weight is the logistic function of its score minus the history log-sum-exp).
  * Sequence b's query and new key sit at position L = cache_len[b] (read on the device):
  *   1. the history: attn_decode of q over cache rows 0 .. L-1;
- *   2. k_new rotated at L (when rope = 1) and v_new are written to cache row L (bf16), and each
+ *   2. k_new rotated at L (when rope = 1, or 1 | ATTN_ROPE_FLAG_INTERLEAVED for the pairs
+ *      (2i, 2i+1), the convention of the cached keys) and v_new are written to cache row L (bf16), and each
  *      query row merges that key into its history output;
  *   3. cache_len[b] becomes L + 1.
  * The result is attention over the L + 1 keys.  Because positions and lengths live on the
@@ -267,7 +295,8 @@ ATTN_API size_t attn_decode_latent_workspace_size(int B, int H, int Lmax);
  * tested": 448-dimensional latent + 64-dimensional RoPE), with W_UK already absorbed into q and
  * W_UV applied by the caller to the latent output.
  *   q          [B,H,512] bfloat16: 448 absorbed-latent dims then 64 RoPE dims (the RoPE dims
- *              are rotated at position cache_len[b] when rope = 1).
+ *              are rotated at position cache_len[b] when rope = 1; pairs (i, i + 32) of those
+ *              64 dims, or (2i, 2i+1) with rope = 1 | ATTN_ROPE_FLAG_INTERLEAVED).
  *   c_cache    [B,Lmax,512] of `dtype` (ATTN_BF16, or ATTN_FP8_E5M2 at half the bytes; every
  *              e5m2 value is an exact f16, so the kernel runs f16 MMAs on the widened cache and
  *              the query in f16): per token the 448-dim latent then the 64-dim rotated key.

@@ -79,6 +79,34 @@ def test_rope_apply_rejects_bad_arguments(L):
         assert L.rope_apply(*a, _stream()) == INVALID, a
 
 
+IL = binding.ROPE_FLAG_INTERLEAVED
+
+
+def test_rope_style_arguments(L):
+    """rope_apply_style takes the two pairings only; the attention calls take the interleaved
+    flag only together with a rotation mode, and refuse the forms that have no kernel."""
+    for style in (-1, 2, 7):
+        assert L.rope_apply_style(FAKE, FAKE2, 0, 1, 1, 1, 8, 0, 1e4, style, _stream()) == INVALID
+    assert L.rope_apply_style(None, FAKE2, 0, 1, 1, 1, 8, 0, 1e4, 1, _stream()) == INVALID
+    assert _prefill(L, rope=IL) == INVALID                    # a pairing without a rotation
+    assert _prefill(L, rope=1 | 32) == INVALID                # an unknown bit
+    assert _prefill(L, rope=-1) == INVALID
+    assert _prefill(L, rope=2 | IL) == UNSUPPORTED            # the kernel rotates half-split only
+    assert _prefill(L, rope=1 | IL, dt=1, D=128) == UNSUPPORTED  # fp8 rotates in the kernel
+    assert _chunk(L, rope=1 | IL, dt=1) == UNSUPPORTED
+    assert _chunk(L, rope=2 | IL) == INVALID
+    assert _decode(L, rope=IL) == INVALID
+    assert _decode(L, rope=2 | IL) == INVALID
+    assert _append(L, rope=IL) == INVALID
+    assert _latent(L, rope=IL) == INVALID
+    assert _latent(L, rope=1 | 64) == INVALID
+    # the binding composes the flag from rope_style
+    assert binding._rope_mode(True, "interleaved") == 1 | IL
+    assert binding._rope_mode(2, "interleaved") == 2 | IL
+    assert binding._rope_mode(False, "interleaved") == 0
+    assert binding._rope_mode(True) == 1
+
+
 def _prefill(L, **kw):
     args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE2, lse=None, dt=0, qs=1.0, ks=1.0, vs=1.0, B=1,
                 Hq=4, Hkv=1, S=128, D=64, causal=1, scale=0.0, rope=1, theta=1e4, pos0=0)

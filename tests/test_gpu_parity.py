@@ -17,6 +17,10 @@ from attention_attn_prefill_02_gb300 import binding, synthetic
 pytestmark = pytest.mark.gpu
 
 BF16_MAX, BF16_MEAN, FP8_MAX, LSE_TOL = 2e-2, 2e-3, 8e-2, 5e-3
+# LSE of a prefill whose Q and K are rotated by the library: the rotated values are rounded to
+# bf16 before Q K^T, which moves each score by up to 2 * 2^-9 * scale * sum_i |q_i k_i| (about
+# 0.03 worst case at D = 128 with N(0,1) inputs, ~1e-3 typical); 1e-2 bounds thousands of rows.
+ROPE_LSE_TOL = 1e-2
 
 
 def f64(t):
@@ -448,3 +452,123 @@ def test_latent_bad_cache_len_sets_status():
     ro, _ = oracle.latent_decode(f64(q[keep]), f64(c[keep]), cl[keep].numpy())
     check(o[keep].cpu(), ro, what="valid rows")
     assert torch.all(o[1].cpu() == 0)
+
+
+# --------------------------------------------------------------------------------------------
+# the interleaved RoPE pairing (2i, 2i+1) through every entry point that rotates
+# --------------------------------------------------------------------------------------------
+
+IL = "interleaved"
+
+
+@pytest.mark.parametrize("shape,pos0,dtype", [
+    ((2, 3, 37, 64), 5, "bf16"),      # per-row kernel (3 heads), whole chunks
+    ((1, 8, 300, 128), 16000, "bf16"),  # per-position kernel, far positions
+    ((1, 1, 3, 6), 11, "bf16"),       # D = 6: one thread per pair
+    ((2, 7, 70, 128), 9, "fp8"),
+    ((1, 2, 5, 10), 0, "fp8"),        # D = 10: one thread per pair
+])
+def test_rope_apply_interleaved(shape, pos0, dtype):
+    x = synthetic.rope_input(*shape, dtype=dtype, seed=shape[2])
+    y = binding.rope_apply(x.cuda(), pos0=pos0, theta=10000.0, rope_style=IL)
+    torch.cuda.synchronize()
+    ref = oracle.rope_rotate_interleaved(f64(x), pos0 + np.arange(shape[2]), 10000.0)
+    if dtype == "bf16":
+        check(y.cpu(), ref, what="rope interleaved bf16")
+        assert (y.cpu() == torch.from_numpy(ref).to(torch.bfloat16)).float().mean() > 0.99
+    else:
+        r = f64(torch.from_numpy(ref).to(torch.float8_e5m2))
+        g = f64(y.cpu())
+        step = np.maximum(np.abs(r), 2.0 ** -14) * 0.25
+        assert np.all(np.abs(g - r) <= step * 1.0001)
+        assert (g == r).mean() > 0.99
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,pos0", [
+    (1, 4, 1, 128, 64, True, 0),       # the tiny config with interleaved pairs
+    (2, 8, 2, 700, 128, True, 3),      # below the pass threshold of the half-split form
+    (1, 4, 1, 1100, 128, True, 0),
+    (1, 2, 2, 300, 64, False, 5000),
+])
+def test_prefill_rope_interleaved(B, Hq, Hkv, S, D, causal, pos0):
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=S + 7)
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, rope=True,
+                                  rope_theta=10000.0, pos0=pos0, want_lse=True, rope_style=IL)
+    status_ok()
+    ro, rl = oracle.prefill(f64(q), f64(k), f64(v), causal=causal, rope=True, theta=10000.0,
+                            pos0=pos0, rope_style=IL)
+    check(o.cpu(), ro, what="O prefill interleaved")
+    check(lse.cpu(), rl, ROPE_LSE_TOL, None, what="LSE prefill interleaved")
+
+
+def test_prefill_chunk_rope_interleaved():
+    B, Hq, Hkv, Sq, Skv, pitch, D = 2, 8, 2, 96, 700, 704, 128
+    q = synthetic.normal((B, Hq, Sq, D), 930, "bf16")
+    kc = synthetic.normal((B, Hkv, pitch, D), 931, "bf16")
+    vc = synthetic.normal((B, Hkv, pitch, D), 932, "bf16")
+    o, lse = binding.attn_prefill_chunk(q.cuda(), kc.cuda(), vc.cuda(), Skv, rope=True,
+                                        rope_theta=10000.0, pos0=4, want_lse=True, rope_style=IL)
+    status_ok()
+    ro, rl = oracle.prefill_chunk(f64(q), f64(kc), f64(vc), Skv, rope=True, theta=10000.0, pos0=4,
+                                  rope_style=IL)
+    check(o.cpu(), ro, what="O chunk interleaved")
+    check(lse.cpu(), rl, ROPE_LSE_TOL, None, what="LSE chunk interleaved")
+
+
+@pytest.mark.parametrize("cache_dtype,B,Hq,Hkv,D,lens", [
+    ("bf16", 3, 32, 8, 128, [2048, 1, 777]),
+    ("bf16", 2, 8, 1, 64, [300, 129]),
+    ("fp8", 3, 24, 2, 128, [1999, 65, 2048]),
+])
+def test_decode_rope_interleaved(cache_dtype, B, Hq, Hkv, D, lens):
+    Lmax = max(lens)
+    q, kc, vc, cl = synthetic.decode_inputs(B, Hq, Hkv, Lmax, D, lens, seed=B + 70,
+                                            cache_dtype=None if cache_dtype == "bf16" else "fp8")
+    o, lse = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda(), want_lse=True,
+                                 rope_style=IL)
+    status_ok()
+    ro, rl = oracle.decode(f64(q), f64(kc), f64(vc), cl.numpy(), rope=True, theta=10000.0,
+                           rope_style=IL)
+    check(o.cpu(), ro, what="O decode interleaved")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE decode interleaved")
+
+
+def test_decode_append_rope_interleaved():
+    B, Hq, Hkv, Lmax, D, lens = 3, 32, 8, 600, 128, [599, 1, 300]
+    q, kc, vc, cl, kn, vn = _append_inputs(B, Hq, Hkv, Lmax, D, lens, seed=77)
+    gk, gv, gl = kc.cuda(), vc.cuda(), cl.cuda()
+    o, lse = binding.attn_decode_append(q.cuda(), kn.cuda(), vn.cuda(), gk, gv, gl, want_lse=True,
+                                        rope=True, rope_theta=10000.0, rope_style=IL)
+    status_ok()
+    ro, rl, krow = oracle.decode_append(f64(q), f64(kc), f64(vc), cl.numpy(), f64(kn), f64(vn),
+                                        rope=True, theta=10000.0, rope_style=IL)
+    check(o.cpu(), ro, what="O append interleaved")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE append interleaved")
+    gk, gv = gk.cpu(), gv.cpu()
+    for b in range(B):
+        L = int(cl[b])
+        np.testing.assert_allclose(f64(gk[b, :, L]), krow[b], rtol=0, atol=1.6e-2)
+        assert torch.equal(gv[b, :, L], vn[b])
+
+
+@pytest.mark.parametrize("cache_dtype", ["bf16", "fp8"])
+def test_latent_decode_rope_interleaved(cache_dtype):
+    B, H, Lmax, lens = 4, 16, 1024, [1024, 1, 500, 64]
+    q, c, cl = synthetic.latent_inputs(B, H, Lmax, lens, seed=91,
+                                       cache_dtype=None if cache_dtype == "bf16" else "fp8")
+    o, lse = binding.attn_decode_latent(q.cuda(), c.cuda(), cl.cuda(), want_lse=True,
+                                        rope_style=IL)
+    status_ok()
+    ro, rl = oracle.latent_decode(f64(q), f64(c), cl.numpy(), rope=True, theta=10000.0,
+                                  rope_style=IL)
+    check(o.cpu(), ro, what="O latent interleaved")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE latent interleaved")
+
+
+def test_rope_styles_differ_on_device():
+    """The two pairings really produce different rotations (D > 2), and the flag reaches the
+    decode kernel: swapping the style changes the result."""
+    q, kc, vc, cl = synthetic.decode_inputs(2, 8, 2, 256, 128, [256, 100], seed=5)
+    a = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda())
+    b = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda(), rope_style=IL)
+    assert (a.float() - b.float()).abs().max().item() > 1e-2
