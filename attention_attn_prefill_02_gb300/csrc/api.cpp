@@ -45,6 +45,9 @@ const char* attn_status_string(attn_status_t s) {
 
 int attn_version(void) { return 100; }
 
+// Head dims of the single-token decode paths (bf16 caches; the fp8 cache is D = 128 only).
+static bool decode_head_dim(int D) { return D == 64 || D == 128 || D == 256; }
+
 attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, int B, int H, int S, int D,
                          int pos0, float theta, attn_stream_t stream) {
   return rope_apply_style(x, y, dtype, B, H, S, D, pos0, theta, ATTN_ROPE_HALF_SPLIT, stream);
@@ -172,7 +175,7 @@ attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, vo
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int Lmax) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || (D != 64 && D != 128) || Hq % Hkv) return 0;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || (!decode_head_dim(D)) || Hq % Hkv) return 0;
   return plan_decode(B, Hq, Hkv, D, Lmax).ws_bytes;
 }
 
@@ -193,7 +196,7 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
   if (!split_rope_arg(rope, 1, &rope, &il)) return ATTN_ERR_INVALID_ARG;
   if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!decode_head_dim(D)) return ATTN_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
   if (dtype == ATTN_FP8_E5M2 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(Lmax) > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
@@ -223,7 +226,7 @@ attn_status_t attn_set_decode_splits(int nsplit) {
 }
 
 size_t attn_decode_append_workspace_size(int B, int Hq, int Hkv, int D, int Lmax) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 2 || (D != 64 && D != 128) || Hq % Hkv) return 0;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 2 || (!decode_head_dim(D)) || Hq % Hkv) return 0;
   return append_ws_bytes(plan_decode(B, Hq, Hkv, D, Lmax), B, Hq);
 }
 
@@ -246,7 +249,7 @@ attn_status_t attn_decode_append(const void* q, const void* k_new, const void* v
   if (!split_rope_arg(rope, 1, &rope, &il)) return ATTN_ERR_INVALID_ARG;
   if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!decode_head_dim(D)) return ATTN_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
   if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(Lmax) > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;

@@ -100,10 +100,16 @@ struct GqaSmem {
   static int bytes(int G) { return kOOff + kComputeWarps * G * D * 4 + 2 * NST * 8 + 1024; }
 };
 
+// CTAs per SM of the bf16 decode: two up to D = 128; one at D = 256, whose 64 KB stages, 64 KB
+// cross-warp reduction and ~230 registers per thread (query fragments and 32 accumulator tiles)
+// leave room for a single CTA.
+__host__ __device__ constexpr int gqa_ctas_per_sm(int D) { return D >= 256 ? 1 : 2; }
+__host__ __device__ constexpr int gqa_stages(int D) { return D >= 256 ? 2 : 3; }
+
 // Grouped-query split-KV decode.  Grid: persistent; items (b, kv head, split) in row-major
 // order, CTA c takes items c, c + grid, ...
 template <int D, int NST>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, gqa_ctas_per_sm(D))
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
   using L = GqaSmem<D, NST>;
@@ -1416,7 +1422,7 @@ attn_status_t launch_gqa_typed(const void* q, const void* k, const void* v, cons
                                int Lmax, void* o, float* lse, int B, int Hq, int Hkv, float scale,
                                const float2* table, int rope_il, void* ws, const DecodePlan& plan,
                                cudaStream_t st) {
-  constexpr int NST = 3;
+  constexpr int NST = gqa_stages(D);
   using L = GqaSmem<D, NST>;
   CUtensorMap tk, tv;
   if (!make_tmap_3d(&tk, k, 2, D, Lmax, static_cast<uint64_t>(B) * Hkv, 64, kTileKeys, 128) ||
@@ -1461,7 +1467,7 @@ attn_status_t launch_gqa_typed(const void* q, const void* k, const void* v, cons
 std::atomic<int> g_forced_decode_splits{0};
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int Lmax) {
-  return plan_common(B * Hkv, Lmax, 2 * sm_count(), 2.0 * D * 2, Hq / Hkv, D,
+  return plan_common(B * Hkv, Lmax, gqa_ctas_per_sm(D) * sm_count(), 2.0 * D * 2, Hq / Hkv, D,
                      g_forced_decode_splits.load());
 }
 
@@ -1653,7 +1659,11 @@ attn_status_t launch_decode_append(const void* q, const void* k_new, const void*
   auto* kc = static_cast<__nv_bfloat16*>(k_cache);
   auto* vc = static_cast<__nv_bfloat16*>(v_cache);
   auto* oo = static_cast<__nv_bfloat16*>(o);
-  if (D == 128)
+  if (D == 256)
+    append_merge_kernel<256><<<grid, threads, 0, st>>>(qq, kn, vn, kc, vc, lens, Lmax, oo,
+                                                              lse_hist, lse, Hq, Hkv, scale,
+                                                              table, rope_il, device_status_ptr());
+  else if (D == 128)
     append_merge_kernel<128><<<grid, threads, 0, st>>>(qq, kn, vn, kc, vc, lens, Lmax, oo,
                                                               lse_hist, lse, Hq, Hkv, scale,
                                                               table, rope_il, device_status_ptr());
@@ -1670,6 +1680,9 @@ attn_status_t launch_decode(const void* q, const void* k, const void* v, const i
                             int Lmax, void* o, float* lse, int B, int Hq, int Hkv, int D,
                             float scale, const float2* table, int rope_il, void* ws,
                             const DecodePlan& plan, cudaStream_t st) {
+  if (D == 256)
+    return launch_gqa_typed<256>(q, k, v, lens, Lmax, o, lse, B, Hq, Hkv, scale, table, rope_il,
+                                 ws, plan, st);
   if (D == 128)
     return launch_gqa_typed<128>(q, k, v, lens, Lmax, o, lse, B, Hq, Hkv, scale, table, rope_il,
                                  ws, plan, st);

@@ -65,7 +65,7 @@ extern "C" ATTN_API attn_status_t attn_decode_noalloc(
   if (!split_rope_arg(rope, 1, &rope, &il)) return ATTN_ERR_INVALID_ARG;
   if (rope && !finite_pos(rope_theta)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16 || dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(Lmax) > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
   attn_status_t st = check_device();

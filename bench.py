@@ -486,6 +486,19 @@ def variants(b, d):
     out["decode_fp8_cache_b128"] = {"graph_ms": round(tg, 5), "gbs": round(nbytes / tg / 1e6, 1),
                                     "frac_of_hbm": round(nbytes / tg / 1e6 / measured_peaks()[0], 4)}
     del q, kc, vc, cl, o
+    # head dim 256 (bf16 cache), batch 64: 1 GiB of history, one CTA per SM
+    q, kc, vc, cl = synthetic.decode_inputs(64, Dd["Hq"], Dd["Hkv"], Dd["L"], 256, Dd["L"], seed=7)
+    q, kc, vc, cl = q.cuda(), kc.cuda(), vc.cuda(), cl.cuda()
+    o = torch.empty((64, Dd["Hq"], 256), dtype=torch.bfloat16, device="cuda")
+
+    def d256():
+        b.attn_decode(q, kc, vc, cl, o=o, rope=True, rope_theta=THETA)
+
+    nbytes = workload.decode_bytes(64, Dd["Hq"], Dd["Hkv"], Dd["L"], 256)
+    tg = time_graph(d256, 50)
+    out["decode_d256_b64"] = {"graph_ms": round(tg, 5), "gbs": round(nbytes / tg / 1e6, 1),
+                              "frac_of_hbm": round(nbytes / tg / 1e6 / measured_peaks()[0], 4)}
+    del q, kc, vc, cl, o
     # fp8 e5m2 latent cache (half the bytes), batch 128
     Lt = LATENT
     lq, lc, ll = synthetic.latent_inputs(Lt["B"], Lt["H"], Lt["L"], Lt["L"], seed=6,

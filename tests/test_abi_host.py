@@ -180,6 +180,11 @@ def test_decode_validation(L):
     assert _decode(L, Hq=64, Hkv=2) == UNSUPPORTED      # group of 32 > 16
     assert _decode(L, dt=1, D=64) == UNSUPPORTED        # fp8 cache only for D = 128
     assert _decode(L, rope=3) == INVALID
+    assert _decode(L, D=256, dt=1) == UNSUPPORTED        # fp8 cache: D = 128 only
+    assert _decode(L, D=512) == UNSUPPORTED
+    # D = 256 (bf16) is a decode head dim: it has a plan (and a workspace when it splits)
+    assert binding.attn_decode_workspace_size(1, 32, 8, 256, 2048) > 0
+    assert binding.attn_decode_append_workspace_size(1, 32, 8, 256, 2048) > 0
 
 
 def _append(L, **kw):

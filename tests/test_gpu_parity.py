@@ -572,3 +572,43 @@ def test_rope_styles_differ_on_device():
     a = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda())
     b = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda(), rope_style=IL)
     assert (a.float() - b.float()).abs().max().item() > 1e-2
+
+
+# --------------------------------------------------------------------------------------------
+# head dim 256 (bf16 caches): decode and append
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens,style", [
+    (1, 32, 8, 2048, [2048], "half"),           # split KV over many CTAs
+    (3, 32, 8, 2048, [2048, 1, 777], "half"),   # ragged, one single-key sequence
+    (2, 16, 1, 300, [300, 129], "half"),        # group of 16, Lmax not a tile multiple
+    (2, 8, 2, 512, [512, 65], IL),
+])
+def test_decode_d256(B, Hq, Hkv, Lmax, lens, style):
+    q, kc, vc, cl = synthetic.decode_inputs(B, Hq, Hkv, Lmax, 256, lens, seed=B + Hq + 256)
+    o, lse = binding.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), cl.cuda(), want_lse=True,
+                                 rope_style=style)
+    status_ok()
+    ro, rl = oracle.decode(f64(q), f64(kc), f64(vc), cl.numpy(), rope=True, theta=10000.0,
+                           rope_style=style)
+    check(o.cpu(), ro, what="O decode D=256")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE decode D=256")
+
+
+def test_decode_append_d256():
+    B, Hq, Hkv, Lmax, D, lens = 3, 16, 4, 400, 256, [399, 1, 200]
+    q, kc, vc, cl, kn, vn = _append_inputs(B, Hq, Hkv, Lmax, D, lens, seed=256)
+    gk, gv, gl = kc.cuda(), vc.cuda(), cl.cuda()
+    o, lse = binding.attn_decode_append(q.cuda(), kn.cuda(), vn.cuda(), gk, gv, gl, want_lse=True,
+                                        rope=True, rope_theta=10000.0)
+    status_ok()
+    ro, rl, krow = oracle.decode_append(f64(q), f64(kc), f64(vc), cl.numpy(), f64(kn), f64(vn),
+                                        rope=True, theta=10000.0)
+    check(o.cpu(), ro, what="O append D=256")
+    check(lse.cpu(), rl, LSE_TOL, None, what="LSE append D=256")
+    assert torch.equal(gl.cpu(), cl + 1)
+    gk, gv = gk.cpu(), gv.cpu()
+    for b in range(B):
+        L = int(cl[b])
+        np.testing.assert_allclose(f64(gk[b, :, L]), krow[b], rtol=0, atol=1.6e-2)
+        assert torch.equal(gv[b, :, L], vn[b])
