@@ -255,7 +255,9 @@ attn_status_t launch_typed_il(const void* x, void* y, int B, int H, int S, int D
     const long long work = static_cast<long long>(B) * S * (D / Vec<T>::N);
     long long blocks = (work + threads - 1) / threads;
     if (blocks > cap) blocks = cap;
-    constexpr int HU = Vec<T>::N == 8 ? 4 : 2;
+    // one 16-byte chunk per head (the half-split form moves two): twice the heads per batch
+    // keep as many loads in flight
+    constexpr int HU = Vec<T>::N == 8 ? 8 : 4;
     rope_il_pos_kernel<T, HU><<<static_cast<int>(blocks), threads, 0, st>>>(
         static_cast<const T*>(x), static_cast<T*>(y), B, H, S, D, pos0, table);
   } else {
