@@ -158,6 +158,39 @@ def attention(q, k, v, causal: bool, scale: float | None = None, q_pos=None):
     return O, LSE
 
 
+def attention_backward(q, k, v, do, causal: bool, scale: float | None = None):
+    """Gradients of the loss L with dL/dO = ``do`` through O = softmax(scale Q K^T + mask) V.
+
+    Inputs as ``attention`` (RoPE, when used, is applied to q and k before this call; its own
+    gradient is the inverse rotation).  Per (b, hq) with KV head h = hq // G, by the chain rule
+    on the definition: P = softmax(S); dV_h += P^T dO; dP = dO V^T; dS = P * (dP - rowsum(dP * P))
+    (the softmax Jacobian); dQ = scale dS K; dK_h += scale dS^T Q.  The KV gradients of a group
+    are summed over its G query heads.  Returns (dQ, dK, dV) in float64.
+    """
+    q, k, v, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, do))
+    B, Hq, Sq, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for hq in range(Hq):
+            h = hq // G
+            s = scores(q[b, hq], k[b, h], scale, causal)
+            m = np.max(s, axis=-1, keepdims=True)
+            e = np.exp(s - m)
+            p = e / np.sum(e, axis=-1, keepdims=True)
+            dv[b, h] += p.T @ do[b, hq]
+            dp = do[b, hq] @ v[b, h].T
+            ds = p * (dp - np.sum(dp * p, axis=-1, keepdims=True))
+            dq[b, hq] = scale * (ds @ k[b, h])
+            dk[b, h] += scale * (ds.T @ q[b, hq])
+    return dq, dk, dv
+
+
 def attention_probs(q, k, causal: bool, scale: float | None = None):
     """The normalised probability matrices P [B,Hq,Sq,Skv] (for invariant checks)."""
     q, k = np.asarray(q, np.float64), np.asarray(k, np.float64)

@@ -245,6 +245,54 @@ def pin_rope_style_through_entry_points(prefill=O.prefill, decode=O.decode,
         np.testing.assert_allclose(x, y, atol=1e-12)
 
 
+def pin_backward_finite_differences(bwd=O.attention_backward):
+    """Central differences of L = sum(O * W) in float64 against the analytic gradients."""
+    for causal in (True, False):
+        q, k, v = rnd(1, 2, 5, 3), rnd(1, 1, 5, 3), rnd(1, 1, 5, 3)
+        W = rnd(1, 2, 5, 3)
+
+        def loss(qq, kk, vv):
+            return float(np.sum(O.attention(qq, kk, vv, causal)[0] * W))
+
+        dq, dk, dv = bwd(q, k, v, W, causal)
+        h = 1e-5
+        for x, g in ((q, dq), (k, dk), (v, dv)):
+            for idx in np.ndindex(x.shape):
+                old = x[idx]
+                x[idx] = old + h
+                lp = loss(q, k, v)
+                x[idx] = old - h
+                lm = loss(q, k, v)
+                x[idx] = old
+                assert abs((lp - lm) / (2 * h) - g[idx]) < 1e-7, (causal, idx)
+
+
+def pin_backward_gqa_equals_repeated(bwd=O.attention_backward):
+    """GQA gradients equal those of MHA on repeated K/V, the K/V ones summed over each group."""
+    q, k, v, do = rnd(2, 4, 6, 8), rnd(2, 2, 6, 8), rnd(2, 2, 6, 8), rnd(2, 4, 6, 8)
+    dq, dk, dv = bwd(q, k, v, do, True)
+    rq, rk, rv = bwd(q, np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1), do, True)
+    np.testing.assert_allclose(dq, rq, atol=1e-12)
+    np.testing.assert_allclose(dk, rk.reshape(2, 2, 2, 6, 8).sum(2), atol=1e-12)
+    np.testing.assert_allclose(dv, rv.reshape(2, 2, 2, 6, 8).sum(2), atol=1e-12)
+
+
+def pin_backward_invariants(bwd=O.attention_backward):
+    """Shifting every key by one vector adds a constant to each row of scores, which the
+    softmax ignores: the key gradients of a head sum to zero.  A zero query attends uniformly,
+    so dV_j is the mean of the dO rows that see key j (causal: row i sees i + 1 keys)."""
+    for causal in (True, False):
+        q, k, v, do = rnd(1, 3, 7, 4), rnd(1, 3, 7, 4), rnd(1, 3, 7, 4), rnd(1, 3, 7, 4)
+        _, dk, _ = bwd(q, k, v, do, causal)
+        np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+    S = 6
+    do = rnd(1, 1, S, 4)
+    _, _, dv = bwd(np.zeros((1, 1, S, 4)), rnd(1, 1, S, 4), rnd(1, 1, S, 4), do, True)
+    for j in range(S):
+        want = sum(do[0, 0, i] / (i + 1) for i in range(j, S))
+        np.testing.assert_allclose(dv[0, 0, j], want, atol=1e-12)
+
+
 def pin_latent_absorbed_equals_explicit(latent=O.latent_decode):
     """Absorbed attention over the shared latent equals the explicit up-projected form.
 
@@ -353,7 +401,8 @@ ALL_PINS = [pin_softmax_sums_to_one, pin_zero_query_is_causal_mean, pin_hand_two
             pin_bruteforce_enumeration, pin_gqa_equals_repeated_mha, pin_rope,
             pin_latent_absorbed_equals_explicit, pin_merge_identity,
             pin_chunk_equals_prompt_rows, pin_append_equals_longer_prompt, pin_rope_interleaved,
-            pin_rope_style_through_entry_points]
+            pin_rope_style_through_entry_points, pin_backward_finite_differences,
+            pin_backward_gqa_equals_repeated, pin_backward_invariants]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -539,6 +588,37 @@ def test_planted_style_plumbing_mistake_is_caught():
                               theta=10000.0, rope_style="half"):
         return O.decode(q, k_cache, v_cache, cache_len, scale, rope, theta)
     assert _fails_some([pin_rope_style_through_entry_points], decode=decode_ignoring_style)
+
+
+def _mutant_backward(kind):
+    def bwd(q, k, v, do, causal, scale=None):
+        q, k, v, do = (np.asarray(t, np.float64) for t in (q, k, v, do))
+        B, Hq, S, D = q.shape
+        G = Hq // k.shape[1]
+        scale = 1 / np.sqrt(D) if scale is None else scale
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        for b in range(B):
+            for hq in range(Hq):
+                h = hq // G
+                s = O.scores(q[b, hq], k[b, h], scale, causal)
+                e = np.exp(s - s.max(-1, keepdims=True))
+                p = e / e.sum(-1, keepdims=True)
+                dv[b, h] += (p @ do[b, hq]) if kind == "dv_no_transpose" else (p.T @ do[b, hq])
+                dp = do[b, hq] @ v[b, h].T
+                ds = p * dp if kind == "no_delta" else p * (dp - np.sum(dp * p, -1, keepdims=True))
+                dq[b, hq] = scale * ((ds.T if kind == "dq_transposed" else ds) @ k[b, h])
+                dk[b, h] += (1.0 if kind == "dk_no_scale" else scale) * (ds.T @ q[b, hq])
+        return dq, dk, dv
+    return bwd
+
+
+BWD_PINS = [pin_backward_finite_differences, pin_backward_gqa_equals_repeated,
+            pin_backward_invariants]
+
+
+@pytest.mark.parametrize("kind", ["dv_no_transpose", "no_delta", "dq_transposed", "dk_no_scale"])
+def test_planted_backward_mistake_is_caught(kind):
+    assert _fails_some(BWD_PINS, bwd=_mutant_backward(kind))
 
 
 def _fails_some(pins, **kw):
