@@ -50,6 +50,11 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.rope_apply_style.argtypes = [vp, vp, i, i, i, i, i, i, f, i, vp]
     L.attn_prefill.restype = i
     L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i, f, f, f, i, i, i, i, i, i, f, i, f, i, vp]
+    L.attn_prefill_backward_workspace_size.restype = sz
+    L.attn_prefill_backward_workspace_size.argtypes = [i, i, i, i]
+    L.attn_prefill_backward.restype = i
+    L.attn_prefill_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
+                                        vp, sz, vp]
     L.attn_prefill_reserve.restype = i
     L.attn_prefill_reserve.argtypes = [i, i, i, i, i]
     L.attn_prefill_chunk.restype = i
@@ -148,6 +153,32 @@ def attn_prefill(q, k, v, causal=True, softmax_scale=0.0, rope=False, rope_theta
                               float(rope_theta), int(pos0),
                               _stream(stream)), "attn_prefill")
     return (o, lse) if (want_lse or lse is not None) else o
+
+
+def attn_prefill_backward_workspace_size(B, Hq, S, D):
+    return int(lib().attn_prefill_backward_workspace_size(B, Hq, S, D))
+
+
+def attn_prefill_backward(q, k, v, o, lse, dout, causal=True, softmax_scale=0.0, dq=None,
+                          dk=None, dv=None, workspace=None, stream=None):
+    """(dQ, dK, dV) bf16 of attn_prefill's attention for q [B,Hq,S,D], k/v [B,Hkv,S,D] (as the
+    forward used them), its output o and LSE, and dout = dL/dO."""
+    _require_cuda(q, k, v, o, lse, dout, dq, dk, dv, workspace)
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(attn_prefill_backward_workspace_size(B, Hq, S, D),
+                                dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    _check(lib().attn_prefill_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                       _ptr(dq), _ptr(dk), _ptr(dv), DTYPE_CODES[q.dtype], B, Hq,
+                                       Hkv, S, D, int(bool(causal)), float(softmax_scale),
+                                       _ptr(workspace), wbytes, _stream(stream)),
+           "attn_prefill_backward")
+    return dq, dk, dv
 
 
 def attn_prefill_chunk(q, k_cache, v_cache, skv, softmax_scale=0.0, rope=True,

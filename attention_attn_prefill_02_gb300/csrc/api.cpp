@@ -120,6 +120,39 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
                         D, causal, scale, tab, rope ? 1 : 0, pos0, as_stream(stream));
 }
 
+size_t attn_prefill_backward_workspace_size(int B, int Hq, int S, int D) {
+  if (B < 1 || Hq < 1 || S < 1 || (D != 64 && D != 128)) return 0;
+  return bwd_workspace_bytes(B, Hq, S, D);
+}
+
+attn_status_t attn_prefill_backward(const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dout, void* dq, void* dk,
+                                    void* dv, attn_dtype_t dtype, int B, int Hq, int Hkv, int S,
+                                    int D, int causal, float softmax_scale, void* workspace,
+                                    size_t workspace_bytes, attn_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(S) > (1LL << 30) ||
+      static_cast<long long>(B) * Hq * S > (1LL << 31) / 128)
+    return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < bwd_workspace_bytes(B, Hq, S, D)) return ATTN_ERR_WORKSPACE;
+  attn_status_t st = check_device();
+  if (st != ATTN_OK) return st;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return launch_prefill_backward(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, causal,
+                                 scale, workspace, as_stream(stream));
+}
+
 attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D) {
   if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || (D != 64 && D != 128)) return ATTN_ERR_INVALID_ARG;
   attn_status_t st = check_device();

@@ -115,6 +115,14 @@ attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, i
                             const float2* table, int rope_il, void* ws, const DecodePlan& plan,
                             cudaStream_t st);
 
+// Attention backward (bf16): workspace = Delta [B*Hq*S] fp32 (256-byte rounded) + the fp32 dQ
+// accumulator [B*Hq*S*D].
+size_t bwd_workspace_bytes(int B, int Hq, int S, int D);
+attn_status_t launch_prefill_backward(const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dout, void* dq, void* dk,
+                                      void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
+                                      float scale, void* ws, cudaStream_t st);
+
 // S query rows at positions Skv - S .. Skv - 1 against Skv keys (rows kv_pitch apart per head);
 // rope_k: the fused RoPE rotates the keys too (else only the queries).
 attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -499,6 +499,23 @@ def variants(b, d):
     out["decode_d256_b64"] = {"graph_ms": round(tg, 5), "gbs": round(nbytes / tg / 1e6, 1),
                               "frac_of_hbm": round(nbytes / tg / 1e6 / measured_peaks()[0], 4)}
     del q, kc, vc, cl, o
+    # backward (dQ, dK, dV) at the causal prefill shape, S = 4096; flops counted as 2.5x the
+    # forward's (five products of the forward's size instead of two)
+    q, k, v = synthetic.prefill_inputs(4, 32, 8, 4096, 128, "bf16", seed=8)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    do = torch.randn_like(q)
+    o, lse = b.attn_prefill(q, k, v, causal=True, want_lse=True)
+    bws = torch.empty(b.attn_prefill_backward_workspace_size(4, 32, 4096, 128), dtype=torch.uint8,
+                      device="cuda")
+    gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    tb = time_call(lambda: b.attn_prefill_backward(q, k, v, o, lse, do, causal=True, dq=gq, dk=gk,
+                                                   dv=gv, workspace=bws), 5, 2)
+    bfl = 2.5 * workload.prefill_flops(4, 32, 4096, 128, True)
+    out["backward_causal_d128_s4096"] = {
+        "ms": round(tb, 4), "tflops": round(bfl / tb / 1e9, 1),
+        "frac_of_bf16_burst_peak": round(bfl / tb / 1e9 / measured_peaks()[1], 4),
+        "flops": "2.5 x forward (5 products)", "path": "mma.sync m16n8k16"}
+    del q, k, v, do, o, lse, bws, gq, gk, gv
     # fp8 e5m2 latent cache (half the bytes), batch 128
     Lt = LATENT
     lq, lc, ll = synthetic.latent_inputs(Lt["B"], Lt["H"], Lt["L"], Lt["L"], seed=6,

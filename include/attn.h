@@ -142,6 +142,31 @@ ATTN_API attn_status_t attn_prefill(const void* q, const void* k, const void* v,
                            int rope, float rope_theta, int pos0, attn_stream_t stream);
 
 /*
+ * attn_prefill_backward — gradients of attn_prefill's attention: dQ, dK, dV.
+ * Defines: the gradient of the softmax attention the pages fuse into serving kernels (the
+ * operation of attn_prefill, differentiated by the chain rule; the pages describe only its
+ * forward use).  With P = softmax(scale Q K^T + causal mask): dV = P^T dO, dS = P * (dO V^T -
+ * rowsum(dO * O)), dQ = scale dS K, dK = scale dS^T Q; a KV head's dK, dV sum over the G query
+ * heads that read it.
+ *   q, k, v  [B,Hq,S,D], [B,Hkv,S,D] bf16 as the forward used them (rotated when its RoPE was
+ *            on: the rotation's gradient is the inverse rotation, applied by the caller).
+ *   o        [B,Hq,S,D] bf16 forward output;  lse  [B,Hq,S] float32 forward LSE (natural log).
+ *   dout     [B,Hq,S,D] bf16, dL/dO.
+ *   dq       [B,Hq,S,D] bf16;  dk, dv  [B,Hkv,S,D] bf16 (written, not accumulated).
+ *   causal   0 or 1; softmax_scale <= 0 means 1/sqrt(D).  dtype ATTN_BF16 only; D in {64, 128}.
+ *   workspace  device buffer of attn_prefill_backward_workspace_size(B, Hq, S, D) bytes, 16-byte
+ *            aligned; no initialisation needed (fp32 row sums and the dQ accumulator).
+ * Errors: INVALID_ARG, UNSUPPORTED (fp8, other D), WORKSPACE, CUDA, NO_DEVICE.
+ */
+ATTN_API size_t attn_prefill_backward_workspace_size(int B, int Hq, int S, int D);
+ATTN_API attn_status_t attn_prefill_backward(const void* q, const void* k, const void* v,
+                                    const void* o, const float* lse, const void* dout, void* dq,
+                                    void* dk, void* dv, attn_dtype_t dtype, int B, int Hq,
+                                    int Hkv, int S, int D, int causal, float softmax_scale,
+                                    void* workspace, size_t workspace_bytes,
+                                    attn_stream_t stream);
+
+/*
  * attn_prefill_reserve — allocate ahead the per-device rotation scratch that attn_prefill
  * (rope = 1, either pairing) and attn_prefill_chunk (rope = 1, bf16) use at this size (S = the
  * query rows), e.g.

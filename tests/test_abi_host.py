@@ -107,6 +107,30 @@ def test_rope_style_arguments(L):
     assert binding._rope_mode(True) == 1
 
 
+def _bwd(L, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE2, do=FAKE, dq=FAKE2, dk=FAKE2, dv=FAKE2,
+                dt=0, B=1, Hq=4, Hkv=1, S=128, D=64, causal=1, scale=0.0, ws=FAKE2, wsb=1 << 30)
+    args.update(kw)
+    return L.attn_prefill_backward(*args.values(), _stream())
+
+
+def test_prefill_backward_validation(L):
+    assert _bwd(L, lse=None) == INVALID
+    assert _bwd(L, ws=None) == INVALID
+    assert _bwd(L, dq=MIS) == INVALID
+    assert _bwd(L, lse=ctypes.c_void_p(0x7F0000000002)) == INVALID
+    assert _bwd(L, Hq=6, Hkv=4) == INVALID
+    assert _bwd(L, causal=2) == INVALID
+    assert _bwd(L, S=0) == INVALID
+    assert _bwd(L, dt=1) == UNSUPPORTED                # bf16 only
+    assert _bwd(L, D=256) == UNSUPPORTED
+    assert _bwd(L, wsb=16) == WORKSPACE
+    n = binding.attn_prefill_backward_workspace_size(2, 8, 300, 128)
+    rows = 2 * 8 * 300
+    assert n == ((rows * 4 + 255) // 256) * 256 + rows * 128 * 4
+    assert binding.attn_prefill_backward_workspace_size(1, 1, 1, 96) == 0
+
+
 def _prefill(L, **kw):
     args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE2, lse=None, dt=0, qs=1.0, ks=1.0, vs=1.0, B=1,
                 Hq=4, Hkv=1, S=128, D=64, causal=1, scale=0.0, rope=1, theta=1e4, pos0=0)

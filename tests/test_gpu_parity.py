@@ -612,3 +612,59 @@ def test_decode_append_d256():
         L = int(cl[b])
         np.testing.assert_allclose(f64(gk[b, :, L]), krow[b], rtol=0, atol=1.6e-2)
         assert torch.equal(gv[b, :, L], vn[b])
+
+
+# --------------------------------------------------------------------------------------------
+# backward: dQ, dK, dV of the prefill attention
+# --------------------------------------------------------------------------------------------
+
+def check_grad(gpu, ref, what):
+    """P and dS are rounded to bf16 (2^-9 relative) before their products and Delta uses the
+    bf16 forward output, so each gradient carries ~0.2-0.5 % relative error: max-abs within
+    2e-2 of the tensor's largest entry, mean-abs within 5e-3 of its mean magnitude."""
+    g = f64(gpu)
+    d = np.abs(g - ref)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite"
+    big, mean = np.abs(ref).max(), np.abs(ref).mean()
+    assert d.max() <= 2e-2 * big, f"{what}: max-abs {d.max():.3e} > 2e-2 * {big:.3e}"
+    assert d.mean() <= 5e-3 * mean, f"{what}: mean-abs {d.mean():.3e} > 5e-3 * {mean:.3e}"
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", [
+    (1, 4, 1, 128, 64, True),      # the tiny config's shape
+    (2, 4, 2, 300, 128, True),     # GQA, ragged tail (several key tiles, partial last)
+    (1, 2, 2, 200, 64, False),
+    (1, 8, 2, 513, 128, True),     # group of 4, one row past whole tiles
+    (1, 2, 1, 77, 128, False),     # shorter than one tile
+    (1, 1, 1, 1, 64, True),        # S = 1
+])
+def test_prefill_backward(B, Hq, Hkv, S, D, causal):
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=S + 11)
+    do = synthetic.normal((B, Hq, S, D), 5000 + S, "bf16")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = binding.attn_prefill(qd, kd, vd, causal=causal, want_lse=True)
+    dq, dk, dv = binding.attn_prefill_backward(qd, kd, vd, o, lse, do.cuda(), causal=causal)
+    status_ok()
+    rq, rk, rv = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do), causal)
+    check_grad(dq.cpu(), rq, "dQ")
+    check_grad(dk.cpu(), rk, "dK")
+    check_grad(dv.cpu(), rv, "dV")
+
+
+def test_prefill_backward_equals_finite_difference_direction():
+    """A directional derivative of sum(O * W) on the device (forward at q +- h u) agrees with
+    <dQ, u> from the backward, independently of the oracle."""
+    B, Hq, Hkv, S, D = 1, 2, 1, 96, 64
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=3)
+    w = synthetic.normal((B, Hq, S, D), 31, "bf16").cuda().float()
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = binding.attn_prefill(qd, kd, vd, causal=True, want_lse=True)
+    dq, _, _ = binding.attn_prefill_backward(qd, kd, vd, o, lse, w.bfloat16(), causal=True)
+    # the oracle's float64 forward gives the finite difference at float64 precision
+    u = np.asarray(synthetic.normal((B, Hq, S, D), 32, "bf16").float())
+    h = 1e-4
+    lp = np.sum(oracle.attention(f64(q) + h * u, f64(k), f64(v), True)[0] * f64(w.cpu()))
+    lm = np.sum(oracle.attention(f64(q) - h * u, f64(k), f64(v), True)[0] * f64(w.cpu()))
+    fd = (lp - lm) / (2 * h)
+    an = float(np.sum(f64(dq.cpu()) * u))
+    assert abs(fd - an) <= 2e-2 * max(1.0, abs(fd)), (fd, an)
