@@ -66,6 +66,23 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const __nv_bfloat16* __r
   }
 }
 
+// The same tile copy as cp.async (16-byte, L2 only), zero-filled past `valid`; the caller
+// commits and waits.
+template <int D>
+__device__ __forceinline__ void prefetch_tile(uint8_t* dst, const __nv_bfloat16* __restrict__ src,
+                                              int valid, int tid) {
+  constexpr int kChunks = D / 8;
+#pragma unroll 4
+  for (int idx = tid; idx < kBwdKeys * kChunks; idx += kBwdThreads) {
+    const int r = idx / kChunks, c = idx % kChunks;
+    const bool in = r < valid;
+    const __nv_bfloat16* g = src + (in ? static_cast<size_t>(r) * D + c * 8 : 0);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst + tile_off(r, c))),
+                 "l"(g), "r"(in ? 16 : 0)
+                 : "memory");
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const BwdParams p) {
   constexpr int E = D / 32;  // elements per lane
@@ -101,13 +118,12 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_dkdv_kernel(const BwdParam
                                              ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + kTile;
-  uint8_t* sQ = sV + kTile;
-  uint8_t* sO = sQ + kTile;  // dO
-  uint8_t* sDs = sO + kTile;
+  uint8_t* sQb = sV + kTile;      // two Q tiles, then two dO tiles (double-buffered)
+  uint8_t* sOb = sQb + 2 * kTile;
+  uint8_t* sDs = sOb + 2 * kTile;
   float* sLse = reinterpret_cast<float*>(sDs + kBwdKeys * kDsPitch);
   float* sDel = sLse + kBwdRows;
-  const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aO = smem_u32(sO),
-                 aDs = smem_u32(sDs);
+  const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aDs = smem_u32(sDs);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3, m8 = lane >> 3;
   const int bhkv = p.B * p.Hkv;
@@ -128,19 +144,46 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_dkdv_kernel(const BwdParam
 
   const int key_lo = kv0 + warp * 16 + g;  // this thread's key rows: key_lo and key_lo + 8
   const int q_first = p.causal ? kv0 : 0;   // earlier query rows see none of these keys
-  for (int gi = 0; gi < p.G; ++gi) {
-    const size_t row0 = (static_cast<size_t>(b) * p.Hq + kvh * p.G + gi) * p.S;
-    for (int q0 = q_first; q0 < p.S; q0 += kBwdRows) {
-      __syncthreads();  // the previous tile's shared data is no longer read
-      load_tile<D>(sQ, p.q + (row0 + q0) * D, p.S - q0, tid);
-      load_tile<D>(sO, p.dout + (row0 + q0) * D, p.S - q0, tid);
+  // the (query head, query tile) steps of this CTA, flattened so the next tile's Q and dO can be
+  // fetched while the current one is processed
+  const int per_head = (p.S - q_first + kBwdRows - 1) / kBwdRows;
+  const int steps = p.G * per_head;
+  auto step_rows = [&](int st, size_t& row0, int& q0) {
+    const int gi = st / per_head;
+    q0 = q_first + (st - gi * per_head) * kBwdRows;
+    row0 = (static_cast<size_t>(b) * p.Hq + kvh * p.G + gi) * p.S;
+  };
+  {
+    size_t r0;
+    int q0;
+    step_rows(0, r0, q0);
+    prefetch_tile<D>(sQb, p.q + (r0 + q0) * D, p.S - q0, tid);
+    prefetch_tile<D>(sOb, p.dout + (r0 + q0) * D, p.S - q0, tid);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int st = 0; st < steps; ++st) {
+    size_t row0;
+    int q0;
+    step_rows(st, row0, q0);
+    const int buf = st & 1;
+    const uint32_t aQ = smem_u32(sQb + buf * kTile), aO = smem_u32(sOb + buf * kTile);
+    {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      __syncthreads();  // this step's tiles have landed; every warp is done with the last step
       if (tid < kBwdRows) {
         const bool ok = q0 + tid < p.S;
         sLse[tid] = ok ? p.lse[row0 + q0 + tid] * kLog2e : INFINITY;
         sDel[tid] = ok ? p.delta[row0 + q0 + tid] : 0.f;
       }
+      if (st + 1 < steps) {  // the next step's tiles into the other buffers
+        size_t r1;
+        int q1;
+        step_rows(st + 1, r1, q1);
+        prefetch_tile<D>(sQb + (buf ^ 1) * kTile, p.q + (r1 + q1) * D, p.S - q1, tid);
+        prefetch_tile<D>(sOb + (buf ^ 1) * kTile, p.dout + (r1 + q1) * D, p.S - q1, tid);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
       __syncthreads();
-
       // S^T (this warp's 16 keys x 64 query rows) = K_w Q^T, and dP^T = V_w dO^T
       float s[8][4], dp[8][4];
 #pragma unroll
@@ -243,6 +286,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_dkdv_kernel(const BwdParam
       }
     }
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   // dK = scale * sum dS^T Q and dV, bf16, rows key_lo and key_lo + 8
   __nv_bfloat16* dkr = p.dk + (static_cast<size_t>(bh) * p.S + key_lo) * D;
   __nv_bfloat16* dvr = p.dv + (static_cast<size_t>(bh) * p.S + key_lo) * D;
@@ -283,7 +327,7 @@ attn_status_t launch_bwd_typed(BwdParams p, cudaStream_t st) {
     if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
   }
   {
-    constexpr int kSmem = 4 * kBwdKeys * D * 2 + kBwdKeys * kDsPitch + 2 * kBwdRows * 4 + 1024;
+    constexpr int kSmem = 6 * kBwdKeys * D * 2 + kBwdKeys * kDsPitch + 2 * kBwdRows * 4 + 1024;
     auto kern = bwd_dkdv_kernel<D>;
     if (!set_smem_attr(reinterpret_cast<const void*>(kern), kSmem)) return ATTN_ERR_CUDA;
     const int tiles = (p.S + kBwdKeys - 1) / kBwdKeys;
