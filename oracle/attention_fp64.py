@@ -94,12 +94,18 @@ def rope_rotate_interleaved(x: np.ndarray, positions: np.ndarray, theta: float) 
 ROPE_STYLES = ("half", "interleaved")
 
 
-def rope_rotate(x: np.ndarray, positions: np.ndarray, theta: float, style: str = "half"):
-    """RoPE in the given pairing convention ("half": (i, i + D/2); "interleaved": (2i, 2i+1))."""
+def rope_rotate(x: np.ndarray, positions: np.ndarray, theta: float, style: str = "half",
+                inverse: bool = False):
+    """RoPE in the given pairing convention ("half": (i, i + D/2); "interleaved": (2i, 2i+1)).
+
+    ``inverse`` rotates by the opposite angles: the transpose of the rotation, which is also
+    the gradient map from rotated to un-rotated vectors (backward through RoPE).
+    """
+    pos = -np.asarray(positions, dtype=np.float64) if inverse else positions
     if style == "half":
-        return rope_rotate_half(x, positions, theta)
+        return rope_rotate_half(x, pos, theta)
     if style == "interleaved":
-        return rope_rotate_interleaved(x, positions, theta)
+        return rope_rotate_interleaved(x, pos, theta)
     raise ValueError(f"unknown RoPE style {style!r}")
 
 

@@ -293,6 +293,36 @@ def pin_backward_invariants(bwd=O.attention_backward):
         np.testing.assert_allclose(dv[0, 0, j], want, atol=1e-12)
 
 
+def pin_rope_inverse_and_backward_chain(rope=O.rope_rotate, bwd=O.attention_backward):
+    """The inverse rotation undoes the rotation, and it carries gradients back through RoPE:
+    for L = sum(attention(R q, R k, v) * W), dL/dq = R^-1 dQ_rot (central differences)."""
+    for style in O.ROPE_STYLES:
+        x = rnd(2, 9, 8)
+        pos = np.arange(9) * 13 + 2
+        np.testing.assert_allclose(rope(rope(x, pos, 100.0, style), pos, 100.0, style, inverse=True),
+                                   x, atol=1e-12)
+        q, k, v, W = rnd(1, 2, 5, 4), rnd(1, 1, 5, 4), rnd(1, 1, 5, 4), rnd(1, 2, 5, 4)
+        p5 = np.arange(5) + 3
+
+        def loss(qq, kk):
+            return float(np.sum(O.attention(rope(qq, p5, 50.0, style), rope(kk, p5, 50.0, style),
+                                            v, True)[0] * W))
+
+        dq_r, dk_r, _ = bwd(rope(q, p5, 50.0, style), rope(k, p5, 50.0, style), v, W, True)
+        dq = rope(dq_r, p5, 50.0, style, inverse=True)
+        dk = rope(dk_r, p5, 50.0, style, inverse=True)
+        h = 1e-5
+        for x, g in ((q, dq), (k, dk)):
+            for idx in np.ndindex(x.shape):
+                old = x[idx]
+                x[idx] = old + h
+                lp = loss(q, k)
+                x[idx] = old - h
+                lm = loss(q, k)
+                x[idx] = old
+                assert abs((lp - lm) / (2 * h) - g[idx]) < 1e-7, (style, idx)
+
+
 def pin_latent_absorbed_equals_explicit(latent=O.latent_decode):
     """Absorbed attention over the shared latent equals the explicit up-projected form.
 
@@ -402,7 +432,8 @@ ALL_PINS = [pin_softmax_sums_to_one, pin_zero_query_is_causal_mean, pin_hand_two
             pin_latent_absorbed_equals_explicit, pin_merge_identity,
             pin_chunk_equals_prompt_rows, pin_append_equals_longer_prompt, pin_rope_interleaved,
             pin_rope_style_through_entry_points, pin_backward_finite_differences,
-            pin_backward_gqa_equals_repeated, pin_backward_invariants]
+            pin_backward_gqa_equals_repeated, pin_backward_invariants,
+            pin_rope_inverse_and_backward_chain]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -580,6 +611,13 @@ def _mutant_rope_interleaved(kind):
 @pytest.mark.parametrize("kind", ["pair_freq_index", "half_pairs", "sign"])
 def test_planted_interleaved_rope_mistake_is_caught(kind):
     assert _fails_some([pin_rope_interleaved], rope=_mutant_rope_interleaved(kind))
+
+
+def test_planted_inverse_rotation_mistake_is_caught():
+    """An 'inverse' that rotates forwards again (sign kept) fails the round trip."""
+    def rope_no_inverse(x, positions, theta, style="half", inverse=False):
+        return O.rope_rotate(x, positions, theta, style)
+    assert _fails_some([pin_rope_inverse_and_backward_chain], rope=rope_no_inverse)
 
 
 def test_planted_style_plumbing_mistake_is_caught():
