@@ -111,14 +111,16 @@ ROPE_STYLES = {"half": 0, "interleaved": 1}
 ROPE_FLAG_INTERLEAVED = 16  # ATTN_ROPE_FLAG_INTERLEAVED, OR'd into the attention calls' rope
 
 
-def rope_apply(x, y=None, pos0=0, theta=10000.0, stream=None, rope_style="half"):
-    """Rotate x [B,H,S,D] at positions pos0 + s into y (new tensor when None; may be x)."""
+def rope_apply(x, y=None, pos0=0, theta=10000.0, stream=None, rope_style="half", inverse=False):
+    """Rotate x [B,H,S,D] at positions pos0 + s into y (new tensor when None; may be x);
+    `inverse` rotates by the opposite angles (gradients back through RoPE)."""
     _require_cuda(x)
     if y is None:
         y = torch.empty_like(x)
     B, H, S, D = x.shape
     _check(lib().rope_apply_style(_ptr(x), _ptr(y), DTYPE_CODES[x.dtype], B, H, S, D, int(pos0),
-                                  float(theta), ROPE_STYLES[rope_style], _stream(stream)),
+                                  float(theta), ROPE_STYLES[rope_style] | (2 if inverse else 0),
+                                  _stream(stream)),
            "rope_apply")
     return y
 

@@ -56,7 +56,7 @@ attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, int B, int 
 attn_status_t rope_apply_style(const void* x, void* y, attn_dtype_t dtype, int B, int H, int S,
                                int D, int pos0, float theta, attn_rope_style_t style,
                                attn_stream_t stream) {
-  if (style != ATTN_ROPE_HALF_SPLIT && style != ATTN_ROPE_INTERLEAVED) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int>(style) < 0 || static_cast<int>(style) > 3) return ATTN_ERR_INVALID_ARG;
   if (!x || !y || !aligned16(x) || !aligned16(y)) return ATTN_ERR_INVALID_ARG;
   if (!valid_dtype(dtype)) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || S < 1 || D < 2 || D > 256 || (D & 1) || pos0 < 0) return ATTN_ERR_INVALID_ARG;
@@ -68,8 +68,9 @@ attn_status_t rope_apply_style(const void* x, void* y, attn_dtype_t dtype, int B
   if (st != ATTN_OK) return st;
   const float2* tab = rope_table(D, theta, pos0 + S, &st);
   if (!tab) return st;
-  return launch_rope(x, y, dtype, B, H, S, D, pos0, tab, style == ATTN_ROPE_INTERLEAVED ? 1 : 0,
-                     as_stream(stream));
+  const int st_bits = static_cast<int>(style);
+  return launch_rope(x, y, dtype, B, H, S, D, pos0, tab, st_bits & 1, as_stream(stream),
+                     (st_bits >> 1) & 1);
 }
 
 attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -74,9 +74,11 @@ inline attn_status_t launch_status() {
 // ------------------------------------------------------------------------------------------
 // entry points implemented per translation unit (called from api.cpp after validation)
 // ------------------------------------------------------------------------------------------
-// interleaved: pairs (2i, 2i+1) instead of (i, i + D/2), same table.
+// interleaved: pairs (2i, 2i+1) instead of (i, i + D/2), same table; inverse: rotate by the
+// opposite angles (the transpose).
 attn_status_t launch_rope(const void* x, void* y, attn_dtype_t dt, int B, int H, int S, int D,
-                          int pos0, const float2* table, int interleaved, cudaStream_t st);
+                          int pos0, const float2* table, int interleaved, cudaStream_t st,
+                          int inverse = 0);
 
 struct DecodePlan {
   int nsplit;      // splits of the key range per (b, kv head)

@@ -78,7 +78,7 @@ struct Vec<__nv_fp8_e5m2> {
 template <typename T>
 __global__ void __launch_bounds__(256) rope_vec_kernel(const T* __restrict__ x, T* y,
                                                        long long rows, int S, int D, int pos0,
-                                                       const float2* __restrict__ table) {
+                                                       const float2* __restrict__ table, float sgn) {
   constexpr int N = Vec<T>::N;
   const int half = D / 2;
   const int chunks = half / N;
@@ -97,8 +97,9 @@ __global__ void __launch_bounds__(256) rope_vec_kernel(const T* __restrict__ x, 
 #pragma unroll
     for (int j = 0; j < N; ++j) {
       const float2 r = __ldg(cs + j);
-      const float a1 = a[j] * r.x - b[j] * r.y;
-      const float b1 = b[j] * r.x + a[j] * r.y;
+      const float sn = r.y * sgn;
+      const float a1 = a[j] * r.x - b[j] * sn;
+      const float b1 = b[j] * r.x + a[j] * sn;
       a[j] = a1;
       b[j] = b1;
     }
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(256) rope_vec_kernel(const T* __restrict__ x, 
 template <typename T, int HU>
 __global__ void __launch_bounds__(256, 2) rope_pos_kernel(const T* __restrict__ x, T* y, int B,
                                                        int H, int S, int D, int pos0,
-                                                       const float2* __restrict__ table) {
+                                                       const float2* __restrict__ table, float sgn) {
   constexpr int N = Vec<T>::N;
   const int half = D / 2;
   const int chunks = half / N;
@@ -129,7 +130,10 @@ __global__ void __launch_bounds__(256, 2) rope_pos_kernel(const T* __restrict__ 
     float2 r[N];
     const float2* cs = table + static_cast<long long>(pos0 + s) * half + i0;
 #pragma unroll
-    for (int j = 0; j < N; ++j) r[j] = __ldg(cs + j);
+    for (int j = 0; j < N; ++j) {
+      r[j] = __ldg(cs + j);
+      r[j].y *= sgn;
+    }
     const size_t row0 = (static_cast<size_t>(b) * H * S + s) * D + i0;
     for (int h = 0; h < H; h += HU) {
       uint4 ra[HU], rc[HU];  // raw chunks: all loads of the batch go out before any use
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(256, 2) rope_pos_kernel(const T* __restrict__ 
 template <typename T>
 __global__ void __launch_bounds__(256) rope_pair_kernel(const T* __restrict__ x, T* y,
                                                         long long rows, int S, int D, int pos0,
-                                                        const float2* __restrict__ table) {
+                                                        const float2* __restrict__ table, float sgn) {
   const int half = D / 2;
   const long long total = rows * half;
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
@@ -174,10 +178,11 @@ __global__ void __launch_bounds__(256) rope_pair_kernel(const T* __restrict__ x,
     const int i = static_cast<int>(t - row * half);
     const int pos = pos0 + static_cast<int>(row % S);
     const float2 r = table[static_cast<long long>(pos) * half + i];
+    const float sn = r.y * sgn;
     const float a = Vec<T>::load1(x + row * D, i);
     const float b = Vec<T>::load1(x + row * D, i + half);
-    Vec<T>::store1(y + row * D, i, a * r.x - b * r.y);
-    Vec<T>::store1(y + row * D, i + half, b * r.x + a * r.y);
+    Vec<T>::store1(y + row * D, i, a * r.x - b * sn);
+    Vec<T>::store1(y + row * D, i + half, b * r.x + a * sn);
   }
 }
 
@@ -186,7 +191,8 @@ __global__ void __launch_bounds__(256) rope_pair_kernel(const T* __restrict__ x,
 template <typename T, int HU>
 __global__ void __launch_bounds__(256, 2) rope_il_pos_kernel(const T* __restrict__ x, T* y, int B,
                                                           int H, int S, int D, int pos0,
-                                                          const float2* __restrict__ table) {
+                                                          const float2* __restrict__ table,
+                                                          float sgn) {
   constexpr int N = Vec<T>::N;
   const int chunks = D / N;
   const long long total = static_cast<long long>(B) * S * chunks;
@@ -200,7 +206,10 @@ __global__ void __launch_bounds__(256, 2) rope_il_pos_kernel(const T* __restrict
     float2 r[N / 2];
     const float2* cs = table + static_cast<long long>(pos0 + s) * (D / 2) + c * (N / 2);
 #pragma unroll
-    for (int j = 0; j < N / 2; ++j) r[j] = __ldg(cs + j);
+    for (int j = 0; j < N / 2; ++j) {
+      r[j] = __ldg(cs + j);
+      r[j].y *= sgn;
+    }
     const size_t row0 = (static_cast<size_t>(b) * H * S + s) * D + c * N;
     for (int h = 0; h < H; h += HU) {
       uint4 ra[HU];
@@ -229,7 +238,8 @@ __global__ void __launch_bounds__(256, 2) rope_il_pos_kernel(const T* __restrict
 template <typename T>
 __global__ void __launch_bounds__(256) rope_il_pair_kernel(const T* __restrict__ x, T* y,
                                                            long long rows, int S, int D, int pos0,
-                                                           const float2* __restrict__ table) {
+                                                           const float2* __restrict__ table,
+                                                           float sgn) {
   const int half = D / 2;
   const long long total = rows * half;
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
@@ -238,16 +248,17 @@ __global__ void __launch_bounds__(256) rope_il_pair_kernel(const T* __restrict__
     const int i = static_cast<int>(t - row * half);
     const int pos = pos0 + static_cast<int>(row % S);
     const float2 r = table[static_cast<long long>(pos) * half + i];
+    const float sn = r.y * sgn;
     const float e = Vec<T>::load1(x + row * D, 2 * i);
     const float o = Vec<T>::load1(x + row * D, 2 * i + 1);
-    Vec<T>::store1(y + row * D, 2 * i, e * r.x - o * r.y);
-    Vec<T>::store1(y + row * D, 2 * i + 1, o * r.x + e * r.y);
+    Vec<T>::store1(y + row * D, 2 * i, e * r.x - o * sn);
+    Vec<T>::store1(y + row * D, 2 * i + 1, o * r.x + e * sn);
   }
 }
 
 template <typename T>
 attn_status_t launch_typed_il(const void* x, void* y, int B, int H, int S, int D, int pos0,
-                              const float2* table, cudaStream_t st) {
+                              const float2* table, float sgn, cudaStream_t st) {
   const int sms = sm_count();
   const int threads = 256;
   const long long cap = static_cast<long long>(sms) * 16;
@@ -259,20 +270,20 @@ attn_status_t launch_typed_il(const void* x, void* y, int B, int H, int S, int D
     // keep as many loads in flight
     constexpr int HU = Vec<T>::N == 8 ? 8 : 4;
     rope_il_pos_kernel<T, HU><<<static_cast<int>(blocks), threads, 0, st>>>(
-        static_cast<const T*>(x), static_cast<T*>(y), B, H, S, D, pos0, table);
+        static_cast<const T*>(x), static_cast<T*>(y), B, H, S, D, pos0, table, sgn);
   } else {
     const long long rows = static_cast<long long>(B) * H * S;
     long long blocks = (rows * (D / 2) + threads - 1) / threads;
     if (blocks > cap) blocks = cap;
     rope_il_pair_kernel<T><<<static_cast<int>(blocks), threads, 0, st>>>(
-        static_cast<const T*>(x), static_cast<T*>(y), rows, S, D, pos0, table);
+        static_cast<const T*>(x), static_cast<T*>(y), rows, S, D, pos0, table, sgn);
   }
   return launch_status();
 }
 
 template <typename T>
 attn_status_t launch_typed(const void* x, void* y, int B, int H, int S, int D, int pos0,
-                           const float2* table, cudaStream_t st) {
+                           const float2* table, float sgn, cudaStream_t st) {
   const long long rows = static_cast<long long>(B) * H * S;
   const int sms = sm_count();
   const int threads = 256;
@@ -283,21 +294,21 @@ attn_status_t launch_typed(const void* x, void* y, int B, int H, int S, int D, i
     if (blocks > cap) blocks = cap;
     constexpr int HU = Vec<T>::N == 8 ? 4 : 2;
     rope_pos_kernel<T, HU><<<static_cast<int>(blocks), threads, 0, st>>>(
-        static_cast<const T*>(x), static_cast<T*>(y), B, H, S, D, pos0, table);
+        static_cast<const T*>(x), static_cast<T*>(y), B, H, S, D, pos0, table, sgn);
   } else if ((D / 2) % Vec<T>::N == 0) {
     const long long work = rows * ((D / 2) / Vec<T>::N);
     long long blocks = (work + threads - 1) / threads;
     const long long cap = static_cast<long long>(sms) * 16;
     if (blocks > cap) blocks = cap;
     rope_vec_kernel<T><<<static_cast<int>(blocks), threads, 0, st>>>(
-        static_cast<const T*>(x), static_cast<T*>(y), rows, S, D, pos0, table);
+        static_cast<const T*>(x), static_cast<T*>(y), rows, S, D, pos0, table, sgn);
   } else {
     const long long work = rows * (D / 2);
     long long blocks = (work + threads - 1) / threads;
     const long long cap = static_cast<long long>(sms) * 16;
     if (blocks > cap) blocks = cap;
     rope_pair_kernel<T><<<static_cast<int>(blocks), threads, 0, st>>>(
-        static_cast<const T*>(x), static_cast<T*>(y), rows, S, D, pos0, table);
+        static_cast<const T*>(x), static_cast<T*>(y), rows, S, D, pos0, table, sgn);
   }
   return launch_status();
 }
@@ -305,13 +316,16 @@ attn_status_t launch_typed(const void* x, void* y, int B, int H, int S, int D, i
 }  // namespace
 
 attn_status_t launch_rope(const void* x, void* y, attn_dtype_t dt, int B, int H, int S, int D,
-                          int pos0, const float2* table, int interleaved, cudaStream_t st) {
+                          int pos0, const float2* table, int interleaved, cudaStream_t st,
+                          int inverse) {
+  const float sgn = inverse ? -1.f : 1.f;  // the inverse rotation: sines negated
   if (interleaved) {
-    if (dt == ATTN_BF16) return launch_typed_il<__nv_bfloat16>(x, y, B, H, S, D, pos0, table, st);
-    return launch_typed_il<__nv_fp8_e5m2>(x, y, B, H, S, D, pos0, table, st);
+    if (dt == ATTN_BF16)
+      return launch_typed_il<__nv_bfloat16>(x, y, B, H, S, D, pos0, table, sgn, st);
+    return launch_typed_il<__nv_fp8_e5m2>(x, y, B, H, S, D, pos0, table, sgn, st);
   }
-  if (dt == ATTN_BF16) return launch_typed<__nv_bfloat16>(x, y, B, H, S, D, pos0, table, st);
-  return launch_typed<__nv_fp8_e5m2>(x, y, B, H, S, D, pos0, table, st);
+  if (dt == ATTN_BF16) return launch_typed<__nv_bfloat16>(x, y, B, H, S, D, pos0, table, sgn, st);
+  return launch_typed<__nv_fp8_e5m2>(x, y, B, H, S, D, pos0, table, sgn, st);
 }
 
 }  // namespace attn

@@ -68,8 +68,16 @@ typedef enum { ATTN_BF16 = 0, ATTN_FP8_E5M2 = 1 } attn_dtype_t;
  *   ATTN_ROPE_HALF_SPLIT   dims (i, i + D/2)  (the default everywhere)
  *   ATTN_ROPE_INTERLEAVED  dims (2i, 2i + 1)
  * The pages do not fix a convention; the interleaved one is the other common form.
+ * The _INVERSE forms (rope_apply_style only) rotate by the opposite angles: the transpose of
+ * the rotation, which maps gradients of rotated Q / K (attn_prefill_backward's dq, dk) back to
+ * the un-rotated inputs.
  */
-typedef enum { ATTN_ROPE_HALF_SPLIT = 0, ATTN_ROPE_INTERLEAVED = 1 } attn_rope_style_t;
+typedef enum {
+  ATTN_ROPE_HALF_SPLIT = 0,
+  ATTN_ROPE_INTERLEAVED = 1,
+  ATTN_ROPE_HALF_SPLIT_INVERSE = 2,
+  ATTN_ROPE_INTERLEAVED_INVERSE = 3
+} attn_rope_style_t;
 
 /* OR'd into the `rope` argument of the attention calls (with a nonzero mode) to select the
  * interleaved pairing; for the latent decode it applies to the 64 RoPE dims. */
@@ -99,8 +107,8 @@ ATTN_API attn_status_t rope_apply(const void* x, void* y, attn_dtype_t dtype, in
 
 /*
  * rope_apply_style — rope_apply with the pairing convention given (rope_apply is this call with
- * ATTN_ROPE_HALF_SPLIT).  Arguments and errors as rope_apply; `style` outside the enum is
- * INVALID_ARG.
+ * ATTN_ROPE_HALF_SPLIT), or its inverse (the _INVERSE styles).  Arguments and errors as
+ * rope_apply; `style` outside the enum is INVALID_ARG.
  */
 ATTN_API attn_status_t rope_apply_style(const void* x, void* y, attn_dtype_t dtype, int B, int H,
                                int S, int D, int pos0, float theta, attn_rope_style_t style,

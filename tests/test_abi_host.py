@@ -85,7 +85,7 @@ IL = binding.ROPE_FLAG_INTERLEAVED
 def test_rope_style_arguments(L):
     """rope_apply_style takes the two pairings only; the attention calls take the interleaved
     flag only together with a rotation mode, and refuse the forms that have no kernel."""
-    for style in (-1, 2, 7):
+    for style in (-1, 4, 7):
         assert L.rope_apply_style(FAKE, FAKE2, 0, 1, 1, 1, 8, 0, 1e4, style, _stream()) == INVALID
     assert L.rope_apply_style(None, FAKE2, 0, 1, 1, 1, 8, 0, 1e4, 1, _stream()) == INVALID
     assert _prefill(L, rope=IL) == INVALID                    # a pairing without a rotation

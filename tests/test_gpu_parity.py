@@ -668,3 +668,43 @@ def test_prefill_backward_equals_finite_difference_direction():
     fd = (lp - lm) / (2 * h)
     an = float(np.sum(f64(dq.cpu()) * u))
     assert abs(fd - an) <= 2e-2 * max(1.0, abs(fd)), (fd, an)
+
+
+@pytest.mark.parametrize("style,dtype,shape", [
+    ("half", "bf16", (2, 4, 70, 128)), ("interleaved", "bf16", (1, 3, 37, 64)),
+    ("half", "fp8", (1, 2, 50, 64)), ("interleaved", "bf16", (1, 1, 3, 6)),
+])
+def test_rope_apply_inverse(style, dtype, shape):
+    x = synthetic.rope_input(*shape, dtype=dtype, seed=shape[2] + 5)
+    y = binding.rope_apply(x.cuda(), pos0=7, theta=10000.0, rope_style=style, inverse=True)
+    torch.cuda.synchronize()
+    ref = oracle.rope_rotate(f64(x), 7 + np.arange(shape[2]), 10000.0, style, inverse=True)
+    if dtype == "bf16":
+        check(y.cpu(), ref, what="inverse rope")
+    else:
+        r = f64(torch.from_numpy(ref).to(torch.float8_e5m2))
+        g = f64(y.cpu())
+        assert np.all(np.abs(g - r) <= np.maximum(np.abs(r), 2.0 ** -14) * 0.25 * 1.0001)
+
+
+@pytest.mark.parametrize("style", ["half", "interleaved"])
+def test_backward_through_rope(style):
+    """RoPE applied by rope_apply, attention, its backward, and the inverse rotation of dQ / dK:
+    the gradients with respect to the un-rotated Q and K."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 200, 128
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=41)
+    do = synthetic.normal((B, Hq, S, D), 42, "bf16")
+    qr = binding.rope_apply(q.cuda(), pos0=3, rope_style=style)
+    kr = binding.rope_apply(k.cuda(), pos0=3, rope_style=style)
+    o, lse = binding.attn_prefill(qr, kr, v.cuda(), causal=True, want_lse=True)
+    dqr, dkr, dv = binding.attn_prefill_backward(qr, kr, v.cuda(), o, lse, do.cuda(), causal=True)
+    dq = binding.rope_apply(dqr, pos0=3, rope_style=style, inverse=True)
+    dk = binding.rope_apply(dkr, pos0=3, rope_style=style, inverse=True)
+    status_ok()
+    pos = 3 + np.arange(S)
+    rq_r, rk_r, rv = oracle.attention_backward(oracle.rope_rotate(f64(q), pos, 10000.0, style),
+                                               oracle.rope_rotate(f64(k), pos, 10000.0, style),
+                                               f64(v), f64(do), True)
+    check_grad(dq.cpu(), oracle.rope_rotate(rq_r, pos, 10000.0, style, inverse=True), "dQ")
+    check_grad(dk.cpu(), oracle.rope_rotate(rk_r, pos, 10000.0, style, inverse=True), "dK")
+    check_grad(dv.cpu(), rv, "dV")
