@@ -887,6 +887,16 @@ def single_case(args):
         q, kc, vc, cl = q.cuda(), kc.cuda(), vc.cuda(), cl.cuda()
         b.attn_rope_table_reserve(128, THETA, 2049)
         fn = lambda: b.attn_decode(q, kc, vc, cl, rope=True, rope_theta=THETA)
+    elif args.case == "backward":
+        q, k, v = synthetic.prefill_inputs(4, 32, 8, args.S, 128, "bf16", seed=1)
+        q, k, v = q.cuda(), k.cuda(), v.cuda()
+        do = torch.randn_like(q)
+        o, lse = b.attn_prefill(q, k, v, causal=True, want_lse=True)
+        bws = torch.empty(b.attn_prefill_backward_workspace_size(4, 32, args.S, 128),
+                          dtype=torch.uint8, device="cuda")
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        fn = lambda: b.attn_prefill_backward(q, k, v, o, lse, do, causal=True, dq=grads[0],
+                                             dk=grads[1], dv=grads[2], workspace=bws)
     elif args.case == "latent":
         q, c, cl = synthetic.latent_inputs(args.B, 16, 2048, 2048, seed=1)
         q, c, cl = q.cuda(), c.cuda(), cl.cuda()
@@ -915,7 +925,8 @@ def main():
                     choices=["prefill", "prefill-fused", "prefill-unfused", "prefill-d64",
                              "decode", "decode-fp8",
                              "latent",
-                             "rope"], help="time one kernel alone (for profiler captures)")
+                             "rope", "backward"],
+                    help="time one kernel alone (for profiler captures)")
     ap.add_argument("--S", type=int, default=4096)
     ap.add_argument("--B", type=int, default=128)
     args = ap.parse_args()
