@@ -54,6 +54,29 @@ int main(void) {
          attn_decode_latent(a, a, (const int32_t*)o, 2048, o, NULL, ATTN_BF16, 1, 17, 0.f, 1,
                             1e4f, o, 1u << 20, NULL),
          ATTN_ERR_UNSUPPORTED);
+  expect("rope style range",
+         rope_apply_style(a, o, ATTN_BF16, 1, 1, 1, 64, 0, 1e4f, (attn_rope_style_t)4, NULL),
+         ATTN_ERR_INVALID_ARG);
+  expect("interleaved flag without a mode",
+         attn_prefill(a, a, a, o, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 1, 4, 1, 128, 64, 1, 0.f,
+                      ATTN_ROPE_FLAG_INTERLEAVED, 1e4f, 0, NULL),
+         ATTN_ERR_INVALID_ARG);
+  expect("interleaved fused form",
+         attn_prefill(a, a, a, o, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 1, 4, 1, 128, 64, 1, 0.f,
+                      2 | ATTN_ROPE_FLAG_INTERLEAVED, 1e4f, 0, NULL),
+         ATTN_ERR_UNSUPPORTED);
+  expect("backward fp8",
+         attn_prefill_backward(a, a, a, a, (const float*)o, a, o, o, o, ATTN_FP8_E5M2, 1, 4, 1,
+                               128, 64, 1, 0.f, o, 1u << 30, NULL),
+         ATTN_ERR_UNSUPPORTED);
+  expect("backward workspace",
+         attn_prefill_backward(a, a, a, a, (const float*)o, a, o, o, o, ATTN_BF16, 1, 4, 1, 128,
+                               64, 1, 0.f, o, 16, NULL),
+         ATTN_ERR_WORKSPACE);
+  if (attn_prefill_backward_workspace_size(1, 4, 128, 64) == 0) {
+    printf("FAIL backward workspace size\n");
+    ++failures;
+  }
   expect("split hook range", attn_set_decode_splits(-1), ATTN_ERR_INVALID_ARG);
   expect("reserve sizes", attn_prefill_reserve(0, 1, 1, 128, 128), ATTN_ERR_INVALID_ARG);
   if (attn_decode_workspace_size(1, 30, 8, 128, 2048) != 0) {
