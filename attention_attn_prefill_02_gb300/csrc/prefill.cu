@@ -857,9 +857,12 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   p.nM = (S + kRowsPerItem - 1) / kRowsPerItem;
   p.nKV = (Skv + BN - 1) / BN;
   p.n_items = p.nM * B * Hq;
-  // causal: blocks of levels give each stream at least 16 items per block while keeping the
-  // heaviest levels first; otherwise all levels of a stream run together
-  p.mblk = causal ? std::max(1, 16 / p.G) : p.nM;
+  // causal, long prompts (more than 16 query-block levels, where the K/V streams outgrow L2):
+  // blocks of levels give each stream at least 16 items per block while keeping the heaviest
+  // levels first.  Shorter causal prompts keep one level per block, i.e. the plain
+  // heaviest-first order the serpentine deal balances best (their K/V fit in L2 anyway).
+  // Without the mask every item weighs the same: all levels of a stream run together.
+  p.mblk = causal ? (p.nM > 16 ? std::max(1, 16 / p.G) : 1) : p.nM;
   p.c_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
   p.v_scale = v_scale;
   p.table = table;
