@@ -1,7 +1,7 @@
 """GPU parity: every entry point, called through the C ABI, against the float64 oracle on the
 same seeded inputs.
 
-Tolerances (north-star): bf16 outputs max-abs <= 2e-2 and mean-abs <= 2e-3; fp8 e5m2 max-abs
+Tolerances (the required parity bounds): bf16 outputs max-abs <= 2e-2 and mean-abs <= 2e-3; fp8 e5m2 max-abs
 <= 8e-2 (oracle on the dequantised inputs).  LSE is compared to 5e-3 absolute (its error is the
 relative error of the row sum, which bf16 rounding of P keeps near 1e-3).
 """
