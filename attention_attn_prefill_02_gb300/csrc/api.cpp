@@ -89,12 +89,13 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   if (!finite_pos(q_scale) || !finite_pos(k_scale) || !finite_pos(v_scale))
     return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(S) > (1LL << 30) || static_cast<long long>(B) * Hq > (1LL << 24))
     return ATTN_ERR_UNSUPPORTED;
   // the interleaved pairing runs only as rope_apply passes (bf16; the kernel's in-tile rotation
-  // is the half-split form)
+  // is the half-split form); so does every rotation at D = 256 (bf16 only, one Q tile per item)
   if (il && (rope == 2 || dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  if (D == 256 && (rope == 2 || dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
   const float2* tab = nullptr;
@@ -104,7 +105,7 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
     if (!tab) return st;
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  if (rope == 1 && dtype == ATTN_BF16 && (S >= kRopePassMinS || il)) {
+  if (rope == 1 && dtype == ATTN_BF16 && (S >= kRopePassMinS || il || D == 256)) {
     // Q and K rotated once each into the library's scratch, then attention without RoPE
     const size_t qb = rope_scratch_q_bytes(B, Hq, S, D);
     uint8_t* sc = static_cast<uint8_t*>(
@@ -155,7 +156,8 @@ attn_status_t attn_prefill_backward(const void* q, const void* k, const void* v,
 }
 
 attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || (D != 64 && D != 128)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || (D != 64 && D != 128 && D != 256))
+    return ATTN_ERR_INVALID_ARG;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
   // Q and K space at every size (the interleaved pairing uses the passes below 1024 rows too)
@@ -181,10 +183,11 @@ attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, vo
   if (!finite_pos(q_scale) || !finite_pos(k_scale) || !finite_pos(v_scale))
     return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(kv_pitch) > (1LL << 30) || static_cast<long long>(B) * Hq > (1LL << 24))
     return ATTN_ERR_UNSUPPORTED;
   if (rope && dtype == ATTN_FP8_E5M2 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D == 256 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   if (il && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;

@@ -30,7 +30,9 @@ namespace {
 
 constexpr int BM = 128;  // query rows per Q tile (TMEM lanes)
 constexpr int BN = 128;  // keys per KV tile
-constexpr int kRowsPerItem = 2 * BM;
+// Q tiles per work item: two (the ping-pong of the two softmax warpgroups) up to D = 128; one
+// at D = 256, whose O takes 256 TMEM columns (S 128 + O 256 fit the 512; two tiles would not).
+__host__ __device__ constexpr int tiles_per_item(int D) { return D >= 256 ? 1 : 2; }
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kRopeWarp0 = 10;  // fused RoPE: warps 10-13 rotate each K tile in shared memory
@@ -81,10 +83,14 @@ struct Cfg {
   static constexpr int kStTileBytes = STAGED ? BM * D : 0;
   // Separate K and V rings; K is fetched one KV step ahead of V, so a K tile has about two KV
   // steps between landing and its first MMA (room for the TMA latency plus the fused RoPE).
-  static constexpr int kKStages = STAGED ? 2 : ESZ == 2 ? (D == 128 ? 3 : 4) : (D == 128 ? 4 : 6);
-  static constexpr int kVStages = STAGED ? 2 : ESZ == 2 ? (D == 128 ? 2 : 3) : (D == 128 ? 4 : 6);
+  // (D = 256: one 64 KB K and one 64 KB V stage next to the 64 KB Q tile)
+  static constexpr int kKStages =
+      STAGED ? 2 : ESZ == 2 ? (D == 256 ? 1 : D == 128 ? 3 : 4) : (D == 128 ? 4 : 6);
+  static constexpr int kVStages =
+      STAGED ? 2 : ESZ == 2 ? (D == 256 ? 1 : D == 128 ? 2 : 3) : (D == 128 ? 4 : 6);
+  static constexpr int kNT = tiles_per_item(D);
   static constexpr int kQOff = 0;
-  static constexpr int kQStOff = kQOff + 2 * kQTileBytes;
+  static constexpr int kQStOff = kQOff + kNT * kQTileBytes;
   static constexpr int kKVOff = kQStOff + 2 * kStTileBytes;
   static constexpr int kKStOff = kKVOff + kKStages * kKVTileBytes;
   static constexpr int kVOff = kKStOff + kKStages * kStTileBytes;
@@ -220,6 +226,8 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
   constexpr bool ROPE = RM == 1;  // Q and K rotated in shared memory
   constexpr bool STAGED = FP8 && ROPE;  // fp8 inputs, RoPE fused: rotate into bf16 Q/K tiles
   using C = Cfg<D, ESZ, STAGED>;
+  constexpr int NT = C::kNT;             // Q tiles per item
+  constexpr int kRowsPerItem = NT * BM;  // query rows per item
   // First TMEM column of P inside S_t.  The RoPE variants (four more warps, so fewer registers
   // per thread) run the softmax in two passes and write P over the upper half of S; the others
   // hold the whole S row in registers and write P over its first columns.
@@ -277,12 +285,12 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
         int m, b, hq;
         item_coords(p, it, m, b, hq);
         const int hkv = hq / p.G;
-        int n[2];
+        int n[2] = {0, 0};
 #pragma unroll
-        for (int t = 0; t < 2; ++t) n[t] = kv_tiles_for(p, m * kRowsPerItem + t * BM);
+        for (int t = 0; t < NT; ++t) n[t] = kv_tiles_for(p, m * kRowsPerItem + t * BM);
         const int nkv = max(n[0], n[1]);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < NT; ++t) {
           if (n[t] == 0 || !ok) continue;
           ok = mbar_wait(&bars->q_empty[t], ph_qe[t] ^ 1, p.status);
           ph_qe[t] ^= 1;
@@ -388,12 +396,12 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
         if (it >= p.n_items) continue;
         int m, b, hq;
         item_coords(p, it, m, b, hq);
-        int n[2];
+        int n[2] = {0, 0};
 #pragma unroll
-        for (int t = 0; t < 2; ++t) n[t] = kv_tiles_for(p, m * kRowsPerItem + t * BM);
+        for (int t = 0; t < NT; ++t) n[t] = kv_tiles_for(p, m * kRowsPerItem + t * BM);
         const int nkv = max(n[0], n[1]);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < NT; ++t) {
           if (n[t] == 0 || !ok) continue;
           ok = mbar_wait(ROPE ? &bars->q_ready[t] : &bars->q_full[t], ph_qf[t], p.status);
           ph_qf[t] ^= 1;
@@ -406,7 +414,7 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
         if (++ks == C::kKStages) { ks = 0; kph ^= 1; }
         tc_fence_after();
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < NT; ++t) {
           if (n[t] == 0) continue;
           issue_s(t, kslot);
           umma_commit(&bars->s_full[t]);
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
             if (++ks == C::kKStages) { ks = 0; kph ^= 1; }
           }
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
+          for (int t = 0; t < NT; ++t) {
             if (!ok) continue;
             if (j - 1 < n[t]) {
               ok = mbar_wait(&bars->p_full[t], ph_pf[t], p.status);
@@ -495,7 +503,9 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
       if (it >= p.n_items) continue;
       int m, b, hq;
       item_coords(p, it, m, b, hq);
-      const int nkv = max(kv_tiles_for(p, m * kRowsPerItem), kv_tiles_for(p, m * kRowsPerItem + BM));
+      const int nkv = NT == 2 ? max(kv_tiles_for(p, m * kRowsPerItem),
+                                    kv_tiles_for(p, m * kRowsPerItem + BM))
+                              : kv_tiles_for(p, m * kRowsPerItem);
       float2 wc[4], ws[4];  // (cos, sin) at this thread's current row
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -574,7 +584,7 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
     }
    }
   }
-  if (warp < 8) {
+  if (warp < 4 * NT) {  // (with one Q tile, warps 4-7 have no role)
     // ------------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2;          // Q tile of this warpgroup
     const int quarter = warp & 3;     // TMEM lane quarter of this warp
@@ -854,6 +864,7 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   p.off = Skv - S;
   p.rope_k = rope_k;
   p.causal = causal;
+  constexpr int kRowsPerItem = tiles_per_item(D) * BM;
   p.nM = (S + kRowsPerItem - 1) / kRowsPerItem;
   p.nKV = (Skv + BN - 1) / BN;
   p.n_items = p.nM * B * Hq;
@@ -888,6 +899,7 @@ attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* 
     return launch_typed<DD, RR, EE>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S, \
                                     Skv, kv_pitch, causal, scale, table, rope_k, pos0, st);
   ATTN_PREFILL_CASE(128, 0, 2)
+  ATTN_PREFILL_CASE(256, 0, 2)
   ATTN_PREFILL_CASE(128, 1, 2)
   ATTN_PREFILL_CASE(64, 0, 2)
   ATTN_PREFILL_CASE(64, 1, 2)

@@ -151,7 +151,10 @@ def test_prefill_validation(L):
     assert _prefill(L, qs=0.0) == INVALID
     assert _prefill(L, lse=ctypes.c_void_p(0x7F0000000002)) == INVALID
     assert _prefill(L, D=96) == UNSUPPORTED
-    assert _prefill(L, D=256) == UNSUPPORTED
+    assert _prefill(L, D=512) == UNSUPPORTED
+    assert _prefill(L, D=256, dt=1) == UNSUPPORTED     # D = 256: bf16 only
+    assert _prefill(L, D=256, rope=2) == UNSUPPORTED   # ... and RoPE through the passes
+    assert _chunk(L, D=256, dt=1, rope=0) == UNSUPPORTED
 
 
 def _chunk(L, **kw):

@@ -708,3 +708,36 @@ def test_backward_through_rope(style):
     check_grad(dq.cpu(), oracle.rope_rotate(rq_r, pos, 10000.0, style, inverse=True), "dQ")
     check_grad(dk.cpu(), oracle.rope_rotate(rk_r, pos, 10000.0, style, inverse=True), "dK")
     check_grad(dv.cpu(), rv, "dV")
+
+
+# --------------------------------------------------------------------------------------------
+# head dim 256 prefill: one Q tile per work item
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,causal,rope", [
+    (1, 4, 1, 128, True, False),
+    (2, 8, 2, 300, True, True),      # ragged tail, RoPE through the rotation passes, GQA
+    (1, 2, 2, 200, False, False),
+    (1, 4, 4, 513, True, True),
+])
+def test_prefill_d256(B, Hq, Hkv, S, causal, rope):
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, 256, "bf16", seed=S + 256)
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, rope=rope,
+                                  rope_theta=10000.0, want_lse=True)
+    status_ok()
+    ro, rl = oracle.prefill(f64(q), f64(k), f64(v), causal=causal, rope=rope, theta=10000.0)
+    check(o.cpu(), ro, what="O prefill D=256")
+    check(lse.cpu(), rl, ROPE_LSE_TOL if rope else LSE_TOL, None, what="LSE prefill D=256")
+
+
+def test_prefill_chunk_d256():
+    B, Hq, Hkv, Sq, Skv, pitch, D = 2, 8, 2, 64, 300, 320, 256
+    q = synthetic.normal((B, Hq, Sq, D), 960, "bf16")
+    kc = synthetic.normal((B, Hkv, pitch, D), 961, "bf16")
+    vc = synthetic.normal((B, Hkv, pitch, D), 962, "bf16")
+    o, lse = binding.attn_prefill_chunk(q.cuda(), kc.cuda(), vc.cuda(), Skv, rope=True,
+                                        rope_theta=10000.0, want_lse=True)
+    status_ok()
+    ro, rl = oracle.prefill_chunk(f64(q), f64(kc), f64(vc), Skv, rope=True, theta=10000.0)
+    check(o.cpu(), ro, what="O chunk D=256")
+    check(lse.cpu(), rl, ROPE_LSE_TOL, None, what="LSE chunk D=256")
