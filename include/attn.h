@@ -135,7 +135,8 @@ ATTN_API attn_status_t rope_apply_style(const void* x, void* y, attn_dtype_t dty
  *                it; the fully fused form, measured beside the other).
  *            | ATTN_ROPE_FLAG_INTERLEAVED: pairs (2i, 2i+1); bf16 with rope = 1 only (always
  *                the rope_apply passes); fp8 or rope = 2 with the flag is UNSUPPORTED.
- *   D in {64, 128}; Hq % Hkv == 0; S >= 1.  fp8 e5m2 inputs: P is rounded to e4m3 for the PV
+ *   D in {64, 128, 256} (256: bf16 only, rope 0 or 1 with the rotation passes); Hq % Hkv == 0;
+ *   S >= 1.  fp8 e5m2 inputs: P is rounded to e4m3 for the PV
  *   product; with rope = 1 (D = 128 only) Q and K are rotated into bf16 tiles inside the
  *   kernel (QK^T then runs in bf16, PV stays fp8), because rotated values re-rounded to fp8
  *   would exceed the fp8 error budget.
@@ -180,7 +181,7 @@ ATTN_API attn_status_t attn_prefill_backward(const void* q, const void* k, const
  * query rows), e.g.
  * before a CUDA-graph capture, which cannot allocate.  Together with attn_rope_table_reserve it
  * leaves nothing to allocate in later calls up to that size.
- * Errors: INVALID_ARG (sizes, D not in {64, 128}), CUDA, NO_DEVICE.
+ * Errors: INVALID_ARG (sizes, D not in {64, 128, 256}), CUDA, NO_DEVICE.
  */
 ATTN_API attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D);
 
@@ -200,7 +201,7 @@ ATTN_API attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D
  *            library's scratch, see attn_prefill_reserve; fp8: inside the kernel, into bf16
  *            tiles); 0: q as given.  1 | ATTN_ROPE_FLAG_INTERLEAVED: pairs (2i, 2i+1), bf16
  *            only (fp8: UNSUPPORTED).
- *   1 <= Sq <= Skv <= kv_pitch; D in {64, 128} (fp8 with rope = 1: D = 128); the other
+ *   1 <= Sq <= Skv <= kv_pitch; D in {64, 128, 256} (fp8: D <= 128; fp8 with rope = 1: D = 128); the other
  *   arguments as attn_prefill.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
  */
@@ -234,7 +235,7 @@ ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int Lm
  *              (may be NULL when that size is 0).  Contents need no initialisation.
  *   dtype      storage type of the caches: ATTN_BF16, or ATTN_FP8_E5M2 (D = 128 only; values
  *              are widened exactly to f16 for the products).  q is always bfloat16.
- *   D in {64, 128}; Hq % Hkv == 0; Hq / Hkv <= 16.
+ *   D in {64, 128, 256}; Hq % Hkv == 0; Hq / Hkv <= 16.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */
 ATTN_API attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -304,7 +305,7 @@ ATTN_API attn_status_t attn_set_decode_splits(int nsplit);
  *   cache_len device int32 [B], 1 <= cache_len[b] <= Lmax - 1, incremented.
  *   o        [B,Hq,D] bf16.   lse  NULL or [B,Hq] float32 (natural log, over the L + 1 keys).
  *   workspace  device buffer of attn_decode_append_workspace_size() bytes (never zero).
- *   dtype    ATTN_BF16 only; D in {64, 128}; Hq / Hkv <= 16.
+ *   dtype    ATTN_BF16 only; D in {64, 128, 256}; Hq / Hkv <= 16.
  * Device errors: a cache_len outside [1, Lmax - 1] sets DEVICE_ARG; that sequence's row is not
  * written, its length not changed, and its output is the history result (zero when L < 1).
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
