@@ -865,15 +865,19 @@ def single_case(args):
 
     torch.cuda.set_device(0)
     b.lib()
-    if args.case in ("prefill", "prefill-fused", "prefill-unfused", "prefill-d64"):
-        D = 64 if args.case == "prefill-d64" else 128
+    if args.case.startswith("prefill"):
+        # the configs' prefill shapes: causal GQA Z=4 Hq=32 Hkv=8 at D=128 (or 256), and the
+        # non-causal Z=4 H=32 D=64 shape; -fp8 cases take e5m2 inputs (per-tensor scale 1)
+        D = 64 if "d64" in args.case else 256 if "d256" in args.case else 128
         Hkv = 32 if D == 64 else 8
-        causal = D == 128
-        q, k, v = synthetic.prefill_inputs(4, 32, Hkv, args.S, D, "bf16", seed=1)
+        causal = D != 64
+        dt = "fp8" if "fp8" in args.case else "bf16"
+        q, k, v = synthetic.prefill_inputs(4, 32, Hkv, args.S, D, dt, seed=1)
         q, k, v = q.cuda(), k.cuda(), v.cuda()
         b.attn_rope_table_reserve(D, THETA, args.S + 1)
         b.attn_prefill_reserve(4, 32, Hkv, args.S, D)
-        # prefill: RoPE as the library chooses; prefill-fused: Q and K rotated in the kernel
+        # prefill: RoPE as the library chooses; prefill-fused: Q and K rotated in the kernel;
+        # the other cases run attention alone
         rope = {"prefill": 1, "prefill-fused": 2}.get(args.case, 0)
         fn = lambda: b.attn_prefill(q, k, v, causal=causal, rope=rope, rope_theta=THETA)
     elif args.case == "decode":
@@ -923,6 +927,7 @@ def main():
     ap.add_argument("--oracle-one-core", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--case", default=None,
                     choices=["prefill", "prefill-fused", "prefill-unfused", "prefill-d64",
+                             "prefill-fp8", "prefill-fp8-d64", "prefill-d256",
                              "decode", "decode-fp8",
                              "latent",
                              "rope", "backward"],

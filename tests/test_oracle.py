@@ -352,6 +352,41 @@ def pin_latent_absorbed_equals_explicit(latent=O.latent_decode):
             np.testing.assert_allclose(o_abs[b, h], ref, rtol=0, atol=1e-10)
 
 
+def pin_latent_rope_by_hand(latent=O.latent_decode):
+    """The latent decode's RoPE branch: rotating the last 64 query dims at position
+    L = cache_len[b] by hand, then float64 SDPA over the cache rows with V = the first 448 dims.
+
+    The rotation is written out pair by pair with math.cos / math.sin at the angle
+    L * theta^(-2i/64): pairs (i, i + 32) of the 64 RoPE dims for the half-split form, (2i, 2i+1)
+    for the interleaved one (Fixed-budget decode audit — 2026-09-11, "Which implementation was
+    tested": 448 latent dims + 64 RoPE dims; only the RoPE part rotates).  The default scale is
+    1/sqrt(512), the dims the scores use.  Ragged lengths, including 1.
+    """
+    dl, dr = FACTS["mla_latent_dims"]["value"], FACTS["mla_rope_dims"]["value"]
+    B, H, Lmax, theta = 3, 4, 21, 10000.0
+    q, c = rnd(B, H, dl + dr), rnd(B, Lmax, dl + dr)
+    lens = np.array([21, 1, 8])
+    for style in ("half", "interleaved"):
+        o, lse = latent(q, c, lens, rope=True, theta=theta, rope_style=style)
+        for b in range(B):
+            L = int(lens[b])
+            qr = q[b].copy()
+            for i in range(dr // 2):
+                a = L * theta ** (-2.0 * i / dr)
+                i1, i2 = (dl + i, dl + i + dr // 2) if style == "half" else (dl + 2 * i, dl + 2 * i + 1)
+                x1, x2 = q[b, :, i1].copy(), q[b, :, i2].copy()
+                qr[:, i1] = x1 * math.cos(a) - x2 * math.sin(a)
+                qr[:, i2] = x2 * math.cos(a) + x1 * math.sin(a)
+            keys = torch.from_numpy(c[b, :L])[None].expand(H, L, dl + dr)
+            vals = torch.from_numpy(c[b, :L, :dl])[None].expand(H, L, dl)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(qr)[:, None], keys, vals, scale=1 / math.sqrt(dl + dr))
+            np.testing.assert_allclose(o[b], ref[:, 0].numpy(), rtol=0, atol=1e-12)
+            s = (qr @ c[b, :L].T) / math.sqrt(dl + dr)
+            ref_l = s.max(-1) + np.log(np.exp(s - s.max(-1, keepdims=True)).sum(-1))
+            np.testing.assert_allclose(lse[b], ref_l, rtol=0, atol=1e-12)
+
+
 def pin_merge_identity(merge=O.merge_one_key, combine=O.combine_partials):
     tol = FACTS["merge_identity_tolerance"]["value"]
     L, D = 37, 8
@@ -429,7 +464,7 @@ def pin_append_equals_longer_prompt(append=O.decode_append, merge=O.merge_one_ke
 ALL_PINS = [pin_softmax_sums_to_one, pin_zero_query_is_causal_mean, pin_hand_two_key_case,
             pin_one_hot_and_single_key, pin_causal_ignores_future, pin_matches_torch_sdpa,
             pin_bruteforce_enumeration, pin_gqa_equals_repeated_mha, pin_rope,
-            pin_latent_absorbed_equals_explicit, pin_merge_identity,
+            pin_latent_absorbed_equals_explicit, pin_latent_rope_by_hand, pin_merge_identity,
             pin_chunk_equals_prompt_rows, pin_append_equals_longer_prompt, pin_rope_interleaved,
             pin_rope_style_through_entry_points, pin_backward_finite_differences,
             pin_backward_gqa_equals_repeated, pin_backward_invariants,
@@ -695,6 +730,48 @@ def test_planted_merge_mistake_is_caught():
 
     assert _fails_some([pin_merge_identity], merge=bad_merge)
     assert _fails_some([pin_merge_identity], combine=bad_combine)
+
+
+def _mutant_latent(kind):
+    """Copies of the latent decode with one planted mistake in its RoPE branch."""
+    def f(q, c_cache, cache_len, scale=None, rope=True, theta=10000.0, d_latent=448, d_rope=64,
+          rope_style="half"):
+        q, c = np.asarray(q, np.float64), np.asarray(c_cache, np.float64)
+        B, H, dqk = q.shape
+        scale = 1.0 / np.sqrt(dqk) if scale is None else scale
+        O_, L_ = np.empty((B, H, d_latent)), np.empty((B, H))
+        for b in range(B):
+            L = int(cache_len[b])
+            pos = L - 1 if kind == "pos_L_minus_1" else L
+            qb = q[b].copy()
+            if rope:
+                lo = 0 if kind == "first_dims" else d_latent
+                part = qb[:, None, lo: lo + d_rope]
+                if kind == "freq_no2":
+                    ang = pos * np.power(theta, -np.arange(d_rope // 2) / d_rope)
+                    cs, sn = np.cos(ang), np.sin(ang)
+                    x1, x2 = part[..., : d_rope // 2], part[..., d_rope // 2:]
+                    rot = np.concatenate([x1 * cs - x2 * sn, x2 * cs + x1 * sn], -1)
+                else:
+                    rot = O.rope_rotate(part, np.array([pos]), theta, rope_style)
+                qb[:, lo: lo + d_rope] = rot[:, 0]
+            cb = c[b, :L]
+            o, l = O.attention(qb[None, :, None, :], cb[None, None], cb[None, None, :, :d_latent],
+                               causal=False, scale=scale)
+            O_[b], L_[b] = o[0, :, 0], l[0, :, 0]
+        return O_, L_
+    return f
+
+
+@pytest.mark.parametrize("kind", ["pos_L_minus_1", "first_dims", "freq_no2"])
+def test_planted_latent_rope_mistake_is_caught(kind):
+    assert _fails_some([pin_latent_rope_by_hand], latent=_mutant_latent(kind))
+
+
+def test_latent_mutant_harness_is_faithful():
+    """With no mistake planted the mutant copy passes the pin (so the failures above come from
+    the planted mistakes, not from the copy)."""
+    pin_latent_rope_by_hand(latent=_mutant_latent("none"))
 
 
 def test_planted_chunk_and_append_mistakes_are_caught():
