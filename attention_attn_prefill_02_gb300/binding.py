@@ -49,23 +49,28 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.rope_apply_style.restype = i
     L.rope_apply_style.argtypes = [vp, vp, i, i, i, i, i, i, f, i, vp]
     L.attn_prefill.restype = i
-    L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i, f, f, f, i, i, i, i, i, i, f, i, f, i, vp]
+    L.attn_prefill.argtypes = [vp, vp, vp, vp, vp, i, f, f, f, i, i, i, i, i, i, f, i, f, i, vp,
+                               sz, vp]
+    L.attn_prefill_workspace_size.restype = sz
+    L.attn_prefill_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    L.attn_prefill_chunk_workspace_size.restype = sz
+    L.attn_prefill_chunk_workspace_size.argtypes = [i, i, i, i, i, i]
     L.attn_prefill_backward_workspace_size.restype = sz
     L.attn_prefill_backward_workspace_size.argtypes = [i, i, i, i]
     L.attn_prefill_backward.restype = i
     L.attn_prefill_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
                                         vp, sz, vp]
-    L.attn_prefill_reserve.restype = i
-    L.attn_prefill_reserve.argtypes = [i, i, i, i, i]
     L.attn_prefill_chunk.restype = i
     L.attn_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, i, f, f, f, i, i, i, i, i, i, i, f, i, f,
-                                     i, vp]
+                                     i, vp, sz, vp]
     L.attn_decode_workspace_size.restype = sz
     L.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
     L.attn_decode.restype = i
     L.attn_decode.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp, sz, vp]
     L.attn_decode_noalloc.restype = i
     L.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp]
+    L.attn_set_prefill_events.restype = i
+    L.attn_set_prefill_events.argtypes = [vp, vp]
     L.attn_set_decode_splits.restype = i
     L.attn_set_decode_splits.argtypes = [i]
     L.attn_decode_append_workspace_size.restype = sz
@@ -79,6 +84,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_decode_latent.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, f, i, f, vp, sz, vp]
     L.attn_rope_table_reserve.restype = i
     L.attn_rope_table_reserve.argtypes = [i, f, i]
+    L.attn_selftest_wait_timeout.restype = i
+    L.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
     L.attn_get_device_status.restype = i
     L.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     _lib = L
@@ -132,28 +139,42 @@ def _rope_mode(rope, rope_style="half"):
     return mode | (ROPE_FLAG_INTERLEAVED if (mode and ROPE_STYLES[rope_style]) else 0)
 
 
-def attn_prefill_reserve(B, Hq, Hkv, S, D):
-    """Allocate ahead (e.g. before a graph capture) what a RoPE prefill of this size needs."""
-    _check(lib().attn_prefill_reserve(B, Hq, Hkv, S, D), "attn_prefill_reserve")
+def attn_prefill_workspace_size(B, Hq, Hkv, S, D, dtype=torch.bfloat16, rope=False,
+                                rope_style="half"):
+    """Bytes of workspace attn_prefill needs (nonzero when RoPE runs as rotation passes)."""
+    return int(lib().attn_prefill_workspace_size(B, Hq, Hkv, S, D, DTYPE_CODES[dtype],
+                                                 _rope_mode(rope, rope_style)))
+
+
+def _workspace(workspace, need, device):
+    """The caller's workspace, or a fresh one of `need` bytes (None when nothing is needed)."""
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return workspace, (0 if workspace is None else workspace.numel() * workspace.element_size())
 
 
 def attn_prefill(q, k, v, causal=True, softmax_scale=0.0, rope=False, rope_theta=10000.0,
                  pos0=0, o=None, lse=None, want_lse=False, q_scale=1.0, k_scale=1.0,
-                 v_scale=1.0, stream=None, rope_style="half"):
-    """O [B,Hq,S,D] bf16 (and LSE [B,Hq,S] fp32 when requested) for q [B,Hq,S,D], k/v [B,Hkv,S,D]."""
-    _require_cuda(q, k, v, o, lse)
+                 v_scale=1.0, stream=None, rope_style="half", workspace=None):
+    """O [B,Hq,S,D] bf16 (and LSE [B,Hq,S] fp32 when requested) for q [B,Hq,S,D], k/v [B,Hkv,S,D].
+    `workspace`: a uint8 CUDA tensor of at least attn_prefill_workspace_size() bytes (allocated
+    here when None and needed)."""
+    _require_cuda(q, k, v, o, lse, workspace)
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
     if o is None:
         o = torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device=q.device)
     if want_lse and lse is None:
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    mode = _rope_mode(rope, rope_style)
+    workspace, wbytes = _workspace(
+        workspace, int(lib().attn_prefill_workspace_size(B, Hq, Hkv, S, D, DTYPE_CODES[q.dtype],
+                                                         mode)), q.device)
     _check(lib().attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                               DTYPE_CODES[q.dtype], float(q_scale), float(k_scale),
                               float(v_scale), B, Hq, Hkv, S, D, int(bool(causal)),
-                              float(softmax_scale), _rope_mode(rope, rope_style),
-                              float(rope_theta), int(pos0),
-                              _stream(stream)), "attn_prefill")
+                              float(softmax_scale), mode, float(rope_theta), int(pos0),
+                              _ptr(workspace), wbytes, _stream(stream)), "attn_prefill")
     return (o, lse) if (want_lse or lse is not None) else o
 
 
@@ -183,23 +204,34 @@ def attn_prefill_backward(q, k, v, o, lse, dout, causal=True, softmax_scale=0.0,
     return dq, dk, dv
 
 
+def attn_prefill_chunk_workspace_size(B, Hq, Sq, D, dtype=torch.bfloat16, rope=True,
+                                      rope_style="half"):
+    return int(lib().attn_prefill_chunk_workspace_size(B, Hq, Sq, D, DTYPE_CODES[dtype],
+                                                       _rope_mode(bool(rope), rope_style)))
+
+
 def attn_prefill_chunk(q, k_cache, v_cache, skv, softmax_scale=0.0, rope=True,
                        rope_theta=10000.0, pos0=0, o=None, lse=None, want_lse=False, q_scale=1.0,
-                       k_scale=1.0, v_scale=1.0, stream=None, rope_style="half"):
+                       k_scale=1.0, v_scale=1.0, stream=None, rope_style="half", workspace=None):
     """O [B,Hq,Sq,D] bf16 for a chunk q [B,Hq,Sq,D] whose rows are the last Sq of `skv` tokens,
     against the first `skv` rows of the caches [B,Hkv,Lmax,D] (keys stored rotated)."""
-    _require_cuda(q, k_cache, v_cache, o, lse)
+    _require_cuda(q, k_cache, v_cache, o, lse, workspace)
     B, Hq, Sq, D = q.shape
     Hkv, pitch = k_cache.shape[1], k_cache.shape[2]
     if o is None:
         o = torch.empty((B, Hq, Sq, D), dtype=torch.bfloat16, device=q.device)
     if want_lse and lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    mode = _rope_mode(bool(rope), rope_style)
+    workspace, wbytes = _workspace(
+        workspace, int(lib().attn_prefill_chunk_workspace_size(B, Hq, Sq, D,
+                                                               DTYPE_CODES[q.dtype], mode)),
+        q.device)
     _check(lib().attn_prefill_chunk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
                                     DTYPE_CODES[q.dtype], float(q_scale), float(k_scale),
                                     float(v_scale), B, Hq, Hkv, Sq, int(skv), pitch, D,
-                                    float(softmax_scale), _rope_mode(bool(rope), rope_style),
-                                    float(rope_theta), int(pos0), _stream(stream)),
+                                    float(softmax_scale), mode, float(rope_theta), int(pos0),
+                                    _ptr(workspace), wbytes, _stream(stream)),
            "attn_prefill_chunk")
     return (o, lse) if (want_lse or lse is not None) else o
 
@@ -249,6 +281,14 @@ def attn_decode_noalloc(q, k_cache, v_cache, cache_len, o=None, lse=None, want_l
                                      D, float(softmax_scale), _rope_mode(bool(rope), rope_style),
                                      float(rope_theta), _stream(stream)), "attn_decode_noalloc")
     return (o, lse) if (want_lse or lse is not None) else o
+
+
+def attn_set_prefill_events(begin=None, end=None):
+    """Record the torch.cuda.Event pair `begin`/`end` around the attention kernel of every later
+    prefill call (both None: stop).  The events must have been recorded once (torch creates the
+    CUDA event on first use)."""
+    h = [None if e is None else ctypes.c_void_p(e.cuda_event) for e in (begin, end)]
+    _check(lib().attn_set_prefill_events(*h), "attn_set_prefill_events")
 
 
 def attn_set_decode_splits(nsplit):
@@ -315,6 +355,13 @@ def attn_decode_latent(q, c_cache, cache_len, o=None, lse=None, want_lse=False,
 def attn_rope_table_reserve(D, theta, max_pos):
     _check(lib().attn_rope_table_reserve(int(D), float(theta), int(max_pos)),
            "attn_rope_table_reserve")
+
+
+def attn_selftest_wait_timeout(timeout_us, stream=None):
+    """Run one bounded wait that must time out after `timeout_us` (sets TIMEOUT in the status
+    word; the kernel returns on its own)."""
+    _check(lib().attn_selftest_wait_timeout(int(timeout_us), _stream(stream)),
+           "attn_selftest_wait_timeout")
 
 
 def attn_get_device_status(stream=None) -> int:

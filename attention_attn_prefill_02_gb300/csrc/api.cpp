@@ -2,6 +2,7 @@
 // Validation happens entirely on the host before anything is enqueued, so an invalid call
 // returns its status without touching the GPU (this is what the CPU-only tests exercise).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -25,6 +26,24 @@ size_t dtype_bytes(attn_dtype_t dt) { return dt == ATTN_BF16 ? 2 : 1; }
 
 bool valid_dtype(int dt) { return dt == ATTN_BF16 || dt == ATTN_FP8_E5M2; }
 
+// Events recorded around the attention kernel of attn_prefill / attn_prefill_chunk (diagnostics,
+// see attn_set_prefill_events); both null when unset.
+std::atomic<cudaEvent_t> g_ev_begin{nullptr}, g_ev_end{nullptr};
+
+attn_status_t timed_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                            attn_dtype_t dt, float q_scale, float k_scale, float v_scale, int B,
+                            int Hq, int Hkv, int S, int Skv, int kv_pitch, int D, int causal,
+                            float scale, const float2* table, int rope_k, int pos0,
+                            cudaStream_t st) {
+  cudaEvent_t e0 = g_ev_begin.load(), e1 = g_ev_end.load();
+  if (e0 && cudaEventRecord(e0, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  const attn_status_t r = launch_prefill(q, k, v, o, lse, dt, q_scale, k_scale, v_scale, B, Hq,
+                                         Hkv, S, Skv, kv_pitch, D, causal, scale, table, rope_k,
+                                         pos0, st);
+  if (r == ATTN_OK && e1 && cudaEventRecord(e1, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  return r;
+}
+
 }  // namespace
 
 extern "C" {
@@ -43,7 +62,7 @@ const char* attn_status_string(attn_status_t s) {
   return "unknown status";
 }
 
-int attn_version(void) { return 100; }
+int attn_version(void) { return 200; }
 
 // Head dims of the single-token decode paths (bf16 caches; the fp8 cache is D = 128 only).
 static bool decode_head_dim(int D) { return D == 64 || D == 128 || D == 256; }
@@ -73,10 +92,20 @@ attn_status_t rope_apply_style(const void* x, void* y, attn_dtype_t dtype, int B
                      (st_bits >> 1) & 1);
 }
 
+size_t attn_prefill_workspace_size(int B, int Hq, int Hkv, int S, int D, attn_dtype_t dtype,
+                                   int rope) {
+  int mode = 0, il = 0;
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || !valid_dtype(dtype)) return 0;
+  if (D != 64 && D != 128 && D != 256) return 0;
+  if (!split_rope_arg(rope, 2, &mode, &il)) return 0;
+  return prefill_ws_bytes(B, Hq, Hkv, S, D, dtype, mode, il);
+}
+
 attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                            attn_dtype_t dtype, float q_scale, float k_scale, float v_scale,
                            int B, int Hq, int Hkv, int S, int D, int causal, float softmax_scale,
-                           int rope, float rope_theta, int pos0, attn_stream_t stream) {
+                           int rope, float rope_theta, int pos0, void* workspace,
+                           size_t workspace_bytes, attn_stream_t stream) {
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
@@ -96,6 +125,9 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   // is the half-split form); so does every rotation at D = 256 (bf16 only, one Q tile per item)
   if (il && (rope == 2 || dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
   if (D == 256 && (rope == 2 || dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  const size_t ws_need = prefill_ws_bytes(B, Hq, Hkv, S, D, dtype, rope, il);
+  if (ws_need > 0 && (!workspace || workspace_bytes < ws_need || !aligned16(workspace)))
+    return ATTN_ERR_WORKSPACE;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
   const float2* tab = nullptr;
@@ -105,20 +137,18 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
     if (!tab) return st;
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  if (rope == 1 && dtype == ATTN_BF16 && (S >= kRopePassMinS || il || D == 256)) {
-    // Q and K rotated once each into the library's scratch, then attention without RoPE
-    const size_t qb = rope_scratch_q_bytes(B, Hq, S, D);
-    uint8_t* sc = static_cast<uint8_t*>(
-        rope_scratch(qb + static_cast<size_t>(B) * Hkv * S * D * 2, &st));
-    if (!sc) return st;
+  if (ws_need > 0) {
+    // Q and K rotated once each into the caller's workspace, then attention without RoPE
+    const size_t qb = prefill_ws_q_bytes(B, Hq, S, D);
+    uint8_t* sc = static_cast<uint8_t*>(workspace);
     st = launch_rope(q, sc, dtype, B, Hq, S, D, pos0, tab, il, as_stream(stream));
     if (st != ATTN_OK) return st;
     st = launch_rope(k, sc + qb, dtype, B, Hkv, S, D, pos0, tab, il, as_stream(stream));
     if (st != ATTN_OK) return st;
-    return launch_prefill(sc, sc + qb, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv,
+    return timed_prefill(sc, sc + qb, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv,
                           S, S, S, D, causal, scale, nullptr, 0, pos0, as_stream(stream));
   }
-  return launch_prefill(q, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, S, S, S,
+  return timed_prefill(q, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, S, S, S,
                         D, causal, scale, tab, rope ? 1 : 0, pos0, as_stream(stream));
 }
 
@@ -155,22 +185,20 @@ attn_status_t attn_prefill_backward(const void* q, const void* k, const void* v,
                                  scale, workspace, as_stream(stream));
 }
 
-attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || (D != 64 && D != 128 && D != 256))
-    return ATTN_ERR_INVALID_ARG;
-  attn_status_t st = check_device();
-  if (st != ATTN_OK) return st;
-  // Q and K space at every size (the interleaved pairing uses the passes below 1024 rows too)
-  const size_t bytes = rope_scratch_q_bytes(B, Hq, S, D) + static_cast<size_t>(B) * Hkv * S * D * 2;
-  return rope_scratch(bytes, &st) ? ATTN_OK : st;
+size_t attn_prefill_chunk_workspace_size(int B, int Hq, int Sq, int D, attn_dtype_t dtype,
+                                         int rope) {
+  int mode = 0, il = 0;
+  if (B < 1 || Hq < 1 || Sq < 1 || !valid_dtype(dtype)) return 0;
+  if (D != 64 && D != 128 && D != 256) return 0;
+  if (!split_rope_arg(rope, 1, &mode, &il)) return 0;
+  return chunk_ws_bytes(B, Hq, Sq, D, dtype, mode);
 }
-
 
 attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, void* o, float* lse,
                                  attn_dtype_t dtype, float q_scale, float k_scale, float v_scale,
                                  int B, int Hq, int Hkv, int Sq, int Skv, int kv_pitch, int D,
                                  float softmax_scale, int rope, float rope_theta, int pos0,
-                                 attn_stream_t stream) {
+                                 void* workspace, size_t workspace_bytes, attn_stream_t stream) {
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
@@ -189,6 +217,9 @@ attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, vo
   if (rope && dtype == ATTN_FP8_E5M2 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (D == 256 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   if (il && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  const size_t ws_need = chunk_ws_bytes(B, Hq, Sq, D, dtype, rope);
+  if (ws_need > 0 && (!workspace || workspace_bytes < ws_need || !aligned16(workspace)))
+    return ATTN_ERR_WORKSPACE;
   attn_status_t st = check_device();
   if (st != ATTN_OK) return st;
   const float2* tab = nullptr;
@@ -197,17 +228,17 @@ attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, vo
     if (!tab) return st;
   }
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  if (rope && dtype == ATTN_BF16) {
-    // the chunk's queries rotated once at their absolute positions, then attention without RoPE
-    void* sq = rope_scratch(rope_scratch_q_bytes(B, Hq, Sq, D), &st);
-    if (!sq) return st;
+  if (ws_need > 0) {
+    // the chunk's queries rotated once at their absolute positions into the caller's
+    // workspace, then attention without RoPE
+    void* sq = workspace;
     st = launch_rope(q, sq, dtype, B, Hq, Sq, D, pos0 + Skv - Sq, tab, il, as_stream(stream));
     if (st != ATTN_OK) return st;
-    return launch_prefill(sq, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, Sq,
+    return timed_prefill(sq, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, Sq,
                           Skv, kv_pitch, D, 1, scale, nullptr, 0, pos0, as_stream(stream));
   }
   // fp8: q rotated into bf16 inside the kernel; the staged keys are widened as stored
-  return launch_prefill(q, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, Sq, Skv,
+  return timed_prefill(q, k, v, o, lse, dtype, q_scale, k_scale, v_scale, B, Hq, Hkv, Sq, Skv,
                         kv_pitch, D, 1, scale, tab, 0, pos0, as_stream(stream));
 }
 
@@ -254,6 +285,13 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
                              tab, il, workspace, plan, as_stream(stream));
   return launch_decode(q, k_cache, v_cache, cache_len, Lmax, o, lse, B, Hq, Hkv, D, scale, tab,
                        il, workspace, plan, as_stream(stream));
+}
+
+attn_status_t attn_set_prefill_events(void* begin_event, void* end_event) {
+  if ((begin_event == nullptr) != (end_event == nullptr)) return ATTN_ERR_INVALID_ARG;
+  g_ev_begin.store(static_cast<cudaEvent_t>(begin_event));
+  g_ev_end.store(static_cast<cudaEvent_t>(end_event));
+  return ATTN_OK;
 }
 
 attn_status_t attn_set_decode_splits(int nsplit) {

@@ -72,8 +72,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and sets the timeout
-// bit of the status word) when the wait ran out; the caller then unwinds without waiting again.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
+// bit of the status word) when the wait ran out after `limit_ns`; the caller then unwinds
+// without waiting again.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                          unsigned long long limit_ns = kWaitTimeoutNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
@@ -81,7 +83,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(a, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       report_status(status, ATTN_ERR_TIMEOUT);
       return false;
     }

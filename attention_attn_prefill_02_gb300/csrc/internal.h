@@ -29,21 +29,28 @@ const float2* rope_table(int D, float theta, int npos, attn_status_t* err);
 // nullptr.  Never allocates.
 const float2* rope_table_find(int D, float theta, int npos);
 
-// Encode a 3-D tiled TMA descriptor for a dense row-major tensor of `elem_bytes`-byte elements
-// with logical sizes {inner, mid, outer} (innermost first), box {box_inner, box_mid, 1} and
-// 128-byte swizzling.  Returns false on failure.
-// Device buffer of at least `bytes` for the Q/K rotated once per prefill call (library-owned,
-// per device, grown on demand; never shrinks).
-void* rope_scratch(size_t bytes, attn_status_t* err);
-
 // Prompt length from which a bf16 RoPE prefill rotates Q and K once per call (rope_apply passes
-// into the scratch, then attention without RoPE) instead of inside the attention kernel, where
-// every query block re-rotates the K tiles it reads.
+// into the caller's workspace, then attention without RoPE) instead of inside the attention
+// kernel, where every query block re-rotates the K tiles it reads.
 constexpr int kRopePassMinS = 1024;
-inline size_t rope_scratch_q_bytes(int B, int Hq, int S, int D) {
+inline size_t prefill_ws_q_bytes(int B, int Hq, int S, int D) {
   return (static_cast<size_t>(B) * Hq * S * D * 2 + 255) & ~size_t(255);
 }
+// Workspace of attn_prefill (rope: the mode without the flag, il: the interleaved flag): the
+// rotated Q (256-byte rounded) then the rotated K, when RoPE runs as rotation passes.
+inline size_t prefill_ws_bytes(int B, int Hq, int Hkv, int S, int D, attn_dtype_t dt, int rope,
+                               int il) {
+  if (rope != 1 || dt != ATTN_BF16 || !(S >= kRopePassMinS || il || D == 256)) return 0;
+  return prefill_ws_q_bytes(B, Hq, S, D) + static_cast<size_t>(B) * Hkv * S * D * 2;
+}
+// Workspace of attn_prefill_chunk: the chunk's rotated queries (bf16 with RoPE).
+inline size_t chunk_ws_bytes(int B, int Hq, int Sq, int D, attn_dtype_t dt, int rope) {
+  return (rope && dt == ATTN_BF16) ? prefill_ws_q_bytes(B, Hq, Sq, D) : 0;
+}
 
+// Encode a 3-D tiled TMA descriptor for a dense row-major tensor of `elem_bytes`-byte elements
+// with logical sizes {inner, mid, outer} (innermost first), box {box_inner, box_mid, 1} and
+// `swizzle_bytes` swizzling.  Returns false on failure.
 // mid_pitch: rows between consecutive outer indices (0: mid, a dense tensor).
 bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
                   uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid,

@@ -161,33 +161,6 @@ EncodeFn encode_fn() {
 }
 }  // namespace
 
-// Scratch of the once-per-call Q/K rotation, one per device, grown when a larger call arrives.
-// Outgrown buffers stay alive (kernels still in flight may read them).
-std::mutex g_scratch_mu;
-std::map<int, std::pair<void*, size_t>> g_scratch;
-std::vector<void*> g_scratch_retired;
-
-void* rope_scratch(size_t bytes, attn_status_t* err) {
-  *err = ATTN_OK;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    *err = ATTN_ERR_NO_DEVICE;
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  auto& ent = g_scratch[dev];
-  if (ent.first && ent.second >= bytes) return ent.first;
-  void* ptr = nullptr;
-  if (cudaMalloc(&ptr, bytes) != cudaSuccess) {
-    cudaGetLastError();
-    *err = ATTN_ERR_CUDA;
-    return nullptr;
-  }
-  if (ent.first) g_scratch_retired.push_back(ent.first);
-  ent = {ptr, bytes};
-  return ptr;
-}
-
 bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner,
                   uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid,
                   int swizzle_bytes, uint64_t mid_pitch) {

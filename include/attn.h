@@ -23,9 +23,12 @@
  *     happens before anything is enqueued; on any error nothing is launched and outputs are
  *     untouched.  Kernels never trap: a device-side problem (a cache_len out of range, a wait
  *     that timed out) sets a device status word read by attn_get_device_status().
- *   - The cos/sin table used by RoPE is built on the host in float64, stored as float32 and
- *     cached per device and (D, theta).  The first call that needs a table (or more positions
- *     than the cached one holds) allocates it with cudaMalloc and copies it synchronously; call
+ *   - Scratch memory comes from the caller: calls that need it take a workspace pointer and
+ *     size (each with a *_workspace_size() query).  The library's own device memory is the
+ *     cos/sin table used by RoPE, the 4-byte status word and attn_decode_noalloc's fixed array.
+ *     The table is built on the host in float64, stored as float32 and cached per device and
+ *     (D, theta).  The first call that needs a table (or more positions than the cached one
+ *     holds) allocates it with cudaMalloc and copies it synchronously; call
  *     attn_rope_table_reserve() first to keep that out of timed regions and graph captures.
  *     Every other path allocates nothing.
  */
@@ -115,6 +118,16 @@ ATTN_API attn_status_t rope_apply_style(const void* x, void* y, attn_dtype_t dty
                                attn_stream_t stream);
 
 /*
+ * attn_prefill_workspace_size — bytes of device workspace attn_prefill needs for these
+ * arguments (dtype and rope as passed to attn_prefill).  Nonzero only where RoPE runs as
+ * rotation passes before the attention kernel: rope = 1 with bf16 inputs and S >= 1024, with
+ * the interleaved flag, or at D = 256; then (B*Hq + B*Hkv)*S*D bf16 values (Q rounded up to
+ * 256 bytes, then K).  0 for invalid arguments.  Needs no device.
+ */
+ATTN_API size_t attn_prefill_workspace_size(int B, int Hq, int Hkv, int S, int D,
+                                            attn_dtype_t dtype, int rope);
+
+/*
  * attn_prefill — grouped-query attention over a whole prompt, one GPU.
  * Defines: softmax(scale * Q K^T + causal mask) V for Hq query heads sharing Hkv KV heads,
  * the causal GQA prefill of Lesson: shape adaptive attention negative 20260722 ("당시 조건")
@@ -128,27 +141,28 @@ ATTN_API attn_status_t rope_apply_style(const void* x, void* y, attn_dtype_t dty
  *   causal   0 or 1; causal hides key j from query i when j > i (S_q == S_kv).
  *   rope     0 = Q and K used as given.  1 and 2 rotate Q and K at positions pos0 + s:
  *            1 = the library's choice: bf16 prompts of S >= 1024 rotate Q and K once per call
- *                (rope_apply passes into library-owned scratch, see attn_prefill_reserve), then
- *                run attention without RoPE; shorter prompts and fp8 rotate both inside the
- *                kernel;
+ *                (rope_apply passes into the caller's workspace), then run attention without
+ *                RoPE; shorter prompts and fp8 rotate both inside the kernel;
  *            2 = both inside the kernel as they are loaded (K once per query block that reads
  *                it; the fully fused form, measured beside the other).
  *            | ATTN_ROPE_FLAG_INTERLEAVED: pairs (2i, 2i+1); bf16 with rope = 1 only (always
  *                the rope_apply passes); fp8 or rope = 2 with the flag is UNSUPPORTED.
+ *   workspace  device buffer of at least attn_prefill_workspace_size(B,Hq,Hkv,S,D,dtype,rope)
+ *            bytes, 16-byte aligned (may be NULL when that size is 0); contents need no
+ *            initialisation.  Calls that run at the same time (e.g. on two streams) need
+ *            workspaces of their own.
  *   D in {64, 128, 256} (256: bf16 only, rope 0 or 1 with the rotation passes); Hq % Hkv == 0;
  *   S >= 1.  fp8 e5m2 inputs: P is rounded to e4m3 for the PV
  *   product; with rope = 1 (D = 128 only) Q and K are rotated into bf16 tiles inside the
  *   kernel (QK^T then runs in bf16, PV stays fp8), because rotated values re-rounded to fp8
  *   would exceed the fp8 error budget.
- *   With rope = 1 the scratch ((Hq + Hkv)*B*S*D bf16, per device, grown on demand, never
- *   shrunk) is allocated on first use; overlapping calls on different streams share it and
- *   must be serialised.
- * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */
 ATTN_API attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                            attn_dtype_t dtype, float q_scale, float k_scale, float v_scale,
                            int B, int Hq, int Hkv, int S, int D, int causal, float softmax_scale,
-                           int rope, float rope_theta, int pos0, attn_stream_t stream);
+                           int rope, float rope_theta, int pos0, void* workspace,
+                           size_t workspace_bytes, attn_stream_t stream);
 
 /*
  * attn_prefill_backward — gradients of attn_prefill's attention: dQ, dK, dV.
@@ -176,14 +190,12 @@ ATTN_API attn_status_t attn_prefill_backward(const void* q, const void* k, const
                                     attn_stream_t stream);
 
 /*
- * attn_prefill_reserve — allocate ahead the per-device rotation scratch that attn_prefill
- * (rope = 1, either pairing) and attn_prefill_chunk (rope = 1, bf16) use at this size (S = the
- * query rows), e.g.
- * before a CUDA-graph capture, which cannot allocate.  Together with attn_rope_table_reserve it
- * leaves nothing to allocate in later calls up to that size.
- * Errors: INVALID_ARG (sizes, D not in {64, 128, 256}), CUDA, NO_DEVICE.
+ * attn_prefill_chunk_workspace_size — bytes of device workspace attn_prefill_chunk needs:
+ * B*Hq*Sq*D bf16 values (rounded up to 256 bytes) for bf16 with rope = 1 (the chunk's queries
+ * rotated once), else 0.  0 for invalid arguments.  Needs no device.
  */
-ATTN_API attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D);
+ATTN_API size_t attn_prefill_chunk_workspace_size(int B, int Hq, int Sq, int D,
+                                                  attn_dtype_t dtype, int rope);
 
 /*
  * attn_prefill_chunk — one chunk of a prompt against a static cache (chunked prefill).
@@ -198,19 +210,33 @@ ATTN_API attn_status_t attn_prefill_reserve(int B, int Hq, int Hkv, int S, int D
  *            as stored (a cache holds them already rotated); rows >= Skv are never read.
  *   o        [B,Hq,Sq,D] bfloat16.   lse  NULL or [B,Hq,Sq] float32 (natural log).
  *   rope     1: q rotated at positions pos0 + Skv - Sq + i (bf16: a rope_apply pass into the
- *            library's scratch, see attn_prefill_reserve; fp8: inside the kernel, into bf16
- *            tiles); 0: q as given.  1 | ATTN_ROPE_FLAG_INTERLEAVED: pairs (2i, 2i+1), bf16
- *            only (fp8: UNSUPPORTED).
+ *            caller's workspace; fp8: inside the kernel, into bf16 tiles); 0: q as given.
+ *            1 | ATTN_ROPE_FLAG_INTERLEAVED: pairs (2i, 2i+1), bf16 only (fp8: UNSUPPORTED).
+ *   workspace  device buffer of at least attn_prefill_chunk_workspace_size(B,Hq,Sq,D,dtype,
+ *            rope) bytes, 16-byte aligned (NULL allowed when that size is 0); no initialisation.
  *   1 <= Sq <= Skv <= kv_pitch; D in {64, 128, 256} (fp8: D <= 128; fp8 with rope = 1: D = 128); the other
  *   arguments as attn_prefill.
- * Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */
 ATTN_API attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, void* o,
                                           float* lse, attn_dtype_t dtype, float q_scale,
                                           float k_scale, float v_scale, int B, int Hq, int Hkv,
                                           int Sq, int Skv, int kv_pitch, int D,
                                           float softmax_scale, int rope, float rope_theta,
-                                          int pos0, attn_stream_t stream);
+                                          int pos0, void* workspace, size_t workspace_bytes,
+                                          attn_stream_t stream);
+
+/*
+ * attn_set_prefill_events — a measurement hook: while set, every attn_prefill and
+ * attn_prefill_chunk call records `begin_event` on its stream just before the attention kernel
+ * is enqueued and `end_event` just after it (the RoPE rotation passes that may precede it stay
+ * outside the pair), so cudaEventElapsedTime gives that kernel's own time inside a longer
+ * sequence of work.  The two are cudaEvent_t handles created by the caller (with timing
+ * enabled); NULL, NULL clears the hook.  Process-wide: set it only while no other thread runs
+ * a prefill.  Not for use during stream capture.  No operation of the pages.
+ * Errors: INVALID_ARG (exactly one of the two NULL).
+ */
+ATTN_API attn_status_t attn_set_prefill_events(void* begin_event, void* end_event);
 
 /*
  * attn_decode_workspace_size — bytes of device workspace attn_decode needs for these sizes
@@ -250,7 +276,8 @@ ATTN_API attn_status_t attn_decode(const void* q, const void* k_cache, const voi
  * process whose device memory is entirely owned by another allocator, or a latency-bound
  * serving loop that cannot afford an allocation's cost or implicit synchronisation.  It takes
  * the same arguments as attn_decode minus the workspace, computes the same result, and calls
- * no cudaMalloc, cudaFree or other allocating routine.  The pages have no counterpart; this is
+ * no cudaMalloc, cudaFree or other allocating routine.  Caches must be bfloat16 (dtype
+ * ATTN_BF16, D in {64, 128, 256}); an fp8 e5m2 cache returns ATTN_ERR_UNSUPPORTED.  The pages have no counterpart; this is
  * an interface convenience around the same kernels.
  *   Scratch: the split partials live in one file-scope device array of 2 MiB (2097152 bytes)
  *   that every GPU loading this library holds until the process exits.  A call whose
@@ -361,6 +388,19 @@ ATTN_API attn_status_t attn_rope_table_reserve(int D, float theta, int max_pos);
  * and clear it.  The return value reports failures of this call itself.
  */
 ATTN_API attn_status_t attn_get_device_status(attn_stream_t stream, int* status_out);
+
+/*
+ * attn_selftest_wait_timeout — a self-test of the kernels' bounded waits: one warp waits on a
+ * shared-memory mbarrier that nothing ever arrives at, through the same bounded-wait routine
+ * every attention kernel uses, with a limit of `timeout_us` microseconds instead of the
+ * kernels' 2 s.  The wait gives up, the kernel sets ATTN_ERR_TIMEOUT in the device status word
+ * (attn_get_device_status then reports it once) and returns; the CUDA context stays usable.
+ * No operation of the pages; it lets a caller or a test check the failure path without
+ * faulting or hanging the GPU.
+ *   timeout_us  1 .. 2000000.
+ * Errors: INVALID_ARG, NO_DEVICE, CUDA.
+ */
+ATTN_API attn_status_t attn_selftest_wait_timeout(unsigned int timeout_us, attn_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,7 @@ int main(void) {
   void* a = (void*)(uintptr_t)0x7F0000000000ull;
   void* o = (void*)(uintptr_t)0x7F0000100000ull;
   void* mis = (void*)(uintptr_t)0x7F0000000008ull;
-  if (attn_version() < 100) {
+  if (attn_version() < 200) {
     printf("FAIL attn_version\n");
     ++failures;
   }
@@ -32,15 +32,15 @@ int main(void) {
          ATTN_ERR_INVALID_ARG);
   expect("prefill misaligned",
          attn_prefill(a, a, a, mis, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 1, 4, 1, 128, 64, 1, 0.f, 1,
-                      1e4f, 0, NULL),
+                      1e4f, 0, NULL, 0, NULL),
          ATTN_ERR_INVALID_ARG);
   expect("prefill head dim",
          attn_prefill(a, a, a, o, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 1, 4, 1, 128, 96, 1, 0.f, 1,
-                      1e4f, 0, NULL),
+                      1e4f, 0, NULL, 0, NULL),
          ATTN_ERR_UNSUPPORTED);
   expect("chunk lengths",
          attn_prefill_chunk(a, a, a, o, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 1, 4, 1, 64, 32, 64, 64,
-                            0.f, 1, 1e4f, 0, NULL),
+                            0.f, 1, 1e4f, 0, NULL, 0, NULL),
          ATTN_ERR_INVALID_ARG);
   expect("decode groups",
          attn_decode(a, a, a, (const int32_t*)o, 2048, o, NULL, ATTN_BF16, 1, 30, 8, 128, 0.f, 1,
@@ -59,11 +59,11 @@ int main(void) {
          ATTN_ERR_INVALID_ARG);
   expect("interleaved flag without a mode",
          attn_prefill(a, a, a, o, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 1, 4, 1, 128, 64, 1, 0.f,
-                      ATTN_ROPE_FLAG_INTERLEAVED, 1e4f, 0, NULL),
+                      ATTN_ROPE_FLAG_INTERLEAVED, 1e4f, 0, NULL, 0, NULL),
          ATTN_ERR_INVALID_ARG);
   expect("interleaved fused form",
          attn_prefill(a, a, a, o, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 1, 4, 1, 128, 64, 1, 0.f,
-                      2 | ATTN_ROPE_FLAG_INTERLEAVED, 1e4f, 0, NULL),
+                      2 | ATTN_ROPE_FLAG_INTERLEAVED, 1e4f, 0, NULL, 0, NULL),
          ATTN_ERR_UNSUPPORTED);
   expect("backward fp8",
          attn_prefill_backward(a, a, a, a, (const float*)o, a, o, o, o, ATTN_FP8_E5M2, 1, 4, 1,
@@ -78,7 +78,19 @@ int main(void) {
     ++failures;
   }
   expect("split hook range", attn_set_decode_splits(-1), ATTN_ERR_INVALID_ARG);
-  expect("reserve sizes", attn_prefill_reserve(0, 1, 1, 128, 128), ATTN_ERR_INVALID_ARG);
+  expect("prefill rotation workspace missing",
+         attn_prefill(a, a, a, o, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 4, 32, 8, 16384, 128, 1, 0.f, 1,
+                      1e4f, 0, NULL, 0, NULL),
+         ATTN_ERR_WORKSPACE);
+  if (attn_prefill_workspace_size(4, 32, 8, 16384, 128, ATTN_BF16, 1) !=
+      (size_t)(4 + 1) * 32 * 16384 * 128 * 2) {
+    printf("FAIL prefill workspace size\n");
+    ++failures;
+  }
+  if (attn_prefill_chunk_workspace_size(1, 4, 32, 64, ATTN_FP8_E5M2, 1) != 0) {
+    printf("FAIL chunk workspace size (fp8 rotates in the kernel)\n");
+    ++failures;
+  }
   if (attn_decode_workspace_size(1, 30, 8, 128, 2048) != 0) {
     printf("FAIL workspace size of an invalid shape\n");
     ++failures;

@@ -133,7 +133,8 @@ def test_prefill_backward_validation(L):
 
 def _prefill(L, **kw):
     args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE2, lse=None, dt=0, qs=1.0, ks=1.0, vs=1.0, B=1,
-                Hq=4, Hkv=1, S=128, D=64, causal=1, scale=0.0, rope=1, theta=1e4, pos0=0)
+                Hq=4, Hkv=1, S=128, D=64, causal=1, scale=0.0, rope=1, theta=1e4, pos0=0,
+                ws=FAKE, wsb=1 << 30)
     args.update(kw)
     return L.attn_prefill(*args.values(), _stream())
 
@@ -146,8 +147,6 @@ def test_prefill_validation(L):
     assert _prefill(L, causal=2) == INVALID
     assert _prefill(L, rope=1, theta=-1.0) == INVALID
     assert _prefill(L, rope=3) == INVALID
-    assert L.attn_prefill_reserve(1, 1, 1, 0, 128) == INVALID
-    assert L.attn_prefill_reserve(1, 1, 1, 4096, 96) == INVALID
     assert _prefill(L, qs=0.0) == INVALID
     assert _prefill(L, lse=ctypes.c_void_p(0x7F0000000002)) == INVALID
     assert _prefill(L, D=96) == UNSUPPORTED
@@ -160,7 +159,7 @@ def test_prefill_validation(L):
 def _chunk(L, **kw):
     args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE2, lse=None, dt=0, qs=1.0, ks=1.0, vs=1.0, B=1,
                 Hq=4, Hkv=1, Sq=32, Skv=300, pitch=320, D=128, scale=0.0, rope=1, theta=1e4,
-                pos0=0)
+                pos0=0, ws=FAKE, wsb=1 << 30)
     args.update(kw)
     return L.attn_prefill_chunk(*args.values(), _stream())
 
@@ -173,6 +172,37 @@ def test_prefill_chunk_validation(L):
     assert _chunk(L, v=MIS) == INVALID
     assert _chunk(L, D=96) == UNSUPPORTED
     assert _chunk(L, dt=1, D=64) == UNSUPPORTED       # fp8 with q RoPE: D = 128 only
+    assert _chunk(L, ws=None, wsb=0) == WORKSPACE     # bf16 with RoPE rotates q into it
+    assert _chunk(L, wsb=32 * 4 * 128 * 2 - 1) == WORKSPACE
+    assert _chunk(L, ws=MIS) == WORKSPACE
+
+
+def test_prefill_workspace_sizes(L):
+    """The caller's workspace holds the rotated Q (rounded up to 256 bytes) then the rotated K
+    exactly when RoPE runs as rotation passes: bf16, rope = 1 and S >= 1024, or the interleaved
+    pairing, or D = 256.  Everything else needs none."""
+    bf16, fp8, il = 0, 1, 16
+    q_bytes = 4 * 32 * 16384 * 128 * 2
+    assert L.attn_prefill_workspace_size(4, 32, 8, 16384, 128, bf16, 1) == \
+        q_bytes + 4 * 8 * 16384 * 128 * 2
+    assert L.attn_prefill_workspace_size(4, 32, 8, 16384, 128, bf16, 2) == 0   # in the kernel
+    assert L.attn_prefill_workspace_size(4, 32, 8, 16384, 128, bf16, 0) == 0
+    assert L.attn_prefill_workspace_size(4, 32, 8, 16384, 128, fp8, 1) == 0    # fp8: in-kernel
+    assert L.attn_prefill_workspace_size(1, 4, 1, 1023, 64, bf16, 1) == 0      # short prompt
+    assert L.attn_prefill_workspace_size(1, 3, 1, 5, 64, bf16, 1 | il) == \
+        ((3 * 5 * 64 * 2 + 255) // 256) * 256 + 5 * 64 * 2
+    assert L.attn_prefill_workspace_size(1, 2, 1, 8, 256, bf16, 1) == 2 * 8 * 256 * 2 + 8 * 256 * 2
+    assert L.attn_prefill_workspace_size(1, 2, 1, 8, 96, bf16, 1) == 0         # invalid -> 0
+    assert L.attn_prefill_workspace_size(1, 2, 1, 8, 64, bf16, 3) == 0
+    assert L.attn_prefill_chunk_workspace_size(2, 8, 33, 128, bf16, 1) == \
+        ((2 * 8 * 33 * 128 * 2 + 255) // 256) * 256
+    assert L.attn_prefill_chunk_workspace_size(2, 8, 33, 128, fp8, 1) == 0
+    assert L.attn_prefill_chunk_workspace_size(2, 8, 33, 128, bf16, 0) == 0
+    # a call that needs it refuses a missing, short or misaligned workspace before any launch
+    assert _prefill(L, S=1024, ws=None, wsb=0) == WORKSPACE
+    assert _prefill(L, S=1024, wsb=L.attn_prefill_workspace_size(1, 4, 1, 1024, 64, bf16, 1) - 1) \
+        == WORKSPACE
+    assert _prefill(L, S=1024, ws=MIS) == WORKSPACE
 
 
 def _decode(L, **kw):
@@ -272,7 +302,8 @@ def test_workspace_sizes_are_consistent(L):
 def test_valid_calls_report_no_device_without_gpu(L):
     assert _prefill(L) == NO_DEVICE
     assert _prefill(L, rope=2) == NO_DEVICE
-    assert L.attn_prefill_reserve(4, 32, 8, 16384, 128) == NO_DEVICE
+    assert _prefill(L, S=16384) == NO_DEVICE
+    assert _prefill(L, ws=None, wsb=0) == NO_DEVICE   # S = 128: the kernel rotates, no workspace
     assert _chunk(L) == NO_DEVICE
     assert _decode(L) == NO_DEVICE
     assert _append(L) == NO_DEVICE
@@ -292,3 +323,15 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cpp", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_selftest_and_event_hook_validation(L):
+    """The bounded-wait self-test takes a limit of 1 us .. 2 s; the measurement hook takes both
+    events or neither.  Both answer on the host before touching a device."""
+    assert L.attn_selftest_wait_timeout(0, _stream()) == INVALID
+    assert L.attn_selftest_wait_timeout(2000001, _stream()) == INVALID
+    assert L.attn_set_prefill_events(FAKE, None) == INVALID
+    assert L.attn_set_prefill_events(None, FAKE) == INVALID
+    assert L.attn_set_prefill_events(None, None) == OK
+    if not torch.cuda.is_available():
+        assert L.attn_selftest_wait_timeout(10000, _stream()) == NO_DEVICE

@@ -127,3 +127,17 @@ def test_latent_decode_b128_full_config():
     d = np.abs(oracle.as_f64(o[pick].cpu()) - ro)
     assert d.max() <= BF16_MAX and d.mean() <= BF16_MEAN, (d.max(), d.mean())
     assert np.abs(oracle.as_f64(lse[pick].cpu()) - rl).max() <= 5e-3
+
+
+def test_causal_prefill_d256_s4096_sampled():
+    """Causal GQA at head dim 256, Z=4 Hq=32 Hkv=8 S=4096 bf16 with RoPE (the D=256 shape the
+    bench times): sampled rows against the oracle."""
+    B, Hq, Hkv, S, D = 4, 32, 8, 4096, 256
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=23)
+    binding.attn_rope_table_reserve(D, 10000.0, S)
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, rope=1,
+                                  rope_theta=10000.0, want_lse=True)
+    assert binding.attn_get_device_status() == 0
+    rows = sample_rows(B, Hq, S, n_random=16, seed=5)
+    ro, rl = oracle_rows(q, k, v, rows, causal=True, rope=True)
+    check_rows(o, lse, rows, ro, rl, BF16_MAX, BF16_MEAN)

@@ -719,6 +719,8 @@ def test_backward_through_rope(style):
     (2, 8, 2, 300, True, True),      # ragged tail, RoPE through the rotation passes, GQA
     (1, 2, 2, 200, False, False),
     (1, 4, 4, 513, True, True),
+    (2, 32, 8, 1024, True, False),   # 256 items, more than the SMs: CTAs run several items, so
+                                     # the single-stage rings and Q/O phases carry over
 ])
 def test_prefill_d256(B, Hq, Hkv, S, causal, rope):
     q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, 256, "bf16", seed=S + 256)

@@ -4,13 +4,14 @@ latency-bound serving loops).  It keeps its split partials in the library's fixe
 array instead of a caller workspace.
 
 Checked through the C ABI against attn_decode (same inputs, the tolerance the other parity tests
-use) on two calls in a row with different inputs, so the second call runs over the first call's
-leftover scratch.  The file is named to be collected last.
+use) and against the float64 oracle, on two calls in a row with different inputs, so the second
+call runs over the first call's leftover scratch.  The file is named to be collected last.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from attention_attn_prefill_02_gb300 import binding, synthetic
 
 pytestmark = pytest.mark.gpu
@@ -28,6 +29,7 @@ def _close(a, b):
 @pytest.mark.parametrize("B,Hq,Hkv,D,Lmax,lens", [
     (1, 32, 8, 128, 2048, [2048]),          # decode config at batch 1: 32 splits of the cache
     (3, 32, 8, 128, 2048, [2048, 1, 700]),  # ragged lengths, still split
+    (2, 16, 4, 256, 2048, [2048, 300]),     # D = 256: one CTA per SM, larger partials
 ])
 def test_noalloc_matches_workspace_decode_twice(B, Hq, Hkv, D, Lmax, lens):
     assert 0 < binding.attn_decode_workspace_size(B, Hq, Hkv, D, Lmax) <= SCRATCH
@@ -41,11 +43,22 @@ def test_noalloc_matches_workspace_decode_twice(B, Hq, Hkv, D, Lmax, lens):
         assert binding.attn_get_device_status() == 0
         _close(out, ref)
         np.testing.assert_allclose(out_lse.cpu().numpy(), ref_lse.cpu().numpy(), atol=5e-3)
+        # and directly against the oracle, at the same bounds
+        ro, rl = oracle.decode(*(oracle.as_f64(t.cpu()) for t in (q, kc, vc)), cl.cpu().numpy(),
+                               rope=True, theta=10000.0)
+        d = np.abs(oracle.as_f64(out.cpu()) - ro)
+        assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS, (d.max(), d.mean())
+        assert np.abs(out_lse.cpu().numpy() - rl).max() <= 5e-3
 
 
 def test_noalloc_rejects_what_it_cannot_do_without_allocating():
     q, kc, vc, cl = synthetic.decode_inputs(1, 16, 1, 64, 128, 64, seed=3)
     q, kc, vc, cl = q.cuda(), kc.cuda(), vc.cuda(), cl.cuda()
+    # fp8 e5m2 caches are not built for this entry point: UNSUPPORTED, nothing launched
+    with pytest.raises(binding.AttnError) as e:
+        binding.attn_decode_noalloc(q, kc.to(torch.float8_e5m2), vc.to(torch.float8_e5m2), cl,
+                                    rope=False)
+    assert e.value.status == 2
     # a RoPE table that was never built would need an allocation: refused before any launch
     with pytest.raises(binding.AttnError) as e:
         binding.attn_decode_noalloc(q, kc, vc, cl, rope=True, rope_theta=12345.5)
