@@ -99,6 +99,8 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static_assert(kKStages <= 8 && kVStages <= 8, "barrier arrays hold 8 stages");
+  // O of the second Q tile exists only with two tiles per item (D = 256 has one)
+  static_assert(kNT == 1 || kColO1 + D <= kTmemCols, "TMEM columns of O1 past the allocation");
   static_assert(!STAGED || D == 128, "fp8 with fused RoPE is built for D = 128");
 };
 
@@ -349,46 +351,50 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop in warp-uniform control flow and one elected lane
+    // issues each MMA and commit: the descriptors then stay warp-uniform, and MMAs go out at
+    // the tensor pipe's rate (a loop run by one lane alone issued them measurably slower).
+    {
       // bf16 (format 1) x bf16, or e5m2 (1) x e5m2 for S and e4m3 (0) P x e5m2 V for PV
       const uint32_t idesc_s = make_idesc(1, 1, false, false, BN, BM);
       const uint32_t idesc_pv = make_idesc(FP8 ? 0u : 1u, 1, false, true, D, BM);  // V MN-major
-      const uint32_t q_base = smem_u32(smem + C::kQOff);
-      const uint32_t k_base = smem_u32(smem + C::kKVOff);
-      const uint32_t v_base = smem_u32(smem + C::kVOff);
+      // descriptors of the first K step of Q tile 0 / ring slot 0; the address field (bits
+      // 0-13, address / 16) of later tiles, slots and K steps is that plus a constant, with no
+      // carry out of the field (shared memory ends below 256 KB)
+      const uint64_t q_desc0 = smem_desc(smem_u32(smem + C::kQOff), 16, C::kSBO, C::kSwzCode);
+      const uint64_t k_desc0 = smem_desc(smem_u32(smem + C::kKVOff), 16, C::kSBO, C::kSwzCode);
+      const uint64_t v_desc0 =
+          smem_desc(smem_u32(smem + C::kVOff), C::kVBoxBytes, C::kVSBO, C::kVSwzCode);
       uint32_t ph_qf[2] = {0, 0}, ph_pf[2] = {0, 0}, ph_oe[2] = {0, 0};
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0;
       bool ok = true;
       auto issue_s = [&](int t, int slot) {
-        const uint32_t qa = q_base + t * C::kQTileBytes;
-        const uint32_t ka = k_base + slot * C::kKVTileBytes;
+        const uint64_t ad = q_desc0 + static_cast<uint64_t>((t * C::kQTileBytes) >> 4);
+        const uint64_t bd = k_desc0 + static_cast<uint64_t>((slot * C::kKVTileBytes) >> 4);
+        const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk) {
           constexpr int kPerBox = C::kSwz / 32;
-          const uint32_t off = (kk / kPerBox) * C::kBoxBytes + (kk % kPerBox) * 32;
-          const uint64_t ad = smem_desc(qa + off, 16, C::kSBO, C::kSwzCode);
-          const uint64_t bd = smem_desc(ka + off, 16, C::kSBO, C::kSwzCode);
+          const uint64_t off = ((kk / kPerBox) * C::kBoxBytes + (kk % kPerBox) * 32) >> 4;
           if constexpr (C::kQKE == 1)
-            umma_ss_f8(tmem + (t ? C::kColS1 : C::kColS0), ad, bd, idesc_s, kk > 0);
+            umma_ss_f8_e(d, ad + off, bd + off, idesc_s, kk > 0);
           else
-            umma_ss(tmem + (t ? C::kColS1 : C::kColS0), ad, bd, idesc_s, kk > 0);
+            umma_ss_e(d, ad + off, bd + off, idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t va = v_base + slot * C::kVTileBytes;
+        const uint64_t bd = v_desc0 + static_cast<uint64_t>((slot * C::kVTileBytes) >> 4);
         const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0) + kPCol;
+        const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
 #pragma unroll
         for (int kk = 0; kk < C::kPVSteps; ++kk) {
           // P: 8 TMEM columns per step (16 bf16 or 32 fp8 keys); V rows of kSwz bytes per key
-          const uint64_t bd =
-              smem_desc(va + kk * C::kPVKeys * C::kVSwz, C::kVBoxBytes, C::kVSBO, C::kVSwzCode);
+          const uint64_t off = (kk * C::kPVKeys * C::kVSwz) >> 4;
           if constexpr (FP8)
-            umma_ts_f8(tmem + (t ? C::kColO1 : C::kColO0), pcol + kk * 8, bd, idesc_pv,
-                       (acc || kk > 0) ? 1u : 0u);
+            umma_ts_f8_e(d, pcol + kk * 8, bd + off, idesc_pv, (acc || kk > 0) ? 1u : 0u);
           else
-            umma_ts(tmem + (t ? C::kColO1 : C::kColO0), pcol + kk * 8, bd, idesc_pv,
-                    (acc || kk > 0) ? 1u : 0u);
+            umma_ts_e(d, pcol + kk * 8, bd + off, idesc_pv, (acc || kk > 0) ? 1u : 0u);
         }
       };
       for (int r = 0; r < rounds && ok; ++r) {
@@ -403,13 +409,14 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           if (n[t] == 0 || !ok) continue;
-          ok = mbar_wait(ROPE ? &bars->q_ready[t] : &bars->q_full[t], ph_qf[t], p.status);
+          ok = mbar_wait_warp(ROPE ? &bars->q_ready[t] : &bars->q_full[t], ph_qf[t], p.status);
           ph_qf[t] ^= 1;
         }
         if (!ok) break;
         // j = 0: S_t = Q_t K_0^T for both tiles
         const int kslot = ks;
-        if (!(ok = mbar_wait(ROPE ? &bars->k_ready[kslot] : &bars->k_full[kslot], kph, p.status)))
+        if (!(ok = mbar_wait_warp(ROPE ? &bars->k_ready[kslot] : &bars->k_full[kslot], kph,
+                                  p.status)))
           break;
         if (++ks == C::kKStages) { ks = 0; kph ^= 1; }
         tc_fence_after();
@@ -417,19 +424,19 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
         for (int t = 0; t < NT; ++t) {
           if (n[t] == 0) continue;
           issue_s(t, kslot);
-          umma_commit(&bars->s_full[t]);
-          if (n[t] == 1) umma_commit(&bars->q_empty[t]);
+          umma_commit_e(&bars->s_full[t]);
+          if (n[t] == 1) umma_commit_e(&bars->q_empty[t]);
         }
-        umma_commit(&bars->k_empty[kslot]);
+        umma_commit_e(&bars->k_empty[kslot]);
         for (int j = 1; j <= nkv && ok; ++j) {
           const int vslot = vs;
-          if (!(ok = mbar_wait(&bars->v_full[vslot], vph, p.status))) break;
+          if (!(ok = mbar_wait_warp(&bars->v_full[vslot], vph, p.status))) break;
           if (++vs == C::kVStages) { vs = 0; vph ^= 1; }
           int kslot2 = -1;
           if (j < nkv) {
             kslot2 = ks;
-            if (!(ok = mbar_wait(ROPE ? &bars->k_ready[kslot2] : &bars->k_full[kslot2], kph,
-                                 p.status)))
+            if (!(ok = mbar_wait_warp(ROPE ? &bars->k_ready[kslot2] : &bars->k_full[kslot2], kph,
+                                      p.status)))
               break;
             if (++ks == C::kKStages) { ks = 0; kph ^= 1; }
           }
@@ -437,25 +444,25 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
           for (int t = 0; t < NT; ++t) {
             if (!ok) continue;
             if (j - 1 < n[t]) {
-              ok = mbar_wait(&bars->p_full[t], ph_pf[t], p.status);
+              ok = mbar_wait_warp(&bars->p_full[t], ph_pf[t], p.status);
               ph_pf[t] ^= 1;
               if (ok && j == 1) {
-                ok = mbar_wait(&bars->o_empty[t], ph_oe[t] ^ 1, p.status);
+                ok = mbar_wait_warp(&bars->o_empty[t], ph_oe[t] ^ 1, p.status);
                 ph_oe[t] ^= 1;
               }
               if (!ok) continue;
               tc_fence_after();
               issue_pv(t, vslot, j > 1);
-              if (j - 1 == n[t] - 1) umma_commit(&bars->o_full[t]);
+              if (j - 1 == n[t] - 1) umma_commit_e(&bars->o_full[t]);
             }
             if (j < n[t]) {
               issue_s(t, kslot2);
-              umma_commit(&bars->s_full[t]);
-              if (j == n[t] - 1) umma_commit(&bars->q_empty[t]);
+              umma_commit_e(&bars->s_full[t]);
+              if (j == n[t] - 1) umma_commit_e(&bars->q_empty[t]);
             }
           }
-          umma_commit(&bars->v_empty[vslot]);
-          if (kslot2 >= 0) umma_commit(&bars->k_empty[kslot2]);
+          umma_commit_e(&bars->v_empty[vslot]);
+          if (kslot2 >= 0) umma_commit_e(&bars->k_empty[kslot2]);
         }
       }
     }
