@@ -69,6 +69,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_decode.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp, sz, vp]
     L.attn_decode_noalloc.restype = i
     L.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp]
+    L.attn_set_prefill_tiles.restype = i
+    L.attn_set_prefill_tiles.argtypes = [i]
     L.attn_set_prefill_events.restype = i
     L.attn_set_prefill_events.argtypes = [vp, vp]
     L.attn_set_decode_splits.restype = i
@@ -281,6 +283,11 @@ def attn_decode_noalloc(q, k_cache, v_cache, cache_len, o=None, lse=None, want_l
                                      D, float(softmax_scale), _rope_mode(bool(rope), rope_style),
                                      float(rope_theta), _stream(stream)), "attn_decode_noalloc")
     return (o, lse) if (want_lse or lse is not None) else o
+
+
+def attn_set_prefill_tiles(q_tiles):
+    """1 or 2 Q tiles per prefill work item for later calls at D <= 128; 0: the default (2)."""
+    _check(lib().attn_set_prefill_tiles(int(q_tiles)), "attn_set_prefill_tiles")
 
 
 def attn_set_prefill_events(begin=None, end=None):

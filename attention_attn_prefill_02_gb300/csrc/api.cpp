@@ -294,6 +294,12 @@ attn_status_t attn_set_prefill_events(void* begin_event, void* end_event) {
   return ATTN_OK;
 }
 
+attn_status_t attn_set_prefill_tiles(int q_tiles) {
+  if (q_tiles < 0 || q_tiles > 2) return ATTN_ERR_INVALID_ARG;
+  force_prefill_tiles(q_tiles);
+  return ATTN_OK;
+}
+
 attn_status_t attn_set_decode_splits(int nsplit) {
   if (nsplit < 0 || nsplit > 1024) return ATTN_ERR_INVALID_ARG;
   force_decode_splits(nsplit);

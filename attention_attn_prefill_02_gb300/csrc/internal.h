@@ -132,6 +132,10 @@ attn_status_t launch_prefill_backward(const void* q, const void* k, const void* 
                                       void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
                                       float scale, void* ws, cudaStream_t st);
 
+// q_tiles 1 or 2: every later prefill at D <= 128 runs that many 128-row Q tiles per work item;
+// 0: the default (two).
+void force_prefill_tiles(int q_tiles);
+
 // S query rows at positions Skv - S .. Skv - 1 against Skv keys (rows kv_pitch apart per head);
 // rope_k: the fused RoPE rotates the keys too (else only the queries).
 attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -21,6 +21,7 @@
 // maximum exceeds it by more than 8 (log2 units); O and the row sum share that stale maximum, so
 // the final O / l is exact.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "common.cuh"
@@ -30,8 +31,10 @@ namespace {
 
 constexpr int BM = 128;  // query rows per Q tile (TMEM lanes)
 constexpr int BN = 128;  // keys per KV tile
-// Q tiles per work item: two (the ping-pong of the two softmax warpgroups) up to D = 128; one
-// at D = 256, whose O takes 256 TMEM columns (S 128 + O 256 fit the 512; two tiles would not).
+// Q tiles per work item by default: two (the ping-pong of the two softmax warpgroups) up to
+// D = 128; one at D = 256, whose O takes 256 TMEM columns (S 128 + O 256 fit the 512; two tiles
+// would not).  D <= 128 can also run one tile per item (128-row items: twice as many, each
+// without the ping-pong), the second tile configuration of the global-vs-per-shape comparison.
 __host__ __device__ constexpr int tiles_per_item(int D) { return D >= 256 ? 1 : 2; }
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -54,7 +57,7 @@ struct Swz {
   static constexpr int kSBO = 8 * kSwz;                                      // 8-row group
 };
 
-template <int D, int ESZ, bool STAGED>
+template <int D, int ESZ, bool STAGED, int NT_ = tiles_per_item(D)>
 struct Cfg {
   // Q / K tiles read by the QK^T MMA
   static constexpr int kQKE = STAGED ? 2 : ESZ;
@@ -88,7 +91,8 @@ struct Cfg {
       STAGED ? 2 : ESZ == 2 ? (D == 256 ? 1 : D == 128 ? 3 : 4) : (D == 128 ? 4 : 6);
   static constexpr int kVStages =
       STAGED ? 2 : ESZ == 2 ? (D == 256 ? 1 : D == 128 ? 2 : 3) : (D == 128 ? 4 : 6);
-  static constexpr int kNT = tiles_per_item(D);
+  static constexpr int kNT = NT_;
+  static_assert(NT_ == 1 || (NT_ == 2 && D <= 128), "two Q tiles per item need D <= 128");
   static constexpr int kQOff = 0;
   static constexpr int kQStOff = kQOff + kNT * kQTileBytes;
   static constexpr int kKVOff = kQStOff + 2 * kStTileBytes;
@@ -220,14 +224,14 @@ __device__ __forceinline__ void rope_rotate_row_fp8_to_bf16(const uint8_t* st, u
 
 // RM, the RoPE mode: 0 none; 1 Q and K rotated inside (the softmax warps rotate each Q tile as
 // it lands, the RoPE warps every K tile).
-template <int D, int RM, int ESZ>
+template <int D, int RM, int ESZ, int NTT>
 __global__ void __launch_bounds__(threads_for(RM), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
   constexpr bool FP8 = ESZ == 1;
   constexpr bool ROPE = RM == 1;  // Q and K rotated in shared memory
   constexpr bool STAGED = FP8 && ROPE;  // fp8 inputs, RoPE fused: rotate into bf16 Q/K tiles
-  using C = Cfg<D, ESZ, STAGED>;
+  using C = Cfg<D, ESZ, STAGED, NTT>;
   constexpr int NT = C::kNT;             // Q tiles per item
   constexpr int kRowsPerItem = NT * BM;  // query rows per item
   // First TMEM column of P inside S_t.  The RoPE variants (four more warps, so fewer registers
@@ -841,13 +845,13 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
   }
 }
 
-template <int D, int RM, int ESZ>
+template <int D, int RM, int ESZ, int NTT>
 attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o, float* lse,
                            float q_scale, float k_scale, float v_scale, int B, int Hq, int Hkv,
                            int S, int Skv, int kv_pitch, int causal, float scale,
                            const float2* table, int rope_k, int pos0, cudaStream_t st) {
   constexpr bool STAGED = ESZ == 1 && RM == 1;
-  using C = Cfg<D, ESZ, STAGED>;
+  using C = Cfg<D, ESZ, STAGED, NTT>;
   // Q / K boxes: as the MMA reads them, or (STAGED) the fp8 staging tiles; V in its own geometry
   constexpr int kQKBoxElems = STAGED ? D : C::kBoxElems;
   constexpr int kQKSwz = STAGED ? 128 : C::kSwz;
@@ -871,7 +875,7 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   p.off = Skv - S;
   p.rope_k = rope_k;
   p.causal = causal;
-  constexpr int kRowsPerItem = tiles_per_item(D) * BM;
+  constexpr int kRowsPerItem = NTT * BM;
   p.nM = (S + kRowsPerItem - 1) / kRowsPerItem;
   p.nKV = (Skv + BN - 1) / BN;
   p.n_items = p.nM * B * Hq;
@@ -885,14 +889,18 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   p.v_scale = v_scale;
   p.table = table;
   p.pos0 = pos0;
-  auto kern = prefill_kernel<D, RM, ESZ>;
+  auto kern = prefill_kernel<D, RM, ESZ, NTT>;
   if (!set_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes)) return ATTN_ERR_CUDA;
   const int grid = std::min(p.n_items, sm_count());
   kern<<<grid, threads_for(RM), C::kSmemBytes, st>>>(tq, tk, tv, p);
   return launch_status();
 }
 
+std::atomic<int> g_forced_tiles{0};  // Q tiles per item for D <= 128 (0: the default, two)
+
 }  // namespace
+
+void force_prefill_tiles(int q_tiles) { g_forced_tiles.store(q_tiles); }
 
 attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
                              attn_dtype_t dt, float q_scale, float k_scale, float v_scale, int B,
@@ -901,18 +909,28 @@ attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* 
                              cudaStream_t st) {
   const int esz = dt == ATTN_BF16 ? 2 : 1;
   const int rm = table == nullptr ? 0 : 1;
-#define ATTN_PREFILL_CASE(DD, RR, EE)                                                          \
-  if (D == DD && rm == RR && esz == EE)                                                        \
-    return launch_typed<DD, RR, EE>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S, \
-                                    Skv, kv_pitch, causal, scale, table, rope_k, pos0, st);
-  ATTN_PREFILL_CASE(128, 0, 2)
-  ATTN_PREFILL_CASE(256, 0, 2)
-  ATTN_PREFILL_CASE(128, 1, 2)
-  ATTN_PREFILL_CASE(64, 0, 2)
-  ATTN_PREFILL_CASE(64, 1, 2)
-  ATTN_PREFILL_CASE(128, 0, 1)
-  ATTN_PREFILL_CASE(64, 0, 1)
-  ATTN_PREFILL_CASE(128, 1, 1)
+  const int nt = D >= 256 ? 1 : (g_forced_tiles.load() == 1 ? 1 : 2);
+#define ATTN_PREFILL_CASE(DD, RR, EE, NN)                                                    \
+  if (D == DD && rm == RR && esz == EE && nt == NN)                                          \
+    return launch_typed<DD, RR, EE, NN>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq,   \
+                                        Hkv, S, Skv, kv_pitch, causal, scale, table, rope_k, \
+                                        pos0, st);
+  ATTN_PREFILL_CASE(128, 0, 2, 2)
+  ATTN_PREFILL_CASE(256, 0, 2, 1)
+  ATTN_PREFILL_CASE(128, 1, 2, 2)
+  ATTN_PREFILL_CASE(64, 0, 2, 2)
+  ATTN_PREFILL_CASE(64, 1, 2, 2)
+  ATTN_PREFILL_CASE(128, 0, 1, 2)
+  ATTN_PREFILL_CASE(64, 0, 1, 2)
+  ATTN_PREFILL_CASE(128, 1, 1, 2)
+  // one Q tile per item (128-row items)
+  ATTN_PREFILL_CASE(128, 0, 2, 1)
+  ATTN_PREFILL_CASE(128, 1, 2, 1)
+  ATTN_PREFILL_CASE(64, 0, 2, 1)
+  ATTN_PREFILL_CASE(64, 1, 2, 1)
+  ATTN_PREFILL_CASE(128, 0, 1, 1)
+  ATTN_PREFILL_CASE(64, 0, 1, 1)
+  ATTN_PREFILL_CASE(128, 1, 1, 1)
 #undef ATTN_PREFILL_CASE
   return ATTN_ERR_UNSUPPORTED;
 }

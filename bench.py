@@ -340,6 +340,7 @@ def protocol(b, d):
     rope_pass = lambda: (b.rope_apply(d["q"], qr, theta=THETA), b.rope_apply(d["k"], kr, theta=THETA))
     out["prefill_s16384"] = interleaved({
         "rope1_eager": pf(1), "rope1_graph": graph_of(pf(1)), "fused_in_kernel_eager": pf(2),
+        "fused_in_kernel_graph": graph_of(pf(2)),
         "unfused_eager": unfused, "no_rope_eager": pf(False),
         "rope_apply_qk_eager": rope_pass, "rope_apply_qk_graph": graph_of(rope_pass)})
     dec = lambda: b.attn_decode(d["dq"], d["dk"], d["dv"], d["dl"], o=d["do"], rope=True,
@@ -374,6 +375,80 @@ def protocol(b, d):
         cfg[str(B)].update(splits)
         del q, kc, vc, cl, o
     out["decode_global_vs_per_shape_graph_ms"] = cfg
+    return out
+
+
+def shape_trace(n=16, seed=11):
+    """A seeded synthetic trace of prefill shapes drawn from the configs' families: the tiny
+    causal GQA shape, non-causal Z x H=32 x D=64, and causal GQA Z x Hq=32 x Hkv=8 x D=128, with
+    batches 1-4 and prompt lengths 128-4096 (bf16)."""
+    import random
+
+    rng = random.Random(seed)
+    shapes = []
+    for _ in range(n):
+        fam = rng.choice(["tiny", "noncausal_d64", "causal_d128", "causal_d128"])
+        if fam == "tiny":
+            shapes.append((1, 4, 1, 128, 64, True))
+        elif fam == "noncausal_d64":
+            shapes.append((rng.choice([1, 2, 4]), 32, 32, rng.choice([256, 1024, 2048]), 64, False))
+        else:
+            shapes.append((rng.choice([1, 2, 4]), 32, 8, rng.choice([512, 1024, 2048, 4096]), 128,
+                           True))
+    return shapes
+
+
+def factorial(b):
+    """The Lesson page's 2x2 (다음에 기억할 것): {one global tile configuration, the best
+    configuration per shape} x {RoPE as separate rotation passes (rope=1 with its workspace),
+    RoPE inside the kernel (rope=2)}, eager and CUDA-graph replay, over a seeded shape trace.
+    Tile configurations: 2 or 1 Q tiles per work item.  Each (shape, config, RoPE form, mode)
+    is timed with the interleaved seeded protocol; the global configuration is the one with
+    the smallest total over the trace, per-shape picks each shape's fastest."""
+    import torch
+    from attention_attn_prefill_02_gb300 import synthetic
+
+    trace = shape_trace()
+    res = {}
+    for si, (B, Hq, Hkv, S, D, causal) in enumerate(trace):
+        q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=200 + si)
+        q, k, v = q.cuda(), k.cuda(), v.cuda()
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(max(16, b.attn_prefill_workspace_size(B, Hq, Hkv, S, D, rope=1)),
+                         dtype=torch.uint8, device="cuda")
+        fns = {}
+        for tiles in (2, 1):
+            for rope in (1, 2):
+                b.attn_set_prefill_tiles(tiles)
+                f = (lambda q=q, k=k, v=v, o=o, ws=ws, rope=rope, causal=causal, tiles=tiles:
+                     (b.attn_set_prefill_tiles(tiles),
+                      b.attn_prefill(q, k, v, causal=causal, rope=rope, rope_theta=THETA, o=o,
+                                     workspace=ws)))
+                fns[f"t{tiles}_r{rope}_eager"] = f
+                fns[f"t{tiles}_r{rope}_graph"] = graph_of(f)  # the config is fixed at capture
+        b.attn_set_prefill_tiles(0)
+        r = interleaved(fns, rounds=9, warmup=3, seed=si)
+        b.attn_set_prefill_tiles(0)
+        res[si] = {k2: v2["median"] for k2, v2 in r.items()}
+        del q, k, v, o, ws
+    out = {"trace": [dict(B=B, Hq=Hq, Hkv=Hkv, S=S, D=D, causal=c) for (B, Hq, Hkv, S, D, c)
+                     in trace], "cells": {}}
+    for rope in (1, 2):
+        for mode in ("eager", "graph"):
+            tot = {t: sum(res[i][f"t{t}_r{rope}_{mode}"] for i in res) for t in (2, 1)}
+            g = min(tot, key=tot.get)
+            best = sum(min(res[i][f"t{t}_r{rope}_{mode}"] for t in (2, 1)) for i in res)
+            out["cells"][f"rope{rope}_{mode}"] = {
+                "global_tiles": g, "global_ms": round(tot[g], 4),
+                "per_shape_ms": round(best, 4),
+                "per_shape_gain_pct": round(100.0 * (tot[g] - best) / tot[g], 3),
+                "per_shape_tiles": [min((2, 1), key=lambda t: res[i][f"t{t}_r{rope}_{mode}"])
+                                    for i in res]}
+    # fused (rope=2) vs rotation passes (rope=1) at each cell's global configuration
+    for mode in ("eager", "graph"):
+        c1, c2 = out["cells"][f"rope1_{mode}"], out["cells"][f"rope2_{mode}"]
+        out["cells"][f"rope2_over_rope1_{mode}"] = round(c1["global_ms"] / c2["global_ms"], 4)
+    out["per_shape_ms"] = {str(i): res[i] for i in res}
     return out
 
 
@@ -810,6 +885,7 @@ def ours(args):
     if rank == 0 and not args.no_variants:
         line["variants"] = variants(b, d)
         line["protocol"] = protocol(b, d)
+        line["factorial"] = factorial(b)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(seconds_budget=20.0)
     if rank == 0:

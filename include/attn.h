@@ -227,6 +227,19 @@ ATTN_API attn_status_t attn_prefill_chunk(const void* q, const void* k, const vo
                                           attn_stream_t stream);
 
 /*
+ * attn_set_prefill_tiles — the prefill's tile configuration, for the "one global configuration
+ * versus per-shape choice" comparison the Lesson page (shape adaptive attention negative
+ * 20260722, 다음에 기억할 것) asks every path to report.  q_tiles = 2: a work item is 256 query
+ * rows (two 128-row Q tiles whose softmaxes alternate with each other's matrix products; the
+ * default); 1: a work item is 128 rows (twice as many items, no alternation); 0 restores the
+ * default.  Applies to every later attn_prefill / attn_prefill_chunk at D <= 128 (D = 256
+ * always runs one tile per item).  Process-wide; set it only while no other thread launches a
+ * prefill.  Results are the same in either configuration up to rounding order.
+ * Errors: INVALID_ARG (q_tiles outside 0..2).
+ */
+ATTN_API attn_status_t attn_set_prefill_tiles(int q_tiles);
+
+/*
  * attn_set_prefill_events — a measurement hook: while set, every attn_prefill and
  * attn_prefill_chunk call records `begin_event` on its stream just before the attention kernel
  * is enqueued and `end_event` just after it (the RoPE rotation passes that may precede it stay

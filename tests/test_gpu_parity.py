@@ -115,6 +115,38 @@ def test_prefill_bf16(B, Hq, Hkv, S, D, causal):
     check(lse.cpu(), rl, LSE_TOL, None, what="LSE")
 
 
+@pytest.mark.parametrize("dtype,B,Hq,Hkv,S,D,causal,rope", [
+    ("bf16", 2, 4, 2, 640, 128, True, 0),     # several items per head, GQA
+    ("bf16", 1, 8, 8, 513, 64, True, 0),      # ragged, MHA, D = 64
+    ("bf16", 1, 4, 1, 1100, 128, True, 1),    # RoPE through the rotation passes
+    ("bf16", 1, 2, 2, 1030, 64, True, 2),     # RoPE inside the kernel
+    ("bf16", 1, 2, 1, 1000, 128, False, 0),   # non-causal, ragged
+    ("fp8", 1, 4, 1, 640, 128, True, 0),
+    ("fp8", 2, 2, 2, 300, 128, True, 1),      # fp8 with the staged in-kernel RoPE
+    ("fp8", 1, 4, 4, 256, 64, False, 0),
+])
+def test_prefill_one_tile_per_item(dtype, B, Hq, Hkv, S, D, causal, rope):
+    """The second tile configuration (one 128-row Q tile per work item) gives the same
+    attention as the oracle."""
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, dtype, seed=S + 71)
+    try:
+        binding.attn_set_prefill_tiles(1)
+        o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, rope=rope,
+                                      rope_theta=10000.0, want_lse=True)
+        status_ok()
+    finally:
+        binding.attn_set_prefill_tiles(0)
+    ro, rl = oracle.prefill(f64(q), f64(k), f64(v), causal=causal, rope=bool(rope),
+                            theta=10000.0)
+    if dtype == "fp8":
+        check(o.cpu(), ro, FP8_MAX, 1e-2, what="O fp8, one tile per item")
+        check(lse.cpu(), rl, 2e-2, None, what="LSE fp8, one tile per item")
+    else:
+        check(o.cpu(), ro, what="O, one tile per item")
+        check(lse.cpu(), rl, ROPE_LSE_TOL if rope else LSE_TOL, None,
+              what="LSE, one tile per item")
+
+
 def test_prefill_unfused_rope_tiny_config():
     """Tiny config: B=1, Hq=4, Hkv=1, S=128, D=64, RoPE 1e4 via rope_apply then attention."""
     q, k, v = synthetic.prefill_inputs(1, 4, 1, 128, 64, "bf16", seed=0)
