@@ -99,7 +99,9 @@ struct Cfg {
   static constexpr int kKStOff = kKVOff + kKStages * kKVTileBytes;
   static constexpr int kVOff = kKStOff + kKStages * kStTileBytes;
   static constexpr int kBarOff = kVOff + kVStages * kVTileBytes;
-  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
+  // + the barrier block (under 1 KB) + slack for aligning the base to 1024 bytes
+  static constexpr int kSmemBytes = kBarOff + 1024 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static_assert(kKStages <= 8 && kVStages <= 8, "barrier arrays hold 8 stages");
@@ -124,14 +126,17 @@ struct Params {
   int pos0;
 };
 
+struct Bars;
 struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
   uint64_t q_ready[2], k_ready[8];  // fused RoPE: tile rotated in shared memory
   uint64_t k_st_full[8], k_st_free[8];  // fp8 + RoPE: K staging tiles (loaded / consumed)
+  uint64_t p_hi[2];  // P of keys 64..127 written (p_full: keys 0..63, or all of P with RoPE)
   uint32_t tmem_slot;
 };
+static_assert(sizeof(Bars) <= 1024, "barrier block");
 
 // Item -> (query block m, batch b, query head hq).  Items are grouped so that the CTAs running
 // at the same time read few K/V streams (one stream = the keys and values of one (batch, KV
@@ -238,6 +243,10 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
   // per thread) run the softmax in two passes and write P over the upper half of S; the others
   // hold the whole S row in registers and write P over its first columns.
   constexpr uint32_t kPCol = ROPE ? (FP8 ? 96u : 64u) : 0u;
+  // P released in two halves (keys 0..63, then 64..127) so that half of the P V products
+  // overlap the softmax: measured faster at D >= 128, slower at D = 64, whose P V products are
+  // short anyway (A/B on one GPU: bf16 / fp8 D=128 -1 to -2.4 %, D=64 +0.8 % / +5 %)
+  constexpr bool kSplitP = D >= 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -250,6 +259,7 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
       mbar_init(&bars->q_empty[t], 1);
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 128);
+      if (kSplitP) mbar_init(&bars->p_hi[t], 128);
       mbar_init(&bars->o_full[t], 1);
       mbar_init(&bars->o_empty[t], 128);
     }
@@ -387,6 +397,20 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
             umma_ss_e(d, ad + off, bd + off, idesc_s, kk > 0);
         }
       };
+      // the P V products of P columns [k0, k1) (k steps of 16 bf16 / 32 fp8 keys)
+      auto issue_pv_part = [&](int t, int slot, bool acc, int k0, int k1) {
+        const uint64_t bd = v_desc0 + static_cast<uint64_t>((slot * C::kVTileBytes) >> 4);
+        const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0) + kPCol;
+        const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
+#pragma unroll
+        for (int kk = k0; kk < k1; ++kk) {
+          const uint64_t off = (kk * C::kPVKeys * C::kVSwz) >> 4;
+          if constexpr (FP8)
+            umma_ts_f8_e(d, pcol + kk * 8, bd + off, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          else
+            umma_ts_e(d, pcol + kk * 8, bd + off, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
       auto issue_pv = [&](int t, int slot, bool acc) {
         const uint64_t bd = v_desc0 + static_cast<uint64_t>((slot * C::kVTileBytes) >> 4);
         const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0) + kPCol;
@@ -447,17 +471,37 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             if (!ok) continue;
-            if (j - 1 < n[t]) {
-              ok = mbar_wait_warp(&bars->p_full[t], ph_pf[t], p.status);
-              ph_pf[t] ^= 1;
-              if (ok && j == 1) {
-                ok = mbar_wait_warp(&bars->o_empty[t], ph_oe[t] ^ 1, p.status);
-                ph_oe[t] ^= 1;
+            if constexpr (kSplitP) {
+              if (j - 1 < n[t]) {
+                // each half of P goes to the tensor core as soon as the softmax has written it
+                ok = mbar_wait_warp(&bars->p_full[t], ph_pf[t], p.status);
+                if (ok && j == 1) {
+                  ok = mbar_wait_warp(&bars->o_empty[t], ph_oe[t] ^ 1, p.status);
+                  ph_oe[t] ^= 1;
+                }
+                if (!ok) continue;
+                tc_fence_after();
+                issue_pv_part(t, vslot, j > 1, 0, C::kPVSteps / 2);
+                ok = mbar_wait_warp(&bars->p_hi[t], ph_pf[t], p.status);
+                ph_pf[t] ^= 1;
+                if (!ok) continue;
+                tc_fence_after();
+                issue_pv_part(t, vslot, true, C::kPVSteps / 2, C::kPVSteps);
+                if (j - 1 == n[t] - 1) umma_commit_e(&bars->o_full[t]);
               }
-              if (!ok) continue;
-              tc_fence_after();
-              issue_pv(t, vslot, j > 1);
-              if (j - 1 == n[t] - 1) umma_commit_e(&bars->o_full[t]);
+            } else {
+              if (j - 1 < n[t]) {
+                ok = mbar_wait_warp(&bars->p_full[t], ph_pf[t], p.status);
+                ph_pf[t] ^= 1;
+                if (ok && j == 1) {
+                  ok = mbar_wait_warp(&bars->o_empty[t], ph_oe[t] ^ 1, p.status);
+                  ph_oe[t] ^= 1;
+                }
+                if (!ok) continue;
+                tc_fence_after();
+                issue_pv(t, vslot, j > 1);
+                if (j - 1 == n[t] - 1) umma_commit_e(&bars->o_full[t]);
+              }
             }
             if (j < n[t]) {
               issue_s(t, kslot2);
@@ -753,57 +797,134 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
         const float2 c2 = make_float2(p.c_log2, p.c_log2);
         const float2 nm2 = make_float2(-m_run, -m_run);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
-        uint32_t pk[FP8 ? 32 : 64];
+        if constexpr (kSplitP) {
+          // O_t holds the tiles before j (their P V products completed before S_t(j) was
+          // signalled); rescale it before this step's P V products accumulate onto it.
+          // tcgen05.ld / st are warp-collective: rescale when any lane of the warp needs it
+          // (lanes that do not have f == 1), eight columns at a time so that the scores stay
+          // in registers meanwhile.
+          if (__any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll 1
+            for (int c = 0; c < D / 8; ++c) {
+              uint32_t ov[8];
+              tmem_ld8(tO + c * 8, ov);
 #pragma unroll
-        for (int e = 0; e < 128; e += 8) {
-          float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
-          float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
-          float2 x2 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5])), c2, nm2);
-          float2 x3 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7])), c2, nm2);
-          x0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
-          x1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
-          x2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
-          x3 = make_float2(fast_exp2(x3.x), fast_exp2(x3.y));
-          acc0 = __fadd2_rn(acc0, x0);
-          acc1 = __fadd2_rn(acc1, x1);
-          acc2 = __fadd2_rn(acc2, x2);
-          acc3 = __fadd2_rn(acc3, x3);
-          if constexpr (FP8) {
-            // e4m3, four keys per TMEM column, lowest key in the lowest byte
-            pk[e / 4] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x0, __NV_SATFINITE, __NV_E4M3)) |
-                        (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x1, __NV_SATFINITE, __NV_E4M3)) << 16);
-            pk[e / 4 + 1] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x2, __NV_SATFINITE, __NV_E4M3)) |
-                            (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x3, __NV_SATFINITE, __NV_E4M3)) << 16);
-          } else {
-            pk[e / 2] = pack_bf16(x0.x, x0.y);
-            pk[e / 2 + 1] = pack_bf16(x1.x, x1.y);
-            pk[e / 2 + 2] = pack_bf16(x2.x, x2.y);
-            pk[e / 2 + 3] = pack_bf16(x3.x, x3.y);
+              for (int e = 0; e < 8; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+              tmem_st8(tO + c * 8, ov);
+            }
           }
-        }
-        const float2 accs = __fadd2_rn(__fadd2_rn(acc0, acc1), __fadd2_rn(acc2, acc3));
-        l += accs.x + accs.y;
-        if constexpr (FP8)
-          tmem_st32(tS, pk);
-        else
-          tmem_st64(tS, pk);
-        }
-        // tcgen05.ld / st are warp-collective: rescale when any lane of the warp needs it
-        // (lanes that do not have f == 1).
-        if (__any_sync(0xffffffffu, f != 1.f)) {
-          // O_t holds the tiles before j (their PV completed before S_t(j) was signalled)
+          // keys 0..63 first: their P is released to the MMA warp (p_full) before the
+          // exponentials of keys 64..127 (p_hi), so half of the P V products overlap the softmax
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tO + c * 32, ov);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[FP8 ? 16 : 32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-            tmem_st32(tO + c * 32, ov);
+            for (int e = 64 * h; e < 64 * h + 64; e += 8) {
+              float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
+              float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
+              float2 x2 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5])), c2, nm2);
+              float2 x3 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7])), c2, nm2);
+              x0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+              x1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+              x2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
+              x3 = make_float2(fast_exp2(x3.x), fast_exp2(x3.y));
+              acc0 = __fadd2_rn(acc0, x0);
+              acc1 = __fadd2_rn(acc1, x1);
+              acc2 = __fadd2_rn(acc2, x2);
+              acc3 = __fadd2_rn(acc3, x3);
+              const int w = e - 64 * h;
+              if constexpr (FP8) {
+                // e4m3, four keys per TMEM column, lowest key in the lowest byte
+                pk[w / 4] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x0, __NV_SATFINITE, __NV_E4M3)) |
+                            (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x1, __NV_SATFINITE, __NV_E4M3)) << 16);
+                pk[w / 4 + 1] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x2, __NV_SATFINITE, __NV_E4M3)) |
+                                (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x3, __NV_SATFINITE, __NV_E4M3)) << 16);
+              } else {
+                pk[w / 2] = pack_bf16(x0.x, x0.y);
+                pk[w / 2 + 1] = pack_bf16(x1.x, x1.y);
+                pk[w / 2 + 2] = pack_bf16(x2.x, x2.y);
+                pk[w / 2 + 3] = pack_bf16(x3.x, x3.y);
+              }
+            }
+            if constexpr (FP8)
+              tmem_st16(tS + 16 * h, pk);
+            else
+              tmem_st32(tS + 32 * h, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(h ? &bars->p_hi[t] : &bars->p_full[t]);
           }
+          const float2 accs = __fadd2_rn(__fadd2_rn(acc0, acc1), __fadd2_rn(acc2, acc3));
+          l += accs.x + accs.y;
+        } else {
+          uint32_t pk[FP8 ? 32 : 64];
+#pragma unroll
+          for (int e = 0; e < 128; e += 8) {
+            float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
+            float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
+            float2 x2 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5])), c2, nm2);
+            float2 x3 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7])), c2, nm2);
+            x0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+            x1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+            x2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
+            x3 = make_float2(fast_exp2(x3.x), fast_exp2(x3.y));
+            acc0 = __fadd2_rn(acc0, x0);
+            acc1 = __fadd2_rn(acc1, x1);
+            acc2 = __fadd2_rn(acc2, x2);
+            acc3 = __fadd2_rn(acc3, x3);
+            if constexpr (FP8) {
+              // e4m3, four keys per TMEM column, lowest key in the lowest byte
+              pk[e / 4] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x0, __NV_SATFINITE, __NV_E4M3)) |
+                          (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x1, __NV_SATFINITE, __NV_E4M3)) << 16);
+              pk[e / 4 + 1] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x2, __NV_SATFINITE, __NV_E4M3)) |
+                              (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x3, __NV_SATFINITE, __NV_E4M3)) << 16);
+            } else {
+              pk[e / 2] = pack_bf16(x0.x, x0.y);
+              pk[e / 2 + 1] = pack_bf16(x1.x, x1.y);
+              pk[e / 2 + 2] = pack_bf16(x2.x, x2.y);
+              pk[e / 2 + 3] = pack_bf16(x3.x, x3.y);
+            }
+          }
+          const float2 accs = __fadd2_rn(__fadd2_rn(acc0, acc1), __fadd2_rn(acc2, acc3));
+          l += accs.x + accs.y;
+          if constexpr (FP8)
+            tmem_st32(tS, pk);
+          else
+            tmem_st64(tS, pk);
+          // O_t holds the tiles before j (their P V products completed before S_t(j) was
+          // signalled); rescale it, warp-uniformly, before P is released
+          if (__any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(tO + c * 32, ov);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+              tmem_st32(tO + c * 32, ov);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full[t]);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[t]);
+        }
+        if constexpr (ROPE) {
+          // (two-pass softmax) P is complete; rescale O, then release both halves at once
+          if (__any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(tO + c * 32, ov);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+              tmem_st32(tO + c * 32, ov);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bars->p_full[t]);
+          if constexpr (kSplitP) mbar_arrive(&bars->p_hi[t]);
+        }
       }
       if (!ok) break;
       // epilogue: O / l -> bf16, LSE
