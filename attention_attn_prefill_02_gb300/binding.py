@@ -71,6 +71,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, i, f, vp]
     L.attn_set_prefill_tiles.restype = i
     L.attn_set_prefill_tiles.argtypes = [i]
+    L.attn_set_backward_path.restype = i
+    L.attn_set_backward_path.argtypes = [i]
     L.attn_set_prefill_events.restype = i
     L.attn_set_prefill_events.argtypes = [vp, vp]
     L.attn_set_decode_splits.restype = i
@@ -288,6 +290,12 @@ def attn_decode_noalloc(q, k_cache, v_cache, cache_len, o=None, lse=None, want_l
 def attn_set_prefill_tiles(q_tiles):
     """1 or 2 Q tiles per prefill work item for later calls at D <= 128; 0: the default (2)."""
     _check(lib().attn_set_prefill_tiles(int(q_tiles)), "attn_set_prefill_tiles")
+
+
+def attn_set_backward_path(path):
+    """Kernels of later attn_prefill_backward calls: 1 = warp-level mma.sync, 2 = tcgen05,
+    0 = the default (tcgen05)."""
+    _check(lib().attn_set_backward_path(int(path)), "attn_set_backward_path")
 
 
 def attn_set_prefill_events(begin=None, end=None):

@@ -300,6 +300,12 @@ attn_status_t attn_set_prefill_tiles(int q_tiles) {
   return ATTN_OK;
 }
 
+attn_status_t attn_set_backward_path(int path) {
+  if (path < 0 || path > 2) return ATTN_ERR_INVALID_ARG;
+  force_backward_path(path);
+  return ATTN_OK;
+}
+
 attn_status_t attn_set_decode_splits(int nsplit) {
   if (nsplit < 0 || nsplit > 1024) return ATTN_ERR_INVALID_ARG;
   force_decode_splits(nsplit);

@@ -15,7 +15,11 @@
 //                          128-byte-swizzled shared tiles); dS^T goes through shared memory and
 //                          the warps add dQ += dS K into the fp32 accumulator (2-wide atomics).
 //   bwd_dq_convert_kernel  dQ = scale * accumulator -> bf16.
+//
+// These warp-level kernels are the second path; the default runs every product on tcgen05
+// (backward_tc.cu) and attn_set_backward_path selects between them.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "common.cuh"
@@ -350,10 +354,19 @@ size_t bwd_workspace_bytes(int B, int Hq, int S, int D) {
   return delta + rows * D * 4;
 }
 
+namespace {
+std::atomic<int> g_bwd_path{0};
+}  // namespace
+
+void force_backward_path(int path) { g_bwd_path.store(path); }
+
 attn_status_t launch_prefill_backward(const void* q, const void* k, const void* v, const void* o,
                                       const float* lse, const void* dout, void* dq, void* dk,
                                       void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
                                       float scale, void* ws, cudaStream_t st) {
+  if (g_bwd_path.load() != 1)
+    return launch_prefill_backward_tc(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, S, D, causal,
+                                      scale, ws, st);
   BwdParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);

@@ -1,0 +1,607 @@
+// backward_tc.cu — gradients of grouped-query attention on the 5th-generation tensor cores:
+// dQ, dK, dV for bf16 Q/K/V at D = 64 / 128, every product on tcgen05 with TMEM accumulators.
+//
+// With P = softmax(scale Q K^T + mask) recomputed from the forward's log-sum-exp, the chain rule
+// gives dV = P^T dO, dP = dO V^T, dS = P * (dP - Delta) with Delta_i = sum_d dO_id O_id,
+// dQ = scale dS K and dK = scale dS^T Q; a KV head's dK and dV sum over the G query heads that
+// read it.  Two kernels, neither with atomics:
+//
+//   bwd_tc_kv_kernel  one CTA per (128-key tile, batch, KV head).  Per step (one 128-row query
+//                     tile of one query head of the group): S^T = K Q^T and dP^T = V dO^T into
+//                     TMEM; four warps (one key row per thread) turn them into P^T and dS^T,
+//                     written back as bf16 over the columns they were read from; then
+//                     dV += P^T dO and dK += dS^T Q with P^T / dS^T as the TMEM A operand.
+//                     TMEM: S^T 128 | dP^T 128 | dV D | dK D columns.
+//   bwd_tc_q_kernel   one CTA per (128-row query tile, batch, query head).  Per key tile:
+//                     S = Q K^T and dP = dO V^T into TMEM, dS (bf16) over S, dQ += dS K.
+//                     TMEM: S 128 | dP 128 | dQ D columns.
+//
+// Each step runs in two halves of 64 columns (query columns in the first kernel, key columns in
+// the second): the tensor core computes the scores of half 1 while the four warps turn half 0
+// into P / dS, and the gradient products of half 0 run while they do half 1.
+//
+// Tiles move by TMA in 128-row boxes of 64 bf16 with the 128-byte swizzle; one shared tile
+// serves as a K-major operand (the Q K^T style products) and an MN-major one (the P V style).
+// Warps 0-3 turn scores into P / dS and write the result, warp 4 loads (TMA, plus the per-row
+// log-sum-exp and Delta of each query tile), warp 5 issues the MMAs (the whole warp in the loop,
+// one elected lane issuing).  Every wait is bounded, and warp-uniform where the warp goes on to
+// a .sync.aligned TMEM access.
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kTcRows = 128;     // keys per key tile, query rows per query tile (TMEM lanes)
+constexpr int kTcHalf = 64;      // columns per half step
+constexpr int kTcThreads = 192;  // 4 score warps, the load warp, the MMA warp
+constexpr int kTcLoader = 4, kTcMma = 5;
+constexpr float kTcLog2e = 1.4426950408889634f;
+
+struct TcParams {
+  const float* lse;    // [B*Hq*S] natural log
+  const float* delta;  // [B*Hq*S]
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  unsigned int* status;
+  int B, Hq, Hkv, G, S, causal, nT;  // nT: 128-row tiles along S
+  float scale;                      // softmax scale
+};
+
+// A [128 x D] bf16 tile as D/64 boxes of [128 rows x 128 bytes] (128-byte swizzle).
+template <int D>
+struct TcTile {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kBoxBytes = kTcRows * 128;
+  static constexpr int kBytes = kBoxes * kBoxBytes;
+  static constexpr int kKSteps = D / 16;  // K steps of 16 when the tile is the K-major operand
+};
+
+// Loads a [128 x D] tile (rows r0.., outer index z) into `dst` through TMA, completing on `bar`.
+template <int D>
+__device__ __forceinline__ void tc_load_tile(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar,
+                                             int r0, int z) {
+#pragma unroll
+  for (int bx = 0; bx < TcTile<D>::kBoxes; ++bx)
+    tma_load_3d(dst + bx * TcTile<D>::kBoxBytes, tm, bar, bx * 64, r0, z);
+}
+
+// D[tmem] = A B^T over the head dim for the 64 B rows b_row0..: A [128 x D] and B [128 x D]
+// K-major tiles in shared memory; the result fills 64 TMEM columns.
+template <int D>
+__device__ __forceinline__ void tc_mma_scores(uint32_t d, uint64_t a0, uint64_t b0, int b_row0,
+                                              uint32_t idesc) {
+  const uint64_t b_off = static_cast<uint64_t>((b_row0 * 128) >> 4);  // 8-row groups stay whole
+#pragma unroll
+  for (int kk = 0; kk < TcTile<D>::kKSteps; ++kk) {
+    const uint64_t off = ((kk / 4) * TcTile<D>::kBoxBytes + (kk % 4) * 32) >> 4;
+    umma_ss_e(d, a0 + off, b0 + b_off + off, idesc, kk > 0);
+  }
+}
+
+// D[tmem] (+)= A X over 64 rows r0..r0+63: A [128 x 64] bf16 packed two per TMEM column at
+// a_tmem.., X rows r0.. of a [128 x D] tile in shared memory read MN-major (D contiguous).
+template <int D>
+__device__ __forceinline__ void tc_mma_grad(uint32_t d, uint32_t a_tmem, uint64_t x0, int r0,
+                                            uint32_t idesc, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < kTcHalf / 16; ++kk) {
+    const uint64_t off = static_cast<uint64_t>(((r0 + kk * 16) * 128) >> 4);
+    umma_ts_e(d, a_tmem + kk * 8, x0 + off, idesc, (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+// One TMEM lane's D accumulator columns, times `mul`, as a bf16 row at dst (written only when
+// `store`).  Every lane of the warp runs the TMEM loads, which are warp-collective
+// (.sync.aligned): rows past S skip only the global store.
+template <int D>
+__device__ __forceinline__ void tc_store_row(__nv_bfloat16* dst, uint32_t taddr, float mul,
+                                             bool store) {
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c * 32, v);
+    if (store) {
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint4 w;
+        w.x = pack_bf16(__uint_as_float(v[q4 * 8 + 0]) * mul, __uint_as_float(v[q4 * 8 + 1]) * mul);
+        w.y = pack_bf16(__uint_as_float(v[q4 * 8 + 2]) * mul, __uint_as_float(v[q4 * 8 + 3]) * mul);
+        w.z = pack_bf16(__uint_as_float(v[q4 * 8 + 4]) * mul, __uint_as_float(v[q4 * 8 + 5]) * mul);
+        w.w = pack_bf16(__uint_as_float(v[q4 * 8 + 6]) * mul, __uint_as_float(v[q4 * 8 + 7]) * mul);
+        reinterpret_cast<uint4*>(dst + c * 32)[q4] = w;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// dK, dV
+// ------------------------------------------------------------------------------------------
+
+template <int D>
+struct KvSmem {
+  using T = TcTile<D>;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + T::kBytes;
+  static constexpr int kQ = kV + T::kBytes;            // two stages
+  static constexpr int kO = kQ + 2 * T::kBytes;        // two stages (dO)
+  static constexpr int kLse = kO + 2 * T::kBytes;      // [2][128] LSE * log2e
+  static constexpr int kDel = kLse + 2 * kTcRows * 4;  // [2][128] Delta
+  static constexpr int kBar = kDel + 2 * kTcRows * 4;
+  // at least 120 KB so that one CTA (and one 512-column TMEM allocation) runs per SM
+  static constexpr int kBytes = std::max(kBar + 256 + 1024, 120 * 1024);
+  static_assert(kBytes <= 232448, "shared memory per CTA");
+};
+
+struct KvBars {
+  uint64_t kv_full, q_full[2], q_empty[2], row_full[2], s_full[2], p_full[2], done;
+  uint32_t tmem_slot;
+};
+static_assert(sizeof(KvBars) <= 256, "barrier block");
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    bwd_tc_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const TcParams p) {
+  using L = KvSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  KvBars* bars = reinterpret_cast<KvBars*>(smem + L::kBar);
+  float* s_lse = reinterpret_cast<float*>(smem + L::kLse);
+  float* s_del = reinterpret_cast<float*>(smem + L::kDel);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bhkv = p.B * p.Hkv;
+  const int tile = blockIdx.x / bhkv;  // key tile 0 first: it meets the most query rows
+  const int bh = blockIdx.x - tile * bhkv;
+  const int b = bh / p.Hkv, kvh = bh - b * p.Hkv;
+  const int kv0 = tile * kTcRows;
+  const int qt0 = p.causal ? tile : 0;  // earlier query tiles see none of these keys
+  const int per_head = p.nT - qt0;
+  const int steps = p.G * per_head;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->q_full[t], 1);
+      mbar_init(&bars->q_empty[t], 1);
+      mbar_init(&bars->row_full[t], 32);
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+    }
+    mbar_init(&bars->done, 1);
+    fence_barrier_init();
+  }
+  if (warp == kTcMma) tmem_alloc(&bars->tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+
+  // step st: query head kvh * G + st / per_head, query tile qt0 + st % per_head
+  auto step_q = [&](int st, int& hq, int& qt) {
+    const int gi = st / per_head;
+    qt = qt0 + (st - gi * per_head);
+    hq = kvh * p.G + gi;
+  };
+
+  if (warp == kTcLoader) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmO);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * TcTile<D>::kBytes);
+      tc_load_tile<D>(smem + L::kK, &tmK, &bars->kv_full, kv0, bh);
+      tc_load_tile<D>(smem + L::kV, &tmV, &bars->kv_full, kv0, bh);
+    }
+    for (int st = 0; st < steps; ++st) {
+      const int sg = st & 1;
+      // stage sg is free once the gradient products of step st - 2 completed (they follow the
+      // score warps' last read of its log-sum-exp and Delta)
+      if (st >= 2 && !mbar_wait_warp(&bars->q_empty[sg], ((st >> 1) & 1) ^ 1, p.status)) break;
+      int hq, qt;
+      step_q(st, hq, qt);
+      const int z = b * p.Hq + hq;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full[sg], 2 * TcTile<D>::kBytes);
+        tc_load_tile<D>(smem + L::kQ + sg * TcTile<D>::kBytes, &tmQ, &bars->q_full[sg],
+                        qt * kTcRows, z);
+        tc_load_tile<D>(smem + L::kO + sg * TcTile<D>::kBytes, &tmO, &bars->q_full[sg],
+                        qt * kTcRows, z);
+      }
+      const size_t rbase = static_cast<size_t>(z) * p.S;
+#pragma unroll
+      for (int i = 0; i < kTcRows / 32; ++i) {
+        const int r = i * 32 + lane, q = qt * kTcRows + r;
+        // rows past S: P = 0 through an infinite log-sum-exp (their scores are masked as well)
+        s_lse[sg * kTcRows + r] = q < p.S ? __ldg(p.lse + rbase + q) * kTcLog2e : INFINITY;
+        s_del[sg * kTcRows + r] = q < p.S ? __ldg(p.delta + rbase + q) : 0.f;
+      }
+      mbar_arrive(&bars->row_full[sg]);
+    }
+  } else if (warp == kTcMma) {
+    const uint32_t idesc_s = make_idesc(1, 1, false, false, kTcHalf, kTcRows);
+    const uint32_t idesc_g = make_idesc(1, 1, false, true, D, kTcRows);  // B MN-major
+    const uint64_t k_desc = smem_desc(smem_u32(smem + L::kK), 16, 1024, 2);
+    const uint64_t v_desc = smem_desc(smem_u32(smem + L::kV), 16, 1024, 2);
+    const uint64_t q_desc0 = smem_desc(smem_u32(smem + L::kQ), 16, 1024, 2);
+    const uint64_t o_desc0 = smem_desc(smem_u32(smem + L::kO), 16, 1024, 2);
+    const uint64_t qg_desc0 = smem_desc(smem_u32(smem + L::kQ), TcTile<D>::kBoxBytes, 1024, 2);
+    const uint64_t og_desc0 = smem_desc(smem_u32(smem + L::kO), TcTile<D>::kBoxBytes, 1024, 2);
+    bool ok = mbar_wait_warp(&bars->kv_full, 0, p.status);
+    for (int st = 0; st < steps && ok; ++st) {
+      const int sg = st & 1;
+      const uint64_t so = static_cast<uint64_t>((sg * TcTile<D>::kBytes) >> 4);
+      if (!(ok = mbar_wait_warp(&bars->q_full[sg], (st >> 1) & 1, p.status))) break;
+      tc_fence_after();
+      // S^T = K Q^T and dP^T = V dO^T, query columns 64h.. of half h.  The previous step's
+      // gradient products, issued before these, read the same columns: the tensor core runs
+      // one CTA's MMAs in issue order.
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tc_mma_scores<D>(tmem + kColS + h * kTcHalf, k_desc, q_desc0 + so, h * kTcHalf, idesc_s);
+        tc_mma_scores<D>(tmem + kColDP + h * kTcHalf, v_desc, o_desc0 + so, h * kTcHalf, idesc_s);
+        umma_commit_e(&bars->s_full[h]);
+      }
+      // dV += P^T dO, dK += dS^T Q over the 64 query rows of each half; P^T / dS^T of half h
+      // sit in columns 32h.. (bf16 pairs)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait_warp(&bars->p_full[h], st & 1, p.status))) break;
+        tc_fence_after();
+        const bool acc = st > 0 || h > 0;
+        tc_mma_grad<D>(tmem + kColDV, tmem + kColS + 32 * h, og_desc0 + so, h * kTcHalf, idesc_g, acc);
+        tc_mma_grad<D>(tmem + kColDK, tmem + kColDP + 32 * h, qg_desc0 + so, h * kTcHalf, idesc_g, acc);
+      }
+      if (!ok) break;
+      umma_commit_e(&bars->q_empty[sg]);
+    }
+    if (ok) umma_commit_e(&bars->done);
+  } else {
+    // ---------------------------------------------------------------- P^T and dS^T, one key row
+    const int kr = warp * 32 + lane;  // warps 0-3: TMEM lane quarters
+    const int key = kv0 + kr;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_off + kColS, tDP = tmem + lane_off + kColDP;
+    const float sl2 = p.scale * kTcLog2e;
+    bool ok = true;
+    for (int st = 0; st < steps && ok; ++st) {
+      const int sg = st & 1;
+      int hq, qt;
+      step_q(st, hq, qt);
+      const int q0 = qt * kTcRows;
+      // masks: the diagonal tile, and the last query or key tile when S is ragged
+      const bool need_mask = (p.causal && qt == tile) || q0 + kTcRows > p.S || kv0 + kTcRows > p.S;
+      if (!(ok = mbar_wait_warp(&bars->row_full[sg], (st >> 1) & 1, p.status))) break;
+      const float* lse_s = s_lse + sg * kTcRows;
+      const float* del_s = s_del + sg * kTcRows;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait_warp(&bars->s_full[h], st & 1, p.status))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const int col = h * kTcHalf + c * 32;  // query column of this chunk in the tile
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tS + col, sv);
+          tmem_ld32(tDP + col, dv);
+          uint32_t pp[16], dd[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + col + e);
+            const float4 d4 = *reinterpret_cast<const float4*>(del_s + col + e);
+            float pr[4] = {fast_exp2(__uint_as_float(sv[e + 0]) * sl2 - l4.x),
+                           fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l4.y),
+                           fast_exp2(__uint_as_float(sv[e + 2]) * sl2 - l4.z),
+                           fast_exp2(__uint_as_float(sv[e + 3]) * sl2 - l4.w)};
+            if (need_mask) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int q = q0 + col + e + u;
+                if (!(key < p.S && q < p.S && (!p.causal || key <= q))) pr[u] = 0.f;
+              }
+            }
+            pp[e / 2] = pack_bf16(pr[0], pr[1]);
+            pp[e / 2 + 1] = pack_bf16(pr[2], pr[3]);
+            dd[e / 2] = pack_bf16(pr[0] * (__uint_as_float(dv[e + 0]) - d4.x),
+                                  pr[1] * (__uint_as_float(dv[e + 1]) - d4.y));
+            dd[e / 2 + 1] = pack_bf16(pr[2] * (__uint_as_float(dv[e + 2]) - d4.z),
+                                      pr[3] * (__uint_as_float(dv[e + 3]) - d4.w));
+          }
+          // bf16 pairs of columns col.. go to col / 2..: columns this thread already read
+          tmem_st16(tS + col / 2, pp);
+          tmem_st16(tDP + col / 2, dd);
+        }
+        if (!ok) break;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[h]);
+      }
+    }
+    // dK = scale * sum dS^T Q and dV, bf16, this thread's key row
+    if (ok && (ok = mbar_wait_warp(&bars->done, 0, p.status))) {
+      tc_fence_after();
+      const size_t row = static_cast<size_t>(bh) * p.S + key;
+      tc_store_row<D>(p.dk + row * D, tmem + lane_off + kColDK, p.scale, key < p.S);
+      tc_store_row<D>(p.dv + row * D, tmem + lane_off + kColDV, 1.f, key < p.S);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTcMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// dQ
+// ------------------------------------------------------------------------------------------
+
+template <int D>
+struct QSmem {
+  using T = TcTile<D>;
+  static constexpr int kQ = 0;
+  static constexpr int kO = kQ + T::kBytes;
+  static constexpr int kK = kO + T::kBytes;      // two stages
+  static constexpr int kV = kK + 2 * T::kBytes;  // two stages
+  static constexpr int kBar = kV + 2 * T::kBytes;
+  static constexpr int kBytes = std::max(kBar + 256 + 1024, 120 * 1024);
+  static_assert(kBytes <= 232448, "shared memory per CTA");
+};
+
+struct QBars {
+  uint64_t qd_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], done;
+  uint32_t tmem_slot;
+};
+static_assert(sizeof(QBars) <= 256, "barrier block");
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    bwd_tc_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const TcParams p) {
+  using L = QSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  QBars* bars = reinterpret_cast<QBars*>(smem + L::kBar);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bhq = p.B * p.Hq;
+  const int lvl = blockIdx.x / bhq;
+  const int qt = p.causal ? p.nT - 1 - lvl : lvl;  // causal: the longest query tiles first
+  const int bh = blockIdx.x - lvl * bhq;
+  const int b = bh / p.Hq, hq = bh - b * p.Hq;
+  const int kvz = b * p.Hkv + hq / p.G;
+  const int q0 = qt * kTcRows;
+  const int steps = p.causal ? qt + 1 : p.nT;  // key tiles this query tile meets
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->qd_full, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->kv_full[t], 1);
+      mbar_init(&bars->kv_empty[t], 1);
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+    }
+    mbar_init(&bars->done, 1);
+    fence_barrier_init();
+  }
+  if (warp == kTcMma) tmem_alloc(&bars->tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+
+  if (warp == kTcLoader) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmO);
+      mbar_arrive_expect_tx(&bars->qd_full, 2 * TcTile<D>::kBytes);
+      tc_load_tile<D>(smem + L::kQ, &tmQ, &bars->qd_full, q0, bh);
+      tc_load_tile<D>(smem + L::kO, &tmO, &bars->qd_full, q0, bh);
+      for (int st = 0; st < steps; ++st) {
+        const int sg = st & 1;
+        if (st >= 2 && !mbar_wait(&bars->kv_empty[sg], ((st >> 1) & 1) ^ 1, p.status)) break;
+        mbar_arrive_expect_tx(&bars->kv_full[sg], 2 * TcTile<D>::kBytes);
+        tc_load_tile<D>(smem + L::kK + sg * TcTile<D>::kBytes, &tmK, &bars->kv_full[sg],
+                        st * kTcRows, kvz);
+        tc_load_tile<D>(smem + L::kV + sg * TcTile<D>::kBytes, &tmV, &bars->kv_full[sg],
+                        st * kTcRows, kvz);
+      }
+    }
+  } else if (warp == kTcMma) {
+    const uint32_t idesc_s = make_idesc(1, 1, false, false, kTcHalf, kTcRows);
+    const uint32_t idesc_g = make_idesc(1, 1, false, true, D, kTcRows);  // B MN-major
+    const uint64_t q_desc = smem_desc(smem_u32(smem + L::kQ), 16, 1024, 2);
+    const uint64_t o_desc = smem_desc(smem_u32(smem + L::kO), 16, 1024, 2);
+    const uint64_t k_desc0 = smem_desc(smem_u32(smem + L::kK), 16, 1024, 2);
+    const uint64_t v_desc0 = smem_desc(smem_u32(smem + L::kV), 16, 1024, 2);
+    const uint64_t kg_desc0 = smem_desc(smem_u32(smem + L::kK), TcTile<D>::kBoxBytes, 1024, 2);
+    bool ok = mbar_wait_warp(&bars->qd_full, 0, p.status);
+    for (int st = 0; st < steps && ok; ++st) {
+      const int sg = st & 1;
+      const uint64_t so = static_cast<uint64_t>((sg * TcTile<D>::kBytes) >> 4);
+      if (!(ok = mbar_wait_warp(&bars->kv_full[sg], (st >> 1) & 1, p.status))) break;
+      tc_fence_after();
+      // S = Q K^T and dP = dO V^T, key columns 64h.. of half h
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tc_mma_scores<D>(tmem + kColS + h * kTcHalf, q_desc, k_desc0 + so, h * kTcHalf, idesc_s);
+        tc_mma_scores<D>(tmem + kColDP + h * kTcHalf, o_desc, v_desc0 + so, h * kTcHalf, idesc_s);
+        umma_commit_e(&bars->s_full[h]);
+      }
+      // dQ += dS K over the 64 keys of each half (dS of half h in S columns 32h..)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait_warp(&bars->p_full[h], st & 1, p.status))) break;
+        tc_fence_after();
+        tc_mma_grad<D>(tmem + kColDQ, tmem + kColS + 32 * h, kg_desc0 + so, h * kTcHalf, idesc_g,
+                       st > 0 || h > 0);
+      }
+      if (!ok) break;
+      umma_commit_e(&bars->kv_empty[sg]);
+    }
+    if (ok) umma_commit_e(&bars->done);
+  } else {
+    // ---------------------------------------------------------------- dS, one query row
+    const int qr = warp * 32 + lane;
+    const int q = q0 + qr;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_off + kColS, tDP = tmem + lane_off + kColDP;
+    const float sl2 = p.scale * kTcLog2e;
+    const size_t row = static_cast<size_t>(bh) * p.S + q;
+    const float l2 = q < p.S ? __ldg(p.lse + row) * kTcLog2e : INFINITY;
+    const float de = q < p.S ? __ldg(p.delta + row) : 0.f;
+    bool ok = true;
+    for (int st = 0; st < steps && ok; ++st) {
+      const int k0 = st * kTcRows;
+      const bool need_mask = (p.causal && st == qt) || k0 + kTcRows > p.S || q0 + kTcRows > p.S;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait_warp(&bars->s_full[h], st & 1, p.status))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const int col = h * kTcHalf + c * 32;  // key column of this chunk in the tile
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tS + col, sv);
+          tmem_ld32(tDP + col, dv);
+          uint32_t dd[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float p0 = fast_exp2(__uint_as_float(sv[e]) * sl2 - l2);
+            float p1 = fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l2);
+            if (need_mask) {
+              const int k = k0 + col + e;
+              if (!(q < p.S && k < p.S && (!p.causal || k <= q))) p0 = 0.f;
+              if (!(q < p.S && k + 1 < p.S && (!p.causal || k + 1 <= q))) p1 = 0.f;
+            }
+            dd[e / 2] = pack_bf16(p0 * (__uint_as_float(dv[e]) - de),
+                                  p1 * (__uint_as_float(dv[e + 1]) - de));
+          }
+          tmem_st16(tS + col / 2, dd);
+        }
+        if (!ok) break;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[h]);
+      }
+    }
+    // dQ = scale * sum dS K, bf16, this thread's query row
+    if (ok && (ok = mbar_wait_warp(&bars->done, 0, p.status))) {
+      tc_fence_after();
+      tc_store_row<D>(p.dq + row * D, tmem + lane_off + kColDQ, p.scale, q < p.S);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTcMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Delta_i = sum_d dO_id O_id, one warp per query row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_tc_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                           const __nv_bfloat16* __restrict__ dout,
+                                                           float* __restrict__ delta,
+                                                           long long rows) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < rows;
+       r += warps) {
+    const __nv_bfloat16* orow = o + r * D + lane * E;
+    const __nv_bfloat16* drow = dout + r * D + lane * E;
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(orow + e));
+      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(drow + e));
+      acc = fmaf(a.x, c.x, fmaf(a.y, c.y, acc));
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o2);
+    if (lane == 0) delta[r] = acc;
+  }
+}
+
+template <int D>
+attn_status_t launch_bwd_tc_typed(const void* q, const void* k, const void* v, const void* o,
+                                  const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                  int B, int Hq, int Hkv, int S, int causal, float scale,
+                                  float* delta, cudaStream_t st) {
+  CUtensorMap tq, tk, tv, to;
+  if (!make_tmap_3d(&tq, q, 2, D, S, static_cast<uint64_t>(B) * Hq, 64, kTcRows, 128) ||
+      !make_tmap_3d(&tk, k, 2, D, S, static_cast<uint64_t>(B) * Hkv, 64, kTcRows, 128) ||
+      !make_tmap_3d(&tv, v, 2, D, S, static_cast<uint64_t>(B) * Hkv, 64, kTcRows, 128) ||
+      !make_tmap_3d(&to, dout, 2, D, S, static_cast<uint64_t>(B) * Hq, 64, kTcRows, 128))
+    return ATTN_ERR_CUDA;
+  const long long rows = static_cast<long long>(B) * Hq * S;
+  {
+    const long long blocks =
+        std::min<long long>((rows * 32 + 255) / 256, static_cast<long long>(sm_count()) * 16);
+    bwd_tc_delta_kernel<D><<<static_cast<int>(blocks), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta,
+        rows);
+    if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
+  }
+  TcParams p;
+  p.lse = lse;
+  p.delta = delta;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.status = device_status_ptr();
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.S = S;
+  p.causal = causal;
+  p.nT = (S + kTcRows - 1) / kTcRows;
+  p.scale = scale;
+  {
+    auto kern = bwd_tc_kv_kernel<D>;
+    if (!set_smem_attr(reinterpret_cast<const void*>(kern), KvSmem<D>::kBytes)) return ATTN_ERR_CUDA;
+    kern<<<p.nT * B * Hkv, kTcThreads, KvSmem<D>::kBytes, st>>>(tq, tk, tv, to, p);
+    if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
+  }
+  {
+    auto kern = bwd_tc_q_kernel<D>;
+    if (!set_smem_attr(reinterpret_cast<const void*>(kern), QSmem<D>::kBytes)) return ATTN_ERR_CUDA;
+    kern<<<p.nT * B * Hq, kTcThreads, QSmem<D>::kBytes, st>>>(tq, tk, tv, to, p);
+  }
+  return launch_status();
+}
+
+}  // namespace
+
+attn_status_t launch_prefill_backward_tc(const void* q, const void* k, const void* v,
+                                         const void* o, const float* lse, const void* dout,
+                                         void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                                         int S, int D, int causal, float scale, void* ws,
+                                         cudaStream_t st) {
+  float* delta = static_cast<float*>(ws);
+  if (D == 128)
+    return launch_bwd_tc_typed<128>(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, S, causal,
+                                    scale, delta, st);
+  return launch_bwd_tc_typed<64>(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, S, causal, scale,
+                                 delta, st);
+}
+
+}  // namespace attn

@@ -132,6 +132,17 @@ attn_status_t launch_prefill_backward(const void* q, const void* k, const void* 
                                       void* dv, int B, int Hq, int Hkv, int S, int D, int causal,
                                       float scale, void* ws, cudaStream_t st);
 
+// The tcgen05 form of the backward (a dK/dV kernel over key tiles and a dQ kernel over query
+// tiles, no atomics); uses the first Delta part of the backward workspace only.
+attn_status_t launch_prefill_backward_tc(const void* q, const void* k, const void* v,
+                                         const void* o, const float* lse, const void* dout,
+                                         void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                                         int S, int D, int causal, float scale, void* ws,
+                                         cudaStream_t st);
+
+// 0: the default backward (tcgen05), 1: the warp-level mma.sync kernels, 2: tcgen05.
+void force_backward_path(int path);
+
 // q_tiles 1 or 2: every later prefill at D <= 128 runs that many 128-row Q tiles per work item;
 // 0: the default (two).
 void force_prefill_tiles(int q_tiles);

@@ -635,13 +635,19 @@ def variants(b, d):
     bws = torch.empty(b.attn_prefill_backward_workspace_size(4, 32, 4096, 128), dtype=torch.uint8,
                       device="cuda")
     gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    tb = time_call(lambda: b.attn_prefill_backward(q, k, v, o, lse, do, causal=True, dq=gq, dk=gk,
-                                                   dv=gv, workspace=bws), 5, 2)
     bfl = 2.5 * workload.prefill_flops(4, 32, 4096, 128, True)
-    out["backward_causal_d128_s4096"] = {
-        "ms": round(tb, 4), "tflops": round(bfl / tb / 1e9, 1),
-        "frac_of_bf16_burst_peak": round(bfl / tb / 1e9 / measured_peaks()[1], 4),
-        "flops": "2.5 x forward (5 products)", "path": "mma.sync m16n8k16"}
+    bwd = {"flops": "2.5 x forward (5 products)"}
+    for path, name in ((2, "tcgen05"), (1, "mma_sync")):
+        b.attn_set_backward_path(path)
+        try:
+            tb = time_call(lambda: b.attn_prefill_backward(q, k, v, o, lse, do, causal=True, dq=gq,
+                                                           dk=gk, dv=gv, workspace=bws), 5, 2)
+        finally:
+            b.attn_set_backward_path(0)
+        bwd[name] = {"ms": round(tb, 4), "tflops": round(bfl / tb / 1e9, 1),
+                     "frac_of_bf16_burst_peak": round(bfl / tb / 1e9 / measured_peaks()[1], 4)}
+    bwd["default"] = "tcgen05"
+    out["backward_causal_d128_s4096"] = bwd
     del q, k, v, do, o, lse, bws, gq, gk, gv
     # fp8 e5m2 latent cache (half the bytes), batch 128
     Lt = LATENT

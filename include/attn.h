@@ -190,6 +190,17 @@ ATTN_API attn_status_t attn_prefill_backward(const void* q, const void* k, const
                                     attn_stream_t stream);
 
 /*
+ * attn_set_backward_path — which kernels attn_prefill_backward runs.  0: the default (2);
+ * 1: warp-level mma.sync kernels (a dK/dV kernel that adds dQ into an fp32 accumulator with
+ * atomics, then a conversion pass); 2: tcgen05 kernels with TMEM accumulators (a dK/dV kernel
+ * over 128-key tiles and a dQ kernel over 128-row query tiles, no atomics; only the row-sum
+ * part of the workspace is used).  Results agree up to rounding order.  Process-wide; set it
+ * only while no other thread runs a backward.
+ * Errors: INVALID_ARG (path outside 0..2).
+ */
+ATTN_API attn_status_t attn_set_backward_path(int path);
+
+/*
  * attn_prefill_chunk_workspace_size — bytes of device workspace attn_prefill_chunk needs:
  * B*Hq*Sq*D bf16 values (rounded up to 256 bytes) for bf16 with rope = 1 (the chunk's queries
  * rotated once), else 0.  0 for invalid arguments.  Needs no device.

@@ -78,6 +78,8 @@ int main(void) {
     ++failures;
   }
   expect("split hook range", attn_set_decode_splits(-1), ATTN_ERR_INVALID_ARG);
+  expect("backward path range", attn_set_backward_path(3), ATTN_ERR_INVALID_ARG);
+  expect("backward path default", attn_set_backward_path(0), ATTN_OK);
   expect("prefill rotation workspace missing",
          attn_prefill(a, a, a, o, NULL, ATTN_BF16, 1.f, 1.f, 1.f, 4, 32, 8, 16384, 128, 1, 0.f, 1,
                       1e4f, 0, NULL, 0, NULL),

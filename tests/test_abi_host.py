@@ -336,5 +336,8 @@ def test_selftest_and_event_hook_validation(L):
     assert L.attn_set_prefill_tiles(3) == INVALID
     assert L.attn_set_prefill_tiles(-1) == INVALID
     assert L.attn_set_prefill_tiles(0) == OK
+    assert L.attn_set_backward_path(3) == INVALID
+    assert L.attn_set_backward_path(-1) == INVALID
+    assert L.attn_set_backward_path(0) == OK
     if not torch.cuda.is_available():
         assert L.attn_selftest_wait_timeout(10000, _stream()) == NO_DEVICE

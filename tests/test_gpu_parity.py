@@ -662,6 +662,14 @@ def check_grad(gpu, ref, what):
     assert d.mean() <= 5e-3 * mean, f"{what}: mean-abs {d.mean():.3e} > 5e-3 * {mean:.3e}"
 
 
+@pytest.fixture(params=[2, 1], ids=["tcgen05", "mma_sync"])
+def bwd_path(request):
+    """Runs a backward test on each of the two kernel paths, then restores the default."""
+    binding.attn_set_backward_path(request.param)
+    yield request.param
+    binding.attn_set_backward_path(0)
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", [
     (1, 4, 1, 128, 64, True),      # the tiny config's shape
     (2, 4, 2, 300, 128, True),     # GQA, ragged tail (several key tiles, partial last)
@@ -669,8 +677,10 @@ def check_grad(gpu, ref, what):
     (1, 8, 2, 513, 128, True),     # group of 4, one row past whole tiles
     (1, 2, 1, 77, 128, False),     # shorter than one tile
     (1, 1, 1, 1, 64, True),        # S = 1
+    (1, 8, 1, 640, 128, False),    # group of 8, five whole tiles: long step rings, no mask
+    (2, 6, 3, 1000, 64, True),     # group of 2 at D = 64, eight tiles, ragged
 ])
-def test_prefill_backward(B, Hq, Hkv, S, D, causal):
+def test_prefill_backward(B, Hq, Hkv, S, D, causal, bwd_path):
     q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=S + 11)
     do = synthetic.normal((B, Hq, S, D), 5000 + S, "bf16")
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
@@ -683,7 +693,7 @@ def test_prefill_backward(B, Hq, Hkv, S, D, causal):
     check_grad(dv.cpu(), rv, "dV")
 
 
-def test_prefill_backward_equals_finite_difference_direction():
+def test_prefill_backward_equals_finite_difference_direction(bwd_path):
     """A directional derivative of sum(O * W) on the device (forward at q +- h u) agrees with
     <dQ, u> from the backward, independently of the oracle."""
     B, Hq, Hkv, S, D = 1, 2, 1, 96, 64
@@ -720,7 +730,7 @@ def test_rope_apply_inverse(style, dtype, shape):
 
 
 @pytest.mark.parametrize("style", ["half", "interleaved"])
-def test_backward_through_rope(style):
+def test_backward_through_rope(style, bwd_path):
     """RoPE applied by rope_apply, attention, its backward, and the inverse rotation of dQ / dK:
     the gradients with respect to the un-rotated Q and K."""
     B, Hq, Hkv, S, D = 1, 4, 2, 200, 128
