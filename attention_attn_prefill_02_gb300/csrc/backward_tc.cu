@@ -17,15 +17,16 @@
 //                     TMEM: S 128 | dP 128 | dQ D columns.
 //
 // Each step runs in two halves of 64 columns (query columns in the first kernel, key columns in
-// the second): the tensor core computes the scores of half 1 while the four warps turn half 0
-// into P / dS, and the gradient products of half 0 run while they do half 1.
+// the second), one per score warpgroup: warpgroup 0 turns half 0 into P / dS while the tensor
+// core computes the scores of half 1, warpgroup 1 does half 1 while the gradient products of
+// half 0 run, so the exponentials of the two halves overlap each other and the MMAs.
 //
 // Tiles move by TMA in 128-row boxes of 64 bf16 with the 128-byte swizzle; one shared tile
 // serves as a K-major operand (the Q K^T style products) and an MN-major one (the P V style).
-// Warps 0-3 turn scores into P / dS and write the result, warp 4 loads (TMA, plus the per-row
-// log-sum-exp and Delta of each query tile), warp 5 issues the MMAs (the whole warp in the loop,
-// one elected lane issuing).  Every wait is bounded, and warp-uniform where the warp goes on to
-// a .sync.aligned TMEM access.
+// Warps 0-7 turn scores into P / dS and write the result (warp w reads TMEM lanes
+// 32 (w % 4)..), warp 8 loads (TMA, plus the per-row log-sum-exp and Delta of each query tile),
+// warp 9 issues the MMAs (the whole warp in the loop, one elected lane issuing).  Every wait is
+// bounded, and warp-uniform where the warp goes on to a .sync.aligned TMEM access.
 #include <algorithm>
 #include <cmath>
 
@@ -36,8 +37,8 @@ namespace {
 
 constexpr int kTcRows = 128;     // keys per key tile, query rows per query tile (TMEM lanes)
 constexpr int kTcHalf = 64;      // columns per half step
-constexpr int kTcThreads = 192;  // 4 score warps, the load warp, the MMA warp
-constexpr int kTcLoader = 4, kTcMma = 5;
+constexpr int kTcThreads = 320;  // 8 score warps (two warpgroups), the load warp, the MMA warp
+constexpr int kTcLoader = 8, kTcMma = 9;
 constexpr float kTcLog2e = 1.4426950408889634f;
 
 struct TcParams {
@@ -94,14 +95,13 @@ __device__ __forceinline__ void tc_mma_grad(uint32_t d, uint32_t a_tmem, uint64_
   }
 }
 
-// One TMEM lane's D accumulator columns, times `mul`, as a bf16 row at dst (written only when
-// `store`).  Every lane of the warp runs the TMEM loads, which are warp-collective
-// (.sync.aligned): rows past S skip only the global store.
-template <int D>
+// Columns 32 c0 .. 32 c1 - 1 of one TMEM lane's accumulator, times `mul`, as bf16 at the same
+// columns of the row dst (written only when `store`).  Every lane of the warp runs the TMEM
+// loads, which are warp-collective (.sync.aligned): rows past S skip only the global store.
 __device__ __forceinline__ void tc_store_row(__nv_bfloat16* dst, uint32_t taddr, float mul,
-                                             bool store) {
+                                             bool store, int c0, int c1) {
 #pragma unroll 1
-  for (int c = 0; c < D / 32; ++c) {
+  for (int c = c0; c < c1; ++c) {
     uint32_t v[32];
     tmem_ld32(taddr + c * 32, v);
     if (store) {
@@ -235,40 +235,59 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t o_desc0 = smem_desc(smem_u32(smem + L::kO), 16, 1024, 2);
     const uint64_t qg_desc0 = smem_desc(smem_u32(smem + L::kQ), TcTile<D>::kBoxBytes, 1024, 2);
     const uint64_t og_desc0 = smem_desc(smem_u32(smem + L::kO), TcTile<D>::kBoxBytes, 1024, 2);
-    bool ok = mbar_wait_warp(&bars->kv_full, 0, p.status);
-    for (int st = 0; st < steps && ok; ++st) {
-      const int sg = st & 1;
-      const uint64_t so = static_cast<uint64_t>((sg * TcTile<D>::kBytes) >> 4);
-      if (!(ok = mbar_wait_warp(&bars->q_full[sg], (st >> 1) & 1, p.status))) break;
+    auto stage_off = [](int st) {
+      return static_cast<uint64_t>(((st & 1) * TcTile<D>::kBytes) >> 4);
+    };
+    // S^T = K Q^T and dP^T = V dO^T of half h (query columns 64h..) of step st
+    auto issue_scores = [&](int st, int h) {
+      const uint64_t so = stage_off(st);
+      tc_mma_scores<D>(tmem + kColS + h * kTcHalf, k_desc, q_desc0 + so, h * kTcHalf, idesc_s);
+      tc_mma_scores<D>(tmem + kColDP + h * kTcHalf, v_desc, o_desc0 + so, h * kTcHalf, idesc_s);
+      umma_commit_e(&bars->s_full[h]);
+    };
+    // dV += P^T dO, dK += dS^T Q over the 64 query rows of half h; P^T / dS^T of half h sit in
+    // columns 64h..64h+31 (bf16 pairs)
+    auto issue_grads = [&](int st, int h) {
+      const uint64_t so = stage_off(st);
+      const bool acc = st > 0 || h > 0;
+      tc_mma_grad<D>(tmem + kColDV, tmem + kColS + kTcHalf * h, og_desc0 + so, h * kTcHalf, idesc_g, acc);
+      tc_mma_grad<D>(tmem + kColDK, tmem + kColDP + kTcHalf * h, qg_desc0 + so, h * kTcHalf, idesc_g, acc);
+    };
+    // Pipelined order: ... grads h0 (st), scores h0 (st + 1), grads h1 (st), scores h1 (st + 1)
+    // ...: the next step's half-0 scores run while warpgroup 1 works on half 1.  Scores of half
+    // h overwrite the columns the grads of half h read, issued before them (the tensor core
+    // runs one CTA's MMAs in issue order), and only after warpgroup h released them.
+    bool ok = mbar_wait_warp(&bars->kv_full, 0, p.status) &&
+              mbar_wait_warp(&bars->q_full[0], 0, p.status);
+    if (ok) {
       tc_fence_after();
-      // S^T = K Q^T and dP^T = V dO^T, query columns 64h.. of half h.  The previous step's
-      // gradient products, issued before these, read the same columns: the tensor core runs
-      // one CTA's MMAs in issue order.
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tc_mma_scores<D>(tmem + kColS + h * kTcHalf, k_desc, q_desc0 + so, h * kTcHalf, idesc_s);
-        tc_mma_scores<D>(tmem + kColDP + h * kTcHalf, v_desc, o_desc0 + so, h * kTcHalf, idesc_s);
-        umma_commit_e(&bars->s_full[h]);
-      }
-      // dV += P^T dO, dK += dS^T Q over the 64 query rows of each half; P^T / dS^T of half h
-      // sit in columns 32h.. (bf16 pairs)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (!(ok = mbar_wait_warp(&bars->p_full[h], st & 1, p.status))) break;
+      issue_scores(0, 0);
+      issue_scores(0, 1);
+    }
+    for (int st = 0; st < steps && ok; ++st) {
+      const bool next = st + 1 < steps;
+      if (!(ok = mbar_wait_warp(&bars->p_full[0], st & 1, p.status))) break;
+      tc_fence_after();
+      issue_grads(st, 0);
+      if (next) {
+        if (!(ok = mbar_wait_warp(&bars->q_full[(st + 1) & 1], ((st + 1) >> 1) & 1, p.status)))
+          break;
         tc_fence_after();
-        const bool acc = st > 0 || h > 0;
-        tc_mma_grad<D>(tmem + kColDV, tmem + kColS + 32 * h, og_desc0 + so, h * kTcHalf, idesc_g, acc);
-        tc_mma_grad<D>(tmem + kColDK, tmem + kColDP + 32 * h, qg_desc0 + so, h * kTcHalf, idesc_g, acc);
+        issue_scores(st + 1, 0);
       }
-      if (!ok) break;
-      umma_commit_e(&bars->q_empty[sg]);
+      if (!(ok = mbar_wait_warp(&bars->p_full[1], st & 1, p.status))) break;
+      tc_fence_after();
+      issue_grads(st, 1);
+      umma_commit_e(&bars->q_empty[st & 1]);
+      if (next) issue_scores(st + 1, 1);
     }
     if (ok) umma_commit_e(&bars->done);
   } else {
     // ---------------------------------------------------------------- P^T and dS^T, one key row
-    const int kr = warp * 32 + lane;  // warps 0-3: TMEM lane quarters
+    const int h = warp >> 2;             // warpgroup h: half h of every step
+    const int kr = (warp & 3) * 32 + lane;  // TMEM lane quarter warp % 4
     const int key = kv0 + kr;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + kColS, tDP = tmem + lane_off + kColDP;
     const float sl2 = p.scale * kTcLog2e;
     bool ok = true;
@@ -280,57 +299,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // masks: the diagonal tile, and the last query or key tile when S is ragged
       const bool need_mask = (p.causal && qt == tile) || q0 + kTcRows > p.S || kv0 + kTcRows > p.S;
       if (!(ok = mbar_wait_warp(&bars->row_full[sg], (st >> 1) & 1, p.status))) break;
+      if (!(ok = mbar_wait_warp(&bars->s_full[h], st & 1, p.status))) break;
+      tc_fence_after();
       const float* lse_s = s_lse + sg * kTcRows;
       const float* del_s = s_del + sg * kTcRows;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        if (!(ok = mbar_wait_warp(&bars->s_full[h], st & 1, p.status))) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          const int col = h * kTcHalf + c * 32;  // query column of this chunk in the tile
-          uint32_t sv[32], dv[32];
-          tmem_ld32(tS + col, sv);
-          tmem_ld32(tDP + col, dv);
-          uint32_t pp[16], dd[16];
+      for (int c = 0; c < 2; ++c) {
+        const int col = h * kTcHalf + c * 32;  // query column of this chunk in the tile
+        uint32_t sv[32], dv[32];
+        tmem_ld32x2(tS + col, sv, tDP + col, dv);
+        uint32_t pp[16], dd[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + col + e);
-            const float4 d4 = *reinterpret_cast<const float4*>(del_s + col + e);
-            float pr[4] = {fast_exp2(__uint_as_float(sv[e + 0]) * sl2 - l4.x),
-                           fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l4.y),
-                           fast_exp2(__uint_as_float(sv[e + 2]) * sl2 - l4.z),
-                           fast_exp2(__uint_as_float(sv[e + 3]) * sl2 - l4.w)};
-            if (need_mask) {
+        for (int e = 0; e < 32; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + col + e);
+          const float4 d4 = *reinterpret_cast<const float4*>(del_s + col + e);
+          float pr[4] = {fast_exp2(__uint_as_float(sv[e + 0]) * sl2 - l4.x),
+                         fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l4.y),
+                         fast_exp2(__uint_as_float(sv[e + 2]) * sl2 - l4.z),
+                         fast_exp2(__uint_as_float(sv[e + 3]) * sl2 - l4.w)};
+          if (need_mask) {
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int q = q0 + col + e + u;
-                if (!(key < p.S && q < p.S && (!p.causal || key <= q))) pr[u] = 0.f;
-              }
+            for (int u = 0; u < 4; ++u) {
+              const int q = q0 + col + e + u;
+              if (!(key < p.S && q < p.S && (!p.causal || key <= q))) pr[u] = 0.f;
             }
-            pp[e / 2] = pack_bf16(pr[0], pr[1]);
-            pp[e / 2 + 1] = pack_bf16(pr[2], pr[3]);
-            dd[e / 2] = pack_bf16(pr[0] * (__uint_as_float(dv[e + 0]) - d4.x),
-                                  pr[1] * (__uint_as_float(dv[e + 1]) - d4.y));
-            dd[e / 2 + 1] = pack_bf16(pr[2] * (__uint_as_float(dv[e + 2]) - d4.z),
-                                      pr[3] * (__uint_as_float(dv[e + 3]) - d4.w));
           }
-          // bf16 pairs of columns col.. go to col / 2..: columns this thread already read
-          tmem_st16(tS + col / 2, pp);
-          tmem_st16(tDP + col / 2, dd);
+          pp[e / 2] = pack_bf16(pr[0], pr[1]);
+          pp[e / 2 + 1] = pack_bf16(pr[2], pr[3]);
+          dd[e / 2] = pack_bf16(pr[0] * (__uint_as_float(dv[e + 0]) - d4.x),
+                                pr[1] * (__uint_as_float(dv[e + 1]) - d4.y));
+          dd[e / 2 + 1] = pack_bf16(pr[2] * (__uint_as_float(dv[e + 2]) - d4.z),
+                                    pr[3] * (__uint_as_float(dv[e + 3]) - d4.w));
         }
-        if (!ok) break;
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[h]);
+        // bf16 pairs of the half's columns go to its first 32 columns (64 h + 16 c ..): columns
+        // this thread already read, never the other half's
+        tmem_st16(tS + h * kTcHalf + c * 16, pp);
+        tmem_st16(tDP + h * kTcHalf + c * 16, dd);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[h]);
     }
-    // dK = scale * sum dS^T Q and dV, bf16, this thread's key row
+    // warpgroup 0: dK = scale * sum dS^T Q; warpgroup 1: dV; bf16, this thread's key row
     if (ok && (ok = mbar_wait_warp(&bars->done, 0, p.status))) {
       tc_fence_after();
       const size_t row = static_cast<size_t>(bh) * p.S + key;
-      tc_store_row<D>(p.dk + row * D, tmem + lane_off + kColDK, p.scale, key < p.S);
-      tc_store_row<D>(p.dv + row * D, tmem + lane_off + kColDV, 1.f, key < p.S);
+      if (h == 0)
+        tc_store_row(p.dk + row * D, tmem + lane_off + kColDK, p.scale, key < p.S, 0, D / 32);
+      else
+        tc_store_row(p.dv + row * D, tmem + lane_off + kColDV, 1.f, key < p.S, 0, D / 32);
     }
   }
   tc_fence_before();
@@ -429,36 +446,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t k_desc0 = smem_desc(smem_u32(smem + L::kK), 16, 1024, 2);
     const uint64_t v_desc0 = smem_desc(smem_u32(smem + L::kV), 16, 1024, 2);
     const uint64_t kg_desc0 = smem_desc(smem_u32(smem + L::kK), TcTile<D>::kBoxBytes, 1024, 2);
-    bool ok = mbar_wait_warp(&bars->qd_full, 0, p.status);
-    for (int st = 0; st < steps && ok; ++st) {
-      const int sg = st & 1;
-      const uint64_t so = static_cast<uint64_t>((sg * TcTile<D>::kBytes) >> 4);
-      if (!(ok = mbar_wait_warp(&bars->kv_full[sg], (st >> 1) & 1, p.status))) break;
+    auto stage_off = [](int st) {
+      return static_cast<uint64_t>(((st & 1) * TcTile<D>::kBytes) >> 4);
+    };
+    // S = Q K^T and dP = dO V^T of half h (key columns 64h..) of key tile st
+    auto issue_scores = [&](int st, int h) {
+      const uint64_t so = stage_off(st);
+      tc_mma_scores<D>(tmem + kColS + h * kTcHalf, q_desc, k_desc0 + so, h * kTcHalf, idesc_s);
+      tc_mma_scores<D>(tmem + kColDP + h * kTcHalf, o_desc, v_desc0 + so, h * kTcHalf, idesc_s);
+      umma_commit_e(&bars->s_full[h]);
+    };
+    // dQ += dS K over the 64 keys of half h (dS of half h in S columns 64h..64h+31)
+    auto issue_grads = [&](int st, int h) {
+      tc_mma_grad<D>(tmem + kColDQ, tmem + kColS + kTcHalf * h, kg_desc0 + stage_off(st),
+                     h * kTcHalf, idesc_g, st > 0 || h > 0);
+    };
+    // the pipelined order of the dK / dV kernel
+    bool ok = mbar_wait_warp(&bars->qd_full, 0, p.status) &&
+              mbar_wait_warp(&bars->kv_full[0], 0, p.status);
+    if (ok) {
       tc_fence_after();
-      // S = Q K^T and dP = dO V^T, key columns 64h.. of half h
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tc_mma_scores<D>(tmem + kColS + h * kTcHalf, q_desc, k_desc0 + so, h * kTcHalf, idesc_s);
-        tc_mma_scores<D>(tmem + kColDP + h * kTcHalf, o_desc, v_desc0 + so, h * kTcHalf, idesc_s);
-        umma_commit_e(&bars->s_full[h]);
-      }
-      // dQ += dS K over the 64 keys of each half (dS of half h in S columns 32h..)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (!(ok = mbar_wait_warp(&bars->p_full[h], st & 1, p.status))) break;
+      issue_scores(0, 0);
+      issue_scores(0, 1);
+    }
+    for (int st = 0; st < steps && ok; ++st) {
+      const bool next = st + 1 < steps;
+      if (!(ok = mbar_wait_warp(&bars->p_full[0], st & 1, p.status))) break;
+      tc_fence_after();
+      issue_grads(st, 0);
+      if (next) {
+        if (!(ok = mbar_wait_warp(&bars->kv_full[(st + 1) & 1], ((st + 1) >> 1) & 1, p.status)))
+          break;
         tc_fence_after();
-        tc_mma_grad<D>(tmem + kColDQ, tmem + kColS + 32 * h, kg_desc0 + so, h * kTcHalf, idesc_g,
-                       st > 0 || h > 0);
+        issue_scores(st + 1, 0);
       }
-      if (!ok) break;
-      umma_commit_e(&bars->kv_empty[sg]);
+      if (!(ok = mbar_wait_warp(&bars->p_full[1], st & 1, p.status))) break;
+      tc_fence_after();
+      issue_grads(st, 1);
+      umma_commit_e(&bars->kv_empty[st & 1]);
+      if (next) issue_scores(st + 1, 1);
     }
     if (ok) umma_commit_e(&bars->done);
   } else {
     // ---------------------------------------------------------------- dS, one query row
-    const int qr = warp * 32 + lane;
+    const int h = warp >> 2;                // warpgroup h: half h of every step
+    const int qr = (warp & 3) * 32 + lane;  // TMEM lane quarter warp % 4
     const int q = q0 + qr;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + kColS, tDP = tmem + lane_off + kColDP;
     const float sl2 = p.scale * kTcLog2e;
     const size_t row = static_cast<size_t>(bh) * p.S + q;
@@ -468,41 +502,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int st = 0; st < steps && ok; ++st) {
       const int k0 = st * kTcRows;
       const bool need_mask = (p.causal && st == qt) || k0 + kTcRows > p.S || q0 + kTcRows > p.S;
+      if (!(ok = mbar_wait_warp(&bars->s_full[h], st & 1, p.status))) break;
+      tc_fence_after();
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        if (!(ok = mbar_wait_warp(&bars->s_full[h], st & 1, p.status))) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          const int col = h * kTcHalf + c * 32;  // key column of this chunk in the tile
-          uint32_t sv[32], dv[32];
-          tmem_ld32(tS + col, sv);
-          tmem_ld32(tDP + col, dv);
-          uint32_t dd[16];
+      for (int c = 0; c < 2; ++c) {
+        const int col = h * kTcHalf + c * 32;  // key column of this chunk in the tile
+        uint32_t sv[32], dv[32];
+        tmem_ld32x2(tS + col, sv, tDP + col, dv);
+        uint32_t dd[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float p0 = fast_exp2(__uint_as_float(sv[e]) * sl2 - l2);
-            float p1 = fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l2);
-            if (need_mask) {
-              const int k = k0 + col + e;
-              if (!(q < p.S && k < p.S && (!p.causal || k <= q))) p0 = 0.f;
-              if (!(q < p.S && k + 1 < p.S && (!p.causal || k + 1 <= q))) p1 = 0.f;
-            }
-            dd[e / 2] = pack_bf16(p0 * (__uint_as_float(dv[e]) - de),
-                                  p1 * (__uint_as_float(dv[e + 1]) - de));
+        for (int e = 0; e < 32; e += 2) {
+          float p0 = fast_exp2(__uint_as_float(sv[e]) * sl2 - l2);
+          float p1 = fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l2);
+          if (need_mask) {
+            const int k = k0 + col + e;
+            if (!(q < p.S && k < p.S && (!p.causal || k <= q))) p0 = 0.f;
+            if (!(q < p.S && k + 1 < p.S && (!p.causal || k + 1 <= q))) p1 = 0.f;
           }
-          tmem_st16(tS + col / 2, dd);
+          dd[e / 2] = pack_bf16(p0 * (__uint_as_float(dv[e]) - de),
+                                p1 * (__uint_as_float(dv[e + 1]) - de));
         }
-        if (!ok) break;
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[h]);
+        // bf16 pairs into the half's first 32 columns (64 h + 16 c ..), already read
+        tmem_st16(tS + h * kTcHalf + c * 16, dd);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[h]);
     }
-    // dQ = scale * sum dS K, bf16, this thread's query row
+    // dQ = scale * sum dS K, bf16, this thread's query row; warpgroup h writes columns
+    // h D / 2 .. (h + 1) D / 2 - 1
     if (ok && (ok = mbar_wait_warp(&bars->done, 0, p.status))) {
       tc_fence_after();
-      tc_store_row<D>(p.dq + row * D, tmem + lane_off + kColDQ, p.scale, q < p.S);
+      tc_store_row(p.dq + row * D, tmem + lane_off + kColDQ, p.scale, q < p.S, h * (D / 64),
+                   (h + 1) * (D / 64));
     }
   }
   tc_fence_before();
