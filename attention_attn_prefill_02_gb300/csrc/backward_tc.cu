@@ -118,6 +118,57 @@ __device__ __forceinline__ void tc_store_row(__nv_bfloat16* dst, uint32_t taddr,
   }
 }
 
+// P^T and dS^T of one key row over 64 query columns (the dK / dV kernel): p = 2^(s scale log2e -
+// lse log2e) and ds = p (dp - Delta), packed as bf16 pairs.  MASK: zero p where the query is past
+// S or (causal) before the key; without it the body has no branch.
+template <bool MASK>
+__device__ __forceinline__ void kv_scores_half(const uint32_t (&sv)[64], const uint32_t (&dv)[64],
+                                               const float* lse_s, const float* del_s, float sl2,
+                                               int key, int q_first, int S, int causal,
+                                               uint32_t (&pp)[32], uint32_t (&dd)[32]) {
+#pragma unroll
+  for (int e = 0; e < kTcHalf; e += 4) {
+    const float4 l4 = *reinterpret_cast<const float4*>(lse_s + e);
+    const float4 d4 = *reinterpret_cast<const float4*>(del_s + e);
+    float pr[4] = {fast_exp2(__uint_as_float(sv[e + 0]) * sl2 - l4.x),
+                   fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l4.y),
+                   fast_exp2(__uint_as_float(sv[e + 2]) * sl2 - l4.z),
+                   fast_exp2(__uint_as_float(sv[e + 3]) * sl2 - l4.w)};
+    if constexpr (MASK) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = q_first + e + u;
+        if (!(key < S && q < S && (!causal || key <= q))) pr[u] = 0.f;
+      }
+    }
+    pp[e / 2] = pack_bf16(pr[0], pr[1]);
+    pp[e / 2 + 1] = pack_bf16(pr[2], pr[3]);
+    dd[e / 2] = pack_bf16(pr[0] * (__uint_as_float(dv[e + 0]) - d4.x),
+                          pr[1] * (__uint_as_float(dv[e + 1]) - d4.y));
+    dd[e / 2 + 1] = pack_bf16(pr[2] * (__uint_as_float(dv[e + 2]) - d4.z),
+                              pr[3] * (__uint_as_float(dv[e + 3]) - d4.w));
+  }
+}
+
+// dS of one query row over 64 key columns (the dQ kernel), packed as bf16 pairs.  MASK as above
+// with the roles of query and key exchanged.
+template <bool MASK>
+__device__ __forceinline__ void q_scores_half(const uint32_t (&sv)[64], const uint32_t (&dv)[64],
+                                              float sl2, float l2, float de, int q, int k_first,
+                                              int S, int causal, uint32_t (&dd)[32]) {
+#pragma unroll
+  for (int e = 0; e < kTcHalf; e += 2) {
+    float p0 = fast_exp2(__uint_as_float(sv[e]) * sl2 - l2);
+    float p1 = fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l2);
+    if constexpr (MASK) {
+      const int k = k_first + e;
+      if (!(q < S && k < S && (!causal || k <= q))) p0 = 0.f;
+      if (!(q < S && k + 1 < S && (!causal || k + 1 <= q))) p1 = 0.f;
+    }
+    dd[e / 2] = pack_bf16(p0 * (__uint_as_float(dv[e]) - de), p1 * (__uint_as_float(dv[e + 1]) - de));
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // dK, dV
 // ------------------------------------------------------------------------------------------
@@ -205,7 +256,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int sg = st & 1;
       // stage sg is free once the gradient products of step st - 2 completed (they follow the
       // score warps' last read of its log-sum-exp and Delta)
-      if (st >= 2 && !mbar_wait_warp(&bars->q_empty[sg], ((st >> 1) & 1) ^ 1, p.status)) break;
+      if (st >= 2 && !mbar_wait_warp_sleep(&bars->q_empty[sg], ((st >> 1) & 1) ^ 1, p.status)) break;
       int hq, qt;
       step_q(st, hq, qt);
       const int z = b * p.Hq + hq;
@@ -257,8 +308,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ...: the next step's half-0 scores run while warpgroup 1 works on half 1.  Scores of half
     // h overwrite the columns the grads of half h read, issued before them (the tensor core
     // runs one CTA's MMAs in issue order), and only after warpgroup h released them.
-    bool ok = mbar_wait_warp(&bars->kv_full, 0, p.status) &&
-              mbar_wait_warp(&bars->q_full[0], 0, p.status);
+    bool ok = mbar_wait_warp_sleep(&bars->kv_full, 0, p.status) &&
+              mbar_wait_warp_sleep(&bars->q_full[0], 0, p.status);
     if (ok) {
       tc_fence_after();
       issue_scores(0, 0);
@@ -266,16 +317,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int st = 0; st < steps && ok; ++st) {
       const bool next = st + 1 < steps;
-      if (!(ok = mbar_wait_warp(&bars->p_full[0], st & 1, p.status))) break;
+      if (!(ok = mbar_wait_warp_sleep(&bars->p_full[0], st & 1, p.status))) break;
       tc_fence_after();
       issue_grads(st, 0);
       if (next) {
-        if (!(ok = mbar_wait_warp(&bars->q_full[(st + 1) & 1], ((st + 1) >> 1) & 1, p.status)))
+        if (!(ok = mbar_wait_warp_sleep(&bars->q_full[(st + 1) & 1], ((st + 1) >> 1) & 1, p.status)))
           break;
         tc_fence_after();
         issue_scores(st + 1, 0);
       }
-      if (!(ok = mbar_wait_warp(&bars->p_full[1], st & 1, p.status))) break;
+      if (!(ok = mbar_wait_warp_sleep(&bars->p_full[1], st & 1, p.status))) break;
       tc_fence_after();
       issue_grads(st, 1);
       umma_commit_e(&bars->q_empty[st & 1]);
@@ -298,50 +349,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int q0 = qt * kTcRows;
       // masks: the diagonal tile, and the last query or key tile when S is ragged
       const bool need_mask = (p.causal && qt == tile) || q0 + kTcRows > p.S || kv0 + kTcRows > p.S;
-      if (!(ok = mbar_wait_warp(&bars->row_full[sg], (st >> 1) & 1, p.status))) break;
-      if (!(ok = mbar_wait_warp(&bars->s_full[h], st & 1, p.status))) break;
+      if (!(ok = mbar_wait_warp_sleep(&bars->row_full[sg], (st >> 1) & 1, p.status))) break;
+      if (!(ok = mbar_wait_warp_sleep(&bars->s_full[h], st & 1, p.status))) break;
       tc_fence_after();
-      const float* lse_s = s_lse + sg * kTcRows;
-      const float* del_s = s_del + sg * kTcRows;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const int col = h * kTcHalf + c * 32;  // query column of this chunk in the tile
-        uint32_t sv[32], dv[32];
-        tmem_ld32x2(tS + col, sv, tDP + col, dv);
-        uint32_t pp[16], dd[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + col + e);
-          const float4 d4 = *reinterpret_cast<const float4*>(del_s + col + e);
-          float pr[4] = {fast_exp2(__uint_as_float(sv[e + 0]) * sl2 - l4.x),
-                         fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l4.y),
-                         fast_exp2(__uint_as_float(sv[e + 2]) * sl2 - l4.z),
-                         fast_exp2(__uint_as_float(sv[e + 3]) * sl2 - l4.w)};
-          if (need_mask) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int q = q0 + col + e + u;
-              if (!(key < p.S && q < p.S && (!p.causal || key <= q))) pr[u] = 0.f;
-            }
-          }
-          pp[e / 2] = pack_bf16(pr[0], pr[1]);
-          pp[e / 2 + 1] = pack_bf16(pr[2], pr[3]);
-          dd[e / 2] = pack_bf16(pr[0] * (__uint_as_float(dv[e + 0]) - d4.x),
-                                pr[1] * (__uint_as_float(dv[e + 1]) - d4.y));
-          dd[e / 2 + 1] = pack_bf16(pr[2] * (__uint_as_float(dv[e + 2]) - d4.z),
-                                    pr[3] * (__uint_as_float(dv[e + 3]) - d4.w));
-        }
-        // bf16 pairs of the half's columns go to its first 32 columns (64 h + 16 c ..): columns
-        // this thread already read, never the other half's
-        tmem_st16(tS + h * kTcHalf + c * 16, pp);
-        tmem_st16(tDP + h * kTcHalf + c * 16, dd);
-      }
+      const float* lse_s = s_lse + sg * kTcRows + h * kTcHalf;
+      const float* del_s = s_del + sg * kTcRows + h * kTcHalf;
+      // the half's 64 query columns of S^T and dP^T, one wait for both loads
+      uint32_t sv[64], dv[64];
+      tmem_ld64x2(tS + h * kTcHalf, sv, tDP + h * kTcHalf, dv);
+      uint32_t pp[32], dd[32];
+      if (need_mask)
+        kv_scores_half<true>(sv, dv, lse_s, del_s, sl2, key, q0 + h * kTcHalf, p.S, p.causal, pp, dd);
+      else
+        kv_scores_half<false>(sv, dv, lse_s, del_s, sl2, key, q0 + h * kTcHalf, p.S, p.causal, pp, dd);
+      // bf16 pairs into the half's first 32 columns (64 h ..), already read
+      tmem_st32(tS + h * kTcHalf, pp);
+      tmem_st32(tDP + h * kTcHalf, dd);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[h]);
     }
     // warpgroup 0: dK = scale * sum dS^T Q; warpgroup 1: dV; bf16, this thread's key row
-    if (ok && (ok = mbar_wait_warp(&bars->done, 0, p.status))) {
+    if (ok && (ok = mbar_wait_warp_sleep(&bars->done, 0, p.status))) {
       tc_fence_after();
       const size_t row = static_cast<size_t>(bh) * p.S + key;
       if (h == 0)
@@ -430,7 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_load_tile<D>(smem + L::kO, &tmO, &bars->qd_full, q0, bh);
       for (int st = 0; st < steps; ++st) {
         const int sg = st & 1;
-        if (st >= 2 && !mbar_wait(&bars->kv_empty[sg], ((st >> 1) & 1) ^ 1, p.status)) break;
+        if (st >= 2 && !mbar_wait_sleep(&bars->kv_empty[sg], ((st >> 1) & 1) ^ 1, p.status)) break;
         mbar_arrive_expect_tx(&bars->kv_full[sg], 2 * TcTile<D>::kBytes);
         tc_load_tile<D>(smem + L::kK + sg * TcTile<D>::kBytes, &tmK, &bars->kv_full[sg],
                         st * kTcRows, kvz);
@@ -462,8 +491,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      h * kTcHalf, idesc_g, st > 0 || h > 0);
     };
     // the pipelined order of the dK / dV kernel
-    bool ok = mbar_wait_warp(&bars->qd_full, 0, p.status) &&
-              mbar_wait_warp(&bars->kv_full[0], 0, p.status);
+    bool ok = mbar_wait_warp_sleep(&bars->qd_full, 0, p.status) &&
+              mbar_wait_warp_sleep(&bars->kv_full[0], 0, p.status);
     if (ok) {
       tc_fence_after();
       issue_scores(0, 0);
@@ -471,16 +500,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int st = 0; st < steps && ok; ++st) {
       const bool next = st + 1 < steps;
-      if (!(ok = mbar_wait_warp(&bars->p_full[0], st & 1, p.status))) break;
+      if (!(ok = mbar_wait_warp_sleep(&bars->p_full[0], st & 1, p.status))) break;
       tc_fence_after();
       issue_grads(st, 0);
       if (next) {
-        if (!(ok = mbar_wait_warp(&bars->kv_full[(st + 1) & 1], ((st + 1) >> 1) & 1, p.status)))
+        if (!(ok = mbar_wait_warp_sleep(&bars->kv_full[(st + 1) & 1], ((st + 1) >> 1) & 1, p.status)))
           break;
         tc_fence_after();
         issue_scores(st + 1, 0);
       }
-      if (!(ok = mbar_wait_warp(&bars->p_full[1], st & 1, p.status))) break;
+      if (!(ok = mbar_wait_warp_sleep(&bars->p_full[1], st & 1, p.status))) break;
       tc_fence_after();
       issue_grads(st, 1);
       umma_commit_e(&bars->kv_empty[st & 1]);
@@ -502,36 +531,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int st = 0; st < steps && ok; ++st) {
       const int k0 = st * kTcRows;
       const bool need_mask = (p.causal && st == qt) || k0 + kTcRows > p.S || q0 + kTcRows > p.S;
-      if (!(ok = mbar_wait_warp(&bars->s_full[h], st & 1, p.status))) break;
+      if (!(ok = mbar_wait_warp_sleep(&bars->s_full[h], st & 1, p.status))) break;
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const int col = h * kTcHalf + c * 32;  // key column of this chunk in the tile
-        uint32_t sv[32], dv[32];
-        tmem_ld32x2(tS + col, sv, tDP + col, dv);
-        uint32_t dd[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p0 = fast_exp2(__uint_as_float(sv[e]) * sl2 - l2);
-          float p1 = fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l2);
-          if (need_mask) {
-            const int k = k0 + col + e;
-            if (!(q < p.S && k < p.S && (!p.causal || k <= q))) p0 = 0.f;
-            if (!(q < p.S && k + 1 < p.S && (!p.causal || k + 1 <= q))) p1 = 0.f;
-          }
-          dd[e / 2] = pack_bf16(p0 * (__uint_as_float(dv[e]) - de),
-                                p1 * (__uint_as_float(dv[e + 1]) - de));
-        }
-        // bf16 pairs into the half's first 32 columns (64 h + 16 c ..), already read
-        tmem_st16(tS + h * kTcHalf + c * 16, dd);
-      }
+      // the half's 64 key columns of S and dP, one wait for both loads
+      uint32_t sv[64], dv[64];
+      tmem_ld64x2(tS + h * kTcHalf, sv, tDP + h * kTcHalf, dv);
+      uint32_t dd[32];
+      if (need_mask)
+        q_scores_half<true>(sv, dv, sl2, l2, de, q, k0 + h * kTcHalf, p.S, p.causal, dd);
+      else
+        q_scores_half<false>(sv, dv, sl2, l2, de, q, k0 + h * kTcHalf, p.S, p.causal, dd);
+      // bf16 pairs into the half's first 32 columns (64 h ..), already read
+      tmem_st32(tS + h * kTcHalf, dd);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[h]);
     }
     // dQ = scale * sum dS K, bf16, this thread's query row; warpgroup h writes columns
     // h D / 2 .. (h + 1) D / 2 - 1
-    if (ok && (ok = mbar_wait_warp(&bars->done, 0, p.status))) {
+    if (ok && (ok = mbar_wait_warp_sleep(&bars->done, 0, p.status))) {
       tc_fence_after();
       tc_store_row(p.dq + row * D, tmem + lane_off + kColDQ, p.scale, q < p.S, h * (D / 64),
                    (h + 1) * (D / 64));
