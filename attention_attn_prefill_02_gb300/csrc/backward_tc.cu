@@ -118,54 +118,63 @@ __device__ __forceinline__ void tc_store_row(__nv_bfloat16* dst, uint32_t taddr,
   }
 }
 
-// P^T and dS^T of one key row over 64 query columns (the dK / dV kernel): p = 2^(s scale log2e -
-// lse log2e) and ds = p (dp - Delta), packed as bf16 pairs.  MASK: zero p where the query is past
-// S or (causal) before the key; without it the body has no branch.
+// P^T and dS^T of one key row over 32 query columns (the dK / dV kernel): p = 2^(s scale log2e -
+// lse log2e) and ds = p (dp - Delta), packed as bf16 pairs, in paired f32x2 arithmetic.  nl_s /
+// nd_s: -lse log2e and -Delta of the 32 queries.  MASK: zero p where the query is past S or
+// (causal) before the key; without it the body has no branch.
 template <bool MASK>
-__device__ __forceinline__ void kv_scores_half(const uint32_t (&sv)[64], const uint32_t (&dv)[64],
-                                               const float* lse_s, const float* del_s, float sl2,
-                                               int key, int q_first, int S, int causal,
-                                               uint32_t (&pp)[32], uint32_t (&dd)[32]) {
+__device__ __forceinline__ void kv_scores_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+                                                const float* nl_s, const float* nd_s, float sl2,
+                                                int key, int q_first, int S, int causal,
+                                                uint32_t (&pp)[16], uint32_t (&dd)[16]) {
+  const float2 c2 = make_float2(sl2, sl2);
 #pragma unroll
-  for (int e = 0; e < kTcHalf; e += 4) {
-    const float4 l4 = *reinterpret_cast<const float4*>(lse_s + e);
-    const float4 d4 = *reinterpret_cast<const float4*>(del_s + e);
-    float pr[4] = {fast_exp2(__uint_as_float(sv[e + 0]) * sl2 - l4.x),
-                   fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l4.y),
-                   fast_exp2(__uint_as_float(sv[e + 2]) * sl2 - l4.z),
-                   fast_exp2(__uint_as_float(sv[e + 3]) * sl2 - l4.w)};
+  for (int e = 0; e < 32; e += 4) {
+    const float4 l4 = *reinterpret_cast<const float4*>(nl_s + e);
+    const float4 d4 = *reinterpret_cast<const float4*>(nd_s + e);
+    float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2,
+                           make_float2(l4.x, l4.y));
+    float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), c2,
+                           make_float2(l4.z, l4.w));
+    x0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+    x1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
     if constexpr (MASK) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int q = q_first + e + u;
-        if (!(key < S && q < S && (!causal || key <= q))) pr[u] = 0.f;
-      }
+      const int q = q_first + e;
+      const bool kin = key < S;
+      if (!(kin && q < S && (!causal || key <= q))) x0.x = 0.f;
+      if (!(kin && q + 1 < S && (!causal || key <= q + 1))) x0.y = 0.f;
+      if (!(kin && q + 2 < S && (!causal || key <= q + 2))) x1.x = 0.f;
+      if (!(kin && q + 3 < S && (!causal || key <= q + 3))) x1.y = 0.f;
     }
-    pp[e / 2] = pack_bf16(pr[0], pr[1]);
-    pp[e / 2 + 1] = pack_bf16(pr[2], pr[3]);
-    dd[e / 2] = pack_bf16(pr[0] * (__uint_as_float(dv[e + 0]) - d4.x),
-                          pr[1] * (__uint_as_float(dv[e + 1]) - d4.y));
-    dd[e / 2 + 1] = pack_bf16(pr[2] * (__uint_as_float(dv[e + 2]) - d4.z),
-                              pr[3] * (__uint_as_float(dv[e + 3]) - d4.w));
+    const float2 g0 = __fmul2_rn(x0, __fadd2_rn(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                                make_float2(d4.x, d4.y)));
+    const float2 g1 = __fmul2_rn(x1, __fadd2_rn(make_float2(__uint_as_float(dv[e + 2]), __uint_as_float(dv[e + 3])),
+                                                make_float2(d4.z, d4.w)));
+    pp[e / 2] = pack_bf16(x0.x, x0.y);
+    pp[e / 2 + 1] = pack_bf16(x1.x, x1.y);
+    dd[e / 2] = pack_bf16(g0.x, g0.y);
+    dd[e / 2 + 1] = pack_bf16(g1.x, g1.y);
   }
 }
 
-// dS of one query row over 64 key columns (the dQ kernel), packed as bf16 pairs.  MASK as above
-// with the roles of query and key exchanged.
+// dS of one query row over 64 key columns (the dQ kernel), packed as bf16 pairs.  nl2 / nde:
+// -lse log2e and -Delta of the row.  MASK as above with the roles of query and key exchanged.
 template <bool MASK>
 __device__ __forceinline__ void q_scores_half(const uint32_t (&sv)[64], const uint32_t (&dv)[64],
-                                              float sl2, float l2, float de, int q, int k_first,
+                                              float sl2, float nl2, float nde, int q, int k_first,
                                               int S, int causal, uint32_t (&dd)[32]) {
+  const float2 c2 = make_float2(sl2, sl2), l2 = make_float2(nl2, nl2), d2 = make_float2(nde, nde);
 #pragma unroll
   for (int e = 0; e < kTcHalf; e += 2) {
-    float p0 = fast_exp2(__uint_as_float(sv[e]) * sl2 - l2);
-    float p1 = fast_exp2(__uint_as_float(sv[e + 1]) * sl2 - l2);
+    float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, l2);
+    x = make_float2(fast_exp2(x.x), fast_exp2(x.y));
     if constexpr (MASK) {
       const int k = k_first + e;
-      if (!(q < S && k < S && (!causal || k <= q))) p0 = 0.f;
-      if (!(q < S && k + 1 < S && (!causal || k + 1 <= q))) p1 = 0.f;
+      if (!(q < S && k < S && (!causal || k <= q))) x.x = 0.f;
+      if (!(q < S && k + 1 < S && (!causal || k + 1 <= q))) x.y = 0.f;
     }
-    dd[e / 2] = pack_bf16(p0 * (__uint_as_float(dv[e]) - de), p1 * (__uint_as_float(dv[e + 1]) - de));
+    const float2 g = __fmul2_rn(x, __fadd2_rn(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), d2));
+    dd[e / 2] = pack_bf16(g.x, g.y);
   }
 }
 
@@ -180,8 +189,8 @@ struct KvSmem {
   static constexpr int kV = kK + T::kBytes;
   static constexpr int kQ = kV + T::kBytes;            // two stages
   static constexpr int kO = kQ + 2 * T::kBytes;        // two stages (dO)
-  static constexpr int kLse = kO + 2 * T::kBytes;      // [2][128] LSE * log2e
-  static constexpr int kDel = kLse + 2 * kTcRows * 4;  // [2][128] Delta
+  static constexpr int kLse = kO + 2 * T::kBytes;      // [2][128] -LSE * log2e
+  static constexpr int kDel = kLse + 2 * kTcRows * 4;  // [2][128] -Delta
   static constexpr int kBar = kDel + 2 * kTcRows * 4;
   // at least 120 KB so that one CTA (and one 512-column TMEM allocation) runs per SM
   static constexpr int kBytes = std::max(kBar + 256 + 1024, 120 * 1024);
@@ -271,9 +280,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int i = 0; i < kTcRows / 32; ++i) {
         const int r = i * 32 + lane, q = qt * kTcRows + r;
-        // rows past S: P = 0 through an infinite log-sum-exp (their scores are masked as well)
-        s_lse[sg * kTcRows + r] = q < p.S ? __ldg(p.lse + rbase + q) * kTcLog2e : INFINITY;
-        s_del[sg * kTcRows + r] = q < p.S ? __ldg(p.delta + rbase + q) : 0.f;
+        // stored negated (-lse log2e, -Delta); rows past S: P = 0 through an infinite
+        // log-sum-exp (their scores are masked as well)
+        s_lse[sg * kTcRows + r] = q < p.S ? -__ldg(p.lse + rbase + q) * kTcLog2e : -INFINITY;
+        s_del[sg * kTcRows + r] = q < p.S ? -__ldg(p.delta + rbase + q) : 0.f;
       }
       mbar_arrive(&bars->row_full[sg]);
     }
@@ -354,17 +364,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const float* lse_s = s_lse + sg * kTcRows + h * kTcHalf;
       const float* del_s = s_del + sg * kTcRows + h * kTcHalf;
-      // the half's 64 query columns of S^T and dP^T, one wait for both loads
-      uint32_t sv[64], dv[64];
-      tmem_ld64x2(tS + h * kTcHalf, sv, tDP + h * kTcHalf, dv);
-      uint32_t pp[32], dd[32];
-      if (need_mask)
-        kv_scores_half<true>(sv, dv, lse_s, del_s, sl2, key, q0 + h * kTcHalf, p.S, p.causal, pp, dd);
-      else
-        kv_scores_half<false>(sv, dv, lse_s, del_s, sl2, key, q0 + h * kTcHalf, p.S, p.causal, pp, dd);
-      // bf16 pairs into the half's first 32 columns (64 h ..), already read
-      tmem_st32(tS + h * kTcHalf, pp);
-      tmem_st32(tDP + h * kTcHalf, dd);
+      // the half's 64 query columns of S^T and dP^T in two chunks of 32 (one wait per chunk)
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        const int col = h * kTcHalf + c * 32;
+        uint32_t sv[32], dv[32];
+        tmem_ld32x2(tS + col, sv, tDP + col, dv);
+        uint32_t pp[16], dd[16];
+        if (need_mask)
+          kv_scores_chunk<true>(sv, dv, lse_s + c * 32, del_s + c * 32, sl2, key, q0 + col, p.S,
+                                p.causal, pp, dd);
+        else
+          kv_scores_chunk<false>(sv, dv, lse_s + c * 32, del_s + c * 32, sl2, key, q0 + col, p.S,
+                                 p.causal, pp, dd);
+        // bf16 pairs into the half's first 32 columns (64 h + 16 c ..), columns already read
+        tmem_st16(tS + h * kTcHalf + c * 16, pp);
+        tmem_st16(tDP + h * kTcHalf + c * 16, dd);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[h]);
@@ -525,8 +541,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tS = tmem + lane_off + kColS, tDP = tmem + lane_off + kColDP;
     const float sl2 = p.scale * kTcLog2e;
     const size_t row = static_cast<size_t>(bh) * p.S + q;
-    const float l2 = q < p.S ? __ldg(p.lse + row) * kTcLog2e : INFINITY;
-    const float de = q < p.S ? __ldg(p.delta + row) : 0.f;
+    const float nl2 = q < p.S ? -__ldg(p.lse + row) * kTcLog2e : -INFINITY;
+    const float nde = q < p.S ? -__ldg(p.delta + row) : 0.f;
     bool ok = true;
     for (int st = 0; st < steps && ok; ++st) {
       const int k0 = st * kTcRows;
@@ -538,9 +554,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_ld64x2(tS + h * kTcHalf, sv, tDP + h * kTcHalf, dv);
       uint32_t dd[32];
       if (need_mask)
-        q_scores_half<true>(sv, dv, sl2, l2, de, q, k0 + h * kTcHalf, p.S, p.causal, dd);
+        q_scores_half<true>(sv, dv, sl2, nl2, nde, q, k0 + h * kTcHalf, p.S, p.causal, dd);
       else
-        q_scores_half<false>(sv, dv, sl2, l2, de, q, k0 + h * kTcHalf, p.S, p.causal, dd);
+        q_scores_half<false>(sv, dv, sl2, nl2, nde, q, k0 + h * kTcHalf, p.S, p.causal, dd);
       // bf16 pairs into the half's first 32 columns (64 h ..), already read
       tmem_st32(tS + h * kTcHalf, dd);
       tmem_wait_st();
