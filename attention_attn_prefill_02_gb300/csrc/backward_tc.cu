@@ -413,15 +413,18 @@ struct QSmem {
   using T = TcTile<D>;
   static constexpr int kQ = 0;
   static constexpr int kO = kQ + T::kBytes;
-  static constexpr int kK = kO + T::kBytes;      // two stages
-  static constexpr int kV = kK + 2 * T::kBytes;  // two stages
-  static constexpr int kBar = kV + 2 * T::kBytes;
+  static constexpr int kKStages = 3, kVStages = 2;
+  // K is read by the scores and the dQ products, V by the scores only: V stages free earlier,
+  // so K gets the extra stage (the loads of a stage have about two steps to land)
+  static constexpr int kK = kO + T::kBytes;
+  static constexpr int kV = kK + kKStages * T::kBytes;
+  static constexpr int kBar = kV + kVStages * T::kBytes;
   static constexpr int kBytes = std::max(kBar + 256 + 1024, 120 * 1024);
   static_assert(kBytes <= 232448, "shared memory per CTA");
 };
 
 struct QBars {
-  uint64_t qd_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], done;
+  uint64_t qd_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], done;
   uint32_t tmem_slot;
 };
 static_assert(sizeof(QBars) <= 256, "barrier block");
@@ -450,10 +453,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->qd_full, 1);
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars->kv_full[t], 1);
-      mbar_init(&bars->kv_empty[t], 1);
+      mbar_init(&bars->v_full[t], 1);
+      mbar_init(&bars->v_empty[t], 1);
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 128);
+    }
+    for (int t = 0; t < 3; ++t) {
+      mbar_init(&bars->k_full[t], 1);
+      mbar_init(&bars->k_empty[t], 1);
     }
     mbar_init(&bars->done, 1);
     fence_barrier_init();
@@ -474,12 +481,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_load_tile<D>(smem + L::kQ, &tmQ, &bars->qd_full, q0, bh);
       tc_load_tile<D>(smem + L::kO, &tmO, &bars->qd_full, q0, bh);
       for (int st = 0; st < steps; ++st) {
-        const int sg = st & 1;
-        if (st >= 2 && !mbar_wait_sleep(&bars->kv_empty[sg], ((st >> 1) & 1) ^ 1, p.status)) break;
-        mbar_arrive_expect_tx(&bars->kv_full[sg], 2 * TcTile<D>::kBytes);
-        tc_load_tile<D>(smem + L::kK + sg * TcTile<D>::kBytes, &tmK, &bars->kv_full[sg],
+        // K stage st % 3 (free once the dQ products of step st - 3 completed), V stage st % 2
+        // (free once the scores of step st - 2 completed)
+        const int ks = st % L::kKStages, vs = st & 1;
+        if (st >= L::kKStages &&
+            !mbar_wait_sleep(&bars->k_empty[ks], ((st / L::kKStages) & 1) ^ 1, p.status))
+          break;
+        mbar_arrive_expect_tx(&bars->k_full[ks], TcTile<D>::kBytes);
+        tc_load_tile<D>(smem + L::kK + ks * TcTile<D>::kBytes, &tmK, &bars->k_full[ks],
                         st * kTcRows, kvz);
-        tc_load_tile<D>(smem + L::kV + sg * TcTile<D>::kBytes, &tmV, &bars->kv_full[sg],
+        if (st >= L::kVStages && !mbar_wait_sleep(&bars->v_empty[vs], ((st >> 1) & 1) ^ 1, p.status))
+          break;
+        mbar_arrive_expect_tx(&bars->v_full[vs], TcTile<D>::kBytes);
+        tc_load_tile<D>(smem + L::kV + vs * TcTile<D>::kBytes, &tmV, &bars->v_full[vs],
                         st * kTcRows, kvz);
       }
     }
@@ -491,28 +505,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t k_desc0 = smem_desc(smem_u32(smem + L::kK), 16, 1024, 2);
     const uint64_t v_desc0 = smem_desc(smem_u32(smem + L::kV), 16, 1024, 2);
     const uint64_t kg_desc0 = smem_desc(smem_u32(smem + L::kK), TcTile<D>::kBoxBytes, 1024, 2);
-    auto stage_off = [](int st) {
-      return static_cast<uint64_t>(((st & 1) * TcTile<D>::kBytes) >> 4);
+    auto k_off = [](int st) {
+      return static_cast<uint64_t>(((st % L::kKStages) * TcTile<D>::kBytes) >> 4);
     };
+    auto v_off = [](int st) { return static_cast<uint64_t>(((st & 1) * TcTile<D>::kBytes) >> 4); };
     // S = Q K^T and dP = dO V^T of half h (key columns 64h..) of key tile st
     auto issue_scores = [&](int st, int h) {
-      const uint64_t so = stage_off(st);
-      tc_mma_scores<D>(tmem + kColS + h * kTcHalf, q_desc, k_desc0 + so, h * kTcHalf, idesc_s);
-      tc_mma_scores<D>(tmem + kColDP + h * kTcHalf, o_desc, v_desc0 + so, h * kTcHalf, idesc_s);
+      tc_mma_scores<D>(tmem + kColS + h * kTcHalf, q_desc, k_desc0 + k_off(st), h * kTcHalf, idesc_s);
+      tc_mma_scores<D>(tmem + kColDP + h * kTcHalf, o_desc, v_desc0 + v_off(st), h * kTcHalf, idesc_s);
       umma_commit_e(&bars->s_full[h]);
     };
     // dQ += dS K over the 64 keys of half h (dS of half h in S columns 64h..64h+31)
     auto issue_grads = [&](int st, int h) {
-      tc_mma_grad<D>(tmem + kColDQ, tmem + kColS + kTcHalf * h, kg_desc0 + stage_off(st),
+      tc_mma_grad<D>(tmem + kColDQ, tmem + kColS + kTcHalf * h, kg_desc0 + k_off(st),
                      h * kTcHalf, idesc_g, st > 0 || h > 0);
     };
-    // the pipelined order of the dK / dV kernel
-    bool ok = mbar_wait_warp_sleep(&bars->qd_full, 0, p.status) &&
-              mbar_wait_warp_sleep(&bars->kv_full[0], 0, p.status);
+    // K and V of key tile st landed
+    auto wait_kv = [&](int st) {
+      return mbar_wait_warp_sleep(&bars->k_full[st % L::kKStages], (st / L::kKStages) & 1, p.status) &&
+             mbar_wait_warp_sleep(&bars->v_full[st & 1], (st >> 1) & 1, p.status);
+    };
+    // the pipelined order of the dK / dV kernel; V stage of step st is released once both
+    // halves of its scores completed, the K stage once its dQ products did
+    bool ok = mbar_wait_warp_sleep(&bars->qd_full, 0, p.status) && wait_kv(0);
     if (ok) {
       tc_fence_after();
       issue_scores(0, 0);
       issue_scores(0, 1);
+      umma_commit_e(&bars->v_empty[0]);
     }
     for (int st = 0; st < steps && ok; ++st) {
       const bool next = st + 1 < steps;
@@ -520,16 +540,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       issue_grads(st, 0);
       if (next) {
-        if (!(ok = mbar_wait_warp_sleep(&bars->kv_full[(st + 1) & 1], ((st + 1) >> 1) & 1, p.status)))
-          break;
+        if (!(ok = wait_kv(st + 1))) break;
         tc_fence_after();
         issue_scores(st + 1, 0);
       }
       if (!(ok = mbar_wait_warp_sleep(&bars->p_full[1], st & 1, p.status))) break;
       tc_fence_after();
       issue_grads(st, 1);
-      umma_commit_e(&bars->kv_empty[st & 1]);
-      if (next) issue_scores(st + 1, 1);
+      umma_commit_e(&bars->k_empty[st % L::kKStages]);
+      if (next) {
+        issue_scores(st + 1, 1);
+        umma_commit_e(&bars->v_empty[(st + 1) & 1]);
+      }
     }
     if (ok) umma_commit_e(&bars->done);
   } else {
