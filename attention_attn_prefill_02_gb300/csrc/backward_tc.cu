@@ -75,11 +75,13 @@ __device__ __forceinline__ void tc_load_tile(uint8_t* dst, const CUtensorMap* tm
 template <int D>
 __device__ __forceinline__ void tc_mma_scores(uint32_t d, uint64_t a0, uint64_t b0, int b_row0,
                                               uint32_t idesc) {
-  const uint64_t b_off = static_cast<uint64_t>((b_row0 * 128) >> 4);  // 8-row groups stay whole
+  const uint64_t b1 = b0 + static_cast<uint64_t>((b_row0 * 128) >> 4);  // 8-row groups stay whole
+  // one 64-column box (four K steps of 32 bytes) per batch of four MMAs
 #pragma unroll
-  for (int kk = 0; kk < TcTile<D>::kKSteps; ++kk) {
-    const uint64_t off = ((kk / 4) * TcTile<D>::kBoxBytes + (kk % 4) * 32) >> 4;
-    umma_ss_e(d, a0 + off, b0 + b_off + off, idesc, kk > 0);
+  for (int bx = 0; bx < TcTile<D>::kBoxes; ++bx) {
+    const uint64_t o = static_cast<uint64_t>((bx * TcTile<D>::kBoxBytes) >> 4);
+    umma_ss_x4(d, a0 + o, b1 + o, a0 + o + 2, b1 + o + 2, a0 + o + 4, b1 + o + 4, a0 + o + 6,
+               b1 + o + 6, idesc, bx > 0);
   }
 }
 
@@ -88,11 +90,10 @@ __device__ __forceinline__ void tc_mma_scores(uint32_t d, uint64_t a0, uint64_t 
 template <int D>
 __device__ __forceinline__ void tc_mma_grad(uint32_t d, uint32_t a_tmem, uint64_t x0, int r0,
                                             uint32_t idesc, bool acc) {
-#pragma unroll
-  for (int kk = 0; kk < kTcHalf / 16; ++kk) {
-    const uint64_t off = static_cast<uint64_t>(((r0 + kk * 16) * 128) >> 4);
-    umma_ts_e(d, a_tmem + kk * 8, x0 + off, idesc, (acc || kk > 0) ? 1u : 0u);
-  }
+  // four K steps of 16 rows (2048 bytes of the tile, 8 TMEM columns of A each), one batch
+  const uint64_t x = x0 + static_cast<uint64_t>((r0 * 128) >> 4);
+  umma_ts_x4(d, a_tmem, x, a_tmem + 8, x + 128, a_tmem + 16, x + 256, a_tmem + 24, x + 384, idesc,
+             acc ? 1u : 0u);
 }
 
 // Columns 32 c0 .. 32 c1 - 1 of one TMEM lane's accumulator, times `mul`, as bf16 at the same
