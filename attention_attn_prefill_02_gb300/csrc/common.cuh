@@ -382,6 +382,16 @@ __device__ __forceinline__ void umma_ss_x2(uint32_t d, uint64_t a0, uint64_t b0,
       : "memory");
 }
 
+__device__ __forceinline__ void umma_ss_f8_x2(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1, uint64_t b1, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 t, %6, %6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %5, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %4, %5, t;\n\t""}" ::"r"(d), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_commit_e(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"

@@ -23,6 +23,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -229,6 +230,47 @@ __device__ __forceinline__ void rope_rotate_row_fp8_to_bf16(const uint8_t* st, u
 
 // RM, the RoPE mode: 0 none; 1 Q and K rotated inside (the softmax warps rotate each Q tile as
 // it lands, the RoPE warps every K tile).
+// MMAs of K steps k0 .. K1 - 1 into D[d], issued in batches of four (then two, then one) under
+// one elect each.  a(kk): the A operand of step kk (a shared-memory descriptor, or a TMEM address
+// when TS); b(kk): the B descriptor.  The first MMA accumulates when `acc`, the rest always.
+template <bool F8, bool TS, int K0, int K1, typename AF, typename BF>
+__device__ __forceinline__ void issue_batched(uint32_t d, AF a, BF b, uint32_t idesc, bool acc) {
+  constexpr int kN = K1 - K0;
+  constexpr int k4 = K0 + kN / 4 * 4, k2 = k4 + (K1 - k4) / 2 * 2;
+#pragma unroll
+  for (int kk = K0; kk < k4; kk += 4) {
+    const uint32_t ac = (acc || kk > K0) ? 1u : 0u;
+    if constexpr (TS) {
+      if constexpr (F8) umma_ts_f8_x4(d, a(kk), b(kk), a(kk + 1), b(kk + 1), a(kk + 2), b(kk + 2), a(kk + 3), b(kk + 3), idesc, ac);
+      else umma_ts_x4(d, a(kk), b(kk), a(kk + 1), b(kk + 1), a(kk + 2), b(kk + 2), a(kk + 3), b(kk + 3), idesc, ac);
+    } else {
+      if constexpr (F8) umma_ss_f8_x4(d, a(kk), b(kk), a(kk + 1), b(kk + 1), a(kk + 2), b(kk + 2), a(kk + 3), b(kk + 3), idesc, ac);
+      else umma_ss_x4(d, a(kk), b(kk), a(kk + 1), b(kk + 1), a(kk + 2), b(kk + 2), a(kk + 3), b(kk + 3), idesc, ac);
+    }
+  }
+#pragma unroll
+  for (int kk = k4; kk < k2; kk += 2) {
+    const uint32_t ac = (acc || kk > K0) ? 1u : 0u;
+    if constexpr (TS) {
+      if constexpr (F8) umma_ts_f8_x2(d, a(kk), b(kk), a(kk + 1), b(kk + 1), idesc, ac);
+      else umma_ts_x2(d, a(kk), b(kk), a(kk + 1), b(kk + 1), idesc, ac);
+    } else {
+      if constexpr (F8) umma_ss_f8_x2(d, a(kk), b(kk), a(kk + 1), b(kk + 1), idesc, ac);
+      else umma_ss_x2(d, a(kk), b(kk), a(kk + 1), b(kk + 1), idesc, ac);
+    }
+  }
+  if constexpr (k2 < K1) {
+    const uint32_t ac = (acc || k2 > K0) ? 1u : 0u;
+    if constexpr (TS) {
+      if constexpr (F8) umma_ts_f8_e(d, a(k2), b(k2), idesc, ac);
+      else umma_ts_e(d, a(k2), b(k2), idesc, ac);
+    } else {
+      if constexpr (F8) umma_ss_f8_e(d, a(k2), b(k2), idesc, ac);
+      else umma_ss_e(d, a(k2), b(k2), idesc, ac);
+    }
+  }
+}
+
 template <int D, int RM, int ESZ, int NTT>
 __global__ void __launch_bounds__(threads_for(RM), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -387,43 +429,29 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
         const uint64_t ad = q_desc0 + static_cast<uint64_t>((t * C::kQTileBytes) >> 4);
         const uint64_t bd = k_desc0 + static_cast<uint64_t>((slot * C::kKVTileBytes) >> 4);
         const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
-#pragma unroll
-        for (int kk = 0; kk < C::kKSteps; ++kk) {
-          constexpr int kPerBox = C::kSwz / 32;
-          const uint64_t off = ((kk / kPerBox) * C::kBoxBytes + (kk % kPerBox) * 32) >> 4;
-          if constexpr (C::kQKE == 1)
-            umma_ss_f8_e(d, ad + off, bd + off, idesc_s, kk > 0);
-          else
-            umma_ss_e(d, ad + off, bd + off, idesc_s, kk > 0);
-        }
+        constexpr int kPerBox = C::kSwz / 32;
+        auto off = [](int kk) {
+          return static_cast<uint64_t>(((kk / kPerBox) * C::kBoxBytes + (kk % kPerBox) * 32) >> 4);
+        };
+        issue_batched<C::kQKE == 1, false, 0, C::kKSteps>(
+            d, [&](int kk) { return ad + off(kk); }, [&](int kk) { return bd + off(kk); }, idesc_s,
+            false);
       };
       // the P V products of P columns [k0, k1) (k steps of 16 bf16 / 32 fp8 keys)
-      auto issue_pv_part = [&](int t, int slot, bool acc, int k0, int k1) {
+      auto issue_pv_part = [&](int t, int slot, bool acc, auto k0c, auto k1c) {
+        constexpr int k0 = decltype(k0c)::value, k1 = decltype(k1c)::value;
         const uint64_t bd = v_desc0 + static_cast<uint64_t>((slot * C::kVTileBytes) >> 4);
         const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0) + kPCol;
         const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
-#pragma unroll
-        for (int kk = k0; kk < k1; ++kk) {
-          const uint64_t off = (kk * C::kPVKeys * C::kVSwz) >> 4;
-          if constexpr (FP8)
-            umma_ts_f8_e(d, pcol + kk * 8, bd + off, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-          else
-            umma_ts_e(d, pcol + kk * 8, bd + off, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-        }
+        issue_batched<FP8, true, k0, k1>(
+            d, [&](int kk) { return pcol + kk * 8; },
+            [&](int kk) { return bd + static_cast<uint64_t>((kk * C::kPVKeys * C::kVSwz) >> 4); },
+            idesc_pv, acc || k0 > 0);
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint64_t bd = v_desc0 + static_cast<uint64_t>((slot * C::kVTileBytes) >> 4);
-        const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0) + kPCol;
-        const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
-#pragma unroll
-        for (int kk = 0; kk < C::kPVSteps; ++kk) {
-          // P: 8 TMEM columns per step (16 bf16 or 32 fp8 keys); V rows of kSwz bytes per key
-          const uint64_t off = (kk * C::kPVKeys * C::kVSwz) >> 4;
-          if constexpr (FP8)
-            umma_ts_f8_e(d, pcol + kk * 8, bd + off, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-          else
-            umma_ts_e(d, pcol + kk * 8, bd + off, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-        }
+        // P: 8 TMEM columns per step (16 bf16 or 32 fp8 keys); V rows of kVSwz bytes per key
+        issue_pv_part(t, slot, acc, std::integral_constant<int, 0>{},
+                      std::integral_constant<int, C::kPVSteps>{});
       };
       for (int r = 0; r < rounds && ok; ++r) {
         const int it = item_for(r, blockIdx.x, gridDim.x);
@@ -481,12 +509,14 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
                 }
                 if (!ok) continue;
                 tc_fence_after();
-                issue_pv_part(t, vslot, j > 1, 0, C::kPVSteps / 2);
+                issue_pv_part(t, vslot, j > 1, std::integral_constant<int, 0>{},
+                              std::integral_constant<int, C::kPVSteps / 2>{});
                 ok = mbar_wait_warp(&bars->p_hi[t], ph_pf[t], p.status);
                 ph_pf[t] ^= 1;
                 if (!ok) continue;
                 tc_fence_after();
-                issue_pv_part(t, vslot, true, C::kPVSteps / 2, C::kPVSteps);
+                issue_pv_part(t, vslot, true, std::integral_constant<int, C::kPVSteps / 2>{},
+                              std::integral_constant<int, C::kPVSteps>{});
                 if (j - 1 == n[t] - 1) umma_commit_e(&bars->o_full[t]);
               }
             } else {
