@@ -533,13 +533,15 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
                 if (j - 1 == n[t] - 1) umma_commit_e(&bars->o_full[t]);
               }
             }
+            // V stage free once the last tile's P V products completed (committed before that
+            // tile's next QK^T, which the commit would otherwise also wait for)
+            if (t == NT - 1) umma_commit_e(&bars->v_empty[vslot]);
             if (j < n[t]) {
               issue_s(t, kslot2);
               umma_commit_e(&bars->s_full[t]);
               if (j == n[t] - 1) umma_commit_e(&bars->q_empty[t]);
             }
           }
-          umma_commit_e(&bars->v_empty[vslot]);
           if (kslot2 >= 0) umma_commit_e(&bars->k_empty[kslot2]);
         }
       }
