@@ -178,7 +178,8 @@ ATTN_API attn_status_t attn_prefill(const void* q, const void* k, const void* v,
  *   dq       [B,Hq,S,D] bf16;  dk, dv  [B,Hkv,S,D] bf16 (written, not accumulated).
  *   causal   0 or 1; softmax_scale <= 0 means 1/sqrt(D).  dtype ATTN_BF16 only; D in {64, 128}.
  *   workspace  device buffer of attn_prefill_backward_workspace_size(B, Hq, S, D) bytes, 16-byte
- *            aligned; no initialisation needed (fp32 row sums and the dQ accumulator).
+ *            aligned; no initialisation needed (fp32 row sums Delta, then the fp32 dQ
+ *            accumulator that only the mma.sync path of attn_set_backward_path uses).
  * Errors: INVALID_ARG, UNSUPPORTED (fp8, other D), WORKSPACE, CUDA, NO_DEVICE.
  */
 ATTN_API size_t attn_prefill_backward_workspace_size(int B, int Hq, int S, int D);
