@@ -17,9 +17,9 @@
 //                     TMEM: S 128 | dP 128 | dQ D columns.
 //
 // Each step runs in two halves of 64 columns (query columns in the first kernel, key columns in
-// the second), one per score warpgroup: warpgroup 0 turns half 0 into P / dS while the tensor
-// core computes the scores of half 1, warpgroup 1 does half 1 while the gradient products of
-// half 0 run, so the exponentials of the two halves overlap each other and the MMAs.
+// the second): the score warps turn half 0 into P / dS while the tensor core computes the
+// scores of half 1, and half 1 while the gradient products of half 0 (and the next step's
+// half-0 scores) run.  Each of the two score warpgroups takes one 32-column chunk of every half.
 //
 // Tiles move by TMA in 128-row boxes of 64 bf16 with the 128-byte swizzle; one shared tile
 // serves as a K-major operand (the Q K^T style products) and an MN-major one (the P V style).
@@ -42,8 +42,10 @@ constexpr int kTcLoader = 8, kTcMma = 9;
 constexpr float kTcLog2e = 1.4426950408889634f;
 
 struct TcParams {
-  const float* lse;    // [B*Hq*S] natural log
-  const float* delta;  // [B*Hq*S]
+  const __nv_bfloat16* q;     // [B*Hq*S, D]
+  const __nv_bfloat16* dout;  // [B*Hq*S, D]
+  const float* lse;           // [B*Hq*S] natural log
+  const float* delta;         // [B*Hq*S]
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -58,7 +60,6 @@ struct TcTile {
   static constexpr int kBoxes = D / 64;
   static constexpr int kBoxBytes = kTcRows * 128;
   static constexpr int kBytes = kBoxes * kBoxBytes;
-  static constexpr int kKSteps = D / 16;  // K steps of 16 when the tile is the K-major operand
 };
 
 // Loads a [128 x D] tile (rows r0.., outer index z) into `dst` through TMA, completing on `bar`.
@@ -85,14 +86,33 @@ __device__ __forceinline__ void tc_mma_scores(uint32_t d, uint64_t a0, uint64_t 
   }
 }
 
-// D[tmem] (+)= A X over 64 rows r0..r0+63: A [128 x 64] bf16 packed two per TMEM column at
-// a_tmem.., X rows r0.. of a [128 x D] tile in shared memory read MN-major (D contiguous).
+// D[tmem] = A B^T over the head dim for the 64 B rows b_row0..: A [128 x D] bf16 in TMEM
+// (a_tmem.., two elements per column, 8 columns per K step of 16), B a [128 x D] K-major tile
+// in shared memory; the result fills 64 TMEM columns.
+template <int D>
+__device__ __forceinline__ void tc_mma_scores_ta(uint32_t d, uint32_t a_tmem, uint64_t b0, int b_row0,
+                                                 uint32_t idesc) {
+  const uint64_t b1 = b0 + static_cast<uint64_t>((b_row0 * 128) >> 4);
+#pragma unroll
+  for (int bx = 0; bx < TcTile<D>::kBoxes; ++bx) {
+    const uint64_t o = static_cast<uint64_t>((bx * TcTile<D>::kBoxBytes) >> 4);
+    const uint32_t a = a_tmem + bx * 32;
+    umma_ts_x4(d, a, b1 + o, a + 8, b1 + o + 2, a + 16, b1 + o + 4, a + 24, b1 + o + 6, idesc,
+               bx > 0);
+  }
+}
+
+// D[tmem] (+)= A X over 64 rows r0..r0+63: A [128 x 64] bf16 packed two per TMEM column (rows
+// 0..31 at a_tmem.., rows 32..63 at a_tmem + 32..), X rows r0.. of a [128 x D] tile in shared
+// memory read MN-major (D contiguous).
 template <int D>
 __device__ __forceinline__ void tc_mma_grad(uint32_t d, uint32_t a_tmem, uint64_t x0, int r0,
                                             uint32_t idesc, bool acc) {
-  // four K steps of 16 rows (2048 bytes of the tile, 8 TMEM columns of A each), one batch
+  // four K steps of 16 rows (2048 bytes of the tile, 8 TMEM columns of A each), one batch; the
+  // half's two 32-column chunks hold their 16 packed columns at the chunk's start (columns
+  // 0..15 and 32..47 of the half)
   const uint64_t x = x0 + static_cast<uint64_t>((r0 * 128) >> 4);
-  umma_ts_x4(d, a_tmem, x, a_tmem + 8, x + 128, a_tmem + 16, x + 256, a_tmem + 24, x + 384, idesc,
+  umma_ts_x4(d, a_tmem, x, a_tmem + 8, x + 128, a_tmem + 32, x + 256, a_tmem + 40, x + 384, idesc,
              acc ? 1u : 0u);
 }
 
@@ -158,15 +178,15 @@ __device__ __forceinline__ void kv_scores_chunk(const uint32_t (&sv)[32], const 
   }
 }
 
-// dS of one query row over 64 key columns (the dQ kernel), packed as bf16 pairs.  nl2 / nde:
+// dS of one query row over 32 key columns (the dQ kernel), packed as bf16 pairs.  nl2 / nde:
 // -lse log2e and -Delta of the row.  MASK as above with the roles of query and key exchanged.
 template <bool MASK>
-__device__ __forceinline__ void q_scores_half(const uint32_t (&sv)[64], const uint32_t (&dv)[64],
-                                              float sl2, float nl2, float nde, int q, int k_first,
-                                              int S, int causal, uint32_t (&dd)[32]) {
+__device__ __forceinline__ void q_scores_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+                                               float sl2, float nl2, float nde, int q, int k_first,
+                                               int S, int causal, uint32_t (&dd)[16]) {
   const float2 c2 = make_float2(sl2, sl2), l2 = make_float2(nl2, nl2), d2 = make_float2(nde, nde);
 #pragma unroll
-  for (int e = 0; e < kTcHalf; e += 2) {
+  for (int e = 0; e < 32; e += 2) {
     float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, l2);
     x = make_float2(fast_exp2(x.x), fast_exp2(x.y));
     if constexpr (MASK) {
@@ -234,7 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&bars->q_empty[t], 1);
       mbar_init(&bars->row_full[t], 32);
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->p_full[t], 256);  // both score warpgroups
     }
     mbar_init(&bars->done, 1);
     fence_barrier_init();
@@ -308,7 +328,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       umma_commit_e(&bars->s_full[h]);
     };
     // dV += P^T dO, dK += dS^T Q over the 64 query rows of half h; P^T / dS^T of half h sit in
-    // columns 64h..64h+31 (bf16 pairs)
+    // columns 64h..64h+15 and 64h+32..64h+47 (bf16 pairs, one block per 32-column chunk)
     auto issue_grads = [&](int st, int h) {
       const uint64_t so = stage_off(st);
       const bool acc = st > 0 || h > 0;
@@ -346,7 +366,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (ok) umma_commit_e(&bars->done);
   } else {
     // ---------------------------------------------------------------- P^T and dS^T, one key row
-    const int h = warp >> 2;             // warpgroup h: half h of every step
+    // Warpgroup c takes the 32-column chunk c of both halves of every step, so a half is done
+    // by both warpgroups at once.
+    const int c = warp >> 2;
     const int kr = (warp & 3) * 32 + lane;  // TMEM lane quarter warp % 4
     const int key = kv0 + kr;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -361,36 +383,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // masks: the diagonal tile, and the last query or key tile when S is ragged
       const bool need_mask = (p.causal && qt == tile) || q0 + kTcRows > p.S || kv0 + kTcRows > p.S;
       if (!(ok = mbar_wait_warp_sleep(&bars->row_full[sg], (st >> 1) & 1, p.status))) break;
-      if (!(ok = mbar_wait_warp_sleep(&bars->s_full[h], st & 1, p.status))) break;
-      tc_fence_after();
-      const float* lse_s = s_lse + sg * kTcRows + h * kTcHalf;
-      const float* del_s = s_del + sg * kTcRows + h * kTcHalf;
-      // the half's 64 query columns of S^T and dP^T in two chunks of 32 (one wait per chunk)
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const int col = h * kTcHalf + c * 32;
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait_warp_sleep(&bars->s_full[h], st & 1, p.status))) break;
+        tc_fence_after();
+        const int col = h * kTcHalf + c * 32;  // this chunk's query columns in the tile
         uint32_t sv[32], dv[32];
         tmem_ld32x2(tS + col, sv, tDP + col, dv);
         uint32_t pp[16], dd[16];
+        const float* lse_s = s_lse + sg * kTcRows + col;
+        const float* del_s = s_del + sg * kTcRows + col;
         if (need_mask)
-          kv_scores_chunk<true>(sv, dv, lse_s + c * 32, del_s + c * 32, sl2, key, q0 + col, p.S,
-                                p.causal, pp, dd);
+          kv_scores_chunk<true>(sv, dv, lse_s, del_s, sl2, key, q0 + col, p.S, p.causal, pp, dd);
         else
-          kv_scores_chunk<false>(sv, dv, lse_s + c * 32, del_s + c * 32, sl2, key, q0 + col, p.S,
-                                 p.causal, pp, dd);
-        // bf16 pairs into the half's first 32 columns (64 h + 16 c ..), columns already read
-        tmem_st16(tS + h * kTcHalf + c * 16, pp);
-        tmem_st16(tDP + h * kTcHalf + c * 16, dd);
+          kv_scores_chunk<false>(sv, dv, lse_s, del_s, sl2, key, q0 + col, p.S, p.causal, pp, dd);
+        // bf16 pairs into the chunk's own first 16 columns, which this thread already read (the
+        // other warpgroup reads only its own chunk's columns)
+        tmem_st16(tS + col, pp);
+        tmem_st16(tDP + col, dd);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[h]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[h]);
     }
     // warpgroup 0: dK = scale * sum dS^T Q; warpgroup 1: dV; bf16, this thread's key row
     if (ok && (ok = mbar_wait_warp_sleep(&bars->done, 0, p.status))) {
       tc_fence_after();
       const size_t row = static_cast<size_t>(bh) * p.S + key;
-      if (h == 0)
+      if (c == 0)
         tc_store_row(p.dk + row * D, tmem + lane_off + kColDK, p.scale, key < p.S, 0, D / 32);
       else
         tc_store_row(p.dv + row * D, tmem + lane_off + kColDV, 1.f, key < p.S, 0, D / 32);
@@ -412,12 +432,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 template <int D>
 struct QSmem {
   using T = TcTile<D>;
-  static constexpr int kQ = 0;
-  static constexpr int kO = kQ + T::kBytes;
-  static constexpr int kKStages = 3, kVStages = 2;
-  // K is read by the scores and the dQ products, V by the scores only: V stages free earlier,
-  // so K gets the extra stage (the loads of a stage have about two steps to land)
-  static constexpr int kK = kO + T::kBytes;
+  // Q and dO live in TMEM (the A operand of the score products).  K is read by the scores and
+  // the dQ products, V by the scores only.
+  static constexpr int kKStages = 4, kVStages = 3;
+  static constexpr int kK = 0;
   static constexpr int kV = kK + kKStages * T::kBytes;
   static constexpr int kBar = kV + kVStages * T::kBytes;
   static constexpr int kBytes = std::max(kBar + 256 + 1024, 120 * 1024);
@@ -425,7 +443,7 @@ struct QSmem {
 };
 
 struct QBars {
-  uint64_t qd_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], done;
+  uint64_t qd_full, k_full[4], k_empty[4], v_full[3], v_empty[3], s_full[2], p_full[2], done;
   uint32_t tmem_slot;
 };
 static_assert(sizeof(QBars) <= 256, "barrier block");
@@ -449,17 +467,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int kvz = b * p.Hkv + hq / p.G;
   const int q0 = qt * kTcRows;
   const int steps = p.causal ? qt + 1 : p.nT;  // key tiles this query tile meets
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  // TMEM: S 128 | dP 128 | dQ D | Q D/2 | dO D/2 columns (bf16 Q and dO rows packed in pairs)
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColQ = 256 + D, kColO = kColQ + D / 2;
+  static_assert(kColO + D / 2 <= 512, "TMEM columns");
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->qd_full, 1);
+    mbar_init(&bars->qd_full, 256);  // both score warpgroups store their operand rows
     for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 256);  // both score warpgroups
+    }
+    for (int t = 0; t < L::kVStages; ++t) {
       mbar_init(&bars->v_full[t], 1);
       mbar_init(&bars->v_empty[t], 1);
-      mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], 128);
     }
-    for (int t = 0; t < 3; ++t) {
+    for (int t = 0; t < L::kKStages; ++t) {
       mbar_init(&bars->k_full[t], 1);
       mbar_init(&bars->k_empty[t], 1);
     }
@@ -474,24 +496,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == kTcLoader) {
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmO);
-      mbar_arrive_expect_tx(&bars->qd_full, 2 * TcTile<D>::kBytes);
-      tc_load_tile<D>(smem + L::kQ, &tmQ, &bars->qd_full, q0, bh);
-      tc_load_tile<D>(smem + L::kO, &tmO, &bars->qd_full, q0, bh);
       for (int st = 0; st < steps; ++st) {
-        // K stage st % 3 (free once the dQ products of step st - 3 completed), V stage st % 2
-        // (free once the scores of step st - 2 completed)
-        const int ks = st % L::kKStages, vs = st & 1;
+        // K stage st % 4 (free once the dQ products of step st - 4 completed), V stage st % 3
+        // (free once the scores of step st - 3 completed)
+        const int ks = st % L::kKStages, vs = st % L::kVStages;
         if (st >= L::kKStages &&
             !mbar_wait_sleep(&bars->k_empty[ks], ((st / L::kKStages) & 1) ^ 1, p.status))
           break;
         mbar_arrive_expect_tx(&bars->k_full[ks], TcTile<D>::kBytes);
         tc_load_tile<D>(smem + L::kK + ks * TcTile<D>::kBytes, &tmK, &bars->k_full[ks],
                         st * kTcRows, kvz);
-        if (st >= L::kVStages && !mbar_wait_sleep(&bars->v_empty[vs], ((st >> 1) & 1) ^ 1, p.status))
+        if (st >= L::kVStages &&
+            !mbar_wait_sleep(&bars->v_empty[vs], ((st / L::kVStages) & 1) ^ 1, p.status))
           break;
         mbar_arrive_expect_tx(&bars->v_full[vs], TcTile<D>::kBytes);
         tc_load_tile<D>(smem + L::kV + vs * TcTile<D>::kBytes, &tmV, &bars->v_full[vs],
@@ -501,22 +519,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == kTcMma) {
     const uint32_t idesc_s = make_idesc(1, 1, false, false, kTcHalf, kTcRows);
     const uint32_t idesc_g = make_idesc(1, 1, false, true, D, kTcRows);  // B MN-major
-    const uint64_t q_desc = smem_desc(smem_u32(smem + L::kQ), 16, 1024, 2);
-    const uint64_t o_desc = smem_desc(smem_u32(smem + L::kO), 16, 1024, 2);
     const uint64_t k_desc0 = smem_desc(smem_u32(smem + L::kK), 16, 1024, 2);
     const uint64_t v_desc0 = smem_desc(smem_u32(smem + L::kV), 16, 1024, 2);
     const uint64_t kg_desc0 = smem_desc(smem_u32(smem + L::kK), TcTile<D>::kBoxBytes, 1024, 2);
     auto k_off = [](int st) {
       return static_cast<uint64_t>(((st % L::kKStages) * TcTile<D>::kBytes) >> 4);
     };
-    auto v_off = [](int st) { return static_cast<uint64_t>(((st & 1) * TcTile<D>::kBytes) >> 4); };
-    // S = Q K^T and dP = dO V^T of half h (key columns 64h..) of key tile st
+    auto v_off = [](int st) {
+      return static_cast<uint64_t>(((st % L::kVStages) * TcTile<D>::kBytes) >> 4);
+    };
+    // S = Q K^T and dP = dO V^T of half h (key columns 64h..) of key tile st, Q and dO from TMEM
     auto issue_scores = [&](int st, int h) {
-      tc_mma_scores<D>(tmem + kColS + h * kTcHalf, q_desc, k_desc0 + k_off(st), h * kTcHalf, idesc_s);
-      tc_mma_scores<D>(tmem + kColDP + h * kTcHalf, o_desc, v_desc0 + v_off(st), h * kTcHalf, idesc_s);
+      tc_mma_scores_ta<D>(tmem + kColS + h * kTcHalf, tmem + kColQ, k_desc0 + k_off(st), h * kTcHalf,
+                          idesc_s);
+      tc_mma_scores_ta<D>(tmem + kColDP + h * kTcHalf, tmem + kColO, v_desc0 + v_off(st),
+                          h * kTcHalf, idesc_s);
       umma_commit_e(&bars->s_full[h]);
     };
-    // dQ += dS K over the 64 keys of half h (dS of half h in S columns 64h..64h+31)
+    // dQ += dS K over the 64 keys of half h (dS of half h in S columns 64h..64h+15 and
+    // 64h+32..64h+47)
     auto issue_grads = [&](int st, int h) {
       tc_mma_grad<D>(tmem + kColDQ, tmem + kColS + kTcHalf * h, kg_desc0 + k_off(st),
                      h * kTcHalf, idesc_g, st > 0 || h > 0);
@@ -524,10 +545,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // K and V of key tile st landed
     auto wait_kv = [&](int st) {
       return mbar_wait_warp_sleep(&bars->k_full[st % L::kKStages], (st / L::kKStages) & 1, p.status) &&
-             mbar_wait_warp_sleep(&bars->v_full[st & 1], (st >> 1) & 1, p.status);
+             mbar_wait_warp_sleep(&bars->v_full[st % L::kVStages], (st / L::kVStages) & 1, p.status);
     };
     // the pipelined order of the dK / dV kernel; V stage of step st is released once both
-    // halves of its scores completed, the K stage once its dQ products did
+    // halves of its scores completed, the K stage once its dQ products did.  qd_full: the score
+    // warps stored Q and dO into TMEM.
     bool ok = mbar_wait_warp_sleep(&bars->qd_full, 0, p.status) && wait_kv(0);
     if (ok) {
       tc_fence_after();
@@ -551,13 +573,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       umma_commit_e(&bars->k_empty[st % L::kKStages]);
       if (next) {
         issue_scores(st + 1, 1);
-        umma_commit_e(&bars->v_empty[(st + 1) & 1]);
+        umma_commit_e(&bars->v_empty[(st + 1) % L::kVStages]);
       }
     }
     if (ok) umma_commit_e(&bars->done);
   } else {
     // ---------------------------------------------------------------- dS, one query row
-    const int h = warp >> 2;                // warpgroup h: half h of every step
+    // Warpgroup c takes the 32-column chunk c of both halves of every key tile.
+    const int c = warp >> 2;
     const int qr = (warp & 3) * 32 + lane;  // TMEM lane quarter warp % 4
     const int q = q0 + qr;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -566,32 +589,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const size_t row = static_cast<size_t>(bh) * p.S + q;
     const float nl2 = q < p.S ? -__ldg(p.lse + row) * kTcLog2e : -INFINITY;
     const float nde = q < p.S ? -__ldg(p.delta + row) : 0.f;
+    {
+      // this thread's row of Q (warpgroup 0) or dO (warpgroup 1) into its TMEM lane as the A
+      // operand of the score products: dims 2i, 2i+1 in column i (zeros past S)
+      const uint4* src = reinterpret_cast<const uint4*>((c == 0 ? p.q : p.dout) + row * D);
+      uint32_t v[D / 2];
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        const uint4 x = q < p.S ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+        v[4 * i] = x.x;
+        v[4 * i + 1] = x.y;
+        v[4 * i + 2] = x.z;
+        v[4 * i + 3] = x.w;
+      }
+      const uint32_t ta = tmem + lane_off + (c == 0 ? kColQ : kColO);
+      if constexpr (D == 128) {
+        tmem_st64(ta, v);
+      } else {
+        tmem_st32(ta, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->qd_full);
+    }
     bool ok = true;
     for (int st = 0; st < steps && ok; ++st) {
       const int k0 = st * kTcRows;
       const bool need_mask = (p.causal && st == qt) || k0 + kTcRows > p.S || q0 + kTcRows > p.S;
-      if (!(ok = mbar_wait_warp_sleep(&bars->s_full[h], st & 1, p.status))) break;
-      tc_fence_after();
-      // the half's 64 key columns of S and dP, one wait for both loads
-      uint32_t sv[64], dv[64];
-      tmem_ld64x2(tS + h * kTcHalf, sv, tDP + h * kTcHalf, dv);
-      uint32_t dd[32];
-      if (need_mask)
-        q_scores_half<true>(sv, dv, sl2, nl2, nde, q, k0 + h * kTcHalf, p.S, p.causal, dd);
-      else
-        q_scores_half<false>(sv, dv, sl2, nl2, nde, q, k0 + h * kTcHalf, p.S, p.causal, dd);
-      // bf16 pairs into the half's first 32 columns (64 h ..), already read
-      tmem_st32(tS + h * kTcHalf, dd);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[h]);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait_warp_sleep(&bars->s_full[h], st & 1, p.status))) break;
+        tc_fence_after();
+        const int col = h * kTcHalf + c * 32;  // this chunk's key columns in the tile
+        uint32_t sv[32], dv[32];
+        tmem_ld32x2(tS + col, sv, tDP + col, dv);
+        uint32_t dd[16];
+        if (need_mask)
+          q_scores_chunk<true>(sv, dv, sl2, nl2, nde, q, k0 + col, p.S, p.causal, dd);
+        else
+          q_scores_chunk<false>(sv, dv, sl2, nl2, nde, q, k0 + col, p.S, p.causal, dd);
+        // bf16 pairs into the chunk's own first 16 S columns, already read by this thread
+        tmem_st16(tS + col, dd);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[h]);
+      }
     }
-    // dQ = scale * sum dS K, bf16, this thread's query row; warpgroup h writes columns
-    // h D / 2 .. (h + 1) D / 2 - 1
+    // dQ = scale * sum dS K, bf16, this thread's query row; warpgroup c writes columns
+    // c D / 2 .. (c + 1) D / 2 - 1
     if (ok && (ok = mbar_wait_warp_sleep(&bars->done, 0, p.status))) {
       tc_fence_after();
-      tc_store_row(p.dq + row * D, tmem + lane_off + kColDQ, p.scale, q < p.S, h * (D / 64),
-                   (h + 1) * (D / 64));
+      tc_store_row(p.dq + row * D, tmem + lane_off + kColDQ, p.scale, q < p.S, c * (D / 64),
+                   (c + 1) * (D / 64));
     }
   }
   tc_fence_before();
@@ -650,6 +699,8 @@ attn_status_t launch_bwd_tc_typed(const void* q, const void* k, const void* v, c
     if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
   }
   TcParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.lse = lse;
   p.delta = delta;
   p.dq = static_cast<__nv_bfloat16*>(dq);
