@@ -141,3 +141,37 @@ def test_causal_prefill_d256_s4096_sampled():
     rows = sample_rows(B, Hq, S, n_random=16, seed=5)
     ro, rl = oracle_rows(q, k, v, rows, causal=True, rope=True)
     check_rows(o, lse, rows, ro, rl, BF16_MAX, BF16_MEAN)
+
+
+@pytest.mark.parametrize("path", [2, 1], ids=["tcgen05", "mma_sync"])
+def test_backward_causal_d128_s4096_group_slice(path):
+    """The backward at the size the bench times (causal GQA Z=4 Hq=32 Hkv=8 D=128 S=4096): the
+    device computes the whole problem; dQ of the four query heads of one KV head of one batch,
+    and that KV head's dK and dV (sums over those four heads), are compared with the oracle's
+    gradients of that group in full (every row, every key)."""
+    B, Hq, Hkv, S, D = 4, 32, 8, 4096, 128
+    G = Hq // Hkv
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=24)
+    do = synthetic.normal((B, Hq, S, D), 25, "bf16")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = binding.attn_prefill(qd, kd, vd, causal=True, want_lse=True)
+    binding.attn_set_backward_path(path)
+    try:
+        dq, dk, dv = binding.attn_prefill_backward(qd, kd, vd, o, lse, do.cuda(), causal=True)
+    finally:
+        binding.attn_set_backward_path(0)
+    assert binding.attn_get_device_status() == 0
+    b, h = 1, 3
+    hs = slice(h * G, (h + 1) * G)
+    rq, rk, rv = oracle.attention_backward(oracle.as_f64(q[b:b + 1, hs]), oracle.as_f64(k[b:b + 1, h:h + 1]),
+                                           oracle.as_f64(v[b:b + 1, h:h + 1]), oracle.as_f64(do[b:b + 1, hs]), True)
+    for what, got, ref in (("dQ", dq[b:b + 1, hs], rq), ("dK", dk[b:b + 1, h:h + 1], rk),
+                           ("dV", dv[b:b + 1, h:h + 1], rv)):
+        g = oracle.as_f64(got.cpu())
+        d = np.abs(g - ref)
+        assert np.all(np.isfinite(g)), what
+        big, mean = np.abs(ref).max(), np.abs(ref).mean()
+        # the bounds of the small-shape backward tests (relative to the largest entry and to the
+        # mean magnitude; bf16 P and dS before every product, fp32 accumulation)
+        assert d.max() <= 2e-2 * big, f"{what}: max-abs {d.max():.3e} > 2e-2 * {big:.3e}"
+        assert d.mean() <= 5e-3 * mean, f"{what}: mean-abs {d.mean():.3e} > 5e-3 * {mean:.3e}"
