@@ -135,6 +135,8 @@ struct Bars {
   uint64_t q_ready[2], k_ready[8];  // fused RoPE: tile rotated in shared memory
   uint64_t k_st_full[8], k_st_free[8];  // fp8 + RoPE: K staging tiles (loaded / consumed)
   uint64_t p_hi[2];  // P of keys 64..127 written (p_full: keys 0..63, or all of P with RoPE)
+  uint64_t s_free[2];   // separate-P form: the softmax has read S_t (its columns may be reused)
+  uint64_t pv_done[2];  // separate-P form: the P V products of the previous step completed
   uint32_t tmem_slot;
 };
 static_assert(sizeof(Bars) <= 1024, "barrier block");
@@ -289,6 +291,13 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
   // overlap the softmax: measured faster at D >= 128, slower at D = 64, whose P V products are
   // short anyway (A/B on one GPU: bf16 / fp8 D=128 -1 to -2.4 %, D=64 +0.8 % / +5 %)
   constexpr bool kSplitP = D >= 128;
+  // Separate P (D = 64 without in-kernel RoPE, where TMEM has room): P_t gets columns of its own
+  // after O1 instead of S_t's, so that S_t(j+1) is issued as soon as the softmax has read S_t(j)
+  // and runs during that softmax; the softmax then waits for the previous P V products
+  // (pv_done) before it rescales O or overwrites P.
+  constexpr uint32_t kPWidth = FP8 ? 32u : 64u;  // TMEM columns of one tile's P
+  constexpr uint32_t kColP0 = C::kColO1 + D, kColP1 = kColP0 + kPWidth;
+  constexpr bool kSepP = !ROPE && !kSplitP && kColP1 + kPWidth <= C::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -318,6 +327,10 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
     }
     mbar_init(&bars->q_ready[0], 128);
     mbar_init(&bars->q_ready[1], 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_free[t], 128);
+      mbar_init(&bars->pv_done[t], 1);
+    }
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&bars->tmem_slot, C::kTmemCols);
@@ -421,7 +434,7 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
       const uint64_t k_desc0 = smem_desc(smem_u32(smem + C::kKVOff), 16, C::kSBO, C::kSwzCode);
       const uint64_t v_desc0 =
           smem_desc(smem_u32(smem + C::kVOff), C::kVBoxBytes, C::kVSBO, C::kVSwzCode);
-      uint32_t ph_qf[2] = {0, 0}, ph_pf[2] = {0, 0}, ph_oe[2] = {0, 0};
+      uint32_t ph_qf[2] = {0, 0}, ph_pf[2] = {0, 0}, ph_oe[2] = {0, 0}, ph_sf[2] = {0, 0};
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0;
       bool ok = true;
@@ -441,7 +454,8 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
       auto issue_pv_part = [&](int t, int slot, bool acc, auto k0c, auto k1c) {
         constexpr int k0 = decltype(k0c)::value, k1 = decltype(k1c)::value;
         const uint64_t bd = v_desc0 + static_cast<uint64_t>((slot * C::kVTileBytes) >> 4);
-        const uint32_t pcol = tmem + (t ? C::kColS1 : C::kColS0) + kPCol;
+        const uint32_t pcol =
+            kSepP ? tmem + (t ? kColP1 : kColP0) : tmem + (t ? C::kColS1 : C::kColS0) + kPCol;
         const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
         issue_batched<FP8, true, k0, k1>(
             d, [&](int kk) { return pcol + kk * 8; },
@@ -499,6 +513,33 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             if (!ok) continue;
+            if constexpr (kSepP) {
+              // S_t(j) first, into the columns the softmax of step j - 1 has read (it runs while
+              // that softmax computes), then P_t(j - 1) V from P's own columns
+              if (j < n[t]) {
+                if (!(ok = mbar_wait_warp(&bars->s_free[t], ph_sf[t], p.status))) continue;
+                ph_sf[t] ^= 1;
+                tc_fence_after();
+                issue_s(t, kslot2);
+                umma_commit_e(&bars->s_full[t]);
+                if (j == n[t] - 1) umma_commit_e(&bars->q_empty[t]);
+              }
+              if (j - 1 < n[t]) {
+                ok = mbar_wait_warp(&bars->p_full[t], ph_pf[t], p.status);
+                ph_pf[t] ^= 1;
+                if (ok && j == 1) {
+                  ok = mbar_wait_warp(&bars->o_empty[t], ph_oe[t] ^ 1, p.status);
+                  ph_oe[t] ^= 1;
+                }
+                if (!ok) continue;
+                tc_fence_after();
+                issue_pv(t, vslot, j > 1);
+                umma_commit_e(&bars->pv_done[t]);
+                if (j - 1 == n[t] - 1) umma_commit_e(&bars->o_full[t]);
+              }
+              if (t == NT - 1) umma_commit_e(&bars->v_empty[vslot]);
+              continue;
+            }
             if constexpr (kSplitP) {
               if (j - 1 < n[t]) {
                 // each half of P goes to the tensor core as soon as the softmax has written it
@@ -543,6 +584,13 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
             }
           }
           if (kslot2 >= 0) umma_commit_e(&bars->k_empty[kslot2]);
+        }
+        if constexpr (kSepP) {
+          // the softmax's last s_free of the item is not waited for (the item's next S needs
+          // none): step over that phase
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            if (n[t] > 0) ph_sf[t] ^= 1;
         }
       }
     }
@@ -679,7 +727,8 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + (t ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
-    uint32_t ph_s = 0, ph_o = 0, ph_q = 0;
+    const uint32_t tP = tmem + lane_off + (t ? kColP1 : kColP0);  // separate-P form only
+    uint32_t ph_s = 0, ph_o = 0, ph_q = 0, ph_pv = 0;
     bool ok = true;
     for (int r = 0; r < rounds && ok; ++r) {
       const int it = item_for(r, blockIdx.x, gridDim.x);
@@ -802,6 +851,11 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
         } else {
         uint32_t sr[128];
         tmem_ld128(tS, sr);
+        if constexpr (kSepP) {
+          // S_t(j) is in registers: its columns may take S_t(j + 1)
+          tc_fence_before();
+          mbar_arrive(&bars->s_free[t]);
+        }
         if (need_mask) {
 #pragma unroll
           for (int e = 0; e < 128; ++e)
@@ -919,12 +973,26 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
           }
           const float2 accs = __fadd2_rn(__fadd2_rn(acc0, acc1), __fadd2_rn(acc2, acc3));
           l += accs.x + accs.y;
-          if constexpr (FP8)
-            tmem_st32(tS, pk);
-          else
-            tmem_st64(tS, pk);
+          if constexpr (kSepP) {
+            // P_t(j - 1) V has completed: P's columns are free and O holds the tiles before j
+            if (j > 0) {
+              if (!(ok = mbar_wait_warp(&bars->pv_done[t], ph_pv, p.status))) break;
+              ph_pv ^= 1;
+              tc_fence_after();
+            }
+            if constexpr (FP8)
+              tmem_st32(tP, pk);
+            else
+              tmem_st64(tP, pk);
+          } else {
+            if constexpr (FP8)
+              tmem_st32(tS, pk);
+            else
+              tmem_st64(tS, pk);
+          }
           // O_t holds the tiles before j (their P V products completed before S_t(j) was
-          // signalled); rescale it, warp-uniformly, before P is released
+          // signalled, or, with separate P, before pv_done); rescale it, warp-uniformly, before
+          // P is released
           if (__any_sync(0xffffffffu, f != 1.f)) {
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -962,6 +1030,8 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
       // epilogue: O / l -> bf16, LSE
       if (!(ok = mbar_wait(&bars->o_full[t], ph_o, p.status))) break;
       ph_o ^= 1;
+      // separate P: the item's last P V completion is covered by o_full; step over its phase
+      if constexpr (kSepP) ph_pv ^= 1;
       tc_fence_after();
       const float inv = p.v_scale / l;
       __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.S + row) * D;
