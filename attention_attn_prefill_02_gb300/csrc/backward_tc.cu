@@ -450,8 +450,7 @@ static_assert(sizeof(QBars) <= 256, "barrier block");
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    bwd_tc_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+    bwd_tc_q_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const TcParams p) {
   using L = QSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -724,7 +723,7 @@ attn_status_t launch_bwd_tc_typed(const void* q, const void* k, const void* v, c
   {
     auto kern = bwd_tc_q_kernel<D>;
     if (!set_smem_attr(reinterpret_cast<const void*>(kern), QSmem<D>::kBytes)) return ATTN_ERR_CUDA;
-    kern<<<p.nT * B * Hq, kTcThreads, QSmem<D>::kBytes, st>>>(tq, tk, tv, to, p);
+    kern<<<p.nT * B * Hq, kTcThreads, QSmem<D>::kBytes, st>>>(tk, tv, p);
   }
   return launch_status();
 }

@@ -304,91 +304,107 @@ __device__ __forceinline__ void umma_ts_f8_e(uint32_t d_tmem, uint32_t a_tmem, u
 // warp sustains about one MMA per 70-100 cycles, below the 64 cycles of an M=128 N=128 K=16
 // product).
 
-__device__ __forceinline__ void umma_ss_x4(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1, uint64_t b1, uint64_t a2, uint64_t b2, uint64_t a3, uint64_t b3, uint32_t idesc,
-                                           uint32_t accumulate) {
+__device__ __forceinline__ void umma_ss_x4(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1,
+                                           uint64_t b1, uint64_t a2, uint64_t b2, uint64_t a3,
+                                           uint64_t b3, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, t, e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, %10, %10;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %9, p;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %9, t;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %9, t;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %9, t;\n\t""}" ::"r"(d), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "l"(a2), "l"(b2), "l"(a3), "l"(b3), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %9, t;\n\t}"
+      :: "r"(d), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "l"(a2), "l"(b2), "l"(a3), "l"(b3), "r"(idesc),
+         "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void umma_ts_x4(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1, uint64_t b1, uint32_t a2, uint64_t b2, uint32_t a3, uint64_t b3, uint32_t idesc,
-                                           uint32_t accumulate) {
+__device__ __forceinline__ void umma_ts_x4(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1,
+                                           uint64_t b1, uint32_t a2, uint64_t b2, uint32_t a3,
+                                           uint64_t b3, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, t, e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, %10, %10;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %9, p;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %9, t;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %9, t;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %9, t;\n\t""}" ::"r"(d), "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(a2), "l"(b2), "r"(a3), "l"(b3), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %9, t;\n\t}"
+      :: "r"(d), "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(a2), "l"(b2), "r"(a3), "l"(b3), "r"(idesc),
+         "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void umma_ss_f8_x4(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1, uint64_t b1, uint64_t a2, uint64_t b2, uint64_t a3, uint64_t b3, uint32_t idesc,
-                                           uint32_t accumulate) {
+__device__ __forceinline__ void umma_ss_f8_x4(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1,
+                                              uint64_t b1, uint64_t a2, uint64_t b2, uint64_t a3,
+                                              uint64_t b3, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, t, e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, %10, %10;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %9, p;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %4, %9, t;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %5, %6, %9, t;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %7, %8, %9, t;\n\t""}" ::"r"(d), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "l"(a2), "l"(b2), "l"(a3), "l"(b3), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %7, %8, %9, t;\n\t}"
+      :: "r"(d), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "l"(a2), "l"(b2), "l"(a3), "l"(b3), "r"(idesc),
+         "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void umma_ts_f8_x4(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1, uint64_t b1, uint32_t a2, uint64_t b2, uint32_t a3, uint64_t b3, uint32_t idesc,
-                                           uint32_t accumulate) {
+__device__ __forceinline__ void umma_ts_f8_x4(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1,
+                                              uint64_t b1, uint32_t a2, uint64_t b2, uint32_t a3,
+                                              uint64_t b3, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, t, e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, %10, %10;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %9, p;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %4, %9, t;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%5], %6, %9, t;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%7], %8, %9, t;\n\t""}" ::"r"(d), "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(a2), "l"(b2), "r"(a3), "l"(b3), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%7], %8, %9, t;\n\t}"
+      :: "r"(d), "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(a2), "l"(b2), "r"(a3), "l"(b3), "r"(idesc),
+         "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void umma_ts_x2(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1, uint64_t b1, uint32_t idesc,
-                                           uint32_t accumulate) {
+__device__ __forceinline__ void umma_ts_x2(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1,
+                                           uint64_t b1, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, t, e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 t, %6, %6;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %5, p;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %5, t;\n\t""}" ::"r"(d), "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %5, t;\n\t}"
+      :: "r"(d), "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void umma_ts_f8_x2(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1, uint64_t b1, uint32_t idesc,
-                                           uint32_t accumulate) {
+__device__ __forceinline__ void umma_ts_f8_x2(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1,
+                                              uint64_t b1, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, t, e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 t, %6, %6;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %5, p;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %4, %5, t;\n\t""}" ::"r"(d), "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %4, %5, t;\n\t}"
+      :: "r"(d), "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void umma_ss_x2(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1, uint64_t b1, uint32_t idesc,
-                                           uint32_t accumulate) {
+__device__ __forceinline__ void umma_ss_x2(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1,
+                                           uint64_t b1, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, t, e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 t, %6, %6;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %5, p;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %5, t;\n\t""}" ::"r"(d), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %5, t;\n\t}"
+      :: "r"(d), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void umma_ss_f8_x2(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1, uint64_t b1, uint32_t idesc,
-                                           uint32_t accumulate) {
+__device__ __forceinline__ void umma_ss_f8_x2(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1,
+                                              uint64_t b1, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p, t, e;\n\telect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 t, %6, %6;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %5, p;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %4, %5, t;\n\t""}" ::"r"(d), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %4, %5, t;\n\t}"
+      :: "r"(d), "l"(a0), "l"(b0), "l"(a1), "l"(b1), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
