@@ -693,6 +693,26 @@ def test_prefill_backward(B, Hq, Hkv, S, D, causal, bwd_path):
     check_grad(dv.cpu(), rv, "dV")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,causal,scale", [
+    (1, 16, 1, 300, 128, True, 0.0),     # a group of 16 query heads on one KV head
+    (2, 4, 4, 257, 64, False, 0.05),     # a softmax scale other than 1/sqrt(D), ragged
+    (1, 2, 1, 129, 128, True, 0.2),      # one row past a whole tile, larger scale
+])
+def test_prefill_backward_groups_and_scales(B, Hq, Hkv, S, D, causal, scale, bwd_path):
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=S + 37)
+    do = synthetic.normal((B, Hq, S, D), 6000 + S, "bf16")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = binding.attn_prefill(qd, kd, vd, causal=causal, softmax_scale=scale, want_lse=True)
+    dq, dk, dv = binding.attn_prefill_backward(qd, kd, vd, o, lse, do.cuda(), causal=causal,
+                                               softmax_scale=scale)
+    status_ok()
+    rq, rk, rv = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do), causal,
+                                           scale=scale if scale > 0 else None)
+    check_grad(dq.cpu(), rq, "dQ")
+    check_grad(dk.cpu(), rk, "dK")
+    check_grad(dv.cpu(), rv, "dV")
+
+
 def test_prefill_backward_equals_finite_difference_direction(bwd_path):
     """A directional derivative of sum(O * W) on the device (forward at q +- h u) agrees with
     <dQ, u> from the backward, independently of the oracle."""
