@@ -760,14 +760,15 @@ constexpr int kLatMaxB = 2048;  // sequences per call (the tile prefix sums live
 constexpr int kLatMaxCtas = ATTN_LAT_MAX_CTAS;
 
 // Cache tile geometry: bf16 tiles of 64 keys x 512 dims (64 KB, three stages) or e5m2 tiles of
-// 64 keys x 512 bytes (32 KB, six stages); both rings hold 192 KB and arrive as TMA boxes of
-// 64 rows x 128 bytes with the 128-byte swizzle.
+// 64 keys x 512 bytes (32 KB, six stages); both rings hold 192 KB.  A tile lands as its 128-byte
+// column chunks, each 64 rows x 128 bytes with the 128-byte swizzle, in ONE TMA copy: the tensor
+// map views the cache as {128 bytes of a row, key, chunk, sequence}, so the box {128 B, 64 keys,
+// all chunks, 1} is laid out chunk-major.  Issued as one box per chunk, the copies held the
+// issuing thread (and with it its warp, and the next block barrier) ~700 cycles per tile.
 template <bool F8>
 struct LatGeo {
   static constexpr int kTileBytes = F8 ? kTileKeys * kLatQK : kLatTileBytes;
   static constexpr int kStages = F8 ? 6 : kLatStages;
-  static constexpr int kBoxElems = F8 ? 128 : 64;
-  static constexpr int kBoxes = kLatQK / kBoxElems;
 };
 constexpr int kLatMaxStages = 6;
 
@@ -891,9 +892,7 @@ struct LatLoader {
     if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) return false;
     mbar_arrive_expect_tx(&full[stage], G::kTileBytes);
     uint8_t* ct = smem + stage * G::kTileBytes;
-#pragma unroll
-    for (int bx = 0; bx < G::kBoxes; ++bx)
-      tma_load_3d(ct + bx * kTileKeys * 128, tm, &full[stage], bx * G::kBoxElems, t0, cur.b);
+    tma_load_4d(ct, tm, &full[stage], 0, t0, 0, cur.b);
     if (++stage == G::kStages) {
       stage = 0;
       phase ^= 1;
@@ -1476,9 +1475,10 @@ void force_decode_splits(int nsplit) { g_forced_decode_splits.store(nsplit); }
 DecodePlan plan_latent(int B, int H, int Lmax) {
   (void)Lmax;
   DecodePlan pl;
-  // At most 128 CTAs: on GB300 the latent stream reached 5.2 TB/s with 128 streaming CTAs and
-  // only 4.6 TB/s with 140 or 152 (measured with the compute removed).  B equal to the CTA
-  // count: one CTA per sequence, no merge.  Otherwise the key tiles of all sequences are spread
+  // At most 128 CTAs: at B = 128 one CTA per sequence on 128 SMs ran 0.047 ms under graph
+  // replay, the stream-K split over 152 SMs 0.068 ms (0.053 ms for its main kernel alone: each
+  // CTA then switches sequence mid-stream).  B equal to the CTA count: one CTA per sequence, no
+  // merge.  Otherwise the key tiles of all sequences are spread
   // evenly over the CTAs and the pieces of split sequences merged afterwards.
   const int ctas = std::min(sm_count(), kLatMaxCtas);
   const bool streamk = B != ctas;
@@ -1697,8 +1697,14 @@ attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, i
   if (B > kLatMaxB) return ATTN_ERR_UNSUPPORTED;
   const bool f8 = dt == ATTN_FP8_E5M2;
   CUtensorMap tc;
-  if (!make_tmap_3d(&tc, c, f8 ? 1 : 2, kLatQK, Lmax, B, f8 ? 128 : 64, kTileKeys, 128))
-    return ATTN_ERR_CUDA;
+  const int esz = f8 ? 1 : 2;
+  const uint32_t chunk = 128 / esz;  // elements per 128-byte column chunk of a cache row
+  const uint64_t dims[4] = {chunk, static_cast<uint64_t>(Lmax), kLatQK / chunk,
+                            static_cast<uint64_t>(B)};
+  const uint64_t strides[3] = {static_cast<uint64_t>(kLatQK) * esz, 128,
+                               static_cast<uint64_t>(Lmax) * kLatQK * esz};
+  const uint32_t box[4] = {chunk, kTileKeys, kLatQK / chunk, 1};
+  if (!make_tmap_4d(&tc, c, esz, dims, strides, box)) return ATTN_ERR_CUDA;
   LatParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.lens = lens;

@@ -56,6 +56,12 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t i
                   uint64_t mid, uint64_t outer, uint32_t box_inner, uint32_t box_mid,
                   int swizzle_bytes, uint64_t mid_pitch = 0);
 
+// Encode a 4-D tiled TMA descriptor over sizes dims[0..3] (innermost first, dims[0] contiguous)
+// with byte strides strides[0..2] for dims 1..3 (any order of magnitude: a view may step through
+// a row in chunks), box box[0..3] and 128-byte swizzling.  Returns false on failure.
+bool make_tmap_4d(CUtensorMap* map, const void* base, int elem_bytes, const uint64_t dims[4],
+                  const uint64_t strides[3], const uint32_t box[4]);
+
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize), done once per (kernel, device, size).
 bool set_smem_attr(const void* kernel, int bytes);
 
