@@ -1068,6 +1068,373 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
   }
 }
 
+// ------------------------------------------------------------------------------------------------
+// D = 256 (bf16): one 128-row Q tile per item, S double-buffered in TMEM, K / V through a ring of
+// 16 KB chunks.
+//
+// With 64 KB K and V tiles, one stage each fits next to the 64 KB Q tile, so the next S could
+// only start once the K stage had been refilled after the previous S: each KV step ran S, the
+// softmax and P V one after the other.  Here the 128 KB of K / V stages form a ring of eight
+// 16 KB chunks in the order the tensor core reads them: a K chunk is one 64-dim column box of a K
+// tile (four K steps of S), a V chunk is 32 keys x 256 dims (two K steps of P V), landed by one
+// 4-D TMA copy as four 128-byte-swizzled 64-dim column groups.  TMEM holds S in two buffers
+// (columns 0 and 128, S_j in buffer j & 1) and O in columns 256..511, so S_{j+1} is computed
+// while the softmax of step j runs, and the tensor core alternates S_{j+2}, P_{j+1} V, ...
+//
+//   warps 0-3   softmax (one TMEM lane quarter each; P released in two halves as above)
+//   warp 4      TMA producer (Q tile, then the chunks in the MMA's order)
+//   warp 5      MMA issuer
+// ------------------------------------------------------------------------------------------------
+constexpr int kD256 = 256;
+constexpr int kD256Threads = 192;
+constexpr int kD256Producer = 4;
+constexpr int kD256Mma = 5;
+constexpr int kD256Chunks = 8;                     // ring slots
+constexpr int kD256ChunkBytes = 16384;
+constexpr int kD256QBoxBytes = BM * 128;          // one 64-dim box of the Q tile
+constexpr int kD256QBytes = 4 * kD256QBoxBytes;   // 64 KB
+constexpr int kD256VKeys = 32;                     // keys per V chunk
+constexpr int kD256VGroupBytes = kD256VKeys * 128; // one 64-dim column group of a V chunk
+constexpr int kD256RingOff = kD256QBytes;
+constexpr int kD256BarOff = kD256RingOff + kD256Chunks * kD256ChunkBytes;
+constexpr int kD256SmemBytes = kD256BarOff + 1024 + 1024;
+static_assert(kD256SmemBytes <= 232448, "shared memory per CTA");
+
+struct D256Bars {
+  uint64_t full[kD256Chunks], empty[kD256Chunks];
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2];  // S_j computed (buffer j & 1)
+  uint64_t p_full, p_hi;  // P of keys 0..63 / 64..127 written
+  uint64_t pv_done;       // the P V products of the step completed
+  uint64_t o_full, o_empty;
+  uint32_t tmem_slot;
+};
+static_assert(sizeof(D256Bars) <= 1024, "barrier block");
+
+__global__ void __launch_bounds__(kD256Threads, 1)
+    prefill_d256_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  D256Bars* bars = reinterpret_cast<D256Bars*>(smem + kD256BarOff);
+  uint8_t* ring = smem + kD256RingOff;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kD256Chunks; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->p_hi, 128);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_empty, 128);
+    fence_barrier_init();
+  }
+  if (warp == kD256Mma) tmem_alloc(&bars->tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_slot;
+  const int rounds = (p.n_items + gridDim.x - 1) / gridDim.x;
+
+  if (warp == kD256Producer) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      uint32_t ph_qe = 0, ph = 0;
+      int slot = 0;
+      bool ok = true;
+      auto next_slot = [&]() -> uint8_t* {
+        if (!(ok = mbar_wait(&bars->empty[slot], ph ^ 1, p.status))) return nullptr;
+        mbar_arrive_expect_tx(&bars->full[slot], kD256ChunkBytes);
+        return ring + slot * kD256ChunkBytes;
+      };
+      auto advance = [&]() {
+        if (++slot == kD256Chunks) { slot = 0; ph ^= 1; }
+      };
+      for (int r = 0; r < rounds && ok; ++r) {
+        const int it = item_for(r, blockIdx.x, gridDim.x);
+        if (it >= p.n_items) continue;
+        int m, b, hq;
+        item_coords(p, it, m, b, hq);
+        const int n = kv_tiles_for(p, m * BM);
+        if (n == 0) continue;
+        const int bhk = b * p.Hkv + hq / p.G;
+        if (!(ok = mbar_wait(&bars->q_empty, ph_qe ^ 1, p.status))) break;
+        ph_qe ^= 1;
+        mbar_arrive_expect_tx(&bars->q_full, kD256QBytes);
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx)
+          tma_load_3d(smem + bx * kD256QBoxBytes, &tmQ, &bars->q_full, bx * 64, m * BM,
+                      b * p.Hq + hq);
+        // the chunks of K_j: four 64-dim column boxes
+        auto load_k = [&](int j) {
+          for (int bx = 0; bx < 4 && ok; ++bx) {
+            uint8_t* dst = next_slot();
+            if (!dst) return;
+            tma_load_3d(dst, &tmK, &bars->full[slot], bx * 64, j * BN, bhk);
+            advance();
+          }
+        };
+        // the chunks of V_j: 32 keys each, all 256 dims in one 4-D copy
+        auto load_v = [&](int j) {
+          for (int c = 0; c < BN / kD256VKeys && ok; ++c) {
+            uint8_t* dst = next_slot();
+            if (!dst) return;
+            tma_load_4d(dst, &tmV, &bars->full[slot], 0, j * BN + c * kD256VKeys, 0, bhk);
+            advance();
+          }
+        };
+        load_k(0);
+        if (n > 1) load_k(1);
+        for (int j = 0; j < n && ok; ++j) {
+          load_v(j);
+          if (j + 2 < n) load_k(j + 2);
+        }
+      }
+    }
+  } else if (warp == kD256Mma) {
+    // ------------------------------------------------------------------ MMA issuer
+    const uint32_t idesc_s = make_idesc(1, 1, false, false, BN, BM);
+    const uint32_t idesc_pv = make_idesc(1, 1, false, true, kD256, BM);  // V MN-major
+    const uint64_t q_desc0 = smem_desc(smem_u32(smem), 16, 1024, 2);
+    const uint64_t r_desc0 = smem_desc(smem_u32(ring), 16, 1024, 2);  // K chunk (K-major)
+    const uint64_t v_desc0 = smem_desc(smem_u32(ring), kD256VGroupBytes, 1024, 2);  // V chunk
+    uint32_t ph = 0, ph_q = 0, ph_pf = 0, ph_oe = 0;
+    int slot = 0;
+    bool ok = true;
+    auto wait_chunk = [&]() {
+      ok = mbar_wait_warp(&bars->full[slot], ph, p.status);
+      tc_fence_after();
+      return ok;
+    };
+    auto release_chunk = [&]() {
+      umma_commit_e(&bars->empty[slot]);
+      if (++slot == kD256Chunks) { slot = 0; ph ^= 1; }
+    };
+    // S_j = Q K_j^T into buffer `buf`: per K chunk (64 dims), its four K steps
+    auto issue_s = [&](int buf) {
+      const uint32_t d = tmem + buf * 128;
+      for (int bx = 0; bx < 4 && ok; ++bx) {
+        if (!wait_chunk()) return;
+        const uint64_t ad = q_desc0 + static_cast<uint64_t>((bx * kD256QBoxBytes) >> 4);
+        const uint64_t bd = r_desc0 + static_cast<uint64_t>((slot * kD256ChunkBytes) >> 4);
+        issue_batched<false, false, 0, 4>(
+            d, [&](int kk) { return ad + static_cast<uint64_t>((kk * 32) >> 4); },
+            [&](int kk) { return bd + static_cast<uint64_t>((kk * 32) >> 4); }, idesc_s, bx > 0);
+        release_chunk();
+      }
+    };
+    // O += P_j V_j for V chunks [c0, c1) (P_j: TMEM columns of buffer `buf`, 8 per 16 keys)
+    auto issue_pv = [&](int buf, int c0, int c1, bool acc) {
+      for (int c = c0; c < c1 && ok; ++c) {
+        if (!wait_chunk()) return;
+        const uint32_t pcol = tmem + buf * 128 + c * 16;
+        const uint64_t bd = v_desc0 + static_cast<uint64_t>((slot * kD256ChunkBytes) >> 4);
+        issue_batched<false, true, 0, 2>(
+            tmem + 256, [&](int kk) { return pcol + kk * 8; },
+            [&](int kk) { return bd + static_cast<uint64_t>((kk * 16 * 128) >> 4); }, idesc_pv,
+            acc || c > 0);
+        release_chunk();
+      }
+    };
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int it = item_for(r, blockIdx.x, gridDim.x);
+      if (it >= p.n_items) continue;
+      int m, b, hq;
+      item_coords(p, it, m, b, hq);
+      const int n = kv_tiles_for(p, m * BM);
+      if (n == 0) continue;
+      if (!(ok = mbar_wait_warp(&bars->q_full, ph_q, p.status))) break;
+      ph_q ^= 1;
+      tc_fence_after();
+      issue_s(0);
+      umma_commit_e(&bars->s_full[0]);
+      if (n > 1) {
+        issue_s(1);
+        umma_commit_e(&bars->s_full[1]);
+      }
+      if (n <= 2) umma_commit_e(&bars->q_empty);
+      for (int j = 0; j < n && ok; ++j) {
+        const int buf = j & 1;
+        // P_j V_j in halves as the softmax releases them; O is free once the previous item's
+        // epilogue has read it
+        if (!(ok = mbar_wait_warp(&bars->p_full, ph_pf, p.status))) break;
+        if (j == 0) {
+          if (!(ok = mbar_wait_warp(&bars->o_empty, ph_oe ^ 1, p.status))) break;
+          ph_oe ^= 1;
+        }
+        tc_fence_after();
+        issue_pv(buf, 0, 2, j > 0);
+        if (!ok) break;
+        if (!(ok = mbar_wait_warp(&bars->p_hi, ph_pf, p.status))) break;
+        ph_pf ^= 1;
+        tc_fence_after();
+        issue_pv(buf, 2, 4, true);
+        if (!ok) break;
+        umma_commit_e(&bars->pv_done);
+        if (j == n - 1) umma_commit_e(&bars->o_full);
+        // S_{j+2} into this buffer (after P_j V read P_j from it: the tensor core runs in order)
+        if (j + 2 < n) {
+          issue_s(buf);
+          umma_commit_e(&bars->s_full[buf]);
+          if (j + 2 == n - 1) umma_commit_e(&bars->q_empty);
+        }
+      }
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ softmax warpgroup
+    const int lrow = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tO = tmem + lane_off + 256;
+    uint32_t ph_s[2] = {0, 0}, ph_o = 0, ph_pv = 0;
+    bool ok = true;
+    for (int r = 0; r < rounds && ok; ++r) {
+      const int it = item_for(r, blockIdx.x, gridDim.x);
+      if (it >= p.n_items) continue;
+      int m, b, hq;
+      item_coords(p, it, m, b, hq);
+      const int r0 = m * BM;
+      const int n = kv_tiles_for(p, r0);
+      if (n == 0) continue;
+      const int row = r0 + lrow;
+      float m_run = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        const int buf = j & 1;
+        const uint32_t tS = tmem + lane_off + buf * 128;
+        if (!(ok = mbar_wait(&bars->s_full[buf], ph_s[buf], p.status))) break;
+        ph_s[buf] ^= 1;
+        tc_fence_after();
+        const bool need_mask = (p.causal && j * BN + BN - 1 > r0 + p.off) || (j * BN + BN > p.Skv);
+        const int lim = (p.causal ? min(row + p.off + 1, p.Skv) : p.Skv) - j * BN;
+        uint32_t sr[128];
+        tmem_ld128(tS, sr);
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 128; ++e)
+            if (e >= lim) sr[e] = __float_as_uint(-INFINITY);
+        }
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 128; e += 8) {
+          a0 = fmax3(a0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+          a1 = fmax3(a1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+          a2 = fmax3(a2, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+          a3 = fmax3(a3, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
+        }
+        const float m_tile = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * p.c_log2;
+        float f = 1.f;
+        if (j == 0) {
+          m_run = m_tile;
+        } else if (m_tile > m_run + kRescaleThreshold) {
+          f = fast_exp2(m_run - m_tile);
+          l *= f;
+          m_run = m_tile;
+        }
+        const float2 c2 = make_float2(p.c_log2, p.c_log2);
+        const float2 nm2 = make_float2(-m_run, -m_run);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 64 * h; e < 64 * h + 64; e += 8) {
+            float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
+            float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nm2);
+            float2 x2 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5])), c2, nm2);
+            float2 x3 = __ffma2_rn(make_float2(__uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7])), c2, nm2);
+            x0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+            x1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+            x2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
+            x3 = make_float2(fast_exp2(x3.x), fast_exp2(x3.y));
+            acc0 = __fadd2_rn(acc0, x0);
+            acc1 = __fadd2_rn(acc1, x1);
+            acc2 = __fadd2_rn(acc2, x2);
+            acc3 = __fadd2_rn(acc3, x3);
+            const int w = (e - 64 * h) / 2;
+            pk[w] = pack_bf16(x0.x, x0.y);
+            pk[w + 1] = pack_bf16(x1.x, x1.y);
+            pk[w + 2] = pack_bf16(x2.x, x2.y);
+            pk[w + 3] = pack_bf16(x3.x, x3.y);
+          }
+          if (h == 0 && j > 0) {
+            // P_{j-1} V has completed: O holds the tiles before j; rescale it (warp-uniformly,
+            // eight columns at a time) before P_j V accumulates onto it
+            if (!(ok = mbar_wait(&bars->pv_done, ph_pv, p.status))) break;
+            ph_pv ^= 1;
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll 1
+              for (int c = 0; c < kD256 / 8; ++c) {
+                uint32_t ov[8];
+                tmem_ld8(tO + c * 8, ov);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+                tmem_st8(tO + c * 8, ov);
+              }
+            }
+          }
+          tmem_st32(tS + 32 * h, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(h ? &bars->p_hi : &bars->p_full);
+        }
+        if (!ok) break;
+        const float2 accs = __fadd2_rn(__fadd2_rn(acc0, acc1), __fadd2_rn(acc2, acc3));
+        l += accs.x + accs.y;
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16, LSE.  The item's last pv_done completes with o_full: consume
+      // it here, so that the phase the next item waits for is never two phases ahead
+      if (!(ok = mbar_wait(&bars->o_full, ph_o, p.status))) break;
+      ph_o ^= 1;
+      if (!(ok = mbar_wait(&bars->pv_done, ph_pv, p.status))) break;
+      ph_pv ^= 1;
+      tc_fence_after();
+      const float inv = p.v_scale / l;
+      __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.S + row) * kD256;
+#pragma unroll 1
+      for (int c = 0; c < kD256 / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tO + c * 32, ov);
+        if (row < p.S) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(ov[q4 * 8 + 0]) * inv, __uint_as_float(ov[q4 * 8 + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(ov[q4 * 8 + 2]) * inv, __uint_as_float(ov[q4 * 8 + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(ov[q4 * 8 + 4]) * inv, __uint_as_float(ov[q4 * 8 + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(ov[q4 * 8 + 6]) * inv, __uint_as_float(ov[q4 * 8 + 7]) * inv);
+            dst[q4] = w;
+          }
+        }
+      }
+      if (p.lse && row < p.S)
+        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.S + row] = (m_run + log2f(l)) * kLn2;
+      tc_fence_before();
+      mbar_arrive(&bars->o_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kD256Mma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 template <int D, int RM, int ESZ, int NTT>
 attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o, float* lse,
                            float q_scale, float k_scale, float v_scale, int B, int Hq, int Hkv,
@@ -1119,6 +1486,50 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   return launch_status();
 }
 
+// D = 256, bf16, no in-kernel RoPE (the rotation passes serve it)
+attn_status_t launch_d256(const void* q, const void* k, const void* v, void* o, float* lse,
+                          float v_scale, int B, int Hq, int Hkv, int S, int Skv, int kv_pitch,
+                          int causal, float scale, cudaStream_t st) {
+  const uint64_t pitch = kv_pitch ? static_cast<uint64_t>(kv_pitch) : static_cast<uint64_t>(Skv);
+  CUtensorMap tq, tk, tv;
+  // V as {64 dims, key, 64-dim column group, (batch, KV head)}: one box = a 32-key chunk
+  const uint64_t vdims[4] = {64, static_cast<uint64_t>(Skv), kD256 / 64,
+                             static_cast<uint64_t>(B) * Hkv};
+  const uint64_t vstrides[3] = {kD256 * 2, 128, pitch * kD256 * 2};
+  const uint32_t vbox[4] = {64, kD256VKeys, kD256 / 64, 1};
+  if (!make_tmap_3d(&tq, q, 2, kD256, S, static_cast<uint64_t>(B) * Hq, 64, BM, 128) ||
+      !make_tmap_3d(&tk, k, 2, kD256, Skv, static_cast<uint64_t>(B) * Hkv, 64, BN, 128,
+                    kv_pitch) ||
+      !make_tmap_4d(&tv, v, 2, vdims, vstrides, vbox))
+    return ATTN_ERR_CUDA;
+  Params p{};
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.status = device_status_ptr();
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.S = S;
+  p.Skv = Skv;
+  p.off = Skv - S;
+  p.rope_k = 0;
+  p.causal = causal;
+  p.nM = (S + BM - 1) / BM;
+  p.nKV = (Skv + BN - 1) / BN;
+  p.n_items = p.nM * B * Hq;
+  p.mblk = causal ? (p.nM > 16 ? std::max(1, 16 / p.G) : 1) : p.nM;
+  p.c_log2 = scale * 1.4426950408889634f;
+  p.v_scale = v_scale;
+  p.table = nullptr;
+  p.pos0 = 0;
+  if (!set_smem_attr(reinterpret_cast<const void*>(prefill_d256_kernel), kD256SmemBytes))
+    return ATTN_ERR_CUDA;
+  const int grid = std::min(p.n_items, sm_count());
+  prefill_d256_kernel<<<grid, kD256Threads, kD256SmemBytes, st>>>(tq, tk, tv, p);
+  return launch_status();
+}
+
 std::atomic<int> g_forced_tiles{0};  // Q tiles per item for D <= 128 (0: the default, two)
 
 }  // namespace
@@ -1139,7 +1550,8 @@ attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* 
                                         Hkv, S, Skv, kv_pitch, causal, scale, table, rope_k, \
                                         pos0, st);
   ATTN_PREFILL_CASE(128, 0, 2, 2)
-  ATTN_PREFILL_CASE(256, 0, 2, 1)
+  if (D == 256 && rm == 0 && esz == 2)
+    return launch_d256(q, k, v, o, lse, v_scale, B, Hq, Hkv, S, Skv, kv_pitch, causal, scale, st);
   ATTN_PREFILL_CASE(128, 1, 2, 2)
   ATTN_PREFILL_CASE(64, 0, 2, 2)
   ATTN_PREFILL_CASE(64, 1, 2, 2)
