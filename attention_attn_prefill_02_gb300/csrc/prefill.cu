@@ -1,6 +1,7 @@
 // prefill.cu — grouped-query attention prefill on the 5th-generation tensor cores (tcgen05).
 //
-// One persistent CTA per SM.  A work item is 256 query rows (two 128-row Q tiles) of one
+// One persistent CTA per SM.  (Head dim 256 runs prefill_d256_kernel, at the end of this file.)
+// A work item is 256 query rows (two 128-row Q tiles) of one
 // (batch, query head); items are ordered heaviest-first for causal attention and dealt to CTAs
 // in a serpentine order (the persistent, causal-aware scheduling of the persistent-attention
 // refactor page, "概要").  Inside a CTA the roles are warp-specialised:
@@ -32,11 +33,10 @@ namespace {
 
 constexpr int BM = 128;  // query rows per Q tile (TMEM lanes)
 constexpr int BN = 128;  // keys per KV tile
-// Q tiles per work item by default: two (the ping-pong of the two softmax warpgroups) up to
-// D = 128; one at D = 256, whose O takes 256 TMEM columns (S 128 + O 256 fit the 512; two tiles
-// would not).  D <= 128 can also run one tile per item (128-row items: twice as many, each
-// without the ping-pong), the second tile configuration of the global-vs-per-shape comparison.
-__host__ __device__ constexpr int tiles_per_item(int D) { return D >= 256 ? 1 : 2; }
+// Q tiles per work item in the kernel below (D <= 128): two by default (the ping-pong of the two
+// softmax warpgroups), or one (128-row items: twice as many, each without the ping-pong), the
+// second tile configuration of the global-vs-per-shape comparison.  D = 256 has a kernel of its
+// own at the end of this file.
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kRopeWarp0 = 10;  // fused RoPE: warps 10-13 rotate each K tile in shared memory
@@ -58,8 +58,9 @@ struct Swz {
   static constexpr int kSBO = 8 * kSwz;                                      // 8-row group
 };
 
-template <int D, int ESZ, bool STAGED, int NT_ = tiles_per_item(D)>
+template <int D, int ESZ, bool STAGED, int NT_>
 struct Cfg {
+  static_assert(D == 64 || D == 128, "the generic kernel's head dims");
   // Q / K tiles read by the QK^T MMA
   static constexpr int kQKE = STAGED ? 2 : ESZ;
   static constexpr int kRowBytes = D * kQKE;
@@ -87,13 +88,10 @@ struct Cfg {
   static constexpr int kStTileBytes = STAGED ? BM * D : 0;
   // Separate K and V rings; K is fetched one KV step ahead of V, so a K tile has about two KV
   // steps between landing and its first MMA (room for the TMA latency plus the fused RoPE).
-  // (D = 256: one 64 KB K and one 64 KB V stage next to the 64 KB Q tile)
-  static constexpr int kKStages =
-      STAGED ? 2 : ESZ == 2 ? (D == 256 ? 1 : D == 128 ? 3 : 4) : (D == 128 ? 4 : 6);
-  static constexpr int kVStages =
-      STAGED ? 2 : ESZ == 2 ? (D == 256 ? 1 : D == 128 ? 2 : 3) : (D == 128 ? 4 : 6);
+  static constexpr int kKStages = STAGED ? 2 : ESZ == 2 ? (D == 128 ? 3 : 4) : (D == 128 ? 4 : 6);
+  static constexpr int kVStages = STAGED ? 2 : ESZ == 2 ? (D == 128 ? 2 : 3) : (D == 128 ? 4 : 6);
   static constexpr int kNT = NT_;
-  static_assert(NT_ == 1 || (NT_ == 2 && D <= 128), "two Q tiles per item need D <= 128");
+  static_assert(NT_ == 1 || NT_ == 2, "one or two Q tiles per item");
   static constexpr int kQOff = 0;
   static constexpr int kQStOff = kQOff + kNT * kQTileBytes;
   static constexpr int kKVOff = kQStOff + 2 * kStTileBytes;
@@ -106,7 +104,6 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
   static_assert(kKStages <= 8 && kVStages <= 8, "barrier arrays hold 8 stages");
-  // O of the second Q tile exists only with two tiles per item (D = 256 has one)
   static_assert(kNT == 1 || kColO1 + D <= kTmemCols, "TMEM columns of O1 past the allocation");
   static_assert(!STAGED || D == 128, "fp8 with fused RoPE is built for D = 128");
 };
