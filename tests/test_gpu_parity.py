@@ -782,7 +782,10 @@ def test_backward_through_rope(style, bwd_path):
     (1, 2, 2, 200, False, False),
     (1, 4, 4, 513, True, True),
     (2, 32, 8, 1024, True, False),   # 256 items, more than the SMs: CTAs run several items, so
-                                     # the single-stage rings and Q/O phases carry over
+                                     # the chunk ring, both S buffers and the Q/O phases carry over
+    (1, 2, 1, 1, True, False),       # one query row, one masked key tile
+    (1, 16, 1, 257, True, False),    # 16 query heads per KV head, ragged tail
+    (1, 4, 2, 640, False, False),    # five KV tiles per item: the 8-chunk ring wraps every step
 ])
 def test_prefill_d256(B, Hq, Hkv, S, causal, rope):
     q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, 256, "bf16", seed=S + 256)
@@ -794,8 +797,9 @@ def test_prefill_d256(B, Hq, Hkv, S, causal, rope):
     check(lse.cpu(), rl, ROPE_LSE_TOL if rope else LSE_TOL, None, what="LSE prefill D=256")
 
 
-def test_prefill_chunk_d256():
-    B, Hq, Hkv, Sq, Skv, pitch, D = 2, 8, 2, 64, 300, 320, 256
+@pytest.mark.parametrize("Sq,Skv,pitch", [(64, 300, 320), (200, 1000, 1000), (1, 129, 160)])
+def test_prefill_chunk_d256(Sq, Skv, pitch):
+    B, Hq, Hkv, D = 2, 8, 2, 256
     q = synthetic.normal((B, Hq, Sq, D), 960, "bf16")
     kc = synthetic.normal((B, Hkv, pitch, D), 961, "bf16")
     vc = synthetic.normal((B, Hkv, pitch, D), 962, "bf16")
