@@ -122,9 +122,10 @@ attn_status_t attn_prefill(const void* q, const void* k, const void* v, void* o,
   if (static_cast<long long>(S) > (1LL << 30) || static_cast<long long>(B) * Hq > (1LL << 24))
     return ATTN_ERR_UNSUPPORTED;
   // the interleaved pairing runs only as rope_apply passes (bf16; the kernel's in-tile rotation
-  // is the half-split form); so does every rotation at D = 256 (bf16 only, one Q tile per item)
+  // is the half-split form); so does every rotation at D = 256, which therefore takes fp8 only
+  // without RoPE (rotated fp8 tiles would have to stay bf16)
   if (il && (rope == 2 || dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
-  if (D == 256 && (rope == 2 || dtype != ATTN_BF16)) return ATTN_ERR_UNSUPPORTED;
+  if (D == 256 && (rope == 2 || (rope && dtype != ATTN_BF16))) return ATTN_ERR_UNSUPPORTED;
   const size_t ws_need = prefill_ws_bytes(B, Hq, Hkv, S, D, dtype, rope, il);
   if (ws_need > 0 && (!workspace || workspace_bytes < ws_need || !aligned16(workspace)))
     return ATTN_ERR_WORKSPACE;
@@ -215,7 +216,6 @@ attn_status_t attn_prefill_chunk(const void* q, const void* k, const void* v, vo
   if (static_cast<long long>(kv_pitch) > (1LL << 30) || static_cast<long long>(B) * Hq > (1LL << 24))
     return ATTN_ERR_UNSUPPORTED;
   if (rope && dtype == ATTN_FP8_E5M2 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (D == 256 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   if (il && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   const size_t ws_need = chunk_ws_bytes(B, Hq, Sq, D, dtype, rope);
   if (ws_need > 0 && (!workspace || workspace_bytes < ws_need || !aligned16(workspace)))

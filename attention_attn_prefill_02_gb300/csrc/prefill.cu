@@ -1088,14 +1088,28 @@ constexpr int kD256Producer = 4;
 constexpr int kD256Mma = 5;
 constexpr int kD256Chunks = 8;                     // ring slots
 constexpr int kD256ChunkBytes = 16384;
-constexpr int kD256QBoxBytes = BM * 128;          // one 64-dim box of the Q tile
-constexpr int kD256QBytes = 4 * kD256QBoxBytes;   // 64 KB
-constexpr int kD256VKeys = 32;                     // keys per V chunk
-constexpr int kD256VGroupBytes = kD256VKeys * 128; // one 64-dim column group of a V chunk
-constexpr int kD256RingOff = kD256QBytes;
-constexpr int kD256BarOff = kD256RingOff + kD256Chunks * kD256ChunkBytes;
-constexpr int kD256SmemBytes = kD256BarOff + 1024 + 1024;
-static_assert(kD256SmemBytes <= 232448, "shared memory per CTA");
+constexpr int kD256QBoxBytes = BM * 128;          // one 128-byte column box of the Q tile
+
+// Geometry by element size (2: bf16; 1: fp8 e5m2, P in e4m3).  Rows of 256 elements are 512 or
+// 256 bytes: four or two 128-byte column boxes.  A K chunk is one box of a K tile (four 32-byte
+// K steps); a V chunk holds kVKeys keys of all 256 dims as kBoxes column groups, two P V K steps
+// (16 bf16 or 32 fp8 keys each).  P takes 8 TMEM columns per K step either way.
+template <int ESZ>
+struct D256Geo {
+  static constexpr int kRowBytes = kD256 * ESZ;
+  static constexpr int kBoxElems = 128 / ESZ;
+  static constexpr int kBoxes = kRowBytes / 128;
+  static constexpr int kQBytes = BM * kRowBytes;
+  static constexpr int kVKeys = kD256ChunkBytes / kRowBytes;
+  static constexpr int kVChunks = BN / kVKeys;
+  static constexpr int kVGroupBytes = kVKeys * 128;
+  static constexpr int kPVKeys = 32 / ESZ;
+  static constexpr int kRingOff = kQBytes;
+  static constexpr int kBarOff = kRingOff + kD256Chunks * kD256ChunkBytes;
+  static constexpr int kSmemBytes = kBarOff + 1024 + 1024;
+  static_assert(kVKeys == 2 * kPVKeys, "two P V K steps per V chunk");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
 
 struct D256Bars {
   uint64_t full[kD256Chunks], empty[kD256Chunks];
@@ -1108,15 +1122,18 @@ struct D256Bars {
 };
 static_assert(sizeof(D256Bars) <= 1024, "barrier block");
 
+template <int ESZ>
 __global__ void __launch_bounds__(kD256Threads, 1)
     prefill_d256_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using G = D256Geo<ESZ>;
+  constexpr bool F8 = ESZ == 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  D256Bars* bars = reinterpret_cast<D256Bars*>(smem + kD256BarOff);
-  uint8_t* ring = smem + kD256RingOff;
+  D256Bars* bars = reinterpret_cast<D256Bars*>(smem + G::kBarOff);
+  uint8_t* ring = smem + G::kRingOff;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kD256Chunks; ++s) {
@@ -1168,26 +1185,26 @@ __global__ void __launch_bounds__(kD256Threads, 1)
         const int bhk = b * p.Hkv + hq / p.G;
         if (!(ok = mbar_wait(&bars->q_empty, ph_qe ^ 1, p.status))) break;
         ph_qe ^= 1;
-        mbar_arrive_expect_tx(&bars->q_full, kD256QBytes);
+        mbar_arrive_expect_tx(&bars->q_full, G::kQBytes);
 #pragma unroll
-        for (int bx = 0; bx < 4; ++bx)
-          tma_load_3d(smem + bx * kD256QBoxBytes, &tmQ, &bars->q_full, bx * 64, m * BM,
-                      b * p.Hq + hq);
-        // the chunks of K_j: four 64-dim column boxes
+        for (int bx = 0; bx < G::kBoxes; ++bx)
+          tma_load_3d(smem + bx * kD256QBoxBytes, &tmQ, &bars->q_full, bx * G::kBoxElems,
+                      m * BM, b * p.Hq + hq);
+        // the chunks of K_j: its 128-byte column boxes
         auto load_k = [&](int j) {
-          for (int bx = 0; bx < 4 && ok; ++bx) {
+          for (int bx = 0; bx < G::kBoxes && ok; ++bx) {
             uint8_t* dst = next_slot();
             if (!dst) return;
-            tma_load_3d(dst, &tmK, &bars->full[slot], bx * 64, j * BN, bhk);
+            tma_load_3d(dst, &tmK, &bars->full[slot], bx * G::kBoxElems, j * BN, bhk);
             advance();
           }
         };
-        // the chunks of V_j: 32 keys each, all 256 dims in one 4-D copy
+        // the chunks of V_j: kVKeys keys each, all 256 dims in one 4-D copy
         auto load_v = [&](int j) {
-          for (int c = 0; c < BN / kD256VKeys && ok; ++c) {
+          for (int c = 0; c < G::kVChunks && ok; ++c) {
             uint8_t* dst = next_slot();
             if (!dst) return;
-            tma_load_4d(dst, &tmV, &bars->full[slot], 0, j * BN + c * kD256VKeys, 0, bhk);
+            tma_load_4d(dst, &tmV, &bars->full[slot], 0, j * BN + c * G::kVKeys, 0, bhk);
             advance();
           }
         };
@@ -1201,11 +1218,12 @@ __global__ void __launch_bounds__(kD256Threads, 1)
     }
   } else if (warp == kD256Mma) {
     // ------------------------------------------------------------------ MMA issuer
+    // bf16 (format 1) x bf16, or e5m2 (1) x e5m2 for S and e4m3 (0) P x e5m2 V for P V
     const uint32_t idesc_s = make_idesc(1, 1, false, false, BN, BM);
-    const uint32_t idesc_pv = make_idesc(1, 1, false, true, kD256, BM);  // V MN-major
+    const uint32_t idesc_pv = make_idesc(F8 ? 0u : 1u, 1, false, true, kD256, BM);  // V MN-major
     const uint64_t q_desc0 = smem_desc(smem_u32(smem), 16, 1024, 2);
     const uint64_t r_desc0 = smem_desc(smem_u32(ring), 16, 1024, 2);  // K chunk (K-major)
-    const uint64_t v_desc0 = smem_desc(smem_u32(ring), kD256VGroupBytes, 1024, 2);  // V chunk
+    const uint64_t v_desc0 = smem_desc(smem_u32(ring), G::kVGroupBytes, 1024, 2);  // V chunk
     uint32_t ph = 0, ph_q = 0, ph_pf = 0, ph_oe = 0;
     int slot = 0;
     bool ok = true;
@@ -1218,29 +1236,29 @@ __global__ void __launch_bounds__(kD256Threads, 1)
       umma_commit_e(&bars->empty[slot]);
       if (++slot == kD256Chunks) { slot = 0; ph ^= 1; }
     };
-    // S_j = Q K_j^T into buffer `buf`: per K chunk (64 dims), its four K steps
+    // S_j = Q K_j^T into buffer `buf`: per K chunk (128 bytes of the rows), its four K steps
     auto issue_s = [&](int buf) {
       const uint32_t d = tmem + buf * 128;
-      for (int bx = 0; bx < 4 && ok; ++bx) {
+      for (int bx = 0; bx < G::kBoxes && ok; ++bx) {
         if (!wait_chunk()) return;
         const uint64_t ad = q_desc0 + static_cast<uint64_t>((bx * kD256QBoxBytes) >> 4);
         const uint64_t bd = r_desc0 + static_cast<uint64_t>((slot * kD256ChunkBytes) >> 4);
-        issue_batched<false, false, 0, 4>(
+        issue_batched<F8, false, 0, 4>(
             d, [&](int kk) { return ad + static_cast<uint64_t>((kk * 32) >> 4); },
             [&](int kk) { return bd + static_cast<uint64_t>((kk * 32) >> 4); }, idesc_s, bx > 0);
         release_chunk();
       }
     };
-    // O += P_j V_j for V chunks [c0, c1) (P_j: TMEM columns of buffer `buf`, 8 per 16 keys)
+    // O += P_j V_j for V chunks [c0, c1) (P_j: TMEM columns of buffer `buf`, 8 per K step)
     auto issue_pv = [&](int buf, int c0, int c1, bool acc) {
       for (int c = c0; c < c1 && ok; ++c) {
         if (!wait_chunk()) return;
         const uint32_t pcol = tmem + buf * 128 + c * 16;
         const uint64_t bd = v_desc0 + static_cast<uint64_t>((slot * kD256ChunkBytes) >> 4);
-        issue_batched<false, true, 0, 2>(
+        issue_batched<F8, true, 0, 2>(
             tmem + 256, [&](int kk) { return pcol + kk * 8; },
-            [&](int kk) { return bd + static_cast<uint64_t>((kk * 16 * 128) >> 4); }, idesc_pv,
-            acc || c > 0);
+            [&](int kk) { return bd + static_cast<uint64_t>((kk * G::kPVKeys * 128) >> 4); },
+            idesc_pv, acc || c > 0);
         release_chunk();
       }
     };
@@ -1271,12 +1289,12 @@ __global__ void __launch_bounds__(kD256Threads, 1)
           ph_oe ^= 1;
         }
         tc_fence_after();
-        issue_pv(buf, 0, 2, j > 0);
+        issue_pv(buf, 0, G::kVChunks / 2, j > 0);
         if (!ok) break;
         if (!(ok = mbar_wait_warp(&bars->p_hi, ph_pf, p.status))) break;
         ph_pf ^= 1;
         tc_fence_after();
-        issue_pv(buf, 2, 4, true);
+        issue_pv(buf, G::kVChunks / 2, G::kVChunks, true);
         if (!ok) break;
         umma_commit_e(&bars->pv_done);
         if (j == n - 1) umma_commit_e(&bars->o_full);
@@ -1342,7 +1360,7 @@ __global__ void __launch_bounds__(kD256Threads, 1)
         float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
+          uint32_t pk[F8 ? 16 : 32];  // 64 keys: packed bf16 pairs or e4m3 quads
 #pragma unroll
           for (int e = 64 * h; e < 64 * h + 64; e += 8) {
             float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
@@ -1357,11 +1375,19 @@ __global__ void __launch_bounds__(kD256Threads, 1)
             acc1 = __fadd2_rn(acc1, x1);
             acc2 = __fadd2_rn(acc2, x2);
             acc3 = __fadd2_rn(acc3, x3);
-            const int w = (e - 64 * h) / 2;
-            pk[w] = pack_bf16(x0.x, x0.y);
-            pk[w + 1] = pack_bf16(x1.x, x1.y);
-            pk[w + 2] = pack_bf16(x2.x, x2.y);
-            pk[w + 3] = pack_bf16(x3.x, x3.y);
+            const int w = e - 64 * h;
+            if constexpr (F8) {
+              // e4m3, four keys per TMEM column, lowest key in the lowest byte
+              pk[w / 4] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x0, __NV_SATFINITE, __NV_E4M3)) |
+                          (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x1, __NV_SATFINITE, __NV_E4M3)) << 16);
+              pk[w / 4 + 1] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x2, __NV_SATFINITE, __NV_E4M3)) |
+                              (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(x3, __NV_SATFINITE, __NV_E4M3)) << 16);
+            } else {
+              pk[w / 2] = pack_bf16(x0.x, x0.y);
+              pk[w / 2 + 1] = pack_bf16(x1.x, x1.y);
+              pk[w / 2 + 2] = pack_bf16(x2.x, x2.y);
+              pk[w / 2 + 3] = pack_bf16(x3.x, x3.y);
+            }
           }
           if (h == 0 && j > 0) {
             // P_{j-1} V has completed: O holds the tiles before j; rescale it (warp-uniformly,
@@ -1380,7 +1406,10 @@ __global__ void __launch_bounds__(kD256Threads, 1)
               }
             }
           }
-          tmem_st32(tS + 32 * h, pk);
+          if constexpr (F8)
+            tmem_st16(tS + 16 * h, pk);
+          else
+            tmem_st32(tS + 32 * h, pk);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(h ? &bars->p_hi : &bars->p_full);
@@ -1483,21 +1512,26 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   return launch_status();
 }
 
-// D = 256, bf16, no in-kernel RoPE (the rotation passes serve it)
+// D = 256 (bf16, or fp8 e5m2 without RoPE), no in-kernel RoPE (the rotation passes serve bf16)
+template <int ESZ>
 attn_status_t launch_d256(const void* q, const void* k, const void* v, void* o, float* lse,
-                          float v_scale, int B, int Hq, int Hkv, int S, int Skv, int kv_pitch,
-                          int causal, float scale, cudaStream_t st) {
+                          float q_scale, float k_scale, float v_scale, int B, int Hq, int Hkv,
+                          int S, int Skv, int kv_pitch, int causal, float scale, cudaStream_t st) {
+  using G = D256Geo<ESZ>;
   const uint64_t pitch = kv_pitch ? static_cast<uint64_t>(kv_pitch) : static_cast<uint64_t>(Skv);
   CUtensorMap tq, tk, tv;
-  // V as {64 dims, key, 64-dim column group, (batch, KV head)}: one box = a 32-key chunk
-  const uint64_t vdims[4] = {64, static_cast<uint64_t>(Skv), kD256 / 64,
-                             static_cast<uint64_t>(B) * Hkv};
-  const uint64_t vstrides[3] = {kD256 * 2, 128, pitch * kD256 * 2};
-  const uint32_t vbox[4] = {64, kD256VKeys, kD256 / 64, 1};
-  if (!make_tmap_3d(&tq, q, 2, kD256, S, static_cast<uint64_t>(B) * Hq, 64, BM, 128) ||
-      !make_tmap_3d(&tk, k, 2, kD256, Skv, static_cast<uint64_t>(B) * Hkv, 64, BN, 128,
-                    kv_pitch) ||
-      !make_tmap_4d(&tv, v, 2, vdims, vstrides, vbox))
+  // V as {128 bytes of a row, key, 128-byte column group, (batch, KV head)}: one box = a chunk
+  const uint64_t vdims[4] = {static_cast<uint64_t>(G::kBoxElems), static_cast<uint64_t>(Skv),
+                             static_cast<uint64_t>(G::kBoxes), static_cast<uint64_t>(B) * Hkv};
+  const uint64_t vstrides[3] = {static_cast<uint64_t>(G::kRowBytes), 128,
+                                pitch * G::kRowBytes};
+  const uint32_t vbox[4] = {static_cast<uint32_t>(G::kBoxElems), static_cast<uint32_t>(G::kVKeys),
+                            static_cast<uint32_t>(G::kBoxes), 1};
+  if (!make_tmap_3d(&tq, q, ESZ, kD256, S, static_cast<uint64_t>(B) * Hq, G::kBoxElems, BM,
+                    128) ||
+      !make_tmap_3d(&tk, k, ESZ, kD256, Skv, static_cast<uint64_t>(B) * Hkv, G::kBoxElems, BN,
+                    128, kv_pitch) ||
+      !make_tmap_4d(&tv, v, ESZ, vdims, vstrides, vbox))
     return ATTN_ERR_CUDA;
   Params p{};
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -1516,14 +1550,14 @@ attn_status_t launch_d256(const void* q, const void* k, const void* v, void* o, 
   p.nKV = (Skv + BN - 1) / BN;
   p.n_items = p.nM * B * Hq;
   p.mblk = causal ? (p.nM > 16 ? std::max(1, 16 / p.G) : 1) : p.nM;
-  p.c_log2 = scale * 1.4426950408889634f;
+  p.c_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
   p.v_scale = v_scale;
   p.table = nullptr;
   p.pos0 = 0;
-  if (!set_smem_attr(reinterpret_cast<const void*>(prefill_d256_kernel), kD256SmemBytes))
-    return ATTN_ERR_CUDA;
+  auto kern = prefill_d256_kernel<ESZ>;
+  if (!set_smem_attr(reinterpret_cast<const void*>(kern), G::kSmemBytes)) return ATTN_ERR_CUDA;
   const int grid = std::min(p.n_items, sm_count());
-  prefill_d256_kernel<<<grid, kD256Threads, kD256SmemBytes, st>>>(tq, tk, tv, p);
+  kern<<<grid, kD256Threads, G::kSmemBytes, st>>>(tq, tk, tv, p);
   return launch_status();
 }
 
@@ -1547,8 +1581,11 @@ attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* 
                                         Hkv, S, Skv, kv_pitch, causal, scale, table, rope_k, \
                                         pos0, st);
   ATTN_PREFILL_CASE(128, 0, 2, 2)
-  if (D == 256 && rm == 0 && esz == 2)
-    return launch_d256(q, k, v, o, lse, v_scale, B, Hq, Hkv, S, Skv, kv_pitch, causal, scale, st);
+  if (D == 256 && rm == 0)
+    return esz == 2 ? launch_d256<2>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S,
+                                     Skv, kv_pitch, causal, scale, st)
+                    : launch_d256<1>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S,
+                                     Skv, kv_pitch, causal, scale, st);
   ATTN_PREFILL_CASE(128, 1, 2, 2)
   ATTN_PREFILL_CASE(64, 0, 2, 2)
   ATTN_PREFILL_CASE(64, 1, 2, 2)

@@ -151,7 +151,8 @@ ATTN_API size_t attn_prefill_workspace_size(int B, int Hq, int Hkv, int S, int D
  *            bytes, 16-byte aligned (may be NULL when that size is 0); contents need no
  *            initialisation.  Calls that run at the same time (e.g. on two streams) need
  *            workspaces of their own.
- *   D in {64, 128, 256} (256: bf16 only, rope 0 or 1 with the rotation passes); Hq % Hkv == 0;
+ *   D in {64, 128, 256} (256: bf16 with rope 0 or 1 through the rotation passes, or fp8 with
+ *   rope 0); Hq % Hkv == 0;
  *   S >= 1.  fp8 e5m2 inputs: P is rounded to e4m3 for the PV
  *   product; with rope = 1 (D = 128 only) Q and K are rotated into bf16 tiles inside the
  *   kernel (QK^T then runs in bf16, PV stays fp8), because rotated values re-rounded to fp8
@@ -226,7 +227,7 @@ ATTN_API size_t attn_prefill_chunk_workspace_size(int B, int Hq, int Sq, int D,
  *            1 | ATTN_ROPE_FLAG_INTERLEAVED: pairs (2i, 2i+1), bf16 only (fp8: UNSUPPORTED).
  *   workspace  device buffer of at least attn_prefill_chunk_workspace_size(B,Hq,Sq,D,dtype,
  *            rope) bytes, 16-byte aligned (NULL allowed when that size is 0); no initialisation.
- *   1 <= Sq <= Skv <= kv_pitch; D in {64, 128, 256} (fp8: D <= 128; fp8 with rope = 1: D = 128); the other
+ *   1 <= Sq <= Skv <= kv_pitch; D in {64, 128, 256} (fp8 with rope = 1: D = 128 only); the other
  *   arguments as attn_prefill.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  */

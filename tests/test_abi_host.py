@@ -151,9 +151,9 @@ def test_prefill_validation(L):
     assert _prefill(L, lse=ctypes.c_void_p(0x7F0000000002)) == INVALID
     assert _prefill(L, D=96) == UNSUPPORTED
     assert _prefill(L, D=512) == UNSUPPORTED
-    assert _prefill(L, D=256, dt=1) == UNSUPPORTED     # D = 256: bf16 only
+    assert _prefill(L, D=256, dt=1) == UNSUPPORTED     # D = 256: fp8 without RoPE only
     assert _prefill(L, D=256, rope=2) == UNSUPPORTED   # ... and RoPE through the passes
-    assert _chunk(L, D=256, dt=1, rope=0) == UNSUPPORTED
+    assert _chunk(L, D=256, dt=1, rope=1) == UNSUPPORTED
 
 
 def _chunk(L, **kw):
@@ -305,6 +305,8 @@ def test_valid_calls_report_no_device_without_gpu(L):
     assert _prefill(L, S=16384) == NO_DEVICE
     assert _prefill(L, ws=None, wsb=0) == NO_DEVICE   # S = 128: the kernel rotates, no workspace
     assert _chunk(L) == NO_DEVICE
+    assert _prefill(L, D=256, dt=1, rope=0) == NO_DEVICE   # fp8 at D = 256 without RoPE
+    assert _chunk(L, D=256, dt=1, rope=0) == NO_DEVICE
     assert _decode(L) == NO_DEVICE
     assert _append(L) == NO_DEVICE
     assert _decode(L, ws=None, wsb=0) in (NO_DEVICE, WORKSPACE)

@@ -797,6 +797,50 @@ def test_prefill_d256(B, Hq, Hkv, S, causal, rope):
     check(lse.cpu(), rl, ROPE_LSE_TOL if rope else LSE_TOL, None, what="LSE prefill D=256")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,S,causal", [
+    (1, 4, 1, 128, True),
+    (2, 8, 2, 300, True),      # ragged tail, GQA
+    (1, 2, 2, 200, False),
+    (1, 16, 1, 257, True),     # 16 query heads per KV head
+    (2, 32, 8, 1024, True),    # 256 items: the chunk ring and the phases carry over between items
+])
+def test_prefill_fp8_d256(B, Hq, Hkv, S, causal):
+    """fp8 e5m2 Q/K/V at head dim 256 (no RoPE): 256-byte rows as two 128-byte column boxes,
+    64-key V chunks, P rounded to e4m3; the oracle runs on the dequantised values."""
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, 256, "fp8", seed=S + 11)
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, want_lse=True)
+    status_ok()
+    ro, rl = oracle.prefill(f64(q), f64(k), f64(v), causal=causal)
+    check(o.cpu(), ro, FP8_MAX, 1e-2, what="O fp8 D=256")
+    check(lse.cpu(), rl, 2e-2, None, what="LSE fp8 D=256")
+
+
+def test_prefill_fp8_d256_scales_and_chunk():
+    """fp8 at head dim 256: the dequantisation scales (q stored halved with q_scale = 2, v
+    quartered with v_scale = 4 give the same attention), and a chunk against a cache of pitch
+    320 whose queries start mid-tile, against the oracle."""
+    B, H, S, D = 1, 2, 200, 256
+    q, k, v = synthetic.prefill_inputs(B, H, H, S, D, "fp8", seed=6)
+    o1 = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    qh = (q.float() / 2).to(torch.float8_e5m2)
+    o2 = binding.attn_prefill(qh.cuda(), k.cuda(), v.cuda(), causal=True, q_scale=2.0)
+    vh = (v.float() / 4).to(torch.float8_e5m2)
+    o3 = binding.attn_prefill(q.cuda(), k.cuda(), vh.cuda(), causal=True, v_scale=4.0)
+    status_ok()
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (o1.float() - o3.float()).abs().max().item() <= 1e-2
+    Bc, Hq, Hkv, Sq, Skv, pitch = 2, 8, 2, 70, 300, 320
+    qc = synthetic.normal((Bc, Hq, Sq, D), 980, "fp8")
+    kc = synthetic.normal((Bc, Hkv, pitch, D), 981, "fp8")
+    vc = synthetic.normal((Bc, Hkv, pitch, D), 982, "fp8")
+    o, lse = binding.attn_prefill_chunk(qc.cuda(), kc.cuda(), vc.cuda(), Skv, rope=False,
+                                        want_lse=True)
+    status_ok()
+    ro, rl = oracle.prefill_chunk(f64(qc), f64(kc), f64(vc), Skv)
+    check(o.cpu(), ro, FP8_MAX, 1e-2, what="O chunk fp8 D=256")
+    check(lse.cpu(), rl, 2e-2, None, what="LSE chunk fp8 D=256")
+
+
 @pytest.mark.parametrize("Sq,Skv,pitch", [(64, 300, 320), (200, 1000, 1000), (1, 129, 160)])
 def test_prefill_chunk_d256(Sq, Skv, pitch):
     B, Hq, Hkv, D = 2, 8, 2, 256
