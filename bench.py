@@ -578,6 +578,16 @@ def variants(b, d):
         "attention_graph_tflops": round(fl256 / t_ag / 1e9, 1),
         "attention_frac_of_bf16_burst": round(fl256 / t_ag / 1e9 / burst, 4)}
     del q, k, v, o, ws
+    # the same shape with fp8 e5m2 inputs (attention alone: fp8 at D = 256 takes no RoPE)
+    q, k, v = synthetic.prefill_inputs(4, 32, 8, 4096, 256, "fp8", seed=9)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    t_fg = time_graph(lambda: b.attn_prefill(q, k, v, causal=True, o=o), 5)
+    out["prefill_d256_s4096"].update({
+        "fp8_attention_graph_ms": round(t_fg, 4),
+        "fp8_attention_graph_tflops": round(fl256 / t_fg / 1e9, 1),
+        "fp8_attention_frac_of_fp8_peak": round(fl256 / t_fg / 1e9 / (2 * burst), 4)})
+    del q, k, v, o
     # decode batch sweep: eager vs CUDA-graph replay, L2-resident vs streaming
     sweep = {}
     Dd = DECODE
