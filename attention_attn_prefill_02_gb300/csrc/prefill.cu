@@ -1066,53 +1066,61 @@ __global__ void __launch_bounds__(threads_for(RM), 1)
 }
 
 // ------------------------------------------------------------------------------------------------
-// D = 256 (bf16): one 128-row Q tile per item, S double-buffered in TMEM, K / V through a ring of
-// 16 KB chunks.
+// One Q tile per item, S double-buffered in TMEM, K / V through a ring of 16 KB chunks: the head
+// dim 256 kernel.  (The geometry below is written for any D whose rows are whole 128-byte
+// boxes; at D = 128 the two-tile kernel above measured faster: fp8 causal S = 16384 3.96 ms
+// against 5.84 ms with this one, so only D = 256 dispatches here.)
 //
-// With 64 KB K and V tiles, one stage each fits next to the 64 KB Q tile, so the next S could
-// only start once the K stage had been refilled after the previous S: each KV step ran S, the
-// softmax and P V one after the other.  Here the 128 KB of K / V stages form a ring of eight
-// 16 KB chunks in the order the tensor core reads them: a K chunk is one 64-dim column box of a K
-// tile (four K steps of S), a V chunk is 32 keys x 256 dims (two K steps of P V), landed by one
-// 4-D TMA copy as four 128-byte-swizzled 64-dim column groups.  TMEM holds S in two buffers
-// (columns 0 and 128, S_j in buffer j & 1) and O in columns 256..511, so S_{j+1} is computed
-// while the softmax of step j runs, and the tensor core alternates S_{j+2}, P_{j+1} V, ...
+// At D = 256, 64 KB K and V tiles leave room for one stage each next to the 64 KB Q tile, so the
+// next S could only start once the K stage had been refilled after the previous S: each KV step
+// ran S, the softmax and P V one after the other.  Here the K / V stages form a ring of 16 KB
+// chunks in the order the tensor core reads them: a K chunk is one 128-byte column box of a K
+// tile (four K steps of S), a V chunk is kVKeys keys x all D dims, landed by one 4-D TMA copy as
+// 128-byte-swizzled column groups.  TMEM holds S in two buffers (columns 0 and 128, S_j in
+// buffer j & 1) and O in columns 256.., so S_{j+1} is computed while the softmax of step j runs,
+// and the tensor core alternates S_{j+2}, P_{j+1} V, ...
 //
 //   warps 0-3   softmax (one TMEM lane quarter each; P released in two halves as above)
 //   warp 4      TMA producer (Q tile, then the chunks in the MMA's order)
 //   warp 5      MMA issuer
 // ------------------------------------------------------------------------------------------------
-constexpr int kD256 = 256;
-constexpr int kD256Threads = 192;
-constexpr int kD256Producer = 4;
-constexpr int kD256Mma = 5;
-constexpr int kD256Chunks = 8;                     // ring slots
-constexpr int kD256ChunkBytes = 16384;
-constexpr int kD256QBoxBytes = BM * 128;          // one 128-byte column box of the Q tile
+constexpr int kT1Threads = 192;
+constexpr int kT1Producer = 4;
+constexpr int kT1Mma = 5;
+constexpr int kT1MaxChunks = 12;
+constexpr int kT1ChunkBytes = 16384;
+constexpr int kT1QBoxBytes = BM * 128;  // one 128-byte column box of the Q tile
 
-// Geometry by element size (2: bf16; 1: fp8 e5m2, P in e4m3).  Rows of 256 elements are 512 or
-// 256 bytes: four or two 128-byte column boxes.  A K chunk is one box of a K tile (four 32-byte
-// K steps); a V chunk holds kVKeys keys of all 256 dims as kBoxes column groups, two P V K steps
-// (16 bf16 or 32 fp8 keys each).  P takes 8 TMEM columns per K step either way.
-template <int ESZ>
-struct D256Geo {
-  static constexpr int kRowBytes = kD256 * ESZ;
+// Geometry by head dim and element size (2: bf16; 1: fp8 e5m2, P in e4m3).  Rows of D * ESZ
+// bytes are kBoxes 128-byte column boxes.  A K chunk is one box of a K tile (four 32-byte K
+// steps of S); a V chunk holds kVKeys keys of all D dims as kBoxes column groups, kSpc P V K
+// steps (16 bf16 or 32 fp8 keys each).  P takes 8 TMEM columns per K step either way.  Each
+// half of P (64 keys, released separately by the softmax) is whole V chunks, or (kSpc = all K
+// steps of the tile: fp8 D = 128) half of the one V chunk.
+template <int D, int ESZ>
+struct T1Geo {
+  static constexpr int kRowBytes = D * ESZ;
   static constexpr int kBoxElems = 128 / ESZ;
   static constexpr int kBoxes = kRowBytes / 128;
   static constexpr int kQBytes = BM * kRowBytes;
-  static constexpr int kVKeys = kD256ChunkBytes / kRowBytes;
+  static constexpr int kVKeys = kT1ChunkBytes / kRowBytes < BN ? kT1ChunkBytes / kRowBytes : BN;
   static constexpr int kVChunks = BN / kVKeys;
   static constexpr int kVGroupBytes = kVKeys * 128;
   static constexpr int kPVKeys = 32 / ESZ;
+  static constexpr int kPVSteps = BN / kPVKeys;
+  static constexpr int kSpc = kVKeys / kPVKeys;
+  static constexpr int kChunks = D == 256 ? 8 : kT1MaxChunks;  // ring slots
   static constexpr int kRingOff = kQBytes;
-  static constexpr int kBarOff = kRingOff + kD256Chunks * kD256ChunkBytes;
+  static constexpr int kBarOff = kRingOff + kChunks * kT1ChunkBytes;
   static constexpr int kSmemBytes = kBarOff + 1024 + 1024;
-  static_assert(kVKeys == 2 * kPVKeys, "two P V K steps per V chunk");
+  static_assert(kRowBytes >= 128 && kRowBytes % 128 == 0, "rows of whole 128-byte boxes");
+  static_assert(kSpc <= kPVSteps / 2 || kSpc == kPVSteps, "P halves and V chunks");
+  static_assert(kChunks <= kT1MaxChunks, "barrier arrays");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
-struct D256Bars {
-  uint64_t full[kD256Chunks], empty[kD256Chunks];
+struct T1Bars {
+  uint64_t full[kT1MaxChunks], empty[kT1MaxChunks];
   uint64_t q_full, q_empty;
   uint64_t s_full[2];  // S_j computed (buffer j & 1)
   uint64_t p_full, p_hi;  // P of keys 0..63 / 64..127 written
@@ -1120,23 +1128,23 @@ struct D256Bars {
   uint64_t o_full, o_empty;
   uint32_t tmem_slot;
 };
-static_assert(sizeof(D256Bars) <= 1024, "barrier block");
+static_assert(sizeof(T1Bars) <= 1024, "barrier block");
 
-template <int ESZ>
-__global__ void __launch_bounds__(kD256Threads, 1)
-    prefill_d256_kernel(const __grid_constant__ CUtensorMap tmQ,
-                        const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using G = D256Geo<ESZ>;
+template <int D, int ESZ>
+__global__ void __launch_bounds__(kT1Threads, 1)
+    prefill_1tile_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using G = T1Geo<D, ESZ>;
   constexpr bool F8 = ESZ == 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  D256Bars* bars = reinterpret_cast<D256Bars*>(smem + G::kBarOff);
+  T1Bars* bars = reinterpret_cast<T1Bars*>(smem + G::kBarOff);
   uint8_t* ring = smem + G::kRingOff;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kD256Chunks; ++s) {
+    for (int s = 0; s < G::kChunks; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
@@ -1151,14 +1159,14 @@ __global__ void __launch_bounds__(kD256Threads, 1)
     mbar_init(&bars->o_empty, 128);
     fence_barrier_init();
   }
-  if (warp == kD256Mma) tmem_alloc(&bars->tmem_slot, 512);
+  if (warp == kT1Mma) tmem_alloc(&bars->tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_slot;
   const int rounds = (p.n_items + gridDim.x - 1) / gridDim.x;
 
-  if (warp == kD256Producer) {
+  if (warp == kT1Producer) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -1169,11 +1177,11 @@ __global__ void __launch_bounds__(kD256Threads, 1)
       bool ok = true;
       auto next_slot = [&]() -> uint8_t* {
         if (!(ok = mbar_wait(&bars->empty[slot], ph ^ 1, p.status))) return nullptr;
-        mbar_arrive_expect_tx(&bars->full[slot], kD256ChunkBytes);
-        return ring + slot * kD256ChunkBytes;
+        mbar_arrive_expect_tx(&bars->full[slot], kT1ChunkBytes);
+        return ring + slot * kT1ChunkBytes;
       };
       auto advance = [&]() {
-        if (++slot == kD256Chunks) { slot = 0; ph ^= 1; }
+        if (++slot == G::kChunks) { slot = 0; ph ^= 1; }
       };
       for (int r = 0; r < rounds && ok; ++r) {
         const int it = item_for(r, blockIdx.x, gridDim.x);
@@ -1188,7 +1196,7 @@ __global__ void __launch_bounds__(kD256Threads, 1)
         mbar_arrive_expect_tx(&bars->q_full, G::kQBytes);
 #pragma unroll
         for (int bx = 0; bx < G::kBoxes; ++bx)
-          tma_load_3d(smem + bx * kD256QBoxBytes, &tmQ, &bars->q_full, bx * G::kBoxElems,
+          tma_load_3d(smem + bx * kT1QBoxBytes, &tmQ, &bars->q_full, bx * G::kBoxElems,
                       m * BM, b * p.Hq + hq);
         // the chunks of K_j: its 128-byte column boxes
         auto load_k = [&](int j) {
@@ -1216,11 +1224,11 @@ __global__ void __launch_bounds__(kD256Threads, 1)
         }
       }
     }
-  } else if (warp == kD256Mma) {
+  } else if (warp == kT1Mma) {
     // ------------------------------------------------------------------ MMA issuer
     // bf16 (format 1) x bf16, or e5m2 (1) x e5m2 for S and e4m3 (0) P x e5m2 V for P V
     const uint32_t idesc_s = make_idesc(1, 1, false, false, BN, BM);
-    const uint32_t idesc_pv = make_idesc(F8 ? 0u : 1u, 1, false, true, kD256, BM);  // V MN-major
+    const uint32_t idesc_pv = make_idesc(F8 ? 0u : 1u, 1, false, true, D, BM);  // V MN-major
     const uint64_t q_desc0 = smem_desc(smem_u32(smem), 16, 1024, 2);
     const uint64_t r_desc0 = smem_desc(smem_u32(ring), 16, 1024, 2);  // K chunk (K-major)
     const uint64_t v_desc0 = smem_desc(smem_u32(ring), G::kVGroupBytes, 1024, 2);  // V chunk
@@ -1234,32 +1242,44 @@ __global__ void __launch_bounds__(kD256Threads, 1)
     };
     auto release_chunk = [&]() {
       umma_commit_e(&bars->empty[slot]);
-      if (++slot == kD256Chunks) { slot = 0; ph ^= 1; }
+      if (++slot == G::kChunks) { slot = 0; ph ^= 1; }
     };
     // S_j = Q K_j^T into buffer `buf`: per K chunk (128 bytes of the rows), its four K steps
     auto issue_s = [&](int buf) {
       const uint32_t d = tmem + buf * 128;
       for (int bx = 0; bx < G::kBoxes && ok; ++bx) {
         if (!wait_chunk()) return;
-        const uint64_t ad = q_desc0 + static_cast<uint64_t>((bx * kD256QBoxBytes) >> 4);
-        const uint64_t bd = r_desc0 + static_cast<uint64_t>((slot * kD256ChunkBytes) >> 4);
+        const uint64_t ad = q_desc0 + static_cast<uint64_t>((bx * kT1QBoxBytes) >> 4);
+        const uint64_t bd = r_desc0 + static_cast<uint64_t>((slot * kT1ChunkBytes) >> 4);
         issue_batched<F8, false, 0, 4>(
             d, [&](int kk) { return ad + static_cast<uint64_t>((kk * 32) >> 4); },
             [&](int kk) { return bd + static_cast<uint64_t>((kk * 32) >> 4); }, idesc_s, bx > 0);
         release_chunk();
       }
     };
-    // O += P_j V_j for V chunks [c0, c1) (P_j: TMEM columns of buffer `buf`, 8 per K step)
-    auto issue_pv = [&](int buf, int c0, int c1, bool acc) {
-      for (int c = c0; c < c1 && ok; ++c) {
-        if (!wait_chunk()) return;
-        const uint32_t pcol = tmem + buf * 128 + c * 16;
-        const uint64_t bd = v_desc0 + static_cast<uint64_t>((slot * kD256ChunkBytes) >> 4);
-        issue_batched<F8, true, 0, 2>(
-            tmem + 256, [&](int kk) { return pcol + kk * 8; },
-            [&](int kk) { return bd + static_cast<uint64_t>((kk * G::kPVKeys * 128) >> 4); },
-            idesc_pv, acc || c > 0);
-        release_chunk();
+    // O += P_j V_j for half `h` of P_j (keys 64h..64h+63; P_j: TMEM columns of buffer `buf`,
+    // 8 per K step): whole V chunks, or half of the tile's one V chunk
+    constexpr int kH = G::kPVSteps / 2;  // K steps per half
+    auto issue_pv = [&](int buf, auto hc, bool acc) {
+      constexpr int h = decltype(hc)::value;
+      const uint32_t pcol = tmem + buf * 128 + h * kH * 8;
+      auto b_of = [&](int kin) {
+        return v_desc0 + static_cast<uint64_t>((slot * kT1ChunkBytes + kin * G::kPVKeys * 128) >> 4);
+      };
+      if constexpr (G::kSpc <= kH) {
+        for (int c = 0; c < kH / G::kSpc && ok; ++c) {
+          if (!wait_chunk()) return;
+          issue_batched<F8, true, 0, G::kSpc>(
+              tmem + 256, [&](int kk) { return pcol + (c * G::kSpc + kk) * 8; },
+              [&](int kk) { return b_of(kk); }, idesc_pv, acc || c > 0);
+          release_chunk();
+        }
+      } else {
+        if (h == 0 && !wait_chunk()) return;
+        issue_batched<F8, true, h * kH, h * kH + kH>(
+            tmem + 256, [&](int kk) { return pcol + (kk - h * kH) * 8; },
+            [&](int kk) { return b_of(kk); }, idesc_pv, acc);
+        if (h == 1) release_chunk();
       }
     };
     for (int r = 0; r < rounds && ok; ++r) {
@@ -1289,12 +1309,12 @@ __global__ void __launch_bounds__(kD256Threads, 1)
           ph_oe ^= 1;
         }
         tc_fence_after();
-        issue_pv(buf, 0, G::kVChunks / 2, j > 0);
+        issue_pv(buf, std::integral_constant<int, 0>{}, j > 0);
         if (!ok) break;
         if (!(ok = mbar_wait_warp(&bars->p_hi, ph_pf, p.status))) break;
         ph_pf ^= 1;
         tc_fence_after();
-        issue_pv(buf, G::kVChunks / 2, G::kVChunks, true);
+        issue_pv(buf, std::integral_constant<int, 1>{}, true);
         if (!ok) break;
         umma_commit_e(&bars->pv_done);
         if (j == n - 1) umma_commit_e(&bars->o_full);
@@ -1397,7 +1417,7 @@ __global__ void __launch_bounds__(kD256Threads, 1)
             tc_fence_after();
             if (__any_sync(0xffffffffu, f != 1.f)) {
 #pragma unroll 1
-              for (int c = 0; c < kD256 / 8; ++c) {
+              for (int c = 0; c < D / 8; ++c) {
                 uint32_t ov[8];
                 tmem_ld8(tO + c * 8, ov);
 #pragma unroll
@@ -1427,9 +1447,9 @@ __global__ void __launch_bounds__(kD256Threads, 1)
       ph_pv ^= 1;
       tc_fence_after();
       const float inv = p.v_scale / l;
-      __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.S + row) * kD256;
+      __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.S + row) * D;
 #pragma unroll 1
-      for (int c = 0; c < kD256 / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
         tmem_ld32(tO + c * 32, ov);
         if (row < p.S) {
@@ -1454,7 +1474,7 @@ __global__ void __launch_bounds__(kD256Threads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kD256Mma) {
+  if (warp == kT1Mma) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -1512,12 +1532,12 @@ attn_status_t launch_typed(const void* q, const void* k, const void* v, void* o,
   return launch_status();
 }
 
-// D = 256 (bf16, or fp8 e5m2 without RoPE), no in-kernel RoPE (the rotation passes serve bf16)
-template <int ESZ>
-attn_status_t launch_d256(const void* q, const void* k, const void* v, void* o, float* lse,
+// one Q tile per item (bf16, or fp8 e5m2), no in-kernel RoPE (the rotation passes serve bf16)
+template <int D, int ESZ>
+attn_status_t launch_1tile(const void* q, const void* k, const void* v, void* o, float* lse,
                           float q_scale, float k_scale, float v_scale, int B, int Hq, int Hkv,
                           int S, int Skv, int kv_pitch, int causal, float scale, cudaStream_t st) {
-  using G = D256Geo<ESZ>;
+  using G = T1Geo<D, ESZ>;
   const uint64_t pitch = kv_pitch ? static_cast<uint64_t>(kv_pitch) : static_cast<uint64_t>(Skv);
   CUtensorMap tq, tk, tv;
   // V as {128 bytes of a row, key, 128-byte column group, (batch, KV head)}: one box = a chunk
@@ -1527,10 +1547,9 @@ attn_status_t launch_d256(const void* q, const void* k, const void* v, void* o, 
                                 pitch * G::kRowBytes};
   const uint32_t vbox[4] = {static_cast<uint32_t>(G::kBoxElems), static_cast<uint32_t>(G::kVKeys),
                             static_cast<uint32_t>(G::kBoxes), 1};
-  if (!make_tmap_3d(&tq, q, ESZ, kD256, S, static_cast<uint64_t>(B) * Hq, G::kBoxElems, BM,
-                    128) ||
-      !make_tmap_3d(&tk, k, ESZ, kD256, Skv, static_cast<uint64_t>(B) * Hkv, G::kBoxElems, BN,
-                    128, kv_pitch) ||
+  if (!make_tmap_3d(&tq, q, ESZ, D, S, static_cast<uint64_t>(B) * Hq, G::kBoxElems, BM, 128) ||
+      !make_tmap_3d(&tk, k, ESZ, D, Skv, static_cast<uint64_t>(B) * Hkv, G::kBoxElems, BN, 128,
+                    kv_pitch) ||
       !make_tmap_4d(&tv, v, ESZ, vdims, vstrides, vbox))
     return ATTN_ERR_CUDA;
   Params p{};
@@ -1554,10 +1573,10 @@ attn_status_t launch_d256(const void* q, const void* k, const void* v, void* o, 
   p.v_scale = v_scale;
   p.table = nullptr;
   p.pos0 = 0;
-  auto kern = prefill_d256_kernel<ESZ>;
+  auto kern = prefill_1tile_kernel<D, ESZ>;
   if (!set_smem_attr(reinterpret_cast<const void*>(kern), G::kSmemBytes)) return ATTN_ERR_CUDA;
   const int grid = std::min(p.n_items, sm_count());
-  kern<<<grid, kD256Threads, G::kSmemBytes, st>>>(tq, tk, tv, p);
+  kern<<<grid, kT1Threads, G::kSmemBytes, st>>>(tq, tk, tv, p);
   return launch_status();
 }
 
@@ -1582,10 +1601,10 @@ attn_status_t launch_prefill(const void* q, const void* k, const void* v, void* 
                                         pos0, st);
   ATTN_PREFILL_CASE(128, 0, 2, 2)
   if (D == 256 && rm == 0)
-    return esz == 2 ? launch_d256<2>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S,
-                                     Skv, kv_pitch, causal, scale, st)
-                    : launch_d256<1>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv, S,
-                                     Skv, kv_pitch, causal, scale, st);
+    return esz == 2 ? launch_1tile<256, 2>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv,
+                                           S, Skv, kv_pitch, causal, scale, st)
+                    : launch_1tile<256, 1>(q, k, v, o, lse, q_scale, k_scale, v_scale, B, Hq, Hkv,
+                                           S, Skv, kv_pitch, causal, scale, st);
   ATTN_PREFILL_CASE(128, 1, 2, 2)
   ATTN_PREFILL_CASE(64, 0, 2, 2)
   ATTN_PREFILL_CASE(64, 1, 2, 2)
