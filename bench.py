@@ -843,7 +843,9 @@ def ours(args):
 
         e2e_pipelined(2)
         torch.cuda.synchronize()
-        n_e2e = max(4, args.steps // 2)
+        # the same K steps as the device-timed region; the first step's copy in and the last
+        # step's copy out (pipeline fill and drain) stay inside the timed region
+        n_e2e = max(4, args.steps)
         # three timed runs, the median kept: the host link is shared with other work on the
         # machine, and one disturbed run should not set the figure
         runs = []
