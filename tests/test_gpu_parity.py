@@ -448,6 +448,9 @@ def test_decode_append_full_cache_sets_status():
     (1, 16, 2048, [2048]),                 # one sequence spread over many SMs
     (2, 5, 200, [200, 37]),
     (160, 16, 256, [256 - (i % 7) * 33 for i in range(160)]),  # more sequences than SMs
+    # one whole sequence per CTA, ragged lengths, Lmax = 200: the last tile's copy runs past the
+    # cache's key extent (zero fill) and past each length (masked)
+    (128, 16, 200, [200 - (i % 5) * 37 for i in range(128)]),
 ])
 def test_latent_decode(B, H, Lmax, lens):
     q, c, cl = synthetic.latent_inputs(B, H, Lmax, lens, seed=B)
@@ -463,6 +466,7 @@ def test_latent_decode(B, H, Lmax, lens):
     (128, 16, 2048, 2048),                 # one whole sequence per CTA
     (2, 5, 200, [200, 37]),
     (160, 16, 256, [256 - (i % 7) * 33 for i in range(160)]),
+    (128, 16, 200, [200 - (i % 5) * 37 for i in range(128)]),
 ])
 def test_latent_decode_fp8_cache(B, H, Lmax, lens):
     """e5m2 latent cache (q bf16): widened exactly to f16 in the MMAs, so the bf16 bounds apply."""
