@@ -739,9 +739,7 @@ constexpr int kLatWarps = 8;                              // compute warps (no s
 constexpr int kLatThreads = kLatWarps * 32;               // warp 0, lane 0 issues the TMA loads)
 constexpr int kLatTileBytes = kTileKeys * kLatQK * 2;     // 64 KB: 64 keys x 512 dims
 constexpr int kLatQPitch = kLatQK * 2 + 16;
-constexpr int kLatPPitch = kTileKeys * 2 + 16;
 constexpr int kLatColsPerWarp = kLatV / kLatWarps;        // 56 = 7 n-tiles of the 448 outputs
-constexpr int kLatKeysPerWarp = kTileKeys / kLatWarps;    // 8 keys scored per warp per tile
 
 __device__ __forceinline__ void lat_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kLatWarps * 32) : "memory");
@@ -759,23 +757,33 @@ constexpr int kLatMaxB = 2048;  // sequences per call (the tile prefix sums live
 #endif
 constexpr int kLatMaxCtas = ATTN_LAT_MAX_CTAS;
 
-// Cache tile geometry: bf16 tiles of 64 keys x 512 dims (64 KB, three stages) or e5m2 tiles of
-// 64 keys x 512 bytes (32 KB, six stages); both rings hold 192 KB.  A tile lands as its 128-byte
-// column chunks, each 64 rows x 128 bytes with the 128-byte swizzle, in ONE TMA copy: the tensor
-// map views the cache as {128 bytes of a row, key, chunk, sequence}, so the box {128 B, 64 keys,
-// all chunks, 1} is laid out chunk-major.  Issued as one box per chunk, the copies held the
-// issuing thread (and with it its warp, and the next block barrier) ~700 cycles per tile.
+// Cache tile geometry: bf16 tiles of 64 keys x 512 dims or e5m2 tiles of 128 keys x 512 bytes,
+// 64 KB either way, three stages (192 KB).  The per-tile work that does not grow with the keys
+// (two block barriers, the maximum exchange, the refill) is spread over twice the keys in the
+// e5m2 tiles.  A tile lands as its 128-byte column chunks, each kKeys rows x 128 bytes with the
+// 128-byte swizzle, in ONE TMA copy: the tensor map views the cache as {128 bytes of a row, key,
+// chunk, sequence}, so the box {128 B, kKeys keys, all chunks, 1} is laid out chunk-major.
+// Issued as one box per chunk, the copies held the issuing thread (and with it its warp, and the
+// next block barrier) ~700 cycles per tile.
 template <bool F8>
 struct LatGeo {
-  static constexpr int kTileBytes = F8 ? kTileKeys * kLatQK : kLatTileBytes;
-  static constexpr int kStages = F8 ? 6 : kLatStages;
+  static constexpr int kKeys = F8 ? 2 * kTileKeys : kTileKeys;  // keys per tile
+  static constexpr int kTileBytes = kKeys * kLatQK * (F8 ? 1 : 2);
+  static constexpr int kStages = kLatStages;
+  static constexpr int kKeysPerWarp = kKeys / kLatWarps;  // keys scored per warp per tile
+  static constexpr int kNS = kKeysPerWarp / 8;            // n8 score tiles per warp
+  static constexpr int kPPitch = kKeys * 2 + 16;          // P row pitch in shared memory
+  static_assert(kTileBytes == kLatTileBytes, "64 KB tiles");
 };
 constexpr int kLatMaxStages = 6;
 
 struct LatSmem {
   static constexpr int kQOff = kLatStages * kLatTileBytes;  // 192 KB of stages for both dtypes
-  static constexpr int kPOff = kQOff + 16 * kLatQPitch;
-  static constexpr int kRedOff = kPOff + 2 * 16 * kLatPPitch;        // [2][warps][16] row max
+  // P [2][16][pitch] reuses the query tile's bytes: the query sits in registers while the tiles
+  // of a segment run (loaded after, and overwritten before, block barriers that P's use is
+  // between)
+  static constexpr int kPOff = kQOff;
+  static constexpr int kRedOff = kQOff + 16 * kLatQPitch;            // [2][warps][16] row max
   static constexpr int kLOff = kRedOff + 2 * kLatWarps * 16 * 4;      // [warps][16] row sums
   static constexpr int kScanOff = kLOff + kLatWarps * 16 * 4;         // [warps] scan scratch
   static constexpr int kPrefOff = kScanOff + 64;                      // [B + 1] tile prefix
@@ -783,6 +791,9 @@ struct LatSmem {
   static constexpr int kBytes = kBarOff + 2 * kLatMaxStages * 8 + 1024;
 };
 static_assert(LatGeo<true>::kStages * LatGeo<true>::kTileBytes == LatSmem::kQOff, "ring size");
+static_assert(2 * 16 * LatGeo<true>::kPPitch <= 16 * kLatQPitch &&
+                  2 * 16 * LatGeo<false>::kPPitch <= 16 * kLatQPitch,
+              "P fits in the query tile's bytes");
 
 struct LatParams {
   const __nv_bfloat16* q;
@@ -800,10 +811,11 @@ struct LatParams {
   float scale_log2;
 };
 
-// Key tiles (64 keys) of sequence b; 0 for an out-of-range length.
+// Key tiles (KEYS keys) of sequence b; 0 for an out-of-range length.
+template <int KEYS>
 __device__ __forceinline__ int lat_tiles(const int32_t* lens, int b, int Lmax) {
   const int len = lens[b];
-  return (len >= 1 && len <= Lmax) ? (len + kTileKeys - 1) / kTileKeys : 0;
+  return (len >= 1 && len <= Lmax) ? (len + KEYS - 1) / KEYS : 0;
 }
 
 // Stream-K split: the T key tiles of all sequences, in order, are cut into gridDim.x equal
@@ -819,6 +831,7 @@ struct LatSeg {
   bool invalid;  // sequence b has an out-of-range length (whole-sequence mode only)
 };
 
+template <int KEYS>
 struct LatSegIter {
   long long lo, hi;
   int b, stride;
@@ -858,8 +871,8 @@ struct LatSegIter {
       const long long s0 = lo > tb ? lo : tb, s1 = hi < te ? hi : te;
       if (s0 >= s1) continue;
       sg.b = cur;
-      sg.k0 = static_cast<int>(s0 - tb) * kTileKeys;
-      sg.k1 = min(static_cast<int>(s1 - tb) * kTileKeys, static_cast<int>(lens[cur]));
+      sg.k0 = static_cast<int>(s0 - tb) * KEYS;
+      sg.k1 = min(static_cast<int>(s1 - tb) * KEYS, static_cast<int>(lens[cur]));
       sg.whole = (s0 == tb && s1 == te);
       sg.invalid = false;
       return true;
@@ -872,7 +885,7 @@ struct LatSegIter {
 template <bool F8>
 struct LatLoader {
   using G = LatGeo<F8>;
-  LatSegIter seg;
+  LatSegIter<G::kKeys> seg;
   LatSeg cur;
   int t0, stage;
   uint32_t phase;
@@ -897,7 +910,7 @@ struct LatLoader {
       stage = 0;
       phase ^= 1;
     }
-    t0 += kTileKeys;
+    t0 += G::kKeys;
     if (t0 >= cur.k1) advance(pref, p.B, p.lens, p.Lmax);
     return true;
   }
@@ -940,7 +953,7 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     const int per = (p.B + kLatThreads - 1) / kLatThreads;
     const int b0 = tid * per, b1 = min(b0 + per, p.B);
     int sum = 0;
-    for (int b = b0; b < b1; ++b) sum += lat_tiles(p.lens, b, p.Lmax);
+    for (int b = b0; b < b1; ++b) sum += lat_tiles<G::kKeys>(p.lens, b, p.Lmax);
     int x = sum;  // inclusive scan over the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -954,7 +967,7 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     int run = base + x - sum;  // exclusive prefix of this thread's chunk
     for (int b = b0; b < b1; ++b) {
       pref[b] = run;
-      run += lat_tiles(p.lens, b, p.Lmax);
+      run += lat_tiles<G::kKeys>(p.lens, b, p.Lmax);
     }
     if (tid == kLatThreads - 1) pref[p.B] = base + x;
   }
@@ -993,7 +1006,7 @@ __global__ void __launch_bounds__(kLatThreads, 1)
   int tcount = 0;
   const int H = p.H;
 
-  LatSegIter segs;
+  LatSegIter<G::kKeys> segs;
   if (p.streamk)
     segs.init(pref, p.B, lo, hi);
   else
@@ -1077,55 +1090,72 @@ __global__ void __launch_bounds__(kLatThreads, 1)
 #pragma unroll
     for (int n = 0; n < kNT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
-    for (int t0 = k0; t0 < k1; t0 += kTileKeys, ++tcount) {
+    constexpr int kNS = G::kNS;         // n8 key tiles this warp scores per tile
+    constexpr int kCh = 4 / kNS;        // independent MMA chains per key tile (four in all)
+    for (int t0 = k0; t0 < k1; t0 += G::kKeys, ++tcount) {
       if (!mbar_wait(&full[stage], phase, p.status)) {
         alive = false;
         break;
       }
       const uint32_t ct = smem_u32(smem + stage * G::kTileBytes);
       const int par = tcount & 1;
-      float s[4];  // rows g / g+8 x keys 8w + 2tq + {0,1}
+      float s[kNS][4];  // rows g / g+8 x keys kKeysPerWarp w + 8 nt + 2 tq + {0,1}
       {
-        float ch[4][4];
+        float ch[kNS][kCh][4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ch[c][0] = ch[c][1] = ch[c][2] = ch[c][3] = 0.f;
+        for (int nt = 0; nt < kNS; ++nt)
+#pragma unroll
+          for (int c = 0; c < kCh; ++c) ch[nt][c][0] = ch[nt][c][1] = ch[nt][c][2] = ch[nt][c][3] = 0.f;
         if constexpr (F8) {
           const uint8_t* kt = smem + stage * G::kTileBytes;
-          const int key = warp * kLatKeysPerWarp + g;
 #pragma unroll
           for (int kk = 0; kk < kLatQK / 16; ++kk) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(
-                kt + (kk >> 3) * kTileKeys * 128 + sw128_offset(key, kk & 7) + 4 * tq);
-            mma_f16_16816(ch[kk & 3], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], e5m2x2_lo(w),
-                          e5m2x2_hi(w));
+#pragma unroll
+            for (int nt = 0; nt < kNS; ++nt) {
+              const int key = warp * G::kKeysPerWarp + nt * 8 + g;
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(
+                  kt + (kk >> 3) * G::kKeys * 128 + sw128_offset(key, kk & 7) + 4 * tq);
+              mma_f16_16816(ch[nt][kk % kCh], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
+                            e5m2x2_lo(w), e5m2x2_hi(w));
+            }
           }
         } else {
-          const int key = warp * kLatKeysPerWarp + (lane & 7);
+          static_assert(F8 || kNS == 1, "bf16 tiles: one key tile per warp");
+          const int key = warp * G::kKeysPerWarp + (lane & 7);
           const int mi = lane >> 3;  // matrix index: 16-byte dim chunk within a pair of k-steps
 #pragma unroll
           for (int kk = 0; kk < kLatQK / 16; kk += 2) {
             const int c = kk * 2 + mi;  // dims 8c .. 8c+7
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
-            mma_bf16_16816(ch[kk & 3], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-            mma_bf16_16816(ch[(kk + 1) & 3], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2],
+            ldsm_x4(ct + (c >> 3) * G::kKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
+            mma_bf16_16816(ch[0][kk & 3], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+            mma_bf16_16816(ch[0][(kk + 1) & 3], qa[kk + 1][0], qa[kk + 1][1], qa[kk + 1][2],
                            qa[kk + 1][3], b2, b3);
           }
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) s[e] = (ch[0][e] + ch[1][e]) + (ch[2][e] + ch[3][e]);
+        for (int nt = 0; nt < kNS; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float v = ch[nt][0][e];
+#pragma unroll
+            for (int c = 1; c < kCh; ++c) v += ch[nt][c][e];
+            s[nt][e] = v;
+          }
       }
       float rm0 = -INFINITY, rm1 = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = t0 + warp * kLatKeysPerWarp + tq * 2 + (e & 1);
-        const float v = key < k1 ? s[e] * p.scale_log2 : -INFINITY;
-        s[e] = v;
-        if (e < 2)
-          rm0 = fmaxf(rm0, v);
-        else
-          rm1 = fmaxf(rm1, v);
-      }
+      for (int nt = 0; nt < kNS; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = t0 + warp * G::kKeysPerWarp + nt * 8 + tq * 2 + (e & 1);
+          const float v = key < k1 ? s[nt][e] * p.scale_log2 : -INFINITY;
+          s[nt][e] = v;
+          if (e < 2)
+            rm0 = fmaxf(rm0, v);
+          else
+            rm1 = fmaxf(rm1, v);
+        }
       rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 1));
       rm0 = fmaxf(rm0, __shfl_xor_sync(0xffffffffu, rm0, 2));
       rm1 = fmaxf(rm1, __shfl_xor_sync(0xffffffffu, rm1, 1));
@@ -1147,16 +1177,21 @@ __global__ void __launch_bounds__(kLatThreads, 1)
       const float c0 = fast_exp2(m0 - base0), c1 = fast_exp2(m1 - base1);
       m0 = mn0;
       m1 = mn1;
-      uint8_t* pw = smem + LatSmem::kPOff + par * 16 * kLatPPitch;
-      const float e0 = fast_exp2(s[0] - base0), e1 = fast_exp2(s[1] - base0);
-      const float e2 = fast_exp2(s[2] - base1), e3 = fast_exp2(s[3] - base1);
-      const int col = warp * kLatKeysPerWarp + tq * 2;
-      *reinterpret_cast<uint32_t*>(pw + g * kLatPPitch + col * 2) =
-          F8 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
-      *reinterpret_cast<uint32_t*>(pw + (g + 8) * kLatPPitch + col * 2) =
-          F8 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
-      l0 = l0 * c0 + (e0 + e1);
-      l1 = l1 * c1 + (e2 + e3);
+      uint8_t* pw = smem + LatSmem::kPOff + par * 16 * G::kPPitch;
+      l0 *= c0;
+      l1 *= c1;
+#pragma unroll
+      for (int nt = 0; nt < kNS; ++nt) {
+        const float e0 = fast_exp2(s[nt][0] - base0), e1 = fast_exp2(s[nt][1] - base0);
+        const float e2 = fast_exp2(s[nt][2] - base1), e3 = fast_exp2(s[nt][3] - base1);
+        const int col = warp * G::kKeysPerWarp + nt * 8 + tq * 2;
+        *reinterpret_cast<uint32_t*>(pw + g * G::kPPitch + col * 2) =
+            F8 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+        *reinterpret_cast<uint32_t*>(pw + (g + 8) * G::kPPitch + col * 2) =
+            F8 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
+        l0 += e0 + e1;
+        l1 += e2 + e3;
+      }
 #pragma unroll
       for (int n = 0; n < kNT; ++n) {
         acc[n][0] *= c0;
@@ -1165,13 +1200,13 @@ __global__ void __launch_bounds__(kLatThreads, 1)
         acc[n][3] *= c1;
       }
       lat_bar_sync();
-      // O[:, this warp's columns] += P (16 x 64) * C[:, cols]
-      const uint32_t ps_addr = ps_addr0 + par * 16 * kLatPPitch;
+      // O[:, this warp's columns] += P (16 x kKeys) * C[:, cols]
+      const uint32_t ps_addr = ps_addr0 + par * 16 * G::kPPitch;
       const int cbase = (warp * kLatColsPerWarp) / 8;  // first 8-column chunk of this warp
 #pragma unroll
-      for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+      for (int kk = 0; kk < G::kKeys / 16; ++kk) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(ps_addr + (lane & 15) * kLatPPitch + (kk * 16 + (lane >> 4) * 8) * 2, a0, a1, a2,
+        ldsm_x4(ps_addr + (lane & 15) * G::kPPitch + (kk * 16 + (lane >> 4) * 8) * 2, a0, a1, a2,
                 a3);
         if constexpr (F8) {
           // chunk c = warp + 8 ci; matrices keys 0-7 / 8-15 of this step (lanes 0-15 address)
@@ -1181,7 +1216,7 @@ __global__ void __launch_bounds__(kLatThreads, 1)
             const int c = warp + 8 * ci;
             if (c >= kLatV / 16) continue;  // warp-uniform: warps 4-7 own three chunks
             uint32_t r0, r1;
-            ldsm_x2_t(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(keyr, c & 7), r0, r1);
+            ldsm_x2_t(ct + (c >> 3) * G::kKeys * 128 + sw128_offset(keyr, c & 7), r0, r1);
             mma_f16_16816(acc[2 * ci], a0, a1, a2, a3, e5m2x2_even(r0), e5m2x2_even(r1));
             mma_f16_16816(acc[2 * ci + 1], a0, a1, a2, a3, e5m2x2_odd(r0), e5m2x2_odd(r1));
           }
@@ -1193,14 +1228,14 @@ __global__ void __launch_bounds__(kLatThreads, 1)
         for (int n2 = 0; n2 < 3; ++n2) {  // n-tiles 2*n2, 2*n2+1
           const int c = cbase + n2 * 2 + (mi >> 1);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
+          ldsm_x4_t(ct + (c >> 3) * G::kKeys * 128 + sw128_offset(key, c & 7), b0, b1, b2, b3);
           mma_bf16_16816(acc[2 * n2], a0, a1, a2, a3, b0, b1);
           mma_bf16_16816(acc[2 * n2 + 1], a0, a1, a2, a3, b2, b3);
         }
         {  // n-tile 6 (two 8x8 matrices: keys 0-7 and 8-15 of this step)
           const int c = cbase + 6;
           uint32_t b0, b1;
-          ldsm_x2_t(ct + (c >> 3) * kTileKeys * 128 + sw128_offset(key, c & 7), b0, b1);
+          ldsm_x2_t(ct + (c >> 3) * G::kKeys * 128 + sw128_offset(key, c & 7), b0, b1);
           mma_bf16_16816(acc[6], a0, a1, a2, a3, b0, b1);
         }
       }
@@ -1703,7 +1738,9 @@ attn_status_t launch_latent(const void* q, const void* c, const int32_t* lens, i
                             static_cast<uint64_t>(B)};
   const uint64_t strides[3] = {static_cast<uint64_t>(kLatQK) * esz, 128,
                                static_cast<uint64_t>(Lmax) * kLatQK * esz};
-  const uint32_t box[4] = {chunk, kTileKeys, kLatQK / chunk, 1};
+  const uint32_t box[4] = {chunk, static_cast<uint32_t>(f8 ? LatGeo<true>::kKeys
+                                                         : LatGeo<false>::kKeys),
+                           kLatQK / chunk, 1};
   if (!make_tmap_4d(&tc, c, esz, dims, strides, box)) return ATTN_ERR_CUDA;
   LatParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
