@@ -1070,8 +1070,10 @@ def single_case(args):
         grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
         fn = lambda: b.attn_prefill_backward(q, k, v, o, lse, do, causal=True, dq=grads[0],
                                              dk=grads[1], dv=grads[2], workspace=bws)
-    elif args.case == "latent":
-        q, c, cl = synthetic.latent_inputs(args.B, 16, 2048, 2048, seed=1)
+    elif args.case in ("latent", "latent-fp8"):
+        q, c, cl = synthetic.latent_inputs(args.B, 16, 2048, 2048, seed=1,
+                                           **({"cache_dtype": "fp8"} if args.case == "latent-fp8"
+                                              else {}))
         q, c, cl = q.cuda(), c.cuda(), cl.cuda()
         b.attn_rope_table_reserve(64, THETA, 2049)
         fn = lambda: b.attn_decode_latent(q, c, cl, rope=True, rope_theta=THETA)
@@ -1098,7 +1100,7 @@ def main():
                     choices=["prefill", "prefill-fused", "prefill-unfused", "prefill-d64",
                              "prefill-fp8", "prefill-fp8-d64", "prefill-d256",
                              "decode", "decode-fp8",
-                             "latent",
+                             "latent", "latent-fp8",
                              "rope", "backward"],
                     help="time one kernel alone (for profiler captures)")
     ap.add_argument("--S", type=int, default=4096)
