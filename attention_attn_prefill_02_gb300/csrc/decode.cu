@@ -916,11 +916,12 @@ struct LatLoader {
   }
 };
 
-// Absorbed latent decode, stream-K over all sequences' key tiles.  Per 64-key tile: warp w
-// scores keys 8w..8w+7 against the 16 query rows over all 512 dims (query fragments held in
-// registers, four independent MMA chains), the tile's row maximum and P go through shared
-// memory, then warp w accumulates its output columns over all 64 keys.  Thread 0 refills each
-// stage as soon as all warps released it.
+// Absorbed latent decode, stream-K over all sequences' key tiles.  Per tile (64 keys for a bf16
+// cache, 128 for e5m2): warp w scores its kKeysPerWarp keys (8 or 16: one or two n8 key tiles)
+// against the 16 query rows over all 512 dims (query fragments held in registers, four
+// independent MMA chains in all), the tile's row maximum and P go through shared memory, then
+// warp w accumulates its output columns over all the tile's keys.  Thread 0 refills each stage
+// as soon as all warps released it.
 //
 // F8: an e5m2 cache.  Every e5m2 value is exactly an f16 value, so the MMAs run in f16 on values
 // widened in registers: key fragments are 4-byte reads of the swizzled tile (4 consecutive
