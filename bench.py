@@ -1098,7 +1098,7 @@ def main():
     ap.add_argument("--oracle-one-core", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--case", default=None,
                     choices=["prefill", "prefill-fused", "prefill-unfused", "prefill-d64",
-                             "prefill-fp8", "prefill-fp8-d64", "prefill-d256",
+                             "prefill-fp8", "prefill-fp8-d64", "prefill-d256", "prefill-fp8-d256",
                              "decode", "decode-fp8",
                              "latent", "latent-fp8",
                              "rope", "backward"],
