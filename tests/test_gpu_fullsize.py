@@ -143,6 +143,18 @@ def test_causal_prefill_d256_s4096_sampled():
     check_rows(o, lse, rows, ro, rl, BF16_MAX, BF16_MEAN)
 
 
+def test_causal_prefill_fp8_d256_s4096_sampled():
+    """fp8 e5m2 causal GQA at head dim 256, Z=4 Hq=32 Hkv=8 S=4096 (the shape the bench times in
+    fp8; no RoPE at D = 256): sampled rows against the oracle on the dequantised inputs."""
+    B, Hq, Hkv, S, D = 4, 32, 8, 4096, 256
+    q, k, v = synthetic.prefill_inputs(B, Hq, Hkv, S, D, "fp8", seed=26)
+    o, lse = binding.attn_prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, want_lse=True)
+    assert binding.attn_get_device_status() == 0
+    rows = sample_rows(B, Hq, S, n_random=16, seed=6)
+    ro, rl = oracle_rows(q, k, v, rows, causal=True, rope=False)
+    check_rows(o, lse, rows, ro, rl, FP8_MAX, 1e-2)
+
+
 @pytest.mark.parametrize("path", [2, 1], ids=["tcgen05", "mma_sync"])
 def test_backward_causal_d128_s4096_group_slice(path):
     """The backward at the size the bench times (causal GQA Z=4 Hq=32 Hkv=8 D=128 S=4096): the
